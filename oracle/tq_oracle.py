@@ -118,7 +118,7 @@ def _Phi_diff(a: float, b: float) -> float:
 _CODEBOOK_CACHE: dict = {}
 
 
-def lloyd_max_codebook(bits: int, blk: int, tol: float = 1e-14, max_iter: int = 100000):
+def lloyd_max_codebook(bits: int, blk: int, max_iter: int = 1000000):
     """Lloyd-Max scalar quantiser for N(0, sigma^2 = 1/blk) with 2^bits
     levels (TurboQuant From Scratch, section 2, step 3: "a Lloyd-Max codebook
     computed once for N(0, 1/d)"; turboquant-pytorch README, lloyd_max.py).
@@ -127,8 +127,10 @@ def lloyd_max_codebook(bits: int, blk: int, tol: float = 1e-14, max_iter: int = 
     alternate the two optimality conditions: boundaries are midpoints of
     neighbouring centroids, centroids are conditional means of their cell,
     c_k = sigma (phi(a) - phi(b)) / (Phi(b) - Phi(a)) with a, b the cell
-    edges in units of sigma.  Stops when no centroid moves by more than
-    tol * sigma.  Returns (centroids ascending, boundaries), float64."""
+    edges in units of sigma.  The iteration converges linearly, so it runs
+    to the fixed point itself: until the centroids stop moving, or the step
+    is below 1e-15 sigma and no longer shrinks (rounding-level oscillation).
+    Returns (centroids ascending, boundaries), float64."""
     key = (bits, blk)
     if key in _CODEBOOK_CACHE:
         c, b = _CODEBOOK_CACHE[key]
@@ -136,6 +138,7 @@ def lloyd_max_codebook(bits: int, blk: int, tol: float = 1e-14, max_iter: int = 
     K = 1 << bits
     sigma = 1.0 / math.sqrt(blk)
     c = [_STD.inv_cdf((k + 0.5) / K) for k in range(K)]   # in units of sigma
+    last = math.inf
     for _ in range(max_iter):
         edges = [-math.inf] + [0.5 * (c[k] + c[k + 1]) for k in range(K - 1)] + [math.inf]
         new = []
@@ -144,8 +147,12 @@ def lloyd_max_codebook(bits: int, blk: int, tol: float = 1e-14, max_iter: int = 
             new.append((_phi(a) - _phi(b)) / _Phi_diff(a, b))
         delta = max(abs(x - y) for x, y in zip(new, c))
         c = new
-        if delta < tol:
+        if delta == 0.0 or (delta < 1e-15 and delta >= last):
             break
+        last = delta
+    # N(0, sigma^2) is symmetric, so is its Lloyd-Max codebook: remove the
+    # rounding-level asymmetry so that the middle boundary is exactly 0.
+    c = [0.5 * (c[k] - c[K - 1 - k]) for k in range(K)]
     cent = np.array(c) * sigma
     bnd = 0.5 * (cent[1:] + cent[:-1])
     _CODEBOOK_CACHE[key] = (cent.copy(), bnd.copy())

@@ -1,0 +1,199 @@
+/*
+ * tq.h - C ABI of libtq: TurboQuant / PolarQuant KV-cache compression and
+ * attention computed directly over the compressed cache, for NVIDIA GB300
+ * (sm_103a).
+ *
+ * The method (per key or value vector x of length d, in blocks of `block`
+ * coordinates; block == d gives one norm per vector, block == 32 gives the
+ * "block-32" layout):
+ *   1. split off the norm n = ||x_j|| of every block and quantise u = x_j/n
+ *      ("TurboQuant From Scratch on Real KV Tensors", section 2, step 1);
+ *   2. rotate y = H D u with D a random +-1 diagonal and H the orthonormal
+ *      Walsh-Hadamard matrix (same section, step 2; ``fwht`` listing);
+ *   3. scalar-quantise every y_i with the Lloyd-Max codebook of N(0, 1/block)
+ *      (same section, step 3);
+ *   4. optionally keep the 1-bit QJL residual sign(S r), r = u - Q(u), plus
+ *      ||r|| ("turboquant-pytorch" README, "The combined estimator");
+ *   5. bit-pack the codes with one fp16 scale per block (llama.cpp-turboquant
+ *      docs/turboquant.md, "How it works" and "GGML Types": 14-byte turbo3
+ *      and 18-byte turbo4 blocks of 32 values).
+ *
+ * Conventions for every call below:
+ *   - Every call returns 0 (TQ_OK) or a negative tq_status; none throws,
+ *     none synchronises the device, none allocates memory.  Device work is
+ *     enqueued on `stream` (a cudaStream_t passed as void*; NULL = the
+ *     legacy default stream).  Errors are reported for invalid arguments
+ *     before anything is enqueued; TQ_ERR_CUDA reports a failed launch
+ *     (cudaGetLastError right after it).
+ *   - The caller owns every buffer.  "device" pointers must be CUDA device
+ *     (or managed) memory, 16-byte aligned unless stated otherwise; "host"
+ *     pointers are ordinary host memory.
+ *   - fp16 values travel as uint16_t bit patterns (IEEE binary16).
+ *   - Reserved fields must be zero.
+ */
+#ifndef TQ_H_
+#define TQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  TQ_OK = 0,
+  TQ_ERR_ARG = -1,          /* NULL pointer, bad shape or stride           */
+  TQ_ERR_UNSUPPORTED = -2,  /* (head_dim, block, bits, qjl_m) not handled  */
+  TQ_ERR_ALIGN = -3,        /* pointer not aligned as required             */
+  TQ_ERR_WORKSPACE = -4,    /* workspace missing or too small              */
+  TQ_ERR_CUDA = -5,         /* kernel launch failed                        */
+  TQ_ERR_TIMEOUT = -6       /* a bounded device-side wait gave up          */
+} tq_status;
+
+typedef enum { TQ_F16 = 0, TQ_F32 = 1 } tq_dtype;
+
+/* Codec settings of one cache (K or V).
+ *   head_dim      d in {64, 128, 256}
+ *   block         rotation + norm block: a power of two >= 32 dividing d
+ *                 (d: one norm per vector; 32: block-32)
+ *   bits          MSE bits per coordinate, 1..4
+ *   qjl_m         0 = no QJL residual; else m rows of S, a multiple of 32,
+ *                 <= 256, and block must equal head_dim
+ *   norm_correct  0/1: store n / ||reconstructed direction|| instead of n,
+ *                 so that the decoded block has the input's norm
+ *                 ("TurboQuant From Scratch", section 2, "Norm correction")
+ *   sign_seed     seed of D: the i-th splitmix64 output (state = seed)
+ *                 gives D_i = -1 when its top bit is set, else +1.  Block j
+ *                 uses D[j*block .. (j+1)*block). */
+typedef struct {
+  int32_t head_dim;
+  int32_t block;
+  int32_t bits;
+  int32_t qjl_m;
+  int32_t norm_correct;
+  int32_t reserved;
+  uint64_t sign_seed;
+} tq_layout;
+
+/* Packed record of one vector (all little endian):
+ *   codes:   d*bits/8 bytes = d/32 groups of 32 rotated coordinates, in
+ *            coordinate order; group = `bits` 32-bit words; word w, nibble k
+ *            (bits 4k..4k+3) holds
+ *              bits=4: code(8w+k)
+ *              bits=3: bits 0-2 = code(8w+k), bit 3 = bit w of code(24+k)
+ *              bits=2: bits 0-1 = code(8w+k), bits 2-3 = code(16+8w+k)
+ *              bits=1: bit p = code(8p+k)
+ *            where code(i) = #{k : y_i > beta_k} indexes the ascending
+ *            centroids of the Lloyd-Max codebook.
+ *   scales:  d/block fp16 values (n, or the norm-corrected value).
+ *   qjl:     qjl_m/8 bytes = m/32 words, bit i of word w = [(S r)_{32w+i} >= 0].
+ *   rnorm:   one fp16 ||r|| (QJL only).
+ * Bytes per element with block 32: 0.4375 at 3 bits, 0.5625 at 4 bits. */
+
+/* Lloyd-Max codebook of N(0, 1/block) with 2^bits levels, solved in double
+ * precision on the host and rounded to nearest float.  centroids: host,
+ * 2^bits floats, ascending; boundaries: host, 2^bits - 1 midpoints.
+ * "TurboQuant From Scratch", section 2, step 3; section 3 (distortion
+ * about 0.118 / 0.0345 / 0.0095 at 2 / 3 / 4 bits). */
+int tq_codebook(int bits, int block, float* centroids, float* boundaries);
+
+/* Same codebook without the rounding to float (host, double). */
+int tq_codebook_f64(int bits, int block, double* centroids, double* boundaries);
+
+/* Sign vector D of a layout: out[i] = +1 or -1 for i < d (host int8). */
+int tq_signs(uint64_t sign_seed, int d, int8_t* out);
+
+/* Per-vector sizes of a layout (host outputs, any may be NULL): bytes of
+ * packed codes, number of fp16 scales, bytes of QJL sign bits. */
+int tq_layout_sizes(const tq_layout* layout, int64_t* code_bytes_per_vec,
+                    int64_t* scales_per_vec, int64_t* qjl_bytes_per_vec);
+
+/* Quantise n_vec vectors (device).
+ *   x            device, row i at x + i*x_row_stride elements, x_dtype
+ *                fp16 or fp32; rows of d contiguous elements; the row
+ *                start must be 16-byte aligned.
+ *   S            device fp32 [qjl_m, d] row major (QJL only, else NULL)
+ *   codes        device [n_vec, code_bytes_per_vec]
+ *   scales       device fp16 [n_vec, d/block]
+ *   qjl_bits     device [n_vec, qjl_m/8]   (QJL only, else NULL)
+ *   qjl_rnorm    device fp16 [n_vec]       (QJL only, else NULL)
+ * Steps: norm split, y = H D u, code = #{k : y > beta_k}, optional norm
+ * correction and QJL, pack (llama.cpp-turboquant, "How it works", Encode).
+ * A zero block gets scale 0 (and, with QJL, rho 0 and all sign bits 1). */
+int tq_quantize_kv(const tq_layout* layout, const void* x, tq_dtype x_dtype, int64_t n_vec,
+                   int64_t x_row_stride, const float* S, uint8_t* codes, uint16_t* scales,
+                   uint8_t* qjl_bits, uint16_t* qjl_rnorm, void* stream);
+
+/* Decode n_vec packed vectors (device) into out [n_vec, d] (fp16 or fp32):
+ * x~ = scale * D H (c + [QJL] rho sqrt(pi/2)/m H D S^T (2s - 1)), i.e.
+ * unpack -> centroid lookup -> inverse rotation -> x scale
+ * (llama.cpp-turboquant, "How it works", Decode; "TurboQuant From
+ * Scratch", section 2, un-rotation and QJL term). */
+int tq_dequantize_kv(const tq_layout* layout, const uint8_t* codes, const uint16_t* scales,
+                     const uint8_t* qjl_bits, const uint16_t* qjl_rnorm, const float* S,
+                     int64_t n_vec, void* out, tq_dtype out_dtype, void* stream);
+
+/* A packed cache of shape [B, Hkv, S_cap] vectors, tokens contiguous within
+ * a (batch, head): record (b, h, t) is vector index (b*Hkv + h)*S_cap + t
+ * of the per-vector arrays above.  All pointers device. */
+typedef struct {
+  const uint8_t* codes;
+  const uint16_t* scales;
+  const uint8_t* qjl_bits;   /* NULL unless layout.qjl_m > 0 */
+  const uint16_t* qjl_rnorm; /* NULL unless layout.qjl_m > 0 */
+  const float* S;            /* NULL unless layout.qjl_m > 0 */
+  tq_layout layout;
+} tq_kv_view;
+
+/* Fused decode attention over the packed cache: one query per
+ * (batch, q-head), q fp16 [B, Hq, d] device, out fp16 [B, Hq, d] device.
+ * q-head h reads KV head h / (Hq/Hkv); batch b attends positions
+ * [0, kv_len[b]) (kv_len: device int32 [B], or NULL for ctx everywhere;
+ * every kv_len[b] must be <= ctx <= S_cap).  softmax_scale <= 0 selects
+ * 1/sqrt(d).  Scores are formed in the rotated domain, <H D q, c> scaled
+ * by the block norms, V is accumulated rotated and rotated back once per
+ * output ("llama.cpp-turboquant", "Fused tile path": K side <Hc,q> =
+ * <c,Hq>, V side sum p_j H c_j = H sum p_j c_j); online fp32 softmax with
+ * the context split into n_split parts merged by log-sum-exp
+ * (n_split = 0: chosen by the library).  workspace: device, at least
+ * tq_decode_workspace_bytes(...) bytes, 16-byte aligned.  With QJL keys the
+ * score adds ||k|| rho sqrt(pi/2)/m <S q, 2s - 1> ("turboquant-pytorch",
+ * "The combined estimator"). */
+int tq_decode_attn(const tq_kv_view* K, const tq_kv_view* V, const uint16_t* q, int B, int Hq,
+                   int Hkv, int64_t S_cap, const int32_t* kv_len, int64_t ctx,
+                   float softmax_scale, uint16_t* out, void* workspace, size_t workspace_bytes,
+                   int n_split, void* stream);
+
+/* Workspace bytes for tq_decode_attn with these sizes (host).  n_split = 0
+ * gives the size for the library's own choice; *n_split_out (may be NULL)
+ * receives the split count that will be used. */
+int tq_decode_workspace_bytes(int B, int Hq, int Hkv, int head_dim, int64_t ctx, int n_split,
+                              size_t* bytes, int* n_split_out);
+
+/* Prefill attention: Tq queries per (batch, q-head) at positions
+ * ctx-Tq .. ctx-1 over cache positions [0, ctx); q fp16 [B, Hq, Tq, d],
+ * out fp16 [B, Hq, Tq, d], both device.  causal != 0: query i attends
+ * positions <= ctx-Tq+i (bottom-right aligned).  K/V tiles are decoded into
+ * shared memory (rotated domain, scaled) and QK^T / PV run on the tensor
+ * cores ("llama.cpp-turboquant", "Prompt processing": the conversion
+ * amortises over the query batch).  QJL keys are not supported here
+ * (TQ_ERR_UNSUPPORTED).  workspace: device, >= tq_prefill_workspace_bytes. */
+int tq_prefill_attn(const tq_kv_view* K, const tq_kv_view* V, const uint16_t* q, int B, int Hq,
+                    int Hkv, int Tq, int64_t S_cap, int64_t ctx, int causal, float softmax_scale,
+                    uint16_t* out, void* workspace, size_t workspace_bytes, void* stream);
+
+int tq_prefill_workspace_bytes(int B, int Hq, int Hkv, int head_dim, int Tq, int64_t ctx,
+                               size_t* bytes);
+
+/* Human-readable text of a tq_status (static storage). */
+const char* tq_strerror(int status);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int tq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TQ_H_ */

@@ -25,3 +25,12 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture(scope="session")
+def tqlib():
+    """The ctypes handle of libtq.so, building it first if it is missing."""
+    from turboquant_kv_cache_gb300 import binding, build
+    if not os.path.exists(build.LIB):
+        build.build()
+    return binding.library()

@@ -1,0 +1,97 @@
+"""The C ABI without a GPU: the library loads, exports every function the
+header declares, and its host-side calls agree with the oracle."""
+import ctypes
+import math
+import os
+import re
+
+import numpy as np
+import pytest
+
+from oracle import tq_oracle as O
+from turboquant_kv_cache_gb300 import binding as tb
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "tq.h")
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(tq_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(tqlib):
+    names = _declared()
+    assert "tq_quantize_kv" in names and "tq_decode_attn" in names and "tq_prefill_attn" in names
+    for n in names:
+        assert hasattr(tqlib, n), n
+
+
+@pytest.mark.parametrize("bits", [1, 2, 3, 4])
+@pytest.mark.parametrize("block", [32, 64, 128, 256])
+def test_codebook_matches_oracle(tqlib, bits, block):
+    c, b = tb.tq_codebook(bits, block, f64=True)
+    oc, ob = O.lloyd_max_codebook(bits, block)
+    assert np.max(np.abs(np.array(c) - oc)) < 1e-12
+    assert np.max(np.abs(np.array(b) - ob)) < 1e-12
+    cf, bf = tb.tq_codebook(bits, block)
+    assert np.array_equal(np.array(cf, dtype=np.float32), oc.astype(np.float32))
+    assert np.array_equal(np.array(bf, dtype=np.float32), ob.astype(np.float32))
+
+
+@pytest.mark.parametrize("seed", [0, 1, 7, 2 ** 63 + 5])
+def test_signs_match_oracle(tqlib, seed):
+    assert tb.tq_signs(seed, 256) == [int(v) for v in O.sign_vector(seed, 256)]
+
+
+def test_layout_sizes(tqlib):
+    assert tb.tq_layout_sizes(tb.make_layout(128, 32, 3)) == (48, 4, 0)
+    assert tb.tq_layout_sizes(tb.make_layout(256, 32, 4)) == (128, 8, 0)
+    assert tb.tq_layout_sizes(tb.make_layout(128, 128, 2, qjl_m=128)) == (32, 1, 16)
+    L = O.Layout(128, 32, 3)
+    assert tb.tq_layout_sizes(tb.make_layout(128, 32, 3))[0] == L.code_bytes
+
+
+@pytest.mark.parametrize("args,status", [
+    ((96, 32, 3), -2), ((128, 16, 3), -2), ((128, 48, 3), -2), ((128, 32, 5), -2), ((128, 32, 0), -2),
+])
+def test_invalid_layouts_rejected(tqlib, args, status):
+    L = tb.make_layout(*args)
+    assert tqlib.tq_layout_sizes(ctypes.byref(L), None, None, None) == status
+
+
+def test_qjl_layout_rules(tqlib):
+    assert tqlib.tq_layout_sizes(ctypes.byref(tb.make_layout(128, 32, 2, qjl_m=128)), None, None, None) == -2
+    assert tqlib.tq_layout_sizes(ctypes.byref(tb.make_layout(128, 128, 2, qjl_m=48)), None, None, None) == -2
+    assert tqlib.tq_layout_sizes(ctypes.byref(tb.make_layout(128, 128, 2, qjl_m=512)), None, None, None) == -2
+
+
+def test_host_side_argument_checks_need_no_gpu(tqlib):
+    L = tb.make_layout(128, 32, 3)
+    # zero vectors: nothing to do
+    assert tqlib.tq_quantize_kv(ctypes.byref(L), None, 0, 0, 128, None, None, None, None, None, None) == 0
+    # missing buffers / bad stride / misaligned pointers are refused before any launch
+    assert tqlib.tq_quantize_kv(ctypes.byref(L), None, 0, 4, 128, None, None, None, None, None, None) == -1
+    assert tqlib.tq_quantize_kv(ctypes.byref(L), ctypes.c_void_p(16), 0, 4, 64, None,
+                                ctypes.c_void_p(16), ctypes.c_void_p(16), None, None, None) == -1
+    assert tqlib.tq_quantize_kv(ctypes.byref(L), ctypes.c_void_p(18), 0, 4, 128, None,
+                                ctypes.c_void_p(16), ctypes.c_void_p(16), None, None, None) == -3
+    assert tqlib.tq_quantize_kv(ctypes.byref(L), ctypes.c_void_p(16), 2, 4, 128, None,
+                                ctypes.c_void_p(16), ctypes.c_void_p(16), None, None, None) == -1
+    bad = tb.tq_layout(128, 32, 3, 0, 0, 7, 1)  # reserved field set
+    assert tqlib.tq_layout_sizes(ctypes.byref(bad), None, None, None) == -1
+
+
+def test_decode_workspace_query(tqlib):
+    nb, ns = tb.tq_decode_workspace_bytes(8, 32, 8, 128, 32768, 16)
+    assert ns == 16 and nb == 8 * 32 * 16 * (128 + 4) * 4
+    nb, ns = tb.tq_decode_workspace_bytes(1, 16, 4, 256, 131072, 0)
+    assert ns >= 1 and nb == 16 * ns * (256 + 4) * 4
+    with pytest.raises(tb.TQError):
+        tb.tq_decode_workspace_bytes(2, 6, 4, 128, 100)
+
+
+def test_strerror_and_version(tqlib):
+    assert tb.tq_strerror(0) == "ok"
+    assert "workspace" in tb.tq_strerror(-4)
+    assert tb.tq_version() >= 100

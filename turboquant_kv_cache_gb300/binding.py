@@ -1,0 +1,254 @@
+"""Thin Python binding of libtq (the C ABI in include/tq.h).
+
+Argument marshalling only: every function here checks shapes, takes raw
+pointers from torch tensors, calls the C entry point of the same name on the
+caller's current CUDA stream and raises TQError on a non-zero status.  All
+computation happens in the library's CUDA kernels; there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libtq.so")
+_lib = None
+
+TQ_F16, TQ_F32 = 0, 1
+
+
+class TQError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        msg = _load().tq_strerror(status).decode() if _lib is not None else str(status)
+        super().__init__(f"{where}: tq status {status} ({msg})")
+
+
+class tq_layout(ctypes.Structure):
+    _fields_ = [("head_dim", ctypes.c_int32), ("block", ctypes.c_int32), ("bits", ctypes.c_int32),
+                ("qjl_m", ctypes.c_int32), ("norm_correct", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("sign_seed", ctypes.c_uint64)]
+
+
+class tq_kv_view(ctypes.Structure):
+    _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("qjl_bits", ctypes.c_void_p),
+                ("qjl_rnorm", ctypes.c_void_p), ("S", ctypes.c_void_p), ("layout", tq_layout)]
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise RuntimeError(f"libtq.so not built at {_LIB_PATH}: run `python -m turboquant_kv_cache_gb300.build`")
+    lib = ctypes.CDLL(_LIB_PATH)
+    P, I, I64, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+    sig = {
+        "tq_codebook": (I, [I, I, P, P]),
+        "tq_codebook_f64": (I, [I, I, P, P]),
+        "tq_signs": (I, [ctypes.c_uint64, I, P]),
+        "tq_layout_sizes": (I, [P, P, P, P]),
+        "tq_quantize_kv": (I, [P, P, I, I64, I64, P, P, P, P, P, P]),
+        "tq_dequantize_kv": (I, [P, P, P, P, P, P, I64, P, I, P]),
+        "tq_decode_attn": (I, [P, P, P, I, I, I, I64, P, I64, ctypes.c_float, P, P, SZ, I, P]),
+        "tq_decode_workspace_bytes": (I, [I, I, I, I, I64, I, P, P]),
+        "tq_prefill_attn": (I, [P, P, P, I, I, I, I, I64, I64, I, ctypes.c_float, P, P, SZ, P]),
+        "tq_prefill_workspace_bytes": (I, [I, I, I, I, I, I64, P]),
+        "tq_strerror": (ctypes.c_char_p, [I]),
+        "tq_version": (I, []),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def library():
+    """The loaded ctypes library (raises if libtq.so is missing)."""
+    return _load()
+
+
+# ------------------------------------------------------------------ helpers
+def make_layout(head_dim, block, bits, qjl_m=0, norm_correct=0, sign_seed=1):
+    return tq_layout(head_dim, block, bits, qjl_m, norm_correct, 0, sign_seed)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(st, where):
+    if st != 0:
+        raise TQError(st, where)
+
+
+def _dtype_code(dt):
+    if dt == torch.float16:
+        return TQ_F16
+    if dt == torch.float32:
+        return TQ_F32
+    raise TypeError(f"unsupported dtype {dt}")
+
+
+# ------------------------------------------------------------------ host calls
+def tq_codebook(bits, block, f64=False):
+    """(centroids, boundaries) as Python lists (host call)."""
+    lib = _load()
+    K = 1 << bits
+    T = ctypes.c_double if f64 else ctypes.c_float
+    c = (T * K)()
+    b = (T * max(K - 1, 1))()
+    _check((lib.tq_codebook_f64 if f64 else lib.tq_codebook)(bits, block, c, b), "tq_codebook")
+    return list(c), list(b)[:K - 1]
+
+
+def tq_signs(sign_seed, d):
+    lib = _load()
+    out = (ctypes.c_int8 * d)()
+    _check(lib.tq_signs(ctypes.c_uint64(sign_seed), d, out), "tq_signs")
+    return list(out)
+
+
+def tq_layout_sizes(layout):
+    lib = _load()
+    cb, ns, qb = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+    _check(lib.tq_layout_sizes(ctypes.byref(layout), ctypes.byref(cb), ctypes.byref(ns), ctypes.byref(qb)),
+           "tq_layout_sizes")
+    return cb.value, ns.value, qb.value
+
+
+def tq_decode_workspace_bytes(B, Hq, Hkv, head_dim, ctx, n_split=0):
+    lib = _load()
+    nb, ns = ctypes.c_size_t(), ctypes.c_int()
+    _check(lib.tq_decode_workspace_bytes(B, Hq, Hkv, head_dim, ctx, n_split, ctypes.byref(nb), ctypes.byref(ns)),
+           "tq_decode_workspace_bytes")
+    return nb.value, ns.value
+
+
+def tq_prefill_workspace_bytes(B, Hq, Hkv, head_dim, Tq, ctx):
+    lib = _load()
+    nb = ctypes.c_size_t()
+    _check(lib.tq_prefill_workspace_bytes(B, Hq, Hkv, head_dim, Tq, ctx, ctypes.byref(nb)),
+           "tq_prefill_workspace_bytes")
+    return nb.value
+
+
+# ------------------------------------------------------------------ packed cache
+class PackedKV:
+    """Device buffers of one packed cache (K or V): codes [N, code_bytes]
+    uint8, scales [N, d/block] fp16, and with QJL qjl [N, m/8] uint8, rnorm
+    [N] fp16 and the projection S [m, d] fp32.  N may carry leading dims."""
+
+    def __init__(self, layout, lead_shape, device="cuda", S=None):
+        cb, ns, qb = tq_layout_sizes(layout)
+        self.layout = layout
+        self.lead_shape = tuple(lead_shape)
+        self.codes = torch.empty(self.lead_shape + (cb,), dtype=torch.uint8, device=device)
+        self.scales = torch.empty(self.lead_shape + (ns,), dtype=torch.float16, device=device)
+        self.qjl = torch.empty(self.lead_shape + (qb,), dtype=torch.uint8, device=device) if qb else None
+        self.rnorm = torch.empty(self.lead_shape, dtype=torch.float16, device=device) if qb else None
+        self.S = S
+
+    @property
+    def n_vec(self):
+        n = 1
+        for s in self.lead_shape:
+            n *= s
+        return n
+
+    def view(self):
+        return tq_kv_view(self.codes.data_ptr(), self.scales.data_ptr(),
+                          self.qjl.data_ptr() if self.qjl is not None else None,
+                          self.rnorm.data_ptr() if self.rnorm is not None else None,
+                          self.S.data_ptr() if self.S is not None else None, self.layout)
+
+    def nbytes(self):
+        n = self.codes.numel() + 2 * self.scales.numel()
+        if self.qjl is not None:
+            n += self.qjl.numel() + 2 * self.rnorm.numel()
+        return n
+
+
+# ------------------------------------------------------------------ device calls
+def tq_quantize_kv(layout, x, S=None, out=None, stream=None):
+    """Quantise x [..., d] (fp16/fp32, CUDA, last dim contiguous) into a
+    PackedKV with leading shape x.shape[:-1]."""
+    lib = _load()
+    d = layout.head_dim
+    if x.shape[-1] != d or x.stride(-1) != 1:
+        raise ValueError("x must have a contiguous last dimension of head_dim")
+    lead = tuple(x.shape[:-1])
+    x2 = x.reshape(-1, d)
+    if out is None:
+        out = PackedKV(layout, lead, device=x.device, S=S)
+    n = x2.shape[0]
+    st = lib.tq_quantize_kv(ctypes.byref(layout), _ptr(x2), _dtype_code(x.dtype), n, x2.stride(0), _ptr(S),
+                            _ptr(out.codes), _ptr(out.scales), _ptr(out.qjl), _ptr(out.rnorm), _stream(stream))
+    _check(st, "tq_quantize_kv")
+    return out
+
+
+def tq_dequantize_kv(packed, out_dtype=torch.float16, stream=None):
+    lib = _load()
+    d = packed.layout.head_dim
+    out = torch.empty(packed.lead_shape + (d,), dtype=out_dtype, device=packed.codes.device)
+    st = lib.tq_dequantize_kv(ctypes.byref(packed.layout), _ptr(packed.codes), _ptr(packed.scales),
+                              _ptr(packed.qjl), _ptr(packed.rnorm), _ptr(packed.S), packed.n_vec, _ptr(out),
+                              _dtype_code(out_dtype), _stream(stream))
+    _check(st, "tq_dequantize_kv")
+    return out
+
+
+def tq_decode_attn(K, V, q, ctx=None, kv_len=None, softmax_scale=0.0, n_split=0, workspace=None, out=None,
+                   stream=None):
+    """q [B, Hq, d] fp16; K, V PackedKV with lead shape [B, Hkv, S_cap]."""
+    lib = _load()
+    B, Hq, d = q.shape
+    _, Hkv, S_cap = K.lead_shape
+    ctx = S_cap if ctx is None else ctx
+    need, ns = tq_decode_workspace_bytes(B, Hq, Hkv, d, ctx, n_split)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    kv, vv = K.view(), V.view()
+    st = lib.tq_decode_attn(ctypes.byref(kv), ctypes.byref(vv), _ptr(q), B, Hq, Hkv, S_cap, _ptr(kv_len), ctx,
+                            float(softmax_scale), _ptr(out), _ptr(workspace), workspace.numel(), n_split,
+                            _stream(stream))
+    _check(st, "tq_decode_attn")
+    return out
+
+
+def tq_prefill_attn(K, V, q, ctx, causal=True, softmax_scale=0.0, workspace=None, out=None, stream=None):
+    """q [B, Hq, Tq, d] fp16 at positions ctx-Tq .. ctx-1."""
+    lib = _load()
+    B, Hq, Tq, d = q.shape
+    _, Hkv, S_cap = K.lead_shape
+    need = tq_prefill_workspace_bytes(B, Hq, Hkv, d, Tq, ctx)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    kv, vv = K.view(), V.view()
+    st = lib.tq_prefill_attn(ctypes.byref(kv), ctypes.byref(vv), _ptr(q), B, Hq, Hkv, Tq, S_cap, ctx,
+                             1 if causal else 0, float(softmax_scale), _ptr(out), _ptr(workspace),
+                             workspace.numel(), _stream(stream))
+    _check(st, "tq_prefill_attn")
+    return out
+
+
+def tq_strerror(status):
+    return _load().tq_strerror(status).decode()
+
+
+def tq_version():
+    return _load().tq_version()

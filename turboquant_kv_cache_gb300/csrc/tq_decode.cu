@@ -1,0 +1,391 @@
+// Fused decode attention over the packed cache, computed in the Hadamard
+// domain, plus the split-K combine that rotates the output back.
+//
+// Per CTA: one (batch, KV head) and one slice of the context.  The G query
+// heads of the GQA group share every K/V record read.  The query is rotated
+// once (q^ = H D q per K block, times softmax_scale * log2 e); a score is
+// sum_j scaleK_j <q^_j, c(codes_j)> (+ the QJL term); V is accumulated
+// rotated, sum_t p_t scaleV c(codes_t); the combine merges the splits by
+// log-sum-exp and applies D H once per output ("llama.cpp-turboquant",
+// "Fused tile path: K and V decoded inside attention").
+#include <cuda_runtime.h>
+#include <math.h>
+
+#include "tq_device.cuh"
+
+namespace tq {
+
+int decode_auto_splits(int B, int Hkv, int64_t ctx);
+size_t decode_ws_bytes(int B, int Hq, int d, int n_split);
+
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kDecThreads = kWarps * 32;
+
+struct DecodeArgs {
+  const uint32_t* kc;
+  const uint16_t* ks;
+  const uint32_t* kq;   // QJL bits
+  const uint16_t* kr;   // QJL rho
+  const float* S;
+  const uint32_t* vc;
+  const uint16_t* vs;
+  const uint16_t* q;
+  const int32_t* kv_len;
+  float* part;          // [B*Hq][n_split][d + 4]
+  int64_t S_cap;
+  int64_t ctx;
+  int Hq, Hkv, n_split;
+  float qscale;         // softmax_scale * log2(e)
+};
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+  return v;
+}
+
+// In-place orthonormal Walsh-Hadamard on rows of a shared [rows][D] array,
+// in blocks of `blk`, executed by the whole CTA.
+template <int D>
+__device__ void smem_wht(float* a, int rows, int blk, float norm) {
+  for (int h = 1; h < blk; h <<= 1) {
+    __syncthreads();
+    for (int e = threadIdx.x; e < rows * D / 2; e += blockDim.x) {
+      const int row = e / (D / 2), k = e % (D / 2);
+      const int i = (k / h) * 2 * h + (k % h);
+      float* r = a + row * D;
+      const float x = r[i], y = r[i + h];
+      r[i] = x + y;
+      r[i + h] = x - y;
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < rows * D; e += blockDim.x) a[e] *= norm;
+  __syncthreads();
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const CodecParams PK, const CodecParams PV,
+                                                                   const DecodeArgs a) {
+  constexpr int CPL = D / 32;  // V coordinates per lane
+  __shared__ float s_q[G][D];          // q, then q^ (rotated, scaled)
+  __shared__ float s_qT[D][G];         // q^ transposed: coordinate-major
+  __shared__ float s_sq[kMaxQjl][G];   // S q (QJL keys)
+  __shared__ float s_centK[16], s_centV[16];
+  __shared__ float s_p[kWarps][32][G];
+  __shared__ float s_ml[kWarps][2][G];
+  __shared__ float s_acc[kWarps][D];   // one head at a time in the final merge
+
+  const int split = blockIdx.x;
+  const int bh = blockIdx.y;           // b * Hkv + kv head
+  const int b = bh / a.Hkv;
+  const int kvh = bh % a.Hkv;
+  const int h0 = kvh * G;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+
+  if (threadIdx.x < 16) {
+    s_centK[threadIdx.x] = PK.centroids[threadIdx.x];
+    s_centV[threadIdx.x] = PV.centroids[threadIdx.x];
+  }
+  for (int e = threadIdx.x; e < G * D; e += kDecThreads) {
+    const int h = e / D, i = e % D;
+    s_q[h][i] = h2f(a.q[((int64_t)b * a.Hq + h0 + h) * D + i]);
+  }
+  __syncthreads();
+  if (PK.m) {  // S q in the input domain, scaled like the scores
+    for (int e = threadIdx.x; e < PK.m * G; e += kDecThreads) {
+      const int i = e / G, h = e % G;
+      float acc = 0.f;
+      for (int k = 0; k < D; ++k) acc = fmaf(__ldg(a.S + (int64_t)i * D + k), s_q[h][k], acc);
+      s_sq[i][h] = acc * a.qscale;
+    }
+  }
+  for (int e = threadIdx.x; e < G * D; e += kDecThreads) {
+    const int h = e / D, i = e % D;
+    if ((PK.sign_bits[i >> 5] >> (i & 31)) & 1u) s_q[h][i] = -s_q[h][i];
+  }
+  smem_wht<D>(&s_q[0][0], G, PK.blk, PK.inv_sqrt_blk * a.qscale);
+  for (int e = threadIdx.x; e < G * D; e += kDecThreads) {
+    const int h = e / D, i = e % D;
+    s_qT[i][h] = s_q[h][i];
+  }
+  __syncthreads();
+
+  int64_t len = a.ctx;
+  if (a.kv_len) len = imin64(len, (int64_t)a.kv_len[b]);
+  const int64_t per = (a.ctx + a.n_split - 1) / a.n_split;
+  const int64_t t_begin = (int64_t)split * per;
+  const int64_t t_end = imin64(t_begin + per, len);
+
+  float m_run[G], l_run[G], acc[G][CPL];
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    m_run[h] = -INFINITY;
+    l_run[h] = 0.f;
+#pragma unroll
+    for (int k = 0; k < CPL; ++k) acc[h][k] = 0.f;
+  }
+  const int kwords = PK.code_bytes / 4, vwords = PV.code_bytes / 4;
+  const int64_t rec0 = (int64_t)bh * a.S_cap;
+
+  for (int64_t c0 = t_begin + (int64_t)wid * 32; c0 < t_end; c0 += kWarps * 32) {
+    const int64_t t = c0 + lane;
+    const bool valid = t < t_end;
+    float s[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) s[h] = 0.f;
+    if (valid) {
+      const uint32_t* rec = a.kc + (rec0 + t) * kwords;
+      const uint16_t* sc = a.ks + (rec0 + t) * PK.nb;
+      const int gpb = PK.blk / 32;  // 32-code groups per block
+      for (int j = 0; j < PK.nb; ++j) {
+        float part[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) part[h] = 0.f;
+        for (int gg = 0; gg < gpb; ++gg) {
+          const int gi = j * gpb + gg;
+          const uint32_t* gw = rec + gi * PK.bits;
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            const uint32_t nib = load_chunk(gw, PK.bits, w);
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+              const float c = s_centK[(nib >> (4 * r)) & 0xf];
+              const int i = gi * 32 + w * 8 + r;
+#pragma unroll
+              for (int h = 0; h < G; ++h) part[h] = fmaf(c, s_qT[i][h], part[h]);
+            }
+          }
+        }
+        const float scj = h2f(sc[j]);
+#pragma unroll
+        for (int h = 0; h < G; ++h) s[h] = fmaf(scj, part[h], s[h]);
+      }
+      if (PK.m) {
+        const float coef = h2f(sc[0]) * h2f(a.kr[rec0 + t]) * kSqrtHalfPi / (float)PK.m;
+        const uint32_t* qb = a.kq + (rec0 + t) * (PK.m / 32);
+        float part[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) part[h] = 0.f;
+        for (int i = 0; i < PK.m; ++i) {
+          const float sgn = ((qb[i >> 5] >> (i & 31)) & 1u) ? 1.f : -1.f;
+#pragma unroll
+          for (int h = 0; h < G; ++h) part[h] = fmaf(sgn, s_sq[i][h], part[h]);
+        }
+#pragma unroll
+        for (int h = 0; h < G; ++h) s[h] = fmaf(coef, part[h], s[h]);
+      }
+    } else {
+#pragma unroll
+      for (int h = 0; h < G; ++h) s[h] = -INFINITY;
+    }
+    // online softmax (base 2), one update per 32-token chunk
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      const float mx = warp_max(s[h]);
+      const float m_new = fmaxf(m_run[h], mx);
+      const float p = valid ? exp2f(s[h] - m_new) : 0.f;
+      const float alpha = m_run[h] == -INFINITY ? 0.f : exp2f(m_run[h] - m_new);
+      l_run[h] = l_run[h] * alpha + warp_sum(p);
+      m_run[h] = m_new;
+#pragma unroll
+      for (int k = 0; k < CPL; ++k) acc[h][k] *= alpha;
+      s_p[wid][lane][h] = p;
+    }
+    __syncwarp();
+    const int n_tok = (int)imin64(32, t_end - c0);
+    for (int tt = 0; tt < n_tok; ++tt) {
+      const int64_t r = rec0 + c0 + tt;
+      const uint32_t* rec = a.vc + r * vwords;
+      const uint16_t* sc = a.vs + r * PV.nb;
+#pragma unroll
+      for (int k = 0; k < CPL; ++k) {
+        const int i = lane + 32 * k;
+        const float v = s_centV[code_at(rec, PV.bits, i)] * h2f(sc[i / PV.blk]);
+#pragma unroll
+        for (int h = 0; h < G; ++h) acc[h][k] = fmaf(s_p[wid][tt][h], v, acc[h][k]);
+      }
+    }
+    __syncwarp();
+  }
+  // merge the warps of the CTA
+  if (lane == 0) {
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      s_ml[wid][0][h] = m_run[h];
+      s_ml[wid][1][h] = l_run[h];
+    }
+  }
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < CPL; ++k) s_acc[wid][lane + 32 * k] = acc[h][k];
+    __syncthreads();
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, s_ml[w][0][h]);
+    float* dst = a.part + (((int64_t)b * a.Hq + h0 + h) * a.n_split + split) * (D + 4);
+    for (int i = threadIdx.x; i < D + 2; i += kDecThreads) {
+      float val = 0.f;
+      if (i == 0) {
+        val = M;
+      } else {
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+          const float mw = s_ml[w][0][h];
+          const float wt = mw == -INFINITY ? 0.f : exp2f(mw - M);
+          val += wt * (i == 1 ? s_ml[w][1][h] : s_acc[w][i - 2]);
+        }
+      }
+      dst[i] = val;
+    }
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(256) decode_combine_kernel(const CodecParams PV, const float* __restrict__ part,
+                                                             int n_split, uint16_t* __restrict__ out) {
+  __shared__ float s_o[D];
+  __shared__ float s_M, s_L;
+  const int row = blockIdx.x;  // b * Hq + h
+  const float* p = part + (int64_t)row * n_split * (D + 4);
+  if (threadIdx.x == 0) {
+    float M = -INFINITY;
+    for (int s = 0; s < n_split; ++s) M = fmaxf(M, p[s * (D + 4)]);
+    float L = 0.f;
+    for (int s = 0; s < n_split; ++s) {
+      const float ms = p[s * (D + 4)];
+      if (ms != -INFINITY) L += exp2f(ms - M) * p[s * (D + 4) + 1];
+    }
+    s_M = M;
+    s_L = L;
+  }
+  __syncthreads();
+  const float M = s_M, L = s_L;
+  for (int i = threadIdx.x; i < D; i += blockDim.x) {
+    float o = 0.f;
+    for (int s = 0; s < n_split; ++s) {
+      const float ms = p[s * (D + 4)];
+      if (ms != -INFINITY) o += exp2f(ms - M) * p[s * (D + 4) + 2 + i];
+    }
+    s_o[i] = L > 0.f ? o / L : 0.f;
+  }
+  // back to the input domain: o = D H O per V block
+  for (int h = 1; h < PV.blk; h <<= 1) {
+    __syncthreads();
+    for (int k = threadIdx.x; k < D / 2; k += blockDim.x) {
+      const int i = (k / h) * 2 * h + (k % h);
+      const float x = s_o[i], y = s_o[i + h];
+      s_o[i] = x + y;
+      s_o[i + h] = x - y;
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < D; i += blockDim.x) {
+    const float v = flip(s_o[i] * PV.inv_sqrt_blk, (PV.sign_bits[i >> 5] >> (i & 31)) & 1u);
+    out[(int64_t)row * D + i] = f2h(v);
+  }
+}
+
+template <int D, int G>
+int launch_decode(const CodecParams& PK, const CodecParams& PV, const DecodeArgs& a, int B, cudaStream_t st) {
+  dim3 grid(a.n_split, B * a.Hkv);
+  decode_split_kernel<D, G><<<grid, kDecThreads, 0, st>>>(PK, PV, a);
+  if (cudaGetLastError() != cudaSuccess) return TQ_ERR_CUDA;
+  return TQ_OK;
+}
+
+template <int D>
+int launch_decode_g(int G, const CodecParams& PK, const CodecParams& PV, const DecodeArgs& a, int B,
+                    cudaStream_t st) {
+  switch (G) {
+    case 1: return launch_decode<D, 1>(PK, PV, a, B, st);
+    case 2: return launch_decode<D, 2>(PK, PV, a, B, st);
+    case 4: return launch_decode<D, 4>(PK, PV, a, B, st);
+    case 8: return launch_decode<D, 8>(PK, PV, a, B, st);
+    default: return TQ_ERR_UNSUPPORTED;
+  }
+}
+
+}  // namespace
+
+int sm_count() {
+  int dev = 0, sms = 152;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  return sms;
+}
+
+int decode_auto_splits(int B, int Hkv, int64_t ctx) {
+  const int units = B * Hkv;
+  int want = (8 * sm_count() + units - 1) / units;
+  const int64_t max_by_len = (ctx + 255) / 256;
+  if (want > max_by_len) want = (int)max_by_len;
+  if (want < 1) want = 1;
+  if (want > 4096) want = 4096;
+  return want;
+}
+
+size_t decode_ws_bytes(int B, int Hq, int d, int n_split) {
+  return (size_t)B * Hq * n_split * (d + 4) * sizeof(float);
+}
+
+}  // namespace tq
+
+extern "C" int tq_decode_workspace_bytes(int B, int Hq, int Hkv, int head_dim, int64_t ctx, int n_split,
+                                         size_t* bytes, int* n_split_out) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || ctx < 0 || n_split < 0 || !bytes) return TQ_ERR_ARG;
+  if (head_dim != 64 && head_dim != 128 && head_dim != 256) return TQ_ERR_UNSUPPORTED;
+  const int ns = n_split ? n_split : tq::decode_auto_splits(B, Hkv, ctx);
+  *bytes = tq::decode_ws_bytes(B, Hq, head_dim, ns);
+  if (n_split_out) *n_split_out = ns;
+  return TQ_OK;
+}
+
+extern "C" int tq_decode_attn(const tq_kv_view* K, const tq_kv_view* V, const uint16_t* q, int B, int Hq,
+                              int Hkv, int64_t S_cap, const int32_t* kv_len, int64_t ctx, float softmax_scale,
+                              uint16_t* out, void* workspace, size_t workspace_bytes, int n_split,
+                              void* stream) {
+  if (!K || !V || !q || !out) return TQ_ERR_ARG;
+  tq::CodecParams PK, PV;
+  int st = tq::make_params(&K->layout, &PK);
+  if (st != TQ_OK) return st;
+  st = tq::make_params(&V->layout, &PV);
+  if (st != TQ_OK) return st;
+  if (PK.d != PV.d || PV.m) return TQ_ERR_UNSUPPORTED;
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || ctx < 0 || ctx > S_cap || n_split < 0) return TQ_ERR_ARG;
+  if (!K->codes || !K->scales || !V->codes || !V->scales) return TQ_ERR_ARG;
+  if (PK.m && (!K->qjl_bits || !K->qjl_rnorm || !K->S)) return TQ_ERR_ARG;
+  if (!tq::aligned16(K->codes) || !tq::aligned16(V->codes) || !tq::aligned16(q) || !tq::aligned16(out))
+    return TQ_ERR_ALIGN;
+  const int ns = n_split ? n_split : tq::decode_auto_splits(B, Hkv, ctx);
+  const size_t need = tq::decode_ws_bytes(B, Hq, PK.d, ns);
+  if (!workspace || workspace_bytes < need) return TQ_ERR_WORKSPACE;
+  if (!tq::aligned16(workspace)) return TQ_ERR_ALIGN;
+  const float sm = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)PK.d);
+  tq::DecodeArgs a{reinterpret_cast<const uint32_t*>(K->codes), K->scales,
+                   reinterpret_cast<const uint32_t*>(K->qjl_bits), K->qjl_rnorm, K->S,
+                   reinterpret_cast<const uint32_t*>(V->codes), V->scales, q, kv_len,
+                   static_cast<float*>(workspace), S_cap, ctx, Hq, Hkv, ns, sm * tq::kLog2e};
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int G = Hq / Hkv;
+  switch (PK.d) {
+    case 64: st = tq::launch_decode_g<64>(G, PK, PV, a, B, s); break;
+    case 128: st = tq::launch_decode_g<128>(G, PK, PV, a, B, s); break;
+    default: st = tq::launch_decode_g<256>(G, PK, PV, a, B, s); break;
+  }
+  if (st != TQ_OK) return st;
+  switch (PK.d) {
+    case 64: tq::decode_combine_kernel<64><<<B * Hq, 64, 0, s>>>(PV, a.part, ns, out); break;
+    case 128: tq::decode_combine_kernel<128><<<B * Hq, 128, 0, s>>>(PV, a.part, ns, out); break;
+    default: tq::decode_combine_kernel<256><<<B * Hq, 256, 0, s>>>(PV, a.part, ns, out); break;
+  }
+  return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+}

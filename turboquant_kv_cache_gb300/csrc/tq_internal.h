@@ -1,0 +1,40 @@
+// Internal definitions shared by the host layer and the CUDA kernels of
+// libtq.  Nothing here is part of the public ABI (include/tq.h).
+#pragma once
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include "tq.h"
+
+namespace tq {
+
+constexpr int kMaxDim = 256;
+constexpr int kMaxQjl = 256;
+
+// Everything a kernel needs to know about one codec layout, passed by value
+// as a kernel parameter (no device-side state in the library).
+struct CodecParams {
+  int d;         // head_dim
+  int blk;       // rotation / norm block
+  int bits;      // MSE bits
+  int m;         // QJL rows (0 = none)
+  int nc;        // norm correction
+  int nb;        // d / blk
+  int code_bytes;  // d * bits / 8
+  int qjl_bytes;   // m / 8
+  float inv_sqrt_blk;                 // 1 / sqrt(blk)
+  uint32_t sign_bits[kMaxDim / 32];   // bit i set <=> D_i = -1
+  float centroids[16];                // ascending, 2^bits used
+  float bounds[16];                   // 2^bits - 1 used
+};
+
+// Fills `p` from a public layout; returns TQ_OK or a tq_status.
+int make_params(const tq_layout* layout, CodecParams* p);
+
+// Validates a public layout without building tables.
+int check_layout(const tq_layout* layout);
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace tq

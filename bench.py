@@ -1,0 +1,388 @@
+"""Benchmark of the TurboQuant KV-cache hot path on one GB300 (or N replicas).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+A step is one fused decode-attention pass (tq_decode_attn) over the packed
+turbo3 cache of a Qwen3-8B-shaped decode batch: B=8, 32 q-heads / 8 KV heads,
+head_dim 128, context 32768, 3-bit codes + one fp16 norm per 32 values.  The
+cache is built once by tq_quantize_kv from seeded N(0,1) fp16 K/V and is
+resident in HBM when timing starts.  `value` is compressed-cache GB/s
+(algorithmic bytes: every packed K/V byte of the context read once).  The
+quantize kernel is timed in the same run on the Llama-3.2-1B-shaped KV
+(16 layers x 8 heads x 2048 tokens x d=64, 4 outlier channels per head),
+4-bit, per-vector and block-32, reported as Gvectors/s.
+
+With --impl reference the float64 CPU oracle is timed instead, on a bounded
+sample of the same workload, on this host's cores.
+
+Multi-GPU: decode shards by (batch, KV head) with no exchange, so N ranks run
+N independent replicas of the workload (weak scaling, no collective on the
+data path; a barrier brackets the timed region).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "fused turbo3 decode-attn HBM GB/s (% of peak); KV quantize Gvectors/s"
+WORKLOAD = "Qwen3-8B-shaped decode: B=8, Hq=32, Hkv=8, d=128, ctx=32768, turbo3 K/V (3-bit + fp16 norm per 32)"
+DEC = dict(B=8, Hq=32, Hkv=8, d=128, ctx=32768)
+TURBO3 = dict(block=32, bits=3)
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def decode_bytes(B, Hkv, ctx, d, k_bits, v_bits, k_block, v_block):
+    """Algorithmic bytes of one decode pass: packed codes + fp16 scales of
+    every K and V token of the context, each read once."""
+    per_k = d * k_bits // 8 + 2 * (d // k_block)
+    per_v = d * v_bits // 8 + 2 * (d // v_block)
+    return B * Hkv * ctx * (per_k + per_v)
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """Samples nvidia-smi while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- GPU arm
+def run_gpu(args, rank, world):
+    import torch
+    from turboquant_kv_cache_gb300 import binding as tb
+    from turboquant_kv_cache_gb300 import inputs
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    B, Hq, Hkv, d, ctx = DEC["B"], DEC["Hq"], DEC["Hkv"], DEC["d"], DEC["ctx"]
+    L = tb.make_layout(d, TURBO3["block"], TURBO3["bits"], 0, 0, 1)
+    # the packed cache, built on the device from the seeded fp16 K/V
+    K = tb.PackedKV(L, (B, Hkv, ctx), device=dev)
+    V = tb.PackedKV(L, (B, Hkv, ctx), device=dev)
+    for b in range(B):                       # one batch row at a time bounds host memory
+        kb = inputs.gaussian((Hkv, ctx, d), 1000 * 11 + b)
+        vb = inputs.gaussian((Hkv, ctx, d), 1000 * 12 + b)
+        for src, dst in ((kb, K), (vb, V)):
+            part = tb.tq_quantize_kv(L, torch.from_numpy(src).to(dev))
+            dst.codes[b].copy_(part.codes)
+            dst.scales[b].copy_(part.scales)
+    q = torch.from_numpy(inputs.gaussian((B, Hq, d), 10)).to(dev)
+    ws_bytes, n_split = tb.tq_decode_workspace_bytes(B, Hq, Hkv, d, ctx, 0)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    out = torch.empty_like(q)
+    flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=dev)
+    nbytes = decode_bytes(B, Hkv, ctx, d, 3, 3, 32, 32)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        tb.tq_decode_attn(K, V, q, ctx=ctx, workspace=ws, out=out, n_split=n_split)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clocks:
+        t0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.zero_()                     # L2 flush between steps, outside the events
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+    if dist:
+        dist.barrier()
+    times = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms = statistics.mean(times)
+    ms_max = ms
+    if dist:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_max = float(t.item())
+    value = world * nbytes / (ms_max * 1e-3) / 1e9
+    peak, peak_kind = _peaks()
+
+    # end to end through the public API: per step, H2D of the new query and
+    # the new K/V token, append-quantise, decode, D2H of the output
+    e2e = e2e_decode(tb, torch, inputs, dev, K, V, L, ws, n_split, args)
+
+    quant = bench_quantize(tb, torch, inputs, dev, args)
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded N(0,1) fp16 K/V/q, quantised on device)",
+            "config": {"workload": WORKLOAD, "n_split": n_split, "algorithmic_bytes_per_step": nbytes,
+                       "l2": "cache 235 MB > L2 and a 512 MB write flushes L2 between steps (outside events)",
+                       "parallelism": f"replicas x{world}"},
+            "percent_of_peak": round(100 * value / world / peak, 2),
+            "roofline": {"bound": "hbm", "achieved": round(value / world, 2), "peak": peak,
+                         "unit": "GB/s", "frac": round(value / world / peak, 4), "traffic": None,
+                         "peak_source": f"{peak_kind} hbm_gbs (burst copy)",
+                         "kernel": "decode_split_kernel + decode_combine_kernel (one tq_decode_attn call)"},
+            "e2e": e2e,
+            "quantize": quant,
+            "gpu_launches": args.steps * 2,
+            "clocks": clocks.summary(),
+            "wall_s_timed": round(wall, 4),
+        }
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_budget)
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def e2e_decode(tb, torch, inputs, dev, K, V, L, ws, n_split, args):
+    B, Hq, Hkv, d, ctx = DEC["B"], DEC["Hq"], DEC["Hkv"], DEC["d"], DEC["ctx"]
+    q_h = torch.from_numpy(inputs.gaussian((B, Hq, d), 10)).pin_memory()
+    kv_h = torch.from_numpy(inputs.gaussian((2, B, Hkv, d), 13)).pin_memory()
+    out_h = torch.empty((B, Hq, d), dtype=torch.float16).pin_memory()
+    q_d = torch.empty((B, Hq, d), dtype=torch.float16, device=dev)
+    kv_d = torch.empty((2, B, Hkv, d), dtype=torch.float16, device=dev)
+    out_d = torch.empty_like(q_d)
+    # the new token of every (b, head) lands in cache slot ctx-1
+    k_slot = tb.PackedKV(L, (B, Hkv), device=dev)
+    nbytes = decode_bytes(B, Hkv, ctx, d, 3, 3, 32, 32)
+
+    def step():
+        q_d.copy_(q_h, non_blocking=True)
+        kv_d.copy_(kv_h, non_blocking=True)
+        for i, cache in enumerate((K, V)):
+            tb.tq_quantize_kv(L, kv_d[i], out=k_slot)
+            cache.codes[:, :, ctx - 1].copy_(k_slot.codes)
+            cache.scales[:, :, ctx - 1].copy_(k_slot.scales)
+        tb.tq_decode_attn(K, V, q_d, ctx=ctx, workspace=ws, out=out_d, n_split=n_split)
+        out_h.copy_(out_d, non_blocking=True)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    torch.cuda.synchronize()
+    dt = (time.perf_counter() - t0) / args.steps
+    return {"value": round(nbytes / dt / 1e9, 2), "unit": "GB/s",
+            "h2d_bytes_per_step": q_h.numel() * 2 + kv_h.numel() * 2,
+            "d2h_bytes_per_step": out_h.numel() * 2,
+            "note": "per step: H2D query + new K/V token, append-quantise, decode, D2H output; host clock"}
+
+
+def bench_quantize(tb, torch, inputs, dev, args):
+    w = inputs.llama1b_kv_workload()
+    k = torch.from_numpy(w["k"]).to(dev)
+    v = torch.from_numpy(w["v"]).to(dev)
+    n_vec = k.numel() // 64 + v.numel() // 64
+    flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=dev)
+    res = {"workload": "Llama-3.2-1B-shaped K and V: 16 layers x 8 heads x 2048 x d=64 fp16, 4 outlier channels x8",
+           "vectors_per_step": n_vec, "unit": "Gvectors/s"}
+    peak, _ = _peaks()
+    for name, block in (("per_vector", 64), ("block32", 32)):
+        L = tb.make_layout(64, block, 4, 0, 0, 1)
+        ok = tb.tq_quantize_kv(L, k)
+        ov = tb.tq_quantize_kv(L, v)
+        for _ in range(max(3, args.warmup)):
+            flush.zero_()
+            tb.tq_quantize_kv(L, k, out=ok)
+            tb.tq_quantize_kv(L, v, out=ov)
+        torch.cuda.synchronize()
+        times = []
+        for _ in range(args.steps):
+            flush.zero_()
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record()
+            tb.tq_quantize_kv(L, k, out=ok)
+            tb.tq_quantize_kv(L, v, out=ov)
+            e.record()
+            times.append((s, e))
+        torch.cuda.synchronize()
+        ms = statistics.mean(s.elapsed_time(e) for s, e in times)
+        bytes_per_vec = 64 * 2 + 64 * 4 // 8 + 2 * (64 // block)
+        gbs = n_vec * bytes_per_vec / (ms * 1e-3) / 1e9
+        res[name] = {"gvec_per_s": round(n_vec / (ms * 1e-3) / 1e9, 3), "ms": round(ms, 5),
+                     "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                                  "frac": round(gbs / peak, 4), "bytes_per_vector": bytes_per_vec}}
+    return res
+
+
+# ---------------------------------------------------------------- CPU oracle
+def _oracle_slice_inputs(b, kvh):
+    """Oracle-encoded packed K/V of one (batch, KV head) of the decode
+    workload (untimed) and its query group."""
+    from oracle import tq_oracle as O
+    from turboquant_kv_cache_gb300 import inputs
+    d, ctx, Hq, Hkv = DEC["d"], DEC["ctx"], DEC["Hq"], DEC["Hkv"]
+    L = O.Layout(d, TURBO3["block"], TURBO3["bits"], 0, 0, 1)
+    k = inputs.gaussian((Hkv, ctx, d), 1000 * 11 + b)[kvh]
+    v = inputs.gaussian((Hkv, ctx, d), 1000 * 12 + b)[kvh]
+    q = inputs.gaussian((DEC["B"], Hq, d), 10)[b]
+    g = Hq // Hkv
+    return L, O.encode(k, L), O.encode(v, L), q[kvh * g:(kvh + 1) * g]
+
+
+def oracle_decode_slice(L, kenc, venc, qg):
+    from oracle import tq_oracle as O
+    kd = O.dequantize(kenc[0], kenc[1], L)
+    vd = O.dequantize(venc[0], venc[1], L)
+    return O.decode_attention(qg[None], kd[None, None], vd[None, None])
+
+
+def _threads():
+    try:
+        from threadpoolctl import threadpool_info
+        return max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
+    except Exception:
+        return int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+
+
+def cpu_baseline(budget_s=12.0):
+    """Times the oracle (as it stands) on this host: dequantise + attend the
+    (batch 0, KV head 0) slice of the decode workload repeatedly until the
+    budget is spent (the slice is encoded once, untimed)."""
+    per_slice = decode_bytes(1, 1, DEC["ctx"], DEC["d"], 3, 3, 32, 32)
+    L, ke, ve, qg = _oracle_slice_inputs(0, 0)
+    done, elapsed = 0, 0.0
+    while elapsed < budget_s or done == 0:
+        t0 = time.perf_counter()
+        oracle_decode_slice(L, ke, ve, qg)
+        elapsed += time.perf_counter() - t0
+        done += 1
+    return {"value": round(done * per_slice / elapsed / 1e9, 5), "unit": "GB/s", "cores": _threads(),
+            "kind": "oracle",
+            "sample": f"{done} passes over one (batch, KV head) slice of the decode workload (32768 tokens: "
+                      f"float64 dequantise of K and V + attention of its 4 q-heads), {elapsed:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    steps = []
+    line_cpu = None
+    per_slice = decode_bytes(1, 1, DEC["ctx"], DEC["d"], 3, 3, 32, 32)
+    L, ke, ve, qg = _oracle_slice_inputs(0, 0)
+    for _ in range(args.warmup):
+        oracle_decode_slice(L, ke, ve, qg)
+    for i in range(args.steps):
+        t0 = time.perf_counter()
+        oracle_decode_slice(L, ke, ve, qg)
+        steps.append(time.perf_counter() - t0)
+    sec = statistics.mean(steps)
+    value = per_slice / sec / 1e9
+    line_cpu = {"value": round(value, 5), "unit": "GB/s", "cores": _threads(), "kind": "oracle",
+                "sample": "one (batch, KV head) slice per step: 32768 tokens, float64 dequantise of K and V + "
+                          "attention of its 4 q-heads"}
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 5), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) fp16 K/V/q)",
+        "config": {"workload": WORKLOAD, "sample": line_cpu["sample"]},
+        "cpu_baseline": line_cpu,
+        "e2e": {"value": round(value, 5), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="tq", choices=["tq", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    run_gpu(args, rank, world)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,116 @@
+"""GPU quantise / dequantise kernels against the float64 oracle, through
+the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import tq_oracle as O
+from turboquant_kv_cache_gb300 import inputs
+
+from _parity import (DEQ_RTOL, compare_codes, compare_qjl, compare_scales, fp16_ulp_diff, rel_l2, to_np,
+                     upload_packed)
+
+pytestmark = pytest.mark.gpu
+
+
+def _x(n, d, seed, dtype, heavy=False):
+    x = (inputs.student_t((n, d), seed, 4.0, np.float32) if heavy else inputs.gaussian((n, d), seed, np.float32))
+    x[3] = 0.0                       # a zero vector
+    x[5] *= 300.0                    # a large one
+    if n > 40:
+        x[40, :32] = 0.0             # a zero 32-block inside a nonzero vector
+    return x.astype(dtype)
+
+
+CASES = [
+    # d, block, bits, dtype, nc, qjl_m
+    (128, 128, 3, np.float32, 0, 0),     # unit-vector round trip shape
+    (128, 32, 3, np.float16, 0, 0),      # turbo3
+    (128, 32, 4, np.float16, 0, 0),      # turbo4
+    (64, 64, 4, np.float16, 0, 0),       # Llama-1B per-vector
+    (64, 32, 4, np.float16, 0, 0),       # Llama-1B block-32
+    (256, 32, 4, np.float16, 0, 0),      # d256 turbo4
+    (256, 32, 3, np.float16, 0, 0),
+    (256, 256, 2, np.float16, 0, 0),
+    (128, 64, 1, np.float32, 0, 0),
+    (128, 128, 2, np.float16, 1, 0),     # norm correction
+    (64, 32, 3, np.float32, 1, 0),
+    (128, 128, 2, np.float16, 0, 128),   # QJL keys
+    (128, 128, 3, np.float32, 0, 64),
+    (64, 64, 1, np.float16, 0, 32),
+    (256, 256, 2, np.float16, 0, 256),
+    (128, 128, 2, np.float16, 1, 128),   # QJL + norm correction
+]
+
+
+@pytest.mark.parametrize("d,blk,bits,dt,nc,m", CASES)
+def test_quantize_matches_oracle(tqlib, d, blk, bits, dt, nc, m):
+    from turboquant_kv_cache_gb300 import binding as tb
+    n = 1037                                   # ragged: not a multiple of any tile
+    x = _x(n, d, 100 + d + bits + m, dt, heavy=(d == 256))
+    S = inputs.qjl_matrix(m, d, 7) if m else None
+    L = tb.make_layout(d, blk, bits, m, nc, 1)
+    Lo = O.Layout(d, blk, bits, m, nc, 1)
+    xg = torch.from_numpy(x).cuda()
+    Sg = torch.from_numpy(S).cuda() if m else None
+    pk = tb.tq_quantize_kv(L, xg, S=Sg)
+    torch.cuda.synchronize()
+    oq = O.quantize(x, Lo, S)
+    n_code, rows = compare_codes(to_np(pk.codes), oq, Lo)
+    assert n_code <= max(5, n * d // 10000)
+    if not m or not nc:
+        compare_scales(to_np(pk.scales)[~rows], oq["scale"][~rows])
+    else:  # QJL + nc: the scale depends on every sign bit too
+        compare_scales(to_np(pk.scales)[~rows], oq["scale"][~rows], max_frac=2e-2)
+    if m:
+        compare_qjl(to_np(pk.qjl), oq, Lo, rows)
+        assert fp16_ulp_diff(to_np(pk.rnorm)[~rows], oq["rho"][~rows]).max() <= 1
+    assert np.all(to_np(pk.scales)[3] == 0)
+
+
+@pytest.mark.parametrize("d,blk,bits,dt,nc,m", CASES)
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.float16])
+def test_dequantize_matches_oracle(tqlib, d, blk, bits, dt, nc, m, out_dtype):
+    from turboquant_kv_cache_gb300 import binding as tb
+    n = 517
+    x = _x(n, d, 200 + d + bits, np.float32)
+    S = inputs.qjl_matrix(m, d, 9) if m else None
+    Lo = O.Layout(d, blk, bits, m, nc, 3)
+    codes, scales, qb, rho = O.encode(x, Lo, S)
+    ref = O.dequantize(codes, scales, Lo, qb, rho, S)
+    L = tb.make_layout(d, blk, bits, m, nc, 3)
+    pk = upload_packed(tb, L, Lo, codes, scales, qb, rho, (n,), S=torch.from_numpy(S).cuda() if m else None)
+    out = tb.tq_dequantize_kv(pk, out_dtype)
+    torch.cuda.synchronize()
+    got = to_np(out.float())
+    err = rel_l2(got, ref)
+    tol = DEQ_RTOL if out_dtype == torch.float16 else 1e-5
+    assert err.max() < tol, err.max()
+    assert np.all(got[3] == 0)
+
+
+def test_roundtrip_unit_vectors_mse(tqlib):
+    """4096 unit vectors, d=128, 3 bits: GPU quantise -> GPU dequantise MSE
+    against the oracle's closed-form distortion (3-bit: 0.0345)."""
+    from turboquant_kv_cache_gb300 import binding as tb
+    w = inputs.unit_roundtrip_workload()
+    x = torch.from_numpy(w["x"]).cuda()
+    L = tb.make_layout(128, 128, 3, 0, 0, 1)
+    pk = tb.tq_quantize_kv(L, x)
+    xr = tb.tq_dequantize_kv(pk, torch.float32)
+    mse = float(((xr - x) ** 2).sum(dim=1).mean())
+    assert abs(mse - O.relative_distortion(3)) / O.relative_distortion(3) < 0.05
+
+
+def test_quantize_row_stride_and_alignment(tqlib):
+    from turboquant_kv_cache_gb300 import binding as tb
+    base = torch.from_numpy(inputs.gaussian((64, 256), 5, np.float16)).cuda()
+    x = base[:, :128]                          # row stride 256 elements
+    L = tb.make_layout(128, 32, 3, 0, 0, 1)
+    a = tb.tq_quantize_kv(L, x)
+    b = tb.tq_quantize_kv(L, x.contiguous())
+    torch.cuda.synchronize()
+    assert torch.equal(a.codes, b.codes) and torch.equal(a.scales, b.scales)
+    with pytest.raises(tb.TQError) as e:
+        tb.tq_quantize_kv(L, base.reshape(-1)[1:1 + 128 * 63].reshape(63, 128))
+    assert e.value.status == -3

@@ -1,0 +1,100 @@
+"""Fused decode attention (tq_decode_attn) against the oracle: the oracle
+encodes the seeded K/V itself, the GPU attends over those packed bytes, and
+the oracle attends over its own explicit dequantisation (no Hadamard-domain
+shortcut), so the rotated-domain identities of the kernel are checked too."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import tq_oracle as O
+from turboquant_kv_cache_gb300 import inputs
+
+from _parity import ATTN_ATOL, to_np, upload_packed
+
+pytestmark = pytest.mark.gpu
+
+
+def _encode_cache(x, Lo, S=None):
+    """x [B, H, S, d] -> oracle packed arrays and its dequantised cache."""
+    B, H, Sc, d = x.shape
+    flat = x.reshape(-1, d)
+    codes, scales, qb, rho = O.encode(flat, Lo, S)
+    deq = O.dequantize(codes, scales, Lo, qb, rho, S).reshape(B, H, Sc, d)
+    return (codes, scales, qb, rho), deq
+
+
+def _run(tb, cfgK, cfgV, B, Hq, Hkv, S_cap, ctx, d, kv_len=None, n_split=0, seed=0, heavy_k=False, S=None):
+    Lk = O.Layout(d, *cfgK)
+    Lv = O.Layout(d, *cfgV)
+    k = (inputs.student_t((B, Hkv, S_cap, d), seed + 1, 4.0, np.float16) if heavy_k
+         else inputs.gaussian((B, Hkv, S_cap, d), seed + 1))
+    v = inputs.gaussian((B, Hkv, S_cap, d), seed + 2)
+    q = inputs.gaussian((B, Hq, d), seed + 3)
+    (kc, ks, kq, kr), kd = _encode_cache(k, Lk, S)
+    (vc, vs, _, _), vd = _encode_cache(v, Lv)
+    Sg = torch.from_numpy(S).cuda() if S is not None else None
+    K = upload_packed(tb, tb.make_layout(d, *cfgK), Lk, kc, ks, kq, kr, (B, Hkv, S_cap), S=Sg)
+    V = upload_packed(tb, tb.make_layout(d, *cfgV), Lv, vc, vs, None, None, (B, Hkv, S_cap))
+    kvl = torch.tensor(kv_len, dtype=torch.int32, device="cuda") if kv_len is not None else None
+    out = tb.tq_decode_attn(K, V, torch.from_numpy(q).cuda(), ctx=ctx, kv_len=kvl, n_split=n_split)
+    torch.cuda.synchronize()
+    lens = kv_len if kv_len is not None else [ctx] * B
+    ref = O.decode_attention(q, kd, vd, lens)
+    return to_np(out.float()), ref, vd
+
+
+CASES = [
+    # name, K (block, bits, m, nc, seed), V (...), B, Hq, Hkv, S_cap, ctx, d
+    ("turbo3_d128_gqa4", (32, 3, 0, 0, 1), (32, 3, 0, 0, 1), 2, 8, 2, 700, 650, 128),
+    ("turbo4k_turbo3v_d256", (32, 4, 0, 0, 1), (32, 3, 0, 0, 1), 1, 8, 2, 530, 513, 256),
+    ("pervec_d64_mha", (64, 4, 0, 0, 5), (32, 3, 0, 0, 6), 2, 2, 2, 300, 300, 64),
+    ("pervec_nc_d128_gqa2", (128, 3, 0, 1, 2), (128, 2, 0, 1, 3), 1, 4, 2, 257, 257, 128),
+    ("block64_d256_gqa8", (64, 3, 0, 0, 1), (64, 4, 0, 0, 2), 1, 8, 1, 200, 190, 256),
+    ("bits1_d128", (32, 1, 0, 0, 1), (32, 2, 0, 0, 1), 1, 4, 1, 100, 97, 128),
+]
+
+
+@pytest.mark.parametrize("name,cK,cV,B,Hq,Hkv,S_cap,ctx,d", CASES)
+@pytest.mark.parametrize("n_split", [0, 1, 7])
+def test_decode_matches_oracle(tqlib, name, cK, cV, B, Hq, Hkv, S_cap, ctx, d, n_split):
+    from turboquant_kv_cache_gb300 import binding as tb
+    got, ref, _ = _run(tb, cK, cV, B, Hq, Hkv, S_cap, ctx, d, n_split=n_split, heavy_k=(d == 256))
+    err = np.abs(got - ref).max()
+    assert err < ATTN_ATOL, (name, err)
+
+
+def test_decode_qjl_keys(tqlib):
+    from turboquant_kv_cache_gb300 import binding as tb
+    S = inputs.qjl_matrix(128, 128, 7)
+    got, ref, _ = _run(tb, (128, 2, 128, 0, 1), (128, 3, 0, 0, 1), 2, 8, 2, 400, 391, 128, S=S)
+    assert np.abs(got - ref).max() < ATTN_ATOL
+
+
+def test_decode_ragged_kv_len_and_empty(tqlib):
+    from turboquant_kv_cache_gb300 import binding as tb
+    got, ref, _ = _run(tb, (32, 3, 0, 0, 1), (32, 3, 0, 0, 1), 3, 8, 2, 520, 500, 128,
+                       kv_len=[500, 37, 0], n_split=5)
+    assert np.abs(got - ref).max() < ATTN_ATOL
+    assert np.all(got[2] == 0)
+
+
+def test_decode_single_token_returns_value(tqlib):
+    from turboquant_kv_cache_gb300 import binding as tb
+    got, ref, vd = _run(tb, (32, 3, 0, 0, 1), (32, 4, 0, 0, 1), 1, 4, 1, 64, 1, 128)
+    assert np.abs(got[0] - vd[0, 0, 0][None, :]).max() < ATTN_ATOL
+
+
+def test_decode_workspace_errors(tqlib):
+    from turboquant_kv_cache_gb300 import binding as tb
+    L = tb.make_layout(128, 32, 3)
+    K = tb.PackedKV(L, (1, 1, 64))
+    q = torch.zeros(1, 4, 128, dtype=torch.float16, device="cuda")
+    small = torch.empty(16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(tb.TQError) as e:
+        tb.tq_decode_attn(K, K, q, ctx=64, workspace=small)
+    assert e.value.status == -4
+    with pytest.raises(tb.TQError) as e:
+        tb.tq_decode_attn(K, K, q, ctx=65)
+    assert e.value.status == -1

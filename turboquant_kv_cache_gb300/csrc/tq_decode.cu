@@ -106,6 +106,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const CodecPa
       for (int k = 0; k < D; ++k) acc = fmaf(__ldg(a.S + (int64_t)i * D + k), s_q[h][k], acc);
       s_sq[i][h] = acc * a.qscale;
     }
+    __syncthreads();  // s_q is rotated in place below
   }
   for (int e = threadIdx.x; e < G * D; e += kDecThreads) {
     const int h = e / D, i = e % D;

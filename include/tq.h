@@ -165,6 +165,32 @@ int tq_decode_attn(const tq_kv_view* K, const tq_kv_view* V, const uint16_t* q, 
                    float softmax_scale, uint16_t* out, void* workspace, size_t workspace_bytes,
                    int n_split, void* stream);
 
+/* Size of the library-owned scratch array used by tq_decode_attn_static. */
+#define TQ_DECODE_STATIC_SCRATCH_BYTES (8u << 20)
+
+/* tq_decode_attn for callers that cannot allocate device memory.  No
+ * counterpart in the source pages: it exists for callers whose device
+ * memory is owned by someone else (a serving runtime or plugin host that
+ * hands out all memory from its own pool and forbids cudaMalloc after
+ * start-up) or who cannot pay for the implicit synchronisation of an
+ * allocation on their hot path.  Same arguments and results as
+ * tq_decode_attn without workspace / workspace_bytes: the split-K partials
+ * go to a file-scope device array of TQ_DECODE_STATIC_SCRATCH_BYTES bytes
+ * inside libtq, which every GPU that loads the library keeps until the
+ * process exits.  Nothing is allocated, neither here nor by the caller.
+ *   - Sizes whose partials need more than that (tq_decode_workspace_bytes)
+ *     are refused with TQ_ERR_WORKSPACE before anything is enqueued.
+ *   - The first call on a device looks up that device's copy of the array
+ *     (cudaGetSymbolAddress, with the device current) and caches it; make
+ *     that first call before any stream capture.
+ *   - All calls on a device share the one array and it keeps the last
+ *     call's contents (no call needs it zeroed): calls that overlap on the
+ *     GPU (other streams, other host threads) race on it and must be
+ *     serialised by the caller. */
+int tq_decode_attn_static(const tq_kv_view* K, const tq_kv_view* V, const uint16_t* q, int B, int Hq,
+                          int Hkv, int64_t S_cap, const int32_t* kv_len, int64_t ctx,
+                          float softmax_scale, uint16_t* out, int n_split, void* stream);
+
 /* Workspace bytes for tq_decode_attn with these sizes (host).  n_split = 0
  * gives the size for the library's own choice; *n_split_out (may be NULL)
  * receives the split count that will be used. */

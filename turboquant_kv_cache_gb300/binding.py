@@ -53,6 +53,7 @@ def _load():
         "tq_dequantize_kv": (I, [P, P, P, P, P, P, I64, P, I, P]),
         "tq_decode_attn": (I, [P, P, P, I, I, I, I64, P, I64, ctypes.c_float, P, P, SZ, I, P]),
         "tq_decode_workspace_bytes": (I, [I, I, I, I, I64, I, P, P]),
+        "tq_decode_attn_static": (I, [P, P, P, I, I, I, I64, P, I64, ctypes.c_float, P, I, P]),
         "tq_prefill_attn": (I, [P, P, P, I, I, I, I, I64, I64, I, ctypes.c_float, P, P, SZ, P]),
         "tq_prefill_workspace_bytes": (I, [I, I, I, I, I, I64, P]),
         "tq_strerror": (ctypes.c_char_p, [I]),
@@ -225,6 +226,22 @@ def tq_decode_attn(K, V, q, ctx=None, kv_len=None, softmax_scale=0.0, n_split=0,
                             float(softmax_scale), _ptr(out), _ptr(workspace), workspace.numel(), n_split,
                             _stream(stream))
     _check(st, "tq_decode_attn")
+    return out
+
+
+def tq_decode_attn_static(K, V, q, ctx=None, kv_len=None, softmax_scale=0.0, n_split=0, out=None, stream=None):
+    """tq_decode_attn without a workspace: the library's own fixed device
+    array holds the split partials (for callers that cannot allocate)."""
+    lib = _load()
+    B, Hq, d = q.shape
+    _, Hkv, S_cap = K.lead_shape
+    ctx = S_cap if ctx is None else ctx
+    if out is None:
+        out = torch.empty_like(q)
+    kv, vv = K.view(), V.view()
+    st = lib.tq_decode_attn_static(ctypes.byref(kv), ctypes.byref(vv), _ptr(q), B, Hq, Hkv, S_cap, _ptr(kv_len),
+                                   ctx, float(softmax_scale), _ptr(out), n_split, _stream(stream))
+    _check(st, "tq_decode_attn_static")
     return out
 
 

@@ -11,6 +11,8 @@
 #include <cuda_runtime.h>
 #include <math.h>
 
+#include <mutex>
+
 #include "tq_device.cuh"
 
 namespace tq {
@@ -389,4 +391,53 @@ extern "C" int tq_decode_attn(const tq_kv_view* K, const tq_kv_view* V, const ui
     default: tq::decode_combine_kernel<256><<<B * Hq, 256, 0, s>>>(PV, a.part, ns, out); break;
   }
   return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------------------
+// Decode attention without any allocation by the caller or the library.
+//
+// Some callers cannot call cudaMalloc at the point where they decode: a
+// serving runtime or plugin host that owns every device allocation through
+// its own fixed pool and forbids new ones after start-up, or a hot path that
+// cannot afford cudaMalloc's implicit device synchronisation.  For them the
+// split-K partials live in one fixed array of device memory that belongs to
+// this library.  Each GPU that loads the library keeps this array for the
+// life of the process.
+namespace tq {
+namespace {
+
+constexpr size_t kStaticDecodeScratch = size_t(TQ_DECODE_STATIC_SCRATCH_BYTES);
+static __device__ __align__(256) unsigned char g_decode_scratch[kStaticDecodeScratch];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void* g_scratch_addr[kMaxDevices] = {};
+
+}  // namespace
+}  // namespace tq
+
+extern "C" int tq_decode_attn_static(const tq_kv_view* K, const tq_kv_view* V, const uint16_t* q, int B, int Hq,
+                                     int Hkv, int64_t S_cap, const int32_t* kv_len, int64_t ctx,
+                                     float softmax_scale, uint16_t* out, int n_split, void* stream) {
+  if (!K || !V) return TQ_ERR_ARG;
+  size_t need = 0;
+  int st = tq_decode_workspace_bytes(B, Hq, Hkv, K->layout.head_dim, ctx, n_split, &need, nullptr);
+  if (st != TQ_OK) return st;
+  if (need > tq::kStaticDecodeScratch) return TQ_ERR_WORKSPACE;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= tq::kMaxDevices) return TQ_ERR_CUDA;
+  void* scratch = nullptr;
+  {
+    // Host code cannot use the array's name as a device address: ask the
+    // runtime for this device's copy once, with this device current.
+    std::lock_guard<std::mutex> lock(tq::g_scratch_mu);
+    if (!tq::g_scratch_addr[dev]) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, tq::g_decode_scratch) != cudaSuccess || !p) return TQ_ERR_CUDA;
+      tq::g_scratch_addr[dev] = p;
+    }
+    scratch = tq::g_scratch_addr[dev];
+  }
+  return tq_decode_attn(K, V, q, B, Hq, Hkv, S_cap, kv_len, ctx, softmax_scale, out, scratch,
+                        tq::kStaticDecodeScratch, n_split, stream);
 }

@@ -13,7 +13,7 @@
  *   3. scalar-quantise every y_i with the Lloyd-Max codebook of N(0, 1/block)
  *      (same section, step 3);
  *   4. optionally keep the 1-bit QJL residual sign(S r), r = u - Q(u), plus
- *      ||r|| ("turboquant-pytorch" README, "The combined estimator");
+ *      ||r|| ("turboquant-pytorch" README, QJL estimator formula);
  *   5. bit-pack the codes with one fp16 scale per block (llama.cpp-turboquant
  *      docs/turboquant.md, "How it works" and "GGML Types": 14-byte turbo3
  *      and 18-byte turbo4 blocks of 32 values).
@@ -159,7 +159,7 @@ typedef struct {
  * (n_split = 0: chosen by the library).  workspace: device, at least
  * tq_decode_workspace_bytes(...) bytes, 16-byte aligned.  With QJL keys the
  * score adds ||k|| rho sqrt(pi/2)/m <S q, 2s - 1> ("turboquant-pytorch",
- * "The combined estimator"). */
+ * QJL estimator formula). */
 int tq_decode_attn(const tq_kv_view* K, const tq_kv_view* V, const uint16_t* q, int B, int Hq,
                    int Hkv, int64_t S_cap, const int32_t* kv_len, int64_t ctx,
                    float softmax_scale, uint16_t* out, void* workspace, size_t workspace_bytes,

@@ -15,7 +15,7 @@ source pages describe the method:
   scalar quantisation for N(0, 1/d), un-rotation, optional QJL residual and
   optional norm correction; section 7 "Finding 4: Block-32": every 32-value
   block rotated and quantised on its own, with its own norm.
-* "turboquant-pytorch" README, "The combined estimator": the QJL inner
+* "turboquant-pytorch" README, QJL estimator formula: the inner
   product estimator <q,k_mse> + ||r|| sqrt(pi/2)/m <Sq, sign(Sr)>.
 * llama.cpp-turboquant "docs/turboquant.md", "How it works" (encode/decode
   pipeline) and "GGML Types" (14-byte turbo3 / 18-byte turbo4 blocks of 32
@@ -70,8 +70,8 @@ def splitmix64_stream(seed: int, count: int) -> list[int]:
 
 def sign_vector(seed: int, d: int) -> np.ndarray:
     """D in {-1,+1}^d: the random diagonal of the randomized Hadamard
-    transform (TurboQuant From Scratch, section 2, step 2, "D = random
-    signs").  D_i = -1 when bit 63 of the i-th splitmix64 output is set."""
+    transform (TurboQuant From Scratch, section 2, step 2: D holds random
+    signs).  D_i = -1 when bit 63 of the i-th splitmix64 output is set."""
     return np.array([-1.0 if (z >> 63) else 1.0 for z in splitmix64_stream(seed, d)])
 
 
@@ -120,8 +120,8 @@ _CODEBOOK_CACHE: dict = {}
 
 def lloyd_max_codebook(bits: int, blk: int, max_iter: int = 1000000):
     """Lloyd-Max scalar quantiser for N(0, sigma^2 = 1/blk) with 2^bits
-    levels (TurboQuant From Scratch, section 2, step 3: "a Lloyd-Max codebook
-    computed once for N(0, 1/d)"; turboquant-pytorch README, lloyd_max.py).
+    levels (TurboQuant From Scratch, section 2, step 3: the codebook is solved once
+    per bit width for N(0, 1/d); turboquant-pytorch README, lloyd_max.py).
 
     Start from the quantiles sigma * Phi^-1((k + 1/2) / 2^bits), then
     alternate the two optimality conditions: boundaries are midpoints of
@@ -212,7 +212,7 @@ class Layout:
 def qjl_term(S: np.ndarray, bits_pm: np.ndarray, rho: np.ndarray) -> np.ndarray:
     """rho * sqrt(pi/2)/m * S^T (2s - 1): the QJL reconstruction of the unit
     residual (TurboQuant From Scratch, section 2, the ``qjl`` branch;
-    turboquant-pytorch README, "The combined estimator").  bits_pm holds
+    turboquant-pytorch README, QJL estimator formula).  bits_pm holds
     +-1 per projection row, shape [N, m]; rho shape [N]."""
     m = S.shape[0]
     return (rho[:, None] * (QJL_CONST / m)) * (bits_pm @ S)
@@ -466,7 +466,7 @@ def prefill_attention(q, Kd, Vd, ctx, causal=True, softmax_scale=None):
 
 
 def qjl_score_estimate(q, k_mse, rho, s_bits, S, knorm):
-    """turboquant-pytorch README "The combined estimator", scaled by the key
+    """turboquant-pytorch README, QJL estimator formula, scaled by the key
     norm: <q,k> ~ ||k|| (<q,u_mse> + rho sqrt(pi/2)/m <Sq, 2s-1>).  Used only
     to check that decoding-then-dot equals the estimator."""
     m = S.shape[0]

@@ -1,0 +1,68 @@
+"""Prefill attention (tq_prefill_attn) against the oracle over an
+oracle-encoded cache: Tq queries at positions ctx-Tq .. ctx-1, causal
+(bottom-right) or full, GQA groups, ragged context and query counts."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import tq_oracle as O
+from turboquant_kv_cache_gb300 import inputs
+
+from _parity import ATTN_ATOL, to_np, upload_packed
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(tb, cK, cV, B, Hq, Hkv, S_cap, ctx, Tq, d, causal=True, heavy=False, seed=50):
+    Lk, Lv = O.Layout(d, *cK), O.Layout(d, *cV)
+    k = (inputs.student_t((B, Hkv, S_cap, d), seed, 4.0) if heavy else inputs.gaussian((B, Hkv, S_cap, d), seed))
+    v = inputs.gaussian((B, Hkv, S_cap, d), seed + 1)
+    q = inputs.gaussian((B, Hq, Tq, d), seed + 2)
+    kc, ks, _, _ = O.encode(k.reshape(-1, d), Lk)
+    vc, vs, _, _ = O.encode(v.reshape(-1, d), Lv)
+    kd = O.dequantize(kc, ks, Lk).reshape(B, Hkv, S_cap, d)
+    vd = O.dequantize(vc, vs, Lv).reshape(B, Hkv, S_cap, d)
+    K = upload_packed(tb, tb.make_layout(d, *cK), Lk, kc, ks, None, None, (B, Hkv, S_cap))
+    V = upload_packed(tb, tb.make_layout(d, *cV), Lv, vc, vs, None, None, (B, Hkv, S_cap))
+    out = tb.tq_prefill_attn(K, V, torch.from_numpy(q).cuda(), ctx, causal=causal)
+    torch.cuda.synchronize()
+    ref = O.prefill_attention(q, kd, vd, ctx, causal=causal)
+    return to_np(out.float()), ref
+
+
+CASES = [
+    # name, K (block, bits, m, nc, seed), V, B, Hq, Hkv, S_cap, ctx, Tq, d
+    ("turbo3_d128_q37", (32, 3, 0, 0, 1), (32, 3, 0, 0, 1), 1, 8, 2, 320, 300, 37, 128),
+    ("turbo4k_d256_q64", (32, 4, 0, 0, 1), (32, 3, 0, 0, 1), 1, 8, 2, 210, 200, 64, 256),
+    ("pervec_d64_tq_eq_ctx", (64, 4, 0, 0, 2), (64, 3, 0, 0, 3), 2, 2, 2, 40, 5, 5, 64),
+    ("q1_like_decode", (32, 3, 0, 0, 1), (32, 3, 0, 0, 1), 2, 8, 2, 150, 129, 1, 128),
+    ("q4", (32, 3, 0, 0, 1), (32, 3, 0, 0, 1), 1, 4, 1, 100, 97, 4, 128),
+    ("q16_gqa8", (64, 3, 0, 0, 1), (32, 4, 0, 0, 1), 1, 8, 1, 90, 80, 16, 128),
+    ("q512_long", (32, 3, 0, 0, 1), (32, 3, 0, 0, 1), 1, 8, 2, 700, 650, 512, 128),
+]
+
+
+@pytest.mark.parametrize("name,cK,cV,B,Hq,Hkv,S_cap,ctx,Tq,d", CASES)
+def test_prefill_matches_oracle(tqlib, name, cK, cV, B, Hq, Hkv, S_cap, ctx, Tq, d):
+    from turboquant_kv_cache_gb300 import binding as tb
+    got, ref = _run(tb, cK, cV, B, Hq, Hkv, S_cap, ctx, Tq, d, heavy=(d == 256))
+    assert np.abs(got - ref).max() < ATTN_ATOL, (name, np.abs(got - ref).max())
+
+
+def test_prefill_non_causal(tqlib):
+    from turboquant_kv_cache_gb300 import binding as tb
+    got, ref = _run(tb, (32, 3, 0, 0, 1), (32, 3, 0, 0, 1), 1, 4, 2, 130, 130, 20, 128, causal=False)
+    assert np.abs(got - ref).max() < ATTN_ATOL
+
+
+def test_prefill_rejects_qjl_keys(tqlib):
+    from turboquant_kv_cache_gb300 import binding as tb
+    L = tb.make_layout(128, 128, 2, 128, 0, 1)
+    Lv = tb.make_layout(128, 128, 3, 0, 0, 1)
+    S = torch.zeros(128, 128, device="cuda")
+    K = tb.PackedKV(L, (1, 1, 16), S=S)
+    V = tb.PackedKV(Lv, (1, 1, 16))
+    q = torch.zeros(1, 2, 4, 128, dtype=torch.float16, device="cuda")
+    with pytest.raises(tb.TQError) as e:
+        tb.tq_prefill_attn(K, V, q, 16)
+    assert e.value.status == -2

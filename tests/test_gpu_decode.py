@@ -65,6 +65,25 @@ def test_decode_matches_oracle(tqlib, name, cK, cV, B, Hq, Hkv, S_cap, ctx, d, n
     assert err < ATTN_ATOL, (name, err)
 
 
+TC_CASES = [
+    # name, B, Hq, Hkv, S_cap, ctx, kv_len, n_split, heavy_k
+    ("long_many_tiles", 2, 8, 2, 4100, 4097, None, 0, False),
+    ("heavy_tailed_keys", 1, 8, 2, 3000, 2999, None, 3, True),
+    ("ragged_splits", 3, 12, 3, 2050, 2050, [2050, 1000, 63], 6, False),
+    ("odd_scap_generic_path", 1, 4, 1, 333, 333, None, 0, False),
+]
+
+
+@pytest.mark.parametrize("name,B,Hq,Hkv,S_cap,ctx,kv_len,n_split,heavy", TC_CASES)
+def test_decode_turbo3_tensor_core_path(tqlib, name, B, Hq, Hkv, S_cap, ctx, kv_len, n_split, heavy):
+    """turbo3 K/V, d=128, GQA 4: the shape of the fused tensor-core kernel."""
+    from turboquant_kv_cache_gb300 import binding as tb
+    got, ref, _ = _run(tb, (32, 3, 0, 0, 1), (32, 3, 0, 0, 1), B, Hq, Hkv, S_cap, ctx, 128, kv_len=kv_len,
+                       n_split=n_split, seed=7, heavy_k=heavy)
+    err = np.abs(got - ref).max()
+    assert err < ATTN_ATOL, (name, err)
+
+
 def test_decode_qjl_keys(tqlib):
     from turboquant_kv_cache_gb300 import binding as tb
     S = inputs.qjl_matrix(128, 128, 7)

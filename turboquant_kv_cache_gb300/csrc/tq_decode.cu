@@ -18,6 +18,12 @@
 namespace tq {
 
 int decode_auto_splits(int B, int Hkv, int64_t ctx);
+bool decode_tc_eligible(const CodecParams& PK, const CodecParams& PV, int G, int64_t S_cap, const void* ks,
+                        const void* vs);
+int launch_decode_tc(const CodecParams& PK, const CodecParams& PV, const uint8_t* kc, const uint16_t* ks,
+                     const uint8_t* vc, const uint16_t* vs, const uint16_t* q, const int32_t* kv_len, float* part,
+                     int B, int Hq, int Hkv, int64_t S_cap, int64_t ctx, int n_split, float qscale,
+                     uint16_t* out, cudaStream_t st);
 size_t decode_ws_bytes(int B, int Hq, int d, int n_split);
 
 namespace {
@@ -320,6 +326,15 @@ int launch_decode_g(int G, const CodecParams& PK, const CodecParams& PV, const D
 
 }  // namespace
 
+int decode_combine(const CodecParams& PV, const float* part, int n_split, uint16_t* out, int rows, cudaStream_t s) {
+  switch (PV.d) {
+    case 64: decode_combine_kernel<64><<<rows, 64, 0, s>>>(PV, part, n_split, out); break;
+    case 128: decode_combine_kernel<128><<<rows, 128, 0, s>>>(PV, part, n_split, out); break;
+    default: decode_combine_kernel<256><<<rows, 256, 0, s>>>(PV, part, n_split, out); break;
+  }
+  return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+}
+
 int sm_count() {
   int dev = 0, sms = 152;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -327,8 +342,9 @@ int sm_count() {
 }
 
 int decode_auto_splits(int B, int Hkv, int64_t ctx) {
+  // one wave at four 4-warp CTAs per SM
   const int units = B * Hkv;
-  int want = (8 * sm_count() + units - 1) / units;
+  int want = (4 * sm_count()) / units;
   const int64_t max_by_len = (ctx + 255) / 256;
   if (want > max_by_len) want = (int)max_by_len;
   if (want < 1) want = 1;
@@ -379,18 +395,16 @@ extern "C" int tq_decode_attn(const tq_kv_view* K, const tq_kv_view* V, const ui
                    static_cast<float*>(workspace), S_cap, ctx, Hq, Hkv, ns, sm * tq::kLog2e};
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int G = Hq / Hkv;
+  if (tq::decode_tc_eligible(PK, PV, G, S_cap, K->scales, V->scales))
+    return tq::launch_decode_tc(PK, PV, K->codes, K->scales, V->codes, V->scales, q, kv_len, a.part, B, Hq, Hkv,
+                                S_cap, ctx, ns, a.qscale, out, s);
   switch (PK.d) {
     case 64: st = tq::launch_decode_g<64>(G, PK, PV, a, B, s); break;
     case 128: st = tq::launch_decode_g<128>(G, PK, PV, a, B, s); break;
     default: st = tq::launch_decode_g<256>(G, PK, PV, a, B, s); break;
   }
   if (st != TQ_OK) return st;
-  switch (PK.d) {
-    case 64: tq::decode_combine_kernel<64><<<B * Hq, 64, 0, s>>>(PV, a.part, ns, out); break;
-    case 128: tq::decode_combine_kernel<128><<<B * Hq, 128, 0, s>>>(PV, a.part, ns, out); break;
-    default: tq::decode_combine_kernel<256><<<B * Hq, 256, 0, s>>>(PV, a.part, ns, out); break;
-  }
-  return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+  return tq::decode_combine(PV, a.part, ns, out, B * Hq, s);
 }
 
 // ---------------------------------------------------------------------------

@@ -10,6 +10,11 @@
 #include "tq_device.cuh"
 
 namespace tq {
+
+bool quantize_fast_eligible(const CodecParams& P, bool f32_input);
+int launch_quantize_fast(const CodecParams& P, const void* x, int64_t n_vec, int64_t stride, uint8_t* codes,
+                         uint16_t* scales, cudaStream_t st);
+
 namespace {
 
 constexpr int kThreads = 256;
@@ -307,6 +312,7 @@ extern "C" int tq_quantize_kv(const tq_layout* layout, const void* x, tq_dtype x
                   reinterpret_cast<uint32_t*>(qjl_bits), qjl_rnorm};
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool f32 = x_dtype == TQ_F32;
+  if (tq::quantize_fast_eligible(P, f32)) return tq::launch_quantize_fast(P, x, n_vec, x_row_stride, codes, scales, s);
   switch (P.d) {
     case 64: return tq::launch_quantize<64>(P, a, f32, s);
     case 128: return tq::launch_quantize<128>(P, a, f32, s);

@@ -96,9 +96,9 @@ __global__ void __launch_bounds__(kFW * 32) quantize_fast_kernel(const CodecPara
     const int64_t v = (tile / nb) * 32 + lane;
     const uint8_t* src = s_buf[wid][buf] + lane * BLK * 2;
 
-    // load, apply D, widen to fp32
-    float x[BLK];
-    float ss = 0.f;
+    // load, apply D, widen to fp32 pairs (2i, 2i+1)
+    float2 x[BLK / 2];
+    float2 ss2 = make_float2(0.f, 0.f);
 #pragma unroll
     for (int k = 0; k < CPI; ++k) {
       const uint4 u = *reinterpret_cast<const uint4*>(src + swz<BLK>(lane, k) * 16);
@@ -107,47 +107,58 @@ __global__ void __launch_bounds__(kFW * 32) quantize_fast_kernel(const CodecPara
       for (int e = 0; e < 4; ++e) {
         const uint32_t sg = a.sgn[(j * BLK) / 2 + 4 * k + e];
         const __half2 h = __hmul2(*reinterpret_cast<const __half2*>(&w[e]), *reinterpret_cast<const __half2*>(&sg));
-        const float2 f = __half22float2(h);
-        x[8 * k + 2 * e] = f.x;
-        x[8 * k + 2 * e + 1] = f.y;
-        ss = fmaf(f.x, f.x, ss);
-        ss = fmaf(f.y, f.y, ss);
+        x[4 * k + e] = __half22float2(h);
+        ss2 = __ffma2_rn(x[4 * k + e], x[4 * k + e], ss2);
       }
     }
     __syncwarp();   // the buffer is refilled two tiles later
-    // unnormalised Walsh-Hadamard transform
+    // unnormalised Walsh-Hadamard transform: stride 1 inside each pair, the
+    // wider strides on whole pairs with packed fp32x2 adds
 #pragma unroll
-    for (int h = 1; h < BLK; h <<= 1) {
+    for (int i = 0; i < BLK / 2; ++i) {
+      const float p = x[i].x, q = x[i].y;
+      x[i] = make_float2(p + q, p - q);
+    }
+    const float2 neg1 = make_float2(-1.f, -1.f);
 #pragma unroll
-      for (int i = 0; i < BLK; ++i) {
+    for (int h = 1; h < BLK / 2; h <<= 1) {
+#pragma unroll
+      for (int i = 0; i < BLK / 2; ++i) {
         if ((i & h) == 0) {
-          const float p = x[i], q = x[i + h];
-          x[i] = p + q;
-          x[i + h] = p - q;
+          const float2 p = x[i], q = x[i + h];
+          x[i] = __fadd2_rn(p, q);
+          x[i + h] = __ffma2_rn(q, neg1, p);
         }
       }
     }
-    const float n = sqrtf(ss);
-    // a*A - B_k with A = 2^20 / (n sqrt(blk)): |y| >= beta_k  <=>  step = 1
+    const float n = sqrtf(ss2.x + ss2.y);
+    // a*A - B_k with A = 2^20 / (n sqrt(blk)): |y| > beta_k  <=>  step = 1
     const float A = n > 0.f ? kStepScale / (n * sqrtf((float)BLK)) : 0.f;
+    const float2 base2 = make_float2((float)HALF_K - 0.5f, (float)HALF_K - 0.5f);
+    const float2 magic2 = make_float2(kMagic, kMagic);
+    // integer of the magic-shifted code is (bits - magic bits); the magic part
+    // of all 8 nibbles is removed once per chunk
+    const uint32_t magic_all = __float_as_uint(kMagic) * 0x11111111u;
     uint32_t words[WPB];
     uint32_t nib[BLK / 8];
 #pragma unroll
     for (int c = 0; c < BLK / 8; ++c) {
-      uint32_t acc = 0u;
+      uint32_t acc = 0u - magic_all;
 #pragma unroll
-      for (int r = 0; r < 8; ++r) {
-        const float y = x[8 * c + r];
-        const float ay = fabsf(y);
-        float cnt = 0.5f;
+      for (int r2 = 0; r2 < 4; ++r2) {
+        const float2 y = x[4 * c + r2];
+        const float ay0 = fabsf(y.x), ay1 = fabsf(y.y);
+        float2 cnt = make_float2(0.5f, 0.5f);
 #pragma unroll
-        for (int kk = 0; kk < HALF_K - 1; ++kk) cnt += __saturatef(fmaf(ay, A, -a.bstep[kk]));
+        for (int kk = 0; kk < HALF_K - 1; ++kk)
+          cnt = __fadd2_rn(cnt, make_float2(__saturatef(fmaf(ay0, A, -a.bstep[kk])),
+                                            __saturatef(fmaf(ay1, A, -a.bstep[kk]))));
         // code = HALF_K - 1 - cnt + 0.5 (y <= 0) or HALF_K - 0.5 + cnt (y > 0)
-        const float sc = copysignf(cnt, y > 0.f ? 1.f : -1.f);
+        const float2 sc = make_float2(copysignf(cnt.x, y.x), copysignf(cnt.y, y.y));
         // small exact sum first; adding 1.5*2^23 then rounds it to an integer
-        const float codef = ((float)HALF_K - 0.5f + sc) + kMagic;
-        const uint32_t bits = __float_as_uint(codef) - __float_as_uint(kMagic);
-        acc += bits << (4 * r);
+        const float2 codef = __fadd2_rn(__fadd2_rn(base2, sc), magic2);
+        acc += __float_as_uint(codef.x) << (8 * r2);
+        acc += __float_as_uint(codef.y) << (8 * r2 + 4);
       }
       nib[c] = n > 0.f ? acc : (uint32_t)(HALF_K - 1) * 0x11111111u;
     }

@@ -76,7 +76,7 @@ class ClockSampler:
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -188,6 +188,7 @@ def run_gpu(args, rank, world):
     e2e = e2e_decode(tb, torch, inputs, dev, K, V, L, ws, n_split, args)
 
     quant = bench_quantize(tb, torch, inputs, dev, args)
+    extra = {} if args.no_extra else bench_extra(tb, torch, inputs, dev, args)
     if rank == 0:
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
@@ -204,6 +205,7 @@ def run_gpu(args, rank, world):
                          "kernel": "decode_split_kernel + decode_combine_kernel (one tq_decode_attn call)"},
             "e2e": e2e,
             "quantize": quant,
+            "other_workloads": extra,
             "gpu_launches": args.steps * 2,
             "clocks": clocks.summary(),
             "wall_s_timed": round(wall, 4),
@@ -241,10 +243,11 @@ def e2e_decode(tb, torch, inputs, dev, K, V, L, ws, n_split, args):
         step()
     torch.cuda.synchronize()
     t0 = time.perf_counter()
-    for _ in range(args.steps):
+    n_e2e = min(args.steps, 200)
+    for _ in range(n_e2e):
         step()
     torch.cuda.synchronize()
-    dt = (time.perf_counter() - t0) / args.steps
+    dt = (time.perf_counter() - t0) / n_e2e
     return {"value": round(nbytes / dt / 1e9, 2), "unit": "GB/s",
             "h2d_bytes_per_step": q_h.numel() * 2 + kv_h.numel() * 2,
             "d2h_bytes_per_step": out_h.numel() * 2,
@@ -270,7 +273,7 @@ def bench_quantize(tb, torch, inputs, dev, args):
             tb.tq_quantize_kv(L, v, out=ov)
         torch.cuda.synchronize()
         times = []
-        for _ in range(args.steps):
+        for _ in range(min(args.steps, 100)):
             flush.zero_()
             s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             s.record()
@@ -286,6 +289,105 @@ def bench_quantize(tb, torch, inputs, dev, args):
                      "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
                                   "frac": round(gbs / peak, 4), "bytes_per_vector": bytes_per_vec}}
     return res
+
+
+def _peak_tflops():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["bf16_tflops"]), "measured bf16_tflops (burst, cuBLAS); fp16 dense rate taken equal"
+    except Exception:
+        return 1900.0, "fallback 1.9 PFLOP/s"
+
+
+def _time(torch, fn, flush, steps, warmup):
+    for _ in range(warmup):
+        flush.zero_()
+        fn()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(steps):
+        flush.zero_()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        fn()
+        e.record()
+        ts.append((s, e))
+    torch.cuda.synchronize()
+    return statistics.mean(s.elapsed_time(e) for s, e in ts)
+
+
+def _cache_from(tb, torch, L, x_np, dev, S=None):
+    """Packed cache of x [B, H, T, d] (numpy fp16), quantised on the device
+    one (batch, head) at a time."""
+    B, H, T, d = x_np.shape
+    pk = tb.PackedKV(L, (B, H, T), device=dev, S=S)
+    for b in range(B):
+        for h in range(H):
+            part = tb.tq_quantize_kv(L, torch.from_numpy(x_np[b, h]).to(dev), S=S)
+            pk.codes[b, h].copy_(part.codes)
+            pk.scales[b, h].copy_(part.scales)
+            if pk.qjl is not None:
+                pk.qjl[b, h].copy_(part.qjl)
+                pk.rnorm[b, h].copy_(part.rnorm)
+    return pk
+
+
+def bench_extra(tb, torch, inputs, dev, args):
+    """The other workloads of the path, each timed on its own (CUDA events,
+    L2 flushed before every step): head_dim 256 / 131072-context decode and
+    512-query causal prefill (turbo4 K, turbo3 V, Student-t keys), and the
+    QJL-key decode (2-bit + 1-bit QJL keys, 3-bit values, 16384 context)."""
+    out = {}
+    flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=dev)
+    hbm, _ = _peaks()
+    tflops, tsrc = _peak_tflops()
+    steps = max(2, min(args.steps, 5))
+    # head_dim 256, 131072 context
+    w = inputs.d256_longctx_workload()
+    Lk = tb.make_layout(256, 32, 4, 0, 0, 1)
+    Lv = tb.make_layout(256, 32, 3, 0, 0, 1)
+    K = _cache_from(tb, torch, Lk, w["k"], dev)
+    V = _cache_from(tb, torch, Lv, w["v"], dev)
+    del w["k"], w["v"]
+    q = torch.from_numpy(w["q"]).to(dev)
+    ctx = 131072
+    ms = _time(torch, lambda: tb.tq_decode_attn(K, V, q, ctx=ctx), flush, steps, 2)
+    nbytes = K.nbytes() + V.nbytes()
+    out["decode_d256_ctx131072"] = {
+        "workload": "B=1, Hq=16, Hkv=4, d=256, ctx=131072, turbo4 K (Student-t nu=4) / turbo3 V",
+        "ms": round(ms, 4), "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1),
+        "roofline": {"bound": "hbm", "achieved": round(nbytes / (ms * 1e-3) / 1e9, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(nbytes / (ms * 1e-3) / 1e9 / hbm, 4)}}
+    qp = torch.from_numpy(w["q_prefill"]).to(dev)
+    Tq = qp.shape[2]
+    ms = _time(torch, lambda: tb.tq_prefill_attn(K, V, qp, ctx, causal=True), flush, 2, 1)
+    pairs = Tq * (ctx - Tq) + Tq * (Tq + 1) // 2       # causal (query, key) pairs per q-head
+    flop = 4.0 * 256 * pairs * 16                       # QK^T + PV, 16 q-heads
+    tf = flop / (ms * 1e-3) / 1e12
+    out["prefill_d256_q512_ctx131072"] = {
+        "workload": "B=1, Hq=16, Hkv=4, d=256, 512 causal queries at 130560..131071 over 131072 context",
+        "ms": round(ms, 3), "TFLOP/s": round(tf, 1),
+        "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": tflops, "unit": "TFLOP/s",
+                     "frac": round(tf / tflops, 4), "peak_source": tsrc, "flop_per_step": flop}}
+    del K, V
+    torch.cuda.empty_cache()
+    # QJL keys
+    w = inputs.qjl_decode_workload()
+    S = torch.from_numpy(w["S"]).to(dev)
+    Lk = tb.make_layout(128, 128, 2, 128, 0, 1)
+    Lv = tb.make_layout(128, 128, 3, 0, 0, 1)
+    K = _cache_from(tb, torch, Lk, w["k"], dev, S=S)
+    V = _cache_from(tb, torch, Lv, w["v"], dev)
+    q = torch.from_numpy(w["q"]).to(dev)
+    ms = _time(torch, lambda: tb.tq_decode_attn(K, V, q, ctx=16384), flush, steps, 2)
+    nbytes = K.nbytes() + V.nbytes()
+    out["decode_qjl_keys_ctx16384"] = {
+        "workload": "B=4, Hq=32, Hkv=8, d=128, ctx=16384; K 2-bit + QJL m=128, V 3-bit, one norm per vector",
+        "ms": round(ms, 4), "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1),
+        "roofline": {"bound": "hbm", "achieved": round(nbytes / (ms * 1e-3) / 1e9, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(nbytes / (ms * 1e-3) / 1e9 / hbm, 4)}}
+    return out
 
 
 # ---------------------------------------------------------------- CPU oracle
@@ -368,10 +470,11 @@ def run_reference(args, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="tq", choices=["tq", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true", help="skip the other workloads (headline only)")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     args = ap.parse_args()
     if args.warmup < 3:

@@ -1,0 +1,502 @@
+// Prefill attention over the packed cache on the 5th-generation tensor cores
+// (tcgen05, TMEM accumulators).
+//
+// Rows: every (batch, KV head) owns R = Tq*G query rows (query i, head h ->
+// row i*G + h).  A CTA takes 128 rows (one per thread and per TMEM lane) and
+// one slice of the context, walking it in 64-token tiles:
+//   * the tile's K and V records are decoded by all 128 threads into shared
+//     memory (rotated domain, centroid * block norm, fp16) in the canonical
+//     no-swizzle core-matrix layout (8 rows x 16 bytes per core matrix), which
+//     serves K as a K-major B operand of S = Q K^T and V as an MN-major B
+//     operand of O = P V; both tiles are double-buffered so the decode of the
+//     next tile overlaps the MMAs of the current one;
+//   * one thread issues S = Q^ K^^T (M 128, N 64, K d) into TMEM;
+//   * each thread reads its row of S, applies the causal / context mask and
+//     an online softmax in base 2 (the reference max moves only when a score
+//     exceeds it by more than 2^8), writes P as fp16 back into TMEM;
+//   * one thread issues O += P V^ (A = P from TMEM, M 128, N d, K 64).
+// Q^ = H D q per K block times softmax_scale * log2 e is prepared once per
+// call by a small kernel.  Partial (m, l, O) per row and context slice go to
+// the workspace in the decode-split format, and the decode combine kernel
+// merges the slices and rotates each output row back (D H per V block).
+// Every mbarrier wait is bounded: on expiry the CTA records an error word in
+// the workspace, frees its TMEM and returns.
+#include <cuda_runtime.h>
+#include <math.h>
+
+#include "tq_device.cuh"
+
+namespace tq {
+
+int decode_combine(const CodecParams& PV, const float* part, int n_split, uint16_t* out, int rows, cudaStream_t s);
+int sm_count();
+
+namespace {
+
+constexpr int kRowsTc = 128;     // query rows per CTA (TMEM lanes)
+constexpr int kTok = 64;         // tokens per KV tile
+constexpr int kThr = 128;
+constexpr uint32_t kColS = 0, kColP = 64;
+// TMEM columns: S (64 fp32) at 0, P (64 fp16 = 32 columns) at 64, O (d fp32)
+// at kColO; a power of two >= the total
+template <int D> __host__ __device__ constexpr uint32_t tmem_cols() { return D == 256 ? 512u : 256u; }
+template <int D> __host__ __device__ constexpr uint32_t col_o() { return D == 256 ? 256u : 128u; }
+constexpr float kLazyP = 8.0f;
+constexpr int kWaitLimit = 1 << 24;
+
+__device__ __forceinline__ uint32_t su32(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
+
+// byte offset of element (row, col) in a core-matrix tile of `cols` columns:
+// core matrix (row/8, col/8) at ((row/8) * (cols/8) + col/8) * 128, row-major
+// 8 x 16 bytes inside.
+__device__ __forceinline__ uint32_t cm_off(int row, int col, int cols) {
+  return (uint32_t)(((row >> 3) * (cols >> 3) + (col >> 3)) * 128 + (row & 7) * 16 + (col & 7) * 2);
+}
+
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | ((uint64_t)1 << 46);
+}
+
+__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, int acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, int acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d),
+      "r"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t phase) {
+  uint32_t done = 0;
+  for (int it = 0; it < kWaitLimit && !done; ++it)
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(bar), "r"(phase)
+        : "memory");
+  return done != 0;
+}
+
+__device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
+__device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory"); }
+
+#define TQ_LD32(taddr, v)                                                                                          \
+  asm volatile(                                                                                                    \
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"  \
+      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"                                             \
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),            \
+        "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),      \
+        "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),    \
+        "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])     \
+      : "r"(taddr))
+
+#define TQ_ST32(taddr, v)                                                                                          \
+  asm volatile(                                                                                                    \
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,"   \
+      "%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n" ::"r"(taddr),                              \
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),           \
+      "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]),   \
+      "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]),  \
+      "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])                                                   \
+      : "memory")
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+__device__ __forceinline__ float ex2f(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// fp16 centroid byte tables: lo/hi bytes of entries 0-3 / 4-7 (t[0..3]) and,
+// for 4-bit codebooks, of entries 8-11 / 12-15 (t[4..7]).
+struct Lut {
+  uint32_t t[8];
+};
+
+__device__ __forceinline__ Lut make_lut(const CodecParams& P) {
+  Lut L;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) L.t[i] = 0u;
+  const int K = 1 << P.bits;
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    if (k < K) {
+      const uint32_t h = f2h(P.centroids[k]);
+      const int half = k >> 3, q = (k & 7) >> 2, sh = 8 * (k & 3);
+      L.t[4 * half + q] |= (h & 0xffu) << sh;        // low bytes
+      L.t[4 * half + 2 + q] |= (h >> 8) << sh;       // high bytes
+    }
+  }
+  return L;
+}
+
+// fp16 values of the 4 codes in the low 16 bits of nibble word n.
+__device__ __forceinline__ void lut4(uint32_t n, const Lut& L, int bits, uint32_t& o01, uint32_t& o23) {
+  const uint32_t s = n & 0x7777u;
+  uint32_t lo = prmt(L.t[0], L.t[1], s);
+  uint32_t hi = prmt(L.t[2], L.t[3], s);
+  if (bits == 4) {
+    // codes 8-15 from the second table, chosen per byte by bit 3
+    const uint32_t lo2 = prmt(L.t[4], L.t[5], s);
+    const uint32_t hi2 = prmt(L.t[6], L.t[7], s);
+    const uint32_t m7 = prmt(0x80808080u, 0x80808080u, n & 0xffffu) ^ 0x80808080u;  // 0x7f where bit 3 set
+    const uint32_t m = m7 | (m7 << 1);
+    lo = (lo & ~m) | (lo2 & m);
+    hi = (hi & ~m) | (hi2 & m);
+  }
+  o01 = prmt(lo, hi, 0x5140);
+  o23 = prmt(lo, hi, 0x7362);
+}
+
+__device__ __forceinline__ uint32_t hmul2u(uint32_t a, __half2 b) {
+  const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&a), b);
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+
+// Decode tokens [t0, t0 + kTok) of one packed (batch, head) row range into a
+// core-matrix tile [kTok][D] (rotated, scaled fp16); tokens at or beyond
+// t_hi are written as zeros.
+template <int D>
+__device__ __forceinline__ void decode_tile_tc(const CodecParams& P, const Lut& L, const uint32_t* __restrict__ codes,
+                                               const uint16_t* __restrict__ scales, int64_t rec0, int64_t t0,
+                                               int64_t t_hi, uint8_t* tile) {
+  constexpr int CH = D / 8;
+  const int words = P.code_bytes / 4;
+  for (int task = threadIdx.x; task < kTok * CH; task += kThr) {
+    const int tok = task / CH, ch = task % CH;
+    const int64_t t = t0 + tok;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (t < t_hi) {
+      const uint32_t* rec = codes + (rec0 + t) * words;
+      const uint32_t nib = load_chunk(rec + (ch >> 2) * P.bits, P.bits, ch & 3);
+      const __half sc = __ushort_as_half(scales[(rec0 + t) * P.nb + (ch * 8) / P.blk]);
+      const __half2 sc2 = __halves2half2(sc, sc);
+      uint32_t a, b, c, d;
+      lut4(nib, L, P.bits, a, b);
+      lut4(nib >> 16, L, P.bits, c, d);
+      v = make_uint4(hmul2u(a, sc2), hmul2u(b, sc2), hmul2u(c, sc2), hmul2u(d, sc2));
+    }
+    *reinterpret_cast<uint4*>(tile + cm_off(tok, ch * 8, D)) = v;
+  }
+}
+
+struct PrefillTcArgs {
+  const uint32_t* kc;
+  const uint16_t* ks;
+  const uint32_t* vc;
+  const uint16_t* vs;
+  const __half* qhat;   // [B*Hkv][R_pad][D]
+  float* part;          // [(b*Hq + h)*Tq + i][n_split][D + 4]
+  int* err;
+  int64_t S_cap, ctx;
+  int Hq, Hkv, Tq, R_pad, n_split, causal;
+  int64_t per;          // tokens per split (multiple of kTok)
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThr, 1) prefill_tc_kernel(const CodecParams PK, const CodecParams PV,
+                                                             const PrefillTcArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint8_t* sQ = smem;                                   // [128][D]
+  uint8_t* sK[2] = {sQ + kRowsTc * D * 2, sQ + kRowsTc * D * 2 + kTok * D * 2};
+  uint8_t* sV[2] = {sK[1] + kTok * D * 2, sK[1] + 2 * kTok * D * 2};
+  __shared__ __align__(8) uint64_t bar_s, bar_o;
+  __shared__ uint32_t tmem_base;
+
+  constexpr uint32_t kTmemCols = tmem_cols<D>();
+  constexpr uint32_t kColO = col_o<D>();
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int G = a.Hq / a.Hkv;
+  const int rt = blockIdx.x;          // row tile
+  const int split = blockIdx.y;
+  const int bh = blockIdx.z;
+  const int b = bh / a.Hkv, kvh = bh % a.Hkv;
+  const int R = a.Tq * G;
+  const int row = rt * kRowsTc + tid;   // this thread's query row
+  const bool row_ok = row < R;
+  const int qi = row_ok ? row / G : a.Tq - 1;
+  const int64_t pos = a.ctx - a.Tq + qi;
+
+  // context slice of this CTA, clipped to what the tile's last row can see
+  const int last_row = min(rt * kRowsTc + kRowsTc, R) - 1;
+  const int64_t max_pos = a.causal ? a.ctx - a.Tq + last_row / G : a.ctx - 1;
+  const int64_t t_lo = (int64_t)split * a.per;
+  const int64_t t_hi = imin64(imin64(t_lo + a.per, a.ctx), max_pos + 1);
+  const int n_tiles = t_hi > t_lo ? (int)((t_hi - t_lo + kTok - 1) / kTok) : 0;
+  const int64_t rec0 = (int64_t)bh * a.S_cap;
+
+  // Q^ rows into the core-matrix tile
+  {
+    const __half* src = a.qhat + ((int64_t)bh * a.R_pad + (int64_t)rt * kRowsTc) * D;
+    for (int e = tid; e < kRowsTc * (D / 8); e += kThr) {
+      const int r = e / (D / 8), ch = e % (D / 8);
+      const uint4 v = *reinterpret_cast<const uint4*>(src + (int64_t)r * D + ch * 8);
+      *reinterpret_cast<uint4*>(sQ + cm_off(r, ch * 8, D)) = v;
+    }
+  }
+  const Lut lk = make_lut(PK), lv = make_lut(PV);
+  if (tid == 0) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(su32(&bar_s)) : "memory");
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(su32(&bar_o)) : "memory");
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(su32(&tmem_base)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
+  }
+  if (n_tiles > 0) decode_tile_tc<D>(PK, lk, a.kc, a.ks, rec0, t_lo, t_hi, sK[0]);
+  if (n_tiles > 0) decode_tile_tc<D>(PV, lv, a.vc, a.vs, rec0, t_lo, t_hi, sV[0]);
+  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = tmem_base;
+  const uint32_t lane_base = tmem + ((uint32_t)(32 * warp) << 16);
+
+  // instruction descriptors: fp32 accumulate, fp16 A/B, M = 128
+  const uint32_t idesc_s = (1u << 4) | ((uint32_t)(kTok >> 3) << 17) | ((uint32_t)(kRowsTc >> 4) << 24);
+  const uint32_t idesc_o = (1u << 4) | (1u << 16) | ((uint32_t)(D >> 3) << 17) | ((uint32_t)(kRowsTc >> 4) << 24);
+  constexpr uint32_t kGroupBytes = (D / 8) * 128;   // one 8-row band of a [rows][D] core-matrix tile
+
+  auto issue_s = [&](int kb) {   // S = Q^ K^(buffer kb)^T
+#pragma unroll 4
+    for (int s = 0; s < D / 16; ++s)
+      mma_ss(tmem + kColS, sdesc(su32(sQ) + s * 256, 128, kGroupBytes), sdesc(su32(sK[kb]) + s * 256, 128, kGroupBytes),
+             idesc_s, s > 0);
+    mma_commit(su32(&bar_s));
+  };
+  auto issue_o = [&](int vb, bool first) {   // O += P V^(buffer vb)
+#pragma unroll
+    for (int s = 0; s < kTok / 16; ++s)
+      mma_ts(tmem + kColO, tmem + kColP + 8 * s, sdesc(su32(sV[vb]) + s * 2 * kGroupBytes, kGroupBytes, 128), idesc_o,
+             (first && s == 0) ? 0 : 1);
+    mma_commit(su32(&bar_o));
+  };
+
+  bool ok = true;
+  if (tid == 0 && n_tiles > 0) issue_s(0);
+  float m_run = -INFINITY, l_run = 0.f;
+  bool o_started = false;
+
+  for (int t = 0; t < n_tiles && ok; ++t) {
+    const int cur = t & 1, nxt = cur ^ 1;
+    const int64_t t0 = t_lo + (int64_t)t * kTok;
+    // decode the next tile while S(t) and O(t-1) are in flight
+    if (t + 1 < n_tiles) decode_tile_tc<D>(PK, lk, a.kc, a.ks, rec0, t0 + kTok, t_hi, sK[nxt]);
+    if (t >= 1) ok = ok && bar_wait(su32(&bar_o), (t - 1) & 1);          // O(t-1) done: P and V(nxt) free
+    if (t + 1 < n_tiles) decode_tile_tc<D>(PV, lv, a.vc, a.vs, rec0, t0 + kTok, t_hi, sV[nxt]);
+    ok = ok && bar_wait(su32(&bar_s), t & 1);                            // S(t) ready
+    fence_after();
+    // ---- softmax on this thread's row of S
+    uint32_t sv[32], sw[32];
+    TQ_LD32(lane_base + kColS, sv);
+    TQ_LD32(lane_base + kColS + 32, sw);
+    asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+    float mx = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < kTok; ++c) {
+      const int64_t tok = t0 + c;
+      const bool valid = row_ok && tok < t_hi && (!a.causal || tok <= pos);
+      float v = __uint_as_float(c < 32 ? sv[c] : sw[c - 32]);
+      v = valid ? v : -INFINITY;
+      if (c < 32) sv[c] = __float_as_uint(v); else sw[c - 32] = __float_as_uint(v);
+      mx = fmaxf(mx, v);
+    }
+    const bool need = mx > m_run + kLazyP;
+    if (__any_sync(0xffffffffu, need)) {
+      const float m_new = need ? mx : m_run;
+      const float alpha = (need && m_run != -INFINITY) ? ex2f(m_run - m_new) : 1.f;
+      m_run = m_new;
+      l_run *= alpha;
+      if (o_started) {   // rescale this row of O (warp-wide TMEM access; alpha = 1 for rows that keep m)
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t ov[32];
+          TQ_LD32(lane_base + kColO + c0, ov);
+          asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+#pragma unroll
+          for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * alpha);
+          TQ_ST32(lane_base + kColO + c0, ov);
+        }
+      }
+    }
+    const float mref = m_run == -INFINITY ? 0.f : m_run;
+    uint32_t pw[32];
+    float sum = 0.f;
+#pragma unroll
+    for (int c = 0; c < 32; ++c) {
+      const float p0 = ex2f(__uint_as_float(c < 16 ? sv[2 * c] : sw[2 * c - 32]) - mref);
+      const float p1 = ex2f(__uint_as_float(c < 16 ? sv[2 * c + 1] : sw[2 * c + 1 - 32]) - mref);
+      sum += p0 + p1;
+      const __half2 h = __floats2half2_rn(p0, p1);
+      pw[c] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    l_run += sum;
+    TQ_ST32(lane_base + kColP, pw);
+    asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");   // decoded tiles -> tensor core
+    fence_before();
+    ok = __syncthreads_and(ok) != 0;   // a timed-out wait stops the whole CTA together
+    fence_after();
+    if (ok && tid == 0) {
+      issue_o(cur, !o_started);
+      if (t + 1 < n_tiles) issue_s(nxt);
+    }
+    o_started = true;
+  }
+  if (n_tiles > 0 && ok) ok = bar_wait(su32(&bar_o), (n_tiles - 1) & 1);
+  ok = __syncthreads_and(ok) != 0;
+  fence_after();
+  // ---- partial (m, l, O) of this row for this context slice
+  if (ok && n_tiles > 0) {
+    for (int c0 = 0; c0 < D; c0 += 32) {
+      uint32_t ov[32];
+      TQ_LD32(lane_base + kColO + c0, ov);
+      asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+      if (row_ok) {
+        const int h = kvh * G + row % G;
+        float* dst = a.part + ((((int64_t)b * a.Hq + h) * a.Tq + qi) * a.n_split + split) * (D + 4);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) dst[2 + c0 + j] = __uint_as_float(ov[j]);
+        if (c0 == 0) {
+          dst[0] = m_run;
+          dst[1] = l_run;
+        }
+      }
+    }
+  } else if (row_ok) {
+    const int h = kvh * G + row % G;
+    float* dst = a.part + ((((int64_t)b * a.Hq + h) * a.Tq + qi) * a.n_split + split) * (D + 4);
+    dst[0] = -INFINITY;
+    dst[1] = 0.f;
+    for (int j = 0; j < D; ++j) dst[2 + j] = 0.f;
+  }
+  if (!ok && tid == 0) atomicExch(a.err, 1);
+  fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(kTmemCols) : "memory");
+  }
+}
+
+// Q^ = (H D q per K block) * softmax_scale * log2 e, fp16, rows i*G + h of
+// each (batch, KV head), zero padded to R_pad rows.
+template <int D>
+__global__ void __launch_bounds__(D) prefill_rotate_q_kernel(const CodecParams PK, const uint16_t* __restrict__ q,
+                                                              __half* __restrict__ qhat, int Hq, int Hkv, int Tq,
+                                                              int R_pad, float qscale) {
+  __shared__ float s[D];
+  const int r = blockIdx.x;        // padded row
+  const int bh = blockIdx.y;
+  const int b = bh / Hkv, kvh = bh % Hkv;
+  const int G = Hq / Hkv;
+  const int i = threadIdx.x;
+  const bool ok = r < Tq * G;
+  float v = 0.f;
+  if (ok) {
+    const int qi = r / G, h = kvh * G + r % G;
+    v = h2f(q[(((int64_t)b * Hq + h) * Tq + qi) * D + i]);
+    v = flip(v, (PK.sign_bits[i >> 5] >> (i & 31)) & 1u);
+  }
+  s[i] = v;
+  for (int hs = 1; hs < PK.blk; hs <<= 1) {
+    __syncthreads();
+    const float x = s[i], y = s[i ^ hs];
+    __syncthreads();
+    s[i] = (i & hs) ? (y - x) : (x + y);
+  }
+  __syncthreads();
+  qhat[((int64_t)bh * R_pad + r) * D + i] = __float2half_rn(s[i] * PK.inv_sqrt_blk * qscale);
+}
+
+template <int D>
+size_t tc_smem() {  // Q tile + double-buffered K and V tiles
+  return (size_t)kRowsTc * D * 2 + 4 * (size_t)kTok * D * 2;
+}
+
+}  // namespace
+
+int prefill_tc_splits(int B, int Hkv, int G, int Tq, int64_t ctx) {
+  const int row_tiles = (Tq * G + kRowsTc - 1) / kRowsTc;
+  const int ctas = row_tiles * B * Hkv;
+  int want = sm_count() / (ctas > 0 ? ctas : 1);
+  const int64_t max_by_len = (ctx + 4 * kTok - 1) / (4 * kTok);
+  if (want > max_by_len) want = (int)max_by_len;
+  return want < 1 ? 1 : want;
+}
+
+size_t prefill_tc_workspace(int B, int Hq, int Hkv, int d, int Tq, int64_t ctx) {
+  const int G = Hq / Hkv;
+  const int R_pad = (Tq * G + kRowsTc - 1) / kRowsTc * kRowsTc;
+  const int ns = prefill_tc_splits(B, Hkv, G, Tq, ctx);
+  const size_t qbytes = (size_t)B * Hkv * R_pad * d * 2;
+  const size_t pbytes = (size_t)B * Hq * Tq * ns * (d + 4) * 4;
+  return 256 + ((qbytes + 255) / 256) * 256 + pbytes;
+}
+
+int launch_prefill_tc(const CodecParams& PK, const CodecParams& PV, const uint8_t* kc, const uint16_t* ks,
+                      const uint8_t* vc, const uint16_t* vs, const uint16_t* q, int B, int Hq, int Hkv, int Tq,
+                      int64_t S_cap, int64_t ctx, int causal, float qscale, uint16_t* out, void* ws,
+                      cudaStream_t st) {
+  const int d = PK.d;
+  const int G = Hq / Hkv;
+  const int R_pad = (Tq * G + kRowsTc - 1) / kRowsTc * kRowsTc;
+  const int ns = prefill_tc_splits(B, Hkv, G, Tq, ctx);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  int* err = reinterpret_cast<int*>(base);
+  const size_t qbytes = (size_t)B * Hkv * R_pad * d * 2;
+  __half* qhat = reinterpret_cast<__half*>(base + 256);
+  float* part = reinterpret_cast<float*>(base + 256 + ((qbytes + 255) / 256) * 256);
+  if (cudaMemsetAsync(err, 0, sizeof(int), st) != cudaSuccess) return TQ_ERR_CUDA;
+  int64_t per = (ctx + ns - 1) / ns;
+  per = (per + kTok - 1) / kTok * kTok;
+  PrefillTcArgs a{reinterpret_cast<const uint32_t*>(kc), ks, reinterpret_cast<const uint32_t*>(vc), vs, qhat, part,
+                  err, S_cap, ctx, Hq, Hkv, Tq, R_pad, ns, causal, per};
+  dim3 qgrid(R_pad, B * Hkv);
+  dim3 grid(R_pad / kRowsTc, ns, B * Hkv);
+  switch (d) {
+    case 64: {
+      prefill_rotate_q_kernel<64><<<qgrid, 64, 0, st>>>(PK, q, qhat, Hq, Hkv, Tq, R_pad, qscale);
+      if (cudaFuncSetAttribute(prefill_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc_smem<64>()))
+        return TQ_ERR_CUDA;
+      prefill_tc_kernel<64><<<grid, kThr, tc_smem<64>(), st>>>(PK, PV, a);
+      break;
+    }
+    case 128: {
+      prefill_rotate_q_kernel<128><<<qgrid, 128, 0, st>>>(PK, q, qhat, Hq, Hkv, Tq, R_pad, qscale);
+      if (cudaFuncSetAttribute(prefill_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)tc_smem<128>()))
+        return TQ_ERR_CUDA;
+      prefill_tc_kernel<128><<<grid, kThr, tc_smem<128>(), st>>>(PK, PV, a);
+      break;
+    }
+    default: {
+      prefill_rotate_q_kernel<256><<<qgrid, 256, 0, st>>>(PK, q, qhat, Hq, Hkv, Tq, R_pad, qscale);
+      if (cudaFuncSetAttribute(prefill_tc_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)tc_smem<256>()))
+        return TQ_ERR_CUDA;
+      prefill_tc_kernel<256><<<grid, kThr, tc_smem<256>(), st>>>(PK, PV, a);
+      break;
+    }
+  }
+  if (cudaGetLastError() != cudaSuccess) return TQ_ERR_CUDA;
+  return decode_combine(PV, part, ns, out, B * Hq * Tq, st);
+}
+
+}  // namespace tq

@@ -35,12 +35,11 @@ namespace {
 
 constexpr int kRowsTc = 128;     // query rows per CTA (TMEM lanes)
 constexpr int kTok = 64;         // tokens per KV tile
-constexpr int kThr = 128;
 constexpr uint32_t kColS = 0, kColP = 64;
-// TMEM columns: S (64 fp32) at 0, P (64 fp16 = 32 columns) at 64, O (d fp32)
-// at kColO; a power of two >= the total
-template <int D> __host__ __device__ constexpr uint32_t tmem_cols() { return D == 256 ? 512u : 256u; }
-template <int D> __host__ __device__ constexpr uint32_t col_o() { return D == 256 ? 256u : 128u; }
+// TMEM columns: S (64 fp32) at 0, P (64 fp16 = 32 columns) at 64, Q^ (D fp16
+// = D/2 columns) at 128, O (D fp32) after it; a power of two >= the total
+template <int D> __host__ __device__ constexpr uint32_t col_o() { return 128u + D / 2; }
+template <int D> __host__ __device__ constexpr uint32_t tmem_cols() { return col_o<D>() + D <= 256u ? 256u : 512u; }
 constexpr float kLazyP = 8.0f;
 constexpr int kWaitLimit = 1 << 24;
 
@@ -168,23 +167,44 @@ __device__ __forceinline__ uint32_t hmul2u(uint32_t a, __half2 b) {
   return *reinterpret_cast<const uint32_t*>(&r);
 }
 
-// Decode tokens [t0, t0 + kTok) of one packed (batch, head) row range into a
-// core-matrix tile [kTok][D] (rotated, scaled fp16); tokens at or beyond
-// t_hi are written as zeros.
+// Packed bytes of tokens [t0, t0 + n) of one array (codes or scales; `sb`
+// bytes per token) staged into smem: the copy starts at the 16-byte boundary
+// at or below the first byte and never reads past the last byte needed.
+// Returns the offset of the first byte inside the staging area.
+__device__ __forceinline__ int stage_bytes(uint8_t* dst, const uint8_t* src_base, int64_t first_rec, int n, int sb,
+                                           int tid, int nthr) {
+  const int64_t s = first_rec * sb, e = s + (int64_t)n * sb;
+  const int64_t s0 = s & ~(int64_t)15;
+  const int chunks = (int)((e - s0 + 15) >> 4);
+  for (int c = tid; c < chunks; c += nthr) {
+    const int64_t at = s0 + 16 * (int64_t)c;
+    const int64_t rem = e - at;
+    const int bytes = rem >= 16 ? 16 : (int)rem;
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 16, %2;\n" ::"r"(su32(dst + 16 * c)), "l"(src_base + at),
+                 "r"(bytes));
+  }
+  return (int)(s - s0);
+}
+
+struct PackedSlot {   // offsets of the four arrays inside one staging slot
+  int kc, ks, vc, vs;
+};
+
+// Decode one 64-token tile from its staged packed bytes into a core-matrix
+// tile [kTok][D] (rotated, scaled fp16); tokens >= n_valid become zeros.
 template <int D>
-__device__ __forceinline__ void decode_tile_tc(const CodecParams& P, const Lut& L, const uint32_t* __restrict__ codes,
-                                               const uint16_t* __restrict__ scales, int64_t rec0, int64_t t0,
-                                               int64_t t_hi, uint8_t* tile) {
+__device__ __forceinline__ void decode_tile_smem(const CodecParams& P, const Lut& L, const uint8_t* codes,
+                                                 const uint8_t* scales, int n_valid, uint8_t* tile, int tid,
+                                                 int nthr) {
   constexpr int CH = D / 8;
-  const int words = P.code_bytes / 4;
-  for (int task = threadIdx.x; task < kTok * CH; task += kThr) {
+  for (int task = tid; task < kTok * CH; task += nthr) {
     const int tok = task / CH, ch = task % CH;
-    const int64_t t = t0 + tok;
     uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (t < t_hi) {
-      const uint32_t* rec = codes + (rec0 + t) * words;
+    if (tok < n_valid) {
+      const uint32_t* rec = reinterpret_cast<const uint32_t*>(codes + tok * P.code_bytes);
       const uint32_t nib = load_chunk(rec + (ch >> 2) * P.bits, P.bits, ch & 3);
-      const __half sc = __ushort_as_half(scales[(rec0 + t) * P.nb + (ch * 8) / P.blk]);
+      const uint16_t sraw = *reinterpret_cast<const uint16_t*>(scales + (tok * P.nb + (ch * 8) / P.blk) * 2);
+      const __half sc = __ushort_as_half(sraw);
       const __half2 sc2 = __halves2half2(sc, sc);
       uint32_t a, b, c, d;
       lut4(nib, L, P.bits, a, b);
@@ -196,43 +216,51 @@ __device__ __forceinline__ void decode_tile_tc(const CodecParams& P, const Lut& 
 }
 
 struct PrefillTcArgs {
-  const uint32_t* kc;
-  const uint16_t* ks;
-  const uint32_t* vc;
-  const uint16_t* vs;
+  const uint8_t* kc;
+  const uint8_t* ks;
+  const uint8_t* vc;
+  const uint8_t* vs;
   const __half* qhat;   // [B*Hkv][R_pad][D]
   float* part;          // [(b*Hq + h)*Tq + i][n_split][D + 4]
   int* err;
   int64_t S_cap, ctx;
   int Hq, Hkv, Tq, R_pad, n_split, causal;
   int64_t per;          // tokens per split (multiple of kTok)
+  int slot_bytes;       // one packed staging slot
+  PackedSlot slot;
 };
 
+constexpr int kThrTc = 256;   // 8 warps: all decode; warps 0-3 own the 128 TMEM rows
+
 template <int D>
-__global__ void __launch_bounds__(kThr, 1) prefill_tc_kernel(const CodecParams PK, const CodecParams PV,
-                                                             const PrefillTcArgs a) {
+__global__ void __launch_bounds__(kThrTc, 1) prefill_tc_kernel(const CodecParams PK, const CodecParams PV,
+                                                               const PrefillTcArgs a) {
+  constexpr uint32_t kTmemCols = tmem_cols<D>();
+  constexpr uint32_t kColQ = 128;                 // Q^ as the A operand of S, D/2 columns
+  constexpr uint32_t kColO = col_o<D>();          // O accumulator, D columns
+  constexpr uint32_t kTileBytes = kTok * D * 2;
+  constexpr uint32_t kGroupBytes = (D / 8) * 128;   // one 8-row band of a [rows][D] core-matrix tile
   extern __shared__ __align__(1024) uint8_t smem[];
-  uint8_t* sQ = smem;                                   // [128][D]
-  uint8_t* sK[2] = {sQ + kRowsTc * D * 2, sQ + kRowsTc * D * 2 + kTok * D * 2};
-  uint8_t* sV[2] = {sK[1] + kTok * D * 2, sK[1] + 2 * kTok * D * 2};
+  uint8_t* sK[2] = {smem, smem + kTileBytes};
+  uint8_t* sV[2] = {smem + 2 * kTileBytes, smem + 3 * kTileBytes};
+  uint8_t* sPk[2] = {smem + 4 * kTileBytes, smem + 4 * kTileBytes + a.slot_bytes};
   __shared__ __align__(8) uint64_t bar_s, bar_o;
   __shared__ uint32_t tmem_base;
+  __shared__ int s_off[2][4];   // byte offsets of the staged arrays per slot
 
-  constexpr uint32_t kTmemCols = tmem_cols<D>();
-  constexpr uint32_t kColO = col_o<D>();
   const int tid = threadIdx.x, warp = tid >> 5;
+  const bool row_warp = warp < 4;
   const int G = a.Hq / a.Hkv;
   const int rt = blockIdx.x;          // row tile
   const int split = blockIdx.y;
   const int bh = blockIdx.z;
   const int b = bh / a.Hkv, kvh = bh % a.Hkv;
   const int R = a.Tq * G;
-  const int row = rt * kRowsTc + tid;   // this thread's query row
-  const bool row_ok = row < R;
-  const int qi = row_ok ? row / G : a.Tq - 1;
+  const int row = rt * kRowsTc + (tid & 127);   // row of this thread (row warps)
+  const bool row_ok = row_warp && row < R;
+  const int qi = row < R ? row / G : a.Tq - 1;
   const int64_t pos = a.ctx - a.Tq + qi;
 
-  // context slice of this CTA, clipped to what the tile's last row can see
   const int last_row = min(rt * kRowsTc + kRowsTc, R) - 1;
   const int64_t max_pos = a.causal ? a.ctx - a.Tq + last_row / G : a.ctx - 1;
   const int64_t t_lo = (int64_t)split * a.per;
@@ -240,16 +268,26 @@ __global__ void __launch_bounds__(kThr, 1) prefill_tc_kernel(const CodecParams P
   const int n_tiles = t_hi > t_lo ? (int)((t_hi - t_lo + kTok - 1) / kTok) : 0;
   const int64_t rec0 = (int64_t)bh * a.S_cap;
 
-  // Q^ rows into the core-matrix tile
-  {
-    const __half* src = a.qhat + ((int64_t)bh * a.R_pad + (int64_t)rt * kRowsTc) * D;
-    for (int e = tid; e < kRowsTc * (D / 8); e += kThr) {
-      const int r = e / (D / 8), ch = e % (D / 8);
-      const uint4 v = *reinterpret_cast<const uint4*>(src + (int64_t)r * D + ch * 8);
-      *reinterpret_cast<uint4*>(sQ + cm_off(r, ch * 8, D)) = v;
+  auto stage = [&](int tile, int slot) {   // packed bytes of `tile` into staging slot `slot`
+    if (tile < n_tiles) {
+      const int64_t t0 = t_lo + (int64_t)tile * kTok;
+      const int n = (int)imin64(kTok, t_hi - t0);
+      uint8_t* base = sPk[slot];
+      const int o0 = stage_bytes(base + a.slot.kc, a.kc, rec0 + t0, n, PK.code_bytes, tid, kThrTc);
+      const int o1 = stage_bytes(base + a.slot.ks, a.ks, rec0 + t0, n, 2 * PK.nb, tid, kThrTc);
+      const int o2 = stage_bytes(base + a.slot.vc, a.vc, rec0 + t0, n, PV.code_bytes, tid, kThrTc);
+      const int o3 = stage_bytes(base + a.slot.vs, a.vs, rec0 + t0, n, 2 * PV.nb, tid, kThrTc);
+      if (tid == 0) {
+        s_off[slot][0] = o0; s_off[slot][1] = o1; s_off[slot][2] = o2; s_off[slot][3] = o3;
+      }
     }
-  }
+    asm volatile("cp.async.commit_group;\n" ::);
+  };
+  auto n_valid_of = [&](int tile) { return (int)imin64(kTok, t_hi - (t_lo + (int64_t)tile * kTok)); };
   const Lut lk = make_lut(PK), lv = make_lut(PV);
+
+  stage(0, 0);
+  stage(1, 1);
   if (tid == 0) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(su32(&bar_s)) : "memory");
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(su32(&bar_o)) : "memory");
@@ -260,28 +298,49 @@ __global__ void __launch_bounds__(kThr, 1) prefill_tc_kernel(const CodecParams P
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
   }
-  if (n_tiles > 0) decode_tile_tc<D>(PK, lk, a.kc, a.ks, rec0, t_lo, t_hi, sK[0]);
-  if (n_tiles > 0) decode_tile_tc<D>(PV, lv, a.vc, a.vs, rec0, t_lo, t_hi, sV[0]);
-  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
   fence_before();
   __syncthreads();
   fence_after();
   const uint32_t tmem = tmem_base;
-  const uint32_t lane_base = tmem + ((uint32_t)(32 * warp) << 16);
+  const uint32_t lane_base = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+  // Q^ rows into TMEM (A operand of S: 2 fp16 per column)
+  if (row_warp) {
+    const __half* src = a.qhat + ((int64_t)bh * a.R_pad + (int64_t)rt * kRowsTc + tid) * D;
+#pragma unroll 1
+    for (int c0 = 0; c0 < D / 2; c0 += 32) {
+      uint32_t w[32];
+#pragma unroll
+      for (int j = 0; j < 32; j += 4) {
+        const uint4 v = *reinterpret_cast<const uint4*>(src + 2 * (c0 + j));
+        w[j] = v.x; w[j + 1] = v.y; w[j + 2] = v.z; w[j + 3] = v.w;
+      }
+      TQ_ST32(lane_base + kColQ + c0, w);
+    }
+    asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
+  }
+  // tile 0 decoded before the first MMA
+  asm volatile("cp.async.wait_group 1;\n" ::);
+  __syncthreads();
+  if (n_tiles > 0) {
+    decode_tile_smem<D>(PK, lk, sPk[0] + a.slot.kc + s_off[0][0], sPk[0] + a.slot.ks + s_off[0][1], n_valid_of(0),
+                        sK[0], tid, kThrTc);
+    decode_tile_smem<D>(PV, lv, sPk[0] + a.slot.vc + s_off[0][2], sPk[0] + a.slot.vs + s_off[0][3], n_valid_of(0),
+                        sV[0], tid, kThrTc);
+  }
+  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+  fence_before();
+  __syncthreads();
+  fence_after();
 
-  // instruction descriptors: fp32 accumulate, fp16 A/B, M = 128
   const uint32_t idesc_s = (1u << 4) | ((uint32_t)(kTok >> 3) << 17) | ((uint32_t)(kRowsTc >> 4) << 24);
   const uint32_t idesc_o = (1u << 4) | (1u << 16) | ((uint32_t)(D >> 3) << 17) | ((uint32_t)(kRowsTc >> 4) << 24);
-  constexpr uint32_t kGroupBytes = (D / 8) * 128;   // one 8-row band of a [rows][D] core-matrix tile
-
-  auto issue_s = [&](int kb) {   // S = Q^ K^(buffer kb)^T
+  auto issue_s = [&](int kb) {   // S = Q^ (TMEM) K^(buffer kb)^T
 #pragma unroll 4
     for (int s = 0; s < D / 16; ++s)
-      mma_ss(tmem + kColS, sdesc(su32(sQ) + s * 256, 128, kGroupBytes), sdesc(su32(sK[kb]) + s * 256, 128, kGroupBytes),
-             idesc_s, s > 0);
+      mma_ts(tmem + kColS, tmem + kColQ + 8 * s, sdesc(su32(sK[kb]) + s * 256, 128, kGroupBytes), idesc_s, s > 0);
     mma_commit(su32(&bar_s));
   };
-  auto issue_o = [&](int vb, bool first) {   // O += P V^(buffer vb)
+  auto issue_o = [&](int vb, bool first) {   // O += P (TMEM) V^(buffer vb)
 #pragma unroll
     for (int s = 0; s < kTok / 16; ++s)
       mma_ts(tmem + kColO, tmem + kColP + 8 * s, sdesc(su32(sV[vb]) + s * 2 * kGroupBytes, kGroupBytes, 128), idesc_o,
@@ -297,59 +356,67 @@ __global__ void __launch_bounds__(kThr, 1) prefill_tc_kernel(const CodecParams P
   for (int t = 0; t < n_tiles && ok; ++t) {
     const int cur = t & 1, nxt = cur ^ 1;
     const int64_t t0 = t_lo + (int64_t)t * kTok;
-    // decode the next tile while S(t) and O(t-1) are in flight
-    if (t + 1 < n_tiles) decode_tile_tc<D>(PK, lk, a.kc, a.ks, rec0, t0 + kTok, t_hi, sK[nxt]);
+    stage(t + 2, cur);                              // slot cur held tile t (already decoded)
+    asm volatile("cp.async.wait_group 1;\n" ::);    // tile t+1 staged (own copies)
+    __syncthreads();
+    if (t + 1 < n_tiles)
+      decode_tile_smem<D>(PK, lk, sPk[nxt] + a.slot.kc + s_off[nxt][0], sPk[nxt] + a.slot.ks + s_off[nxt][1],
+                          n_valid_of(t + 1), sK[nxt], tid, kThrTc);
     if (t >= 1) ok = ok && bar_wait(su32(&bar_o), (t - 1) & 1);          // O(t-1) done: P and V(nxt) free
-    if (t + 1 < n_tiles) decode_tile_tc<D>(PV, lv, a.vc, a.vs, rec0, t0 + kTok, t_hi, sV[nxt]);
-    ok = ok && bar_wait(su32(&bar_s), t & 1);                            // S(t) ready
-    fence_after();
-    // ---- softmax on this thread's row of S
-    uint32_t sv[32], sw[32];
-    TQ_LD32(lane_base + kColS, sv);
-    TQ_LD32(lane_base + kColS + 32, sw);
-    asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
-    float mx = -INFINITY;
+    if (t + 1 < n_tiles)
+      decode_tile_smem<D>(PV, lv, sPk[nxt] + a.slot.vc + s_off[nxt][2], sPk[nxt] + a.slot.vs + s_off[nxt][3],
+                          n_valid_of(t + 1), sV[nxt], tid, kThrTc);
+    if (row_warp) {
+      ok = ok && bar_wait(su32(&bar_s), t & 1);                          // S(t) ready
+      fence_after();
+      // ---- softmax on this thread's row of S
+      uint32_t sv[32], sw[32];
+      TQ_LD32(lane_base + kColS, sv);
+      TQ_LD32(lane_base + kColS + 32, sw);
+      asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+      float mx = -INFINITY;
 #pragma unroll
-    for (int c = 0; c < kTok; ++c) {
-      const int64_t tok = t0 + c;
-      const bool valid = row_ok && tok < t_hi && (!a.causal || tok <= pos);
-      float v = __uint_as_float(c < 32 ? sv[c] : sw[c - 32]);
-      v = valid ? v : -INFINITY;
-      if (c < 32) sv[c] = __float_as_uint(v); else sw[c - 32] = __float_as_uint(v);
-      mx = fmaxf(mx, v);
-    }
-    const bool need = mx > m_run + kLazyP;
-    if (__any_sync(0xffffffffu, need)) {
-      const float m_new = need ? mx : m_run;
-      const float alpha = (need && m_run != -INFINITY) ? ex2f(m_run - m_new) : 1.f;
-      m_run = m_new;
-      l_run *= alpha;
-      if (o_started) {   // rescale this row of O (warp-wide TMEM access; alpha = 1 for rows that keep m)
+      for (int c = 0; c < kTok; ++c) {
+        const int64_t tok = t0 + c;
+        const bool valid = row_ok && tok < t_hi && (!a.causal || tok <= pos);
+        float v = __uint_as_float(c < 32 ? sv[c] : sw[c - 32]);
+        v = valid ? v : -INFINITY;
+        if (c < 32) sv[c] = __float_as_uint(v); else sw[c - 32] = __float_as_uint(v);
+        mx = fmaxf(mx, v);
+      }
+      const bool need = mx > m_run + kLazyP;
+      if (__any_sync(0xffffffffu, need)) {
+        const float m_new = need ? mx : m_run;
+        const float alpha = (need && m_run != -INFINITY) ? ex2f(m_run - m_new) : 1.f;
+        m_run = m_new;
+        l_run *= alpha;
+        if (o_started) {   // rescale this row of O (alpha = 1 for rows that keep m)
 #pragma unroll 1
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          uint32_t ov[32];
-          TQ_LD32(lane_base + kColO + c0, ov);
-          asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t ov[32];
+            TQ_LD32(lane_base + kColO + c0, ov);
+            asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
 #pragma unroll
-          for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * alpha);
-          TQ_ST32(lane_base + kColO + c0, ov);
+            for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * alpha);
+            TQ_ST32(lane_base + kColO + c0, ov);
+          }
         }
       }
-    }
-    const float mref = m_run == -INFINITY ? 0.f : m_run;
-    uint32_t pw[32];
-    float sum = 0.f;
+      const float mref = m_run == -INFINITY ? 0.f : m_run;
+      uint32_t pw[32];
+      float sum = 0.f;
 #pragma unroll
-    for (int c = 0; c < 32; ++c) {
-      const float p0 = ex2f(__uint_as_float(c < 16 ? sv[2 * c] : sw[2 * c - 32]) - mref);
-      const float p1 = ex2f(__uint_as_float(c < 16 ? sv[2 * c + 1] : sw[2 * c + 1 - 32]) - mref);
-      sum += p0 + p1;
-      const __half2 h = __floats2half2_rn(p0, p1);
-      pw[c] = *reinterpret_cast<const uint32_t*>(&h);
+      for (int c = 0; c < 32; ++c) {
+        const float p0 = ex2f(__uint_as_float(c < 16 ? sv[2 * c] : sw[2 * c - 32]) - mref);
+        const float p1 = ex2f(__uint_as_float(c < 16 ? sv[2 * c + 1] : sw[2 * c + 1 - 32]) - mref);
+        sum += p0 + p1;
+        const __half2 h = __floats2half2_rn(p0, p1);
+        pw[c] = *reinterpret_cast<const uint32_t*>(&h);
+      }
+      l_run += sum;
+      TQ_ST32(lane_base + kColP, pw);
+      asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
     }
-    l_run += sum;
-    TQ_ST32(lane_base + kColP, pw);
-    asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");   // decoded tiles -> tensor core
     fence_before();
     ok = __syncthreads_and(ok) != 0;   // a timed-out wait stops the whole CTA together
@@ -363,29 +430,30 @@ __global__ void __launch_bounds__(kThr, 1) prefill_tc_kernel(const CodecParams P
   if (n_tiles > 0 && ok) ok = bar_wait(su32(&bar_o), (n_tiles - 1) & 1);
   ok = __syncthreads_and(ok) != 0;
   fence_after();
+  asm volatile("cp.async.wait_group 0;\n" ::);
   // ---- partial (m, l, O) of this row for this context slice
-  if (ok && n_tiles > 0) {
-    for (int c0 = 0; c0 < D; c0 += 32) {
-      uint32_t ov[32];
-      TQ_LD32(lane_base + kColO + c0, ov);
-      asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
-      if (row_ok) {
-        const int h = kvh * G + row % G;
-        float* dst = a.part + ((((int64_t)b * a.Hq + h) * a.Tq + qi) * a.n_split + split) * (D + 4);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) dst[2 + c0 + j] = __uint_as_float(ov[j]);
-        if (c0 == 0) {
-          dst[0] = m_run;
-          dst[1] = l_run;
-        }
-      }
-    }
-  } else if (row_ok) {
+  if (row_warp) {
     const int h = kvh * G + row % G;
     float* dst = a.part + ((((int64_t)b * a.Hq + h) * a.Tq + qi) * a.n_split + split) * (D + 4);
-    dst[0] = -INFINITY;
-    dst[1] = 0.f;
-    for (int j = 0; j < D; ++j) dst[2 + j] = 0.f;
+    if (ok && n_tiles > 0) {
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t ov[32];
+        TQ_LD32(lane_base + kColO + c0, ov);
+        asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+        if (row_ok) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) dst[2 + c0 + j] = __uint_as_float(ov[j]);
+          if (c0 == 0) {
+            dst[0] = m_run;
+            dst[1] = l_run;
+          }
+        }
+      }
+    } else if (row_ok) {
+      dst[0] = -INFINITY;
+      dst[1] = 0.f;
+      for (int j = 0; j < D; ++j) dst[2 + j] = 0.f;
+    }
   }
   if (!ok && tid == 0) atomicExch(a.err, 1);
   fence_before();
@@ -426,8 +494,8 @@ __global__ void __launch_bounds__(D) prefill_rotate_q_kernel(const CodecParams P
 }
 
 template <int D>
-size_t tc_smem() {  // Q tile + double-buffered K and V tiles
-  return (size_t)kRowsTc * D * 2 + 4 * (size_t)kTok * D * 2;
+size_t tc_smem(int slot_bytes) {  // double-buffered decoded K and V tiles + two packed staging slots
+  return 4 * (size_t)kTok * D * 2 + 2 * (size_t)slot_bytes;
 }
 
 }  // namespace
@@ -466,32 +534,41 @@ int launch_prefill_tc(const CodecParams& PK, const CodecParams& PV, const uint8_
   if (cudaMemsetAsync(err, 0, sizeof(int), st) != cudaSuccess) return TQ_ERR_CUDA;
   int64_t per = (ctx + ns - 1) / ns;
   per = (per + kTok - 1) / kTok * kTok;
-  PrefillTcArgs a{reinterpret_cast<const uint32_t*>(kc), ks, reinterpret_cast<const uint32_t*>(vc), vs, qhat, part,
-                  err, S_cap, ctx, Hq, Hkv, Tq, R_pad, ns, causal, per};
+  // staging slot: each array padded to 16 bytes plus 16 bytes of alignment slack
+  auto pad = [](int bytes) { return (bytes + 16 + 15) / 16 * 16; };
+  PackedSlot slot;
+  slot.kc = 0;
+  slot.ks = slot.kc + pad(kTok * PK.code_bytes);
+  slot.vc = slot.ks + pad(kTok * 2 * PK.nb);
+  slot.vs = slot.vc + pad(kTok * PV.code_bytes);
+  const int slot_bytes = slot.vs + pad(kTok * 2 * PV.nb);
+  PrefillTcArgs a{kc, reinterpret_cast<const uint8_t*>(ks), vc, reinterpret_cast<const uint8_t*>(vs), qhat, part,
+                  err, S_cap, ctx, Hq, Hkv, Tq, R_pad, ns, causal, per, slot_bytes, slot};
   dim3 qgrid(R_pad, B * Hkv);
   dim3 grid(R_pad / kRowsTc, ns, B * Hkv);
   switch (d) {
     case 64: {
       prefill_rotate_q_kernel<64><<<qgrid, 64, 0, st>>>(PK, q, qhat, Hq, Hkv, Tq, R_pad, qscale);
-      if (cudaFuncSetAttribute(prefill_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc_smem<64>()))
+      const size_t sm = tc_smem<64>(slot_bytes);
+      if (cudaFuncSetAttribute(prefill_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm))
         return TQ_ERR_CUDA;
-      prefill_tc_kernel<64><<<grid, kThr, tc_smem<64>(), st>>>(PK, PV, a);
+      prefill_tc_kernel<64><<<grid, kThrTc, sm, st>>>(PK, PV, a);
       break;
     }
     case 128: {
       prefill_rotate_q_kernel<128><<<qgrid, 128, 0, st>>>(PK, q, qhat, Hq, Hkv, Tq, R_pad, qscale);
-      if (cudaFuncSetAttribute(prefill_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)tc_smem<128>()))
+      const size_t sm = tc_smem<128>(slot_bytes);
+      if (cudaFuncSetAttribute(prefill_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm))
         return TQ_ERR_CUDA;
-      prefill_tc_kernel<128><<<grid, kThr, tc_smem<128>(), st>>>(PK, PV, a);
+      prefill_tc_kernel<128><<<grid, kThrTc, sm, st>>>(PK, PV, a);
       break;
     }
     default: {
       prefill_rotate_q_kernel<256><<<qgrid, 256, 0, st>>>(PK, q, qhat, Hq, Hkv, Tq, R_pad, qscale);
-      if (cudaFuncSetAttribute(prefill_tc_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)tc_smem<256>()))
+      const size_t sm = tc_smem<256>(slot_bytes);
+      if (cudaFuncSetAttribute(prefill_tc_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm))
         return TQ_ERR_CUDA;
-      prefill_tc_kernel<256><<<grid, kThr, tc_smem<256>(), st>>>(PK, PV, a);
+      prefill_tc_kernel<256><<<grid, kThrTc, sm, st>>>(PK, PV, a);
       break;
     }
   }

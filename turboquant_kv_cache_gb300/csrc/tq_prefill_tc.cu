@@ -34,6 +34,8 @@ int sm_count();
 namespace {
 
 constexpr int kRowsTc = 128;     // query rows per CTA (TMEM lanes)
+constexpr int kThrTc = 256;      // 8 warps: all decode; warps 0-3 own the 128 TMEM rows
+constexpr int kThrTcConst = kThrTc;
 constexpr int kTok = 64;         // tokens per KV tile
 constexpr uint32_t kColS = 0, kColP = 64;
 // TMEM columns: S (64 fp32) at 0, P (64 fp16 = 32 columns) at 64, Q^ (D fp16
@@ -190,28 +192,72 @@ struct PackedSlot {   // offsets of the four arrays inside one staging slot
   int kc, ks, vc, vs;
 };
 
-// Decode one 64-token tile from its staged packed bytes into a core-matrix
-// tile [kTok][D] (rotated, scaled fp16); tokens >= n_valid become zeros.
-template <int D>
-__device__ __forceinline__ void decode_tile_smem(const CodecParams& P, const Lut& L, const uint8_t* codes,
-                                                 const uint8_t* scales, int n_valid, uint8_t* tile, int tid,
-                                                 int nthr) {
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];\n" : "=r"(v) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint16_t lds16(uint32_t addr) {
+  uint16_t v;
+  asm volatile("ld.shared.u16 %0, [%1];\n" : "=h"(v) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+// Nibble word (8 codes) of chunk w (0..3) of a 32-code group at shared
+// address g, for a compile-time bit width.
+template <int BITS>
+__device__ __forceinline__ uint32_t chunk_smem(uint32_t g, int w) {
+  if (BITS == 4) return lds32(g + 4 * w);
+  if (BITS == 3) {
+    if (w < 3) return lds32(g + 4 * w) & 0x77777777u;
+    return ((lds32(g) >> 3) & 0x11111111u) | ((lds32(g + 4) >> 2) & 0x22222222u) |
+           ((lds32(g + 8) >> 1) & 0x44444444u);
+  }
+  if (BITS == 2) return w < 2 ? (lds32(g + 4 * w) & 0x33333333u) : ((lds32(g + 4 * (w - 2)) >> 2) & 0x33333333u);
+  return (lds32(g) >> w) & 0x11111111u;
+}
+
+// Decode one 64-token tile from its staged packed bytes (shared addresses
+// codes / scales) into a core-matrix tile [kTok][D] at shared address tile:
+// rotated, scaled fp16; tokens >= n_valid become zeros.  Thread tid always
+// decodes the same 8-code chunk (tid % (D/8)) of a set of tokens.
+template <int D, int BITS>
+__device__ __forceinline__ void decode_tile_bits(const CodecParams& P, const Lut& L, uint32_t codes, uint32_t scales,
+                                                 int n_valid, uint32_t tile, int tid) {
   constexpr int CH = D / 8;
-  for (int task = tid; task < kTok * CH; task += nthr) {
-    const int tok = task / CH, ch = task % CH;
+  constexpr int TPASS = kThrTcConst / CH;     // tokens per pass
+  const int ch = tid % CH, tok0 = tid / CH;
+  const uint32_t grp = (uint32_t)((ch >> 2) * BITS * 4);
+  const int w = ch & 3;
+  const uint32_t sidx = (uint32_t)((ch * 8) / P.blk) * 2;
+#pragma unroll 2
+  for (int tok = tok0; tok < kTok; tok += TPASS) {
     uint4 v = make_uint4(0u, 0u, 0u, 0u);
     if (tok < n_valid) {
-      const uint32_t* rec = reinterpret_cast<const uint32_t*>(codes + tok * P.code_bytes);
-      const uint32_t nib = load_chunk(rec + (ch >> 2) * P.bits, P.bits, ch & 3);
-      const uint16_t sraw = *reinterpret_cast<const uint16_t*>(scales + (tok * P.nb + (ch * 8) / P.blk) * 2);
-      const __half sc = __ushort_as_half(sraw);
+      const uint32_t nib = chunk_smem<BITS>(codes + tok * P.code_bytes + grp, w);
+      const __half sc = __ushort_as_half(lds16(scales + tok * P.nb * 2 + sidx));
       const __half2 sc2 = __halves2half2(sc, sc);
       uint32_t a, b, c, d;
-      lut4(nib, L, P.bits, a, b);
-      lut4(nib >> 16, L, P.bits, c, d);
+      lut4(nib, L, BITS, a, b);
+      lut4(nib >> 16, L, BITS, c, d);
       v = make_uint4(hmul2u(a, sc2), hmul2u(b, sc2), hmul2u(c, sc2), hmul2u(d, sc2));
     }
-    *reinterpret_cast<uint4*>(tile + cm_off(tok, ch * 8, D)) = v;
+    sts128(tile + cm_off(tok, ch * 8, D), v);
+  }
+}
+
+template <int D>
+__device__ __forceinline__ void decode_tile_smem(const CodecParams& P, const Lut& L, uint32_t codes, uint32_t scales,
+                                                 int n_valid, uint32_t tile, int tid) {
+  switch (P.bits) {
+    case 4: decode_tile_bits<D, 4>(P, L, codes, scales, n_valid, tile, tid); break;
+    case 3: decode_tile_bits<D, 3>(P, L, codes, scales, n_valid, tile, tid); break;
+    case 2: decode_tile_bits<D, 2>(P, L, codes, scales, n_valid, tile, tid); break;
+    default: decode_tile_bits<D, 1>(P, L, codes, scales, n_valid, tile, tid); break;
   }
 }
 
@@ -230,7 +276,6 @@ struct PrefillTcArgs {
   PackedSlot slot;
 };
 
-constexpr int kThrTc = 256;   // 8 warps: all decode; warps 0-3 own the 128 TMEM rows
 
 template <int D>
 __global__ void __launch_bounds__(kThrTc, 1) prefill_tc_kernel(const CodecParams PK, const CodecParams PV,
@@ -244,6 +289,9 @@ __global__ void __launch_bounds__(kThrTc, 1) prefill_tc_kernel(const CodecParams
   uint8_t* sK[2] = {smem, smem + kTileBytes};
   uint8_t* sV[2] = {smem + 2 * kTileBytes, smem + 3 * kTileBytes};
   uint8_t* sPk[2] = {smem + 4 * kTileBytes, smem + 4 * kTileBytes + a.slot_bytes};
+  const uint32_t aK[2] = {su32(sK[0]), su32(sK[1])};
+  const uint32_t aV[2] = {su32(sV[0]), su32(sV[1])};
+  const uint32_t aPk[2] = {su32(sPk[0]), su32(sPk[1])};
   __shared__ __align__(8) uint64_t bar_s, bar_o;
   __shared__ uint32_t tmem_base;
   __shared__ int s_off[2][4];   // byte offsets of the staged arrays per slot
@@ -322,10 +370,10 @@ __global__ void __launch_bounds__(kThrTc, 1) prefill_tc_kernel(const CodecParams
   asm volatile("cp.async.wait_group 1;\n" ::);
   __syncthreads();
   if (n_tiles > 0) {
-    decode_tile_smem<D>(PK, lk, sPk[0] + a.slot.kc + s_off[0][0], sPk[0] + a.slot.ks + s_off[0][1], n_valid_of(0),
-                        sK[0], tid, kThrTc);
-    decode_tile_smem<D>(PV, lv, sPk[0] + a.slot.vc + s_off[0][2], sPk[0] + a.slot.vs + s_off[0][3], n_valid_of(0),
-                        sV[0], tid, kThrTc);
+    decode_tile_smem<D>(PK, lk, aPk[0] + a.slot.kc + s_off[0][0], aPk[0] + a.slot.ks + s_off[0][1], n_valid_of(0),
+                        aK[0], tid);
+    decode_tile_smem<D>(PV, lv, aPk[0] + a.slot.vc + s_off[0][2], aPk[0] + a.slot.vs + s_off[0][3], n_valid_of(0),
+                        aV[0], tid);
   }
   asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
   fence_before();
@@ -337,13 +385,13 @@ __global__ void __launch_bounds__(kThrTc, 1) prefill_tc_kernel(const CodecParams
   auto issue_s = [&](int kb) {   // S = Q^ (TMEM) K^(buffer kb)^T
 #pragma unroll 4
     for (int s = 0; s < D / 16; ++s)
-      mma_ts(tmem + kColS, tmem + kColQ + 8 * s, sdesc(su32(sK[kb]) + s * 256, 128, kGroupBytes), idesc_s, s > 0);
+      mma_ts(tmem + kColS, tmem + kColQ + 8 * s, sdesc(aK[kb] + s * 256, 128, kGroupBytes), idesc_s, s > 0);
     mma_commit(su32(&bar_s));
   };
   auto issue_o = [&](int vb, bool first) {   // O += P (TMEM) V^(buffer vb)
 #pragma unroll
     for (int s = 0; s < kTok / 16; ++s)
-      mma_ts(tmem + kColO, tmem + kColP + 8 * s, sdesc(su32(sV[vb]) + s * 2 * kGroupBytes, kGroupBytes, 128), idesc_o,
+      mma_ts(tmem + kColO, tmem + kColP + 8 * s, sdesc(aV[vb] + s * 2 * kGroupBytes, kGroupBytes, 128), idesc_o,
              (first && s == 0) ? 0 : 1);
     mma_commit(su32(&bar_o));
   };
@@ -360,12 +408,12 @@ __global__ void __launch_bounds__(kThrTc, 1) prefill_tc_kernel(const CodecParams
     asm volatile("cp.async.wait_group 1;\n" ::);    // tile t+1 staged (own copies)
     __syncthreads();
     if (t + 1 < n_tiles)
-      decode_tile_smem<D>(PK, lk, sPk[nxt] + a.slot.kc + s_off[nxt][0], sPk[nxt] + a.slot.ks + s_off[nxt][1],
-                          n_valid_of(t + 1), sK[nxt], tid, kThrTc);
+      decode_tile_smem<D>(PK, lk, aPk[nxt] + a.slot.kc + s_off[nxt][0], aPk[nxt] + a.slot.ks + s_off[nxt][1],
+                          n_valid_of(t + 1), aK[nxt], tid);
     if (t >= 1) ok = ok && bar_wait(su32(&bar_o), (t - 1) & 1);          // O(t-1) done: P and V(nxt) free
     if (t + 1 < n_tiles)
-      decode_tile_smem<D>(PV, lv, sPk[nxt] + a.slot.vc + s_off[nxt][2], sPk[nxt] + a.slot.vs + s_off[nxt][3],
-                          n_valid_of(t + 1), sV[nxt], tid, kThrTc);
+      decode_tile_smem<D>(PV, lv, aPk[nxt] + a.slot.vc + s_off[nxt][2], aPk[nxt] + a.slot.vs + s_off[nxt][3],
+                          n_valid_of(t + 1), aV[nxt], tid);
     if (row_warp) {
       ok = ok && bar_wait(su32(&bar_s), t & 1);                          // S(t) ready
       fence_after();

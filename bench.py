@@ -118,6 +118,47 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- GPU arm
+def headline_cache(tb, torch, inputs, dev):
+    """The packed turbo3 cache of the Qwen3-8B-shaped decode batch, built on
+    the device from the seeded fp16 K/V, and its query batch."""
+    B, Hq, Hkv, d, ctx = DEC["B"], DEC["Hq"], DEC["Hkv"], DEC["d"], DEC["ctx"]
+    L = tb.make_layout(d, TURBO3["block"], TURBO3["bits"], 0, 0, 1)
+    K = tb.PackedKV(L, (B, Hkv, ctx), device=dev)
+    V = tb.PackedKV(L, (B, Hkv, ctx), device=dev)
+    for b in range(B):                       # one batch row at a time bounds host memory
+        kb = inputs.gaussian((Hkv, ctx, d), 1000 * 11 + b)
+        vb = inputs.gaussian((Hkv, ctx, d), 1000 * 12 + b)
+        for src, dst in ((kb, K), (vb, V)):
+            part = tb.tq_quantize_kv(L, torch.from_numpy(src).to(dev))
+            dst.codes[b].copy_(part.codes)
+            dst.scales[b].copy_(part.scales)
+    q = torch.from_numpy(inputs.gaussian((B, Hq, d), 10)).to(dev)
+    return L, K, V, q
+
+
+def run_only(args, tb, torch, inputs, dev):
+    """One workload on its own (for profiler runs): the same inputs and calls
+    as the full run, `--warmup` untimed then `--steps` timed passes, one JSON
+    line with the result and no contract keys."""
+    res = {"only": args.only}
+    if args.only == "decode":
+        B, Hq, Hkv, d, ctx = DEC["B"], DEC["Hq"], DEC["Hkv"], DEC["d"], DEC["ctx"]
+        L, K, V, q = headline_cache(tb, torch, inputs, dev)
+        ws_bytes, n_split = tb.tq_decode_workspace_bytes(B, Hq, Hkv, d, ctx, 0)
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+        out = torch.empty_like(q)
+        flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=dev)
+        ms = _time(torch, lambda: tb.tq_decode_attn(K, V, q, ctx=ctx, workspace=ws, out=out, n_split=n_split),
+                   flush, args.steps, args.warmup)
+        nbytes = decode_bytes(B, Hkv, ctx, d, 3, 3, 32, 32)
+        res.update(workload=WORKLOAD, ms=round(ms, 5), GBps=round(nbytes / (ms * 1e-3) / 1e9, 1))
+    elif args.only == "quantize":
+        res.update(bench_quantize(tb, torch, inputs, dev, args))
+    else:
+        res.update(bench_extra(tb, torch, inputs, dev, args, which=args.only))
+    print(json.dumps(res), flush=True)
+
+
 def run_gpu(args, rank, world):
     import torch
     from turboquant_kv_cache_gb300 import binding as tb
@@ -130,19 +171,10 @@ def run_gpu(args, rank, world):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
 
+    if args.only:
+        return run_only(args, tb, torch, inputs, dev)
     B, Hq, Hkv, d, ctx = DEC["B"], DEC["Hq"], DEC["Hkv"], DEC["d"], DEC["ctx"]
-    L = tb.make_layout(d, TURBO3["block"], TURBO3["bits"], 0, 0, 1)
-    # the packed cache, built on the device from the seeded fp16 K/V
-    K = tb.PackedKV(L, (B, Hkv, ctx), device=dev)
-    V = tb.PackedKV(L, (B, Hkv, ctx), device=dev)
-    for b in range(B):                       # one batch row at a time bounds host memory
-        kb = inputs.gaussian((Hkv, ctx, d), 1000 * 11 + b)
-        vb = inputs.gaussian((Hkv, ctx, d), 1000 * 12 + b)
-        for src, dst in ((kb, K), (vb, V)):
-            part = tb.tq_quantize_kv(L, torch.from_numpy(src).to(dev))
-            dst.codes[b].copy_(part.codes)
-            dst.scales[b].copy_(part.scales)
-    q = torch.from_numpy(inputs.gaussian((B, Hq, d), 10)).to(dev)
+    L, K, V, q = headline_cache(tb, torch, inputs, dev)
     ws_bytes, n_split = tb.tq_decode_workspace_bytes(B, Hq, Hkv, d, ctx, 0)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     out = torch.empty_like(q)
@@ -193,7 +225,7 @@ def run_gpu(args, rank, world):
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max, 5),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16 x f16 -> f32",
             "data": "synthetic (seeded N(0,1) fp16 K/V/q, quantised on device)",
             "config": {"workload": WORKLOAD, "n_split": n_split, "algorithmic_bytes_per_step": nbytes,
                        "l2": "cache 235 MB > L2 and a 512 MB write flushes L2 between steps (outside events)",
@@ -202,7 +234,7 @@ def run_gpu(args, rank, world):
             "roofline": {"bound": "hbm", "achieved": round(value / world, 2), "peak": peak,
                          "unit": "GB/s", "frac": round(value / world / peak, 4), "traffic": None,
                          "peak_source": f"{peak_kind} hbm_gbs (burst copy)",
-                         "kernel": "decode_split_kernel + decode_combine_kernel (one tq_decode_attn call)"},
+                         "kernel": "decode_tc_kernel + decode_combine_kernel (one tq_decode_attn call, events around both)"},
             "e2e": e2e,
             "quantize": quant,
             "other_workloads": extra,
@@ -267,7 +299,7 @@ def bench_quantize(tb, torch, inputs, dev, args):
         L = tb.make_layout(64, block, 4, 0, 0, 1)
         ok = tb.tq_quantize_kv(L, k)
         ov = tb.tq_quantize_kv(L, v)
-        for _ in range(max(3, args.warmup)):
+        for _ in range(args.warmup if args.only else max(3, args.warmup)):
             flush.zero_()
             tb.tq_quantize_kv(L, k, out=ok)
             tb.tq_quantize_kv(L, v, out=ov)
@@ -333,7 +365,7 @@ def _cache_from(tb, torch, L, x_np, dev, S=None):
     return pk
 
 
-def bench_extra(tb, torch, inputs, dev, args):
+def bench_extra(tb, torch, inputs, dev, args, which=None):
     """The other workloads of the path, each timed on its own (CUDA events,
     L2 flushed before every step): head_dim 256 / 131072-context decode and
     512-query causal prefill (turbo4 K, turbo3 V, Student-t keys), and the
@@ -343,6 +375,18 @@ def bench_extra(tb, torch, inputs, dev, args):
     hbm, _ = _peaks()
     tflops, tsrc = _peak_tflops()
     steps = max(2, min(args.steps, 5))
+    warm = 2
+    if which:
+        steps, warm = args.steps, args.warmup
+    if which in (None, "decode_d256", "prefill"):
+        out.update(_extra_d256(tb, torch, inputs, dev, flush, hbm, tflops, tsrc, steps, warm, which))
+    if which in (None, "decode_qjl"):
+        out.update(_extra_qjl(tb, torch, inputs, dev, flush, hbm, steps, warm))
+    return out
+
+
+def _extra_d256(tb, torch, inputs, dev, flush, hbm, tflops, tsrc, steps, warm, which):
+    out = {}
     # head_dim 256, 131072 context
     w = inputs.d256_longctx_workload()
     Lk = tb.make_layout(256, 32, 4, 0, 0, 1)
@@ -352,16 +396,20 @@ def bench_extra(tb, torch, inputs, dev, args):
     del w["k"], w["v"]
     q = torch.from_numpy(w["q"]).to(dev)
     ctx = 131072
-    ms = _time(torch, lambda: tb.tq_decode_attn(K, V, q, ctx=ctx), flush, steps, 2)
-    nbytes = K.nbytes() + V.nbytes()
-    out["decode_d256_ctx131072"] = {
-        "workload": "B=1, Hq=16, Hkv=4, d=256, ctx=131072, turbo4 K (Student-t nu=4) / turbo3 V",
-        "ms": round(ms, 4), "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1),
-        "roofline": {"bound": "hbm", "achieved": round(nbytes / (ms * 1e-3) / 1e9, 1), "peak": hbm, "unit": "GB/s",
-                     "frac": round(nbytes / (ms * 1e-3) / 1e9 / hbm, 4)}}
+    if which != "prefill":
+        ms = _time(torch, lambda: tb.tq_decode_attn(K, V, q, ctx=ctx), flush, steps, warm)
+        nbytes = K.nbytes() + V.nbytes()
+        out["decode_d256_ctx131072"] = {
+            "workload": "B=1, Hq=16, Hkv=4, d=256, ctx=131072, turbo4 K (Student-t nu=4) / turbo3 V",
+            "ms": round(ms, 4), "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1),
+            "roofline": {"bound": "hbm", "achieved": round(nbytes / (ms * 1e-3) / 1e9, 1), "peak": hbm,
+                         "unit": "GB/s", "frac": round(nbytes / (ms * 1e-3) / 1e9 / hbm, 4)}}
+    if which == "decode_d256":
+        return out
     qp = torch.from_numpy(w["q_prefill"]).to(dev)
     Tq = qp.shape[2]
-    ms = _time(torch, lambda: tb.tq_prefill_attn(K, V, qp, ctx, causal=True), flush, 2, 1)
+    ms = _time(torch, lambda: tb.tq_prefill_attn(K, V, qp, ctx, causal=True), flush,
+               steps if which else 2, warm if which else 1)
     pairs = Tq * (ctx - Tq) + Tq * (Tq + 1) // 2       # causal (query, key) pairs per q-head
     flop = 4.0 * 256 * pairs * 16                       # QK^T + PV, 16 q-heads
     tf = flop / (ms * 1e-3) / 1e12
@@ -372,6 +420,11 @@ def bench_extra(tb, torch, inputs, dev, args):
                      "frac": round(tf / tflops, 4), "peak_source": tsrc, "flop_per_step": flop}}
     del K, V
     torch.cuda.empty_cache()
+    return out
+
+
+def _extra_qjl(tb, torch, inputs, dev, flush, hbm, steps, warm):
+    out = {}
     # QJL keys
     w = inputs.qjl_decode_workload()
     S = torch.from_numpy(w["S"]).to(dev)
@@ -380,7 +433,7 @@ def bench_extra(tb, torch, inputs, dev, args):
     K = _cache_from(tb, torch, Lk, w["k"], dev, S=S)
     V = _cache_from(tb, torch, Lv, w["v"], dev)
     q = torch.from_numpy(w["q"]).to(dev)
-    ms = _time(torch, lambda: tb.tq_decode_attn(K, V, q, ctx=16384), flush, steps, 2)
+    ms = _time(torch, lambda: tb.tq_decode_attn(K, V, q, ctx=16384), flush, steps, warm)
     nbytes = K.nbytes() + V.nbytes()
     out["decode_qjl_keys_ctx16384"] = {
         "workload": "B=4, Hq=32, Hkv=8, d=128, ctx=16384; K 2-bit + QJL m=128, V 3-bit, one norm per vector",
@@ -476,6 +529,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true", help="skip the other workloads (headline only)")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--only", default=None,
+                    choices=["decode", "quantize", "prefill", "decode_d256", "decode_qjl"],
+                    help="time one workload alone and print its result only (profiler runs)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -259,48 +259,104 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const CodecPa
   }
 }
 
+constexpr int kCombWarps = 2;  // rows per CTA: many small CTAs spread the L2 reads over the SMs
+
+// One warp per output row (b, head[, query]); lane holds the D/32 consecutive
+// coordinates E*lane .. E*lane+E-1.  Merges the split partials (log-sum-exp
+// weights), divides by the total mass and rotates back (D H per V block)
+// with in-lane and shuffle butterflies.  Launched as a programmatic
+// dependent of the split kernel: the wait below holds until that grid has
+// finished and its partials are visible.
 template <int D>
-__global__ void __launch_bounds__(256) decode_combine_kernel(const CodecParams PV, const float* __restrict__ part,
-                                                             int n_split, uint16_t* __restrict__ out) {
-  __shared__ float s_o[D];
-  __shared__ float s_M, s_L;
-  const int row = blockIdx.x;  // b * Hq + h
+__global__ void __launch_bounds__(kCombWarps * 32) decode_combine_kernel(const CodecParams PV, const float* __restrict__ part,
+                                                             int n_split, uint16_t* __restrict__ out, int rows) {
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+  constexpr int E = D / 32;
+  const int row = blockIdx.x * kCombWarps + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (row >= rows) return;
   const float* p = part + (int64_t)row * n_split * (D + 4);
-  if (threadIdx.x == 0) {
-    float M = -INFINITY;
-    for (int s = 0; s < n_split; ++s) M = fmaxf(M, p[s * (D + 4)]);
-    float L = 0.f;
-    for (int s = 0; s < n_split; ++s) {
-      const float ms = p[s * (D + 4)];
-      if (ms != -INFINITY) L += exp2f(ms - M) * p[s * (D + 4) + 1];
+  // The values of the first kPre splits are loaded before anything else, so
+  // that every load of the row is in flight at once: one round trip to L2
+  // instead of a chain of them.  Lane s holds split s's (m, l).
+  constexpr int kPre = 64 / E;   // 32, 16, 8 splits for d = 64, 128, 256
+  float2 v[kPre][E / 2];
+#pragma unroll
+  for (int j = 0; j < kPre; ++j)
+#pragma unroll
+    for (int e = 0; e < E / 2; ++e)
+      v[j][e] = j < n_split ? *reinterpret_cast<const float2*>(p + j * (D + 4) + 2 + E * lane + 2 * e)
+                            : make_float2(0.f, 0.f);
+  const float m_l = lane < n_split ? p[lane * (D + 4)] : -INFINITY;
+  const float l_l = lane < n_split ? p[lane * (D + 4) + 1] : 0.f;
+  float M = m_l;
+  for (int s = lane + 32; s < n_split; s += 32) M = fmaxf(M, p[s * (D + 4)]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
+  // weight of split s: exp2(m_s - M), zero for an empty split
+  const float w_l = m_l == -INFINITY ? 0.f : exp2f(m_l - M);
+  float L = w_l * l_l;
+  float o[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) o[e] = 0.f;
+#pragma unroll
+  for (int j = 0; j < kPre; ++j) {
+    const float w = __shfl_sync(kFull, w_l, j);   // zero for j >= n_split
+#pragma unroll
+    for (int e = 0; e < E / 2; ++e) {
+      o[2 * e] = fmaf(w, v[j][e].x, o[2 * e]);
+      o[2 * e + 1] = fmaf(w, v[j][e].y, o[2 * e + 1]);
     }
-    s_M = M;
-    s_L = L;
   }
-  __syncthreads();
-  const float M = s_M, L = s_L;
-  for (int i = threadIdx.x; i < D; i += blockDim.x) {
-    float o = 0.f;
-    for (int s = 0; s < n_split; ++s) {
-      const float ms = p[s * (D + 4)];
-      if (ms != -INFINITY) o += exp2f(ms - M) * p[s * (D + 4) + 2 + i];
-    }
-    s_o[i] = L > 0.f ? o / L : 0.f;
-  }
-  // back to the input domain: o = D H O per V block
-  for (int h = 1; h < PV.blk; h <<= 1) {
-    __syncthreads();
-    for (int k = threadIdx.x; k < D / 2; k += blockDim.x) {
-      const int i = (k / h) * 2 * h + (k % h);
-      const float x = s_o[i], y = s_o[i + h];
-      s_o[i] = x + y;
-      s_o[i + h] = x - y;
+  for (int s = kPre; s < n_split; ++s) {   // only for more splits than kPre
+    const float* ps = p + s * (D + 4);
+    const float ms = ps[0];
+    const float w = ms == -INFINITY ? 0.f : exp2f(ms - M);
+    if (s >= 32) L = fmaf(lane == 0 ? w : 0.f, ps[1], L);
+#pragma unroll
+    for (int e = 0; e < E; e += 2) {
+      const float2 x = *reinterpret_cast<const float2*>(ps + 2 + E * lane + e);
+      o[e] = fmaf(w, x.x, o[e]);
+      o[e + 1] = fmaf(w, x.y, o[e + 1]);
     }
   }
-  __syncthreads();
-  for (int i = threadIdx.x; i < D; i += blockDim.x) {
-    const float v = flip(s_o[i] * PV.inv_sqrt_blk, (PV.sign_bits[i >> 5] >> (i & 31)) & 1u);
-    out[(int64_t)row * D + i] = f2h(v);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(kFull, L, off);
+  const float inv = L > 0.f ? PV.inv_sqrt_blk / L : 0.f;
+  // unnormalised Walsh-Hadamard per V block: strides below E inside the
+  // lane, the rest across lanes
+  for (int h = 1; h < E && h < PV.blk; h <<= 1) {
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      if ((e & h) == 0) {
+        const float x = o[e], y = o[e + h];
+        o[e] = x + y;
+        o[e + h] = x - y;
+      }
+    }
+  }
+  for (int h = E; h < PV.blk; h <<= 1) {
+    const int lo = h / E;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const float q = __shfl_xor_sync(kFull, o[e], lo);
+      o[e] = (lane & lo) ? (q - o[e]) : (o[e] + q);
+    }
+  }
+  uint32_t packed[E / 2];
+#pragma unroll
+  for (int e = 0; e < E; e += 2) {
+    const int i = E * lane + e;
+    const float v0 = flip(o[e] * inv, (PV.sign_bits[i >> 5] >> (i & 31)) & 1u);
+    const float v1 = flip(o[e + 1] * inv, (PV.sign_bits[(i + 1) >> 5] >> ((i + 1) & 31)) & 1u);
+    packed[e / 2] = (uint32_t)f2h(v0) | ((uint32_t)f2h(v1) << 16);
+  }
+  uint16_t* dst = out + (int64_t)row * D + E * lane;
+  if (E == 8) {
+    *reinterpret_cast<uint4*>(dst) = make_uint4(packed[0], packed[1 % (E / 2)], packed[2 % (E / 2)], packed[3 % (E / 2)]);
+  } else if (E == 4) {
+    *reinterpret_cast<uint2*>(dst) = make_uint2(packed[0], packed[1 % (E / 2)]);
+  } else {
+    *reinterpret_cast<uint32_t*>(dst) = packed[0];
   }
 }
 
@@ -327,12 +383,23 @@ int launch_decode_g(int G, const CodecParams& PK, const CodecParams& PV, const D
 }  // namespace
 
 int decode_combine(const CodecParams& PV, const float* part, int n_split, uint16_t* out, int rows, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((rows + kCombWarps - 1) / kCombWarps));
+  cfg.blockDim = dim3(kCombWarps * 32);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e;
   switch (PV.d) {
-    case 64: decode_combine_kernel<64><<<rows, 64, 0, s>>>(PV, part, n_split, out); break;
-    case 128: decode_combine_kernel<128><<<rows, 128, 0, s>>>(PV, part, n_split, out); break;
-    default: decode_combine_kernel<256><<<rows, 256, 0, s>>>(PV, part, n_split, out); break;
+    case 64: e = cudaLaunchKernelEx(&cfg, decode_combine_kernel<64>, PV, part, n_split, out, rows); break;
+    case 128: e = cudaLaunchKernelEx(&cfg, decode_combine_kernel<128>, PV, part, n_split, out, rows); break;
+    default: e = cudaLaunchKernelEx(&cfg, decode_combine_kernel<256>, PV, part, n_split, out, rows); break;
   }
-  return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+  return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }
 
 int sm_count() {

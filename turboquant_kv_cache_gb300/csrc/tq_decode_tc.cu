@@ -154,7 +154,6 @@ __global__ void __launch_bounds__(kT, 4) decode_tc_kernel(const CodecParams PK, 
   uint8_t* ring = smem;                                                 // [kStages][kStageBytes]
   uint16_t* sPh = reinterpret_cast<uint16_t*>(smem + kStages * kStageBytes);  // [kW][kG][kWarpTok] fp16 p
   uint16_t* sVT = sPh + kW * kG * kWarpTok;                             // [kW][4 blocks][kWarpTok] fp16
-  float* sq = reinterpret_cast<float*>(sVT + kW * 4 * kWarpTok);        // [kG][kD]
   __shared__ float s_ml[kW][2][kG];
 
   const int split = blockIdx.x;
@@ -200,41 +199,51 @@ __global__ void __launch_bounds__(kT, 4) decode_tc_kernel(const CodecParams PK, 
     cp_commit();
   }
 
-  // q^ = H (D q) per 32-block, times softmax_scale * log2 e (K's layout)
-  for (int e = tid; e < kG * kD; e += kT) {
-    const int h = e / kD, i = e % kD;
-    const float v = h2f(a.q[((int64_t)b * a.Hq + h0 + h) * kD + i]);
-    sq[e] = flip(v, (PK.sign_bits[i >> 5] >> (i & 31)) & 1u);
-  }
-  for (int hs = 1; hs < 32; hs <<= 1) {
-    __syncthreads();
-    for (int e = tid; e < kG * kD / 2; e += kT) {
-      const int r = e / (kD / 2), k = e % (kD / 2);
-      const int i = (k / hs) * 2 * hs + (k % hs);
-      float* row = sq + r * kD;
-      const float x = row[i], y = row[i + hs];
-      row[i] = x + y;
-      row[i + hs] = x - y;
-    }
-  }
-  __syncthreads();
-  const float qn = PK.inv_sqrt_blk * a.qscale;
   // B fragments of the K side.  Lane t of a quad owns 32-block t; K tile
   // (s, half) holds chunk s, codes 4*half..4*half+3 of every block; the
   // columns are (head, block) pairs, zero unless the block is the lane's.
+  // Each lane rotates its own two (head, block t) slices of q in registers:
+  // q^ = H (D q) per 32-block, times softmax_scale * log2 e (K's layout).
+  const float qn = PK.inv_sqrt_blk * a.qscale;
+  const bool on = (g & 3) == t;
   uint32_t bq[4][2][2][2];
 #pragma unroll
-  for (int s = 0; s < 4; ++s)
+  for (int nt = 0; nt < 2; ++nt) {
+    const int h = 2 * nt + (g >> 2);
+    const uint4* qp = reinterpret_cast<const uint4*>(a.q + ((int64_t)b * a.Hq + h0 + h) * kD + 32 * t);
+    const uint32_t sb = PK.sign_bits[t];
+    float v[32];
 #pragma unroll
-    for (int half = 0; half < 2; ++half)
+    for (int k = 0; k < 4; ++k) {
+      const uint4 u = qp[k];
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        const int h = 2 * nt + (g >> 2);
-        const float* qh = sq + h * kD + 32 * t + 8 * s + 4 * half;
-        const bool on = (g & 3) == t;
-        bq[s][half][nt][0] = on ? pack_h2(qh[0] * qn, qh[1] * qn) : 0u;
-        bq[s][half][nt][1] = on ? pack_h2(qh[2] * qn, qh[3] * qn) : 0u;
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = unpack_h2(w[e]);
+        v[8 * k + 2 * e] = flip(f.x, (sb >> (8 * k + 2 * e)) & 1u);
+        v[8 * k + 2 * e + 1] = flip(f.y, (sb >> (8 * k + 2 * e + 1)) & 1u);
       }
+    }
+#pragma unroll
+    for (int hs = 1; hs < 32; hs <<= 1) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        if ((i & hs) == 0) {
+          const float x = v[i], y = v[i + hs];
+          v[i] = x + y;
+          v[i + hs] = x - y;
+        }
+      }
+    }
+#pragma unroll
+    for (int s2 = 0; s2 < 4; ++s2)
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const float* qh = v + 8 * s2 + 4 * half;
+        bq[s2][half][nt][0] = on ? pack_h2(qh[0] * qn, qh[1] * qn) : 0u;
+        bq[s2][half][nt][1] = on ? pack_h2(qh[2] * qn, qh[3] * qn) : 0u;
+      }
+  }
   // fp16 centroid tables: low / high bytes of codes 0-3 and 4-7
   uint32_t ktl0, ktl1, kth0, kth1, vtl0, vtl1, vth0, vth1;
   {
@@ -417,6 +426,8 @@ __global__ void __launch_bounds__(kT, 4) decode_tc_kernel(const CodecParams PK, 
     }
     __syncwarp();
   }
+  // the combine kernel may be scheduled now; it waits for this grid to finish
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   // full sums per head: the 8 lanes g of a (t) column hold partial sums
   float l_run[2];
 #pragma unroll
@@ -479,7 +490,7 @@ __global__ void __launch_bounds__(kT, 4) decode_tc_kernel(const CodecParams PK, 
 }
 
 constexpr size_t kSmem = (size_t)kStages * kStageBytes + (size_t)kW * kG * kWarpTok * 2 +
-                         (size_t)kW * 4 * kWarpTok * 2 + (size_t)kG * kD * 4;
+                         (size_t)kW * 4 * kWarpTok * 2;
 static_assert((size_t)kStages * kStageBytes >= (size_t)kW * kG * kD * 4, "ring too small for the merge");
 
 }  // namespace

@@ -477,6 +477,8 @@ __global__ void __launch_bounds__(kThrTc, 1) prefill_tc_kernel(const CodecParams
   }
   if (n_tiles > 0 && ok) ok = bar_wait(su32(&bar_o), (n_tiles - 1) & 1);
   ok = __syncthreads_and(ok) != 0;
+  // the combine kernel may be scheduled now; it waits for this grid to finish
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   fence_after();
   asm volatile("cp.async.wait_group 0;\n" ::);
   // ---- partial (m, l, O) of this row for this context slice

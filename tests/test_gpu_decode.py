@@ -117,3 +117,37 @@ def test_decode_workspace_errors(tqlib):
     with pytest.raises(tb.TQError) as e:
         tb.tq_decode_attn(K, K, q, ctx=65)
     assert e.value.status == -1
+
+
+TC_LAYOUT_CASES = [
+    # name, K (block, bits, m, nc, seed), V, B, Hq, Hkv, S_cap, ctx, kv_len, n_split, d, heavy_k
+    ("d256_turbo4k_turbo3v", (32, 4, 0, 0, 1), (32, 3, 0, 0, 1), 1, 8, 2, 3000, 2999, None, 0, 256, True),
+    ("d256_turbo3_ragged", (32, 3, 0, 0, 1), (32, 3, 0, 0, 2), 2, 8, 2, 1030, 1029, [1029, 77], 4, 256, False),
+    ("d256_bits2k", (32, 2, 0, 0, 3), (32, 3, 0, 0, 1), 1, 4, 1, 600, 600, None, 2, 256, False),
+    ("d128_turbo4k", (32, 4, 0, 0, 1), (32, 3, 0, 0, 1), 1, 8, 2, 1500, 1499, None, 0, 128, True),
+    ("d128_bits2k_block32", (32, 2, 0, 0, 4), (32, 3, 0, 0, 1), 2, 8, 2, 900, 899, [899, 450], 3, 128, False),
+    ("d128_turbo3k_pervec_v", (32, 3, 0, 0, 1), (128, 3, 0, 0, 2), 1, 8, 2, 1000, 1000, None, 0, 128, False),
+    ("d128_pervec_2bit_k", (128, 2, 0, 0, 1), (128, 3, 0, 0, 1), 2, 8, 2, 1000, 999, [999, 1], 0, 128, True),
+    ("d128_pervec_2bit_k_v32", (128, 2, 0, 0, 2), (32, 3, 0, 0, 1), 1, 4, 1, 800, 777, None, 4, 128, False),
+]
+
+
+@pytest.mark.parametrize("name,cK,cV,B,Hq,Hkv,S_cap,ctx,kv_len,n_split,d,heavy", TC_LAYOUT_CASES)
+def test_decode_tensor_core_layouts(tqlib, name, cK, cV, B, Hq, Hkv, S_cap, ctx, kv_len, n_split, d, heavy):
+    """Every layout combination of the tensor-core decode kernel (GQA 4),
+    several tiles, partial last steps, ragged lengths and split counts."""
+    from turboquant_kv_cache_gb300 import binding as tb
+    got, ref, _ = _run(tb, cK, cV, B, Hq, Hkv, S_cap, ctx, d, kv_len=kv_len, n_split=n_split, seed=11,
+                       heavy_k=heavy)
+    err = np.abs(got - ref).max()
+    assert err < ATTN_ATOL, (name, err)
+
+
+def test_decode_qjl_keys_long_ragged(tqlib):
+    """QJL keys (2-bit + m=128 signs) with 3-bit per-vector values over many
+    tiles, ragged lengths and splits: the tensor-core QJL path."""
+    from turboquant_kv_cache_gb300 import binding as tb
+    S = inputs.qjl_matrix(128, 128, 7)
+    got, ref, _ = _run(tb, (128, 2, 128, 0, 1), (128, 3, 0, 0, 1), 2, 8, 2, 2000, 1999, 128,
+                       kv_len=[1999, 333], n_split=5, S=S)
+    assert np.abs(got - ref).max() < ATTN_ATOL

@@ -18,12 +18,12 @@
 namespace tq {
 
 int decode_auto_splits(int B, int Hkv, int64_t ctx);
-bool decode_tc_eligible(const CodecParams& PK, const CodecParams& PV, int G, int64_t S_cap, const void* ks,
-                        const void* vs);
-int launch_decode_tc(const CodecParams& PK, const CodecParams& PV, const uint8_t* kc, const uint16_t* ks,
-                     const uint8_t* vc, const uint16_t* vs, const uint16_t* q, const int32_t* kv_len, float* part,
-                     int B, int Hq, int Hkv, int64_t S_cap, int64_t ctx, int n_split, float qscale,
-                     uint16_t* out, cudaStream_t st);
+bool decode_tc_eligible(const CodecParams& PK, const CodecParams& PV, int G, int64_t S_cap, const tq_kv_view* K,
+                        const tq_kv_view* V);
+size_t decode_tc_extra_bytes(int B, int Hq);
+int launch_decode_tc(const CodecParams& PK, const CodecParams& PV, const tq_kv_view* K, const tq_kv_view* V,
+                     const uint16_t* q, const int32_t* kv_len, float* part, size_t part_bytes, int B, int Hq, int Hkv,
+                     int64_t S_cap, int64_t ctx, int n_split, float qscale, uint16_t* out, cudaStream_t st);
 size_t decode_ws_bytes(int B, int Hq, int d, int n_split);
 
 namespace {
@@ -419,8 +419,14 @@ int decode_auto_splits(int B, int Hkv, int64_t ctx) {
   return want;
 }
 
-size_t decode_ws_bytes(int B, int Hq, int d, int n_split) {
+// Split partials [B*Hq][n_split][d + 4] fp32, then (256-byte aligned) the
+// tensor-core path's per-call extras (S q rows of QJL keys).
+size_t decode_part_bytes(int B, int Hq, int d, int n_split) {
   return (size_t)B * Hq * n_split * (d + 4) * sizeof(float);
+}
+
+size_t decode_ws_bytes(int B, int Hq, int d, int n_split) {
+  return (decode_part_bytes(B, Hq, d, n_split) + 255) / 256 * 256 + decode_tc_extra_bytes(B, Hq);
 }
 
 }  // namespace tq
@@ -462,9 +468,9 @@ extern "C" int tq_decode_attn(const tq_kv_view* K, const tq_kv_view* V, const ui
                    static_cast<float*>(workspace), S_cap, ctx, Hq, Hkv, ns, sm * tq::kLog2e};
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int G = Hq / Hkv;
-  if (tq::decode_tc_eligible(PK, PV, G, S_cap, K->scales, V->scales))
-    return tq::launch_decode_tc(PK, PV, K->codes, K->scales, V->codes, V->scales, q, kv_len, a.part, B, Hq, Hkv,
-                                S_cap, ctx, ns, a.qscale, out, s);
+  if (tq::decode_tc_eligible(PK, PV, G, S_cap, K, V))
+    return tq::launch_decode_tc(PK, PV, K, V, q, kv_len, a.part, tq::decode_part_bytes(B, Hq, PK.d, ns), B, Hq,
+                                Hkv, S_cap, ctx, ns, a.qscale, out, s);
   switch (PK.d) {
     case 64: st = tq::launch_decode_g<64>(G, PK, PV, a, B, s); break;
     case 128: st = tq::launch_decode_g<128>(G, PK, PV, a, B, s); break;

@@ -1,27 +1,33 @@
-// Tensor-core decode attention for the turbo3 cache (3-bit codes, one fp16
-// norm per 32 values) at head_dim 128 with GQA groups of 4.
+// Tensor-core decode attention over the packed cache, GQA groups of 4.
 //
-// Same mathematics as the CUDA-core split kernel (scores <H D q, c> scaled
-// by the block norms, online softmax in base 2, V accumulated in the rotated
-// domain, partials merged and rotated back by the combine kernel), mapped
-// onto m16n8k16 fp16 MMAs with fp32 accumulation:
+// Same mathematics as the CUDA-core split kernel (scores <H D q, c> times the
+// block norms, plus the QJL term for QJL keys; online softmax in base 2; V
+// accumulated in the rotated domain; partials merged and rotated back by the
+// combine kernel), mapped onto m16n8k16 fp16 MMAs with fp32 accumulation.
 //
-//  * Staging: a CTA owns (batch, KV head, context slice).  64-token tiles of
-//    K codes / K scales / V codes / V scales stream into a 4-stage shared
-//    memory ring with 16-byte cp.async (zero-filled past the slice).  Each of
-//    the 4 warps takes 16 tokens of a tile.
+//  * Work split: a CTA owns (batch, KV head, context slice).  A pipeline of
+//    one warp (head_dim 128) or two warps (head_dim 256, each taking 128
+//    dimensions and exchanging partial scores through shared memory) walks
+//    32-token steps of the slice; the CTA's pipelines interleave the steps.
+//  * Staging: each pipeline streams its own steps (K codes, K norms, QJL
+//    bits and rho, V codes, V norms) into a 3-slot ring with 16-byte
+//    cp.async, two steps ahead of the one being computed.  Past the end of
+//    the slice the copies zero-fill.
 //  * Code -> fp16: an 8-code chunk of the packed layout is a nibble word;
-//    byte permutes against two 8-byte tables (low and high bytes of the fp16
-//    centroids) give the fp16 values, four codes per two permutes.
-//  * K side: lane t of a quad decodes, at step s, chunk s of group (t+s)&3,
-//    so every lane runs the same instructions (chunk 3 needs the bit-3
-//    gather).  The MMA columns are (head, block) pairs and q^ is masked to
-//    each block's coordinates, so one accumulator collects all K tiles; the
-//    epilogue weights the 4 block columns by the tokens' block norms.
-//  * V side: chunks decode the same way into row fragments, movmatrix
-//    transposes them into B fragments (tokens along k), and the A operand
-//    holds P' = p * scaleV with rows (head, block); the accumulator entry
-//    whose row block matches its column's block is the output.
+//    byte permutes against the low-byte and high-byte tables of the fp16
+//    centroids give four codes per two permutes (16-entry tables for 4-bit
+//    codes pick between two 8-entry halves by bit 3).  With one norm per 32
+//    values the tables of a (token, block) are the centroids times that
+//    norm (built once per block); 4-bit codes multiply by the norm after the
+//    lookup instead; per-vector norms multiply the score (K) or p (V).
+//  * K side: lane t of a quad decodes 32-block t of tokens g and g+8 of a
+//    16-token MMA tile; the B operand is q^ of head (g & 3), so every lane
+//    ends with the scores of its own two heads.  QJL sign bits enter as a
+//    second accumulator whose A operand is 2*s (0 or 2.0, built from the bit
+//    word by a shift and a mask) against S q.
+//  * V side: the same decode into row fragments, movmatrix transposes them
+//    into A fragments with tokens along k, B holds p (fp16) of the head
+//    columns; the accumulator columns of a lane are the heads of its scores.
 //  * Softmax: the running max only moves when a score exceeds it by more
 //    than 2^8 (lazy rescaling); partial (m, l, acc) per CTA go to the
 //    workspace in the split-kernel format.
@@ -36,50 +42,65 @@ int decode_combine(const CodecParams& PV, const float* part, int n_split, uint16
 
 namespace {
 
-constexpr int kW = 4;                 // warps per CTA
-constexpr int kT = kW * 32;           // threads per CTA
-constexpr int kWarpTok = 32;          // tokens per warp per step (two 16-token MMA tiles)
-constexpr int kTileTok = kWarpTok * kW;   // tokens per stage
-constexpr int kStages = 3;
-constexpr int kD = 128;
-constexpr int kG = 4;                 // q heads per KV head
-constexpr int kRecC = 48;             // code bytes per token (128 coords x 3 bits)
-constexpr int kRecS = 8;              // scale bytes per token (4 blocks x fp16)
-constexpr int kOffKc = 0;
-constexpr int kOffKs = kOffKc + kTileTok * kRecC;
-constexpr int kOffVc = kOffKs + kTileTok * kRecS;
-constexpr int kOffVs = kOffVc + kTileTok * kRecC;
-constexpr int kStageBytes = kOffVs + kTileTok * kRecS;   // 14336
-constexpr float kLazy = 8.0f;         // rescale threshold, log2 units
+constexpr int kG = 4;          // q heads per KV head
+constexpr int kTok = 32;       // tokens per step
+constexpr int kThreads = 128;  // 4 warps
+constexpr int kSlots = 3;
+constexpr int kQjlM = 128;     // QJL rows supported here
+constexpr float kLazy = 8.0f;  // rescale threshold, log2 units
+
+template <int D, int KB, int VB, bool KPV, bool VPV, bool QJL>
+struct Cfg {
+  static constexpr int NH = D / 128;  // warps per pipeline
+  static constexpr int P = 4 / NH;    // pipelines per CTA
+  static constexpr int KREC = D * KB / 8;
+  static constexpr int KSB = KPV ? 2 : D / 16;
+  static constexpr int QB = QJL ? kQjlM / 8 : 0;
+  static constexpr int QR = QJL ? 2 : 0;
+  static constexpr int VREC = D * VB / 8;
+  static constexpr int VSB = VPV ? 2 : D / 16;
+  static constexpr int OKC = 0;
+  static constexpr int OKS = OKC + kTok * KREC;
+  static constexpr int OQB = OKS + kTok * KSB;
+  static constexpr int OQR = OQB + kTok * QB;
+  static constexpr int OVC = OQR + kTok * QR;
+  static constexpr int OVS = OVC + kTok * VREC;
+  static constexpr int STAGE = OVS + kTok * VSB;
+  static constexpr size_t SMEM = (size_t)P * kSlots * STAGE      // rings
+                                 + (size_t)4 * kG * kTok * 2       // p per warp
+                                 + (NH > 1 ? (size_t)4 * 32 * 8 * 4 : 0);  // partial-score exchange
+  static_assert(STAGE % 16 == 0, "stage sub-arrays stay 16-byte aligned");
+  static_assert((size_t)P * kSlots * STAGE >= (size_t)P * kG * D * 4, "ring too small for the merge");
+};
 
 struct TcArgs {
   const uint8_t* kc;
   const uint8_t* ks;
+  const uint8_t* kq;   // QJL bits
+  const uint8_t* kr;   // QJL rho
   const uint8_t* vc;
   const uint8_t* vs;
   const uint16_t* q;
+  const uint16_t* sq;  // S q * scale, fp16 [B*Hq][128] (QJL)
+  const float* sqsum;  // per-head sum of sq (QJL)
   const int32_t* kv_len;
   float* part;
   int64_t S_cap;
   int64_t ctx;
-  int64_t per;          // tokens per split (multiple of kTileTok)
+  int64_t per;  // tokens per split (multiple of 128)
   int Hq, Hkv, n_split;
   float qscale;
 };
 
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void cp_async16(void* dst, const void* src, int bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(smem_u32(dst)), "l"(src), "r"(bytes));
+__device__ __forceinline__ uint32_t su32(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
+__device__ __forceinline__ void cp16(uint32_t dst, const void* src, int bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(bytes));
 }
 __device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;\n" ::); }
 template <int N>
 __device__ __forceinline__ void cp_wait() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
 }
-
 __device__ __forceinline__ void mma16816(float* c, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
                                          uint32_t b1) {
   asm volatile(
@@ -88,130 +109,244 @@ __device__ __forceinline__ void mma16816(float* c, uint32_t a0, uint32_t a1, uin
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
-
 __device__ __forceinline__ uint32_t movtrans(uint32_t x) {
   uint32_t y;
   asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(y) : "r"(x));
   return y;
 }
-
 __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
-  const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b));
-  return *reinterpret_cast<const uint32_t*>(&r);
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
 }
-
-__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
-  const __half2 h = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&h);
-}
-
-__device__ __forceinline__ float2 unpack_h2(uint32_t v) {
-  return __half22float2(*reinterpret_cast<const __half2*>(&v));
-}
-
-// Nibble words of the four 8-code chunks of one 3-bit group (words w0..w2).
-// Chunk 3's bits ride in bit 3 of every nibble; the shifts of the gather are
-// done as high-half multiplies so they leave the integer logic pipe.
-__device__ __forceinline__ void chunks3(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t* n) {
-  n[0] = w0 & 0x77777777u;
-  n[1] = w1 & 0x77777777u;
-  n[2] = w2 & 0x77777777u;
-  n[3] = __umulhi(w0 & 0x88888888u, 1u << 29) + __umulhi(w1 & 0x88888888u, 1u << 30) +
-         __umulhi(w2 & 0x88888888u, 1u << 31);
-}
-
-// Byte permute with the selector taken as is: every selector here has bit 3
-// of each nibble clear, so no masking is needed (the C intrinsic masks).
+// Byte permute with the selector taken as is (the C intrinsic masks it).
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t d;
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
   return d;
 }
-
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
-
-// Four fp16x2 registers (codes 0-1, 2-3, 4-5, 6-7) of a nibble word: byte
-// permutes against the low-byte and high-byte tables of the fp16 centroids.
-__device__ __forceinline__ void lut8(uint32_t n, uint32_t tl0, uint32_t tl1, uint32_t th0, uint32_t th1,
-                                     uint32_t* o) {
-  uint32_t lo = prmt(tl0, tl1, n);
-  uint32_t hi = prmt(th0, th1, n);
-  o[0] = prmt(lo, hi, 0x5140);
-  o[1] = prmt(lo, hi, 0x7362);
-  const uint32_t n2 = __umulhi(n, 1u << 16);
-  lo = prmt(tl0, tl1, n2);
-  hi = prmt(th0, th1, n2);
-  o[2] = prmt(lo, hi, 0x5140);
-  o[3] = prmt(lo, hi, 0x7362);
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds16(uint32_t a) {
+  unsigned short v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t a) {
+  uint2 v;
+  asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ void sts16(uint32_t a, uint32_t v) {
+  asm volatile("st.shared.u16 [%0], %1;" ::"r"(a), "h"((unsigned short)v));
+}
+__device__ __forceinline__ void sts128f(uint32_t a, float x, float y, float z, float w) {
+  asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(a), "f"(x), "f"(y), "f"(z), "f"(w));
+}
+__device__ __forceinline__ float4 lds128f(uint32_t a) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ void pair_sync(int id) {
+  asm volatile("bar.sync %0, 64;" ::"r"(id) : "memory");
+}
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+__device__ __forceinline__ float2 unpack_h2(uint32_t v) {
+  return __half22float2(*reinterpret_cast<const __half2*>(&v));
 }
 
-__global__ void __launch_bounds__(kT, 4) decode_tc_kernel(const CodecParams PK, const CodecParams PV, const TcArgs a) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  uint8_t* ring = smem;                                                 // [kStages][kStageBytes]
-  uint16_t* sPh = reinterpret_cast<uint16_t*>(smem + kStages * kStageBytes);  // [kW][kG][kWarpTok] fp16 p
-  uint16_t* sVT = sPh + kW * kG * kWarpTok;                             // [kW][4 blocks][kWarpTok] fp16
-  __shared__ float s_ml[kW][2][kG];
+// Nibble words (code k of chunk c in bits 4k..4k+2) of one 32-code group,
+// from its packed words w (see the layout in include/tq.h).
+template <int BITS>
+__device__ __forceinline__ void chunk_words(const uint32_t* w, uint32_t* n) {
+  if (BITS == 4) {
+    n[0] = w[0]; n[1] = w[1]; n[2] = w[2]; n[3] = w[3];
+  } else if (BITS == 3) {
+    n[0] = w[0] & 0x77777777u;
+    n[1] = w[1] & 0x77777777u;
+    n[2] = w[2] & 0x77777777u;
+    // chunk 3 rides in bit 3 of every nibble; the shifts run as high-half
+    // multiplies, off the integer logic pipe
+    n[3] = __umulhi(w[0] & 0x88888888u, 1u << 29) + __umulhi(w[1] & 0x88888888u, 1u << 30) +
+           __umulhi(w[2] & 0x88888888u, 1u << 31);
+  } else {
+    n[0] = w[0] & 0x33333333u;
+    n[1] = w[1] & 0x33333333u;
+    n[2] = __umulhi(w[0], 1u << 30) & 0x33333333u;
+    n[3] = __umulhi(w[1], 1u << 30) & 0x33333333u;
+  }
+}
 
-  const int split = blockIdx.x;
-  const int bh = blockIdx.y;
-  const int b = bh / a.Hkv, kvh = bh % a.Hkv;
-  const int h0 = kvh * kG;
-  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+template <int BITS>
+__device__ __forceinline__ void load_group(uint32_t a, uint32_t* w) {
+  if (BITS == 4) {
+    const uint4 v = lds128(a);
+    w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+  } else if (BITS == 3) {
+    w[0] = lds32(a); w[1] = lds32(a + 4); w[2] = lds32(a + 8);
+  } else {
+    const uint2 v = lds64(a);
+    w[0] = v.x; w[1] = v.y;
+  }
+}
+
+// Lookup tables of one codebook (optionally scaled): low and high bytes of
+// the fp16 values, entries 0-7 in t[0..3], entries 8-15 in t[4..7].
+struct Tab {
+  uint32_t t[8];
+};
+
+// fp16 centroid pairs (c0,c1), (c2,c3), ... of a codebook (up to 16 entries)
+template <int BITS>
+struct Cent {
+  uint32_t c2[(1 << BITS) / 2];
+};
+
+template <int BITS>
+__device__ __forceinline__ Cent<BITS> make_cent(const CodecParams& P) {
+  Cent<BITS> c;
+#pragma unroll
+  for (int k = 0; k < (1 << BITS) / 2; ++k)
+    c.c2[k] = (uint32_t)f2h(P.centroids[2 * k]) | ((uint32_t)f2h(P.centroids[2 * k + 1]) << 16);
+  return c;
+}
+
+// tables of the centroids times the fp16 norm s (s = 1.0 for unscaled)
+template <int BITS>
+__device__ __forceinline__ Tab make_tab(const Cent<BITS>& c, uint32_t s) {
+  const uint32_t s2 = s | (s << 16);
+  Tab T;
+  uint32_t h[8];
+#pragma unroll
+  for (int k = 0; k < (1 << BITS) / 2; ++k) h[k] = hmul2(c.c2[k], s2);
+  if (BITS == 2) {
+    T.t[0] = prmt(h[0], h[1], 0x6420);
+    T.t[2] = prmt(h[0], h[1], 0x7531);
+    T.t[1] = T.t[0];
+    T.t[3] = T.t[2];
+  } else {
+    T.t[0] = prmt(h[0], h[1], 0x6420);
+    T.t[1] = prmt(h[2], h[3], 0x6420);
+    T.t[2] = prmt(h[0], h[1], 0x7531);
+    T.t[3] = prmt(h[2], h[3], 0x7531);
+    if (BITS == 4) {
+      T.t[4] = prmt(h[4], h[5], 0x6420);
+      T.t[5] = prmt(h[6], h[7], 0x6420);
+      T.t[6] = prmt(h[4], h[5], 0x7531);
+      T.t[7] = prmt(h[6], h[7], 0x7531);
+    }
+  }
+  return T;
+}
+
+// Four fp16x2 registers (codes 0-1, 2-3, 4-5, 6-7) of a nibble word.
+template <int BITS>
+__device__ __forceinline__ void lut8(uint32_t n, const Tab& T, uint32_t* o) {
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    const uint32_t s = half ? __umulhi(n, 1u << 16) : n;
+    uint32_t lo, hi;
+    if (BITS == 4) {
+      const uint32_t s7 = s & 0x7777u;
+      const uint32_t lo0 = prmt(T.t[0], T.t[1], s7), hi0 = prmt(T.t[2], T.t[3], s7);
+      const uint32_t lo1 = prmt(T.t[4], T.t[5], s7), hi1 = prmt(T.t[6], T.t[7], s7);
+      // byte mask 0xff where bit 3 of the nibble is set: bit 3 moved to the
+      // byte-select bit 2 picks 0x00 / 0xff from the constant pair
+      const uint32_t m = prmt(0u, 0xffffffffu, __umulhi(s, 1u << 31));
+      lo = (lo0 & ~m) | (lo1 & m);
+      hi = (hi0 & ~m) | (hi1 & m);
+    } else {
+      lo = prmt(T.t[0], T.t[1], s);
+      hi = prmt(T.t[2], T.t[3], s);
+    }
+    o[2 * half] = prmt(lo, hi, 0x5140);
+    o[2 * half + 1] = prmt(lo, hi, 0x7362);
+  }
+}
+
+template <int D, int KB, int VB, bool KPV, bool VPV, bool QJL>
+__global__ void __launch_bounds__(kThreads, 4) decode_tc_kernel(const CodecParams PK, const CodecParams PV,
+                                                               const TcArgs a) {
+  using C = Cfg<D, KB, VB, KPV, VPV, QJL>;
+  constexpr int NH = C::NH, P = C::P;
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ float s_ml[4][2][kG];
+
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, tid = threadIdx.x;
   const int g = lane >> 2, t = lane & 3;
+  const int pi = wid / NH, hw = wid % NH;  // pipeline, dimension half
+  const int split = blockIdx.x, bh = blockIdx.y;
+  const int b = bh / a.Hkv, kvh = bh % a.Hkv, h0 = kvh * kG;
 
   int64_t len = a.ctx;
   if (a.kv_len) len = imin64(len, (int64_t)a.kv_len[b]);
   const int64_t t_begin = (int64_t)split * a.per;
   const int64_t t_end = imin64(t_begin + a.per, len);
-  const int n_tiles = t_end > t_begin ? (int)((t_end - t_begin + kTileTok - 1) / kTileTok) : 0;
+  const int n_sub = t_end > t_begin ? (int)((t_end - t_begin + kTok - 1) / kTok) : 0;
+  const int n_it = n_sub > pi ? (n_sub - pi + P - 1) / P : 0;
   const int64_t rec0 = (int64_t)bh * a.S_cap;
+  const uint32_t ring = su32(smem) + pi * kSlots * C::STAGE;
+  const int plane = hw * 32 + lane;  // lane within the pipeline
 
-  auto load_stage = [&](int slot, int tile) {
-    uint8_t* dst = ring + slot * kStageBytes;
-    const int64_t t0 = t_begin + (int64_t)tile * kTileTok;
-    const int nv = (int)imin64(kTileTok, t_end - t0);
-    // codes: 3 chunks of 16 B per token
-    for (int c = tid; c < kTileTok * 3; c += kT) {
-      const bool ok = c / 3 < nv;
-      const int64_t off = ok ? (rec0 + t0) * kRecC + (int64_t)c * 16 : 0;
-      cp_async16(dst + kOffKc + c * 16, a.kc + off, ok ? 16 : 0);
-      cp_async16(dst + kOffVc + c * 16, a.vc + off, ok ? 16 : 0);
-    }
-    // scales: one 16 B chunk per two tokens
-    if (tid < kTileTok / 2) {
-      const int c = tid;
-      const int bytes = (int)imin64(16, (int64_t)(nv - 2 * c) * kRecS);
-      const bool ok = bytes > 0;
-      const int64_t off = ok ? (rec0 + t0) * kRecS + (int64_t)c * 16 : 0;
-      cp_async16(dst + kOffKs + c * 16, a.ks + off, ok ? bytes : 0);
-      cp_async16(dst + kOffVs + c * 16, a.vs + off, ok ? bytes : 0);
+  // ---- staging: every 16-byte chunk of every stream of a step, spread over
+  // the pipeline's lanes; zero-filled past the end of the slice
+  auto stream = [&](uint32_t dst, const uint8_t* base, int per_tok, int64_t tok0, int nv) {
+    const int chunks = kTok * per_tok / 16;
+    const uint8_t* src = base + tok0 * per_tok;
+    const int valid = nv * per_tok;
+    for (int c = plane; c < chunks; c += 32 * NH) {
+      int bytes = valid - 16 * c;
+      bytes = bytes < 0 ? 0 : (bytes > 16 ? 16 : bytes);
+      cp16(dst + 16 * c, bytes ? src + 16 * c : base, bytes);
     }
   };
-
-  // prologue: start the first stages while the query is rotated
+  int ld_it = 0;
+  auto load_next = [&](int slot) {
+    const int64_t t0 = t_begin + (int64_t)kTok * (pi + P * ld_it);
+    const int nv = (int)imin64(kTok, t_end - t0);
+    const int64_t tok0 = rec0 + t0;
+    const uint32_t dst = ring + slot * C::STAGE;
+    stream(dst + C::OKC, a.kc, C::KREC, tok0, nv);
+    stream(dst + C::OKS, a.ks, C::KSB, tok0, nv);
+    if (QJL) {
+      stream(dst + C::OQB, a.kq, C::QB, tok0, nv);
+      stream(dst + C::OQR, a.kr, C::QR, tok0, nv);
+    }
+    stream(dst + C::OVC, a.vc, C::VREC, tok0, nv);
+    stream(dst + C::OVS, a.vs, C::VSB, tok0, nv);
+    ++ld_it;
+  };
 #pragma unroll
-  for (int st = 0; st < kStages - 1; ++st) {
-    if (st < n_tiles) load_stage(st, st);
+  for (int s = 0; s < kSlots - 1; ++s) {
+    if (s < n_it) load_next(s);
     cp_commit();
   }
 
-  // B fragments of the K side.  Lane t of a quad owns 32-block t; K tile
-  // (s, half) holds chunk s, codes 4*half..4*half+3 of every block; the
-  // columns are (head, block) pairs, zero unless the block is the lane's.
-  // Each lane rotates its own two (head, block t) slices of q in registers:
-  // q^ = H (D q) per 32-block, times softmax_scale * log2 e (K's layout).
-  const float qn = PK.inv_sqrt_blk * a.qscale;
-  const bool on = (g & 3) == t;
-  uint32_t bq[4][2][2][2];
-#pragma unroll
-  for (int nt = 0; nt < 2; ++nt) {
-    const int h = 2 * nt + (g >> 2);
-    const uint4* qp = reinterpret_cast<const uint4*>(a.q + ((int64_t)b * a.Hq + h0 + h) * kD + 32 * t);
-    const uint32_t sb = PK.sign_bits[t];
+  // ---- q^ = H (D q) of head (g & 3) over this lane's 32-block, times
+  // softmax_scale * log2 e (K's layout), as B fragments
+  uint32_t bq[4][2][2];
+  {
+    const float qn = PK.inv_sqrt_blk * a.qscale;
+    const int blk = 4 * hw + t;  // the lane's 32-value group
+    const uint4* qp = reinterpret_cast<const uint4*>(a.q + ((int64_t)b * a.Hq + h0 + (g & 3)) * D + 32 * blk);
+    const uint32_t sb = PK.sign_bits[blk];
     float v[32];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -224,310 +359,470 @@ __global__ void __launch_bounds__(kT, 4) decode_tc_kernel(const CodecParams PK, 
         v[8 * k + 2 * e + 1] = flip(f.y, (sb >> (8 * k + 2 * e + 1)) & 1u);
       }
     }
+    // Walsh-Hadamard over the block (when the K block is the whole vector,
+    // the cross-block stages follow below through shuffles)
 #pragma unroll
-    for (int hs = 1; hs < 32; hs <<= 1) {
+    for (int hs = 1; hs < 32; hs <<= 1)
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
+      for (int i = 0; i < 32; ++i)
         if ((i & hs) == 0) {
           const float x = v[i], y = v[i + hs];
           v[i] = x + y;
           v[i + hs] = x - y;
         }
-      }
+    if (KPV) {
+      // blocks of 128 (head_dim 128): butterflies across the quad's lanes
+#pragma unroll
+      for (int o = 1; o < 4; o <<= 1)
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float p = __shfl_xor_sync(kFull, v[i], o);
+          v[i] = (t & o) ? (p - v[i]) : (v[i] + p);
+        }
     }
 #pragma unroll
     for (int s2 = 0; s2 < 4; ++s2)
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         const float* qh = v + 8 * s2 + 4 * half;
-        bq[s2][half][nt][0] = on ? pack_h2(qh[0] * qn, qh[1] * qn) : 0u;
-        bq[s2][half][nt][1] = on ? pack_h2(qh[2] * qn, qh[3] * qn) : 0u;
+        bq[s2][half][0] = pack_h2(qh[0] * qn, qh[1] * qn);
+        bq[s2][half][1] = pack_h2(qh[2] * qn, qh[3] * qn);
       }
   }
-  // fp16 centroid tables: low / high bytes of codes 0-3 and 4-7
-  uint32_t ktl0, ktl1, kth0, kth1, vtl0, vtl1, vth0, vth1;
-  {
-    uint32_t lo[2] = {0, 0}, hi[2] = {0, 0}, vlo[2] = {0, 0}, vhi[2] = {0, 0};
+  // QJL: B fragments of S q for rows (32t + p, 32t + p + 16), and the sums
+  uint32_t bj[QJL ? 8 : 1][2];
+  float sqs[2] = {0.f, 0.f};
+  if (QJL) {
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
+    const uint16_t* sq = a.sq + ((int64_t)b * a.Hq + h0 + (g & 3)) * kQjlM + 32 * t;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const uint32_t hk = f2h(PK.centroids[k]), hv = f2h(PV.centroids[k]);
-      lo[k >> 2] |= (hk & 0xffu) << (8 * (k & 3));
-      hi[k >> 2] |= (hk >> 8) << (8 * (k & 3));
-      vlo[k >> 2] |= (hv & 0xffu) << (8 * (k & 3));
-      vhi[k >> 2] |= (hv >> 8) << (8 * (k & 3));
+    for (int j = 0; j < 8; ++j) {
+      bj[j][0] = (uint32_t)sq[2 * j] | ((uint32_t)sq[2 * j + 16] << 16);
+      bj[j][1] = (uint32_t)sq[2 * j + 1] | ((uint32_t)sq[2 * j + 17] << 16);
     }
-    ktl0 = lo[0]; ktl1 = lo[1]; kth0 = hi[0]; kth1 = hi[1];
-    vtl0 = vlo[0]; vtl1 = vlo[1]; vth0 = vhi[0]; vth1 = vhi[1];
+    sqs[0] = a.sqsum[(int64_t)b * a.Hq + h0 + ((2 * t) & 3)];
+    sqs[1] = a.sqsum[(int64_t)b * a.Hq + h0 + ((2 * t + 1) & 3)];
   }
 
-  // V accumulator: M tile (s, pr) = coords of chunk s, codes {2pr, 2pr+1}
-  // (rows 0-7) and {2pr+4, 2pr+5} (rows 8-15) of block g/2; columns = heads.
+  const Cent<KB> kcent = make_cent<KB>(PK);
+  const Cent<VB> vcent = make_cent<VB>(PV);
+  const uint32_t one_h = 0x3C00u;
+  // tables that do not depend on the token
+  Tab kfix, vfix;
+  if (KPV || KB == 4) kfix = make_tab<KB>(kcent, one_h);
+  if (VPV) vfix = make_tab<VB>(vcent, one_h);
+
   float acc[4][2][4];
 #pragma unroll
   for (int s = 0; s < 4; ++s)
 #pragma unroll
     for (int pr = 0; pr < 2; ++pr) acc[s][pr][0] = acc[s][pr][1] = acc[s][pr][2] = acc[s][pr][3] = 0.f;
-  // running max per lane head (2*nt + t/2), warp-uniform; per-lane partial sums
+  // running max / partial sums of the lane's heads 2(t&1), 2(t&1)+1
   float m_run[2] = {-INFINITY, -INFINITY}, l_part[2] = {0.f, 0.f};
-  uint16_t* myP = sPh + wid * kG * kWarpTok;
-  uint16_t* myVT = sVT + wid * 4 * kWarpTok;
-  const int tok0 = kWarpTok * wid;
-  // per-lane byte offsets inside a stage
-  const int offK = kOffKc + (tok0 + g) * kRecC + 12 * t;
-  const int offKs = kOffKs + (tok0 + g) * kRecS + 4 * (t & 1);
-  const int offV = kOffVc + (tok0 + g) * kRecC + 12 * t;
-  const int offVs = kOffVs + (tok0 + lane) * kRecS;
-  uint16_t* pW = myP + (t >> 1) * kWarpTok + g;              // p writes: head 2*nt + t/2
-  const uint16_t* pR = myP + (g & 3) * kWarpTok + 2 * t;     // p reads: head g (g < 4)
-  const uint16_t* vR = myVT + (g >> 1) * kWarpTok + 2 * t;   // scale pairs: block g/2
+  const uint32_t pBase = su32(smem + (size_t)P * kSlots * C::STAGE) + wid * kG * kTok * 2;
+  const uint32_t pW = pBase + 2 * ((2 * (t & 1)) * kTok + g);
+  const uint32_t pR = pBase + 2 * ((g & 3) * kTok + 2 * t);
+  const uint32_t xBase = su32(smem + (size_t)P * kSlots * C::STAGE + 4 * kG * kTok * 2);
+  const int grp = 4 * hw + t;  // the lane's 32-value group of K and V
 
-  for (int tile = 0; tile < n_tiles; ++tile) {
-    cp_wait<kStages - 2>();
-    __syncthreads();
-    {
-      const int nx = tile + kStages - 1;
-      if (nx < n_tiles) load_stage(nx % kStages, nx);
-      cp_commit();
-    }
-    const uint8_t* st = ring + (tile % kStages) * kStageBytes;
-    const int64_t tbase = t_begin + (int64_t)tile * kTileTok + tok0;
-    const bool partial = tbase + kWarpTok > t_end;   // only the slice's last tile
+  for (int it = 0; it < n_it; ++it) {
+    const int slot = it % kSlots;
+    cp_wait<kSlots - 2>();
+    if (NH > 1) pair_sync(1 + pi); else __syncwarp();
+    // both warps are past the previous step: its slot takes the next load
+    if (it + kSlots - 1 < n_it) load_next((it + kSlots - 1) % kSlots);
+    cp_commit();
+    const uint32_t st = ring + slot * C::STAGE;
+    const int64_t tbase = t_begin + (int64_t)kTok * (pi + P * it);
 
-    // V scales of the warp's 32 tokens, transposed to [block][token]
-    {
-      const uint2 sv = *reinterpret_cast<const uint2*>(st + offVs);
-      myVT[0 * kWarpTok + lane] = (uint16_t)(sv.x & 0xffffu);
-      myVT[1 * kWarpTok + lane] = (uint16_t)(sv.x >> 16);
-      myVT[2 * kWarpTok + lane] = (uint16_t)(sv.y & 0xffffu);
-      myVT[3 * kWarpTok + lane] = (uint16_t)(sv.y >> 16);
-    }
-
-    // ---- scores S[token, (h, j)] for two 16-token tiles
-    float S[2][2][2];   // [tile u][row r][nt]
+    // ---- scores: S[u][r][c] for token 16u + 8r + g, head 2(t&1) + c
+    float S[2][2][2];
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
-      // two accumulator chains per n tile (even / odd chunk) for more ILP
-      float P[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      float Q[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      const uint32_t* k0 = reinterpret_cast<const uint32_t*>(st + offK + 16 * u * kRecC);
-      const uint32_t* k1 = reinterpret_cast<const uint32_t*>(st + offK + (16 * u + 8) * kRecC);
-      uint32_t n0[4], n1[4];
-      chunks3(k0[0], k0[1], k0[2], n0);
-      chunks3(k1[0], k1[1], k1[2], n1);
+      float Pm[4] = {0.f, 0.f, 0.f, 0.f};
+      float Pq[4] = {0.f, 0.f, 0.f, 0.f};
+      const int tok0 = 16 * u + g, tok1 = tok0 + 8;
+      uint32_t w0[4], w1[4], n0[4], n1[4];
+      load_group<KB>(st + C::OKC + tok0 * C::KREC + grp * 4 * KB, w0);
+      load_group<KB>(st + C::OKC + tok1 * C::KREC + grp * 4 * KB, w1);
+      chunk_words<KB>(w0, n0);
+      chunk_words<KB>(w1, n1);
+      Tab T0, T1;
+      uint32_t s0h = 0, s1h = 0;
+      if (KPV || KB == 4) {
+        T0 = kfix;
+        T1 = kfix;
+        if (!KPV) {
+          s0h = lds16(st + C::OKS + tok0 * C::KSB + 2 * grp);
+          s1h = lds16(st + C::OKS + tok1 * C::KSB + 2 * grp);
+          s0h |= s0h << 16;
+          s1h |= s1h << 16;
+        }
+      } else {
+        T0 = make_tab<KB>(kcent, lds16(st + C::OKS + tok0 * C::KSB + 2 * grp));
+        T1 = make_tab<KB>(kcent, lds16(st + C::OKS + tok1 * C::KSB + 2 * grp));
+      }
 #pragma unroll
       for (int s = 0; s < 4; ++s) {
         uint32_t x0[4], x1[4];
-        lut8(n0[s], ktl0, ktl1, kth0, kth1, x0);
-        lut8(n1[s], ktl0, ktl1, kth0, kth1, x1);
+        lut8<KB>(n0[s], T0, x0);
+        lut8<KB>(n1[s], T1, x1);
+        if (KB == 4 && !KPV) {
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-          float* c = (s & 1) ? Q[nt] : P[nt];
-          mma16816(c, x0[0], x1[0], x0[1], x1[1], bq[s][0][nt][0], bq[s][0][nt][1]);
-          mma16816(c, x0[2], x1[2], x0[3], x1[3], bq[s][1][nt][0], bq[s][1][nt][1]);
+          for (int e = 0; e < 4; ++e) {
+            x0[e] = hmul2(x0[e], s0h);
+            x1[e] = hmul2(x1[e], s1h);
+          }
+        }
+        mma16816(Pm, x0[0], x1[0], x0[1], x1[1], bq[s][0][0], bq[s][0][1]);
+        mma16816(Pm, x0[2], x1[2], x0[3], x1[3], bq[s][1][0], bq[s][1][1]);
+      }
+      if (QJL) {
+        const uint32_t q0 = lds32(st + C::OQB + tok0 * C::QB + 4 * t);
+        const uint32_t q1 = lds32(st + C::OQB + tok1 * C::QB + 4 * t);
+        // 2*s as fp16 (0 or 2.0): bits p and p+16 land on bits 14 and 30
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int p0 = 2 * j, p1 = 2 * j + 1;
+          const uint32_t a0 = (p0 <= 14 ? (q0 << (14 - p0)) : (q0 >> (p0 - 14))) & 0x40004000u;
+          const uint32_t a2 = (p1 <= 14 ? (q0 << (14 - p1)) : (q0 >> (p1 - 14))) & 0x40004000u;
+          const uint32_t a1 = (p0 <= 14 ? (q1 << (14 - p0)) : (q1 >> (p0 - 14))) & 0x40004000u;
+          const uint32_t a3 = (p1 <= 14 ? (q1 << (14 - p1)) : (q1 >> (p1 - 14))) & 0x40004000u;
+          mma16816(Pq, a0, a1, a2, a3, bj[j][0], bj[j][1]);
         }
       }
+      if (KPV) {
+        const float sc0 = h2f((uint16_t)lds16(st + C::OKS + tok0 * C::KSB));
+        const float sc1 = h2f((uint16_t)lds16(st + C::OKS + tok1 * C::KSB));
+        if (QJL) {
+          const float r0 = sc0 * h2f((uint16_t)lds16(st + C::OQR + tok0 * 2));
+          const float r1 = sc1 * h2f((uint16_t)lds16(st + C::OQR + tok1 * 2));
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
+          for (int c = 0; c < 2; ++c) {
+            S[u][0][c] = fmaf(r0, Pq[c] - sqs[c], sc0 * Pm[c]);
+            S[u][1][c] = fmaf(r1, Pq[2 + c] - sqs[c], sc1 * Pm[2 + c]);
+          }
+        } else {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) P[nt][e] += Q[nt][e];
-      // weight the block columns by the block norms; column pair (j0, j0+1)
+          for (int c = 0; c < 2; ++c) {
+            S[u][0][c] = sc0 * Pm[c];
+            S[u][1][c] = sc1 * Pm[2 + c];
+          }
+        }
+      } else {
 #pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const float2 scf = unpack_h2(*reinterpret_cast<const uint32_t*>(st + offKs + (16 * u + 8 * r) * kRecS));
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-          float v = fmaf(scf.x, P[nt][2 * r], scf.y * P[nt][2 * r + 1]);
-          S[u][r][nt] = v + __shfl_xor_sync(kFull, v, 1);
+        for (int c = 0; c < 2; ++c) {
+          S[u][0][c] = Pm[c];
+          S[u][1][c] = Pm[2 + c];
         }
       }
     }
-    if (partial) {
+    if (NH > 1) {
+      // the other half of the dimensions: same lane of the partner warp
+      const uint32_t mine = xBase + ((pi * 2 + hw) * 32 + lane) * 32;
+      const uint32_t other = xBase + ((pi * 2 + (hw ^ 1)) * 32 + lane) * 32;
+      sts128f(mine, S[0][0][0], S[0][0][1], S[0][1][0], S[0][1][1]);
+      sts128f(mine + 16, S[1][0][0], S[1][0][1], S[1][1][0], S[1][1][1]);
+      pair_sync(1 + pi);
+      const float4 o0 = lds128f(other), o1 = lds128f(other + 16);
+      S[0][0][0] += o0.x; S[0][0][1] += o0.y; S[0][1][0] += o0.z; S[0][1][1] += o0.w;
+      S[1][0][0] += o1.x; S[1][0][1] += o1.y; S[1][1][0] += o1.z; S[1][1][1] += o1.w;
+    }
+    if (tbase + kTok > t_end) {  // the slice's last step
 #pragma unroll
       for (int u = 0; u < 2; ++u)
 #pragma unroll
         for (int r = 0; r < 2; ++r)
-          if (tbase + 16 * u + g + 8 * r >= t_end) S[u][r][0] = S[u][r][1] = -INFINITY;
+          if (tbase + 16 * u + 8 * r + g >= t_end) S[u][r][0] = S[u][r][1] = -INFINITY;
     }
-    // ---- online softmax with lazy rescaling: the reference max moves only
-    // when some score exceeds it by more than 2^8
+
+    // ---- online softmax with lazy rescaling
     bool need = false;
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-      const float m = fmaxf(fmaxf(S[0][0][nt], S[0][1][nt]), fmaxf(S[1][0][nt], S[1][1][nt]));
-      need |= m > m_run[nt] + kLazy;
+    for (int c = 0; c < 2; ++c) {
+      const float m = fmaxf(fmaxf(S[0][0][c], S[0][1][c]), fmaxf(S[1][0][c], S[1][1][c]));
+      need |= m > m_run[c] + kLazy;
     }
     if (__any_sync(kFull, need)) {
       float al[2];
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        float m = fmaxf(fmaxf(S[0][0][nt], S[0][1][nt]), fmaxf(S[1][0][nt], S[1][1][nt]));
+      for (int c = 0; c < 2; ++c) {
+        float m = fmaxf(fmaxf(S[0][0][c], S[0][1][c]), fmaxf(S[1][0][c], S[1][1][c]));
         m = fmaxf(m, __shfl_xor_sync(kFull, m, 4));
         m = fmaxf(m, __shfl_xor_sync(kFull, m, 8));
         m = fmaxf(m, __shfl_xor_sync(kFull, m, 16));
-        const float mn = fmaxf(m_run[nt], m);
-        al[nt] = (m_run[nt] == -INFINITY) ? 0.f : ex2(m_run[nt] - mn);
-        m_run[nt] = mn;
-        l_part[nt] *= al[nt];
+        const float mn = fmaxf(m_run[c], m);
+        al[c] = (m_run[c] == -INFINITY) ? 0.f : ex2(m_run[c] - mn);
+        m_run[c] = mn;
+        l_part[c] *= al[c];
       }
-      // V accumulator columns are heads 2t, 2t+1 (lanes t < 2)
-      const float aA = al[t & 1];
-      const float aB = __shfl_xor_sync(kFull, al[t & 1], 2);
 #pragma unroll
       for (int s = 0; s < 4; ++s)
 #pragma unroll
         for (int pr = 0; pr < 2; ++pr) {
-          acc[s][pr][0] *= aA;
-          acc[s][pr][1] *= aB;
-          acc[s][pr][2] *= aA;
-          acc[s][pr][3] *= aB;
+          acc[s][pr][0] *= al[0];
+          acc[s][pr][1] *= al[1];
+          acc[s][pr][2] *= al[0];
+          acc[s][pr][3] *= al[1];
         }
     }
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-      // no valid token seen yet implies every score here is -inf
-      const float mref = m_run[nt] == -INFINITY ? 0.f : m_run[nt];
+    for (int u = 0; u < 2; ++u)
 #pragma unroll
-      for (int u = 0; u < 2; ++u)
+      for (int r = 0; r < 2; ++r) {
+        float vs = 1.f;
+        if (VPV) vs = h2f((uint16_t)lds16(st + C::OVS + (16 * u + 8 * r + g) * C::VSB));
 #pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          const float p = ex2(S[u][r][nt] - mref);   // -inf scores give 0
-          l_part[nt] += p;
-          if ((t & 1) == 0) pW[2 * nt * kWarpTok + 16 * u + 8 * r] = f2h(p);
+        for (int c = 0; c < 2; ++c) {
+          // no valid token seen yet implies every score here is -inf
+          const float mref = m_run[c] == -INFINITY ? 0.f : m_run[c];
+          const float p = ex2(S[u][r][c] - mref);
+          l_part[c] += p;
+          if (t < 2) sts16(pW + 2 * (c * kTok + 16 * u + 8 * r), f2h(VPV ? p * vs : p));
         }
-    }
+      }
     __syncwarp();
-    // ---- V side: O^T[coord, h] += (V^ * scaleV)^T P, 16 tokens per k step
+
+    // ---- V side: O^T[coord, head] += V^T P, 16 tokens per k step
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
-      uint32_t pb0 = *reinterpret_cast<const uint32_t*>(pR + 16 * u);
-      uint32_t pb1 = *reinterpret_cast<const uint32_t*>(pR + 16 * u + 8);
-      if (g >= kG) pb0 = pb1 = 0u;
-      const uint32_t sv01 = *reinterpret_cast<const uint32_t*>(vR + 16 * u);
-      const uint32_t sv89 = *reinterpret_cast<const uint32_t*>(vR + 16 * u + 8);
-      const uint32_t* v0 = reinterpret_cast<const uint32_t*>(st + offV + 16 * u * kRecC);
-      const uint32_t* v1 = reinterpret_cast<const uint32_t*>(st + offV + (16 * u + 8) * kRecC);
-      uint32_t n0[4], n1[4];
-      chunks3(v0[0], v0[1], v0[2], n0);
-      chunks3(v1[0], v1[1], v1[2], n1);
+      const uint32_t pb0 = lds32(pR + 2 * 16 * u);
+      const uint32_t pb1 = lds32(pR + 2 * (16 * u + 8));
+      const int tok0 = 16 * u + g, tok1 = tok0 + 8;
+      uint32_t w0[4], w1[4], n0[4], n1[4];
+      load_group<VB>(st + C::OVC + tok0 * C::VREC + grp * 4 * VB, w0);
+      load_group<VB>(st + C::OVC + tok1 * C::VREC + grp * 4 * VB, w1);
+      chunk_words<VB>(w0, n0);
+      chunk_words<VB>(w1, n1);
+      Tab T0, T1;
+      if (VPV) {
+        T0 = vfix;
+        T1 = vfix;
+      } else {
+        T0 = make_tab<VB>(vcent, lds16(st + C::OVS + tok0 * C::VSB + 2 * grp));
+        T1 = make_tab<VB>(vcent, lds16(st + C::OVS + tok1 * C::VSB + 2 * grp));
+      }
 #pragma unroll
       for (int s = 0; s < 4; ++s) {
         uint32_t x0[4], x1[4];
-        lut8(n0[s], vtl0, vtl1, vth0, vth1, x0);
-        lut8(n1[s], vtl0, vtl1, vth0, vth1, x1);
+        lut8<VB>(n0[s], T0, x0);
+        lut8<VB>(n1[s], T1, x1);
 #pragma unroll
-        for (int pr = 0; pr < 2; ++pr) {
-          const uint32_t a0 = hmul2(movtrans(x0[pr]), sv01);
-          const uint32_t a1 = hmul2(movtrans(x0[pr + 2]), sv01);
-          const uint32_t a2 = hmul2(movtrans(x1[pr]), sv89);
-          const uint32_t a3 = hmul2(movtrans(x1[pr + 2]), sv89);
-          mma16816(acc[s][pr], a0, a1, a2, a3, pb0, pb1);
-        }
+        for (int pr = 0; pr < 2; ++pr)
+          mma16816(acc[s][pr], movtrans(x0[pr]), movtrans(x0[pr + 2]), movtrans(x1[pr]), movtrans(x1[pr + 2]), pb0,
+                   pb1);
       }
     }
     __syncwarp();
   }
   // the combine kernel may be scheduled now; it waits for this grid to finish
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
-  // full sums per head: the 8 lanes g of a (t) column hold partial sums
+
+  // ---- merge the pipelines through shared memory, then write the partial
   float l_run[2];
 #pragma unroll
-  for (int nt = 0; nt < 2; ++nt) {
-    float v = l_part[nt];
+  for (int c = 0; c < 2; ++c) {
+    float v = l_part[c];
     v += __shfl_xor_sync(kFull, v, 4);
     v += __shfl_xor_sync(kFull, v, 8);
     v += __shfl_xor_sync(kFull, v, 16);
-    l_run[nt] = v;
+    l_run[c] = v;
   }
   cp_wait<0>();
   __syncthreads();
-
-  // ---- per-warp results to shared memory (reusing the ring), then merge
-  float* sO = reinterpret_cast<float*>(ring);   // [kW][kG][kD]
+  float* sO = reinterpret_cast<float*>(smem);  // [P][kG][D]
   {
-    float* ow = sO + wid * kG * kD;
+    float* ow = sO + pi * kG * D;
     if (t < 2) {
-      const int blk = g >> 1, e = g & 1;
+      // accumulator row g of tile (s, pr): coordinate of the transposed
+      // fragment, lane t's columns are heads 2t, 2t+1
+      const int blk = 4 * hw + (g >> 1), e = g & 1;
 #pragma unroll
       for (int s = 0; s < 4; ++s)
 #pragma unroll
         for (int pr = 0; pr < 2; ++pr) {
-          const int c0 = 32 * blk + 8 * s + 2 * pr + e;     // row g
-          const int c1 = c0 + 4;                            // row g + 8
-          ow[(2 * t) * kD + c0] = acc[s][pr][0];
-          ow[(2 * t + 1) * kD + c0] = acc[s][pr][1];
-          ow[(2 * t) * kD + c1] = acc[s][pr][2];
-          ow[(2 * t + 1) * kD + c1] = acc[s][pr][3];
+          const int c0 = 32 * blk + 8 * s + 2 * pr + e;
+          const int c1 = c0 + 4;
+          ow[(2 * t) * D + c0] = acc[s][pr][0];
+          ow[(2 * t + 1) * D + c0] = acc[s][pr][1];
+          ow[(2 * t) * D + c1] = acc[s][pr][2];
+          ow[(2 * t + 1) * D + c1] = acc[s][pr][3];
         }
     }
-    if (g == 0 && (t & 1) == 0) {
+    if (hw == 0 && g == 0 && t < 2) {
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        const int h = 2 * nt + (t >> 1);
-        s_ml[wid][0][h] = m_run[nt];
-        s_ml[wid][1][h] = l_run[nt];
+      for (int c = 0; c < 2; ++c) {
+        s_ml[pi][0][2 * t + c] = m_run[c];
+        s_ml[pi][1][2 * t + c] = l_run[c];
       }
     }
   }
   __syncthreads();
-  for (int e = tid; e < kG * (kD + 2); e += kT) {
-    const int h = e / (kD + 2), i = e % (kD + 2);
+  for (int e = tid; e < kG * (D + 2); e += kThreads) {
+    const int h = e / (D + 2), i = e % (D + 2);
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kW; ++w) M = fmaxf(M, s_ml[w][0][h]);
+    for (int w = 0; w < P; ++w) M = fmaxf(M, s_ml[w][0][h]);
     float val = 0.f;
     if (i == 0) {
       val = M;
     } else {
 #pragma unroll
-      for (int w = 0; w < kW; ++w) {
+      for (int w = 0; w < P; ++w) {
         const float mw = s_ml[w][0][h];
         const float wt = mw == -INFINITY ? 0.f : exp2f(mw - M);
-        val += wt * (i == 1 ? s_ml[w][1][h] : sO[(w * kG + h) * kD + i - 2]);
+        val += wt * (i == 1 ? s_ml[w][1][h] : sO[(w * kG + h) * D + i - 2]);
       }
     }
-    a.part[(((int64_t)b * a.Hq + h0 + h) * a.n_split + split) * (kD + 4) + i] = val;
+    a.part[(((int64_t)b * a.Hq + h0 + h) * a.n_split + split) * (D + 4) + i] = val;
   }
 }
 
-constexpr size_t kSmem = (size_t)kStages * kStageBytes + (size_t)kW * kG * kWarpTok * 2 +
-                         (size_t)kW * 4 * kWarpTok * 2;
-static_assert((size_t)kStages * kStageBytes >= (size_t)kW * kG * kD * 4, "ring too small for the merge");
-
-}  // namespace
-
-// Eligible: d 128, K and V 3-bit with 32-value blocks, no QJL / norm
-// correction dependence (the scale is whatever is stored), 4 q heads per KV
-// head, even S_cap and 16-byte aligned scale arrays.
-bool decode_tc_eligible(const CodecParams& PK, const CodecParams& PV, int G, int64_t S_cap, const void* ks,
-                        const void* vs) {
-  return PK.d == 128 && PV.d == 128 && PK.bits == 3 && PV.bits == 3 && PK.blk == 32 && PV.blk == 32 && !PK.m &&
-         !PV.m && G == kG && (S_cap % 2) == 0 && aligned16(ks) && aligned16(vs);
+// S q of every (batch, q head) for QJL keys, times softmax_scale * log2 e *
+// sqrt(pi/2) / m, rounded to fp16, and the sum of each row of it.
+__global__ void __launch_bounds__(kQjlM) qjl_prep_kernel(const uint16_t* __restrict__ q, const float* __restrict__ S,
+                                                         int d, float coef, uint16_t* __restrict__ sq,
+                                                         float* __restrict__ sqsum) {
+  __shared__ float s_q[kMaxDim];
+  __shared__ float s_red[kQjlM / 32];
+  const int row = blockIdx.x, i = threadIdx.x;
+  for (int j = i; j < d; j += kQjlM) s_q[j] = h2f(q[(int64_t)row * d + j]);
+  __syncthreads();
+  float v = 0.f;
+  for (int j = 0; j < d; ++j) v = fmaf(S[(int64_t)i * d + j], s_q[j], v);
+  const uint16_t h = f2h(v * coef);
+  sq[(int64_t)row * kQjlM + i] = h;
+  float r = h2f(h);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) r += __shfl_xor_sync(kFull, r, o);
+  if ((i & 31) == 0) s_red[i >> 5] = r;
+  __syncthreads();
+  if (i == 0) {
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < kQjlM / 32; ++w) tot += s_red[w];
+    sqsum[row] = tot;
+  }
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 }
 
-int64_t decode_tc_per_split(int64_t ctx, int n_split) {
-  int64_t per = (ctx + n_split - 1) / n_split;
-  per = (per + kTileTok - 1) / kTileTok * kTileTok;
-  return per > 0 ? per : kTileTok;
-}
-
-int launch_decode_tc(const CodecParams& PK, const CodecParams& PV, const uint8_t* kc, const uint16_t* ks,
-                     const uint8_t* vc, const uint16_t* vs, const uint16_t* q, const int32_t* kv_len, float* part,
-                     int B, int Hq, int Hkv, int64_t S_cap, int64_t ctx, int n_split, float qscale,
-                     uint16_t* out, cudaStream_t st) {
+template <int D, int KB, int VB, bool KPV, bool VPV, bool QJL>
+int launch_cfg(const CodecParams& PK, const CodecParams& PV, const TcArgs& a, int B, cudaStream_t st) {
+  using C = Cfg<D, KB, VB, KPV, VPV, QJL>;
+  auto kern = decode_tc_kernel<D, KB, VB, KPV, VPV, QJL>;
   static bool attr_set[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return TQ_ERR_CUDA;
   if (!attr_set[dev]) {
-    if (cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem) !=
-        cudaSuccess)
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM) != cudaSuccess)
       return TQ_ERR_CUDA;
     attr_set[dev] = true;
   }
-  TcArgs a{kc, reinterpret_cast<const uint8_t*>(ks), vc, reinterpret_cast<const uint8_t*>(vs), q, kv_len, part,
-           S_cap, ctx, decode_tc_per_split(ctx, n_split), Hq, Hkv, n_split, qscale};
-  dim3 grid(n_split, B * Hkv);
-  decode_tc_kernel<<<grid, kT, kSmem, st>>>(PK, PV, a);
-  if (cudaGetLastError() != cudaSuccess) return TQ_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)a.n_split, (unsigned)(B * a.Hkv));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = QJL ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, PK, PV, a) != cudaSuccess) return TQ_ERR_CUDA;
+  return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+}
+
+}  // namespace
+
+// Eligible layouts: head_dim 128 or 256 with 4 q heads per KV head; K codes
+// of 2-4 bits, V codes of 3 bits, each with one norm per 32 values or per
+// vector (the combinations instantiated below); QJL keys with m = 128 on
+// 2-bit per-vector K at head_dim 128; every array 16-byte aligned and every
+// per-token stream's row pitch (S_cap times its bytes per token) a multiple
+// of 16.
+bool decode_tc_eligible(const CodecParams& PK, const CodecParams& PV, int G, int64_t S_cap, const tq_kv_view* K,
+                        const tq_kv_view* V) {
+  if (G != kG || PK.d != PV.d || (PK.d != 128 && PK.d != 256) || PV.bits != 3) return false;
+  const bool kpv = PK.blk == PK.d, vpv = PV.blk == PV.d;
+  // every per-token stream must keep 16-byte aligned rows for cp.async
+  const int64_t streams[6] = {PK.code_bytes, 2 * PK.nb, PK.qjl_bytes, PK.m ? 2 : 0, PV.code_bytes, 2 * PV.nb};
+  for (int i = 0; i < 6; ++i)
+    if ((S_cap * streams[i]) % 16 != 0) return false;
+  if ((!kpv && PK.blk != 32) || (!vpv && PV.blk != 32)) return false;
+  bool ok;
+  if (PK.d == 256) {
+    ok = !kpv && !vpv && !PK.m && PK.bits >= 2 && PK.bits <= 4;
+  } else if (PK.m) {
+    ok = PK.m == kQjlM && kpv && vpv && PK.bits == 2;
+  } else if (kpv) {
+    ok = PK.bits == 2;
+  } else {
+    ok = PK.bits == 3 || ((PK.bits == 2 || PK.bits == 4) && !vpv);
+  }
+  if (!ok) return false;
+  if (!aligned16(K->codes) || !aligned16(K->scales) || !aligned16(V->codes) || !aligned16(V->scales)) return false;
+  if (PK.m && (!aligned16(K->qjl_bits) || !aligned16(K->qjl_rnorm) || !K->S)) return false;
+  return true;
+}
+
+int64_t decode_tc_per_split(int64_t ctx, int n_split) {
+  int64_t per = (ctx + n_split - 1) / n_split;
+  per = (per + kThreads - 1) / kThreads * kThreads;
+  return per > 0 ? per : kThreads;
+}
+
+// Extra workspace after the partials: S q rows and their sums (QJL keys).
+size_t decode_tc_extra_bytes(int B, int Hq) {
+  return (size_t)B * Hq * (kQjlM * 2 + 4) + 256;
+}
+
+int launch_decode_tc(const CodecParams& PK, const CodecParams& PV, const tq_kv_view* K, const tq_kv_view* V,
+                     const uint16_t* q, const int32_t* kv_len, float* part, size_t part_bytes, int B, int Hq, int Hkv,
+                     int64_t S_cap, int64_t ctx, int n_split, float qscale, uint16_t* out, cudaStream_t st) {
+  TcArgs a{};
+  a.kc = K->codes;
+  a.ks = reinterpret_cast<const uint8_t*>(K->scales);
+  a.kq = K->qjl_bits;
+  a.kr = reinterpret_cast<const uint8_t*>(K->qjl_rnorm);
+  a.vc = V->codes;
+  a.vs = reinterpret_cast<const uint8_t*>(V->scales);
+  a.q = q;
+  a.kv_len = kv_len;
+  a.part = part;
+  a.S_cap = S_cap;
+  a.ctx = ctx;
+  a.per = decode_tc_per_split(ctx, n_split);
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.n_split = n_split;
+  a.qscale = qscale;
+  if (PK.m) {
+    uint8_t* extra = reinterpret_cast<uint8_t*>(part) + ((part_bytes + 255) / 256) * 256;
+    uint16_t* sq = reinterpret_cast<uint16_t*>(extra);
+    float* sqsum = reinterpret_cast<float*>(extra + (((size_t)B * Hq * kQjlM * 2 + 15) / 16) * 16);
+    a.sq = sq;
+    a.sqsum = sqsum;
+    qjl_prep_kernel<<<B * Hq, kQjlM, 0, st>>>(q, K->S, PK.d, qscale * kSqrtHalfPi / (float)PK.m, sq, sqsum);
+    if (cudaGetLastError() != cudaSuccess) return TQ_ERR_CUDA;
+  }
+  const bool kpv = PK.blk == PK.d, vpv = PV.blk == PV.d;
+  int r;
+  if (PK.d == 256) {
+    r = PK.bits == 4 ? launch_cfg<256, 4, 3, false, false, false>(PK, PV, a, B, st)
+        : PK.bits == 3 ? launch_cfg<256, 3, 3, false, false, false>(PK, PV, a, B, st)
+                       : launch_cfg<256, 2, 3, false, false, false>(PK, PV, a, B, st);
+  } else if (PK.m) {
+    r = launch_cfg<128, 2, 3, true, true, true>(PK, PV, a, B, st);
+  } else if (kpv) {
+    r = vpv ? launch_cfg<128, 2, 3, true, true, false>(PK, PV, a, B, st)
+            : launch_cfg<128, 2, 3, true, false, false>(PK, PV, a, B, st);
+  } else {
+    r = PK.bits == 4 ? launch_cfg<128, 4, 3, false, false, false>(PK, PV, a, B, st)
+        : PK.bits == 3 ? (vpv ? launch_cfg<128, 3, 3, false, true, false>(PK, PV, a, B, st)
+                              : launch_cfg<128, 3, 3, false, false, false>(PK, PV, a, B, st))
+                       : launch_cfg<128, 2, 3, false, false, false>(PK, PV, a, B, st);
+  }
+  if (r != TQ_OK) return r;
   return decode_combine(PV, part, n_split, out, B * Hq, st);
 }
 

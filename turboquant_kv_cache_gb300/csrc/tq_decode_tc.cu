@@ -161,8 +161,12 @@ __device__ __forceinline__ float4 lds128f(uint32_t a) {
   asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(a));
   return v;
 }
-__device__ __forceinline__ void pair_sync(int id) {
-  asm volatile("bar.sync %0, 64;" ::"r"(id) : "memory");
+// Named barrier of the two warps of pipeline pi (ids 1 and 2; 0 is __syncthreads).
+__device__ __forceinline__ void pair_sync(int pi) {
+  if (pi == 0)
+    asm volatile("bar.sync 1, 64;" ::: "memory");
+  else
+    asm volatile("bar.sync 2, 64;" ::: "memory");
 }
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
   const __half2 h = __floats2half2_rn(lo, hi);
@@ -170,6 +174,34 @@ __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
 }
 __device__ __forceinline__ float2 unpack_h2(uint32_t v) {
   return __half22float2(*reinterpret_cast<const __half2*>(&v));
+}
+
+// One step (kTok tokens) of a per-token stream of BYTES bytes per token,
+// as 16-byte copies spread over the pipeline's 32 * NH lanes.
+template <int BYTES, int NH>
+__device__ __forceinline__ void copy_full(uint32_t dst, const uint8_t* src, int plane) {
+  constexpr int CH = kTok * BYTES / 16, STEP = 32 * NH;
+#pragma unroll
+  for (int k = 0; k < (CH + STEP - 1) / STEP; ++k) {
+    const int c = plane + k * STEP;
+    if (CH % STEP == 0 || c < CH) cp16(dst + 16 * c, src + 16 * c, 16);
+  }
+}
+
+// The same for a step with only nv valid tokens: the rest is zero-filled.
+template <int BYTES, int NH>
+__device__ __forceinline__ void copy_part(uint32_t dst, const uint8_t* base, int64_t tok0, int nv, int plane) {
+  constexpr int CH = kTok * BYTES / 16, STEP = 32 * NH;
+  const uint8_t* src = base + tok0 * BYTES;
+#pragma unroll
+  for (int k = 0; k < (CH + STEP - 1) / STEP; ++k) {
+    const int c = plane + k * STEP;
+    if (CH % STEP == 0 || c < CH) {
+      int bytes = nv * BYTES - 16 * c;
+      bytes = bytes < 0 ? 0 : (bytes > 16 ? 16 : bytes);
+      cp16(dst + 16 * c, bytes ? src + 16 * c : base, bytes);
+    }
+  }
 }
 
 // Nibble words (code k of chunk c in bits 4k..4k+2) of one 32-code group,
@@ -307,30 +339,32 @@ __global__ void __launch_bounds__(kThreads, 4) decode_tc_kernel(const CodecParam
 
   // ---- staging: every 16-byte chunk of every stream of a step, spread over
   // the pipeline's lanes; zero-filled past the end of the slice
-  auto stream = [&](uint32_t dst, const uint8_t* base, int per_tok, int64_t tok0, int nv) {
-    const int chunks = kTok * per_tok / 16;
-    const uint8_t* src = base + tok0 * per_tok;
-    const int valid = nv * per_tok;
-    for (int c = plane; c < chunks; c += 32 * NH) {
-      int bytes = valid - 16 * c;
-      bytes = bytes < 0 ? 0 : (bytes > 16 ? 16 : bytes);
-      cp16(dst + 16 * c, bytes ? src + 16 * c : base, bytes);
-    }
-  };
   int ld_it = 0;
   auto load_next = [&](int slot) {
     const int64_t t0 = t_begin + (int64_t)kTok * (pi + P * ld_it);
-    const int nv = (int)imin64(kTok, t_end - t0);
     const int64_t tok0 = rec0 + t0;
     const uint32_t dst = ring + slot * C::STAGE;
-    stream(dst + C::OKC, a.kc, C::KREC, tok0, nv);
-    stream(dst + C::OKS, a.ks, C::KSB, tok0, nv);
-    if (QJL) {
-      stream(dst + C::OQB, a.kq, C::QB, tok0, nv);
-      stream(dst + C::OQR, a.kr, C::QR, tok0, nv);
+    const int64_t rem = t_end - t0;
+    if (rem >= kTok) {
+      copy_full<C::KREC, NH>(dst + C::OKC, a.kc + tok0 * C::KREC, plane);
+      copy_full<C::KSB, NH>(dst + C::OKS, a.ks + tok0 * C::KSB, plane);
+      if (QJL) {
+        copy_full<C::QB, NH>(dst + C::OQB, a.kq + tok0 * C::QB, plane);
+        copy_full<C::QR, NH>(dst + C::OQR, a.kr + tok0 * C::QR, plane);
+      }
+      copy_full<C::VREC, NH>(dst + C::OVC, a.vc + tok0 * C::VREC, plane);
+      copy_full<C::VSB, NH>(dst + C::OVS, a.vs + tok0 * C::VSB, plane);
+    } else {
+      const int nv = (int)rem;
+      copy_part<C::KREC, NH>(dst + C::OKC, a.kc, tok0, nv, plane);
+      copy_part<C::KSB, NH>(dst + C::OKS, a.ks, tok0, nv, plane);
+      if (QJL) {
+        copy_part<C::QB, NH>(dst + C::OQB, a.kq, tok0, nv, plane);
+        copy_part<C::QR, NH>(dst + C::OQR, a.kr, tok0, nv, plane);
+      }
+      copy_part<C::VREC, NH>(dst + C::OVC, a.vc, tok0, nv, plane);
+      copy_part<C::VSB, NH>(dst + C::OVS, a.vs, tok0, nv, plane);
     }
-    stream(dst + C::OVC, a.vc, C::VREC, tok0, nv);
-    stream(dst + C::OVS, a.vs, C::VSB, tok0, nv);
     ++ld_it;
   };
 #pragma unroll
@@ -428,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, 4) decode_tc_kernel(const CodecParam
   for (int it = 0; it < n_it; ++it) {
     const int slot = it % kSlots;
     cp_wait<kSlots - 2>();
-    if (NH > 1) pair_sync(1 + pi); else __syncwarp();
+    if (NH > 1) pair_sync(pi); else __syncwarp();
     // both warps are past the previous step: its slot takes the next load
     if (it + kSlots - 1 < n_it) load_next((it + kSlots - 1) % kSlots);
     cp_commit();
@@ -523,7 +557,7 @@ __global__ void __launch_bounds__(kThreads, 4) decode_tc_kernel(const CodecParam
       const uint32_t other = xBase + ((pi * 2 + (hw ^ 1)) * 32 + lane) * 32;
       sts128f(mine, S[0][0][0], S[0][0][1], S[0][1][0], S[0][1][1]);
       sts128f(mine + 16, S[1][0][0], S[1][0][1], S[1][1][0], S[1][1][1]);
-      pair_sync(1 + pi);
+      pair_sync(pi);
       const float4 o0 = lds128f(other), o1 = lds128f(other + 16);
       S[0][0][0] += o0.x; S[0][0][1] += o0.y; S[0][1][0] += o0.z; S[0][1][1] += o0.w;
       S[1][0][0] += o1.x; S[1][0][1] += o1.y; S[1][1][0] += o1.z; S[1][1][1] += o1.w;

@@ -259,68 +259,12 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const CodecPa
   }
 }
 
-constexpr int kCombWarps = 2;  // rows per CTA: many small CTAs spread the L2 reads over the SMs
-
-// One warp per output row (b, head[, query]); lane holds the D/32 consecutive
-// coordinates E*lane .. E*lane+E-1.  Merges the split partials (log-sum-exp
-// weights), divides by the total mass and rotates back (D H per V block)
-// with in-lane and shuffle butterflies.  Launched as a programmatic
-// dependent of the split kernel: the wait below holds until that grid has
-// finished and its partials are visible.
+// Final step of a merged row: divide by the total mass, rotate back (D H per
+// V block) with in-lane and shuffle butterflies, store fp16.  Lane holds the
+// D/32 consecutive coordinates E*lane .. E*lane+E-1.
 template <int D>
-__global__ void __launch_bounds__(kCombWarps * 32) decode_combine_kernel(const CodecParams PV, const float* __restrict__ part,
-                                                             int n_split, uint16_t* __restrict__ out, int rows) {
-  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+__device__ __forceinline__ void finish_row(const CodecParams& PV, float* o, float L, uint16_t* dst_row, int lane) {
   constexpr int E = D / 32;
-  const int row = blockIdx.x * kCombWarps + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-  if (row >= rows) return;
-  const float* p = part + (int64_t)row * n_split * (D + 4);
-  // The values of the first kPre splits are loaded before anything else, so
-  // that every load of the row is in flight at once: one round trip to L2
-  // instead of a chain of them.  Lane s holds split s's (m, l).
-  constexpr int kPre = 64 / E;   // 32, 16, 8 splits for d = 64, 128, 256
-  float2 v[kPre][E / 2];
-#pragma unroll
-  for (int j = 0; j < kPre; ++j)
-#pragma unroll
-    for (int e = 0; e < E / 2; ++e)
-      v[j][e] = j < n_split ? *reinterpret_cast<const float2*>(p + j * (D + 4) + 2 + E * lane + 2 * e)
-                            : make_float2(0.f, 0.f);
-  const float m_l = lane < n_split ? p[lane * (D + 4)] : -INFINITY;
-  const float l_l = lane < n_split ? p[lane * (D + 4) + 1] : 0.f;
-  float M = m_l;
-  for (int s = lane + 32; s < n_split; s += 32) M = fmaxf(M, p[s * (D + 4)]);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
-  // weight of split s: exp2(m_s - M), zero for an empty split
-  const float w_l = m_l == -INFINITY ? 0.f : exp2f(m_l - M);
-  float L = w_l * l_l;
-  float o[E];
-#pragma unroll
-  for (int e = 0; e < E; ++e) o[e] = 0.f;
-#pragma unroll
-  for (int j = 0; j < kPre; ++j) {
-    const float w = __shfl_sync(kFull, w_l, j);   // zero for j >= n_split
-#pragma unroll
-    for (int e = 0; e < E / 2; ++e) {
-      o[2 * e] = fmaf(w, v[j][e].x, o[2 * e]);
-      o[2 * e + 1] = fmaf(w, v[j][e].y, o[2 * e + 1]);
-    }
-  }
-  for (int s = kPre; s < n_split; ++s) {   // only for more splits than kPre
-    const float* ps = p + s * (D + 4);
-    const float ms = ps[0];
-    const float w = ms == -INFINITY ? 0.f : exp2f(ms - M);
-    if (s >= 32) L = fmaf(lane == 0 ? w : 0.f, ps[1], L);
-#pragma unroll
-    for (int e = 0; e < E; e += 2) {
-      const float2 x = *reinterpret_cast<const float2*>(ps + 2 + E * lane + e);
-      o[e] = fmaf(w, x.x, o[e]);
-      o[e + 1] = fmaf(w, x.y, o[e + 1]);
-    }
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(kFull, L, off);
   const float inv = L > 0.f ? PV.inv_sqrt_blk / L : 0.f;
   // unnormalised Walsh-Hadamard per V block: strides below E inside the
   // lane, the rest across lanes
@@ -350,7 +294,7 @@ __global__ void __launch_bounds__(kCombWarps * 32) decode_combine_kernel(const C
     const float v1 = flip(o[e + 1] * inv, (PV.sign_bits[(i + 1) >> 5] >> ((i + 1) & 31)) & 1u);
     packed[e / 2] = (uint32_t)f2h(v0) | ((uint32_t)f2h(v1) << 16);
   }
-  uint16_t* dst = out + (int64_t)row * D + E * lane;
+  uint16_t* dst = dst_row + E * lane;
   if (E == 8) {
     *reinterpret_cast<uint4*>(dst) = make_uint4(packed[0], packed[1 % (E / 2)], packed[2 % (E / 2)], packed[3 % (E / 2)]);
   } else if (E == 4) {
@@ -358,6 +302,118 @@ __global__ void __launch_bounds__(kCombWarps * 32) decode_combine_kernel(const C
   } else {
     *reinterpret_cast<uint32_t*>(dst) = packed[0];
   }
+}
+
+constexpr int kCombWarps = 2;  // rows per CTA: many small CTAs spread the L2 reads over the SMs
+
+// One warp per output row (b, head[, query]); lane holds the D/32 consecutive
+// coordinates E*lane .. E*lane+E-1.  Merges the split partials (log-sum-exp
+// weights), divides by the total mass and rotates back (D H per V block)
+// with in-lane and shuffle butterflies.  Launched as a programmatic
+// dependent of the split kernel: the wait below holds until that grid has
+// finished and its partials are visible.
+template <int D>
+__global__ void __launch_bounds__(kCombWarps * 32) decode_combine_kernel(const CodecParams PV, const float* __restrict__ part,
+                                                             int n_split, uint16_t* __restrict__ out, int rows) {
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+  constexpr int E = D / 32;
+  const int row = blockIdx.x * kCombWarps + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  const float* p = part + (int64_t)row * n_split * (D + 4);
+  // Up to kPre splits (more go to the wide kernel): their values are loaded
+  // before anything else, so that every load of the row is in flight at
+  // once, one round trip to L2 instead of a chain of them.  Lane s holds
+  // split s's (m, l).
+  constexpr int kPre = 64 / E;   // 32, 16, 8 splits for d = 64, 128, 256
+  float2 v[kPre][E / 2];
+#pragma unroll
+  for (int j = 0; j < kPre; ++j)
+#pragma unroll
+    for (int e = 0; e < E / 2; ++e)
+      v[j][e] = j < n_split ? *reinterpret_cast<const float2*>(p + j * (D + 4) + 2 + E * lane + 2 * e)
+                            : make_float2(0.f, 0.f);
+  const float m_l = lane < n_split ? p[lane * (D + 4)] : -INFINITY;
+  const float l_l = lane < n_split ? p[lane * (D + 4) + 1] : 0.f;
+  float M = m_l;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
+  // weight of split s: exp2(m_s - M), zero for an empty split
+  const float w_l = m_l == -INFINITY ? 0.f : exp2f(m_l - M);
+  float L = w_l * l_l;
+  float o[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) o[e] = 0.f;
+#pragma unroll
+  for (int j = 0; j < kPre; ++j) {
+    const float w = __shfl_sync(kFull, w_l, j);   // zero for j >= n_split
+#pragma unroll
+    for (int e = 0; e < E / 2; ++e) {
+      o[2 * e] = fmaf(w, v[j][e].x, o[2 * e]);
+      o[2 * e + 1] = fmaf(w, v[j][e].y, o[2 * e + 1]);
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(kFull, L, off);
+  finish_row<D>(PV, o, L, out + (int64_t)row * D, lane);
+}
+
+// Many splits (more than the narrow kernel preloads): one CTA per row, the
+// warps take interleaved subsets of the splits, then one warp sums them.
+constexpr int kWideWarps = 8;
+
+template <int D>
+__global__ void __launch_bounds__(kWideWarps * 32) decode_combine_wide_kernel(const CodecParams PV,
+                                                                             const float* __restrict__ part,
+                                                                             int n_split, uint16_t* __restrict__ out) {
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+  constexpr int E = D / 32;
+  __shared__ float s_o[kWideWarps][D];
+  __shared__ float s_x[kWideWarps];
+  const int row = blockIdx.x, w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const float* p = part + (int64_t)row * n_split * (D + 4);
+  float M = -INFINITY;
+  for (int s = threadIdx.x; s < n_split; s += kWideWarps * 32) M = fmaxf(M, p[s * (D + 4)]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
+  if (lane == 0) s_x[w] = M;
+  __syncthreads();
+  M = s_x[0];
+#pragma unroll
+  for (int i = 1; i < kWideWarps; ++i) M = fmaxf(M, s_x[i]);
+  float o[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) o[e] = 0.f;
+  float L = 0.f;
+#pragma unroll 4
+  for (int s = w; s < n_split; s += kWideWarps) {
+    const float* ps = p + s * (D + 4);
+    const float ms = ps[0];
+    const float wt = ms == -INFINITY ? 0.f : exp2f(ms - M);
+    L = fmaf(wt, ps[1], L);
+#pragma unroll
+    for (int e = 0; e < E; e += 2) {
+      const float2 v = *reinterpret_cast<const float2*>(ps + 2 + E * lane + e);
+      o[e] = fmaf(wt, v.x, o[e]);
+      o[e + 1] = fmaf(wt, v.y, o[e + 1]);
+    }
+  }
+  __syncthreads();  // every warp has read s_x
+#pragma unroll
+  for (int e = 0; e < E; ++e) s_o[w][E * lane + e] = o[e];
+  if (lane == 0) s_x[w] = L;
+  __syncthreads();
+  if (w != 0) return;
+  L = 0.f;
+#pragma unroll
+  for (int i = 0; i < kWideWarps; ++i) L += s_x[i];
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    float v = 0.f;
+#pragma unroll
+    for (int i = 0; i < kWideWarps; ++i) v += s_o[i][E * lane + e];
+    o[e] = v;
+  }
+  finish_row<D>(PV, o, L, out + (int64_t)row * D, lane);
 }
 
 template <int D, int G>
@@ -394,6 +450,16 @@ int decode_combine(const CodecParams& PV, const float* part, int n_split, uint16
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cudaError_t e;
+  if (n_split > 64 / (PV.d / 32)) {   // beyond the narrow kernel's preload window
+    cfg.gridDim = dim3((unsigned)rows);
+    cfg.blockDim = dim3(kWideWarps * 32);
+    switch (PV.d) {
+      case 64: e = cudaLaunchKernelEx(&cfg, decode_combine_wide_kernel<64>, PV, part, n_split, out); break;
+      case 128: e = cudaLaunchKernelEx(&cfg, decode_combine_wide_kernel<128>, PV, part, n_split, out); break;
+      default: e = cudaLaunchKernelEx(&cfg, decode_combine_wide_kernel<256>, PV, part, n_split, out); break;
+    }
+    return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+  }
   switch (PV.d) {
     case 64: e = cudaLaunchKernelEx(&cfg, decode_combine_kernel<64>, PV, part, n_split, out, rows); break;
     case 128: e = cudaLaunchKernelEx(&cfg, decode_combine_kernel<128>, PV, part, n_split, out, rows); break;

@@ -713,29 +713,41 @@ __global__ void __launch_bounds__(kThreads, 4) decode_tc_kernel(const CodecParam
 }
 
 // S q of every (batch, q head) for QJL keys, times softmax_scale * log2 e *
-// sqrt(pi/2) / m, rounded to fp16, and the sum of each row of it.
+// sqrt(pi/2) / m, rounded to fp16, and the sum of each row of it.  One CTA
+// per (batch, KV head) serves its 4 q heads; thread i owns row i of S.
 __global__ void __launch_bounds__(kQjlM) qjl_prep_kernel(const uint16_t* __restrict__ q, const float* __restrict__ S,
                                                          int d, float coef, uint16_t* __restrict__ sq,
                                                          float* __restrict__ sqsum) {
-  __shared__ float s_q[kMaxDim];
-  __shared__ float s_red[kQjlM / 32];
-  const int row = blockIdx.x, i = threadIdx.x;
-  for (int j = i; j < d; j += kQjlM) s_q[j] = h2f(q[(int64_t)row * d + j]);
+  __shared__ float s_q[kG][kMaxDim];
+  __shared__ float s_red[kG][kQjlM / 32];
+  const int grp = blockIdx.x, i = threadIdx.x;  // rows grp*4 .. grp*4+3 of q
+  for (int e = i; e < kG * d; e += kQjlM) s_q[e / d][e % d] = h2f(q[(int64_t)grp * kG * d + e]);
   __syncthreads();
-  float v = 0.f;
-  for (int j = 0; j < d; ++j) v = fmaf(S[(int64_t)i * d + j], s_q[j], v);
-  const uint16_t h = f2h(v * coef);
-  sq[(int64_t)row * kQjlM + i] = h;
-  float r = h2f(h);
+  float v[kG] = {0.f, 0.f, 0.f, 0.f};
+  const float4* Si = reinterpret_cast<const float4*>(S + (int64_t)i * d);
+  for (int j4 = 0; j4 < d / 4; ++j4) {
+    const float4 sv = Si[j4];
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) r += __shfl_xor_sync(kFull, r, o);
-  if ((i & 31) == 0) s_red[i >> 5] = r;
+    for (int h = 0; h < kG; ++h) {
+      const float* qh = s_q[h] + 4 * j4;
+      v[h] = fmaf(sv.x, qh[0], fmaf(sv.y, qh[1], fmaf(sv.z, qh[2], fmaf(sv.w, qh[3], v[h]))));
+    }
+  }
+#pragma unroll
+  for (int h = 0; h < kG; ++h) {
+    const uint16_t hv = f2h(v[h] * coef);
+    sq[((int64_t)grp * kG + h) * kQjlM + i] = hv;
+    float r = h2f(hv);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) r += __shfl_xor_sync(kFull, r, o);
+    if ((i & 31) == 0) s_red[h][i >> 5] = r;
+  }
   __syncthreads();
-  if (i == 0) {
+  if (i < kG) {
     float tot = 0.f;
 #pragma unroll
-    for (int w = 0; w < kQjlM / 32; ++w) tot += s_red[w];
-    sqsum[row] = tot;
+    for (int w = 0; w < kQjlM / 32; ++w) tot += s_red[i][w];
+    sqsum[(int64_t)grp * kG + i] = tot;
   }
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 }
@@ -795,7 +807,7 @@ bool decode_tc_eligible(const CodecParams& PK, const CodecParams& PV, int G, int
   }
   if (!ok) return false;
   if (!aligned16(K->codes) || !aligned16(K->scales) || !aligned16(V->codes) || !aligned16(V->scales)) return false;
-  if (PK.m && (!aligned16(K->qjl_bits) || !aligned16(K->qjl_rnorm) || !K->S)) return false;
+  if (PK.m && (!aligned16(K->qjl_bits) || !aligned16(K->qjl_rnorm) || !K->S || !aligned16(K->S))) return false;
   return true;
 }
 
@@ -836,7 +848,7 @@ int launch_decode_tc(const CodecParams& PK, const CodecParams& PV, const tq_kv_v
     float* sqsum = reinterpret_cast<float*>(extra + (((size_t)B * Hq * kQjlM * 2 + 15) / 16) * 16);
     a.sq = sq;
     a.sqsum = sqsum;
-    qjl_prep_kernel<<<B * Hq, kQjlM, 0, st>>>(q, K->S, PK.d, qscale * kSqrtHalfPi / (float)PK.m, sq, sqsum);
+    qjl_prep_kernel<<<B * Hkv, kQjlM, 0, st>>>(q, K->S, PK.d, qscale * kSqrtHalfPi / (float)PK.m, sq, sqsum);
     if (cudaGetLastError() != cudaSuccess) return TQ_ERR_CUDA;
   }
   const bool kpv = PK.blk == PK.d, vpv = PV.blk == PV.d;

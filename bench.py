@@ -52,6 +52,12 @@ def _peaks():
         return 6800.0, "fallback"
 
 
+# DRAM bytes (read + write) of one decode_tc_kernel launch of the headline
+# workload, from the ncu capture summarised in
+# profiles/decode_tc_qwen3_8b_turbo3_ctx32768.md (None once the kernel changes).
+DECODE_TRAFFIC_BYTES = (235.011072 + 3.253504) * 1e6
+
+
 def decode_bytes(B, Hkv, ctx, d, k_bits, v_bits, k_block, v_block):
     """Algorithmic bytes of one decode pass: packed codes + fp16 scales of
     every K and V token of the context, each read once."""
@@ -232,7 +238,8 @@ def run_gpu(args, rank, world):
                        "parallelism": f"replicas x{world}"},
             "percent_of_peak": round(100 * value / world / peak, 2),
             "roofline": {"bound": "hbm", "achieved": round(value / world, 2), "peak": peak,
-                         "unit": "GB/s", "frac": round(value / world / peak, 4), "traffic": None,
+                         "unit": "GB/s", "frac": round(value / world / peak, 4),
+                         "traffic": DECODE_TRAFFIC_BYTES,
                          "peak_source": f"{peak_kind} hbm_gbs (burst copy)",
                          "kernel": "decode_tc_kernel + decode_combine_kernel (one tq_decode_attn call, events around both)"},
             "e2e": e2e,

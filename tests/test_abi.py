@@ -82,11 +82,18 @@ def test_host_side_argument_checks_need_no_gpu(tqlib):
     assert tqlib.tq_layout_sizes(ctypes.byref(bad), None, None, None) == -1
 
 
+def _decode_ws(B, Hq, d, ns):
+    # split partials [B*Hq][n_split][d + 4] fp32, rounded up to 256 bytes, then
+    # the tensor-core path's S q rows (fp16, m = 128) and row sums of QJL keys
+    part = B * Hq * ns * (d + 4) * 4
+    return (part + 255) // 256 * 256 + B * Hq * (128 * 2 + 4) + 256
+
+
 def test_decode_workspace_query(tqlib):
     nb, ns = tb.tq_decode_workspace_bytes(8, 32, 8, 128, 32768, 16)
-    assert ns == 16 and nb == 8 * 32 * 16 * (128 + 4) * 4
+    assert ns == 16 and nb == _decode_ws(8, 32, 128, 16)
     nb, ns = tb.tq_decode_workspace_bytes(1, 16, 4, 256, 131072, 0)
-    assert ns >= 1 and nb == 16 * ns * (256 + 4) * 4
+    assert ns >= 1 and nb == _decode_ws(1, 16, 256, ns)
     with pytest.raises(tb.TQError):
         tb.tq_decode_workspace_bytes(2, 6, 4, 128, 100)
 

@@ -389,7 +389,30 @@ def bench_extra(tb, torch, inputs, dev, args, which=None):
         out.update(_extra_d256(tb, torch, inputs, dev, flush, hbm, tflops, tsrc, steps, warm, which))
     if which in (None, "decode_qjl"):
         out.update(_extra_qjl(tb, torch, inputs, dev, flush, hbm, steps, warm))
+    if which in (None, "quantize_qjl"):
+        out.update(_extra_qjl_quantize(tb, torch, inputs, dev, flush, hbm, steps, warm))
     return out
+
+
+def _extra_qjl_quantize(tb, torch, inputs, dev, flush, hbm, steps, warm):
+    """Quantise the QJL-key workload's keys (B=4 x 8 KV heads x 16384 tokens,
+    d=128, 2-bit + QJL m=128): one call over all 524,288 vectors."""
+    w = inputs.qjl_decode_workload()
+    S = torch.from_numpy(w["S"]).to(dev)
+    L = tb.make_layout(128, 128, 2, 128, 0, 1)
+    k = torch.from_numpy(w["k"]).to(dev).reshape(-1, 128)
+    n = k.shape[0]
+    o = tb.tq_quantize_kv(L, k, S=S)
+    ms = _time(torch, lambda: tb.tq_quantize_kv(L, k, S=S, out=o), flush, steps, warm)
+    nbytes = n * (128 * 2 + 128 * 2 // 8 + 2 + 128 // 8 + 2)   # fp16 in; codes, norm, bits, rho out
+    gfma = n * 128 * 128 / 1e9
+    return {"quantize_qjl_keys_524288": {
+        "workload": "524,288 keys of d=128 (4 x 8 heads x 16384 tokens), 2-bit + QJL m=128, one norm per vector",
+        "ms": round(ms, 4), "Gvec/s": round(n / (ms * 1e-3) / 1e9, 3),
+        "projection_GFMA_per_s": round(gfma / (ms * 1e-3), 1),
+        "roofline": {"bound": "hbm", "achieved": round(nbytes / (ms * 1e-3) / 1e9, 1), "peak": hbm,
+                     "unit": "GB/s", "frac": round(nbytes / (ms * 1e-3) / 1e9 / hbm, 4),
+                     "bytes_per_vector": nbytes // n}}}
 
 
 def _extra_d256(tb, torch, inputs, dev, flush, hbm, tflops, tsrc, steps, warm, which):
@@ -537,7 +560,7 @@ def main():
     ap.add_argument("--no-extra", action="store_true", help="skip the other workloads (headline only)")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--only", default=None,
-                    choices=["decode", "quantize", "prefill", "decode_d256", "decode_qjl"],
+                    choices=["decode", "quantize", "prefill", "decode_d256", "decode_qjl", "quantize_qjl"],
                     help="time one workload alone and print its result only (profiler runs)")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -14,6 +14,9 @@ namespace tq {
 bool quantize_fast_eligible(const CodecParams& P, bool f32_input);
 int launch_quantize_fast(const CodecParams& P, const void* x, int64_t n_vec, int64_t stride, uint8_t* codes,
                          uint16_t* scales, cudaStream_t st);
+bool quantize_qjl_eligible(const CodecParams& P);
+int launch_quantize_qjl(const CodecParams& P, const void* x, bool f32, int64_t n_vec, int64_t stride, const float* S,
+                        uint8_t* codes, uint16_t* scales, uint8_t* qjl_bits, uint16_t* qjl_rnorm, cudaStream_t st);
 
 namespace {
 
@@ -313,6 +316,8 @@ extern "C" int tq_quantize_kv(const tq_layout* layout, const void* x, tq_dtype x
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool f32 = x_dtype == TQ_F32;
   if (tq::quantize_fast_eligible(P, f32)) return tq::launch_quantize_fast(P, x, n_vec, x_row_stride, codes, scales, s);
+  if (tq::quantize_qjl_eligible(P))
+    return tq::launch_quantize_qjl(P, x, f32, n_vec, x_row_stride, S, codes, scales, qjl_bits, qjl_rnorm, s);
   switch (P.d) {
     case 64: return tq::launch_quantize<64>(P, a, f32, s);
     case 128: return tq::launch_quantize<128>(P, a, f32, s);

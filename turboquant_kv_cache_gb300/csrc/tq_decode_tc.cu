@@ -35,6 +35,7 @@
 #include <math.h>
 
 #include "tq_device.cuh"
+#include "tq_lut.cuh"
 
 namespace tq {
 
@@ -201,115 +202,6 @@ __device__ __forceinline__ void copy_part(uint32_t dst, const uint8_t* base, int
       bytes = bytes < 0 ? 0 : (bytes > 16 ? 16 : bytes);
       cp16(dst + 16 * c, bytes ? src + 16 * c : base, bytes);
     }
-  }
-}
-
-// Nibble words (code k of chunk c in bits 4k..4k+2) of one 32-code group,
-// from its packed words w (see the layout in include/tq.h).
-template <int BITS>
-__device__ __forceinline__ void chunk_words(const uint32_t* w, uint32_t* n) {
-  if (BITS == 4) {
-    n[0] = w[0]; n[1] = w[1]; n[2] = w[2]; n[3] = w[3];
-  } else if (BITS == 3) {
-    n[0] = w[0] & 0x77777777u;
-    n[1] = w[1] & 0x77777777u;
-    n[2] = w[2] & 0x77777777u;
-    // chunk 3 rides in bit 3 of every nibble; the shifts run as high-half
-    // multiplies, off the integer logic pipe
-    n[3] = __umulhi(w[0] & 0x88888888u, 1u << 29) + __umulhi(w[1] & 0x88888888u, 1u << 30) +
-           __umulhi(w[2] & 0x88888888u, 1u << 31);
-  } else {
-    n[0] = w[0] & 0x33333333u;
-    n[1] = w[1] & 0x33333333u;
-    n[2] = __umulhi(w[0], 1u << 30) & 0x33333333u;
-    n[3] = __umulhi(w[1], 1u << 30) & 0x33333333u;
-  }
-}
-
-template <int BITS>
-__device__ __forceinline__ void load_group(uint32_t a, uint32_t* w) {
-  if (BITS == 4) {
-    const uint4 v = lds128(a);
-    w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
-  } else if (BITS == 3) {
-    w[0] = lds32(a); w[1] = lds32(a + 4); w[2] = lds32(a + 8);
-  } else {
-    const uint2 v = lds64(a);
-    w[0] = v.x; w[1] = v.y;
-  }
-}
-
-// Lookup tables of one codebook (optionally scaled): low and high bytes of
-// the fp16 values, entries 0-7 in t[0..3], entries 8-15 in t[4..7].
-struct Tab {
-  uint32_t t[8];
-};
-
-// fp16 centroid pairs (c0,c1), (c2,c3), ... of a codebook (up to 16 entries)
-template <int BITS>
-struct Cent {
-  uint32_t c2[(1 << BITS) / 2];
-};
-
-template <int BITS>
-__device__ __forceinline__ Cent<BITS> make_cent(const CodecParams& P) {
-  Cent<BITS> c;
-#pragma unroll
-  for (int k = 0; k < (1 << BITS) / 2; ++k)
-    c.c2[k] = (uint32_t)f2h(P.centroids[2 * k]) | ((uint32_t)f2h(P.centroids[2 * k + 1]) << 16);
-  return c;
-}
-
-// tables of the centroids times the fp16 norm s (s = 1.0 for unscaled)
-template <int BITS>
-__device__ __forceinline__ Tab make_tab(const Cent<BITS>& c, uint32_t s) {
-  const uint32_t s2 = s | (s << 16);
-  Tab T;
-  uint32_t h[8];
-#pragma unroll
-  for (int k = 0; k < (1 << BITS) / 2; ++k) h[k] = hmul2(c.c2[k], s2);
-  if (BITS == 2) {
-    T.t[0] = prmt(h[0], h[1], 0x6420);
-    T.t[2] = prmt(h[0], h[1], 0x7531);
-    T.t[1] = T.t[0];
-    T.t[3] = T.t[2];
-  } else {
-    T.t[0] = prmt(h[0], h[1], 0x6420);
-    T.t[1] = prmt(h[2], h[3], 0x6420);
-    T.t[2] = prmt(h[0], h[1], 0x7531);
-    T.t[3] = prmt(h[2], h[3], 0x7531);
-    if (BITS == 4) {
-      T.t[4] = prmt(h[4], h[5], 0x6420);
-      T.t[5] = prmt(h[6], h[7], 0x6420);
-      T.t[6] = prmt(h[4], h[5], 0x7531);
-      T.t[7] = prmt(h[6], h[7], 0x7531);
-    }
-  }
-  return T;
-}
-
-// Four fp16x2 registers (codes 0-1, 2-3, 4-5, 6-7) of a nibble word.
-template <int BITS>
-__device__ __forceinline__ void lut8(uint32_t n, const Tab& T, uint32_t* o) {
-#pragma unroll
-  for (int half = 0; half < 2; ++half) {
-    const uint32_t s = half ? __umulhi(n, 1u << 16) : n;
-    uint32_t lo, hi;
-    if (BITS == 4) {
-      const uint32_t s7 = s & 0x7777u;
-      const uint32_t lo0 = prmt(T.t[0], T.t[1], s7), hi0 = prmt(T.t[2], T.t[3], s7);
-      const uint32_t lo1 = prmt(T.t[4], T.t[5], s7), hi1 = prmt(T.t[6], T.t[7], s7);
-      // byte mask 0xff where bit 3 of the nibble is set: bit 3 moved to the
-      // byte-select bit 2 picks 0x00 / 0xff from the constant pair
-      const uint32_t m = prmt(0u, 0xffffffffu, __umulhi(s, 1u << 31));
-      lo = (lo0 & ~m) | (lo1 & m);
-      hi = (hi0 & ~m) | (hi1 & m);
-    } else {
-      lo = prmt(T.t[0], T.t[1], s);
-      hi = prmt(T.t[2], T.t[3], s);
-    }
-    o[2 * half] = prmt(lo, hi, 0x5140);
-    o[2 * half + 1] = prmt(lo, hi, 0x7362);
   }
 }
 

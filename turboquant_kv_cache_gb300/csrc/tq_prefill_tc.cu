@@ -25,6 +25,7 @@
 #include <math.h>
 
 #include "tq_device.cuh"
+#include "tq_lut.cuh"
 
 namespace tq {
 
@@ -125,50 +126,6 @@ __device__ __forceinline__ float ex2f(float x) {
 
 // fp16 centroid byte tables: lo/hi bytes of entries 0-3 / 4-7 (t[0..3]) and,
 // for 4-bit codebooks, of entries 8-11 / 12-15 (t[4..7]).
-struct Lut {
-  uint32_t t[8];
-};
-
-__device__ __forceinline__ Lut make_lut(const CodecParams& P) {
-  Lut L;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) L.t[i] = 0u;
-  const int K = 1 << P.bits;
-#pragma unroll
-  for (int k = 0; k < 16; ++k) {
-    if (k < K) {
-      const uint32_t h = f2h(P.centroids[k]);
-      const int half = k >> 3, q = (k & 7) >> 2, sh = 8 * (k & 3);
-      L.t[4 * half + q] |= (h & 0xffu) << sh;        // low bytes
-      L.t[4 * half + 2 + q] |= (h >> 8) << sh;       // high bytes
-    }
-  }
-  return L;
-}
-
-// fp16 values of the 4 codes in the low 16 bits of nibble word n.
-__device__ __forceinline__ void lut4(uint32_t n, const Lut& L, int bits, uint32_t& o01, uint32_t& o23) {
-  const uint32_t s = n & 0x7777u;
-  uint32_t lo = prmt(L.t[0], L.t[1], s);
-  uint32_t hi = prmt(L.t[2], L.t[3], s);
-  if (bits == 4) {
-    // codes 8-15 from the second table, chosen per byte by bit 3
-    const uint32_t lo2 = prmt(L.t[4], L.t[5], s);
-    const uint32_t hi2 = prmt(L.t[6], L.t[7], s);
-    const uint32_t m7 = prmt(0x80808080u, 0x80808080u, n & 0xffffu) ^ 0x80808080u;  // 0x7f where bit 3 set
-    const uint32_t m = m7 | (m7 << 1);
-    lo = (lo & ~m) | (lo2 & m);
-    hi = (hi & ~m) | (hi2 & m);
-  }
-  o01 = prmt(lo, hi, 0x5140);
-  o23 = prmt(lo, hi, 0x7362);
-}
-
-__device__ __forceinline__ uint32_t hmul2u(uint32_t a, __half2 b) {
-  const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&a), b);
-  return *reinterpret_cast<const uint32_t*>(&r);
-}
-
 // Packed bytes of tokens [t0, t0 + n) of one array (codes or scales; `sb`
 // bytes per token) staged into smem: the copy starts at the 16-byte boundary
 // at or below the first byte and never reads past the last byte needed.
@@ -207,57 +164,78 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
                : "memory");
 }
 
-// Nibble word (8 codes) of chunk w (0..3) of a 32-code group at shared
-// address g, for a compile-time bit width.
-template <int BITS>
-__device__ __forceinline__ uint32_t chunk_smem(uint32_t g, int w) {
-  if (BITS == 4) return lds32(g + 4 * w);
-  if (BITS == 3) {
-    if (w < 3) return lds32(g + 4 * w) & 0x77777777u;
-    return ((lds32(g) >> 3) & 0x11111111u) | ((lds32(g + 4) >> 2) & 0x22222222u) |
-           ((lds32(g + 8) >> 1) & 0x44444444u);
+// Decode one kTok-token tile from its staged packed bytes (shared addresses
+// codes / scales) into a core-matrix tile [kTok][D] at shared address tile:
+// rotated, scaled fp16; tokens >= n_valid become zeros.  Work items are
+// (token, 32-value group) pairs, so every thread runs the same instructions;
+// 8 consecutive items are 8 tokens of one group, which spread one 16-byte
+// store per lane over all banks.  Up to 3 bits the group's fp16 table is the
+// centroids times its norm; 4-bit codes multiply after the lookup.
+template <int D, int BITS>
+__device__ __forceinline__ void decode_tile_items(const CodecParams& P, const uint32_t* c2, const Tab& fixed,
+                                                  uint32_t codes, uint32_t scales, int n_valid, uint32_t tile,
+                                                  int tid) {
+  constexpr int G8 = D / 32;
+  constexpr int ITEMS = kTok * G8;
+#pragma unroll
+  for (int item = tid; item < ITEMS; item += kThrTcConst) {
+    const int tok = 8 * (item / (8 * G8)) + (item & 7);
+    const int grp = (item >> 3) % G8;
+    const uint32_t dst = tile + cm_off(tok, 32 * grp, D);
+    if (tok < n_valid) {
+      uint32_t w[4], n[4];
+#pragma unroll
+      for (int k = 0; k < BITS; ++k) w[k] = lds32(codes + tok * P.code_bytes + grp * 4 * BITS + 4 * k);
+      chunk_words<BITS>(w, n);
+      const uint32_t sc = lds16(scales + tok * P.nb * 2 + ((32 * grp) / P.blk) * 2);
+      Tab T;
+      uint32_t s2 = 0;
+      if (BITS == 4) {
+        T = fixed;
+        s2 = sc | (sc << 16);
+      } else {
+        T = make_tab_p<BITS>(c2, sc);
+      }
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t o[4];
+        lut8<BITS>(n[c], T, o);
+        if (BITS == 4) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) o[e] = lut_hmul2(o[e], s2);
+        }
+        sts128(dst + 128 * c, make_uint4(o[0], o[1], o[2], o[3]));
+      }
+    } else {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) sts128(dst + 128 * c, make_uint4(0u, 0u, 0u, 0u));
+    }
   }
-  if (BITS == 2) return w < 2 ? (lds32(g + 4 * w) & 0x33333333u) : ((lds32(g + 4 * (w - 2)) >> 2) & 0x33333333u);
-  return (lds32(g) >> w) & 0x11111111u;
 }
 
-// Decode one 64-token tile from its staged packed bytes (shared addresses
-// codes / scales) into a core-matrix tile [kTok][D] at shared address tile:
-// rotated, scaled fp16; tokens >= n_valid become zeros.  Thread tid always
-// decodes the same 8-code chunk (tid % (D/8)) of a set of tokens.
-template <int D, int BITS>
-__device__ __forceinline__ void decode_tile_bits(const CodecParams& P, const Lut& L, uint32_t codes, uint32_t scales,
-                                                 int n_valid, uint32_t tile, int tid) {
-  constexpr int CH = D / 8;
-  constexpr int TPASS = kThrTcConst / CH;     // tokens per pass
-  const int ch = tid % CH, tok0 = tid / CH;
-  const uint32_t grp = (uint32_t)((ch >> 2) * BITS * 4);
-  const int w = ch & 3;
-  const uint32_t sidx = (uint32_t)((ch * 8) / P.blk) * 2;
-#pragma unroll 2
-  for (int tok = tok0; tok < kTok; tok += TPASS) {
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (tok < n_valid) {
-      const uint32_t nib = chunk_smem<BITS>(codes + tok * P.code_bytes + grp, w);
-      const __half sc = __ushort_as_half(lds16(scales + tok * P.nb * 2 + sidx));
-      const __half2 sc2 = __halves2half2(sc, sc);
-      uint32_t a, b, c, d;
-      lut4(nib, L, BITS, a, b);
-      lut4(nib >> 16, L, BITS, c, d);
-      v = make_uint4(hmul2u(a, sc2), hmul2u(b, sc2), hmul2u(c, sc2), hmul2u(d, sc2));
-    }
-    sts128(tile + cm_off(tok, ch * 8, D), v);
-  }
+// One codebook in the forms the tile decoder uses: fp16 centroid pairs
+// (16 entries, unused ones zero) and, for 4-bit codes, the unscaled tables.
+struct CodeTabs {
+  uint32_t c2[8];
+  Tab fixed;
+};
+__device__ __forceinline__ CodeTabs make_code_tabs(const CodecParams& P) {
+  CodeTabs c;
+#pragma unroll
+  for (int k = 0; k < 8; ++k)
+    c.c2[k] = (uint32_t)f2h(P.centroids[2 * k]) | ((uint32_t)f2h(P.centroids[2 * k + 1]) << 16);
+  c.fixed = make_tab_p<4>(c.c2, 0x3C00u);
+  return c;
 }
 
 template <int D>
-__device__ __forceinline__ void decode_tile_smem(const CodecParams& P, const Lut& L, uint32_t codes, uint32_t scales,
-                                                 int n_valid, uint32_t tile, int tid) {
+__device__ __forceinline__ void decode_tile_smem(const CodecParams& P, const CodeTabs& ct, uint32_t codes,
+                                                 uint32_t scales, int n_valid, uint32_t tile, int tid) {
   switch (P.bits) {
-    case 4: decode_tile_bits<D, 4>(P, L, codes, scales, n_valid, tile, tid); break;
-    case 3: decode_tile_bits<D, 3>(P, L, codes, scales, n_valid, tile, tid); break;
-    case 2: decode_tile_bits<D, 2>(P, L, codes, scales, n_valid, tile, tid); break;
-    default: decode_tile_bits<D, 1>(P, L, codes, scales, n_valid, tile, tid); break;
+    case 4: decode_tile_items<D, 4>(P, ct.c2, ct.fixed, codes, scales, n_valid, tile, tid); break;
+    case 3: decode_tile_items<D, 3>(P, ct.c2, ct.fixed, codes, scales, n_valid, tile, tid); break;
+    case 2: decode_tile_items<D, 2>(P, ct.c2, ct.fixed, codes, scales, n_valid, tile, tid); break;
+    default: decode_tile_items<D, 1>(P, ct.c2, ct.fixed, codes, scales, n_valid, tile, tid); break;
   }
 }
 
@@ -332,7 +310,7 @@ __global__ void __launch_bounds__(kThrTc, 1) prefill_tc_kernel(const CodecParams
     asm volatile("cp.async.commit_group;\n" ::);
   };
   auto n_valid_of = [&](int tile) { return (int)imin64(kTok, t_hi - (t_lo + (int64_t)tile * kTok)); };
-  const Lut lk = make_lut(PK), lv = make_lut(PV);
+  const CodeTabs lk = make_code_tabs(PK), lv = make_code_tabs(PV);
 
   stage(0, 0);
   stage(1, 1);
@@ -422,16 +400,21 @@ __global__ void __launch_bounds__(kThrTc, 1) prefill_tc_kernel(const CodecParams
       TQ_LD32(lane_base + kColS, sv);
       TQ_LD32(lane_base + kColS + 32, sw);
       asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+      // columns [0, nv_row) of this tile are valid for this row (context end,
+      // causal limit); only tiles on a boundary need the mask
+      const int64_t lim = a.causal ? imin64(t_hi, pos + 1) : t_hi;
+      const int64_t room = lim - t0;
+      const int nv_row = row_ok ? (room <= 0 ? 0 : (room >= kTok ? kTok : (int)room)) : 0;
+      if (__any_sync(0xffffffffu, nv_row < kTok)) {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          if (c >= nv_row) sv[c] = __float_as_uint(-INFINITY);
+          if (c + 32 >= nv_row) sw[c] = __float_as_uint(-INFINITY);
+        }
+      }
       float mx = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < kTok; ++c) {
-        const int64_t tok = t0 + c;
-        const bool valid = row_ok && tok < t_hi && (!a.causal || tok <= pos);
-        float v = __uint_as_float(c < 32 ? sv[c] : sw[c - 32]);
-        v = valid ? v : -INFINITY;
-        if (c < 32) sv[c] = __float_as_uint(v); else sw[c - 32] = __float_as_uint(v);
-        mx = fmaxf(mx, v);
-      }
+      for (int c = 0; c < 32; ++c) mx = fmaxf(mx, fmaxf(__uint_as_float(sv[c]), __uint_as_float(sw[c])));
       const bool need = mx > m_run + kLazyP;
       if (__any_sync(0xffffffffu, need)) {
         const float m_new = need ? mx : m_run;
@@ -551,12 +534,26 @@ size_t tc_smem(int slot_bytes) {  // double-buffered decoded K and V tiles + two
 }  // namespace
 
 int prefill_tc_splits(int B, int Hkv, int G, int Tq, int64_t ctx) {
+  // One CTA per SM at a time: pick the context split that fills whole waves
+  // best (at least 90% of the last wave busy), preferring fewer splits, each
+  // split at least 4 tiles long.
   const int row_tiles = (Tq * G + kRowsTc - 1) / kRowsTc;
-  const int ctas = row_tiles * B * Hkv;
-  int want = sm_count() / (ctas > 0 ? ctas : 1);
+  const int64_t ctas = (int64_t)row_tiles * B * Hkv;
+  const int sms = sm_count();
   const int64_t max_by_len = (ctx + 4 * kTok - 1) / (4 * kTok);
-  if (want > max_by_len) want = (int)max_by_len;
-  return want < 1 ? 1 : want;
+  int best = 1;
+  double best_eff = 0.0;
+  for (int ns = 1; ns <= 32 && ns <= max_by_len; ++ns) {
+    const int64_t n = ctas * ns;
+    const int64_t waves = (n + sms - 1) / sms;
+    const double eff = (double)n / (double)(waves * sms);
+    if (eff > best_eff + 1e-9 && (ns == 1 || eff >= 0.9 || eff > best_eff + 0.05)) {
+      best = ns;
+      best_eff = eff;
+    }
+    if (eff >= 0.97) break;
+  }
+  return best;
 }
 
 size_t prefill_tc_workspace(int B, int Hq, int Hkv, int d, int Tq, int64_t ctx) {

@@ -164,6 +164,33 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
                : "memory");
 }
 
+// Per-thread constants of the tile decoder: the thread's (token, 32-value
+// group) work items and their byte offsets, the same for every tile.
+template <int D>
+struct ItemPlan {
+  static constexpr int G8 = D / 32;
+  static constexpr int N = (kTok * G8 + kThrTcConst - 1) / kThrTcConst;   // items per thread
+  int tok[N];
+  uint32_t code_off[N], sc_off[N], dst_off[N];
+};
+
+template <int D>
+__device__ __forceinline__ ItemPlan<D> make_plan(const CodecParams& P, int tid) {
+  ItemPlan<D> pl;
+  constexpr int G8 = D / 32;
+#pragma unroll
+  for (int k = 0; k < ItemPlan<D>::N; ++k) {
+    const int item = tid + k * kThrTcConst;
+    const int tok = 8 * (item / (8 * G8)) + (item & 7);
+    const int grp = (item >> 3) % G8;
+    pl.tok[k] = item < kTok * G8 ? tok : kTok;   // kTok: no item
+    pl.code_off[k] = (uint32_t)(tok * P.code_bytes + grp * 4 * P.bits);
+    pl.sc_off[k] = (uint32_t)(tok * P.nb * 2 + ((32 * grp) / P.blk) * 2);
+    pl.dst_off[k] = cm_off(tok, 32 * grp, D);
+  }
+  return pl;
+}
+
 // Decode one kTok-token tile from its staged packed bytes (shared addresses
 // codes / scales) into a core-matrix tile [kTok][D] at shared address tile:
 // rotated, scaled fp16; tokens >= n_valid become zeros.  Work items are
@@ -172,22 +199,18 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
 // store per lane over all banks.  Up to 3 bits the group's fp16 table is the
 // centroids times its norm; 4-bit codes multiply after the lookup.
 template <int D, int BITS>
-__device__ __forceinline__ void decode_tile_items(const CodecParams& P, const uint32_t* c2, const Tab& fixed,
-                                                  uint32_t codes, uint32_t scales, int n_valid, uint32_t tile,
-                                                  int tid) {
-  constexpr int G8 = D / 32;
-  constexpr int ITEMS = kTok * G8;
+__device__ __forceinline__ void decode_tile_items(const ItemPlan<D>& pl, const uint32_t* c2, const Tab& fixed,
+                                                  uint32_t codes, uint32_t scales, int n_valid, uint32_t tile) {
 #pragma unroll
-  for (int item = tid; item < ITEMS; item += kThrTcConst) {
-    const int tok = 8 * (item / (8 * G8)) + (item & 7);
-    const int grp = (item >> 3) % G8;
-    const uint32_t dst = tile + cm_off(tok, 32 * grp, D);
-    if (tok < n_valid) {
+  for (int k = 0; k < ItemPlan<D>::N; ++k) {
+    if (pl.tok[k] >= kTok) continue;   // only when kTok * D/32 is not a multiple of the thread count
+    const uint32_t dst = tile + pl.dst_off[k];
+    if (n_valid == kTok || pl.tok[k] < n_valid) {
       uint32_t w[4], n[4];
 #pragma unroll
-      for (int k = 0; k < BITS; ++k) w[k] = lds32(codes + tok * P.code_bytes + grp * 4 * BITS + 4 * k);
+      for (int b = 0; b < BITS; ++b) w[b] = lds32(codes + pl.code_off[k] + 4 * b);
       chunk_words<BITS>(w, n);
-      const uint32_t sc = lds16(scales + tok * P.nb * 2 + ((32 * grp) / P.blk) * 2);
+      const uint32_t sc = lds16(scales + pl.sc_off[k]);
       Tab T;
       uint32_t s2 = 0;
       if (BITS == 4) {
@@ -229,13 +252,13 @@ __device__ __forceinline__ CodeTabs make_code_tabs(const CodecParams& P) {
 }
 
 template <int D>
-__device__ __forceinline__ void decode_tile_smem(const CodecParams& P, const CodeTabs& ct, uint32_t codes,
-                                                 uint32_t scales, int n_valid, uint32_t tile, int tid) {
-  switch (P.bits) {
-    case 4: decode_tile_items<D, 4>(P, ct.c2, ct.fixed, codes, scales, n_valid, tile, tid); break;
-    case 3: decode_tile_items<D, 3>(P, ct.c2, ct.fixed, codes, scales, n_valid, tile, tid); break;
-    case 2: decode_tile_items<D, 2>(P, ct.c2, ct.fixed, codes, scales, n_valid, tile, tid); break;
-    default: decode_tile_items<D, 1>(P, ct.c2, ct.fixed, codes, scales, n_valid, tile, tid); break;
+__device__ __forceinline__ void decode_tile_smem(int bits, const ItemPlan<D>& pl, const CodeTabs& ct, uint32_t codes,
+                                                 uint32_t scales, int n_valid, uint32_t tile) {
+  switch (bits) {
+    case 4: decode_tile_items<D, 4>(pl, ct.c2, ct.fixed, codes, scales, n_valid, tile); break;
+    case 3: decode_tile_items<D, 3>(pl, ct.c2, ct.fixed, codes, scales, n_valid, tile); break;
+    case 2: decode_tile_items<D, 2>(pl, ct.c2, ct.fixed, codes, scales, n_valid, tile); break;
+    default: decode_tile_items<D, 1>(pl, ct.c2, ct.fixed, codes, scales, n_valid, tile); break;
   }
 }
 
@@ -264,12 +287,12 @@ __global__ void __launch_bounds__(kThrTc, 1) prefill_tc_kernel(const CodecParams
   constexpr uint32_t kTileBytes = kTok * D * 2;
   constexpr uint32_t kGroupBytes = (D / 8) * 128;   // one 8-row band of a [rows][D] core-matrix tile
   extern __shared__ __align__(1024) uint8_t smem[];
-  uint8_t* sK[2] = {smem, smem + kTileBytes};
-  uint8_t* sV[2] = {smem + 2 * kTileBytes, smem + 3 * kTileBytes};
-  uint8_t* sPk[2] = {smem + 4 * kTileBytes, smem + 4 * kTileBytes + a.slot_bytes};
-  const uint32_t aK[2] = {su32(sK[0]), su32(sK[1])};
-  const uint32_t aV[2] = {su32(sV[0]), su32(sV[1])};
-  const uint32_t aPk[2] = {su32(sPk[0]), su32(sPk[1])};
+  // buffers b = 0, 1: decoded K and V tiles, staged packed bytes
+  const uint32_t a_smem = su32(smem);
+  auto aK = [&](int kb) { return a_smem + (uint32_t)kb * kTileBytes; };
+  auto aV = [&](int kb) { return a_smem + (uint32_t)(2 + kb) * kTileBytes; };
+  auto aPk = [&](int kb) { return a_smem + 4 * kTileBytes + (uint32_t)(kb * a.slot_bytes); };
+  auto sPk = [&](int kb) { return smem + 4 * kTileBytes + kb * a.slot_bytes; };
   __shared__ __align__(8) uint64_t bar_s, bar_o;
   __shared__ uint32_t tmem_base;
   __shared__ int s_off[2][4];   // byte offsets of the staged arrays per slot
@@ -298,7 +321,7 @@ __global__ void __launch_bounds__(kThrTc, 1) prefill_tc_kernel(const CodecParams
     if (tile < n_tiles) {
       const int64_t t0 = t_lo + (int64_t)tile * kTok;
       const int n = (int)imin64(kTok, t_hi - t0);
-      uint8_t* base = sPk[slot];
+      uint8_t* base = sPk(slot);
       const int o0 = stage_bytes(base + a.slot.kc, a.kc, rec0 + t0, n, PK.code_bytes, tid, kThrTc);
       const int o1 = stage_bytes(base + a.slot.ks, a.ks, rec0 + t0, n, 2 * PK.nb, tid, kThrTc);
       const int o2 = stage_bytes(base + a.slot.vc, a.vc, rec0 + t0, n, PV.code_bytes, tid, kThrTc);
@@ -311,6 +334,8 @@ __global__ void __launch_bounds__(kThrTc, 1) prefill_tc_kernel(const CodecParams
   };
   auto n_valid_of = [&](int tile) { return (int)imin64(kTok, t_hi - (t_lo + (int64_t)tile * kTok)); };
   const CodeTabs lk = make_code_tabs(PK), lv = make_code_tabs(PV);
+  const ItemPlan<D> plk = make_plan<D>(PK, tid), plv = make_plan<D>(PV, tid);
+  const int kbits = PK.bits, vbits = PV.bits;
 
   stage(0, 0);
   stage(1, 1);
@@ -348,10 +373,10 @@ __global__ void __launch_bounds__(kThrTc, 1) prefill_tc_kernel(const CodecParams
   asm volatile("cp.async.wait_group 1;\n" ::);
   __syncthreads();
   if (n_tiles > 0) {
-    decode_tile_smem<D>(PK, lk, aPk[0] + a.slot.kc + s_off[0][0], aPk[0] + a.slot.ks + s_off[0][1], n_valid_of(0),
-                        aK[0], tid);
-    decode_tile_smem<D>(PV, lv, aPk[0] + a.slot.vc + s_off[0][2], aPk[0] + a.slot.vs + s_off[0][3], n_valid_of(0),
-                        aV[0], tid);
+    decode_tile_smem<D>(kbits, plk, lk, aPk(0) + a.slot.kc + s_off[0][0], aPk(0) + a.slot.ks + s_off[0][1], n_valid_of(0),
+                        aK(0));
+    decode_tile_smem<D>(vbits, plv, lv, aPk(0) + a.slot.vc + s_off[0][2], aPk(0) + a.slot.vs + s_off[0][3], n_valid_of(0),
+                        aV(0));
   }
   asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
   fence_before();
@@ -363,13 +388,13 @@ __global__ void __launch_bounds__(kThrTc, 1) prefill_tc_kernel(const CodecParams
   auto issue_s = [&](int kb) {   // S = Q^ (TMEM) K^(buffer kb)^T
 #pragma unroll 4
     for (int s = 0; s < D / 16; ++s)
-      mma_ts(tmem + kColS, tmem + kColQ + 8 * s, sdesc(aK[kb] + s * 256, 128, kGroupBytes), idesc_s, s > 0);
+      mma_ts(tmem + kColS, tmem + kColQ + 8 * s, sdesc(aK(kb) + s * 256, 128, kGroupBytes), idesc_s, s > 0);
     mma_commit(su32(&bar_s));
   };
   auto issue_o = [&](int vb, bool first) {   // O += P (TMEM) V^(buffer vb)
 #pragma unroll
     for (int s = 0; s < kTok / 16; ++s)
-      mma_ts(tmem + kColO, tmem + kColP + 8 * s, sdesc(aV[vb] + s * 2 * kGroupBytes, kGroupBytes, 128), idesc_o,
+      mma_ts(tmem + kColO, tmem + kColP + 8 * s, sdesc(aV(vb) + s * 2 * kGroupBytes, kGroupBytes, 128), idesc_o,
              (first && s == 0) ? 0 : 1);
     mma_commit(su32(&bar_o));
   };
@@ -386,12 +411,12 @@ __global__ void __launch_bounds__(kThrTc, 1) prefill_tc_kernel(const CodecParams
     asm volatile("cp.async.wait_group 1;\n" ::);    // tile t+1 staged (own copies)
     __syncthreads();
     if (t + 1 < n_tiles)
-      decode_tile_smem<D>(PK, lk, aPk[nxt] + a.slot.kc + s_off[nxt][0], aPk[nxt] + a.slot.ks + s_off[nxt][1],
-                          n_valid_of(t + 1), aK[nxt], tid);
+      decode_tile_smem<D>(kbits, plk, lk, aPk(nxt) + a.slot.kc + s_off[nxt][0], aPk(nxt) + a.slot.ks + s_off[nxt][1],
+                          n_valid_of(t + 1), aK(nxt));
     if (t >= 1) ok = ok && bar_wait(su32(&bar_o), (t - 1) & 1);          // O(t-1) done: P and V(nxt) free
     if (t + 1 < n_tiles)
-      decode_tile_smem<D>(PV, lv, aPk[nxt] + a.slot.vc + s_off[nxt][2], aPk[nxt] + a.slot.vs + s_off[nxt][3],
-                          n_valid_of(t + 1), aV[nxt], tid);
+      decode_tile_smem<D>(vbits, plv, lv, aPk(nxt) + a.slot.vc + s_off[nxt][2], aPk(nxt) + a.slot.vs + s_off[nxt][3],
+                          n_valid_of(t + 1), aV(nxt));
     if (row_warp) {
       ok = ok && bar_wait(su32(&bar_s), t & 1);                          // S(t) ready
       fence_after();

@@ -38,6 +38,7 @@ constexpr int kRowsTc = 128;     // query rows per CTA (TMEM lanes)
 constexpr int kThrTc = 256;      // 8 warps: all decode; warps 0-3 own the 128 TMEM rows
 constexpr int kThrTcConst = kThrTc;
 constexpr int kTok = 64;         // tokens per KV tile
+constexpr int kProducerWarps = 8;   // decoding warps of the warp-specialised kernel
 constexpr uint32_t kColS = 0, kColP = 64;
 // TMEM columns: S (64 fp32) at 0, P (64 fp16 = 32 columns) at 64, Q^ (D fp16
 // = D/2 columns) at 128, O (D fp32) after it; a power of two >= the total
@@ -166,21 +167,21 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
 
 // Per-thread constants of the tile decoder: the thread's (token, 32-value
 // group) work items and their byte offsets, the same for every tile.
-template <int D>
+template <int D, int NT = kThrTcConst>
 struct ItemPlan {
   static constexpr int G8 = D / 32;
-  static constexpr int N = (kTok * G8 + kThrTcConst - 1) / kThrTcConst;   // items per thread
+  static constexpr int N = (kTok * G8 + NT - 1) / NT;   // items per decoding thread
   int tok[N];
   uint32_t code_off[N], sc_off[N], dst_off[N];
 };
 
-template <int D>
-__device__ __forceinline__ ItemPlan<D> make_plan(const CodecParams& P, int tid) {
-  ItemPlan<D> pl;
+template <int D, int NT = kThrTcConst>
+__device__ __forceinline__ ItemPlan<D, NT> make_plan(const CodecParams& P, int tid) {
+  ItemPlan<D, NT> pl;
   constexpr int G8 = D / 32;
 #pragma unroll
-  for (int k = 0; k < ItemPlan<D>::N; ++k) {
-    const int item = tid + k * kThrTcConst;
+  for (int k = 0; k < ItemPlan<D, NT>::N; ++k) {
+    const int item = tid + k * NT;
     const int tok = 8 * (item / (8 * G8)) + (item & 7);
     const int grp = (item >> 3) % G8;
     pl.tok[k] = item < kTok * G8 ? tok : kTok;   // kTok: no item
@@ -198,11 +199,11 @@ __device__ __forceinline__ ItemPlan<D> make_plan(const CodecParams& P, int tid) 
 // 8 consecutive items are 8 tokens of one group, which spread one 16-byte
 // store per lane over all banks.  Up to 3 bits the group's fp16 table is the
 // centroids times its norm; 4-bit codes multiply after the lookup.
-template <int D, int BITS>
-__device__ __forceinline__ void decode_tile_items(const ItemPlan<D>& pl, const uint32_t* c2, const Tab& fixed,
+template <int D, int BITS, int NT>
+__device__ __forceinline__ void decode_tile_items(const ItemPlan<D, NT>& pl, const uint32_t* c2, const Tab& fixed,
                                                   uint32_t codes, uint32_t scales, int n_valid, uint32_t tile) {
 #pragma unroll
-  for (int k = 0; k < ItemPlan<D>::N; ++k) {
+  for (int k = 0; k < ItemPlan<D, NT>::N; ++k) {
     if (pl.tok[k] >= kTok) continue;   // only when kTok * D/32 is not a multiple of the thread count
     const uint32_t dst = tile + pl.dst_off[k];
     if (n_valid == kTok || pl.tok[k] < n_valid) {
@@ -251,14 +252,14 @@ __device__ __forceinline__ CodeTabs make_code_tabs(const CodecParams& P) {
   return c;
 }
 
-template <int D>
-__device__ __forceinline__ void decode_tile_smem(int bits, const ItemPlan<D>& pl, const CodeTabs& ct, uint32_t codes,
-                                                 uint32_t scales, int n_valid, uint32_t tile) {
+template <int D, int NT>
+__device__ __forceinline__ void decode_tile_smem(int bits, const ItemPlan<D, NT>& pl, const CodeTabs& ct,
+                                                 uint32_t codes, uint32_t scales, int n_valid, uint32_t tile) {
   switch (bits) {
-    case 4: decode_tile_items<D, 4>(pl, ct.c2, ct.fixed, codes, scales, n_valid, tile); break;
-    case 3: decode_tile_items<D, 3>(pl, ct.c2, ct.fixed, codes, scales, n_valid, tile); break;
-    case 2: decode_tile_items<D, 2>(pl, ct.c2, ct.fixed, codes, scales, n_valid, tile); break;
-    default: decode_tile_items<D, 1>(pl, ct.c2, ct.fixed, codes, scales, n_valid, tile); break;
+    case 4: decode_tile_items<D, 4, NT>(pl, ct.c2, ct.fixed, codes, scales, n_valid, tile); break;
+    case 3: decode_tile_items<D, 3, NT>(pl, ct.c2, ct.fixed, codes, scales, n_valid, tile); break;
+    case 2: decode_tile_items<D, 2, NT>(pl, ct.c2, ct.fixed, codes, scales, n_valid, tile); break;
+    default: decode_tile_items<D, 1, NT>(pl, ct.c2, ct.fixed, codes, scales, n_valid, tile); break;
   }
 }
 
@@ -373,9 +374,9 @@ __global__ void __launch_bounds__(kThrTc, 1) prefill_tc_kernel(const CodecParams
   asm volatile("cp.async.wait_group 1;\n" ::);
   __syncthreads();
   if (n_tiles > 0) {
-    decode_tile_smem<D>(kbits, plk, lk, aPk(0) + a.slot.kc + s_off[0][0], aPk(0) + a.slot.ks + s_off[0][1], n_valid_of(0),
+    decode_tile_smem<D, kThrTcConst>(kbits, plk, lk, aPk(0) + a.slot.kc + s_off[0][0], aPk(0) + a.slot.ks + s_off[0][1], n_valid_of(0),
                         aK(0));
-    decode_tile_smem<D>(vbits, plv, lv, aPk(0) + a.slot.vc + s_off[0][2], aPk(0) + a.slot.vs + s_off[0][3], n_valid_of(0),
+    decode_tile_smem<D, kThrTcConst>(vbits, plv, lv, aPk(0) + a.slot.vc + s_off[0][2], aPk(0) + a.slot.vs + s_off[0][3], n_valid_of(0),
                         aV(0));
   }
   asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
@@ -411,11 +412,11 @@ __global__ void __launch_bounds__(kThrTc, 1) prefill_tc_kernel(const CodecParams
     asm volatile("cp.async.wait_group 1;\n" ::);    // tile t+1 staged (own copies)
     __syncthreads();
     if (t + 1 < n_tiles)
-      decode_tile_smem<D>(kbits, plk, lk, aPk(nxt) + a.slot.kc + s_off[nxt][0], aPk(nxt) + a.slot.ks + s_off[nxt][1],
+      decode_tile_smem<D, kThrTcConst>(kbits, plk, lk, aPk(nxt) + a.slot.kc + s_off[nxt][0], aPk(nxt) + a.slot.ks + s_off[nxt][1],
                           n_valid_of(t + 1), aK(nxt));
     if (t >= 1) ok = ok && bar_wait(su32(&bar_o), (t - 1) & 1);          // O(t-1) done: P and V(nxt) free
     if (t + 1 < n_tiles)
-      decode_tile_smem<D>(vbits, plv, lv, aPk(nxt) + a.slot.vc + s_off[nxt][2], aPk(nxt) + a.slot.vs + s_off[nxt][3],
+      decode_tile_smem<D, kThrTcConst>(vbits, plv, lv, aPk(nxt) + a.slot.vc + s_off[nxt][2], aPk(nxt) + a.slot.vs + s_off[nxt][3],
                           n_valid_of(t + 1), aV(nxt));
     if (row_warp) {
       ok = ok && bar_wait(su32(&bar_s), t & 1);                          // S(t) ready
@@ -521,6 +522,281 @@ __global__ void __launch_bounds__(kThrTc, 1) prefill_tc_kernel(const CodecParams
   }
 }
 
+// Warp-specialised prefill: warps 0-3 (consumers) own the 128 TMEM rows, run
+// the softmax and (one thread) issue the MMAs; the NP producer warps stage
+// the packed bytes and decode K/V tiles into double buffers.  Handoffs go
+// through mbarriers: kfull/vfull (a decoded tile is in buffer b; the
+// producers arrive), kfree/vfree (the MMA that read buffer b is done; a
+// tcgen05.commit arrives), s_done / o_done (S(t) written / O(t) done).  Every
+// barrier is waited on at most one phase behind its last completion, so a
+// parity wait is never confused by a later phase.  Waits are bounded: a wait
+// that gives up raises a CTA-wide abort flag, after which the roles run out
+// their loops (keeping the named-barrier counts) without further work.
+template <int D, int NP>
+__global__ void __launch_bounds__(128 + 32 * NP, 1) prefill_ws_kernel(const CodecParams PK, const CodecParams PV,
+                                                                      const PrefillTcArgs a) {
+  constexpr int kThr = 128 + 32 * NP;
+  constexpr int kProd = 32 * NP;
+  constexpr uint32_t kTmemCols = tmem_cols<D>();
+  constexpr uint32_t kColQ = 128;
+  constexpr uint32_t kColO = col_o<D>();
+  constexpr uint32_t kTileBytes = kTok * D * 2;
+  constexpr uint32_t kGroupBytes = (D / 8) * 128;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  __shared__ __align__(8) uint64_t bars[10];   // kfull[2], vfull[2], kfree[2], vfree[2], s_done, o_done
+  __shared__ uint32_t tmem_base;
+  __shared__ int s_off[2][4];
+  __shared__ volatile int s_abort;
+
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const bool consumer = warp < 4;
+  const int G = a.Hq / a.Hkv;
+  const int rt = blockIdx.x, split = blockIdx.y, bh = blockIdx.z;
+  const int b = bh / a.Hkv, kvh = bh % a.Hkv;
+  const int R = a.Tq * G;
+  const int row = rt * kRowsTc + (tid & 127);
+  const bool row_ok = consumer && row < R;
+  const int qi = row < R ? row / G : a.Tq - 1;
+  const int64_t pos = a.ctx - a.Tq + qi;
+  const int last_row = min(rt * kRowsTc + kRowsTc, R) - 1;
+  const int64_t max_pos = a.causal ? a.ctx - a.Tq + last_row / G : a.ctx - 1;
+  const int64_t t_lo = (int64_t)split * a.per;
+  const int64_t t_hi = imin64(imin64(t_lo + a.per, a.ctx), max_pos + 1);
+  const int n_tiles = t_hi > t_lo ? (int)((t_hi - t_lo + kTok - 1) / kTok) : 0;
+  const int64_t rec0 = (int64_t)bh * a.S_cap;
+
+  const uint32_t a_smem = su32(smem);
+  auto aK = [&](int kb) { return a_smem + (uint32_t)kb * kTileBytes; };
+  auto aV = [&](int kb) { return a_smem + (uint32_t)(2 + kb) * kTileBytes; };
+  auto aPk = [&](int kb) { return a_smem + 4 * kTileBytes + (uint32_t)(kb * a.slot_bytes); };
+  uint8_t* const pk_base = smem + 4 * kTileBytes;
+  const uint32_t kfull = su32(&bars[0]), vfull = su32(&bars[2]), kfree = su32(&bars[4]), vfree = su32(&bars[6]);
+  const uint32_t s_done = su32(&bars[8]), o_done = su32(&bars[9]);
+  auto n_valid_of = [&](int tile) { return (int)imin64(kTok, t_hi - (t_lo + (int64_t)tile * kTok)); };
+  auto wait = [&](uint32_t bar, uint32_t parity) {
+    if (s_abort) return false;
+    if (bar_wait(bar, parity)) return true;
+    s_abort = 1;
+    return false;
+  };
+
+  if (tid == 0) {
+    s_abort = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(su32(&bars[i])), "r"(kProd) : "memory");
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(su32(&bars[4 + i])) : "memory");
+    }
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(s_done) : "memory");
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(o_done) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(su32(&tmem_base)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
+  }
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = tmem_base;
+
+  if (!consumer) {
+    // ================= producers: stage and decode
+    const int ptid = tid - 128;
+    const CodeTabs lk = make_code_tabs(PK), lv = make_code_tabs(PV);
+    const ItemPlan<D, kProd> plk = make_plan<D, kProd>(PK, ptid), plv = make_plan<D, kProd>(PV, ptid);
+    auto stage = [&](int tile) {
+      const int slot = tile & 1;
+      if (tile < n_tiles) {
+        const int64_t t0 = t_lo + (int64_t)tile * kTok;
+        const int n = (int)imin64(kTok, t_hi - t0);
+        uint8_t* base = pk_base + slot * a.slot_bytes;
+        const int o0 = stage_bytes(base + a.slot.kc, a.kc, rec0 + t0, n, PK.code_bytes, ptid, kProd);
+        const int o1 = stage_bytes(base + a.slot.ks, a.ks, rec0 + t0, n, 2 * PK.nb, ptid, kProd);
+        const int o2 = stage_bytes(base + a.slot.vc, a.vc, rec0 + t0, n, PV.code_bytes, ptid, kProd);
+        const int o3 = stage_bytes(base + a.slot.vs, a.vs, rec0 + t0, n, 2 * PV.nb, ptid, kProd);
+        if (ptid == 0) {
+          s_off[slot][0] = o0; s_off[slot][1] = o1; s_off[slot][2] = o2; s_off[slot][3] = o3;
+        }
+      }
+      asm volatile("cp.async.commit_group;\n" ::);
+    };
+    stage(0);
+    stage(1);
+    for (int t = 0; t < n_tiles; ++t) {
+      const int kb = t & 1;
+      const uint32_t use = (uint32_t)(t >> 1);   // use number of buffer kb
+      asm volatile("cp.async.wait_group 1;\n" ::);
+      asm volatile("bar.sync 1, %0;\n" ::"n"(kProd) : "memory");   // tile t staged (all producers' copies)
+      const int nv = n_valid_of(t);
+      if (t >= 2) wait(kfree + 8 * kb, (use - 1) & 1);   // S(t-2) has read K buffer kb
+      if (!s_abort)
+        decode_tile_smem<D, kProd>(PK.bits, plk, lk, aPk(kb) + a.slot.kc + s_off[kb][0],
+                                   aPk(kb) + a.slot.ks + s_off[kb][1], nv, aK(kb));
+      asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+      asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(kfull + 8 * kb) : "memory");
+      if (t >= 2) wait(vfree + 8 * kb, (use - 1) & 1);   // O(t-2) has read V buffer kb
+      if (!s_abort)
+        decode_tile_smem<D, kProd>(PV.bits, plv, lv, aPk(kb) + a.slot.vc + s_off[kb][2],
+                                   aPk(kb) + a.slot.vs + s_off[kb][3], nv, aV(kb));
+      asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+      asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(vfull + 8 * kb) : "memory");
+      asm volatile("bar.sync 1, %0;\n" ::"n"(kProd) : "memory");   // every producer is done with slot kb
+      stage(t + 2);
+    }
+    asm volatile("cp.async.wait_group 0;\n" ::);
+  } else {
+    // ================= consumers: softmax rows, one thread issues the MMAs
+    const uint32_t lane_base = tmem + ((uint32_t)(32 * warp) << 16);
+    {
+      const __half* src = a.qhat + ((int64_t)bh * a.R_pad + (int64_t)rt * kRowsTc + tid) * D;
+#pragma unroll 1
+      for (int c0 = 0; c0 < D / 2; c0 += 32) {
+        uint32_t w[32];
+#pragma unroll
+        for (int j = 0; j < 32; j += 4) {
+          const uint4 v = *reinterpret_cast<const uint4*>(src + 2 * (c0 + j));
+          w[j] = v.x; w[j + 1] = v.y; w[j + 2] = v.z; w[j + 3] = v.w;
+        }
+        TQ_ST32(lane_base + kColQ + c0, w);
+      }
+      asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
+    }
+    fence_before();
+    asm volatile("bar.sync 2, 128;\n" ::: "memory");
+    fence_after();
+    const uint32_t idesc_s = (1u << 4) | ((uint32_t)(kTok >> 3) << 17) | ((uint32_t)(kRowsTc >> 4) << 24);
+    const uint32_t idesc_o = (1u << 4) | (1u << 16) | ((uint32_t)(D >> 3) << 17) | ((uint32_t)(kRowsTc >> 4) << 24);
+    auto issue_s = [&](int t) {   // S = Q^ (TMEM) K^(buffer)^T, once K(t) is decoded
+      const int kb = t & 1;
+      if (!wait(kfull + 8 * kb, (uint32_t)(t >> 1) & 1)) return;
+      fence_after();
+#pragma unroll 4
+      for (int s = 0; s < D / 16; ++s)
+        mma_ts(tmem + kColS, tmem + kColQ + 8 * s, sdesc(aK(kb) + s * 256, 128, kGroupBytes), idesc_s, s > 0);
+      mma_commit(s_done);
+      mma_commit(kfree + 8 * kb);
+    };
+    auto issue_o = [&](int t) {   // O += P (TMEM) V^(buffer), once V(t) is decoded
+      const int kb = t & 1;
+      if (!wait(vfull + 8 * kb, (uint32_t)(t >> 1) & 1)) return;
+      fence_after();
+#pragma unroll
+      for (int s = 0; s < kTok / 16; ++s)
+        mma_ts(tmem + kColO, tmem + kColP + 8 * s, sdesc(aV(kb) + s * 2 * kGroupBytes, kGroupBytes, 128), idesc_o,
+               (t == 0 && s == 0) ? 0 : 1);
+      mma_commit(o_done);
+      mma_commit(vfree + 8 * kb);
+    };
+    if (tid == 0 && n_tiles > 0) issue_s(0);
+    float m_run = -INFINITY, l_run = 0.f;
+    for (int t = 0; t < n_tiles; ++t) {
+      const int64_t t0 = t_lo + (int64_t)t * kTok;
+      uint32_t sv[32], sw[32];
+      const bool have_s = wait(s_done, (uint32_t)t & 1);   // S(t) written
+      fence_after();
+      if (have_s) {
+        TQ_LD32(lane_base + kColS, sv);
+        TQ_LD32(lane_base + kColS + 32, sw);
+        asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+      } else {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) sv[c] = sw[c] = __float_as_uint(-INFINITY);
+      }
+      const int64_t lim = a.causal ? imin64(t_hi, pos + 1) : t_hi;
+      const int64_t room = lim - t0;
+      const int nv_row = row_ok ? (room <= 0 ? 0 : (room >= kTok ? kTok : (int)room)) : 0;
+      if (__any_sync(0xffffffffu, nv_row < kTok)) {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          if (c >= nv_row) sv[c] = __float_as_uint(-INFINITY);
+          if (c + 32 >= nv_row) sw[c] = __float_as_uint(-INFINITY);
+        }
+      }
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 32; ++c) mx = fmaxf(mx, fmaxf(__uint_as_float(sv[c]), __uint_as_float(sw[c])));
+      // O(t-1) must be done before P is rewritten or O rescaled
+      if (t >= 1) wait(o_done, (uint32_t)(t - 1) & 1);
+      fence_after();
+      const bool need = mx > m_run + kLazyP;
+      if (__any_sync(0xffffffffu, need)) {
+        const float m_new = need ? mx : m_run;
+        const float alpha = (need && m_run != -INFINITY) ? ex2f(m_run - m_new) : 1.f;
+        m_run = m_new;
+        l_run *= alpha;
+        if (t >= 1) {
+#pragma unroll 1
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t ov[32];
+            TQ_LD32(lane_base + kColO + c0, ov);
+            asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+#pragma unroll
+            for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * alpha);
+            TQ_ST32(lane_base + kColO + c0, ov);
+          }
+        }
+      }
+      const float mref = m_run == -INFINITY ? 0.f : m_run;
+      uint32_t pw[32];
+      float sum = 0.f;
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        const float p0 = ex2f(__uint_as_float(c < 16 ? sv[2 * c] : sw[2 * c - 32]) - mref);
+        const float p1 = ex2f(__uint_as_float(c < 16 ? sv[2 * c + 1] : sw[2 * c + 1 - 32]) - mref);
+        sum += p0 + p1;
+        const __half2 h = __floats2half2_rn(p0, p1);
+        pw[c] = *reinterpret_cast<const uint32_t*>(&h);
+      }
+      l_run += sum;
+      TQ_ST32(lane_base + kColP, pw);
+      asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
+      fence_before();
+      asm volatile("bar.sync 2, 128;\n" ::: "memory");   // P(t) complete, S(t) read by every row
+      fence_after();
+      if (tid == 0 && !s_abort) {
+        issue_o(t);
+        if (t + 1 < n_tiles) issue_s(t + 1);
+      }
+    }
+    if (n_tiles > 0) wait(o_done, (uint32_t)(n_tiles - 1) & 1);
+    fence_after();
+    const bool ok = !s_abort;
+    const int h = kvh * G + row % G;
+    float* dst = a.part + ((((int64_t)b * a.Hq + h) * a.Tq + qi) * a.n_split + split) * (D + 4);
+    if (ok && n_tiles > 0) {
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t ov[32];
+        TQ_LD32(lane_base + kColO + c0, ov);
+        asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+        if (row_ok) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) dst[2 + c0 + j] = __uint_as_float(ov[j]);
+          if (c0 == 0) {
+            dst[0] = m_run;
+            dst[1] = l_run;
+          }
+        }
+      }
+    } else if (row_ok) {
+      dst[0] = -INFINITY;
+      dst[1] = 0.f;
+      for (int j = 0; j < D; ++j) dst[2 + j] = 0.f;
+    }
+  }
+  // the combine kernel may be scheduled now; it waits for this grid to finish
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+  fence_before();
+  __syncthreads();
+  if (tid == 0 && s_abort) atomicExch(a.err, 1);
+  if (warp == 0) {
+    fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(kTmemCols) : "memory");
+  }
+}
+
 // Q^ = (H D q per K block) * softmax_scale * log2 e, fp16, rows i*G + h of
 // each (batch, KV head), zero padded to R_pad rows.
 template <int D>
@@ -622,25 +898,28 @@ int launch_prefill_tc(const CodecParams& PK, const CodecParams& PV, const uint8_
     case 64: {
       prefill_rotate_q_kernel<64><<<qgrid, 64, 0, st>>>(PK, q, qhat, Hq, Hkv, Tq, R_pad, qscale);
       const size_t sm = tc_smem<64>(slot_bytes);
-      if (cudaFuncSetAttribute(prefill_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm))
+      if (cudaFuncSetAttribute(prefill_ws_kernel<64, kProducerWarps>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)sm))
         return TQ_ERR_CUDA;
-      prefill_tc_kernel<64><<<grid, kThrTc, sm, st>>>(PK, PV, a);
+      prefill_ws_kernel<64, kProducerWarps><<<grid, 128 + 32 * kProducerWarps, sm, st>>>(PK, PV, a);
       break;
     }
     case 128: {
       prefill_rotate_q_kernel<128><<<qgrid, 128, 0, st>>>(PK, q, qhat, Hq, Hkv, Tq, R_pad, qscale);
       const size_t sm = tc_smem<128>(slot_bytes);
-      if (cudaFuncSetAttribute(prefill_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm))
+      if (cudaFuncSetAttribute(prefill_ws_kernel<128, kProducerWarps>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)sm))
         return TQ_ERR_CUDA;
-      prefill_tc_kernel<128><<<grid, kThrTc, sm, st>>>(PK, PV, a);
+      prefill_ws_kernel<128, kProducerWarps><<<grid, 128 + 32 * kProducerWarps, sm, st>>>(PK, PV, a);
       break;
     }
     default: {
       prefill_rotate_q_kernel<256><<<qgrid, 256, 0, st>>>(PK, q, qhat, Hq, Hkv, Tq, R_pad, qscale);
       const size_t sm = tc_smem<256>(slot_bytes);
-      if (cudaFuncSetAttribute(prefill_tc_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm))
+      if (cudaFuncSetAttribute(prefill_ws_kernel<256, kProducerWarps>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)sm))
         return TQ_ERR_CUDA;
-      prefill_tc_kernel<256><<<grid, kThrTc, sm, st>>>(PK, PV, a);
+      prefill_ws_kernel<256, kProducerWarps><<<grid, 128 + 32 * kProducerWarps, sm, st>>>(PK, PV, a);
       break;
     }
   }

@@ -2,19 +2,20 @@
 // (tcgen05, TMEM accumulators).
 //
 // Rows: every (batch, KV head) owns R = Tq*G query rows (query i, head h ->
-// row i*G + h).  A CTA takes 128 rows (one per thread and per TMEM lane) and
-// one slice of the context, walking it in 64-token tiles:
-//   * the tile's K and V records are decoded by all 128 threads into shared
-//     memory (rotated domain, centroid * block norm, fp16) in the canonical
-//     no-swizzle core-matrix layout (8 rows x 16 bytes per core matrix), which
-//     serves K as a K-major B operand of S = Q K^T and V as an MN-major B
-//     operand of O = P V; both tiles are double-buffered so the decode of the
-//     next tile overlaps the MMAs of the current one;
-//   * one thread issues S = Q^ K^^T (M 128, N 64, K d) into TMEM;
-//   * each thread reads its row of S, applies the causal / context mask and
-//     an online softmax in base 2 (the reference max moves only when a score
-//     exceeds it by more than 2^8), writes P as fp16 back into TMEM;
-//   * one thread issues O += P V^ (A = P from TMEM, M 128, N d, K 64).
+// row i*G + h).  A CTA takes 128 rows (one per consumer thread and per TMEM
+// lane) and one slice of the context, walking it in 64-token tiles, with two
+// warp roles:
+//   * producer warps stage the packed K/V bytes with cp.async and decode each
+//     tile into shared memory (rotated domain, centroid * block norm, fp16)
+//     in the canonical no-swizzle core-matrix layout (8 rows x 16 bytes per
+//     core matrix), which serves K as a K-major B operand of S = Q K^T and V
+//     as an MN-major B operand of O = P V; K and V tiles are double-buffered,
+//     so decoding runs ahead of the MMAs;
+//   * consumer warps: one thread issues S = Q^ K^^T (M 128, N 64, K d) into
+//     TMEM and O += P V^ (A = P from TMEM, M 128, N d, K 64); each consumer
+//     thread reads its row of S, applies the causal / context mask and an
+//     online softmax in base 2 (the reference max moves only when a score
+//     exceeds it by more than 2^8) and writes P as fp16 back into TMEM.
 // Q^ = H D q per K block times softmax_scale * log2 e is prepared once per
 // call by a small kernel.  Partial (m, l, O) per row and context slice go to
 // the workspace in the decode-split format, and the decode combine kernel
@@ -35,17 +36,19 @@ int sm_count();
 namespace {
 
 constexpr int kRowsTc = 128;     // query rows per CTA (TMEM lanes)
-constexpr int kThrTc = 256;      // 8 warps: all decode; warps 0-3 own the 128 TMEM rows
-constexpr int kThrTcConst = kThrTc;
 constexpr int kTok = 64;         // tokens per KV tile
-constexpr int kProducerWarps = 8;   // decoding warps of the warp-specialised kernel
+constexpr int kProducerWarps = 8;   // decoding warps without register rebalancing
+constexpr int kProducerWarpsRB = 16; // decoding warps with setmaxnreg rebalancing
+constexpr int kConsRegs = 128, kDecRegs = 88;
 constexpr uint32_t kColS = 0, kColP = 64;
-// TMEM columns: S (64 fp32) at 0, P (64 fp16 = 32 columns) at 64, Q^ (D fp16
-// = D/2 columns) at 128, O (D fp32) after it; a power of two >= the total
+// TMEM columns: S (64 fp32) at 0, two P buffers (64 fp16 = 32 columns each) at
+// 64 and 96, Q^ (D fp16 = D/2 columns) at 128, O (D fp32) after it; a power
+// of two >= the total (exactly 512 at head_dim 256)
 template <int D> __host__ __device__ constexpr uint32_t col_o() { return 128u + D / 2; }
 template <int D> __host__ __device__ constexpr uint32_t tmem_cols() { return col_o<D>() + D <= 256u ? 256u : 512u; }
 constexpr float kLazyP = 8.0f;
-constexpr int kWaitLimit = 1 << 24;
+constexpr uint32_t kSuspendNs = 1000000;        // try_wait sleep hint
+constexpr uint64_t kWaitNs = 2000000000ull;     // give up a wait after 2 s
 
 __device__ __forceinline__ uint32_t su32(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
 
@@ -61,13 +64,6 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t
          ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | ((uint64_t)1 << 46);
 }
 
-__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, int acc) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
-      "l"(a), "l"(b), "r"(idesc), "r"(acc)
-      : "memory");
-}
-
 __device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, int acc) {
   asm volatile(
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d),
@@ -79,15 +75,32 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(bar) : "memory");
 }
 
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait for the phase of parity `phase` of an mbarrier.  The thread sleeps in
+// try_wait (suspend-time hint 1 ms; it wakes as soon as the phase completes)
+// instead of spinning; the whole wait is bounded by kWaitNs of wall time.
 __device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t phase) {
   uint32_t done = 0;
-  for (int it = 0; it < kWaitLimit && !done; ++it)
+  uint64_t t0 = 0;
+  for (int it = 0; !done; ++it) {
     asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
         : "=r"(done)
-        : "r"(bar), "r"(phase)
+        : "r"(bar), "r"(phase), "r"(kSuspendNs)
         : "memory");
-  return done != 0;
+    if (done) break;
+    if (it == 0) {
+      t0 = global_ns();
+    } else if (global_ns() - t0 > kWaitNs) {
+      return false;
+    }
+  }
+  return true;
 }
 
 __device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
@@ -113,11 +126,6 @@ __device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::aft
       "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])                                                   \
       : "memory")
 
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
-  uint32_t d;
-  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
-  return d;
-}
 
 __device__ __forceinline__ float ex2f(float x) {
   float y;
@@ -127,29 +135,6 @@ __device__ __forceinline__ float ex2f(float x) {
 
 // fp16 centroid byte tables: lo/hi bytes of entries 0-3 / 4-7 (t[0..3]) and,
 // for 4-bit codebooks, of entries 8-11 / 12-15 (t[4..7]).
-// Packed bytes of tokens [t0, t0 + n) of one array (codes or scales; `sb`
-// bytes per token) staged into smem: the copy starts at the 16-byte boundary
-// at or below the first byte and never reads past the last byte needed.
-// Returns the offset of the first byte inside the staging area.
-__device__ __forceinline__ int stage_bytes(uint8_t* dst, const uint8_t* src_base, int64_t first_rec, int n, int sb,
-                                           int tid, int nthr) {
-  const int64_t s = first_rec * sb, e = s + (int64_t)n * sb;
-  const int64_t s0 = s & ~(int64_t)15;
-  const int chunks = (int)((e - s0 + 15) >> 4);
-  for (int c = tid; c < chunks; c += nthr) {
-    const int64_t at = s0 + 16 * (int64_t)c;
-    const int64_t rem = e - at;
-    const int bytes = rem >= 16 ? 16 : (int)rem;
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 16, %2;\n" ::"r"(su32(dst + 16 * c)), "l"(src_base + at),
-                 "r"(bytes));
-  }
-  return (int)(s - s0);
-}
-
-struct PackedSlot {   // offsets of the four arrays inside one staging slot
-  int kc, ks, vc, vs;
-};
-
 __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
   uint32_t v;
   asm volatile("ld.shared.b32 %0, [%1];\n" : "=r"(v) : "r"(addr));
@@ -167,7 +152,7 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
 
 // Per-thread constants of the tile decoder: the thread's (token, 32-value
 // group) work items and their byte offsets, the same for every tile.
-template <int D, int NT = kThrTcConst>
+template <int D, int NT>
 struct ItemPlan {
   static constexpr int G8 = D / 32;
   static constexpr int N = (kTok * G8 + NT - 1) / NT;   // items per decoding thread
@@ -175,7 +160,7 @@ struct ItemPlan {
   uint32_t code_off[N], sc_off[N], dst_off[N];
 };
 
-template <int D, int NT = kThrTcConst>
+template <int D, int NT>
 __device__ __forceinline__ ItemPlan<D, NT> make_plan(const CodecParams& P, int tid) {
   ItemPlan<D, NT> pl;
   constexpr int G8 = D / 32;
@@ -192,26 +177,75 @@ __device__ __forceinline__ ItemPlan<D, NT> make_plan(const CodecParams& P, int t
   return pl;
 }
 
-// Decode one kTok-token tile from its staged packed bytes (shared addresses
-// codes / scales) into a core-matrix tile [kTok][D] at shared address tile:
-// rotated, scaled fp16; tokens >= n_valid become zeros.  Work items are
-// (token, 32-value group) pairs, so every thread runs the same instructions;
-// 8 consecutive items are 8 tokens of one group, which spread one 16-byte
-// store per lane over all banks.  Up to 3 bits the group's fp16 table is the
-// centroids times its norm; 4-bit codes multiply after the lookup.
-template <int D, int BITS, int NT>
-__device__ __forceinline__ void decode_tile_items(const ItemPlan<D, NT>& pl, const uint32_t* c2, const Tab& fixed,
-                                                  uint32_t codes, uint32_t scales, int n_valid, uint32_t tile) {
+// Packed words and fp16 norm of a thread's items of one tile, loaded from
+// global memory (read-only path) a tile ahead of their decode.
+template <int D, int NT>
+struct ItemRegs {
+  uint32_t w[ItemPlan<D, NT>::N][4];
+  uint32_t sc[ItemPlan<D, NT>::N];
+};
+
+__device__ __forceinline__ uint32_t ldg32(const uint8_t* p) {
+  uint32_t v;
+  asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint32_t ldg16(const uint8_t* p) {
+  unsigned short v;
+  asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
+  return v;
+}
+
+template <int D, int NT, int BITS>
+__device__ __forceinline__ void load_items_b(const ItemPlan<D, NT>& pl, const uint8_t* codes, const uint8_t* scales,
+                                             int n_valid, ItemRegs<D, NT>& r) {
 #pragma unroll
   for (int k = 0; k < ItemPlan<D, NT>::N; ++k) {
-    if (pl.tok[k] >= kTok) continue;   // only when kTok * D/32 is not a multiple of the thread count
+    if (pl.tok[k] < n_valid) {
+      const uint8_t* c = codes + pl.code_off[k];
+      if (BITS == 4) {
+        uint4 v;
+        asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                     : "l"(c));
+        r.w[k][0] = v.x; r.w[k][1] = v.y; r.w[k][2] = v.z; r.w[k][3] = v.w;
+      } else if (BITS == 2) {
+        uint2 v;
+        asm volatile("ld.global.nc.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(c));
+        r.w[k][0] = v.x; r.w[k][1] = v.y;
+      } else {
+#pragma unroll
+        for (int b = 0; b < BITS; ++b) r.w[k][b] = ldg32(c + 4 * b);
+      }
+      r.sc[k] = ldg16(scales + pl.sc_off[k]);
+    }
+  }
+}
+
+template <int D, int NT>
+__device__ __forceinline__ void load_items(int bits, const ItemPlan<D, NT>& pl, const uint8_t* codes,
+                                           const uint8_t* scales, int n_valid, ItemRegs<D, NT>& r) {
+  switch (bits) {
+    case 4: load_items_b<D, NT, 4>(pl, codes, scales, n_valid, r); break;
+    case 3: load_items_b<D, NT, 3>(pl, codes, scales, n_valid, r); break;
+    case 2: load_items_b<D, NT, 2>(pl, codes, scales, n_valid, r); break;
+    default: load_items_b<D, NT, 1>(pl, codes, scales, n_valid, r); break;
+  }
+}
+
+// Decode a thread's items of one tile from registers into the core-matrix
+// tile at shared address `tile` (same rules as decode_tile_items).
+template <int D, int NT, int BITS>
+__device__ __forceinline__ void decode_regs_b(const ItemPlan<D, NT>& pl, const ItemRegs<D, NT>& r, const uint32_t* c2,
+                                              const Tab& fixed, int n_valid, uint32_t tile) {
+#pragma unroll
+  for (int k = 0; k < ItemPlan<D, NT>::N; ++k) {
+    if (pl.tok[k] >= kTok) continue;
     const uint32_t dst = tile + pl.dst_off[k];
     if (n_valid == kTok || pl.tok[k] < n_valid) {
-      uint32_t w[4], n[4];
-#pragma unroll
-      for (int b = 0; b < BITS; ++b) w[b] = lds32(codes + pl.code_off[k] + 4 * b);
-      chunk_words<BITS>(w, n);
-      const uint32_t sc = lds16(scales + pl.sc_off[k]);
+      uint32_t n[4];
+      chunk_words<BITS>(r.w[k], n);
+      const uint32_t sc = r.sc[k];
       Tab T;
       uint32_t s2 = 0;
       if (BITS == 4) {
@@ -253,15 +287,16 @@ __device__ __forceinline__ CodeTabs make_code_tabs(const CodecParams& P) {
 }
 
 template <int D, int NT>
-__device__ __forceinline__ void decode_tile_smem(int bits, const ItemPlan<D, NT>& pl, const CodeTabs& ct,
-                                                 uint32_t codes, uint32_t scales, int n_valid, uint32_t tile) {
+__device__ __forceinline__ void decode_regs(int bits, const ItemPlan<D, NT>& pl, const ItemRegs<D, NT>& r,
+                                            const CodeTabs& ct, int n_valid, uint32_t tile) {
   switch (bits) {
-    case 4: decode_tile_items<D, 4, NT>(pl, ct.c2, ct.fixed, codes, scales, n_valid, tile); break;
-    case 3: decode_tile_items<D, 3, NT>(pl, ct.c2, ct.fixed, codes, scales, n_valid, tile); break;
-    case 2: decode_tile_items<D, 2, NT>(pl, ct.c2, ct.fixed, codes, scales, n_valid, tile); break;
-    default: decode_tile_items<D, 1, NT>(pl, ct.c2, ct.fixed, codes, scales, n_valid, tile); break;
+    case 4: decode_regs_b<D, NT, 4>(pl, r, ct.c2, ct.fixed, n_valid, tile); break;
+    case 3: decode_regs_b<D, NT, 3>(pl, r, ct.c2, ct.fixed, n_valid, tile); break;
+    case 2: decode_regs_b<D, NT, 2>(pl, r, ct.c2, ct.fixed, n_valid, tile); break;
+    default: decode_regs_b<D, NT, 1>(pl, r, ct.c2, ct.fixed, n_valid, tile); break;
   }
 }
+
 
 struct PrefillTcArgs {
   const uint8_t* kc;
@@ -274,279 +309,36 @@ struct PrefillTcArgs {
   int64_t S_cap, ctx;
   int Hq, Hkv, Tq, R_pad, n_split, causal;
   int64_t per;          // tokens per split (multiple of kTok)
-  int slot_bytes;       // one packed staging slot
-  PackedSlot slot;
 };
 
-
-template <int D>
-__global__ void __launch_bounds__(kThrTc, 1) prefill_tc_kernel(const CodecParams PK, const CodecParams PV,
-                                                               const PrefillTcArgs a) {
-  constexpr uint32_t kTmemCols = tmem_cols<D>();
-  constexpr uint32_t kColQ = 128;                 // Q^ as the A operand of S, D/2 columns
-  constexpr uint32_t kColO = col_o<D>();          // O accumulator, D columns
-  constexpr uint32_t kTileBytes = kTok * D * 2;
-  constexpr uint32_t kGroupBytes = (D / 8) * 128;   // one 8-row band of a [rows][D] core-matrix tile
-  extern __shared__ __align__(1024) uint8_t smem[];
-  // buffers b = 0, 1: decoded K and V tiles, staged packed bytes
-  const uint32_t a_smem = su32(smem);
-  auto aK = [&](int kb) { return a_smem + (uint32_t)kb * kTileBytes; };
-  auto aV = [&](int kb) { return a_smem + (uint32_t)(2 + kb) * kTileBytes; };
-  auto aPk = [&](int kb) { return a_smem + 4 * kTileBytes + (uint32_t)(kb * a.slot_bytes); };
-  auto sPk = [&](int kb) { return smem + 4 * kTileBytes + kb * a.slot_bytes; };
-  __shared__ __align__(8) uint64_t bar_s, bar_o;
-  __shared__ uint32_t tmem_base;
-  __shared__ int s_off[2][4];   // byte offsets of the staged arrays per slot
-
-  const int tid = threadIdx.x, warp = tid >> 5;
-  const bool row_warp = warp < 4;
-  const int G = a.Hq / a.Hkv;
-  const int rt = blockIdx.x;          // row tile
-  const int split = blockIdx.y;
-  const int bh = blockIdx.z;
-  const int b = bh / a.Hkv, kvh = bh % a.Hkv;
-  const int R = a.Tq * G;
-  const int row = rt * kRowsTc + (tid & 127);   // row of this thread (row warps)
-  const bool row_ok = row_warp && row < R;
-  const int qi = row < R ? row / G : a.Tq - 1;
-  const int64_t pos = a.ctx - a.Tq + qi;
-
-  const int last_row = min(rt * kRowsTc + kRowsTc, R) - 1;
-  const int64_t max_pos = a.causal ? a.ctx - a.Tq + last_row / G : a.ctx - 1;
-  const int64_t t_lo = (int64_t)split * a.per;
-  const int64_t t_hi = imin64(imin64(t_lo + a.per, a.ctx), max_pos + 1);
-  const int n_tiles = t_hi > t_lo ? (int)((t_hi - t_lo + kTok - 1) / kTok) : 0;
-  const int64_t rec0 = (int64_t)bh * a.S_cap;
-
-  auto stage = [&](int tile, int slot) {   // packed bytes of `tile` into staging slot `slot`
-    if (tile < n_tiles) {
-      const int64_t t0 = t_lo + (int64_t)tile * kTok;
-      const int n = (int)imin64(kTok, t_hi - t0);
-      uint8_t* base = sPk(slot);
-      const int o0 = stage_bytes(base + a.slot.kc, a.kc, rec0 + t0, n, PK.code_bytes, tid, kThrTc);
-      const int o1 = stage_bytes(base + a.slot.ks, a.ks, rec0 + t0, n, 2 * PK.nb, tid, kThrTc);
-      const int o2 = stage_bytes(base + a.slot.vc, a.vc, rec0 + t0, n, PV.code_bytes, tid, kThrTc);
-      const int o3 = stage_bytes(base + a.slot.vs, a.vs, rec0 + t0, n, 2 * PV.nb, tid, kThrTc);
-      if (tid == 0) {
-        s_off[slot][0] = o0; s_off[slot][1] = o1; s_off[slot][2] = o2; s_off[slot][3] = o3;
-      }
-    }
-    asm volatile("cp.async.commit_group;\n" ::);
-  };
-  auto n_valid_of = [&](int tile) { return (int)imin64(kTok, t_hi - (t_lo + (int64_t)tile * kTok)); };
-  const CodeTabs lk = make_code_tabs(PK), lv = make_code_tabs(PV);
-  const ItemPlan<D> plk = make_plan<D>(PK, tid), plv = make_plan<D>(PV, tid);
-  const int kbits = PK.bits, vbits = PV.bits;
-
-  stage(0, 0);
-  stage(1, 1);
-  if (tid == 0) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(su32(&bar_s)) : "memory");
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(su32(&bar_o)) : "memory");
-  }
-  if (warp == 0) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(su32(&tmem_base)),
-                 "r"(kTmemCols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
-  }
-  fence_before();
-  __syncthreads();
-  fence_after();
-  const uint32_t tmem = tmem_base;
-  const uint32_t lane_base = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
-  // Q^ rows into TMEM (A operand of S: 2 fp16 per column)
-  if (row_warp) {
-    const __half* src = a.qhat + ((int64_t)bh * a.R_pad + (int64_t)rt * kRowsTc + tid) * D;
-#pragma unroll 1
-    for (int c0 = 0; c0 < D / 2; c0 += 32) {
-      uint32_t w[32];
-#pragma unroll
-      for (int j = 0; j < 32; j += 4) {
-        const uint4 v = *reinterpret_cast<const uint4*>(src + 2 * (c0 + j));
-        w[j] = v.x; w[j + 1] = v.y; w[j + 2] = v.z; w[j + 3] = v.w;
-      }
-      TQ_ST32(lane_base + kColQ + c0, w);
-    }
-    asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
-  }
-  // tile 0 decoded before the first MMA
-  asm volatile("cp.async.wait_group 1;\n" ::);
-  __syncthreads();
-  if (n_tiles > 0) {
-    decode_tile_smem<D, kThrTcConst>(kbits, plk, lk, aPk(0) + a.slot.kc + s_off[0][0], aPk(0) + a.slot.ks + s_off[0][1], n_valid_of(0),
-                        aK(0));
-    decode_tile_smem<D, kThrTcConst>(vbits, plv, lv, aPk(0) + a.slot.vc + s_off[0][2], aPk(0) + a.slot.vs + s_off[0][3], n_valid_of(0),
-                        aV(0));
-  }
-  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-  fence_before();
-  __syncthreads();
-  fence_after();
-
-  const uint32_t idesc_s = (1u << 4) | ((uint32_t)(kTok >> 3) << 17) | ((uint32_t)(kRowsTc >> 4) << 24);
-  const uint32_t idesc_o = (1u << 4) | (1u << 16) | ((uint32_t)(D >> 3) << 17) | ((uint32_t)(kRowsTc >> 4) << 24);
-  auto issue_s = [&](int kb) {   // S = Q^ (TMEM) K^(buffer kb)^T
-#pragma unroll 4
-    for (int s = 0; s < D / 16; ++s)
-      mma_ts(tmem + kColS, tmem + kColQ + 8 * s, sdesc(aK(kb) + s * 256, 128, kGroupBytes), idesc_s, s > 0);
-    mma_commit(su32(&bar_s));
-  };
-  auto issue_o = [&](int vb, bool first) {   // O += P (TMEM) V^(buffer vb)
-#pragma unroll
-    for (int s = 0; s < kTok / 16; ++s)
-      mma_ts(tmem + kColO, tmem + kColP + 8 * s, sdesc(aV(vb) + s * 2 * kGroupBytes, kGroupBytes, 128), idesc_o,
-             (first && s == 0) ? 0 : 1);
-    mma_commit(su32(&bar_o));
-  };
-
-  bool ok = true;
-  if (tid == 0 && n_tiles > 0) issue_s(0);
-  float m_run = -INFINITY, l_run = 0.f;
-  bool o_started = false;
-
-  for (int t = 0; t < n_tiles && ok; ++t) {
-    const int cur = t & 1, nxt = cur ^ 1;
-    const int64_t t0 = t_lo + (int64_t)t * kTok;
-    stage(t + 2, cur);                              // slot cur held tile t (already decoded)
-    asm volatile("cp.async.wait_group 1;\n" ::);    // tile t+1 staged (own copies)
-    __syncthreads();
-    if (t + 1 < n_tiles)
-      decode_tile_smem<D, kThrTcConst>(kbits, plk, lk, aPk(nxt) + a.slot.kc + s_off[nxt][0], aPk(nxt) + a.slot.ks + s_off[nxt][1],
-                          n_valid_of(t + 1), aK(nxt));
-    if (t >= 1) ok = ok && bar_wait(su32(&bar_o), (t - 1) & 1);          // O(t-1) done: P and V(nxt) free
-    if (t + 1 < n_tiles)
-      decode_tile_smem<D, kThrTcConst>(vbits, plv, lv, aPk(nxt) + a.slot.vc + s_off[nxt][2], aPk(nxt) + a.slot.vs + s_off[nxt][3],
-                          n_valid_of(t + 1), aV(nxt));
-    if (row_warp) {
-      ok = ok && bar_wait(su32(&bar_s), t & 1);                          // S(t) ready
-      fence_after();
-      // ---- softmax on this thread's row of S
-      uint32_t sv[32], sw[32];
-      TQ_LD32(lane_base + kColS, sv);
-      TQ_LD32(lane_base + kColS + 32, sw);
-      asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
-      // columns [0, nv_row) of this tile are valid for this row (context end,
-      // causal limit); only tiles on a boundary need the mask
-      const int64_t lim = a.causal ? imin64(t_hi, pos + 1) : t_hi;
-      const int64_t room = lim - t0;
-      const int nv_row = row_ok ? (room <= 0 ? 0 : (room >= kTok ? kTok : (int)room)) : 0;
-      if (__any_sync(0xffffffffu, nv_row < kTok)) {
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          if (c >= nv_row) sv[c] = __float_as_uint(-INFINITY);
-          if (c + 32 >= nv_row) sw[c] = __float_as_uint(-INFINITY);
-        }
-      }
-      float mx = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < 32; ++c) mx = fmaxf(mx, fmaxf(__uint_as_float(sv[c]), __uint_as_float(sw[c])));
-      const bool need = mx > m_run + kLazyP;
-      if (__any_sync(0xffffffffu, need)) {
-        const float m_new = need ? mx : m_run;
-        const float alpha = (need && m_run != -INFINITY) ? ex2f(m_run - m_new) : 1.f;
-        m_run = m_new;
-        l_run *= alpha;
-        if (o_started) {   // rescale this row of O (alpha = 1 for rows that keep m)
-#pragma unroll 1
-          for (int c0 = 0; c0 < D; c0 += 32) {
-            uint32_t ov[32];
-            TQ_LD32(lane_base + kColO + c0, ov);
-            asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
-#pragma unroll
-            for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * alpha);
-            TQ_ST32(lane_base + kColO + c0, ov);
-          }
-        }
-      }
-      const float mref = m_run == -INFINITY ? 0.f : m_run;
-      uint32_t pw[32];
-      float sum = 0.f;
-#pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const float p0 = ex2f(__uint_as_float(c < 16 ? sv[2 * c] : sw[2 * c - 32]) - mref);
-        const float p1 = ex2f(__uint_as_float(c < 16 ? sv[2 * c + 1] : sw[2 * c + 1 - 32]) - mref);
-        sum += p0 + p1;
-        const __half2 h = __floats2half2_rn(p0, p1);
-        pw[c] = *reinterpret_cast<const uint32_t*>(&h);
-      }
-      l_run += sum;
-      TQ_ST32(lane_base + kColP, pw);
-      asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
-    }
-    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");   // decoded tiles -> tensor core
-    fence_before();
-    ok = __syncthreads_and(ok) != 0;   // a timed-out wait stops the whole CTA together
-    fence_after();
-    if (ok && tid == 0) {
-      issue_o(cur, !o_started);
-      if (t + 1 < n_tiles) issue_s(nxt);
-    }
-    o_started = true;
-  }
-  if (n_tiles > 0 && ok) ok = bar_wait(su32(&bar_o), (n_tiles - 1) & 1);
-  ok = __syncthreads_and(ok) != 0;
-  // the combine kernel may be scheduled now; it waits for this grid to finish
-  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
-  fence_after();
-  asm volatile("cp.async.wait_group 0;\n" ::);
-  // ---- partial (m, l, O) of this row for this context slice
-  if (row_warp) {
-    const int h = kvh * G + row % G;
-    float* dst = a.part + ((((int64_t)b * a.Hq + h) * a.Tq + qi) * a.n_split + split) * (D + 4);
-    if (ok && n_tiles > 0) {
-      for (int c0 = 0; c0 < D; c0 += 32) {
-        uint32_t ov[32];
-        TQ_LD32(lane_base + kColO + c0, ov);
-        asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
-        if (row_ok) {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) dst[2 + c0 + j] = __uint_as_float(ov[j]);
-          if (c0 == 0) {
-            dst[0] = m_run;
-            dst[1] = l_run;
-          }
-        }
-      }
-    } else if (row_ok) {
-      dst[0] = -INFINITY;
-      dst[1] = 0.f;
-      for (int j = 0; j < D; ++j) dst[2 + j] = 0.f;
-    }
-  }
-  if (!ok && tid == 0) atomicExch(a.err, 1);
-  fence_before();
-  __syncthreads();
-  if (warp == 0) {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(kTmemCols) : "memory");
-  }
-}
 
 // Warp-specialised prefill: warps 0-3 (consumers) own the 128 TMEM rows, run
 // the softmax and (one thread) issue the MMAs; the NP producer warps stage
 // the packed bytes and decode K/V tiles into double buffers.  Handoffs go
 // through mbarriers: kfull/vfull (a decoded tile is in buffer b; the
 // producers arrive), kfree/vfree (the MMA that read buffer b is done; a
-// tcgen05.commit arrives), s_done / o_done (S(t) written / O(t) done).  Every
+// tcgen05.commit arrives), s_done (S(t) written) and pfree (the O product that
+// read P buffer b is done; P is double-buffered in TMEM).  Every
 // barrier is waited on at most one phase behind its last completion, so a
 // parity wait is never confused by a later phase.  Waits are bounded: a wait
 // that gives up raises a CTA-wide abort flag, after which the roles run out
 // their loops (keeping the named-barrier counts) without further work.
-template <int D, int NP>
+template <int D, int NP, int NB, bool RB>
 __global__ void __launch_bounds__(128 + 32 * NP, 1) prefill_ws_kernel(const CodecParams PK, const CodecParams PV,
                                                                       const PrefillTcArgs a) {
-  constexpr int kThr = 128 + 32 * NP;
   constexpr int kProd = 32 * NP;
+  constexpr int kHalf = kProd / 2;   // decoders per side (K or V)
   constexpr uint32_t kTmemCols = tmem_cols<D>();
   constexpr uint32_t kColQ = 128;
   constexpr uint32_t kColO = col_o<D>();
   constexpr uint32_t kTileBytes = kTok * D * 2;
   constexpr uint32_t kGroupBytes = (D / 8) * 128;
   extern __shared__ __align__(1024) uint8_t smem[];
-  __shared__ __align__(8) uint64_t bars[10];   // kfull[2], vfull[2], kfree[2], vfree[2], s_done, o_done
+  // kfull[NB], vfull[NB], kfree[NB], vfree[NB], s_done, pfree[2]
+  __shared__ __align__(8) uint64_t bars[4 * NB + 3];
   __shared__ uint32_t tmem_base;
-  __shared__ int s_off[2][4];
   __shared__ volatile int s_abort;
+  __shared__ CodeTabs s_tabs[2];   // K and V codebooks (fp16 pairs, unscaled 4-bit tables)
 
   const int tid = threadIdx.x, warp = tid >> 5;
   const bool consumer = warp < 4;
@@ -566,12 +358,12 @@ __global__ void __launch_bounds__(128 + 32 * NP, 1) prefill_ws_kernel(const Code
   const int64_t rec0 = (int64_t)bh * a.S_cap;
 
   const uint32_t a_smem = su32(smem);
+  // NB decoded K buffers, then NB decoded V buffers
   auto aK = [&](int kb) { return a_smem + (uint32_t)kb * kTileBytes; };
-  auto aV = [&](int kb) { return a_smem + (uint32_t)(2 + kb) * kTileBytes; };
-  auto aPk = [&](int kb) { return a_smem + 4 * kTileBytes + (uint32_t)(kb * a.slot_bytes); };
-  uint8_t* const pk_base = smem + 4 * kTileBytes;
-  const uint32_t kfull = su32(&bars[0]), vfull = su32(&bars[2]), kfree = su32(&bars[4]), vfree = su32(&bars[6]);
-  const uint32_t s_done = su32(&bars[8]), o_done = su32(&bars[9]);
+  auto aV = [&](int kb) { return a_smem + (uint32_t)(NB + kb) * kTileBytes; };
+  const uint32_t kfull = su32(&bars[0]), vfull = su32(&bars[NB]), kfree = su32(&bars[2 * NB]),
+                 vfree = su32(&bars[3 * NB]);
+  const uint32_t s_done = su32(&bars[4 * NB]), pfree = su32(&bars[4 * NB + 1]);  // pfree[b]: O that read P buffer b is done
   auto n_valid_of = [&](int tile) { return (int)imin64(kTok, t_hi - (t_lo + (int64_t)tile * kTok)); };
   auto wait = [&](uint32_t bar, uint32_t parity) {
     if (s_abort) return false;
@@ -581,14 +373,17 @@ __global__ void __launch_bounds__(128 + 32 * NP, 1) prefill_ws_kernel(const Code
   };
 
   if (tid == 0) {
+    s_tabs[0] = make_code_tabs(PK);
+    s_tabs[1] = make_code_tabs(PV);
+  }
+  if (tid == 0) {
     s_abort = 0;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(su32(&bars[i])), "r"(kProd) : "memory");
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(su32(&bars[4 + i])) : "memory");
-    }
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(s_done) : "memory");
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(o_done) : "memory");
+    for (int i = 0; i < 2 * NB; ++i)   // kfull, vfull: every decoder of that side arrives
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(su32(&bars[i])), "r"(kHalf) : "memory");
+#pragma unroll
+    for (int i = 2 * NB; i < 4 * NB + 3; ++i)   // one arrival: a tcgen05.commit
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(su32(&bars[i])) : "memory");
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
   if (warp == 0) {
@@ -603,52 +398,41 @@ __global__ void __launch_bounds__(128 + 32 * NP, 1) prefill_ws_kernel(const Code
   const uint32_t tmem = tmem_base;
 
   if (!consumer) {
-    // ================= producers: stage and decode
-    const int ptid = tid - 128;
-    const CodeTabs lk = make_code_tabs(PK), lv = make_code_tabs(PV);
-    const ItemPlan<D, kProd> plk = make_plan<D, kProd>(PK, ptid), plv = make_plan<D, kProd>(PV, ptid);
-    auto stage = [&](int tile) {
-      const int slot = tile & 1;
-      if (tile < n_tiles) {
-        const int64_t t0 = t_lo + (int64_t)tile * kTok;
-        const int n = (int)imin64(kTok, t_hi - t0);
-        uint8_t* base = pk_base + slot * a.slot_bytes;
-        const int o0 = stage_bytes(base + a.slot.kc, a.kc, rec0 + t0, n, PK.code_bytes, ptid, kProd);
-        const int o1 = stage_bytes(base + a.slot.ks, a.ks, rec0 + t0, n, 2 * PK.nb, ptid, kProd);
-        const int o2 = stage_bytes(base + a.slot.vc, a.vc, rec0 + t0, n, PV.code_bytes, ptid, kProd);
-        const int o3 = stage_bytes(base + a.slot.vs, a.vs, rec0 + t0, n, 2 * PV.nb, ptid, kProd);
-        if (ptid == 0) {
-          s_off[slot][0] = o0; s_off[slot][1] = o1; s_off[slot][2] = o2; s_off[slot][3] = o3;
-        }
-      }
-      asm volatile("cp.async.commit_group;\n" ::);
+    // ================= decoders: half the decoder warps fill the NB K buffers,
+    // the other half the NB V buffers, each at its own pace (K waits only for
+    // the S products, V only for the O products).  Each thread loads its
+    // items' packed words for tile t+1 into registers before decoding tile t,
+    // so the global latency hides behind the decode.
+    if (RB) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(kDecRegs));
+    const bool kside = warp < 4 + NP / 2;
+    const int ptid = tid - (kside ? 128 : 128 + kHalf);
+    const CodecParams& P = kside ? PK : PV;
+    const CodeTabs& ct = s_tabs[kside ? 0 : 1];
+    const uint8_t* codes = kside ? a.kc : a.vc;
+    const uint8_t* scales = kside ? a.ks : a.vs;
+    const uint32_t full = kside ? kfull : vfull, free_bar = kside ? kfree : vfree;
+    const ItemPlan<D, kHalf> pl = make_plan<D, kHalf>(P, ptid);
+    ItemRegs<D, kHalf> ra, rn;
+    auto load = [&](int t, ItemRegs<D, kHalf>& r) {
+      const int64_t rec = rec0 + t_lo + (int64_t)t * kTok;
+      load_items<D, kHalf>(P.bits, pl, codes + rec * P.code_bytes, scales + rec * 2 * P.nb, n_valid_of(t), r);
     };
-    stage(0);
-    stage(1);
-    for (int t = 0; t < n_tiles; ++t) {
-      const int kb = t & 1;
-      const uint32_t use = (uint32_t)(t >> 1);   // use number of buffer kb
-      asm volatile("cp.async.wait_group 1;\n" ::);
-      asm volatile("bar.sync 1, %0;\n" ::"n"(kProd) : "memory");   // tile t staged (all producers' copies)
-      const int nv = n_valid_of(t);
-      if (t >= 2) wait(kfree + 8 * kb, (use - 1) & 1);   // S(t-2) has read K buffer kb
-      if (!s_abort)
-        decode_tile_smem<D, kProd>(PK.bits, plk, lk, aPk(kb) + a.slot.kc + s_off[kb][0],
-                                   aPk(kb) + a.slot.ks + s_off[kb][1], nv, aK(kb));
+    auto step = [&](int t, const ItemRegs<D, kHalf>& r, ItemRegs<D, kHalf>& next) {
+      if (t + 1 < n_tiles) load(t + 1, next);
+      const int kb = t % NB;
+      if (t >= NB) wait(free_bar + 8 * kb, (uint32_t)(t / NB - 1) & 1);   // the product NB tiles back is done
+      if (!s_abort) decode_regs<D, kHalf>(P.bits, pl, r, ct, n_valid_of(t), kside ? aK(kb) : aV(kb));
       asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-      asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(kfull + 8 * kb) : "memory");
-      if (t >= 2) wait(vfree + 8 * kb, (use - 1) & 1);   // O(t-2) has read V buffer kb
-      if (!s_abort)
-        decode_tile_smem<D, kProd>(PV.bits, plv, lv, aPk(kb) + a.slot.vc + s_off[kb][2],
-                                   aPk(kb) + a.slot.vs + s_off[kb][3], nv, aV(kb));
-      asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-      asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(vfull + 8 * kb) : "memory");
-      asm volatile("bar.sync 1, %0;\n" ::"n"(kProd) : "memory");   // every producer is done with slot kb
-      stage(t + 2);
+      asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(full + 8 * kb) : "memory");
+    };
+    if (n_tiles > 0) load(0, ra);
+    for (int t = 0; t < n_tiles; t += 2) {
+      step(t, ra, rn);
+      if (t + 1 < n_tiles) step(t + 1, rn, ra);
     }
-    asm volatile("cp.async.wait_group 0;\n" ::);
   } else {
     // ================= consumers: softmax rows, one thread issues the MMAs
+    if (RB) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(kConsRegs));
     const uint32_t lane_base = tmem + ((uint32_t)(32 * warp) << 16);
     {
       const __half* src = a.qhat + ((int64_t)bh * a.R_pad + (int64_t)rt * kRowsTc + tid) * D;
@@ -670,8 +454,8 @@ __global__ void __launch_bounds__(128 + 32 * NP, 1) prefill_ws_kernel(const Code
     const uint32_t idesc_s = (1u << 4) | ((uint32_t)(kTok >> 3) << 17) | ((uint32_t)(kRowsTc >> 4) << 24);
     const uint32_t idesc_o = (1u << 4) | (1u << 16) | ((uint32_t)(D >> 3) << 17) | ((uint32_t)(kRowsTc >> 4) << 24);
     auto issue_s = [&](int t) {   // S = Q^ (TMEM) K^(buffer)^T, once K(t) is decoded
-      const int kb = t & 1;
-      if (!wait(kfull + 8 * kb, (uint32_t)(t >> 1) & 1)) return;
+      const int kb = t % NB;
+      if (!wait(kfull + 8 * kb, (uint32_t)(t / NB) & 1)) return;
       fence_after();
 #pragma unroll 4
       for (int s = 0; s < D / 16; ++s)
@@ -680,14 +464,14 @@ __global__ void __launch_bounds__(128 + 32 * NP, 1) prefill_ws_kernel(const Code
       mma_commit(kfree + 8 * kb);
     };
     auto issue_o = [&](int t) {   // O += P (TMEM) V^(buffer), once V(t) is decoded
-      const int kb = t & 1;
-      if (!wait(vfull + 8 * kb, (uint32_t)(t >> 1) & 1)) return;
+      const int kb = t % NB, pb = t & 1;
+      if (!wait(vfull + 8 * kb, (uint32_t)(t / NB) & 1)) return;
       fence_after();
 #pragma unroll
       for (int s = 0; s < kTok / 16; ++s)
-        mma_ts(tmem + kColO, tmem + kColP + 8 * s, sdesc(aV(kb) + s * 2 * kGroupBytes, kGroupBytes, 128), idesc_o,
-               (t == 0 && s == 0) ? 0 : 1);
-      mma_commit(o_done);
+        mma_ts(tmem + kColO, tmem + kColP + 32 * pb + 8 * s, sdesc(aV(kb) + s * 2 * kGroupBytes, kGroupBytes, 128),
+               idesc_o, (t == 0 && s == 0) ? 0 : 1);
+      mma_commit(pfree + 8 * pb);
       mma_commit(vfree + 8 * kb);
     };
     if (tid == 0 && n_tiles > 0) issue_s(0);
@@ -705,6 +489,12 @@ __global__ void __launch_bounds__(128 + 32 * NP, 1) prefill_ws_kernel(const Code
 #pragma unroll
         for (int c = 0; c < 32; ++c) sv[c] = sw[c] = __float_as_uint(-INFINITY);
       }
+      // every row has S(t) in registers: S(t+1) can overwrite it and run on
+      // the tensor pipe while this softmax proceeds
+      fence_before();
+      asm volatile("bar.sync 2, 128;\n" ::: "memory");
+      fence_after();
+      if (tid == 0 && !s_abort && t + 1 < n_tiles) issue_s(t + 1);
       const int64_t lim = a.causal ? imin64(t_hi, pos + 1) : t_hi;
       const int64_t room = lim - t0;
       const int nv_row = row_ok ? (room <= 0 ? 0 : (room >= kTok ? kTok : (int)room)) : 0;
@@ -718,9 +508,6 @@ __global__ void __launch_bounds__(128 + 32 * NP, 1) prefill_ws_kernel(const Code
       float mx = -INFINITY;
 #pragma unroll
       for (int c = 0; c < 32; ++c) mx = fmaxf(mx, fmaxf(__uint_as_float(sv[c]), __uint_as_float(sw[c])));
-      // O(t-1) must be done before P is rewritten or O rescaled
-      if (t >= 1) wait(o_done, (uint32_t)(t - 1) & 1);
-      fence_after();
       const bool need = mx > m_run + kLazyP;
       if (__any_sync(0xffffffffu, need)) {
         const float m_new = need ? mx : m_run;
@@ -728,6 +515,9 @@ __global__ void __launch_bounds__(128 + 32 * NP, 1) prefill_ws_kernel(const Code
         m_run = m_new;
         l_run *= alpha;
         if (t >= 1) {
+          // O(t-1), the last product issued on O, must be done before O is rescaled
+          wait(pfree + 8 * ((t - 1) & 1), (uint32_t)((t - 1) >> 1) & 1);
+          fence_after();
 #pragma unroll 1
           for (int c0 = 0; c0 < D; c0 += 32) {
             uint32_t ov[32];
@@ -739,6 +529,9 @@ __global__ void __launch_bounds__(128 + 32 * NP, 1) prefill_ws_kernel(const Code
           }
         }
       }
+      // P buffer t&1 was last read by O(t-2)
+      if (t >= 2) wait(pfree + 8 * (t & 1), (uint32_t)((t - 2) >> 1) & 1);
+      fence_after();
       const float mref = m_run == -INFINITY ? 0.f : m_run;
       uint32_t pw[32];
       float sum = 0.f;
@@ -751,17 +544,14 @@ __global__ void __launch_bounds__(128 + 32 * NP, 1) prefill_ws_kernel(const Code
         pw[c] = *reinterpret_cast<const uint32_t*>(&h);
       }
       l_run += sum;
-      TQ_ST32(lane_base + kColP, pw);
+      TQ_ST32(lane_base + kColP + 32 * (t & 1), pw);
       asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
       fence_before();
-      asm volatile("bar.sync 2, 128;\n" ::: "memory");   // P(t) complete, S(t) read by every row
+      asm volatile("bar.sync 2, 128;\n" ::: "memory");   // P(t) complete
       fence_after();
-      if (tid == 0 && !s_abort) {
-        issue_o(t);
-        if (t + 1 < n_tiles) issue_s(t + 1);
-      }
+      if (tid == 0 && !s_abort) issue_o(t);
     }
-    if (n_tiles > 0) wait(o_done, (uint32_t)(n_tiles - 1) & 1);
+    if (n_tiles > 0) wait(pfree + 8 * ((n_tiles - 1) & 1), (uint32_t)((n_tiles - 1) >> 1) & 1);
     fence_after();
     const bool ok = !s_abort;
     const int h = kvh * G + row % G;
@@ -828,8 +618,8 @@ __global__ void __launch_bounds__(D) prefill_rotate_q_kernel(const CodecParams P
 }
 
 template <int D>
-size_t tc_smem(int slot_bytes) {  // double-buffered decoded K and V tiles + two packed staging slots
-  return 4 * (size_t)kTok * D * 2 + 2 * (size_t)slot_bytes;
+size_t tc_smem(int nb) {  // nb decoded K tiles and nb decoded V tiles
+  return (size_t)2 * nb * kTok * D * 2;
 }
 
 }  // namespace
@@ -866,6 +656,35 @@ size_t prefill_tc_workspace(int B, int Hq, int Hkv, int d, int Tq, int64_t ctx) 
   return 256 + ((qbytes + 255) / 256) * 256 + pbytes;
 }
 
+// The warp-specialised kernel with 16 decoder warps and setmaxnreg moving
+// registers to the consumers, when its launch register count makes that
+// split exact (launch total >= consumer + decoder shares); otherwise 8
+// decoder warps without rebalancing.
+template <int D>
+int launch_ws(const CodecParams& PK, const CodecParams& PV, const PrefillTcArgs& a, dim3 grid, cudaStream_t st) {
+  const size_t sm = tc_smem<D>(3);
+  static int use_rb = -1;   // decided once per process (the kernel image is fixed)
+  if (use_rb < 0) {
+    cudaFuncAttributes fa;
+    use_rb = 0;
+    if (cudaFuncGetAttributes(&fa, prefill_ws_kernel<D, kProducerWarpsRB, 3, true>) == cudaSuccess) {
+      const long launch = (long)(128 + 32 * kProducerWarpsRB) * fa.numRegs;
+      const long need = 128L * kConsRegs + 32L * kProducerWarpsRB * kDecRegs;
+      use_rb = (fa.numRegs >= kDecRegs && fa.numRegs <= kConsRegs && launch >= need) ? 1 : 0;
+    }
+  }
+  if (use_rb) {
+    auto k = prefill_ws_kernel<D, kProducerWarpsRB, 3, true>;
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm)) return TQ_ERR_CUDA;
+    k<<<grid, 128 + 32 * kProducerWarpsRB, sm, st>>>(PK, PV, a);
+  } else {
+    auto k = prefill_ws_kernel<D, kProducerWarps, 3, false>;
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm)) return TQ_ERR_CUDA;
+    k<<<grid, 128 + 32 * kProducerWarps, sm, st>>>(PK, PV, a);
+  }
+  return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+}
+
 int launch_prefill_tc(const CodecParams& PK, const CodecParams& PV, const uint8_t* kc, const uint16_t* ks,
                       const uint8_t* vc, const uint16_t* vs, const uint16_t* q, int B, int Hq, int Hkv, int Tq,
                       int64_t S_cap, int64_t ctx, int causal, float qscale, uint16_t* out, void* ws,
@@ -882,47 +701,26 @@ int launch_prefill_tc(const CodecParams& PK, const CodecParams& PV, const uint8_
   if (cudaMemsetAsync(err, 0, sizeof(int), st) != cudaSuccess) return TQ_ERR_CUDA;
   int64_t per = (ctx + ns - 1) / ns;
   per = (per + kTok - 1) / kTok * kTok;
-  // staging slot: each array padded to 16 bytes plus 16 bytes of alignment slack
-  auto pad = [](int bytes) { return (bytes + 16 + 15) / 16 * 16; };
-  PackedSlot slot;
-  slot.kc = 0;
-  slot.ks = slot.kc + pad(kTok * PK.code_bytes);
-  slot.vc = slot.ks + pad(kTok * 2 * PK.nb);
-  slot.vs = slot.vc + pad(kTok * PV.code_bytes);
-  const int slot_bytes = slot.vs + pad(kTok * 2 * PV.nb);
   PrefillTcArgs a{kc, reinterpret_cast<const uint8_t*>(ks), vc, reinterpret_cast<const uint8_t*>(vs), qhat, part,
-                  err, S_cap, ctx, Hq, Hkv, Tq, R_pad, ns, causal, per, slot_bytes, slot};
+                  err, S_cap, ctx, Hq, Hkv, Tq, R_pad, ns, causal, per};
   dim3 qgrid(R_pad, B * Hkv);
   dim3 grid(R_pad / kRowsTc, ns, B * Hkv);
+  int r;
   switch (d) {
-    case 64: {
+    case 64:
       prefill_rotate_q_kernel<64><<<qgrid, 64, 0, st>>>(PK, q, qhat, Hq, Hkv, Tq, R_pad, qscale);
-      const size_t sm = tc_smem<64>(slot_bytes);
-      if (cudaFuncSetAttribute(prefill_ws_kernel<64, kProducerWarps>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)sm))
-        return TQ_ERR_CUDA;
-      prefill_ws_kernel<64, kProducerWarps><<<grid, 128 + 32 * kProducerWarps, sm, st>>>(PK, PV, a);
+      r = launch_ws<64>(PK, PV, a, grid, st);
       break;
-    }
-    case 128: {
+    case 128:
       prefill_rotate_q_kernel<128><<<qgrid, 128, 0, st>>>(PK, q, qhat, Hq, Hkv, Tq, R_pad, qscale);
-      const size_t sm = tc_smem<128>(slot_bytes);
-      if (cudaFuncSetAttribute(prefill_ws_kernel<128, kProducerWarps>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)sm))
-        return TQ_ERR_CUDA;
-      prefill_ws_kernel<128, kProducerWarps><<<grid, 128 + 32 * kProducerWarps, sm, st>>>(PK, PV, a);
+      r = launch_ws<128>(PK, PV, a, grid, st);
       break;
-    }
-    default: {
+    default:
       prefill_rotate_q_kernel<256><<<qgrid, 256, 0, st>>>(PK, q, qhat, Hq, Hkv, Tq, R_pad, qscale);
-      const size_t sm = tc_smem<256>(slot_bytes);
-      if (cudaFuncSetAttribute(prefill_ws_kernel<256, kProducerWarps>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)sm))
-        return TQ_ERR_CUDA;
-      prefill_ws_kernel<256, kProducerWarps><<<grid, 128 + 32 * kProducerWarps, sm, st>>>(PK, PV, a);
+      r = launch_ws<256>(PK, PV, a, grid, st);
       break;
-    }
   }
+  if (r != TQ_OK) return r;
   if (cudaGetLastError() != cudaSuccess) return TQ_ERR_CUDA;
   return decode_combine(PV, part, ns, out, B * Hq * Tq, st);
 }

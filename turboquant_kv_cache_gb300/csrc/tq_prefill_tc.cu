@@ -2,20 +2,22 @@
 // (tcgen05, TMEM accumulators).
 //
 // Rows: every (batch, KV head) owns R = Tq*G query rows (query i, head h ->
-// row i*G + h).  A CTA takes 128 rows (one per consumer thread and per TMEM
-// lane) and one slice of the context, walking it in 64-token tiles, with two
-// warp roles:
-//   * producer warps stage the packed K/V bytes with cp.async and decode each
-//     tile into shared memory (rotated domain, centroid * block norm, fp16)
-//     in the canonical no-swizzle core-matrix layout (8 rows x 16 bytes per
-//     core matrix), which serves K as a K-major B operand of S = Q K^T and V
-//     as an MN-major B operand of O = P V; K and V tiles are double-buffered,
-//     so decoding runs ahead of the MMAs;
-//   * consumer warps: one thread issues S = Q^ K^^T (M 128, N 64, K d) into
-//     TMEM and O += P V^ (A = P from TMEM, M 128, N d, K 64); each consumer
-//     thread reads its row of S, applies the causal / context mask and an
-//     online softmax in base 2 (the reference max moves only when a score
-//     exceeds it by more than 2^8) and writes P as fp16 back into TMEM.
+// row i*G + h).  A CTA takes 128 rows (one per softmax thread and per TMEM
+// lane) and one slice of the context, walking it in 64-token tiles, with
+// three warp roles:
+//   * decoder warps (one group for K, one for V) load the packed codes and
+//     block norms of the next tile into registers and decode the current one
+//     into shared memory (rotated domain, centroid * block norm, fp16) in the
+//     canonical no-swizzle core-matrix layout (8 rows x 16 bytes per core
+//     matrix), which serves K as a K-major B operand of S = Q K^T and V as an
+//     MN-major B operand of O = P V; each side has a ring of three buffers;
+//   * one MMA warp issues S = Q^ K^^T (A = Q^ from TMEM, M 128, N 64, K d)
+//     and O += P V^ (A = P from TMEM, M 128, N d, K 64) as their inputs
+//     become ready;
+//   * the softmax warps read their row of S, apply the causal / context mask
+//     and an online softmax in base 2 (the reference max moves only when a
+//     score exceeds it by more than 2^8) and write P as fp16 back into TMEM
+//     (two P buffers, so P(t+1) is written while O(t) runs).
 // Q^ = H D q per K block times softmax_scale * log2 e is prepared once per
 // call by a small kernel.  Partial (m, l, O) per row and context slice go to
 // the workspace in the decode-split format, and the decode combine kernel
@@ -37,8 +39,10 @@ namespace {
 
 constexpr int kRowsTc = 128;     // query rows per CTA (TMEM lanes)
 constexpr int kTok = 64;         // tokens per KV tile
-constexpr int kProducerWarps = 8;   // decoding warps without register rebalancing
-constexpr int kProducerWarpsRB = 16; // decoding warps with setmaxnreg rebalancing
+// decoding warps (K side, V side): 8 + 7 with setmaxnreg rebalancing (20 warps
+// in all), 4 + 3 without (12 warps); 4-bit K codes cost more to decode than
+// 3-bit V codes, so the K side gets the extra warp
+constexpr int kDecK_RB = 8, kDecV_RB = 7, kDecK = 4, kDecV = 3;
 constexpr int kConsRegs = 128, kDecRegs = 88;
 constexpr uint32_t kColS = 0, kColP = 64;
 // TMEM columns: S (64 fp32) at 0, two P buffers (64 fp16 = 32 columns each) at
@@ -64,16 +68,24 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t
          ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | ((uint64_t)1 << 46);
 }
 
-__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, int acc) {
+// Warp-wide forms: every lane of a converged warp executes them and the lane
+// that elect.sync picks (the same one each time for a full, converged warp)
+// issues the MMA or the commit, so an MMA and the commit that tracks it come
+// from one thread.
+__device__ __forceinline__ void mma_ts_elect(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, int acc) {
   asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d),
+      "{\n .reg .pred p, e;\n elect.sync _|e, 0xffffffff;\n setp.ne.b32 p, %4, 0;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d),
       "r"(a), "l"(b), "r"(idesc), "r"(acc)
       : "memory");
 }
-
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(bar) : "memory");
+__device__ __forceinline__ void commit_elect(uint32_t bar) {
+  asm volatile(
+      "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
+      " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(bar)
+      : "memory");
 }
+
 
 __device__ __forceinline__ uint64_t global_ns() {
   uint64_t t;
@@ -85,7 +97,13 @@ __device__ __forceinline__ uint64_t global_ns() {
 // try_wait (suspend-time hint 1 ms; it wakes as soon as the phase completes)
 // instead of spinning; the whole wait is bounded by kWaitNs of wall time.
 __device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t phase) {
-  uint32_t done = 0;
+  uint32_t done;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(done)
+      : "r"(bar), "r"(phase)
+      : "memory");
+  if (done) return true;
   uint64_t t0 = 0;
   for (int it = 0; !done; ++it) {
     asm volatile(
@@ -312,44 +330,76 @@ struct PrefillTcArgs {
 };
 
 
-// Warp-specialised prefill: warps 0-3 (consumers) own the 128 TMEM rows, run
-// the softmax and (one thread) issue the MMAs; the NP producer warps stage
-// the packed bytes and decode K/V tiles into double buffers.  Handoffs go
-// through mbarriers: kfull/vfull (a decoded tile is in buffer b; the
-// producers arrive), kfree/vfree (the MMA that read buffer b is done; a
-// tcgen05.commit arrives), s_done (S(t) written) and pfree (the O product that
-// read P buffer b is done; P is double-buffered in TMEM).  Every
-// barrier is waited on at most one phase behind its last completion, so a
-// parity wait is never confused by a later phase.  Waits are bounded: a wait
-// that gives up raises a CTA-wide abort flag, after which the roles run out
-// their loops (keeping the named-barrier counts) without further work.
-template <int D, int NP, int NB, bool RB>
-__global__ void __launch_bounds__(128 + 32 * NP, 1) prefill_ws_kernel(const CodecParams PK, const CodecParams PV,
-                                                                      const PrefillTcArgs a) {
-  constexpr int kProd = 32 * NP;
-  constexpr int kHalf = kProd / 2;   // decoders per side (K or V)
+// A decoder role: NT threads decode every tile of one side (K or V) into
+// the NB-deep ring of shared buffers at buf0.  Each thread loads its items'
+// packed words for tile t+1 into registers before decoding tile t, so the
+// global latency hides behind the decode; buffer t % NB is refilled once the
+// MMA that read it NB tiles earlier has completed.
+template <int D, int NT, int NB, class NValid, class Wait>
+__device__ __forceinline__ void decoder_role(const CodecParams& P, const CodeTabs& ct, const uint8_t* codes,
+                                             const uint8_t* scales, int ptid, uint32_t full, uint32_t free_bar,
+                                             uint32_t buf0, uint32_t tile_bytes, int64_t rec0, int64_t t_lo,
+                                             int n_tiles, NValid n_valid_of, Wait wait, volatile int& abort) {
+  const ItemPlan<D, NT> pl = make_plan<D, NT>(P, ptid);
+  ItemRegs<D, NT> ra, rn;
+  auto load = [&](int t, ItemRegs<D, NT>& r) {
+    const int64_t rec = rec0 + t_lo + (int64_t)t * kTok;
+    load_items<D, NT>(P.bits, pl, codes + rec * P.code_bytes, scales + rec * 2 * P.nb, n_valid_of(t), r);
+  };
+  auto step = [&](int t, const ItemRegs<D, NT>& r, ItemRegs<D, NT>& next) {
+    if (t + 1 < n_tiles) load(t + 1, next);
+    const int kb = t % NB;
+    if (t >= NB) wait(free_bar + 8 * kb, (uint32_t)(t / NB - 1) & 1);   // the product NB tiles back is done
+    if (!abort) decode_regs<D, NT>(P.bits, pl, r, ct, n_valid_of(t), buf0 + (uint32_t)kb * tile_bytes);
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(full + 8 * kb) : "memory");
+  };
+  if (n_tiles > 0) load(0, ra);
+  for (int t = 0; t < n_tiles; t += 2) {
+    step(t, ra, rn);
+    if (t + 1 < n_tiles) step(t + 1, rn, ra);
+  }
+}
+
+// Warp-specialised prefill.  Warps 0-3 (softmax) own the 128 TMEM rows;
+// warp 4 issues every MMA; NK warps decode K tiles and NV warps decode V
+// tiles into NB-deep rings of shared buffers, each side at its own pace.
+// Handoffs go through mbarriers:
+//   kfull/vfull[b]  a decoded tile is in buffer b (every decoder of the side arrives)
+//   kfree/vfree[b]  the MMA that read buffer b is done (tcgen05.commit)
+//   q_full          Q^ is in TMEM (one arrival per softmax warp)
+//   s_full          S(t) is in TMEM (commit)
+//   s_free          every softmax warp holds S(t) in registers (one arrival per warp)
+//   p_full[b]       P(t), t & 1 = b, is in TMEM (one arrival per softmax warp)
+//   o_done[b]       O += P(t) V(t), t & 1 = b, is done (commit)
+// The MMA warp issues S(t+1) as soon as S(t) has been read, so it runs on
+// the tensor pipe during the softmax of tile t, and O(t) as soon as P(t) is
+// written.  Every barrier is waited on at most one phase behind its last
+// completion, so a parity wait is never confused by a later phase.  Waits are
+// bounded: a wait that gives up raises a CTA-wide abort flag, after which the
+// roles run out their loops without further work or waits.
+template <int D, int NK, int NV, int NB, bool RB>
+__global__ void __launch_bounds__(160 + 32 * (NK + NV), 1) prefill_ws_kernel(const CodecParams PK, const CodecParams PV,
+                                                                             const PrefillTcArgs a) {
+  static_assert((160 + 32 * (NK + NV)) % 128 == 0, "whole warpgroups (setmaxnreg acts per warpgroup)");
+  constexpr int kNK = 32 * NK, kNV = 32 * NV;
   constexpr uint32_t kTmemCols = tmem_cols<D>();
   constexpr uint32_t kColQ = 128;
   constexpr uint32_t kColO = col_o<D>();
   constexpr uint32_t kTileBytes = kTok * D * 2;
   constexpr uint32_t kGroupBytes = (D / 8) * 128;
   extern __shared__ __align__(1024) uint8_t smem[];
-  // kfull[NB], vfull[NB], kfree[NB], vfree[NB], s_done, pfree[2]
-  __shared__ __align__(8) uint64_t bars[4 * NB + 3];
+  // kfull[NB], vfull[NB], kfree[NB], vfree[NB], q_full, s_full, s_free, p_full[2], o_done[2]
+  __shared__ __align__(8) uint64_t bars[4 * NB + 7];
   __shared__ uint32_t tmem_base;
   __shared__ volatile int s_abort;
   __shared__ CodeTabs s_tabs[2];   // K and V codebooks (fp16 pairs, unscaled 4-bit tables)
 
-  const int tid = threadIdx.x, warp = tid >> 5;
-  const bool consumer = warp < 4;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = a.Hq / a.Hkv;
   const int rt = blockIdx.x, split = blockIdx.y, bh = blockIdx.z;
   const int b = bh / a.Hkv, kvh = bh % a.Hkv;
   const int R = a.Tq * G;
-  const int row = rt * kRowsTc + (tid & 127);
-  const bool row_ok = consumer && row < R;
-  const int qi = row < R ? row / G : a.Tq - 1;
-  const int64_t pos = a.ctx - a.Tq + qi;
   const int last_row = min(rt * kRowsTc + kRowsTc, R) - 1;
   const int64_t max_pos = a.causal ? a.ctx - a.Tq + last_row / G : a.ctx - 1;
   const int64_t t_lo = (int64_t)split * a.per;
@@ -363,7 +413,8 @@ __global__ void __launch_bounds__(128 + 32 * NP, 1) prefill_ws_kernel(const Code
   auto aV = [&](int kb) { return a_smem + (uint32_t)(NB + kb) * kTileBytes; };
   const uint32_t kfull = su32(&bars[0]), vfull = su32(&bars[NB]), kfree = su32(&bars[2 * NB]),
                  vfree = su32(&bars[3 * NB]);
-  const uint32_t s_done = su32(&bars[4 * NB]), pfree = su32(&bars[4 * NB + 1]);  // pfree[b]: O that read P buffer b is done
+  const uint32_t q_full = su32(&bars[4 * NB]), s_full = su32(&bars[4 * NB + 1]), s_free = su32(&bars[4 * NB + 2]),
+                 p_full = su32(&bars[4 * NB + 3]), o_done = su32(&bars[4 * NB + 5]);
   auto n_valid_of = [&](int tile) { return (int)imin64(kTok, t_hi - (t_lo + (int64_t)tile * kTok)); };
   auto wait = [&](uint32_t bar, uint32_t parity) {
     if (s_abort) return false;
@@ -375,15 +426,22 @@ __global__ void __launch_bounds__(128 + 32 * NP, 1) prefill_ws_kernel(const Code
   if (tid == 0) {
     s_tabs[0] = make_code_tabs(PK);
     s_tabs[1] = make_code_tabs(PV);
-  }
-  if (tid == 0) {
     s_abort = 0;
 #pragma unroll
-    for (int i = 0; i < 2 * NB; ++i)   // kfull, vfull: every decoder of that side arrives
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(su32(&bars[i])), "r"(kHalf) : "memory");
+    for (int i = 0; i < NB; ++i) {
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(kfull + 8 * i), "r"(kNK) : "memory");
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(vfull + 8 * i), "r"(kNV) : "memory");
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(kfree + 8 * i) : "memory");
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(vfree + 8 * i) : "memory");
+    }
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 4;\n" ::"r"(q_full) : "memory");
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(s_full) : "memory");
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 4;\n" ::"r"(s_free) : "memory");
 #pragma unroll
-    for (int i = 2 * NB; i < 4 * NB + 3; ++i)   // one arrival: a tcgen05.commit
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(su32(&bars[i])) : "memory");
+    for (int i = 0; i < 2; ++i) {
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 4;\n" ::"r"(p_full + 8 * i) : "memory");
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(o_done + 8 * i) : "memory");
+    }
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
   if (warp == 0) {
@@ -396,43 +454,68 @@ __global__ void __launch_bounds__(128 + 32 * NP, 1) prefill_ws_kernel(const Code
   __syncthreads();
   fence_after();
   const uint32_t tmem = tmem_base;
+  // a softmax warp's signal: its lanes' TMEM accesses are complete, then one arrival
+  auto warp_arrive = [&](uint32_t bar) {
+    fence_before();
+    __syncwarp();
+    if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
+  };
 
-  if (!consumer) {
-    // ================= decoders: half the decoder warps fill the NB K buffers,
-    // the other half the NB V buffers, each at its own pace (K waits only for
-    // the S products, V only for the O products).  Each thread loads its
-    // items' packed words for tile t+1 into registers before decoding tile t,
-    // so the global latency hides behind the decode.
+  if (warp >= 5) {
+    // ================= decoders: NK warps fill the K ring, NV warps the V
+    // ring.  Each thread loads its items' packed words for tile t+1 into
+    // registers before decoding tile t, so the global latency hides behind
+    // the decode.
     if (RB) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(kDecRegs));
-    const bool kside = warp < 4 + NP / 2;
-    const int ptid = tid - (kside ? 128 : 128 + kHalf);
-    const CodecParams& P = kside ? PK : PV;
-    const CodeTabs& ct = s_tabs[kside ? 0 : 1];
-    const uint8_t* codes = kside ? a.kc : a.vc;
-    const uint8_t* scales = kside ? a.ks : a.vs;
-    const uint32_t full = kside ? kfull : vfull, free_bar = kside ? kfree : vfree;
-    const ItemPlan<D, kHalf> pl = make_plan<D, kHalf>(P, ptid);
-    ItemRegs<D, kHalf> ra, rn;
-    auto load = [&](int t, ItemRegs<D, kHalf>& r) {
-      const int64_t rec = rec0 + t_lo + (int64_t)t * kTok;
-      load_items<D, kHalf>(P.bits, pl, codes + rec * P.code_bytes, scales + rec * 2 * P.nb, n_valid_of(t), r);
-    };
-    auto step = [&](int t, const ItemRegs<D, kHalf>& r, ItemRegs<D, kHalf>& next) {
-      if (t + 1 < n_tiles) load(t + 1, next);
-      const int kb = t % NB;
-      if (t >= NB) wait(free_bar + 8 * kb, (uint32_t)(t / NB - 1) & 1);   // the product NB tiles back is done
-      if (!s_abort) decode_regs<D, kHalf>(P.bits, pl, r, ct, n_valid_of(t), kside ? aK(kb) : aV(kb));
-      asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-      asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(full + 8 * kb) : "memory");
-    };
-    if (n_tiles > 0) load(0, ra);
-    for (int t = 0; t < n_tiles; t += 2) {
-      step(t, ra, rn);
-      if (t + 1 < n_tiles) step(t + 1, rn, ra);
+    if (warp < 5 + NK)
+      decoder_role<D, kNK, NB>(PK, s_tabs[0], a.kc, a.ks, tid - 160, kfull, kfree, aK(0), kTileBytes, rec0, t_lo,
+                               n_tiles, n_valid_of, wait, s_abort);
+    else
+      decoder_role<D, kNV, NB>(PV, s_tabs[1], a.vc, a.vs, tid - 160 - kNK, vfull, vfree, aV(0), kTileBytes, rec0,
+                               t_lo, n_tiles, n_valid_of, wait, s_abort);
+  } else if (warp == 4) {
+    // ================= MMA issue: the whole warp walks the schedule, one
+    // elected lane issues each MMA and commit.
+    if (RB) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(kDecRegs));
+    const uint32_t idesc_s = (1u << 4) | ((uint32_t)(kTok >> 3) << 17) | ((uint32_t)(kRowsTc >> 4) << 24);
+    const uint32_t idesc_o = (1u << 4) | (1u << 16) | ((uint32_t)(D >> 3) << 17) | ((uint32_t)(kRowsTc >> 4) << 24);
+    bool ok = n_tiles > 0 && wait(q_full, 0);
+    for (int t = 0; t <= n_tiles && ok; ++t) {
+      if (t < n_tiles) {   // S(t) = Q^ (TMEM) K^(t)^T, once K(t) is decoded and S(t-1) has been read
+        const int kb = t % NB;
+        ok = wait(kfull + 8 * kb, (uint32_t)(t / NB) & 1) && (t == 0 || wait(s_free, (uint32_t)(t - 1) & 1));
+        if (!ok) break;
+        fence_after();
+        __syncwarp();
+        const uint64_t dk = sdesc(aK(kb), 128, kGroupBytes);   // + 16 per 16 columns of d (256 bytes)
+#pragma unroll 1
+        for (int s = 0; s < D / 16; ++s)
+          mma_ts_elect(tmem + kColS, tmem + kColQ + 8 * s, dk + (uint64_t)(16 * s), idesc_s, s > 0);
+        commit_elect(s_full);
+        commit_elect(kfree + 8 * kb);
+      }
+      if (t > 0) {   // O += P(u) (TMEM) V^(u), u = t-1, once P(u) is written and V(u) decoded
+        const int u = t - 1, vb = u % NB, pb = u & 1;
+        ok = wait(p_full + 8 * pb, (uint32_t)(u >> 1) & 1) && wait(vfull + 8 * vb, (uint32_t)(u / NB) & 1);
+        if (!ok) break;
+        fence_after();
+        __syncwarp();
+        const uint64_t dv = sdesc(aV(vb), kGroupBytes, 128);   // + per 16 tokens (2 groups)
+#pragma unroll
+        for (int s = 0; s < kTok / 16; ++s)
+          mma_ts_elect(tmem + kColO, tmem + kColP + 32 * pb + 8 * s, dv + (uint64_t)(s * (2 * kGroupBytes >> 4)),
+                       idesc_o, (u == 0 && s == 0) ? 0 : 1);
+        commit_elect(o_done + 8 * pb);
+        commit_elect(vfree + 8 * vb);
+      }
     }
   } else {
-    // ================= consumers: softmax rows, one thread issues the MMAs
+    // ================= softmax: one row per thread
     if (RB) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(kConsRegs));
+    const int row = rt * kRowsTc + tid;
+    const bool row_ok = row < R;
+    const int qi = row_ok ? row / G : a.Tq - 1;
+    const int64_t pos = a.ctx - a.Tq + qi;
     const uint32_t lane_base = tmem + ((uint32_t)(32 * warp) << 16);
     {
       const __half* src = a.qhat + ((int64_t)bh * a.R_pad + (int64_t)rt * kRowsTc + tid) * D;
@@ -448,38 +531,12 @@ __global__ void __launch_bounds__(128 + 32 * NP, 1) prefill_ws_kernel(const Code
       }
       asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
     }
-    fence_before();
-    asm volatile("bar.sync 2, 128;\n" ::: "memory");
-    fence_after();
-    const uint32_t idesc_s = (1u << 4) | ((uint32_t)(kTok >> 3) << 17) | ((uint32_t)(kRowsTc >> 4) << 24);
-    const uint32_t idesc_o = (1u << 4) | (1u << 16) | ((uint32_t)(D >> 3) << 17) | ((uint32_t)(kRowsTc >> 4) << 24);
-    auto issue_s = [&](int t) {   // S = Q^ (TMEM) K^(buffer)^T, once K(t) is decoded
-      const int kb = t % NB;
-      if (!wait(kfull + 8 * kb, (uint32_t)(t / NB) & 1)) return;
-      fence_after();
-#pragma unroll 4
-      for (int s = 0; s < D / 16; ++s)
-        mma_ts(tmem + kColS, tmem + kColQ + 8 * s, sdesc(aK(kb) + s * 256, 128, kGroupBytes), idesc_s, s > 0);
-      mma_commit(s_done);
-      mma_commit(kfree + 8 * kb);
-    };
-    auto issue_o = [&](int t) {   // O += P (TMEM) V^(buffer), once V(t) is decoded
-      const int kb = t % NB, pb = t & 1;
-      if (!wait(vfull + 8 * kb, (uint32_t)(t / NB) & 1)) return;
-      fence_after();
-#pragma unroll
-      for (int s = 0; s < kTok / 16; ++s)
-        mma_ts(tmem + kColO, tmem + kColP + 32 * pb + 8 * s, sdesc(aV(kb) + s * 2 * kGroupBytes, kGroupBytes, 128),
-               idesc_o, (t == 0 && s == 0) ? 0 : 1);
-      mma_commit(pfree + 8 * pb);
-      mma_commit(vfree + 8 * kb);
-    };
-    if (tid == 0 && n_tiles > 0) issue_s(0);
+    warp_arrive(q_full);
     float m_run = -INFINITY, l_run = 0.f;
     for (int t = 0; t < n_tiles; ++t) {
       const int64_t t0 = t_lo + (int64_t)t * kTok;
       uint32_t sv[32], sw[32];
-      const bool have_s = wait(s_done, (uint32_t)t & 1);   // S(t) written
+      const bool have_s = wait(s_full, (uint32_t)t & 1);   // S(t) written
       fence_after();
       if (have_s) {
         TQ_LD32(lane_base + kColS, sv);
@@ -489,12 +546,7 @@ __global__ void __launch_bounds__(128 + 32 * NP, 1) prefill_ws_kernel(const Code
 #pragma unroll
         for (int c = 0; c < 32; ++c) sv[c] = sw[c] = __float_as_uint(-INFINITY);
       }
-      // every row has S(t) in registers: S(t+1) can overwrite it and run on
-      // the tensor pipe while this softmax proceeds
-      fence_before();
-      asm volatile("bar.sync 2, 128;\n" ::: "memory");
-      fence_after();
-      if (tid == 0 && !s_abort && t + 1 < n_tiles) issue_s(t + 1);
+      warp_arrive(s_free);   // S(t+1) may overwrite S now
       const int64_t lim = a.causal ? imin64(t_hi, pos + 1) : t_hi;
       const int64_t room = lim - t0;
       const int nv_row = row_ok ? (room <= 0 ? 0 : (room >= kTok ? kTok : (int)room)) : 0;
@@ -505,9 +557,11 @@ __global__ void __launch_bounds__(128 + 32 * NP, 1) prefill_ws_kernel(const Code
           if (c + 32 >= nv_row) sw[c] = __float_as_uint(-INFINITY);
         }
       }
-      float mx = -INFINITY;
+      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int c = 0; c < 32; ++c) mx = fmaxf(mx, fmaxf(__uint_as_float(sv[c]), __uint_as_float(sw[c])));
+      for (int c = 0; c < 32; ++c)
+        m4[c & 3] = fmaxf(m4[c & 3], fmaxf(__uint_as_float(sv[c]), __uint_as_float(sw[c])));
+      const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
       const bool need = mx > m_run + kLazyP;
       if (__any_sync(0xffffffffu, need)) {
         const float m_new = need ? mx : m_run;
@@ -516,7 +570,7 @@ __global__ void __launch_bounds__(128 + 32 * NP, 1) prefill_ws_kernel(const Code
         l_run *= alpha;
         if (t >= 1) {
           // O(t-1), the last product issued on O, must be done before O is rescaled
-          wait(pfree + 8 * ((t - 1) & 1), (uint32_t)((t - 1) >> 1) & 1);
+          wait(o_done + 8 * ((t - 1) & 1), (uint32_t)((t - 1) >> 1) & 1);
           fence_after();
 #pragma unroll 1
           for (int c0 = 0; c0 < D; c0 += 32) {
@@ -530,28 +584,25 @@ __global__ void __launch_bounds__(128 + 32 * NP, 1) prefill_ws_kernel(const Code
         }
       }
       // P buffer t&1 was last read by O(t-2)
-      if (t >= 2) wait(pfree + 8 * (t & 1), (uint32_t)((t - 2) >> 1) & 1);
+      if (t >= 2) wait(o_done + 8 * (t & 1), (uint32_t)((t - 2) >> 1) & 1);
       fence_after();
       const float mref = m_run == -INFINITY ? 0.f : m_run;
       uint32_t pw[32];
-      float sum = 0.f;
+      float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
         const float p0 = ex2f(__uint_as_float(c < 16 ? sv[2 * c] : sw[2 * c - 32]) - mref);
         const float p1 = ex2f(__uint_as_float(c < 16 ? sv[2 * c + 1] : sw[2 * c + 1 - 32]) - mref);
-        sum += p0 + p1;
+        s4[c & 3] += p0 + p1;
         const __half2 h = __floats2half2_rn(p0, p1);
         pw[c] = *reinterpret_cast<const uint32_t*>(&h);
       }
-      l_run += sum;
+      l_run += (s4[0] + s4[1]) + (s4[2] + s4[3]);
       TQ_ST32(lane_base + kColP + 32 * (t & 1), pw);
       asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
-      fence_before();
-      asm volatile("bar.sync 2, 128;\n" ::: "memory");   // P(t) complete
-      fence_after();
-      if (tid == 0 && !s_abort) issue_o(t);
+      warp_arrive(p_full + 8 * (t & 1));
     }
-    if (n_tiles > 0) wait(pfree + 8 * ((n_tiles - 1) & 1), (uint32_t)((n_tiles - 1) >> 1) & 1);
+    if (n_tiles > 0) wait(o_done + 8 * ((n_tiles - 1) & 1), (uint32_t)((n_tiles - 1) >> 1) & 1);
     fence_after();
     const bool ok = !s_abort;
     const int h = kvh * G + row % G;
@@ -656,31 +707,32 @@ size_t prefill_tc_workspace(int B, int Hq, int Hkv, int d, int Tq, int64_t ctx) 
   return 256 + ((qbytes + 255) / 256) * 256 + pbytes;
 }
 
-// The warp-specialised kernel with 16 decoder warps and setmaxnreg moving
-// registers to the consumers, when its launch register count makes that
-// split exact (launch total >= consumer + decoder shares); otherwise 8
-// decoder warps without rebalancing.
+// The warp-specialised kernel with 15 decoder warps and setmaxnreg moving
+// registers to the softmax warps, when its launch register count makes that
+// split exact (launch total >= softmax + other shares); otherwise 7 decoder
+// warps without rebalancing.
 template <int D>
 int launch_ws(const CodecParams& PK, const CodecParams& PV, const PrefillTcArgs& a, dim3 grid, cudaStream_t st) {
   const size_t sm = tc_smem<D>(3);
+  constexpr int kThreadsRB = 160 + 32 * (kDecK_RB + kDecV_RB), kThreads = 160 + 32 * (kDecK + kDecV);
   static int use_rb = -1;   // decided once per process (the kernel image is fixed)
   if (use_rb < 0) {
     cudaFuncAttributes fa;
     use_rb = 0;
-    if (cudaFuncGetAttributes(&fa, prefill_ws_kernel<D, kProducerWarpsRB, 3, true>) == cudaSuccess) {
-      const long launch = (long)(128 + 32 * kProducerWarpsRB) * fa.numRegs;
-      const long need = 128L * kConsRegs + 32L * kProducerWarpsRB * kDecRegs;
+    if (cudaFuncGetAttributes(&fa, prefill_ws_kernel<D, kDecK_RB, kDecV_RB, 3, true>) == cudaSuccess) {
+      const long launch = (long)kThreadsRB * fa.numRegs;
+      const long need = 128L * kConsRegs + (long)(kThreadsRB - 128) * kDecRegs;
       use_rb = (fa.numRegs >= kDecRegs && fa.numRegs <= kConsRegs && launch >= need) ? 1 : 0;
     }
   }
   if (use_rb) {
-    auto k = prefill_ws_kernel<D, kProducerWarpsRB, 3, true>;
+    auto k = prefill_ws_kernel<D, kDecK_RB, kDecV_RB, 3, true>;
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm)) return TQ_ERR_CUDA;
-    k<<<grid, 128 + 32 * kProducerWarpsRB, sm, st>>>(PK, PV, a);
+    k<<<grid, kThreadsRB, sm, st>>>(PK, PV, a);
   } else {
-    auto k = prefill_ws_kernel<D, kProducerWarps, 3, false>;
+    auto k = prefill_ws_kernel<D, kDecK, kDecV, 3, false>;
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm)) return TQ_ERR_CUDA;
-    k<<<grid, 128 + 32 * kProducerWarps, sm, st>>>(PK, PV, a);
+    k<<<grid, kThreads, sm, st>>>(PK, PV, a);
   }
   return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }

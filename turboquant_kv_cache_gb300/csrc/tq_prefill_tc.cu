@@ -11,7 +11,7 @@
 //     canonical no-swizzle core-matrix layout (8 rows x 16 bytes per core
 //     matrix), which serves K as a K-major B operand of S = Q K^T and V as an
 //     MN-major B operand of O = P V; each side has a ring of three buffers;
-//   * one MMA warp issues S = Q^ K^^T (A = Q^ from TMEM, M 128, N 64, K d)
+//   * two MMA warps issue S = Q^ K^^T (A = Q^ from TMEM, M 128, N 64, K d)
 //     and O += P V^ (A = P from TMEM, M 128, N d, K 64) as their inputs
 //     become ready;
 //   * the softmax warps read their row of S, apply the causal / context mask
@@ -39,10 +39,10 @@ namespace {
 
 constexpr int kRowsTc = 128;     // query rows per CTA (TMEM lanes)
 constexpr int kTok = 64;         // tokens per KV tile
-// decoding warps (K side, V side): 8 + 7 with setmaxnreg rebalancing (20 warps
-// in all), 4 + 3 without (12 warps); 4-bit K codes cost more to decode than
-// 3-bit V codes, so the K side gets the extra warp
-constexpr int kDecK_RB = 8, kDecV_RB = 7, kDecK = 4, kDecV = 3;
+// decoding warps (K side, V side): 8 + 6 with setmaxnreg rebalancing (20 warps
+// in all), 4 + 2 without (12 warps); 4-bit K codes cost more to decode than
+// 3-bit V codes, so the K side gets the extra warps
+constexpr int kDecK_RB = 8, kDecV_RB = 6, kDecK = 4, kDecV = 2;
 constexpr int kConsRegs = 128, kDecRegs = 88;
 constexpr uint32_t kColS = 0, kColP = 64;
 // TMEM columns: S (64 fp32) at 0, two P buffers (64 fp16 = 32 columns each) at
@@ -362,8 +362,9 @@ __device__ __forceinline__ void decoder_role(const CodecParams& P, const CodeTab
 }
 
 // Warp-specialised prefill.  Warps 0-3 (softmax) own the 128 TMEM rows;
-// warp 4 issues every MMA; NK warps decode K tiles and NV warps decode V
-// tiles into NB-deep rings of shared buffers, each side at its own pace.
+// warp 4 issues the S products and warp 5 the O products; NK warps decode K
+// tiles and NV warps decode V tiles into NB-deep rings of shared buffers,
+// each side at its own pace.
 // Handoffs go through mbarriers:
 //   kfull/vfull[b]  a decoded tile is in buffer b (every decoder of the side arrives)
 //   kfree/vfree[b]  the MMA that read buffer b is done (tcgen05.commit)
@@ -372,16 +373,15 @@ __device__ __forceinline__ void decoder_role(const CodecParams& P, const CodeTab
 //   s_free          every softmax warp holds S(t) in registers (one arrival per warp)
 //   p_full[b]       P(t), t & 1 = b, is in TMEM (one arrival per softmax warp)
 //   o_done[b]       O += P(t) V(t), t & 1 = b, is done (commit)
-// The MMA warp issues S(t+1) as soon as S(t) has been read, so it runs on
-// the tensor pipe during the softmax of tile t, and O(t) as soon as P(t) is
-// written.  Every barrier is waited on at most one phase behind its last
+// S(t+1) is issued as soon as S(t) has been read, so it runs on the tensor
+// pipe during the softmax of tile t, and O(t) as soon as P(t) is written.  Every barrier is waited on at most one phase behind its last
 // completion, so a parity wait is never confused by a later phase.  Waits are
 // bounded: a wait that gives up raises a CTA-wide abort flag, after which the
 // roles run out their loops without further work or waits.
 template <int D, int NK, int NV, int NB, bool RB>
-__global__ void __launch_bounds__(160 + 32 * (NK + NV), 1) prefill_ws_kernel(const CodecParams PK, const CodecParams PV,
+__global__ void __launch_bounds__(192 + 32 * (NK + NV), 1) prefill_ws_kernel(const CodecParams PK, const CodecParams PV,
                                                                              const PrefillTcArgs a) {
-  static_assert((160 + 32 * (NK + NV)) % 128 == 0, "whole warpgroups (setmaxnreg acts per warpgroup)");
+  static_assert((192 + 32 * (NK + NV)) % 128 == 0, "whole warpgroups (setmaxnreg acts per warpgroup)");
   constexpr int kNK = 32 * NK, kNV = 32 * NV;
   constexpr uint32_t kTmemCols = tmem_cols<D>();
   constexpr uint32_t kColQ = 128;
@@ -461,53 +461,60 @@ __global__ void __launch_bounds__(160 + 32 * (NK + NV), 1) prefill_ws_kernel(con
     if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
   };
 
-  if (warp >= 5) {
+  if (warp >= 6) {
     // ================= decoders: NK warps fill the K ring, NV warps the V
     // ring.  Each thread loads its items' packed words for tile t+1 into
     // registers before decoding tile t, so the global latency hides behind
     // the decode.
     if (RB) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(kDecRegs));
-    if (warp < 5 + NK)
-      decoder_role<D, kNK, NB>(PK, s_tabs[0], a.kc, a.ks, tid - 160, kfull, kfree, aK(0), kTileBytes, rec0, t_lo,
+    if (warp < 6 + NK)
+      decoder_role<D, kNK, NB>(PK, s_tabs[0], a.kc, a.ks, tid - 192, kfull, kfree, aK(0), kTileBytes, rec0, t_lo,
                                n_tiles, n_valid_of, wait, s_abort);
     else
-      decoder_role<D, kNV, NB>(PV, s_tabs[1], a.vc, a.vs, tid - 160 - kNK, vfull, vfree, aV(0), kTileBytes, rec0,
+      decoder_role<D, kNV, NB>(PV, s_tabs[1], a.vc, a.vs, tid - 192 - kNK, vfull, vfree, aV(0), kTileBytes, rec0,
                                t_lo, n_tiles, n_valid_of, wait, s_abort);
   } else if (warp == 4) {
-    // ================= MMA issue: the whole warp walks the schedule, one
-    // elected lane issues each MMA and commit.
+    // ================= S issue: S(t) = Q^ (TMEM) K^(t)^T once K(t) is decoded
+    // and S(t-1) has been read.  The whole warp walks the schedule, one
+    // elected lane issues each MMA and commit.  S and O have a warp each, so
+    // neither stream of MMAs waits behind the other's handoffs.
     if (RB) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(kDecRegs));
     const uint32_t idesc_s = (1u << 4) | ((uint32_t)(kTok >> 3) << 17) | ((uint32_t)(kRowsTc >> 4) << 24);
-    const uint32_t idesc_o = (1u << 4) | (1u << 16) | ((uint32_t)(D >> 3) << 17) | ((uint32_t)(kRowsTc >> 4) << 24);
     bool ok = n_tiles > 0 && wait(q_full, 0);
-    for (int t = 0; t <= n_tiles && ok; ++t) {
-      if (t < n_tiles) {   // S(t) = Q^ (TMEM) K^(t)^T, once K(t) is decoded and S(t-1) has been read
-        const int kb = t % NB;
-        ok = wait(kfull + 8 * kb, (uint32_t)(t / NB) & 1) && (t == 0 || wait(s_free, (uint32_t)(t - 1) & 1));
-        if (!ok) break;
-        fence_after();
-        __syncwarp();
-        const uint64_t dk = sdesc(aK(kb), 128, kGroupBytes);   // + 16 per 16 columns of d (256 bytes)
-#pragma unroll 1
-        for (int s = 0; s < D / 16; ++s)
-          mma_ts_elect(tmem + kColS, tmem + kColQ + 8 * s, dk + (uint64_t)(16 * s), idesc_s, s > 0);
-        commit_elect(s_full);
-        commit_elect(kfree + 8 * kb);
-      }
-      if (t > 0) {   // O += P(u) (TMEM) V^(u), u = t-1, once P(u) is written and V(u) decoded
-        const int u = t - 1, vb = u % NB, pb = u & 1;
-        ok = wait(p_full + 8 * pb, (uint32_t)(u >> 1) & 1) && wait(vfull + 8 * vb, (uint32_t)(u / NB) & 1);
-        if (!ok) break;
-        fence_after();
-        __syncwarp();
-        const uint64_t dv = sdesc(aV(vb), kGroupBytes, 128);   // + per 16 tokens (2 groups)
+    for (int t = 0; t < n_tiles && ok; ++t) {
+      const int kb = t % NB;
+      ok = wait(kfull + 8 * kb, (uint32_t)(t / NB) & 1) && (t == 0 || wait(s_free, (uint32_t)(t - 1) & 1));
+      if (!ok) break;
+      fence_after();
+      __syncwarp();
+      // fully unrolled: back-to-back MMAs in straight-line code keep the
+      // tensor pipe fed; an issue loop with a branch per MMA does not
+      const uint64_t dk = sdesc(aK(kb), 128, kGroupBytes);   // + 16 per 16 columns of d (256 bytes)
 #pragma unroll
-        for (int s = 0; s < kTok / 16; ++s)
-          mma_ts_elect(tmem + kColO, tmem + kColP + 32 * pb + 8 * s, dv + (uint64_t)(s * (2 * kGroupBytes >> 4)),
-                       idesc_o, (u == 0 && s == 0) ? 0 : 1);
-        commit_elect(o_done + 8 * pb);
-        commit_elect(vfree + 8 * vb);
-      }
+      for (int s = 0; s < D / 16; ++s)
+        mma_ts_elect(tmem + kColS, tmem + kColQ + 8 * s, dk + (uint64_t)(16 * s), idesc_s, s > 0);
+      commit_elect(s_full);
+      commit_elect(kfree + 8 * kb);
+    }
+  } else if (warp == 5) {
+    // ================= O issue: O += P(t) (TMEM) V^(t) once P(t) is written
+    // and V(t) decoded
+    if (RB) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(kDecRegs));
+    const uint32_t idesc_o = (1u << 4) | (1u << 16) | ((uint32_t)(D >> 3) << 17) | ((uint32_t)(kRowsTc >> 4) << 24);
+    bool ok = true;
+    for (int t = 0; t < n_tiles && ok; ++t) {
+      const int vb = t % NB, pb = t & 1;
+      ok = wait(p_full + 8 * pb, (uint32_t)(t >> 1) & 1) && wait(vfull + 8 * vb, (uint32_t)(t / NB) & 1);
+      if (!ok) break;
+      fence_after();
+      __syncwarp();
+      const uint64_t dv = sdesc(aV(vb), kGroupBytes, 128);   // + per 16 tokens (2 groups)
+#pragma unroll
+      for (int s = 0; s < kTok / 16; ++s)
+        mma_ts_elect(tmem + kColO, tmem + kColP + 32 * pb + 8 * s, dv + (uint64_t)(s * (2 * kGroupBytes >> 4)),
+                     idesc_o, (t == 0 && s == 0) ? 0 : 1);
+      commit_elect(o_done + 8 * pb);
+      commit_elect(vfree + 8 * vb);
     }
   } else {
     // ================= softmax: one row per thread
@@ -707,14 +714,14 @@ size_t prefill_tc_workspace(int B, int Hq, int Hkv, int d, int Tq, int64_t ctx) 
   return 256 + ((qbytes + 255) / 256) * 256 + pbytes;
 }
 
-// The warp-specialised kernel with 15 decoder warps and setmaxnreg moving
+// The warp-specialised kernel with 14 decoder warps and setmaxnreg moving
 // registers to the softmax warps, when its launch register count makes that
-// split exact (launch total >= softmax + other shares); otherwise 7 decoder
+// split exact (launch total >= softmax + other shares); otherwise 6 decoder
 // warps without rebalancing.
 template <int D>
 int launch_ws(const CodecParams& PK, const CodecParams& PV, const PrefillTcArgs& a, dim3 grid, cudaStream_t st) {
   const size_t sm = tc_smem<D>(3);
-  constexpr int kThreadsRB = 160 + 32 * (kDecK_RB + kDecV_RB), kThreads = 160 + 32 * (kDecK + kDecV);
+  constexpr int kThreadsRB = 192 + 32 * (kDecK_RB + kDecV_RB), kThreads = 192 + 32 * (kDecK + kDecV);
   static int use_rb = -1;   // decided once per process (the kernel image is fixed)
   if (use_rb < 0) {
     cudaFuncAttributes fa;

@@ -85,6 +85,15 @@ __device__ __forceinline__ void commit_elect(uint32_t bar) {
       " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(bar)
       : "memory");
 }
+// The same, arriving on the mbarrier at this offset in both CTAs of the pair.
+__device__ __forceinline__ void commit_elect_pair(uint32_t bar) {
+  const uint16_t mask = 0x3;
+  asm volatile(
+      "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
+      " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n}\n" ::"r"(bar),
+      "h"(mask)
+      : "memory");
+}
 
 
 __device__ __forceinline__ uint64_t global_ns() {
@@ -96,21 +105,40 @@ __device__ __forceinline__ uint64_t global_ns() {
 // Wait for the phase of parity `phase` of an mbarrier.  The thread sleeps in
 // try_wait (suspend-time hint 1 ms; it wakes as soon as the phase completes)
 // instead of spinning; the whole wait is bounded by kWaitNs of wall time.
+// CLUSTER: the arrivals come from the other CTA of the pair as well, so the
+// wait acquires at cluster scope.
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t phase) {
   uint32_t done;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(done)
-      : "r"(bar), "r"(phase)
-      : "memory");
+  if (CLUSTER)
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(bar), "r"(phase)
+        : "memory");
+  else
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(bar), "r"(phase)
+        : "memory");
   if (done) return true;
   uint64_t t0 = 0;
   for (int it = 0; !done; ++it) {
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(done)
-        : "r"(bar), "r"(phase), "r"(kSuspendNs)
-        : "memory");
+    if (CLUSTER)
+      asm volatile(
+          "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n"
+          " selp.u32 %0, 1, 0, p;\n}\n"
+          : "=r"(done)
+          : "r"(bar), "r"(phase), "r"(kSuspendNs)
+          : "memory");
+    else
+      asm volatile(
+          "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
+          : "=r"(done)
+          : "r"(bar), "r"(phase), "r"(kSuspendNs)
+          : "memory");
     if (done) break;
     if (it == 0) {
       t0 = global_ns();
@@ -123,6 +151,10 @@ __device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t phase) {
 
 __device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
 __device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory"); }
+// every thread of both CTAs of the cluster
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
 
 #define TQ_LD32(taddr, v)                                                                                          \
   asm volatile(                                                                                                    \
@@ -167,27 +199,36 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                : "memory");
 }
+__device__ __forceinline__ uint32_t mapa_peer(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
 
 // Per-thread constants of the tile decoder: the thread's (token, 32-value
 // group) work items and their byte offsets, the same for every tile.
+// A thread decodes items of the TOK tokens of a tile that start at tok0
+// (all of the tile, or the half a CTA of a pair decodes).
 template <int D, int NT>
 struct ItemPlan {
   static constexpr int G8 = D / 32;
-  static constexpr int N = (kTok * G8 + NT - 1) / NT;   // items per decoding thread
+  static constexpr int TOK = kTok / 2;
+  static constexpr int N = (TOK * G8 + NT - 1) / NT;   // items per decoding thread
   int tok[N];
   uint32_t code_off[N], sc_off[N], dst_off[N];
 };
 
 template <int D, int NT>
-__device__ __forceinline__ ItemPlan<D, NT> make_plan(const CodecParams& P, int tid) {
+__device__ __forceinline__ ItemPlan<D, NT> make_plan(const CodecParams& P, int tid, int tok0) {
   ItemPlan<D, NT> pl;
   constexpr int G8 = D / 32;
+  constexpr int TOK = ItemPlan<D, NT>::TOK;
 #pragma unroll
   for (int k = 0; k < ItemPlan<D, NT>::N; ++k) {
     const int item = tid + k * NT;
-    const int tok = 8 * (item / (8 * G8)) + (item & 7);
+    const int tok = tok0 + 8 * (item / (8 * G8)) + (item & 7);
     const int grp = (item >> 3) % G8;
-    pl.tok[k] = item < kTok * G8 ? tok : kTok;   // kTok: no item
+    pl.tok[k] = item < TOK * G8 ? tok : kTok;   // kTok: no item
     pl.code_off[k] = (uint32_t)(tok * P.code_bytes + grp * 4 * P.bits);
     pl.sc_off[k] = (uint32_t)(tok * P.nb * 2 + ((32 * grp) / P.blk) * 2);
     pl.dst_off[k] = cm_off(tok, 32 * grp, D);
@@ -256,10 +297,11 @@ __device__ __forceinline__ void load_items(int bits, const ItemPlan<D, NT>& pl, 
 template <int D, int NT, int BITS>
 __device__ __forceinline__ void decode_regs_b(const ItemPlan<D, NT>& pl, const ItemRegs<D, NT>& r, const uint32_t* c2,
                                               const Tab& fixed, int n_valid, uint32_t tile) {
+  auto sts2 = [&](uint32_t off, uint4 v) { sts128(tile + off, v); };
 #pragma unroll
   for (int k = 0; k < ItemPlan<D, NT>::N; ++k) {
     if (pl.tok[k] >= kTok) continue;
-    const uint32_t dst = tile + pl.dst_off[k];
+    const uint32_t dst = pl.dst_off[k];
     if (n_valid == kTok || pl.tok[k] < n_valid) {
       uint32_t n[4];
       chunk_words<BITS>(r.w[k], n);
@@ -280,11 +322,11 @@ __device__ __forceinline__ void decode_regs_b(const ItemPlan<D, NT>& pl, const I
 #pragma unroll
           for (int e = 0; e < 4; ++e) o[e] = lut_hmul2(o[e], s2);
         }
-        sts128(dst + 128 * c, make_uint4(o[0], o[1], o[2], o[3]));
+        sts2(dst + 128 * c, make_uint4(o[0], o[1], o[2], o[3]));
       }
     } else {
 #pragma unroll
-      for (int c = 0; c < 4; ++c) sts128(dst + 128 * c, make_uint4(0u, 0u, 0u, 0u));
+      for (int c = 0; c < 4; ++c) sts2(dst + 128 * c, make_uint4(0u, 0u, 0u, 0u));
     }
   }
 }
@@ -330,17 +372,30 @@ struct PrefillTcArgs {
 };
 
 
-// A decoder role: NT threads decode every tile of one side (K or V) into
-// the NB-deep ring of shared buffers at buf0.  Each thread loads its items'
-// packed words for tile t+1 into registers before decoding tile t, so the
-// global latency hides behind the decode; buffer t % NB is refilled once the
-// MMA that read it NB tiles earlier has completed.
-template <int D, int NT, int NB, class NValid, class Wait>
+// A decoder role: NT threads of each CTA of a pair decode half of every tile
+// of one side (K or V), tokens [32 rank, 32 rank + 32), into the NB-deep ring
+// of shared buffers; in the core-matrix layout that half is one contiguous
+// block (32 d fp16), which one thread then copies into the same place in the
+// peer CTA with a bulk shared::cluster copy that completes on the peer's full
+// barrier.  So each CTA holds whole tiles for its own MMAs at half the decode
+// work.  Each thread loads its items' packed words for tile t+1 into
+// registers before decoding tile t, so the global latency hides behind the
+// decode.  Buffer t % NB is refilled once the products that read it NB tiles
+// earlier have completed in both CTAs (its free barrier takes a commit from
+// each; the peer's commit also implies that the copy out of this buffer has
+// landed).  Before returning, the role waits for the products of its last
+// tiles, so no arrival from the peer can still be on its way to this CTA.
+// BAR_ID: the named barrier that gathers the side's NT threads.
+template <int D, int NT, int NB, int BAR_ID, class NValid, class Wait>
 __device__ __forceinline__ void decoder_role(const CodecParams& P, const CodeTabs& ct, const uint8_t* codes,
                                              const uint8_t* scales, int ptid, uint32_t full, uint32_t free_bar,
                                              uint32_t buf0, uint32_t tile_bytes, int64_t rec0, int64_t t_lo,
-                                             int n_tiles, NValid n_valid_of, Wait wait, volatile int& abort) {
-  const ItemPlan<D, NT> pl = make_plan<D, NT>(P, ptid);
+                                             int n_tiles, uint32_t rank, NValid n_valid_of, Wait wait,
+                                             volatile int& abort) {
+  constexpr uint32_t kHalfBytes = 32u * D * 2;
+  const ItemPlan<D, NT> pl = make_plan<D, NT>(P, ptid, (int)rank * ItemPlan<D, NT>::TOK);
+  const uint32_t half_off = rank * kHalfBytes;
+  const uint32_t peer_buf0 = mapa_peer(buf0, rank ^ 1u), peer_full = mapa_peer(full, rank ^ 1u);
   ItemRegs<D, NT> ra, rn;
   auto load = [&](int t, ItemRegs<D, NT>& r) {
     const int64_t rec = rec0 + t_lo + (int64_t)t * kTok;
@@ -349,25 +404,47 @@ __device__ __forceinline__ void decoder_role(const CodecParams& P, const CodeTab
   auto step = [&](int t, const ItemRegs<D, NT>& r, ItemRegs<D, NT>& next) {
     if (t + 1 < n_tiles) load(t + 1, next);
     const int kb = t % NB;
-    if (t >= NB) wait(free_bar + 8 * kb, (uint32_t)(t / NB - 1) & 1);   // the product NB tiles back is done
-    if (!abort) decode_regs<D, NT>(P.bits, pl, r, ct, n_valid_of(t), buf0 + (uint32_t)kb * tile_bytes);
+    if (t >= NB) wait(free_bar + 8 * kb, (uint32_t)(t / NB - 1) & 1);   // the products NB tiles back are done
+    const uint32_t tile = buf0 + (uint32_t)kb * tile_bytes;
+    if (!abort) decode_regs<D, NT>(P.bits, pl, r, ct, n_valid_of(t), tile);
+    // the stores before the tensor cores and the bulk copy (async proxy) read them
     asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(full + 8 * kb) : "memory");
+    asm volatile("bar.sync %0, %1;\n" ::"n"(BAR_ID), "n"(NT) : "memory");
+    if (ptid == 0) {
+      asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(full + 8 * kb) : "memory");
+      if (!abort) {
+        const uint32_t pbar = peer_full + 8 * kb;
+        asm volatile("mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;\n" ::"r"(pbar),
+                     "n"(kHalfBytes)
+                     : "memory");
+        asm volatile(
+            "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+                peer_buf0 + (uint32_t)kb * tile_bytes + half_off),
+            "r"(tile + half_off), "n"(kHalfBytes), "r"(pbar)
+            : "memory");
+      }
+    }
   };
   if (n_tiles > 0) load(0, ra);
   for (int t = 0; t < n_tiles; t += 2) {
     step(t, ra, rn);
     if (t + 1 < n_tiles) step(t + 1, rn, ra);
   }
+  for (int t = n_tiles > NB ? n_tiles - NB : 0; t < n_tiles; ++t) wait(free_bar + 8 * (t % NB), (uint32_t)(t / NB) & 1);
 }
 
-// Warp-specialised prefill.  Warps 0-3 (softmax) own the 128 TMEM rows;
-// warp 4 issues the S products and warp 5 the O products; NK warps decode K
-// tiles and NV warps decode V tiles into NB-deep rings of shared buffers,
-// each side at its own pace.
+// Warp-specialised prefill, launched as clusters of two CTAs that take
+// consecutive 128-row tiles of the same (batch, KV head, context slice) and
+// share the tile decode (see decoder_role).  Warps 0-3 (softmax) own the 128
+// TMEM rows; warp 4 issues the S products and warp 5 the O products; NK warps
+// decode K tiles and NV warps decode V tiles into NB-deep rings of shared
+// buffers, each side at its own pace.
 // Handoffs go through mbarriers:
-//   kfull/vfull[b]  a decoded tile is in buffer b (every decoder of the side arrives)
-//   kfree/vfree[b]  the MMA that read buffer b is done (tcgen05.commit)
+//   kfull/vfull[b]  a decoded tile is in buffer b (one arrival for this CTA's
+//                   half, one with the byte count of the peer's half, whose
+//                   bulk copy completes the transaction)
+//   kfree/vfree[b]  the products that read buffer b are done in both CTAs
+//                   (a multicast tcgen05.commit from each)
 //   q_full          Q^ is in TMEM (one arrival per softmax warp)
 //   s_full          S(t) is in TMEM (commit)
 //   s_free          every softmax warp holds S(t) in registers (one arrival per warp)
@@ -396,11 +473,14 @@ __global__ void __launch_bounds__(192 + 32 * (NK + NV), 1) prefill_ws_kernel(con
   __shared__ CodeTabs s_tabs[2];   // K and V codebooks (fp16 pairs, unscaled 4-bit tables)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  uint32_t rank;   // 0 or 1 within the pair
+  asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(rank));
   const int G = a.Hq / a.Hkv;
   const int rt = blockIdx.x, split = blockIdx.y, bh = blockIdx.z;
   const int b = bh / a.Hkv, kvh = bh % a.Hkv;
   const int R = a.Tq * G;
-  const int last_row = min(rt * kRowsTc + kRowsTc, R) - 1;
+  // both CTAs of the pair walk the same tiles: the causal limit of the pair's last row
+  const int last_row = min((rt & ~1) * kRowsTc + 2 * kRowsTc, R) - 1;
   const int64_t max_pos = a.causal ? a.ctx - a.Tq + last_row / G : a.ctx - 1;
   const int64_t t_lo = (int64_t)split * a.per;
   const int64_t t_hi = imin64(imin64(t_lo + a.per, a.ctx), max_pos + 1);
@@ -422,6 +502,12 @@ __global__ void __launch_bounds__(192 + 32 * (NK + NV), 1) prefill_ws_kernel(con
     s_abort = 1;
     return false;
   };
+  auto wait_cl = [&](uint32_t bar, uint32_t parity) {   // barriers the peer CTA arrives on
+    if (s_abort) return false;
+    if (bar_wait<true>(bar, parity)) return true;
+    s_abort = 1;
+    return false;
+  };
 
   if (tid == 0) {
     s_tabs[0] = make_code_tabs(PK);
@@ -429,10 +515,10 @@ __global__ void __launch_bounds__(192 + 32 * (NK + NV), 1) prefill_ws_kernel(con
     s_abort = 0;
 #pragma unroll
     for (int i = 0; i < NB; ++i) {
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(kfull + 8 * i), "r"(kNK) : "memory");
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(vfull + 8 * i), "r"(kNV) : "memory");
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(kfree + 8 * i) : "memory");
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(vfree + 8 * i) : "memory");
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 2;\n" ::"r"(kfull + 8 * i) : "memory");
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 2;\n" ::"r"(vfull + 8 * i) : "memory");
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 2;\n" ::"r"(kfree + 8 * i) : "memory");
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 2;\n" ::"r"(vfree + 8 * i) : "memory");
     }
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 4;\n" ::"r"(q_full) : "memory");
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(s_full) : "memory");
@@ -450,8 +536,9 @@ __global__ void __launch_bounds__(192 + 32 * (NK + NV), 1) prefill_ws_kernel(con
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
   }
+  // both CTAs' barriers are initialised before either arrives on the other's
   fence_before();
-  __syncthreads();
+  cluster_sync();
   fence_after();
   const uint32_t tmem = tmem_base;
   // a softmax warp's signal: its lanes' TMEM accesses are complete, then one arrival
@@ -468,11 +555,11 @@ __global__ void __launch_bounds__(192 + 32 * (NK + NV), 1) prefill_ws_kernel(con
     // the decode.
     if (RB) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(kDecRegs));
     if (warp < 6 + NK)
-      decoder_role<D, kNK, NB>(PK, s_tabs[0], a.kc, a.ks, tid - 192, kfull, kfree, aK(0), kTileBytes, rec0, t_lo,
-                               n_tiles, n_valid_of, wait, s_abort);
+      decoder_role<D, kNK, NB, 1>(PK, s_tabs[0], a.kc, a.ks, tid - 192, kfull, kfree, aK(0), kTileBytes, rec0, t_lo,
+                               n_tiles, rank, n_valid_of, wait_cl, s_abort);
     else
-      decoder_role<D, kNV, NB>(PV, s_tabs[1], a.vc, a.vs, tid - 192 - kNK, vfull, vfree, aV(0), kTileBytes, rec0,
-                               t_lo, n_tiles, n_valid_of, wait, s_abort);
+      decoder_role<D, kNV, NB, 2>(PV, s_tabs[1], a.vc, a.vs, tid - 192 - kNK, vfull, vfree, aV(0), kTileBytes, rec0,
+                               t_lo, n_tiles, rank, n_valid_of, wait_cl, s_abort);
   } else if (warp == 4) {
     // ================= S issue: S(t) = Q^ (TMEM) K^(t)^T once K(t) is decoded
     // and S(t-1) has been read.  The whole warp walks the schedule, one
@@ -483,7 +570,7 @@ __global__ void __launch_bounds__(192 + 32 * (NK + NV), 1) prefill_ws_kernel(con
     bool ok = n_tiles > 0 && wait(q_full, 0);
     for (int t = 0; t < n_tiles && ok; ++t) {
       const int kb = t % NB;
-      ok = wait(kfull + 8 * kb, (uint32_t)(t / NB) & 1) && (t == 0 || wait(s_free, (uint32_t)(t - 1) & 1));
+      ok = wait_cl(kfull + 8 * kb, (uint32_t)(t / NB) & 1) && (t == 0 || wait(s_free, (uint32_t)(t - 1) & 1));
       if (!ok) break;
       fence_after();
       __syncwarp();
@@ -494,7 +581,7 @@ __global__ void __launch_bounds__(192 + 32 * (NK + NV), 1) prefill_ws_kernel(con
       for (int s = 0; s < D / 16; ++s)
         mma_ts_elect(tmem + kColS, tmem + kColQ + 8 * s, dk + (uint64_t)(16 * s), idesc_s, s > 0);
       commit_elect(s_full);
-      commit_elect(kfree + 8 * kb);
+      commit_elect_pair(kfree + 8 * kb);
     }
   } else if (warp == 5) {
     // ================= O issue: O += P(t) (TMEM) V^(t) once P(t) is written
@@ -504,7 +591,7 @@ __global__ void __launch_bounds__(192 + 32 * (NK + NV), 1) prefill_ws_kernel(con
     bool ok = true;
     for (int t = 0; t < n_tiles && ok; ++t) {
       const int vb = t % NB, pb = t & 1;
-      ok = wait(p_full + 8 * pb, (uint32_t)(t >> 1) & 1) && wait(vfull + 8 * vb, (uint32_t)(t / NB) & 1);
+      ok = wait(p_full + 8 * pb, (uint32_t)(t >> 1) & 1) && wait_cl(vfull + 8 * vb, (uint32_t)(t / NB) & 1);
       if (!ok) break;
       fence_after();
       __syncwarp();
@@ -514,7 +601,7 @@ __global__ void __launch_bounds__(192 + 32 * (NK + NV), 1) prefill_ws_kernel(con
         mma_ts_elect(tmem + kColO, tmem + kColP + 32 * pb + 8 * s, dv + (uint64_t)(s * (2 * kGroupBytes >> 4)),
                      idesc_o, (t == 0 && s == 0) ? 0 : 1);
       commit_elect(o_done + 8 * pb);
-      commit_elect(vfree + 8 * vb);
+      commit_elect_pair(vfree + 8 * vb);
     }
   } else {
     // ================= softmax: one row per thread
@@ -636,8 +723,9 @@ __global__ void __launch_bounds__(192 + 32 * (NK + NV), 1) prefill_ws_kernel(con
   }
   // the combine kernel may be scheduled now; it waits for this grid to finish
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+  // neither CTA leaves while the other may still store into its shared memory
   fence_before();
-  __syncthreads();
+  cluster_sync();
   if (tid == 0 && s_abort) atomicExch(a.err, 1);
   if (warp == 0) {
     fence_after();
@@ -686,7 +774,7 @@ int prefill_tc_splits(int B, int Hkv, int G, int Tq, int64_t ctx) {
   // One CTA per SM at a time: pick the context split that fills whole waves
   // best (at least 90% of the last wave busy), preferring fewer splits, each
   // split at least 4 tiles long.
-  const int row_tiles = (Tq * G + kRowsTc - 1) / kRowsTc;
+  const int row_tiles = (Tq * G + 2 * kRowsTc - 1) / (2 * kRowsTc) * 2;   // whole CTA pairs
   const int64_t ctas = (int64_t)row_tiles * B * Hkv;
   const int sms = sm_count();
   const int64_t max_by_len = (ctx + 4 * kTok - 1) / (4 * kTok);
@@ -705,9 +793,10 @@ int prefill_tc_splits(int B, int Hkv, int G, int Tq, int64_t ctx) {
   return best;
 }
 
+// Q^ rows are padded to whole CTA pairs (256 rows).
 size_t prefill_tc_workspace(int B, int Hq, int Hkv, int d, int Tq, int64_t ctx) {
   const int G = Hq / Hkv;
-  const int R_pad = (Tq * G + kRowsTc - 1) / kRowsTc * kRowsTc;
+  const int R_pad = (Tq * G + 2 * kRowsTc - 1) / (2 * kRowsTc) * (2 * kRowsTc);
   const int ns = prefill_tc_splits(B, Hkv, G, Tq, ctx);
   const size_t qbytes = (size_t)B * Hkv * R_pad * d * 2;
   const size_t pbytes = (size_t)B * Hq * Tq * ns * (d + 4) * 4;
@@ -732,16 +821,31 @@ int launch_ws(const CodecParams& PK, const CodecParams& PV, const PrefillTcArgs&
       use_rb = (fa.numRegs >= kDecRegs && fa.numRegs <= kConsRegs && launch >= need) ? 1 : 0;
     }
   }
+  // clusters of two CTAs along x (grid.x is even)
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.dynamicSmemBytes = sm;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e;
   if (use_rb) {
     auto k = prefill_ws_kernel<D, kDecK_RB, kDecV_RB, 3, true>;
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm)) return TQ_ERR_CUDA;
-    k<<<grid, kThreadsRB, sm, st>>>(PK, PV, a);
+    cfg.blockDim = dim3(kThreadsRB);
+    e = cudaLaunchKernelEx(&cfg, k, PK, PV, a);
   } else {
     auto k = prefill_ws_kernel<D, kDecK, kDecV, 3, false>;
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm)) return TQ_ERR_CUDA;
-    k<<<grid, kThreads, sm, st>>>(PK, PV, a);
+    cfg.blockDim = dim3(kThreads);
+    e = cudaLaunchKernelEx(&cfg, k, PK, PV, a);
   }
-  return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+  return e == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }
 
 int launch_prefill_tc(const CodecParams& PK, const CodecParams& PV, const uint8_t* kc, const uint16_t* ks,
@@ -750,7 +854,7 @@ int launch_prefill_tc(const CodecParams& PK, const CodecParams& PV, const uint8_
                       cudaStream_t st) {
   const int d = PK.d;
   const int G = Hq / Hkv;
-  const int R_pad = (Tq * G + kRowsTc - 1) / kRowsTc * kRowsTc;
+  const int R_pad = (Tq * G + 2 * kRowsTc - 1) / (2 * kRowsTc) * (2 * kRowsTc);
   const int ns = prefill_tc_splits(B, Hkv, G, Tq, ctx);
   uint8_t* base = static_cast<uint8_t*>(ws);
   int* err = reinterpret_cast<int*>(base);

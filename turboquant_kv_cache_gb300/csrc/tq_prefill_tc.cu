@@ -39,11 +39,11 @@ namespace {
 
 constexpr int kRowsTc = 128;     // query rows per CTA (TMEM lanes)
 constexpr int kTok = 64;         // tokens per KV tile
-// decoding warps (K side, V side): 8 + 6 with setmaxnreg rebalancing (20 warps
-// in all), 4 + 2 without (12 warps); 4-bit K codes cost more to decode than
-// 3-bit V codes, so the K side gets the extra warps
-constexpr int kDecK_RB = 8, kDecV_RB = 6, kDecK = 4, kDecV = 2;
-constexpr int kConsRegs = 128, kDecRegs = 88;
+// decoding warps (K side, V side): 9 + 9 with setmaxnreg rebalancing (24 warps
+// in all, so every decoder thread has at most one 32-code item of its half
+// tile at head_dim 256), 4 + 2 without (12 warps)
+constexpr int kDecK_RB = 9, kDecV_RB = 9, kDecK = 4, kDecV = 2;
+constexpr int kConsRegs = 128, kDecRegs = 64;
 constexpr uint32_t kColS = 0, kColP = 64;
 // TMEM columns: S (64 fp32) at 0, two P buffers (64 fp16 = 32 columns each) at
 // 64 and 96, Q^ (D fp16 = D/2 columns) at 128, O (D fp32) after it; a power
@@ -249,9 +249,11 @@ __device__ __forceinline__ uint32_t ldg32(const uint8_t* p) {
   asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(v) : "l"(p));
   return v;
 }
+// straight into a 32-bit register (zero-extended by the load itself, so no
+// instruction has to wait for the value before it is used)
 __device__ __forceinline__ uint32_t ldg16(const uint8_t* p) {
-  unsigned short v;
-  asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
+  uint32_t v;
+  asm volatile("ld.global.nc.u16 %0, [%1];" : "=r"(v) : "l"(p));
   return v;
 }
 
@@ -272,9 +274,17 @@ __device__ __forceinline__ void load_items_b(const ItemPlan<D, NT>& pl, const ui
         uint2 v;
         asm volatile("ld.global.nc.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(c));
         r.w[k][0] = v.x; r.w[k][1] = v.y;
+      } else if (BITS == 3) {
+        // 12 bytes at a 4-byte aligned offset: two 8-byte loads of the 16
+        // bytes around them (the decode picks the three words, so nothing
+        // waits on the loads here).  An 8-byte aligned group is never the
+        // last of its row (the last group index, d/32 - 1, is odd), so the
+        // second load stays inside the row.
+        const uint8_t* c8 = c - (pl.code_off[k] & 4u);
+        asm volatile("ld.global.nc.v2.u32 {%0,%1}, [%2];" : "=r"(r.w[k][0]), "=r"(r.w[k][1]) : "l"(c8));
+        asm volatile("ld.global.nc.v2.u32 {%0,%1}, [%2];" : "=r"(r.w[k][2]), "=r"(r.w[k][3]) : "l"(c8 + 8));
       } else {
-#pragma unroll
-        for (int b = 0; b < BITS; ++b) r.w[k][b] = ldg32(c + 4 * b);
+        r.w[k][0] = ldg32(c);
       }
       r.sc[k] = ldg16(scales + pl.sc_off[k]);
     }
@@ -304,7 +314,13 @@ __device__ __forceinline__ void decode_regs_b(const ItemPlan<D, NT>& pl, const I
     const uint32_t dst = pl.dst_off[k];
     if (n_valid == kTok || pl.tok[k] < n_valid) {
       uint32_t n[4];
-      chunk_words<BITS>(r.w[k], n);
+      if (BITS == 3) {   // the group's three words out of the 16 loaded bytes
+        const bool sh = (pl.code_off[k] & 4u) != 0;
+        const uint32_t w3[3] = {sh ? r.w[k][1] : r.w[k][0], sh ? r.w[k][2] : r.w[k][1], sh ? r.w[k][3] : r.w[k][2]};
+        chunk_words<3>(w3, n);
+      } else {
+        chunk_words<BITS>(r.w[k], n);
+      }
       const uint32_t sc = r.sc[k];
       Tab T;
       uint32_t s2 = 0;
@@ -378,9 +394,8 @@ struct PrefillTcArgs {
 // block (32 d fp16), which one thread then copies into the same place in the
 // peer CTA with a bulk shared::cluster copy that completes on the peer's full
 // barrier.  So each CTA holds whole tiles for its own MMAs at half the decode
-// work.  Each thread loads its items' packed words for tile t+1 into
-// registers before decoding tile t, so the global latency hides behind the
-// decode.  Buffer t % NB is refilled once the products that read it NB tiles
+// work.  Each thread loads its items' packed words two tiles ahead into
+// registers, so the global latency hides behind two tile decodes.  Buffer t % NB is refilled once the products that read it NB tiles
 // earlier have completed in both CTAs (its free barrier takes a commit from
 // each; the peer's commit also implies that the copy out of this buffer has
 // landed).  Before returning, the role waits for the products of its last
@@ -396,13 +411,14 @@ __device__ __forceinline__ void decoder_role(const CodecParams& P, const CodeTab
   const ItemPlan<D, NT> pl = make_plan<D, NT>(P, ptid, (int)rank * ItemPlan<D, NT>::TOK);
   const uint32_t half_off = rank * kHalfBytes;
   const uint32_t peer_buf0 = mapa_peer(buf0, rank ^ 1u), peer_full = mapa_peer(full, rank ^ 1u);
-  ItemRegs<D, NT> ra, rn;
+  ItemRegs<D, NT> r0, r1, r2;
   auto load = [&](int t, ItemRegs<D, NT>& r) {
     const int64_t rec = rec0 + t_lo + (int64_t)t * kTok;
     load_items<D, NT>(P.bits, pl, codes + rec * P.code_bytes, scales + rec * 2 * P.nb, n_valid_of(t), r);
   };
-  auto step = [&](int t, const ItemRegs<D, NT>& r, ItemRegs<D, NT>& next) {
-    if (t + 1 < n_tiles) load(t + 1, next);
+  // tile t decodes from registers loaded two steps earlier; the load of tile
+  // t+2 is issued after tile t's arrivals, so no arrival waits on it
+  auto step = [&](int t, const ItemRegs<D, NT>& r, ItemRegs<D, NT>& next2) {
     const int kb = t % NB;
     if (t >= NB) wait(free_bar + 8 * kb, (uint32_t)(t / NB - 1) & 1);   // the products NB tiles back are done
     const uint32_t tile = buf0 + (uint32_t)kb * tile_bytes;
@@ -413,8 +429,9 @@ __device__ __forceinline__ void decoder_role(const CodecParams& P, const CodeTab
     if (ptid == 0) {
       asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(full + 8 * kb) : "memory");
       if (!abort) {
+        // only a byte count: the data itself is ordered by the copy's complete_tx
         const uint32_t pbar = peer_full + 8 * kb;
-        asm volatile("mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;\n" ::"r"(pbar),
+        asm volatile("mbarrier.arrive.expect_tx.relaxed.cluster.shared::cluster.b64 _, [%0], %1;\n" ::"r"(pbar),
                      "n"(kHalfBytes)
                      : "memory");
         asm volatile(
@@ -424,11 +441,14 @@ __device__ __forceinline__ void decoder_role(const CodecParams& P, const CodeTab
             : "memory");
       }
     }
+    if (t + 2 < n_tiles) load(t + 2, next2);
   };
-  if (n_tiles > 0) load(0, ra);
-  for (int t = 0; t < n_tiles; t += 2) {
-    step(t, ra, rn);
-    if (t + 1 < n_tiles) step(t + 1, rn, ra);
+  if (n_tiles > 0) load(0, r0);
+  if (n_tiles > 1) load(1, r1);
+  for (int t = 0; t < n_tiles; t += 3) {
+    step(t, r0, r2);
+    if (t + 1 < n_tiles) step(t + 1, r1, r0);
+    if (t + 2 < n_tiles) step(t + 2, r2, r1);
   }
   for (int t = n_tiles > NB ? n_tiles - NB : 0; t < n_tiles; ++t) wait(free_bar + 8 * (t % NB), (uint32_t)(t / NB) & 1);
 }
@@ -803,7 +823,7 @@ size_t prefill_tc_workspace(int B, int Hq, int Hkv, int d, int Tq, int64_t ctx) 
   return 256 + ((qbytes + 255) / 256) * 256 + pbytes;
 }
 
-// The warp-specialised kernel with 14 decoder warps and setmaxnreg moving
+// The warp-specialised kernel with 18 decoder warps and setmaxnreg moving
 // registers to the softmax warps, when its launch register count makes that
 // split exact (launch total >= softmax + other shares); otherwise 6 decoder
 // warps without rebalancing.

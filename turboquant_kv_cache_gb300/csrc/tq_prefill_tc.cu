@@ -426,7 +426,7 @@ __device__ __forceinline__ void decoder_role(const CodecParams& P, const CodeTab
     // the stores before the tensor cores and the bulk copy (async proxy) read them
     asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
     asm volatile("bar.sync %0, %1;\n" ::"n"(BAR_ID), "n"(NT) : "memory");
-    if (ptid == 0) {
+    if (ptid == NT - 32) {   // the last warp's first thread: it has no item when the half tile has fewer items than threads
       asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(full + 8 * kb) : "memory");
       if (!abort) {
         // only a byte count: the data itself is ordered by the copy's complete_tx

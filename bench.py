@@ -264,17 +264,15 @@ def e2e_decode(tb, torch, inputs, dev, K, V, L, ws, n_split, args):
     q_d = torch.empty((B, Hq, d), dtype=torch.float16, device=dev)
     kv_d = torch.empty((2, B, Hkv, d), dtype=torch.float16, device=dev)
     out_d = torch.empty_like(q_d)
-    # the new token of every (b, head) lands in cache slot ctx-1
-    k_slot = tb.PackedKV(L, (B, Hkv), device=dev)
+    # the new token of every (b, head) is quantised straight into cache slot ctx-1
+    pos = torch.full((B,), ctx - 1, dtype=torch.int32, device=dev)
     nbytes = decode_bytes(B, Hkv, ctx, d, 3, 3, 32, 32)
 
     def step():
         q_d.copy_(q_h, non_blocking=True)
         kv_d.copy_(kv_h, non_blocking=True)
         for i, cache in enumerate((K, V)):
-            tb.tq_quantize_kv(L, kv_d[i], out=k_slot)
-            cache.codes[:, :, ctx - 1].copy_(k_slot.codes)
-            cache.scales[:, :, ctx - 1].copy_(k_slot.scales)
+            tb.tq_append_kv(cache, kv_d[i].unsqueeze(2), pos)
         tb.tq_decode_attn(K, V, q_d, ctx=ctx, workspace=ws, out=out_d, n_split=n_split)
         out_h.copy_(out_d, non_blocking=True)
 

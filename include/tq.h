@@ -125,6 +125,27 @@ int tq_quantize_kv(const tq_layout* layout, const void* x, tq_dtype x_dtype, int
                    int64_t x_row_stride, const float* S, uint8_t* codes, uint16_t* scales,
                    uint8_t* qjl_bits, uint16_t* qjl_rnorm, void* stream);
 
+/* Quantise new tokens straight into their slots of a preallocated cache
+ * (device).  Every key and value is quantised as it enters the cache
+ * ("TurboQuant From Scratch on Real KV Tensors", section 1, the cache
+ * update); this is tq_quantize_kv with the output records placed by
+ * position instead of by input order.
+ *   x            device, B*H*n_new rows ordered (b, h, j), row i at
+ *                x + i*x_row_stride elements, x_dtype fp16 or fp32, 16-byte
+ *                aligned rows (as tq_quantize_kv)
+ *   pos          device int32 [B]: token j of (b, h) goes to cache slot
+ *                pos[b] + j; slots outside [0, S_cap) are not written
+ *                (nothing else is touched)
+ *   codes, scales, qjl_bits, qjl_rnorm
+ *                the cache arrays [B, H, S_cap, ...] in the tq_kv_view layout
+ *   S            device fp32 [qjl_m, d] (QJL only, else NULL)
+ * Returns TQ_ERR_ARG for negative sizes or a NULL pos, the tq_quantize_kv
+ * errors otherwise; B*H*n_new == 0 is a no-op.  The records written are
+ * identical to tq_quantize_kv of the same rows. */
+int tq_append_kv(const tq_layout* layout, const void* x, tq_dtype x_dtype, int B, int H, int n_new,
+                 int64_t x_row_stride, const int32_t* pos, int64_t S_cap, const float* S, uint8_t* codes,
+                 uint16_t* scales, uint8_t* qjl_bits, uint16_t* qjl_rnorm, void* stream);
+
 /* Decode n_vec packed vectors (device) into out [n_vec, d] (fp16 or fp32):
  * x~ = scale * D H (c + [QJL] rho sqrt(pi/2)/m H D S^T (2s - 1)), i.e.
  * unpack -> centroid lookup -> inverse rotation -> x scale

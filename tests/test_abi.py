@@ -82,6 +82,26 @@ def test_host_side_argument_checks_need_no_gpu(tqlib):
     assert tqlib.tq_layout_sizes(ctypes.byref(bad), None, None, None) == -1
 
 
+def test_append_argument_checks_need_no_gpu(tqlib):
+    L = tb.make_layout(128, 32, 3)
+    P16 = ctypes.c_void_p(16)
+    # no tokens: nothing to do, even without buffers
+    assert tqlib.tq_append_kv(ctypes.byref(L), None, 0, 2, 8, 0, 128, None, 64, None, None, None, None, None,
+                              None) == 0
+    # negative sizes, a missing position array or S_cap 0 are refused
+    assert tqlib.tq_append_kv(ctypes.byref(L), P16, 0, -1, 8, 1, 128, P16, 64, None, P16, P16, None, None,
+                              None) == -1
+    assert tqlib.tq_append_kv(ctypes.byref(L), P16, 0, 2, 8, 1, 128, None, 64, None, P16, P16, None, None,
+                              None) == -1
+    assert tqlib.tq_append_kv(ctypes.byref(L), P16, 0, 2, 8, 1, 128, P16, 0, None, P16, P16, None, None,
+                              None) == -1
+    # then the quantise checks: misaligned rows, bad stride
+    assert tqlib.tq_append_kv(ctypes.byref(L), ctypes.c_void_p(18), 0, 2, 8, 1, 128, P16, 64, None, P16, P16,
+                              None, None, None) == -3
+    assert tqlib.tq_append_kv(ctypes.byref(L), P16, 0, 2, 8, 1, 64, P16, 64, None, P16, P16, None, None,
+                              None) == -1
+
+
 def _decode_ws(B, Hq, d, ns):
     # split partials [B*Hq][n_split][d + 4] fp32, rounded up to 256 bytes, then
     # the tensor-core path's S q rows (fp16, m = 128) and row sums of QJL keys

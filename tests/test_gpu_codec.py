@@ -114,3 +114,79 @@ def test_quantize_row_stride_and_alignment(tqlib):
     with pytest.raises(tb.TQError) as e:
         tb.tq_quantize_kv(L, base.reshape(-1)[1:1 + 128 * 63].reshape(63, 128))
     assert e.value.status == -3
+
+
+APPEND_CASES = [
+    # d, block, bits, dtype, nc, qjl_m  (fast, general and QJL quantise kernels)
+    (128, 32, 3, np.float16, 0, 0),
+    (64, 64, 4, np.float16, 0, 0),
+    (128, 64, 1, np.float32, 0, 0),
+    (128, 128, 2, np.float16, 1, 0),
+    (128, 128, 2, np.float16, 0, 128),
+    (128, 128, 3, np.float32, 0, 64),
+]
+
+
+@pytest.mark.parametrize("d,blk,bits,dt,nc,m", APPEND_CASES)
+def test_append_into_cache_matches_oracle(tqlib, d, blk, bits, dt, nc, m):
+    """tq_append_kv writes token j of (b, h) to slot pos[b] + j of a
+    [B, H, S_cap] cache: the records equal tq_quantize_kv of the same rows
+    (and the oracle), slots past S_cap and every other slot stay as they
+    were."""
+    from turboquant_kv_cache_gb300 import binding as tb
+    B, H, n_new, S_cap = 3, 2, 5, 40
+    pos = np.array([0, 17, 37], dtype=np.int32)          # the last batch runs past the end
+    x = _x(B * H * n_new, d, 300 + d + bits + m, dt).reshape(B, H, n_new, d)
+    S = inputs.qjl_matrix(m, d, 7) if m else None
+    L = tb.make_layout(d, blk, bits, m, nc, 1)
+    Lo = O.Layout(d, blk, bits, m, nc, 1)
+    Sg = torch.from_numpy(S).cuda() if m else None
+    cache = tb.PackedKV(L, (B, H, S_cap), device="cuda", S=Sg)
+    cache.codes.fill_(0xA5)
+    cache.scales.view(torch.int16).fill_(0x1357)
+    if m:
+        cache.qjl.fill_(0x5A)
+        cache.rnorm.view(torch.int16).fill_(0x2468)
+    before = {k: to_np(v).copy() for k, v in (("codes", cache.codes), ("scales", cache.scales),
+                                              ("qjl", cache.qjl), ("rnorm", cache.rnorm)) if v is not None}
+    xg = torch.from_numpy(x).cuda()
+    tb.tq_append_kv(cache, xg, torch.from_numpy(pos).cuda())
+    ref = tb.tq_quantize_kv(L, xg.reshape(-1, d), S=Sg)
+    torch.cuda.synchronize()
+    written = np.zeros((B, H, S_cap), dtype=bool)
+    rows, slots = [], []
+    for b in range(B):
+        for h in range(H):
+            for j in range(n_new):
+                s = pos[b] + j
+                if s < S_cap:
+                    written[b, h, s] = True
+                    rows.append((b * H + h) * n_new + j)
+                    slots.append((b, h, s))
+    rows = np.array(rows)
+    sl = tuple(np.array(slots).T)
+    got = {k: to_np(v) for k, v in (("codes", cache.codes), ("scales", cache.scales),
+                                    ("qjl", cache.qjl), ("rnorm", cache.rnorm)) if v is not None}
+    refs = {k: to_np(v) for k, v in (("codes", ref.codes), ("scales", ref.scales),
+                                     ("qjl", ref.qjl), ("rnorm", ref.rnorm)) if v is not None}
+    for k in got:
+        assert np.array_equal(got[k][sl], refs[k][rows]), k          # same kernel, same records
+        assert np.array_equal(got[k][~written], before[k][~written]), k   # nothing else touched
+    oq = O.quantize(x.reshape(-1, d)[rows], Lo, S)
+    n_code, bad = compare_codes(got["codes"][sl], oq, Lo)
+    assert n_code <= 5
+    compare_scales(got["scales"][sl][~bad], oq["scale"][~bad], max_frac=2e-2 if (m and nc) else 1e-3)
+
+
+def test_append_no_tokens_and_errors(tqlib):
+    from turboquant_kv_cache_gb300 import binding as tb
+    L = tb.make_layout(128, 32, 3)
+    cache = tb.PackedKV(L, (2, 2, 8), device="cuda")
+    cache.codes.fill_(7)
+    x = torch.zeros((2, 2, 0, 128), dtype=torch.float16, device="cuda")
+    tb.tq_append_kv(cache, x, torch.zeros(2, dtype=torch.int32, device="cuda"))
+    torch.cuda.synchronize()
+    assert bool((cache.codes == 7).all())
+    with pytest.raises(ValueError):
+        tb.tq_append_kv(cache, torch.zeros((2, 2, 1, 128), dtype=torch.float16, device="cuda"),
+                        torch.zeros(2, dtype=torch.int64, device="cuda"))

@@ -50,6 +50,7 @@ def _load():
         "tq_signs": (I, [ctypes.c_uint64, I, P]),
         "tq_layout_sizes": (I, [P, P, P, P]),
         "tq_quantize_kv": (I, [P, P, I, I64, I64, P, P, P, P, P, P]),
+        "tq_append_kv": (I, [P, P, I, I, I, I, I64, P, I64, P, P, P, P, P, P]),
         "tq_dequantize_kv": (I, [P, P, P, P, P, P, I64, P, I, P]),
         "tq_decode_attn": (I, [P, P, P, I, I, I, I64, P, I64, ctypes.c_float, P, P, SZ, I, P]),
         "tq_decode_workspace_bytes": (I, [I, I, I, I, I64, I, P, P]),
@@ -196,6 +197,29 @@ def tq_quantize_kv(layout, x, S=None, out=None, stream=None):
                             _ptr(out.codes), _ptr(out.scales), _ptr(out.qjl), _ptr(out.rnorm), _stream(stream))
     _check(st, "tq_quantize_kv")
     return out
+
+
+def tq_append_kv(cache, x, pos, stream=None):
+    """Quantise new tokens x [B, H, n_new, d] (fp16/fp32, CUDA, last dim
+    contiguous, rows of one (b, h) contiguous) into a PackedKV cache of
+    leading shape [B, H, S_cap]: token j of (b, h) lands in slot pos[b] + j
+    (pos: int32 CUDA tensor [B]); slots outside [0, S_cap) are skipped."""
+    lib = _load()
+    layout = cache.layout
+    d = layout.head_dim
+    if x.dim() != 4 or x.shape[-1] != d or x.stride(-1) != 1:
+        raise ValueError("x must be [B, H, n_new, head_dim] with a contiguous last dimension")
+    B, H, n_new, _ = x.shape
+    if len(cache.lead_shape) != 3 or tuple(cache.lead_shape[:2]) != (B, H):
+        raise ValueError("cache must have leading shape [B, H, S_cap] matching x")
+    if pos.dtype != torch.int32 or pos.numel() != B or not pos.is_cuda:
+        raise ValueError("pos must be an int32 CUDA tensor of B slot offsets")
+    x2 = x.reshape(-1, d)
+    st = lib.tq_append_kv(ctypes.byref(layout), _ptr(x2), _dtype_code(x.dtype), B, H, n_new, x2.stride(0),
+                          _ptr(pos.contiguous()), cache.lead_shape[2], _ptr(cache.S), _ptr(cache.codes),
+                          _ptr(cache.scales), _ptr(cache.qjl), _ptr(cache.rnorm), _stream(stream))
+    _check(st, "tq_append_kv")
+    return cache
 
 
 def tq_dequantize_kv(packed, out_dtype=torch.float16, stream=None):

@@ -13,10 +13,11 @@ namespace tq {
 
 bool quantize_fast_eligible(const CodecParams& P, bool f32_input);
 int launch_quantize_fast(const CodecParams& P, const void* x, int64_t n_vec, int64_t stride, uint8_t* codes,
-                         uint16_t* scales, cudaStream_t st);
+                         uint16_t* scales, const RowMap& map, cudaStream_t st);
 bool quantize_qjl_eligible(const CodecParams& P);
 int launch_quantize_qjl(const CodecParams& P, const void* x, bool f32, int64_t n_vec, int64_t stride, const float* S,
-                        uint8_t* codes, uint16_t* scales, uint8_t* qjl_bits, uint16_t* qjl_rnorm, cudaStream_t st);
+                        uint8_t* codes, uint16_t* scales, uint8_t* qjl_bits, uint16_t* qjl_rnorm, const RowMap& map,
+                        cudaStream_t st);
 
 namespace {
 
@@ -31,6 +32,7 @@ struct QuantArgs {
   uint16_t* scales;
   uint32_t* qjl;
   uint16_t* rnorm;
+  RowMap map;   // vector -> record
 };
 
 template <int D, bool F32>
@@ -62,6 +64,7 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(const CodecParams P,
        base += nwarps * VPW) {
     const int64_t v = base + vs;
     const bool valid = v < a.n_vec;
+    const int64_t rv = valid ? map_row(a.map, v) : -1;   // output record
     float x[8];
     if (valid) {
       if (F32) {
@@ -147,9 +150,9 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(const CodecParams P,
         }
       }
       __syncwarp();
-      if (valid && sub < P.m / 32) a.qjl[v * (P.m / 32) + sub] = s_bits[wid][vs][sub];
+      if (rv >= 0 && sub < P.m / 32) a.qjl[rv * (P.m / 32) + sub] = s_bits[wid][vs][sub];
       const float rho16 = __half2float(__float2half_rn(rho));
-      if (valid && sub == 0) a.rnorm[v] = f2h(rho);
+      if (rv >= 0 && sub == 0) a.rnorm[rv] = f2h(rho);
       if (P.nc) {  // renormalise the QJL-corrected direction
         float u[8];
 #pragma unroll
@@ -174,13 +177,13 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(const CodecParams P,
       __syncwarp();
     }
     // S7: pack and store
-    if (valid && (sub % tpb) == 0) a.scales[v * P.nb + sub / tpb] = f2h(scale);
+    if (rv >= 0 && (sub % tpb) == 0) a.scales[rv * P.nb + sub / tpb] = f2h(scale);
     const int gi = sub >> 2, w = sub & 3;
-    uint32_t* rec = a.codes + v * words_per_vec;
+    uint32_t* rec = a.codes + rv * words_per_vec;
     const uint32_t n1 = __shfl_sync(kFull, nib, lane + 1 < 32 ? lane + 1 : lane);
     const uint32_t n2 = __shfl_sync(kFull, nib, lane + 2 < 32 ? lane + 2 : lane);
     const uint32_t n3 = __shfl_sync(kFull, nib, lane | 3);
-    if (valid) {
+    if (rv >= 0) {
       switch (P.bits) {
         case 4: rec[gi * 4 + w] = nib; break;
         case 3:
@@ -296,11 +299,15 @@ int launch_dequantize(const CodecParams& P, const DequantArgs& a, bool f32, cuda
 }  // namespace
 }  // namespace tq
 
-extern "C" int tq_quantize_kv(const tq_layout* layout, const void* x, tq_dtype x_dtype, int64_t n_vec,
-                              int64_t x_row_stride, const float* S, uint8_t* codes, uint16_t* scales,
-                              uint8_t* qjl_bits, uint16_t* qjl_rnorm, void* stream) {
-  tq::CodecParams P;
-  int st = tq::make_params(layout, &P);
+namespace tq {
+namespace {
+
+// tq_quantize_kv and tq_append_kv: checks, then the fastest eligible kernel.
+int quantize_common(const tq_layout* layout, const void* x, tq_dtype x_dtype, int64_t n_vec, int64_t x_row_stride,
+                    const float* S, uint8_t* codes, uint16_t* scales, uint8_t* qjl_bits, uint16_t* qjl_rnorm,
+                    const RowMap& map, void* stream) {
+  CodecParams P;
+  int st = make_params(layout, &P);
   if (st != TQ_OK) return st;
   if (x_dtype != TQ_F16 && x_dtype != TQ_F32) return TQ_ERR_ARG;
   if (n_vec < 0 || x_row_stride < P.d) return TQ_ERR_ARG;
@@ -308,21 +315,42 @@ extern "C" int tq_quantize_kv(const tq_layout* layout, const void* x, tq_dtype x
   if (!x || !codes || !scales) return TQ_ERR_ARG;
   if (P.m && (!S || !qjl_bits || !qjl_rnorm)) return TQ_ERR_ARG;
   const int esz = x_dtype == TQ_F32 ? 4 : 2;
-  if (!tq::aligned16(x) || (x_row_stride * esz) % 16 || !tq::aligned16(codes) || !tq::aligned16(scales))
-    return TQ_ERR_ALIGN;
-  if (P.m && (!tq::aligned16(S) || !tq::aligned16(qjl_bits) || !tq::aligned16(qjl_rnorm))) return TQ_ERR_ALIGN;
-  tq::QuantArgs a{x, n_vec, x_row_stride, S, reinterpret_cast<uint32_t*>(codes), scales,
-                  reinterpret_cast<uint32_t*>(qjl_bits), qjl_rnorm};
+  if (!aligned16(x) || (x_row_stride * esz) % 16 || !aligned16(codes) || !aligned16(scales)) return TQ_ERR_ALIGN;
+  if (P.m && (!aligned16(S) || !aligned16(qjl_bits) || !aligned16(qjl_rnorm))) return TQ_ERR_ALIGN;
+  QuantArgs a{x, n_vec, x_row_stride, S, reinterpret_cast<uint32_t*>(codes), scales,
+              reinterpret_cast<uint32_t*>(qjl_bits), qjl_rnorm, map};
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool f32 = x_dtype == TQ_F32;
-  if (tq::quantize_fast_eligible(P, f32)) return tq::launch_quantize_fast(P, x, n_vec, x_row_stride, codes, scales, s);
-  if (tq::quantize_qjl_eligible(P))
-    return tq::launch_quantize_qjl(P, x, f32, n_vec, x_row_stride, S, codes, scales, qjl_bits, qjl_rnorm, s);
+  if (quantize_fast_eligible(P, f32)) return launch_quantize_fast(P, x, n_vec, x_row_stride, codes, scales, map, s);
+  if (quantize_qjl_eligible(P))
+    return launch_quantize_qjl(P, x, f32, n_vec, x_row_stride, S, codes, scales, qjl_bits, qjl_rnorm, map, s);
   switch (P.d) {
-    case 64: return tq::launch_quantize<64>(P, a, f32, s);
-    case 128: return tq::launch_quantize<128>(P, a, f32, s);
-    default: return tq::launch_quantize<256>(P, a, f32, s);
+    case 64: return launch_quantize<64>(P, a, f32, s);
+    case 128: return launch_quantize<128>(P, a, f32, s);
+    default: return launch_quantize<256>(P, a, f32, s);
   }
+}
+
+}  // namespace
+}  // namespace tq
+
+extern "C" int tq_quantize_kv(const tq_layout* layout, const void* x, tq_dtype x_dtype, int64_t n_vec,
+                              int64_t x_row_stride, const float* S, uint8_t* codes, uint16_t* scales,
+                              uint8_t* qjl_bits, uint16_t* qjl_rnorm, void* stream) {
+  const tq::RowMap identity{nullptr, 1, 1, 0};
+  return tq::quantize_common(layout, x, x_dtype, n_vec, x_row_stride, S, codes, scales, qjl_bits, qjl_rnorm,
+                             identity, stream);
+}
+
+extern "C" int tq_append_kv(const tq_layout* layout, const void* x, tq_dtype x_dtype, int B, int H, int n_new,
+                            int64_t x_row_stride, const int32_t* pos, int64_t S_cap, const float* S, uint8_t* codes,
+                            uint16_t* scales, uint8_t* qjl_bits, uint16_t* qjl_rnorm, void* stream) {
+  if (B < 0 || H < 0 || n_new < 0 || S_cap < 0) return TQ_ERR_ARG;
+  if ((int64_t)B * H * n_new == 0) return TQ_OK;
+  if (!pos || S_cap == 0) return TQ_ERR_ARG;
+  const tq::RowMap map{pos, n_new, H, S_cap};
+  return tq::quantize_common(layout, x, x_dtype, (int64_t)B * H * n_new, x_row_stride, S, codes, scales, qjl_bits,
+                             qjl_rnorm, map, stream);
 }
 
 extern "C" int tq_dequantize_kv(const tq_layout* layout, const uint8_t* codes, const uint16_t* scales,

@@ -22,6 +22,14 @@ __device__ __forceinline__ uint32_t sign_byte(const CodecParams& P, int i0) {
   return (P.sign_bits[i0 >> 5] >> (i0 & 31)) & 0xffu;
 }
 
+// Record of quantised vector i under a RowMap, or -1 when it is not stored.
+__device__ __forceinline__ int64_t map_row(const RowMap& m, int64_t i) {
+  if (!m.pos) return i;
+  const int64_t bh = i / m.n_new;
+  const int64_t slot = (int64_t)m.pos[bh / m.H] + (i - bh * m.n_new);
+  return (slot >= 0 && slot < m.S_cap) ? bh * m.S_cap + slot : -1;
+}
+
 __device__ __forceinline__ float flip(float v, uint32_t bit) {
   return __uint_as_float(__float_as_uint(v) ^ (bit << 31));
 }

@@ -37,4 +37,14 @@ int check_layout(const tq_layout* layout);
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Where quantised vector i is stored.  pos == NULL: record i.  Otherwise the
+// input holds n_new new tokens of every (batch, head) of a [B, H, S_cap]
+// cache, vector i = (b*H + h)*n_new + j, and it goes to record
+// (b*H + h)*S_cap + pos[b] + j; a slot outside [0, S_cap) is not written.
+struct RowMap {
+  const int32_t* pos;   // device [B], or NULL
+  int32_t n_new, H;
+  int64_t S_cap;
+};
+
 }  // namespace tq

@@ -29,8 +29,9 @@ struct FastQuantArgs {
   const __half* x;
   int64_t n_vec;
   int64_t stride;   // elements between rows
-  uint32_t* codes;  // [n_vec][words per vector]
+  uint32_t* codes;  // [records][words per vector]
   uint16_t* scales;
+  RowMap map;       // vector -> record
   float bstep[8];   // 2^20 * positive boundaries beta_{K/2} .. beta_{K-2}
   uint32_t sgn[128];  // fp16x2 +-1 multipliers of D, pairs (2i, 2i+1)
 };
@@ -177,11 +178,12 @@ __global__ void __launch_bounds__(kFW * 32) quantize_fast_kernel(const CodecPara
         for (int w = 0; w < 2; ++w) words[2 * gi + w] = N[w] | (N[w + 2] << 2);
       }
     }
-    if (v < a.n_vec) {
-      uint32_t* dst = a.codes + v * words_per_vec + j * WPB;
+    const int64_t r = v < a.n_vec ? map_row(a.map, v) : -1;
+    if (r >= 0) {
+      uint32_t* dst = a.codes + r * words_per_vec + j * WPB;
 #pragma unroll
       for (int w = 0; w < WPB; ++w) dst[w] = words[w];
-      a.scales[v * nb + j] = f2h(n);
+      a.scales[r * nb + j] = f2h(n);
     }
   }
 }
@@ -205,8 +207,9 @@ bool quantize_fast_eligible(const CodecParams& P, bool f32_input) {
 }
 
 int launch_quantize_fast(const CodecParams& P, const void* x, int64_t n_vec, int64_t stride, uint8_t* codes,
-                         uint16_t* scales, cudaStream_t st) {
+                         uint16_t* scales, const RowMap& map, cudaStream_t st) {
   FastQuantArgs a;
+  a.map = map;
   a.x = static_cast<const __half*>(x);
   a.n_vec = n_vec;
   a.stride = stride;

@@ -33,6 +33,7 @@ struct QjlArgs {
   uint16_t* scales;
   uint8_t* qjl;
   uint16_t* rnorm;
+  RowMap map;   // vector -> record
 };
 
 __device__ __forceinline__ uint32_t su32(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
@@ -159,13 +160,14 @@ __global__ void __launch_bounds__(kQT, 2) quantize_qjl_kernel(const CodecParams 
       *reinterpret_cast<uint4*>(sRlo + lv * LD + i0) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
       if (sub == 0) sRho[lv] = sqrtf(r2);
       // codes and the fp16 norm (one block per vector)
-      if (valid && sub == 0) a.scales[v] = f2h(n);
+      const int64_t rv = valid ? map_row(a.map, v) : -1;
+      if (rv >= 0 && sub == 0) a.scales[rv] = f2h(n);
       const int gi = sub >> 2, w = sub & 3;
-      uint32_t* rec = a.codes + v * words_per_vec;
+      uint32_t* rec = a.codes + rv * words_per_vec;
       const uint32_t n1 = __shfl_sync(kFull, nib, lane + 1 < 32 ? lane + 1 : lane);
       const uint32_t n2 = __shfl_sync(kFull, nib, lane + 2 < 32 ? lane + 2 : lane);
       const uint32_t n3 = __shfl_sync(kFull, nib, lane | 3);
-      if (valid) {
+      if (rv >= 0) {
         switch (P.bits) {
           case 4: rec[gi * 4 + w] = nib; break;
           case 3:
@@ -231,12 +233,14 @@ __global__ void __launch_bounds__(kQT, 2) quantize_qjl_kernel(const CodecParams 
     for (int e = tid; e < kQV * bpv / 4; e += kQT) {
       const int lv = (4 * e) / bpv;
       const int64_t v = v0 + lv;
-      if (v < a.n_vec)
-        *reinterpret_cast<uint32_t*>(a.qjl + v * bpv + (4 * e) % bpv) = *reinterpret_cast<const uint32_t*>(sBits + 4 * e);
+      const int64_t rv = v < a.n_vec ? map_row(a.map, v) : -1;
+      if (rv >= 0)
+        *reinterpret_cast<uint32_t*>(a.qjl + rv * bpv + (4 * e) % bpv) = *reinterpret_cast<const uint32_t*>(sBits + 4 * e);
     }
     for (int lv = tid; lv < kQV; lv += kQT) {
       const int64_t v = v0 + lv;
-      if (v < a.n_vec) a.rnorm[v] = f2h(sRho[lv]);
+      const int64_t rv = v < a.n_vec ? map_row(a.map, v) : -1;
+      if (rv >= 0) a.rnorm[rv] = f2h(sRho[lv]);
     }
     __syncthreads();
   }
@@ -277,8 +281,9 @@ bool quantize_qjl_eligible(const CodecParams& P) {
 }
 
 int launch_quantize_qjl(const CodecParams& P, const void* x, bool f32, int64_t n_vec, int64_t stride, const float* S,
-                        uint8_t* codes, uint16_t* scales, uint8_t* qjl_bits, uint16_t* qjl_rnorm, cudaStream_t st) {
-  QjlArgs a{x, n_vec, stride, S, reinterpret_cast<uint32_t*>(codes), scales, qjl_bits, qjl_rnorm};
+                        uint8_t* codes, uint16_t* scales, uint8_t* qjl_bits, uint16_t* qjl_rnorm, const RowMap& map,
+                        cudaStream_t st) {
+  QjlArgs a{x, n_vec, stride, S, reinterpret_cast<uint32_t*>(codes), scales, qjl_bits, qjl_rnorm, map};
   switch (P.d) {
     case 64: return f32 ? launch_qjl<64, true>(P, a, st) : launch_qjl<64, false>(P, a, st);
     case 128: return f32 ? launch_qjl<128, true>(P, a, st) : launch_qjl<128, false>(P, a, st);

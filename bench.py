@@ -142,6 +142,43 @@ def headline_cache(tb, torch, inputs, dev):
     return L, K, V, q
 
 
+def bench_depth(tb, torch, dev, L, K, V, q, steps, warm):
+    """The headline decode at growing context depth (same batch, heads and
+    layout): one tq_decode_attn call per step, L2 flushed before each.  Depths
+    up to the headline's 32768 read prefixes of its cache; 65536 and 131072
+    read a cache of that length made by repeating it along the context (the
+    kernel reads every byte either way).  GB/s that holds or rises with depth
+    is decode that does not degrade with context."""
+    B, Hq, Hkv, d = DEC["B"], DEC["Hq"], DEC["Hkv"], DEC["d"]
+    flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=dev)
+    out = torch.empty_like(q)
+    res = {}
+    S0 = K.lead_shape[2]
+    for ctx in (2048, 8192, 32768, 65536, 131072):
+        if ctx <= S0:
+            Kc, Vc = K, V
+        else:
+            rep_n = ctx // S0
+            Kc = tb.PackedKV(L, (B, Hkv, ctx), device=dev)
+            Vc = tb.PackedKV(L, (B, Hkv, ctx), device=dev)
+            for src, dst in ((K, Kc), (V, Vc)):
+                for r in range(rep_n):
+                    dst.codes[:, :, r * S0:(r + 1) * S0].copy_(src.codes)
+                    dst.scales[:, :, r * S0:(r + 1) * S0].copy_(src.scales)
+        ws_bytes, n_split = tb.tq_decode_workspace_bytes(B, Hq, Hkv, d, ctx, 0)
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+        ms = _time(torch, lambda: tb.tq_decode_attn(Kc, Vc, q, ctx=ctx, workspace=ws, out=out, n_split=n_split),
+                   flush, steps, warm)
+        nbytes = decode_bytes(B, Hkv, ctx, d, 3, 3, 32, 32)
+        res[str(ctx)] = {"us": round(ms * 1e3, 2), "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1),
+                         "n_split": n_split}
+        if Kc is not K:
+            del Kc, Vc
+            torch.cuda.empty_cache()
+    return {"workload": "the headline decode (B=8, Hq=32, Hkv=8, d=128, turbo3) at context depth 2K-128K",
+            "by_ctx": res}
+
+
 def run_only(args, tb, torch, inputs, dev):
     """One workload on its own (for profiler runs): the same inputs and calls
     as the full run, `--warmup` untimed then `--steps` timed passes, one JSON
@@ -160,6 +197,9 @@ def run_only(args, tb, torch, inputs, dev):
         res.update(workload=WORKLOAD, ms=round(ms, 5), GBps=round(nbytes / (ms * 1e-3) / 1e9, 1))
     elif args.only == "quantize":
         res.update(bench_quantize(tb, torch, inputs, dev, args))
+    elif args.only == "decode_depth":
+        L, K, V, q = headline_cache(tb, torch, inputs, dev)
+        res.update(bench_depth(tb, torch, dev, L, K, V, q, args.steps, args.warmup))
     else:
         res.update(bench_extra(tb, torch, inputs, dev, args, which=args.only))
     print(json.dumps(res), flush=True)
@@ -226,6 +266,7 @@ def run_gpu(args, rank, world):
     e2e = e2e_decode(tb, torch, inputs, dev, K, V, L, ws, n_split, args)
 
     quant = bench_quantize(tb, torch, inputs, dev, args)
+    depth = None if args.no_extra else bench_depth(tb, torch, dev, L, K, V, q, max(3, min(args.steps, 20)), 3)
     extra = {} if args.no_extra else bench_extra(tb, torch, inputs, dev, args)
     if rank == 0:
         line = {
@@ -244,6 +285,7 @@ def run_gpu(args, rank, world):
                          "kernel": "decode_tc_kernel + decode_combine_kernel (one tq_decode_attn call, events around both)"},
             "e2e": e2e,
             "quantize": quant,
+            "decode_vs_depth": depth,
             "other_workloads": extra,
             "gpu_launches": args.steps * 2,
             "clocks": clocks.summary(),
@@ -558,7 +600,7 @@ def main():
     ap.add_argument("--no-extra", action="store_true", help="skip the other workloads (headline only)")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--only", default=None,
-                    choices=["decode", "quantize", "prefill", "decode_d256", "decode_qjl", "quantize_qjl"],
+                    choices=["decode", "quantize", "prefill", "decode_d256", "decode_qjl", "quantize_qjl", "decode_depth"],
                     help="time one workload alone and print its result only (profiler runs)")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -53,6 +53,8 @@ typedef enum {
 
 typedef enum { TQ_F16 = 0, TQ_F32 = 1 } tq_dtype;
 
+typedef enum { TQ_CODEBOOK_GAUSSIAN = 0, TQ_CODEBOOK_BETA = 1 } tq_codebook_kind_t;
+
 /* Codec settings of one cache (K or V).
  *   head_dim      d in {64, 128, 256}
  *   block         rotation + norm block: a power of two >= 32 dividing d
@@ -63,6 +65,12 @@ typedef enum { TQ_F16 = 0, TQ_F32 = 1 } tq_dtype;
  *   norm_correct  0/1: store n / ||reconstructed direction|| instead of n,
  *                 so that the decoded block has the input's norm
  *                 ("TurboQuant From Scratch", section 2, "Norm correction")
+ *   codebook      TQ_CODEBOOK_GAUSSIAN (0): Lloyd-Max for N(0, 1/block);
+ *                 TQ_CODEBOOK_BETA (1): Lloyd-Max for the exact law of one
+ *                 coordinate of a random unit vector in R^block, i.e.
+ *                 (x + 1)/2 ~ Beta((block-1)/2, (block-1)/2)
+ *                 (llama.cpp-turboquant, "How it works"); other values are
+ *                 TQ_ERR_ARG
  *   sign_seed     seed of D: the i-th splitmix64 output (state = seed)
  *                 gives D_i = -1 when its top bit is set, else +1.  Block j
  *                 uses D[j*block .. (j+1)*block). */
@@ -72,7 +80,7 @@ typedef struct {
   int32_t bits;
   int32_t qjl_m;
   int32_t norm_correct;
-  int32_t reserved;
+  int32_t codebook;
   uint64_t sign_seed;
 } tq_layout;
 
@@ -97,6 +105,13 @@ typedef struct {
  * "TurboQuant From Scratch", section 2, step 3; section 3 (distortion
  * about 0.118 / 0.0345 / 0.0095 at 2 / 3 / 4 bits). */
 int tq_codebook(int bits, int block, float* centroids, float* boundaries);
+
+/* The codebook of a layout's `codebook` kind in double precision (host):
+ * TQ_CODEBOOK_GAUSSIAN is tq_codebook_f64; TQ_CODEBOOK_BETA solves
+ * Lloyd-Max for the density (1 - x^2)^((block-3)/2) / B(1/2, (block-1)/2)
+ * on [-1, 1] (block a power of two in 32..256, else TQ_ERR_UNSUPPORTED).
+ * boundaries may be NULL. */
+int tq_codebook_kind(int bits, int block, int kind, double* centroids, double* boundaries);
 
 /* Same codebook without the rounding to float (host, double). */
 int tq_codebook_f64(int bits, int block, double* centroids, double* boundaries);

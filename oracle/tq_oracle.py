@@ -22,7 +22,9 @@ source pages describe the method:
   values, i.e. the bytes per element the packed layout here keeps).
 
 Readings where the pages are silent (each also listed in the design notes):
-* Codebook target distribution: Gaussian N(0, 1/blk), blk = rotation block.
+* Codebook target distribution: Gaussian N(0, 1/blk), blk = rotation block
+  (codebook 0); codebook 1 is the exact Beta law of a rotated unit-vector
+  coordinate (a listed variant of the llama.cpp page).
 * Sign vector D: splitmix64 stream seeded with ``sign_seed``; D_i = -1 when
   the top bit of the i-th output is set.
 * Bucketize ties go to the lower code (code = #{k : y > beta_k}).
@@ -159,6 +161,75 @@ def lloyd_max_codebook(bits: int, blk: int, max_iter: int = 1000000):
     return cent, bnd
 
 
+def _beta_cell(alpha: float, e0: np.ndarray, e1: np.ndarray):
+    """Mass and first moment of the cells [e0, e1] under the law of one
+    coordinate of a uniformly random unit vector in R^blk, alpha = (blk-1)/2:
+    (x + 1)/2 ~ Beta(alpha, alpha), density (1 - x^2)^(alpha-1) / B(1/2, alpha).
+    The mass is the regularised incomplete beta function (scipy), taken
+    from the nearer end of [-1, 1]; the moment is exact:
+    int x (1 - x^2)^(alpha-1) dx = -(1 - x^2)^alpha / (2 alpha)."""
+    from scipy import special
+    z0, z1 = (1.0 + e0) / 2.0, (1.0 + e1) / 2.0
+    upper = e0 >= 0.0
+    low = special.betainc(alpha, alpha, z1) - special.betainc(alpha, alpha, z0)
+    high = special.betainc(alpha, alpha, 1.0 - z0) - special.betainc(alpha, alpha, 1.0 - z1)
+    mass = np.where(upper, high, low)
+    norm = special.beta(0.5, alpha)
+    mom = (np.power(np.clip(1.0 - e0 * e0, 0.0, None), alpha) -
+           np.power(np.clip(1.0 - e1 * e1, 0.0, None), alpha)) / (2.0 * alpha * norm)
+    return mass, mom
+
+
+def lloyd_max_beta_codebook(bits: int, blk: int):
+    """Lloyd-Max quantiser with 2^bits levels for the exact law of one
+    coordinate of a rotated unit vector in R^blk, (x + 1)/2 ~
+    Beta((blk-1)/2, (blk-1)/2) (llama.cpp-turboquant "How it works": the
+    Beta((d-1)/2, (d-1)/2) codebook).  The fixed point of "boundaries =
+    midpoints, centroids = conditional means", solved by a root finder on
+    step(c) - c from the scaled Gaussian codebook, then polished with plain
+    steps until they stop moving.  blk >= 2 (blk = 3: the uniform law on
+    [-1, 1]).  Returns (centroids ascending, boundaries), float64."""
+    from scipy import optimize
+    key = ("beta", bits, blk)
+    if key in _CODEBOOK_CACHE:
+        c, b = _CODEBOOK_CACHE[key]
+        return c.copy(), b.copy()
+    K = 1 << bits
+    alpha = 0.5 * (blk - 1)
+
+    def step(c):
+        edges = np.clip(np.concatenate([[-1.0], 0.5 * (c[1:] + c[:-1]), [1.0]]), -1.0, 1.0)
+        mass, mom = _beta_cell(alpha, edges[:-1], edges[1:])
+        return mom / mass
+
+    c0, _ = lloyd_max_codebook(bits, max(blk, 1))
+    c0 = np.clip(c0, -1.0 + 1.0 / K, 1.0 - 1.0 / K)
+    import warnings
+    with warnings.catch_warnings():   # fsolve reports the rounding floor as slow progress
+        warnings.simplefilter("ignore", RuntimeWarning)
+        c = optimize.fsolve(lambda v: step(v) - v, c0, xtol=1e-13)
+    last = math.inf
+    for _ in range(2000):
+        new = step(c)
+        delta = float(np.max(np.abs(new - c)))
+        c = new
+        if delta == 0.0 or (delta < 1e-17 and delta >= last):
+            break
+        last = delta
+    c = 0.5 * (c - c[::-1])
+    bnd = 0.5 * (c[1:] + c[:-1])
+    _CODEBOOK_CACHE[key] = (c.copy(), bnd.copy())
+    return c, bnd
+
+
+def codebook_for(L) -> tuple:
+    """The codebook a layout selects: Gaussian N(0, 1/blk) (codebook 0) or
+    the exact Beta law (codebook 1)."""
+    if getattr(L, "codebook", 0) == 1:
+        return lloyd_max_beta_codebook(L.bits, L.blk)
+    return lloyd_max_codebook(L.bits, L.blk)
+
+
 def relative_distortion(bits: int) -> float:
     """D_b = E[(Z - Q(Z))^2] / sigma^2 of the Lloyd-Max quantiser, computed
     from the optimality conditions as 1 - sum_k P_k c_k^2 / sigma^2."""
@@ -179,8 +250,9 @@ class Layout:
     QJL rows m (0 = none, requires blk == d), norm correction flag, and the
     seed of the sign vector."""
 
-    def __init__(self, head_dim, block, bits, qjl_m=0, norm_correct=0, sign_seed=1):
+    def __init__(self, head_dim, block, bits, qjl_m=0, norm_correct=0, sign_seed=1, codebook=0):
         self.d = int(head_dim)
+        self.codebook = int(codebook)
         self.blk = int(block)
         self.bits = int(bits)
         self.m = int(qjl_m)
@@ -235,7 +307,7 @@ def quantize(x, L: Layout, S=None):
     assert d == L.d
     D = sign_vector(L.seed, d)
     H = hadamard_matrix(L.blk)
-    cent, bnd = lloyd_max_codebook(L.bits, L.blk)
+    cent, bnd = codebook_for(L)
     codes = np.zeros((N, d), dtype=np.int64)
     y_all = np.zeros((N, d))
     scale = np.zeros((N, L.nb))
@@ -393,7 +465,7 @@ def dequantize(codes_packed, scales, L: Layout, qjl_packed=None, rho=None, S=Non
     N = codes.shape[0]
     D = sign_vector(L.seed, L.d)
     H = hadamard_matrix(L.blk)
-    cent, _ = lloyd_max_codebook(L.bits, L.blk)
+    cent, _ = codebook_for(L)
     sc = np.asarray(scales, dtype=np.float16).astype(np.float64).reshape(N, L.nb)
     out = np.zeros((N, L.d))
     for j in range(L.nb):

@@ -33,7 +33,7 @@ def compare_codes(gpu_packed, oq, L):
     ocodes = oq["codes"]
     diff = gcodes != ocodes
     if diff.any():
-        _, bnd = O.lloyd_max_codebook(L.bits, L.blk)
+        _, bnd = O.codebook_for(L)
         y = oq["y"][diff]
         near = np.min(np.abs(y[:, None] - bnd[None, :]), axis=1) < TIE
         assert near.all(), f"{(~near).sum()} code mismatches away from a boundary"

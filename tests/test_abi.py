@@ -39,6 +39,26 @@ def test_codebook_matches_oracle(tqlib, bits, block):
     assert np.array_equal(np.array(bf, dtype=np.float32), ob.astype(np.float32))
 
 
+@pytest.mark.parametrize("bits", [1, 2, 3, 4])
+@pytest.mark.parametrize("block", [32, 64, 128, 256])
+def test_beta_codebook_matches_oracle(tqlib, bits, block):
+    c, b = tb.tq_codebook_kind(bits, block, tb.CODEBOOK_BETA)
+    oc, ob = O.lloyd_max_beta_codebook(bits, block)
+    assert np.max(np.abs(np.array(c) - oc)) < 1e-12
+    assert np.max(np.abs(np.array(b) - ob)) < 1e-12
+    g, _ = tb.tq_codebook_kind(bits, block, tb.CODEBOOK_GAUSSIAN)
+    assert g == tb.tq_codebook(bits, block, f64=True)[0]
+
+
+def test_codebook_kind_rules(tqlib):
+    c = (ctypes.c_double * 16)()
+    assert tqlib.tq_codebook_kind(3, 32, 2, c, None) == -1
+    assert tqlib.tq_codebook_kind(3, 16, 1, c, None) == -2
+    assert tqlib.tq_codebook_kind(3, 512, 1, c, None) == -2
+    assert tqlib.tq_layout_sizes(ctypes.byref(tb.make_layout(128, 32, 3, codebook=1)), None, None, None) == 0
+    assert tqlib.tq_layout_sizes(ctypes.byref(tb.make_layout(128, 32, 3, codebook=2)), None, None, None) == -1
+
+
 @pytest.mark.parametrize("seed", [0, 1, 7, 2 ** 63 + 5])
 def test_signs_match_oracle(tqlib, seed):
     assert tb.tq_signs(seed, 256) == [int(v) for v in O.sign_vector(seed, 256)]
@@ -78,7 +98,7 @@ def test_host_side_argument_checks_need_no_gpu(tqlib):
                                 ctypes.c_void_p(16), ctypes.c_void_p(16), None, None, None) == -3
     assert tqlib.tq_quantize_kv(ctypes.byref(L), ctypes.c_void_p(16), 2, 4, 128, None,
                                 ctypes.c_void_p(16), ctypes.c_void_p(16), None, None, None) == -1
-    bad = tb.tq_layout(128, 32, 3, 0, 0, 7, 1)  # reserved field set
+    bad = tb.tq_layout(128, 32, 3, 0, 0, 7, 1)  # no such codebook kind
     assert tqlib.tq_layout_sizes(ctypes.byref(bad), None, None, None) == -1
 
 

@@ -190,3 +190,35 @@ def test_append_no_tokens_and_errors(tqlib):
     with pytest.raises(ValueError):
         tb.tq_append_kv(cache, torch.zeros((2, 2, 1, 128), dtype=torch.float16, device="cuda"),
                         torch.zeros(2, dtype=torch.int64, device="cuda"))
+
+
+BETA_CASES = [
+    # d, block, bits, dtype, nc, qjl_m with the exact Beta codebook (kind 1)
+    (128, 32, 3, np.float16, 0, 0),      # fast quantise kernel
+    (64, 64, 4, np.float16, 0, 0),
+    (256, 256, 2, np.float32, 1, 0),     # general kernel, norm correction
+    (128, 128, 2, np.float16, 0, 128),   # QJL kernel
+]
+
+
+@pytest.mark.parametrize("d,blk,bits,dt,nc,m", BETA_CASES)
+def test_beta_codebook_quantize_dequantize(tqlib, d, blk, bits, dt, nc, m):
+    from turboquant_kv_cache_gb300 import binding as tb
+    n = 777
+    x = _x(n, d, 400 + d + bits + m, dt)
+    S = inputs.qjl_matrix(m, d, 7) if m else None
+    L = tb.make_layout(d, blk, bits, m, nc, 1, codebook=tb.CODEBOOK_BETA)
+    Lo = O.Layout(d, blk, bits, m, nc, 1, codebook=1)
+    Sg = torch.from_numpy(S).cuda() if m else None
+    pk = tb.tq_quantize_kv(L, torch.from_numpy(x).cuda(), S=Sg)
+    torch.cuda.synchronize()
+    oq = O.quantize(x, Lo, S)
+    n_code, rows = compare_codes(to_np(pk.codes), oq, Lo)
+    assert n_code <= 5
+    compare_scales(to_np(pk.scales)[~rows], oq["scale"][~rows], max_frac=2e-2 if (m and nc) else 1e-3)
+    # the oracle's own encoding decoded on the GPU
+    codes, scales, qb, rho = O.encode(x.astype(np.float64), Lo, S)
+    ref = O.dequantize(codes, scales, Lo, qb, rho, S)
+    up = upload_packed(tb, L, Lo, codes, scales, qb, rho, (n,), S=Sg)
+    got = to_np(tb.tq_dequantize_kv(up, torch.float32))
+    assert rel_l2(got, ref).max() < 1e-5

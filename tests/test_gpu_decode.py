@@ -53,6 +53,9 @@ CASES = [
     ("pervec_nc_d128_gqa2", (128, 3, 0, 1, 2), (128, 2, 0, 1, 3), 1, 4, 2, 257, 257, 128),
     ("block64_d256_gqa8", (64, 3, 0, 0, 1), (64, 4, 0, 0, 2), 1, 8, 1, 200, 190, 256),
     ("bits1_d128", (32, 1, 0, 0, 1), (32, 2, 0, 0, 1), 1, 4, 1, 100, 97, 128),
+    # exact Beta codebooks (codebook kind 1): the tensor-core and CUDA-core paths
+    ("beta_turbo3_d128_gqa4", (32, 3, 0, 0, 1, 1), (32, 3, 0, 0, 1, 1), 2, 8, 2, 700, 650, 128),
+    ("beta_pervec_d64", (64, 4, 0, 0, 5, 1), (64, 2, 0, 0, 6, 1), 1, 2, 2, 300, 280, 64),
 ]
 
 

@@ -365,3 +365,41 @@ def test_attention_degenerate_cases():
     assert np.allclose(out[0, 0], V[0, 0].mean(axis=0), atol=1e-14)
     out1 = O.decode_attention(q, K, V, kv_len=[1])
     assert np.allclose(out1[0, 1], V[0, 0, 0], atol=1e-15)
+
+
+# ---------------------------------------------------------------- Beta codebook
+def test_beta_codebook_uniform_law_closed_form():
+    """blk = 3: one coordinate of a random unit vector in R^3 is uniform on
+    [-1, 1] (Archimedes), and the Lloyd-Max quantiser of a uniform law is
+    the uniform one: centroids -1 + (2k + 1)/K."""
+    for bits in (1, 2, 3, 4):
+        K = 1 << bits
+        c, b = O.lloyd_max_beta_codebook(bits, 3)
+        assert np.max(np.abs(c - (-1.0 + (2.0 * np.arange(K) + 1.0) / K))) < 1e-12
+        assert np.max(np.abs(b - (-1.0 + 2.0 * np.arange(1, K) / K))) < 1e-12
+
+
+def test_beta_codebook_is_the_fixed_point_by_quadrature():
+    """Centroids equal the conditional means of their cells under the density
+    (1 - x^2)^((blk-3)/2), computed here by plain trapezoid quadrature (no
+    incomplete beta function), and the codebook is symmetric."""
+    for blk, bits in ((32, 3), (64, 4), (256, 2)):
+        c, b = O.lloyd_max_beta_codebook(bits, blk)
+        assert np.allclose(c, -c[::-1], atol=1e-15)
+        edges = np.concatenate([[-1.0], b, [1.0]])
+        for k in range(len(c)):
+            x = np.linspace(edges[k], edges[k + 1], 200001)
+            f = np.power(np.clip(1.0 - x * x, 0.0, None), 0.5 * (blk - 3))
+            assert abs(np.trapezoid(x * f, x) / np.trapezoid(f, x) - c[k]) < 1e-9 * max(1.0, abs(c[k]) * 10)
+
+
+def test_beta_codebook_tends_to_gaussian():
+    """As blk grows, sqrt(blk) x a rotated coordinate tends to N(0, 1): the
+    scaled Beta codebook approaches the Gaussian one, monotonically."""
+    g, _ = O.lloyd_max_codebook(3, 1)
+    errs = []
+    for blk in (32, 256, 4096):
+        c, _ = O.lloyd_max_beta_codebook(3, blk)
+        errs.append(np.max(np.abs(c * np.sqrt(blk) - g)))
+    assert errs[0] > errs[1] > errs[2]
+    assert errs[2] < 2e-3

@@ -27,7 +27,7 @@ class TQError(RuntimeError):
 
 class tq_layout(ctypes.Structure):
     _fields_ = [("head_dim", ctypes.c_int32), ("block", ctypes.c_int32), ("bits", ctypes.c_int32),
-                ("qjl_m", ctypes.c_int32), ("norm_correct", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("qjl_m", ctypes.c_int32), ("norm_correct", ctypes.c_int32), ("codebook", ctypes.c_int32),
                 ("sign_seed", ctypes.c_uint64)]
 
 
@@ -47,6 +47,7 @@ def _load():
     sig = {
         "tq_codebook": (I, [I, I, P, P]),
         "tq_codebook_f64": (I, [I, I, P, P]),
+        "tq_codebook_kind": (I, [I, I, I, P, P]),
         "tq_signs": (I, [ctypes.c_uint64, I, P]),
         "tq_layout_sizes": (I, [P, P, P, P]),
         "tq_quantize_kv": (I, [P, P, I, I64, I64, P, P, P, P, P, P]),
@@ -74,8 +75,11 @@ def library():
 
 
 # ------------------------------------------------------------------ helpers
-def make_layout(head_dim, block, bits, qjl_m=0, norm_correct=0, sign_seed=1):
-    return tq_layout(head_dim, block, bits, qjl_m, norm_correct, 0, sign_seed)
+CODEBOOK_GAUSSIAN, CODEBOOK_BETA = 0, 1
+
+
+def make_layout(head_dim, block, bits, qjl_m=0, norm_correct=0, sign_seed=1, codebook=CODEBOOK_GAUSSIAN):
+    return tq_layout(head_dim, block, bits, qjl_m, norm_correct, codebook, sign_seed)
 
 
 def _ptr(t):
@@ -110,6 +114,17 @@ def tq_codebook(bits, block, f64=False):
     c = (T * K)()
     b = (T * max(K - 1, 1))()
     _check((lib.tq_codebook_f64 if f64 else lib.tq_codebook)(bits, block, c, b), "tq_codebook")
+    return list(c), list(b)[:K - 1]
+
+
+def tq_codebook_kind(bits, block, kind):
+    """(centroids, boundaries) in double precision for a codebook kind
+    (CODEBOOK_GAUSSIAN or CODEBOOK_BETA)."""
+    lib = _load()
+    K = 1 << bits
+    c = (ctypes.c_double * K)()
+    b = (ctypes.c_double * max(K - 1, 1))()
+    _check(lib.tq_codebook_kind(bits, block, kind, c, b), "tq_codebook_kind")
     return list(c), list(b)[:K - 1]
 
 

@@ -3,6 +3,7 @@
 #include <cmath>
 #include <cstring>
 #include <mutex>
+#include <utility>
 
 #include "tq_internal.h"
 
@@ -53,15 +54,132 @@ void solve_unit_codebook(int levels, double* c) {
   for (int k = 0; k < levels; ++k) c[k] = sym[k];
 }
 
+// Lloyd-Max quantiser of one coordinate of a uniformly random unit vector
+// in R^blk: density f(x) = (1 - x^2)^a / B(1/2, a + 1) on [-1, 1] with
+// a = (blk - 3)/2, i.e. (x + 1)/2 ~ Beta((blk - 1)/2, (blk - 1)/2)
+// (llama.cpp-turboquant, "How it works": the exact Beta distribution of
+// the rotated coordinates).  blk is even here, so a is a half-integer and
+// J_p(x) = int_0^x (1 - t^2)^p dt follows from J_{1/2}(x) =
+// (x sqrt(1 - x^2) + asin x)/2 by J_p = x (1 - x^2)^p / (2p + 1) +
+// 2p/(2p + 1) J_{p-1}, every term positive for x >= 0.  The first moment of a
+// cell is exact: int x (1 - x^2)^a dx = -(1 - x^2)^(a + 1) / (2 (a + 1)).
+double beta_J(double x, double a) {
+  const double ax = std::fabs(x);
+  const double w = std::fmax(0.0, 1.0 - ax * ax);
+  const double sw = std::sqrt(w);
+  double J = 0.5 * (ax * sw + std::asin(std::fmin(ax, 1.0)));
+  double wp = w * sw;   // w^p, p = 3/2, 5/2, ...
+  for (double p = 1.5; p <= a + 1e-9; p += 1.0, wp *= w) J = ax * wp / (2.0 * p + 1.0) + (2.0 * p / (2.0 * p + 1.0)) * J;
+  return x < 0.0 ? -J : J;
+}
+
+// One Lloyd step for the Beta density: boundaries at midpoints, centroids
+// the conditional means of their cells.
+void beta_lloyd_step(int levels, double a, double norm, const double* c, double* out) {
+  double edge[17];
+  edge[0] = -1.0;
+  edge[levels] = 1.0;
+  for (int k = 1; k < levels; ++k) edge[k] = 0.5 * (c[k - 1] + c[k]);
+  double J[17];
+  for (int k = 0; k <= levels; ++k) J[k] = beta_J(edge[k], a);
+  for (int k = 0; k < levels; ++k) {
+    const double e0 = edge[k], e1 = edge[k + 1];
+    const double mass = (J[k + 1] - J[k]) / norm;
+    const double mom = (std::pow(std::fmax(0.0, 1.0 - e0 * e0), a + 1.0) -
+                        std::pow(std::fmax(0.0, 1.0 - e1 * e1), a + 1.0)) / (2.0 * (a + 1.0) * norm);
+    out[k] = mom / mass;
+  }
+}
+
+// The fixed point of the Lloyd step, found by Newton's method on
+// F(c) = step(c) - c (finite-difference Jacobian, at most 16 x 16) from the
+// scaled Gaussian codebook, then polished with plain steps until nothing
+// moves.  Plain Lloyd converges linearly and slowly here; Newton needs a
+// handful of iterations.
+void solve_beta_codebook(int levels, int blk, double* c) {
+  const double a = 0.5 * (blk - 3);
+  const double norm = 2.0 * beta_J(1.0, a);   // B(1/2, a + 1)
+  solve_unit_codebook(levels, c);
+  for (int k = 0; k < levels; ++k) c[k] /= std::sqrt(static_cast<double>(blk));
+  const double h = 1e-7 / std::sqrt(static_cast<double>(blk));
+  double F[16], Jm[16][17], tp[16], tm[16], cp[16];
+  for (int it = 0; it < 60; ++it) {
+    beta_lloyd_step(levels, a, norm, c, F);
+    double res = 0.0;
+    for (int k = 0; k < levels; ++k) {
+      F[k] -= c[k];
+      res = std::fmax(res, std::fabs(F[k]));
+    }
+    if (res < 1e-15 / std::sqrt(static_cast<double>(blk))) break;
+    for (int jcol = 0; jcol < levels; ++jcol) {
+      for (int k = 0; k < levels; ++k) cp[k] = c[k];
+      cp[jcol] = c[jcol] + h;
+      beta_lloyd_step(levels, a, norm, cp, tp);
+      cp[jcol] = c[jcol] - h;
+      beta_lloyd_step(levels, a, norm, cp, tm);
+      for (int k = 0; k < levels; ++k) Jm[k][jcol] = (tp[k] - tm[k]) / (2.0 * h) - (k == jcol ? 1.0 : 0.0);
+    }
+    for (int k = 0; k < levels; ++k) Jm[k][levels] = -F[k];
+    // Gaussian elimination with partial pivoting
+    for (int col = 0; col < levels; ++col) {
+      int piv = col;
+      for (int r = col + 1; r < levels; ++r)
+        if (std::fabs(Jm[r][col]) > std::fabs(Jm[piv][col])) piv = r;
+      if (piv != col)
+        for (int q = 0; q <= levels; ++q) std::swap(Jm[col][q], Jm[piv][q]);
+      if (Jm[col][col] == 0.0) break;
+      for (int r = col + 1; r < levels; ++r) {
+        const double f = Jm[r][col] / Jm[col][col];
+        for (int q = col; q <= levels; ++q) Jm[r][q] -= f * Jm[col][q];
+      }
+    }
+    for (int r = levels - 1; r >= 0; --r) {
+      double v = Jm[r][levels];
+      for (int q = r + 1; q < levels; ++q) v -= Jm[r][q] * cp[q];
+      cp[r] = v / Jm[r][r];
+    }
+    for (int k = 0; k < levels; ++k) c[k] += cp[k];
+  }
+  double last = INFINITY;
+  for (int it = 0; it < 100000; ++it) {
+    beta_lloyd_step(levels, a, norm, c, tp);
+    double moved = 0.0;
+    for (int k = 0; k < levels; ++k) {
+      moved = std::fmax(moved, std::fabs(tp[k] - c[k]));
+      c[k] = tp[k];
+    }
+    if (moved == 0.0 || (moved < 1e-16 && moved >= last)) break;
+    last = moved;
+  }
+  double sym[16];
+  for (int k = 0; k < levels; ++k) sym[k] = 0.5 * (c[k] - c[levels - 1 - k]);
+  for (int k = 0; k < levels; ++k) c[k] = sym[k];
+}
+
 struct CodebookCache {
   std::mutex mu;
   bool ready[5] = {false, false, false, false, false};
   double unit[5][16];
+  // Beta codebooks per (bits, log2 block) for blocks 32..256
+  bool beta_ready[5][9] = {};
+  double beta[5][9][16];
 };
 
 CodebookCache& cache() {
   static CodebookCache c;
   return c;
+}
+
+const double* beta_codebook(int bits, int blk) {
+  int lb = 0;
+  while ((1 << lb) < blk) ++lb;
+  CodebookCache& cc = cache();
+  std::lock_guard<std::mutex> lock(cc.mu);
+  if (!cc.beta_ready[bits][lb]) {
+    solve_beta_codebook(1 << bits, blk, cc.beta[bits][lb]);
+    cc.beta_ready[bits][lb] = true;
+  }
+  return cc.beta[bits][lb];
 }
 
 const double* unit_codebook(int bits) {
@@ -88,7 +206,7 @@ bool pow2(int v) { return v > 0 && (v & (v - 1)) == 0; }
 
 int check_layout(const tq_layout* L) {
   if (!L) return TQ_ERR_ARG;
-  if (L->reserved != 0) return TQ_ERR_ARG;
+  if (L->codebook != TQ_CODEBOOK_GAUSSIAN && L->codebook != TQ_CODEBOOK_BETA) return TQ_ERR_ARG;
   if (L->head_dim != 64 && L->head_dim != 128 && L->head_dim != 256) return TQ_ERR_UNSUPPORTED;
   if (!pow2(L->block) || L->block < 32 || L->head_dim % L->block) return TQ_ERR_UNSUPPORTED;
   if (L->bits < 1 || L->bits > 4) return TQ_ERR_UNSUPPORTED;
@@ -116,7 +234,7 @@ int make_params(const tq_layout* L, CodecParams* p) {
   for (int i = 0; i < L->head_dim; ++i)
     if (splitmix64_next(state) >> 63) p->sign_bits[i >> 5] |= 1u << (i & 31);
   double c[16], b[16];
-  tq_codebook_f64(L->bits, L->block, c, b);
+  tq_codebook_kind(L->bits, L->block, L->codebook, c, b);
   const int K = 1 << L->bits;
   for (int k = 0; k < K; ++k) p->centroids[k] = static_cast<float>(c[k]);
   for (int k = 0; k + 1 < K; ++k) p->bounds[k] = static_cast<float>(b[k]);
@@ -133,6 +251,18 @@ int tq_codebook_f64(int bits, int block, double* centroids, double* boundaries) 
   const int K = 1 << bits;
   const double sigma = 1.0 / std::sqrt(static_cast<double>(block));
   for (int k = 0; k < K; ++k) centroids[k] = u[k] * sigma;
+  if (boundaries)
+    for (int k = 0; k + 1 < K; ++k) boundaries[k] = 0.5 * (centroids[k] + centroids[k + 1]);
+  return TQ_OK;
+}
+
+int tq_codebook_kind(int bits, int block, int kind, double* centroids, double* boundaries) {
+  if (kind == TQ_CODEBOOK_GAUSSIAN) return tq_codebook_f64(bits, block, centroids, boundaries);
+  if (kind != TQ_CODEBOOK_BETA || bits < 1 || bits > 4 || !centroids) return TQ_ERR_ARG;
+  if (block < 32 || block > 256 || (block & (block - 1))) return TQ_ERR_UNSUPPORTED;
+  const double* u = tq::beta_codebook(bits, block);
+  const int K = 1 << bits;
+  for (int k = 0; k < K; ++k) centroids[k] = u[k];
   if (boundaries)
     for (int k = 0; k + 1 < K; ++k) boundaries[k] = 0.5 * (centroids[k] + centroids[k + 1]);
   return TQ_OK;

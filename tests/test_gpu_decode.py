@@ -154,3 +154,45 @@ def test_decode_qjl_keys_long_ragged(tqlib):
     got, ref, _ = _run(tb, (128, 2, 128, 0, 1), (128, 3, 0, 0, 1), 2, 8, 2, 2000, 1999, 128,
                        kv_len=[1999, 333], n_split=5, S=S)
     assert np.abs(got - ref).max() < ATTN_ATOL
+
+
+def test_append_and_decode_replay_in_a_cuda_graph(tqlib):
+    """tq_append_kv + tq_decode_attn captured once in a CUDA graph and
+    replayed with new inputs give the same bytes as the calls issued one by
+    one (nothing in the calls allocates, synchronises or reads host state)."""
+    from turboquant_kv_cache_gb300 import binding as tb
+    B, Hq, Hkv, d, S_cap = 2, 8, 2, 128, 512
+    L = tb.make_layout(d, 32, 3, 0, 0, 1)
+    k0 = torch.from_numpy(inputs.gaussian((B, Hkv, S_cap, d), 71)).cuda()
+    v0 = torch.from_numpy(inputs.gaussian((B, Hkv, S_cap, d), 72)).cuda()
+
+    def fresh():
+        return tb.tq_quantize_kv(L, k0), tb.tq_quantize_kv(L, v0)
+
+    def run(K, V, q, kn, vn, pos, ws, out):
+        tb.tq_append_kv(K, kn, pos)
+        tb.tq_append_kv(V, vn, pos)
+        tb.tq_decode_attn(K, V, q, ctx=S_cap, workspace=ws, out=out)
+
+    q = torch.empty((B, Hq, d), dtype=torch.float16, device="cuda")
+    kn = torch.empty((B, Hkv, 1, d), dtype=torch.float16, device="cuda")
+    vn = torch.empty_like(kn)
+    pos = torch.full((B,), S_cap - 1, dtype=torch.int32, device="cuda")
+    need, _ = tb.tq_decode_workspace_bytes(B, Hq, Hkv, d, S_cap, 0)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    out = torch.empty_like(q)
+    Kg, Vg = fresh()
+    run(Kg, Vg, q.normal_(), kn.normal_(), vn.normal_(), pos, ws, out)   # warm-up outside capture
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        run(Kg, Vg, q, kn, vn, pos, ws, out)
+    for seed in (5, 6):
+        torch.manual_seed(seed)
+        q.normal_(); kn.normal_(); vn.normal_()
+        Ke, Ve = fresh()
+        oe = torch.empty_like(q)
+        run(Ke, Ve, q, kn, vn, pos, ws.clone(), oe)
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, oe)
+        assert torch.equal(Kg.codes[:, :, S_cap - 1], Ke.codes[:, :, S_cap - 1])

@@ -151,15 +151,21 @@ int tq_quantize_kv(const tq_layout* layout, const void* x, tq_dtype x_dtype, int
  *   pos          device int32 [B]: token j of (b, h) goes to cache slot
  *                pos[b] + j; slots outside [0, S_cap) are not written
  *                (nothing else is touched)
+ *   page_table, page_size, pages_per_seq
+ *                NULL, 0, 0 for a contiguous [B, H, S_cap] cache, else the
+ *                paging of tq_kv_view (slot t of batch b is row t % page_size
+ *                of page page_table[b*pages_per_seq + t/page_size]; S_cap
+ *                <= pages_per_seq*page_size)
  *   codes, scales, qjl_bits, qjl_rnorm
- *                the cache arrays [B, H, S_cap, ...] in the tq_kv_view layout
+ *                the cache arrays in the tq_kv_view layout
  *   S            device fp32 [qjl_m, d] (QJL only, else NULL)
  * Returns TQ_ERR_ARG for negative sizes or a NULL pos, the tq_quantize_kv
  * errors otherwise; B*H*n_new == 0 is a no-op.  The records written are
  * identical to tq_quantize_kv of the same rows. */
 int tq_append_kv(const tq_layout* layout, const void* x, tq_dtype x_dtype, int B, int H, int n_new,
-                 int64_t x_row_stride, const int32_t* pos, int64_t S_cap, const float* S, uint8_t* codes,
-                 uint16_t* scales, uint8_t* qjl_bits, uint16_t* qjl_rnorm, void* stream);
+                 int64_t x_row_stride, const int32_t* pos, int64_t S_cap, const int32_t* page_table,
+                 int page_size, int pages_per_seq, const float* S, uint8_t* codes, uint16_t* scales,
+                 uint8_t* qjl_bits, uint16_t* qjl_rnorm, void* stream);
 
 /* Decode n_vec packed vectors (device) into out [n_vec, d] (fp16 or fp32):
  * x~ = scale * D H (c + [QJL] rho sqrt(pi/2)/m H D S^T (2s - 1)), i.e.
@@ -170,9 +176,18 @@ int tq_dequantize_kv(const tq_layout* layout, const uint8_t* codes, const uint16
                      const uint8_t* qjl_bits, const uint16_t* qjl_rnorm, const float* S,
                      int64_t n_vec, void* out, tq_dtype out_dtype, void* stream);
 
-/* A packed cache of shape [B, Hkv, S_cap] vectors, tokens contiguous within
- * a (batch, head): record (b, h, t) is vector index (b*Hkv + h)*S_cap + t
- * of the per-vector arrays above.  All pointers device. */
+/* A packed cache, all pointers device.
+ *   page_table == NULL: [B, Hkv, S_cap] vectors, tokens contiguous within a
+ *     (batch, head): record (b, h, t) is vector index (b*Hkv + h)*S_cap + t
+ *     of the per-vector arrays above.
+ *   page_table != NULL (paged): the arrays hold pages of page_size tokens,
+ *     [num_pages, Hkv, page_size] vectors; token t of batch b lives in page
+ *     p = page_table[b*pages_per_seq + t/page_size] (device int32) at record
+ *     (p*Hkv + h)*page_size + t % page_size.  page_size is a positive
+ *     multiple of 32, S_cap must be <= pages_per_seq*page_size, and the K and
+ *     V views of one call share page_table, page_size and pages_per_seq
+ *     (else TQ_ERR_ARG).  Pages of a sequence need not be contiguous or
+ *     ordered; entries of the table past a sequence's length are not read. */
 typedef struct {
   const uint8_t* codes;
   const uint16_t* scales;
@@ -180,6 +195,9 @@ typedef struct {
   const uint16_t* qjl_rnorm; /* NULL unless layout.qjl_m > 0 */
   const float* S;            /* NULL unless layout.qjl_m > 0 */
   tq_layout layout;
+  const int32_t* page_table; /* NULL: contiguous [B, Hkv, S_cap] */
+  int32_t page_size;
+  int32_t pages_per_seq;
 } tq_kv_view;
 
 /* Fused decode attention over the packed cache: one query per

@@ -105,21 +105,53 @@ def test_host_side_argument_checks_need_no_gpu(tqlib):
 def test_append_argument_checks_need_no_gpu(tqlib):
     L = tb.make_layout(128, 32, 3)
     P16 = ctypes.c_void_p(16)
+    NP = (None, 0, 0)  # contiguous cache: no page table
+
+    def app(x, dt, B, H, n, stride, pos, S_cap, paging=NP, codes=P16, scales=P16):
+        return tqlib.tq_append_kv(ctypes.byref(L), x, dt, B, H, n, stride, pos, S_cap, *paging, None, codes,
+                                  scales, None, None, None)
+
     # no tokens: nothing to do, even without buffers
-    assert tqlib.tq_append_kv(ctypes.byref(L), None, 0, 2, 8, 0, 128, None, 64, None, None, None, None, None,
-                              None) == 0
+    assert app(None, 0, 2, 8, 0, 128, None, 64, codes=None, scales=None) == 0
     # negative sizes, a missing position array or S_cap 0 are refused
-    assert tqlib.tq_append_kv(ctypes.byref(L), P16, 0, -1, 8, 1, 128, P16, 64, None, P16, P16, None, None,
-                              None) == -1
-    assert tqlib.tq_append_kv(ctypes.byref(L), P16, 0, 2, 8, 1, 128, None, 64, None, P16, P16, None, None,
-                              None) == -1
-    assert tqlib.tq_append_kv(ctypes.byref(L), P16, 0, 2, 8, 1, 128, P16, 0, None, P16, P16, None, None,
-                              None) == -1
+    assert app(P16, 0, -1, 8, 1, 128, P16, 64) == -1
+    assert app(P16, 0, 2, 8, 1, 128, None, 64) == -1
+    assert app(P16, 0, 2, 8, 1, 128, P16, 0) == -1
     # then the quantise checks: misaligned rows, bad stride
-    assert tqlib.tq_append_kv(ctypes.byref(L), ctypes.c_void_p(18), 0, 2, 8, 1, 128, P16, 64, None, P16, P16,
-                              None, None, None) == -3
-    assert tqlib.tq_append_kv(ctypes.byref(L), P16, 0, 2, 8, 1, 64, P16, 64, None, P16, P16, None, None,
-                              None) == -1
+    assert app(ctypes.c_void_p(18), 0, 2, 8, 1, 128, P16, 64) == -3
+    assert app(P16, 0, 2, 8, 1, 64, P16, 64) == -1
+    # paging: a table needs a page size that is a positive multiple of 32 and
+    # pages_per_seq * page_size >= S_cap
+    assert app(P16, 0, 2, 8, 1, 128, P16, 64, (P16, 0, 4)) == -1
+    assert app(P16, 0, 2, 8, 1, 128, P16, 64, (P16, 48, 2)) == -1
+    assert app(P16, 0, 2, 8, 1, 128, P16, 64, (P16, 32, 1)) == -1
+
+
+def test_paging_checks_need_no_gpu(tqlib):
+    """A page table with a page size that is not a positive multiple of 32,
+    too few pages for S_cap, or K and V views that disagree on paging are
+    refused before anything reaches the device."""
+    L = tb.make_layout(128, 32, 3)
+    P16 = ctypes.c_void_p(16)
+
+    def view(pt, ps, pps):
+        return tb.tq_kv_view(16, 16, None, None, None, L, pt, ps, pps)
+
+    def dec(K, V, S_cap=128):
+        return tqlib.tq_decode_attn(ctypes.byref(K), ctypes.byref(V), P16, 1, 4, 1, S_cap, None, 64, 0.0, P16,
+                                    P16, 1 << 20, 0, None)
+
+    def pre(K, V, S_cap=128):
+        return tqlib.tq_prefill_attn(ctypes.byref(K), ctypes.byref(V), P16, 1, 4, 1, 8, S_cap, 64, 1, 0.0, P16,
+                                     P16, 1 << 20, None)
+
+    for f in (dec, pre):
+        assert f(view(16, 48, 4), view(16, 48, 4)) == -1   # page size not a multiple of 32
+        assert f(view(16, 0, 4), view(16, 0, 4)) == -1
+        assert f(view(16, 32, 3), view(16, 32, 3)) == -1   # 96 slots < S_cap 128
+        assert f(view(16, 32, 4), view(32, 32, 4)) == -1   # K and V tables differ
+        assert f(view(16, 32, 4), view(None, 0, 0)) == -1  # K paged, V contiguous
+        assert f(view(16, 64, 2), view(16, 32, 4)) == -1
 
 
 def _decode_ws(B, Hq, d, ns):

@@ -33,7 +33,8 @@ class tq_layout(ctypes.Structure):
 
 class tq_kv_view(ctypes.Structure):
     _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("qjl_bits", ctypes.c_void_p),
-                ("qjl_rnorm", ctypes.c_void_p), ("S", ctypes.c_void_p), ("layout", tq_layout)]
+                ("qjl_rnorm", ctypes.c_void_p), ("S", ctypes.c_void_p), ("layout", tq_layout),
+                ("page_table", ctypes.c_void_p), ("page_size", ctypes.c_int32), ("pages_per_seq", ctypes.c_int32)]
 
 
 def _load():
@@ -51,7 +52,7 @@ def _load():
         "tq_signs": (I, [ctypes.c_uint64, I, P]),
         "tq_layout_sizes": (I, [P, P, P, P]),
         "tq_quantize_kv": (I, [P, P, I, I64, I64, P, P, P, P, P, P]),
-        "tq_append_kv": (I, [P, P, I, I, I, I, I64, P, I64, P, P, P, P, P, P]),
+        "tq_append_kv": (I, [P, P, I, I, I, I, I64, P, I64, P, I, I, P, P, P, P, P, P]),
         "tq_dequantize_kv": (I, [P, P, P, P, P, P, I64, P, I, P]),
         "tq_decode_attn": (I, [P, P, P, I, I, I, I64, P, I64, ctypes.c_float, P, P, SZ, I, P]),
         "tq_decode_workspace_bytes": (I, [I, I, I, I, I64, I, P, P]),
@@ -163,12 +164,23 @@ def tq_prefill_workspace_bytes(B, Hq, Hkv, head_dim, Tq, ctx):
 class PackedKV:
     """Device buffers of one packed cache (K or V): codes [N, code_bytes]
     uint8, scales [N, d/block] fp16, and with QJL qjl [N, m/8] uint8, rnorm
-    [N] fp16 and the projection S [m, d] fp32.  N may carry leading dims."""
+    [N] fp16 and the projection S [m, d] fp32.  N may carry leading dims.
 
-    def __init__(self, layout, lead_shape, device="cuda", S=None):
+    As an attention cache the lead shape is [B, Hkv, S_cap] (contiguous), or
+    [num_pages, Hkv, page_size] with page_table an int32 CUDA tensor
+    [B, pages_per_seq] (paged: token t of batch b is row t % page_size of
+    page page_table[b, t // page_size])."""
+
+    def __init__(self, layout, lead_shape, device="cuda", S=None, page_table=None):
         cb, ns, qb = tq_layout_sizes(layout)
         self.layout = layout
         self.lead_shape = tuple(lead_shape)
+        self.page_table = page_table
+        if page_table is not None:
+            if (page_table.dtype != torch.int32 or page_table.dim() != 2 or not page_table.is_cuda
+                    or len(self.lead_shape) != 3):
+                raise ValueError("paged cache: lead shape [num_pages, Hkv, page_size] and an int32 CUDA "
+                                 "page table [B, pages_per_seq]")
         self.codes = torch.empty(self.lead_shape + (cb,), dtype=torch.uint8, device=device)
         self.scales = torch.empty(self.lead_shape + (ns,), dtype=torch.float16, device=device)
         self.qjl = torch.empty(self.lead_shape + (qb,), dtype=torch.uint8, device=device) if qb else None
@@ -182,11 +194,29 @@ class PackedKV:
             n *= s
         return n
 
+    @property
+    def heads(self):
+        return self.lead_shape[1]
+
+    @property
+    def batch(self):
+        return self.page_table.shape[0] if self.page_table is not None else self.lead_shape[0]
+
+    @property
+    def capacity(self):
+        """Slots per (batch, head): S_cap."""
+        if self.page_table is not None:
+            return self.page_table.shape[1] * self.lead_shape[2]
+        return self.lead_shape[2]
+
     def view(self):
+        pt = self.page_table
         return tq_kv_view(self.codes.data_ptr(), self.scales.data_ptr(),
                           self.qjl.data_ptr() if self.qjl is not None else None,
                           self.rnorm.data_ptr() if self.rnorm is not None else None,
-                          self.S.data_ptr() if self.S is not None else None, self.layout)
+                          self.S.data_ptr() if self.S is not None else None, self.layout,
+                          pt.data_ptr() if pt is not None else None,
+                          self.lead_shape[2] if pt is not None else 0, pt.shape[1] if pt is not None else 0)
 
     def nbytes(self):
         n = self.codes.numel() + 2 * self.scales.numel()
@@ -225,14 +255,17 @@ def tq_append_kv(cache, x, pos, stream=None):
     if x.dim() != 4 or x.shape[-1] != d or x.stride(-1) != 1:
         raise ValueError("x must be [B, H, n_new, head_dim] with a contiguous last dimension")
     B, H, n_new, _ = x.shape
-    if len(cache.lead_shape) != 3 or tuple(cache.lead_shape[:2]) != (B, H):
-        raise ValueError("cache must have leading shape [B, H, S_cap] matching x")
+    if len(cache.lead_shape) != 3 or (cache.batch, cache.heads) != (B, H):
+        raise ValueError("cache must have leading shape [B, H, S_cap] (or be paged for B sequences) matching x")
     if pos.dtype != torch.int32 or pos.numel() != B or not pos.is_cuda:
         raise ValueError("pos must be an int32 CUDA tensor of B slot offsets")
     x2 = x.reshape(-1, d)
+    pt = cache.page_table
     st = lib.tq_append_kv(ctypes.byref(layout), _ptr(x2), _dtype_code(x.dtype), B, H, n_new, x2.stride(0),
-                          _ptr(pos.contiguous()), cache.lead_shape[2], _ptr(cache.S), _ptr(cache.codes),
-                          _ptr(cache.scales), _ptr(cache.qjl), _ptr(cache.rnorm), _stream(stream))
+                          _ptr(pos.contiguous()), cache.capacity, _ptr(pt),
+                          cache.lead_shape[2] if pt is not None else 0, pt.shape[1] if pt is not None else 0,
+                          _ptr(cache.S), _ptr(cache.codes), _ptr(cache.scales), _ptr(cache.qjl), _ptr(cache.rnorm),
+                          _stream(stream))
     _check(st, "tq_append_kv")
     return cache
 
@@ -248,12 +281,20 @@ def tq_dequantize_kv(packed, out_dtype=torch.float16, stream=None):
     return out
 
 
+def _cache_for(K, V, B):
+    """Heads and S_cap of a K/V cache pair read by B sequences."""
+    if K.batch < B or V.batch < B or (K.heads, K.capacity) != (V.heads, V.capacity):
+        raise ValueError("K and V caches must hold the same heads and slots for at least B sequences")
+    return K.heads, K.capacity
+
+
 def tq_decode_attn(K, V, q, ctx=None, kv_len=None, softmax_scale=0.0, n_split=0, workspace=None, out=None,
                    stream=None):
-    """q [B, Hq, d] fp16; K, V PackedKV with lead shape [B, Hkv, S_cap]."""
+    """q [B, Hq, d] fp16; K, V PackedKV caches (contiguous [B, Hkv, S_cap]
+    or paged with one page table)."""
     lib = _load()
     B, Hq, d = q.shape
-    _, Hkv, S_cap = K.lead_shape
+    Hkv, S_cap = _cache_for(K, V, B)
     ctx = S_cap if ctx is None else ctx
     need, ns = tq_decode_workspace_bytes(B, Hq, Hkv, d, ctx, n_split)
     if workspace is None:
@@ -273,7 +314,7 @@ def tq_decode_attn_static(K, V, q, ctx=None, kv_len=None, softmax_scale=0.0, n_s
     array holds the split partials (for callers that cannot allocate)."""
     lib = _load()
     B, Hq, d = q.shape
-    _, Hkv, S_cap = K.lead_shape
+    Hkv, S_cap = _cache_for(K, V, B)
     ctx = S_cap if ctx is None else ctx
     if out is None:
         out = torch.empty_like(q)
@@ -288,7 +329,7 @@ def tq_prefill_attn(K, V, q, ctx, causal=True, softmax_scale=0.0, workspace=None
     """q [B, Hq, Tq, d] fp16 at positions ctx-Tq .. ctx-1."""
     lib = _load()
     B, Hq, Tq, d = q.shape
-    _, Hkv, S_cap = K.lead_shape
+    Hkv, S_cap = _cache_for(K, V, B)
     need = tq_prefill_workspace_bytes(B, Hq, Hkv, d, Tq, ctx)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)

@@ -337,18 +337,22 @@ int quantize_common(const tq_layout* layout, const void* x, tq_dtype x_dtype, in
 extern "C" int tq_quantize_kv(const tq_layout* layout, const void* x, tq_dtype x_dtype, int64_t n_vec,
                               int64_t x_row_stride, const float* S, uint8_t* codes, uint16_t* scales,
                               uint8_t* qjl_bits, uint16_t* qjl_rnorm, void* stream) {
-  const tq::RowMap identity{nullptr, 1, 1, 0};
+  const tq::RowMap identity{nullptr, 1, 1, 0, {nullptr, 0, 0}};
   return tq::quantize_common(layout, x, x_dtype, n_vec, x_row_stride, S, codes, scales, qjl_bits, qjl_rnorm,
                              identity, stream);
 }
 
 extern "C" int tq_append_kv(const tq_layout* layout, const void* x, tq_dtype x_dtype, int B, int H, int n_new,
-                            int64_t x_row_stride, const int32_t* pos, int64_t S_cap, const float* S, uint8_t* codes,
-                            uint16_t* scales, uint8_t* qjl_bits, uint16_t* qjl_rnorm, void* stream) {
+                            int64_t x_row_stride, const int32_t* pos, int64_t S_cap, const int32_t* page_table,
+                            int page_size, int pages_per_seq, const float* S, uint8_t* codes, uint16_t* scales,
+                            uint8_t* qjl_bits, uint16_t* qjl_rnorm, void* stream) {
   if (B < 0 || H < 0 || n_new < 0 || S_cap < 0) return TQ_ERR_ARG;
   if ((int64_t)B * H * n_new == 0) return TQ_OK;
   if (!pos || S_cap == 0) return TQ_ERR_ARG;
-  const tq::RowMap map{pos, n_new, H, S_cap};
+  if (page_table && (page_size <= 0 || page_size % 32 || pages_per_seq <= 0 ||
+                     (int64_t)page_size * pages_per_seq < S_cap))
+    return TQ_ERR_ARG;
+  const tq::RowMap map{pos, n_new, H, S_cap, {page_table, page_table ? page_size : 0, page_table ? pages_per_seq : 0}};
   return tq::quantize_common(layout, x, x_dtype, (int64_t)B * H * n_new, x_row_stride, S, codes, scales, qjl_bits,
                              qjl_rnorm, map, stream);
 }

@@ -42,6 +42,7 @@ struct DecodeArgs {
   const uint16_t* q;
   const int32_t* kv_len;
   float* part;          // [B*Hq][n_split][d + 4]
+  PageMap pages;        // paging of both caches (table NULL: contiguous)
   int64_t S_cap;
   int64_t ctx;
   int Hq, Hkv, n_split;
@@ -142,7 +143,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const CodecPa
     for (int k = 0; k < CPL; ++k) acc[h][k] = 0.f;
   }
   const int kwords = PK.code_bytes / 4, vwords = PV.code_bytes / 4;
-  const int64_t rec0 = (int64_t)bh * a.S_cap;
+  auto rec_of = [&](int64_t t) { return cache_rec(a.pages, a.Hkv, a.S_cap, b, kvh, t); };
 
   for (int64_t c0 = t_begin + (int64_t)wid * 32; c0 < t_end; c0 += kWarps * 32) {
     const int64_t t = c0 + lane;
@@ -151,8 +152,9 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const CodecPa
 #pragma unroll
     for (int h = 0; h < G; ++h) s[h] = 0.f;
     if (valid) {
-      const uint32_t* rec = a.kc + (rec0 + t) * kwords;
-      const uint16_t* sc = a.ks + (rec0 + t) * PK.nb;
+      const int64_t rt = rec_of(t);
+      const uint32_t* rec = a.kc + rt * kwords;
+      const uint16_t* sc = a.ks + rt * PK.nb;
       const int gpb = PK.blk / 32;  // 32-code groups per block
       for (int j = 0; j < PK.nb; ++j) {
         float part[G];
@@ -178,8 +180,8 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const CodecPa
         for (int h = 0; h < G; ++h) s[h] = fmaf(scj, part[h], s[h]);
       }
       if (PK.m) {
-        const float coef = h2f(sc[0]) * h2f(a.kr[rec0 + t]) * kSqrtHalfPi / (float)PK.m;
-        const uint32_t* qb = a.kq + (rec0 + t) * (PK.m / 32);
+        const float coef = h2f(sc[0]) * h2f(a.kr[rt]) * kSqrtHalfPi / (float)PK.m;
+        const uint32_t* qb = a.kq + rt * (PK.m / 32);
         float part[G];
 #pragma unroll
         for (int h = 0; h < G; ++h) part[h] = 0.f;
@@ -211,7 +213,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const CodecPa
     __syncwarp();
     const int n_tok = (int)imin64(32, t_end - c0);
     for (int tt = 0; tt < n_tok; ++tt) {
-      const int64_t r = rec0 + c0 + tt;
+      const int64_t r = rec_of(c0 + tt);
       const uint32_t* rec = a.vc + r * vwords;
       const uint16_t* sc = a.vs + r * PV.nb;
 #pragma unroll
@@ -521,6 +523,7 @@ extern "C" int tq_decode_attn(const tq_kv_view* K, const tq_kv_view* V, const ui
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || ctx < 0 || ctx > S_cap || n_split < 0) return TQ_ERR_ARG;
   if (!K->codes || !K->scales || !V->codes || !V->scales) return TQ_ERR_ARG;
   if (PK.m && (!K->qjl_bits || !K->qjl_rnorm || !K->S)) return TQ_ERR_ARG;
+  if (tq::check_paging(K, S_cap) != TQ_OK || !tq::same_paging(K, V)) return TQ_ERR_ARG;
   if (!tq::aligned16(K->codes) || !tq::aligned16(V->codes) || !tq::aligned16(q) || !tq::aligned16(out))
     return TQ_ERR_ALIGN;
   const int ns = n_split ? n_split : tq::decode_auto_splits(B, Hkv, ctx);
@@ -531,7 +534,9 @@ extern "C" int tq_decode_attn(const tq_kv_view* K, const tq_kv_view* V, const ui
   tq::DecodeArgs a{reinterpret_cast<const uint32_t*>(K->codes), K->scales,
                    reinterpret_cast<const uint32_t*>(K->qjl_bits), K->qjl_rnorm, K->S,
                    reinterpret_cast<const uint32_t*>(V->codes), V->scales, q, kv_len,
-                   static_cast<float*>(workspace), S_cap, ctx, Hq, Hkv, ns, sm * tq::kLog2e};
+                   static_cast<float*>(workspace),
+                   {K->page_table, K->page_table ? K->page_size : 0, K->page_table ? K->pages_per_seq : 0},
+                   S_cap, ctx, Hq, Hkv, ns, sm * tq::kLog2e};
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int G = Hq / Hkv;
   if (tq::decode_tc_eligible(PK, PV, G, S_cap, K, V))

@@ -86,6 +86,7 @@ struct TcArgs {
   const float* sqsum;  // per-head sum of sq (QJL)
   const int32_t* kv_len;
   float* part;
+  PageMap pages;       // paging of both caches (table NULL: contiguous)
   int64_t S_cap;
   int64_t ctx;
   int64_t per;  // tokens per split (multiple of 128)
@@ -225,7 +226,6 @@ __global__ void __launch_bounds__(kThreads, 4) decode_tc_kernel(const CodecParam
   const int64_t t_end = imin64(t_begin + a.per, len);
   const int n_sub = t_end > t_begin ? (int)((t_end - t_begin + kTok - 1) / kTok) : 0;
   const int n_it = n_sub > pi ? (n_sub - pi + P - 1) / P : 0;
-  const int64_t rec0 = (int64_t)bh * a.S_cap;
   const uint32_t ring = su32(smem) + pi * kSlots * C::STAGE;
   const int plane = hw * 32 + lane;  // lane within the pipeline
 
@@ -234,7 +234,8 @@ __global__ void __launch_bounds__(kThreads, 4) decode_tc_kernel(const CodecParam
   int ld_it = 0;
   auto load_next = [&](int slot) {
     const int64_t t0 = t_begin + (int64_t)kTok * (pi + P * ld_it);
-    const int64_t tok0 = rec0 + t0;
+    // a step never crosses a page: steps and pages are both 32-token aligned
+    const int64_t tok0 = cache_rec(a.pages, a.Hkv, a.S_cap, b, kvh, t0);
     const uint32_t dst = ring + slot * C::STAGE;
     const int64_t rem = t_end - t0;
     if (rem >= kTok) {
@@ -684,8 +685,10 @@ bool decode_tc_eligible(const CodecParams& PK, const CodecParams& PV, int G, int
   const bool kpv = PK.blk == PK.d, vpv = PV.blk == PV.d;
   // every per-token stream must keep 16-byte aligned rows for cp.async
   const int64_t streams[6] = {PK.code_bytes, 2 * PK.nb, PK.qjl_bytes, PK.m ? 2 : 0, PV.code_bytes, 2 * PV.nb};
+  // (a paged cache's rows are its pages)
+  const int64_t row = K->page_table ? K->page_size : S_cap;
   for (int i = 0; i < 6; ++i)
-    if ((S_cap * streams[i]) % 16 != 0) return false;
+    if ((row * streams[i]) % 16 != 0) return false;
   if ((!kpv && PK.blk != 32) || (!vpv && PV.blk != 32)) return false;
   bool ok;
   if (PK.d == 256) {
@@ -727,6 +730,7 @@ int launch_decode_tc(const CodecParams& PK, const CodecParams& PV, const tq_kv_v
   a.q = q;
   a.kv_len = kv_len;
   a.part = part;
+  a.pages = {K->page_table, K->page_table ? K->page_size : 0, K->page_table ? K->pages_per_seq : 0};
   a.S_cap = S_cap;
   a.ctx = ctx;
   a.per = decode_tc_per_split(ctx, n_split);

@@ -22,12 +22,21 @@ __device__ __forceinline__ uint32_t sign_byte(const CodecParams& P, int i0) {
   return (P.sign_bits[i0 >> 5] >> (i0 & 31)) & 0xffu;
 }
 
+// Record of token t of (batch b, head h) in a cache of H heads and S_cap
+// slots, contiguous or paged.
+__device__ __forceinline__ int64_t cache_rec(const PageMap& pm, int H, int64_t S_cap, int b, int h, int64_t t) {
+  if (!pm.table) return ((int64_t)b * H + h) * S_cap + t;
+  const int64_t page = pm.table[(int64_t)b * pm.pages_per_seq + t / pm.page_size];
+  return (page * H + h) * pm.page_size + t % pm.page_size;
+}
+
 // Record of quantised vector i under a RowMap, or -1 when it is not stored.
 __device__ __forceinline__ int64_t map_row(const RowMap& m, int64_t i) {
   if (!m.pos) return i;
   const int64_t bh = i / m.n_new;
   const int64_t slot = (int64_t)m.pos[bh / m.H] + (i - bh * m.n_new);
-  return (slot >= 0 && slot < m.S_cap) ? bh * m.S_cap + slot : -1;
+  if (slot < 0 || slot >= m.S_cap) return -1;
+  return cache_rec(m.pages, m.H, m.S_cap, (int)(bh / m.H), (int)(bh % m.H), slot);
 }
 
 __device__ __forceinline__ float flip(float v, uint32_t bit) {

@@ -37,14 +37,34 @@ int check_layout(const tq_layout* layout);
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Paging of a cache (tq_kv_view): table == NULL for contiguous
+// [B, H, S_cap] records.
+struct PageMap {
+  const int32_t* table;   // device [B][pages_per_seq], or NULL
+  int32_t page_size, pages_per_seq;
+};
+
 // Where quantised vector i is stored.  pos == NULL: record i.  Otherwise the
-// input holds n_new new tokens of every (batch, head) of a [B, H, S_cap]
-// cache, vector i = (b*H + h)*n_new + j, and it goes to record
-// (b*H + h)*S_cap + pos[b] + j; a slot outside [0, S_cap) is not written.
+// input holds n_new new tokens of every (batch, head) of a cache of H heads
+// and S_cap slots, vector i = (b*H + h)*n_new + j, and it goes to the record
+// of slot pos[b] + j (contiguous or paged, see PageMap); a slot outside
+// [0, S_cap) is not written.
 struct RowMap {
   const int32_t* pos;   // device [B], or NULL
   int32_t n_new, H;
   int64_t S_cap;
+  PageMap pages;
 };
+
+// Checks a view's paging against the call's S_cap; TQ_OK or TQ_ERR_ARG.
+inline int check_paging(const tq_kv_view* v, int64_t S_cap) {
+  if (!v->page_table) return TQ_OK;
+  if (v->page_size <= 0 || v->page_size % 32 || v->pages_per_seq <= 0) return TQ_ERR_ARG;
+  return (int64_t)v->page_size * v->pages_per_seq >= S_cap ? TQ_OK : TQ_ERR_ARG;
+}
+inline bool same_paging(const tq_kv_view* a, const tq_kv_view* b) {
+  return a->page_table == b->page_table && (!a->page_table || (a->page_size == b->page_size &&
+                                                               a->pages_per_seq == b->pages_per_seq));
+}
 
 }  // namespace tq

@@ -9,7 +9,7 @@ size_t prefill_tc_workspace(int B, int Hq, int Hkv, int d, int Tq, int64_t ctx);
 int launch_prefill_tc(const CodecParams& PK, const CodecParams& PV, const uint8_t* kc, const uint16_t* ks,
                       const uint8_t* vc, const uint16_t* vs, const uint16_t* q, int B, int Hq, int Hkv, int Tq,
                       int64_t S_cap, int64_t ctx, int causal, float qscale, uint16_t* out, void* ws,
-                      cudaStream_t st);
+                      const PageMap& pages, cudaStream_t st);
 }  // namespace tq
 
 extern "C" int tq_prefill_workspace_bytes(int B, int Hq, int Hkv, int head_dim, int Tq, int64_t ctx,
@@ -32,6 +32,7 @@ extern "C" int tq_prefill_attn(const tq_kv_view* K, const tq_kv_view* V, const u
   if (PK.d != PV.d || PK.m || PV.m) return TQ_ERR_UNSUPPORTED;
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || Tq < 0 || ctx < Tq || ctx > S_cap) return TQ_ERR_ARG;
   if (!K->codes || !K->scales || !V->codes || !V->scales) return TQ_ERR_ARG;
+  if (tq::check_paging(K, S_cap) != TQ_OK || !tq::same_paging(K, V)) return TQ_ERR_ARG;
   if (!tq::aligned16(K->codes) || !tq::aligned16(V->codes) || !tq::aligned16(q) || !tq::aligned16(out))
     return TQ_ERR_ALIGN;
   if (Tq == 0) return TQ_OK;
@@ -40,5 +41,7 @@ extern "C" int tq_prefill_attn(const tq_kv_view* K, const tq_kv_view* V, const u
   if (!tq::aligned16(workspace)) return TQ_ERR_ALIGN;
   const float sm = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)PK.d);
   return tq::launch_prefill_tc(PK, PV, K->codes, K->scales, V->codes, V->scales, q, B, Hq, Hkv, Tq, S_cap, ctx,
-                               causal ? 1 : 0, sm * tq::kLog2e, out, workspace, static_cast<cudaStream_t>(stream));
+                               causal ? 1 : 0, sm * tq::kLog2e, out, workspace,
+                               {K->page_table, K->page_table ? K->page_size : 0, K->page_table ? K->pages_per_seq : 0},
+                               static_cast<cudaStream_t>(stream));
 }

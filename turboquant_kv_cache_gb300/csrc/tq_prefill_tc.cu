@@ -385,6 +385,7 @@ struct PrefillTcArgs {
   int64_t S_cap, ctx;
   int Hq, Hkv, Tq, R_pad, n_split, causal;
   int64_t per;          // tokens per split (multiple of kTok)
+  PageMap pages;        // paging of both caches (table NULL: contiguous)
 };
 
 
@@ -401,10 +402,10 @@ struct PrefillTcArgs {
 // landed).  Before returning, the role waits for the products of its last
 // tiles, so no arrival from the peer can still be on its way to this CTA.
 // BAR_ID: the named barrier that gathers the side's NT threads.
-template <int D, int NT, int NB, int BAR_ID, class NValid, class Wait>
+template <int D, int NT, int NB, int BAR_ID, class RecOf, class NValid, class Wait>
 __device__ __forceinline__ void decoder_role(const CodecParams& P, const CodeTabs& ct, const uint8_t* codes,
                                              const uint8_t* scales, int ptid, uint32_t full, uint32_t free_bar,
-                                             uint32_t buf0, uint32_t tile_bytes, int64_t rec0, int64_t t_lo,
+                                             uint32_t buf0, uint32_t tile_bytes, RecOf rec_of, int64_t t_lo,
                                              int n_tiles, uint32_t rank, NValid n_valid_of, Wait wait,
                                              volatile int& abort) {
   constexpr uint32_t kHalfBytes = 32u * D * 2;
@@ -413,8 +414,12 @@ __device__ __forceinline__ void decoder_role(const CodecParams& P, const CodeTab
   const uint32_t peer_buf0 = mapa_peer(buf0, rank ^ 1u), peer_full = mapa_peer(full, rank ^ 1u);
   ItemRegs<D, NT> r0, r1, r2;
   auto load = [&](int t, ItemRegs<D, NT>& r) {
-    const int64_t rec = rec0 + t_lo + (int64_t)t * kTok;
-    load_items<D, NT>(P.bits, pl, codes + rec * P.code_bytes, scales + rec * 2 * P.nb, n_valid_of(t), r);
+    // the record of this CTA's half, less the half's offset that the item
+    // offsets carry (a half never crosses a page: both are 32-token aligned)
+    const int half0 = (int)rank * ItemPlan<D, NT>::TOK;
+    const int nv = n_valid_of(t);
+    const int64_t rec = nv > half0 ? rec_of(t_lo + (int64_t)t * kTok + half0) - half0 : 0;
+    load_items<D, NT>(P.bits, pl, codes + rec * P.code_bytes, scales + rec * 2 * P.nb, nv, r);
   };
   // tile t decodes from registers loaded two steps earlier; the load of tile
   // t+2 is issued after tile t's arrivals, so no arrival waits on it
@@ -505,7 +510,7 @@ __global__ void __launch_bounds__(192 + 32 * (NK + NV), 1) prefill_ws_kernel(con
   const int64_t t_lo = (int64_t)split * a.per;
   const int64_t t_hi = imin64(imin64(t_lo + a.per, a.ctx), max_pos + 1);
   const int n_tiles = t_hi > t_lo ? (int)((t_hi - t_lo + kTok - 1) / kTok) : 0;
-  const int64_t rec0 = (int64_t)bh * a.S_cap;
+  auto rec_of = [&](int64_t t) { return cache_rec(a.pages, a.Hkv, a.S_cap, b, kvh, t); };
 
   const uint32_t a_smem = su32(smem);
   // NB decoded K buffers, then NB decoded V buffers
@@ -575,10 +580,10 @@ __global__ void __launch_bounds__(192 + 32 * (NK + NV), 1) prefill_ws_kernel(con
     // the decode.
     if (RB) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(kDecRegs));
     if (warp < 6 + NK)
-      decoder_role<D, kNK, NB, 1>(PK, s_tabs[0], a.kc, a.ks, tid - 192, kfull, kfree, aK(0), kTileBytes, rec0, t_lo,
+      decoder_role<D, kNK, NB, 1>(PK, s_tabs[0], a.kc, a.ks, tid - 192, kfull, kfree, aK(0), kTileBytes, rec_of, t_lo,
                                n_tiles, rank, n_valid_of, wait_cl, s_abort);
     else
-      decoder_role<D, kNV, NB, 2>(PV, s_tabs[1], a.vc, a.vs, tid - 192 - kNK, vfull, vfree, aV(0), kTileBytes, rec0,
+      decoder_role<D, kNV, NB, 2>(PV, s_tabs[1], a.vc, a.vs, tid - 192 - kNK, vfull, vfree, aV(0), kTileBytes, rec_of,
                                t_lo, n_tiles, rank, n_valid_of, wait_cl, s_abort);
   } else if (warp == 4) {
     // ================= S issue: S(t) = Q^ (TMEM) K^(t)^T once K(t) is decoded
@@ -871,7 +876,7 @@ int launch_ws(const CodecParams& PK, const CodecParams& PV, const PrefillTcArgs&
 int launch_prefill_tc(const CodecParams& PK, const CodecParams& PV, const uint8_t* kc, const uint16_t* ks,
                       const uint8_t* vc, const uint16_t* vs, const uint16_t* q, int B, int Hq, int Hkv, int Tq,
                       int64_t S_cap, int64_t ctx, int causal, float qscale, uint16_t* out, void* ws,
-                      cudaStream_t st) {
+                      const PageMap& pages, cudaStream_t st) {
   const int d = PK.d;
   const int G = Hq / Hkv;
   const int R_pad = (Tq * G + 2 * kRowsTc - 1) / (2 * kRowsTc) * (2 * kRowsTc);
@@ -885,7 +890,7 @@ int launch_prefill_tc(const CodecParams& PK, const CodecParams& PV, const uint8_
   int64_t per = (ctx + ns - 1) / ns;
   per = (per + kTok - 1) / kTok * kTok;
   PrefillTcArgs a{kc, reinterpret_cast<const uint8_t*>(ks), vc, reinterpret_cast<const uint8_t*>(vs), qhat, part,
-                  err, S_cap, ctx, Hq, Hkv, Tq, R_pad, ns, causal, per};
+                  err, S_cap, ctx, Hq, Hkv, Tq, R_pad, ns, causal, per, pages};
   dim3 qgrid(R_pad, B * Hkv);
   dim3 grid(R_pad / kRowsTc, ns, B * Hkv);
   int r;

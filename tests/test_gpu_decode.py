@@ -146,6 +146,31 @@ def test_decode_tensor_core_layouts(tqlib, name, cK, cV, B, Hq, Hkv, S_cap, ctx,
     assert err < ATTN_ATOL, (name, err)
 
 
+AUTO_SPLIT_CASES = [
+    # the library's own split count (n_split 0) on the tensor-core kernel:
+    # name, K (block, bits, m, nc, seed), V, B, Hq, Hkv, S_cap, ctx, kv_len, heavy_k
+    ("turbo3_ragged", (32, 3, 0, 0, 1), (32, 3, 0, 0, 2), 3, 12, 3, 2050, 2050, [2050, 1000, 63], False),
+    ("empty_and_short_units", (32, 3, 0, 0, 1), (32, 3, 0, 0, 1), 3, 8, 2, 600, 600, [500, 0, 129], False),
+    ("one_partial_step", (32, 3, 0, 0, 3), (32, 3, 0, 0, 4), 2, 8, 2, 100, 100, None, False),
+    ("more_units_than_sms", (32, 3, 0, 0, 1), (32, 3, 0, 0, 1), 16, 32, 8, 300, 300, None, False),
+    ("turbo4k_heavy", (32, 4, 0, 0, 1), (32, 3, 0, 0, 1), 1, 8, 2, 3000, 2999, None, True),
+    ("bits2k", (32, 2, 0, 0, 5), (32, 3, 0, 0, 6), 2, 4, 1, 1030, 1029, [1029, 640], False),
+    ("beta_codebook", (32, 3, 0, 0, 1, 1), (32, 3, 0, 0, 1, 1), 2, 8, 2, 1500, 1400, None, False),
+]
+
+
+@pytest.mark.parametrize("name,cK,cV,B,Hq,Hkv,S_cap,ctx,kv_len,heavy", AUTO_SPLIT_CASES)
+def test_decode_auto_splits(tqlib, name, cK, cV, B, Hq, Hkv, S_cap, ctx, kv_len, heavy):
+    """Ragged and empty (batch, KV head) units, a single partial step, more
+    units than SMs and every K width, at the library's own split count."""
+    from turboquant_kv_cache_gb300 import binding as tb
+    got, ref, _ = _run(tb, cK, cV, B, Hq, Hkv, S_cap, ctx, 128, kv_len=kv_len, n_split=0, seed=21, heavy_k=heavy)
+    err = np.abs(got - ref).max()
+    assert err < ATTN_ATOL, (name, err)
+    if kv_len is not None and 0 in kv_len:
+        assert np.all(got[kv_len.index(0)] == 0)
+
+
 def test_decode_qjl_keys_long_ragged(tqlib):
     """QJL keys (2-bit + m=128 signs) with 3-bit per-vector values over many
     tiles, ragged lengths and splits: the tensor-core QJL path."""

@@ -54,6 +54,12 @@ def _cache(tb, cfg, B, H, S_cap, d, seed, S=None, heavy=False):
 DECODE_CASES = [
     # name, K (block, bits, m, nc, seed), V, B, Hq, Hkv, S_cap, ctx, kv_len, n_split, d, page_size, qjl
     ("tc_turbo3_d128_p32", (32, 3, 0, 0, 1), (32, 3, 0, 0, 1), 2, 8, 2, 2048, 2000, [2000, 777], 0, 128, 32, False),
+    ("tc_turbo3_d128_p96_split_kernel", (32, 3, 0, 0, 1), (32, 3, 0, 0, 1), 2, 8, 2, 960, 900, [900, 500], 3, 128,
+     96, False),
+    ("tc_turbo3_d128_p128_empty_batch", (32, 3, 0, 0, 1), (32, 3, 0, 0, 1), 3, 8, 2, 1024, 1000, [1000, 130, 0], 0, 128,
+     128, False),
+    ("tc_turbo4k_d128_p256", (32, 4, 0, 0, 1), (32, 3, 0, 0, 1), 2, 8, 2, 2048, 2048, None, 0, 128, 256,
+     False),
     ("tc_turbo3_d128_p256", (32, 3, 0, 0, 1), (32, 3, 0, 0, 1), 3, 8, 2, 4096, 4096, [4096, 1, 2500], 5, 128, 256,
      False),
     ("tc_d256_turbo4k_p64", (32, 4, 0, 0, 1), (32, 3, 0, 0, 1), 1, 8, 2, 1536, 1500, None, 0, 256, 64, False),

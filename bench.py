@@ -179,6 +179,26 @@ def bench_depth(tb, torch, dev, L, K, V, q, steps, warm):
             "by_ctx": res}
 
 
+def bench_window(tb, torch, inputs, dev, K, V, q, steps, warm, W=128):
+    """The headline decode with an fp16 residual window of the last W tokens
+    of every (batch, KV head) (tq_decode_attn_window): the packed cache plus
+    W unquantised keys and values, one call per step, L2 flushed before each;
+    the plain decode is timed beside it for the window's cost."""
+    B, Hq, Hkv, d, ctx = DEC["B"], DEC["Hq"], DEC["Hkv"], DEC["d"], DEC["ctx"]
+    flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=dev)
+    kw = torch.from_numpy(inputs.gaussian((B, Hkv, W, d), 13)).to(dev)
+    vw = torch.from_numpy(inputs.gaussian((B, Hkv, W, d), 14)).to(dev)
+    ws = torch.empty(tb.tq_decode_window_workspace_bytes(B, Hq, Hkv, d, ctx, 0), dtype=torch.uint8, device=dev)
+    out = torch.empty_like(q)
+    ms_w = _time(torch, lambda: tb.tq_decode_attn_window(K, V, q, kw, vw, ctx=ctx, workspace=ws, out=out),
+                 flush, steps, warm)
+    ms_0 = _time(torch, lambda: tb.tq_decode_attn(K, V, q, ctx=ctx, workspace=ws, out=out), flush, steps, warm)
+    nbytes = decode_bytes(B, Hkv, ctx, d, 3, 3, 32, 32) + 2 * B * Hkv * W * d * 2
+    return {"workload": f"the headline decode plus an fp16 window of {W} tokens per (batch, KV head)",
+            "us": round(ms_w * 1e3, 2), "GB/s": round(nbytes / (ms_w * 1e-3) / 1e9, 1),
+            "bytes_per_step": nbytes, "plain_decode_us": round(ms_0 * 1e3, 2)}
+
+
 def run_only(args, tb, torch, inputs, dev):
     """One workload on its own (for profiler runs): the same inputs and calls
     as the full run, `--warmup` untimed then `--steps` timed passes, one JSON
@@ -200,6 +220,9 @@ def run_only(args, tb, torch, inputs, dev):
     elif args.only == "decode_depth":
         L, K, V, q = headline_cache(tb, torch, inputs, dev)
         res.update(bench_depth(tb, torch, dev, L, K, V, q, args.steps, args.warmup))
+    elif args.only == "decode_window":
+        L, K, V, q = headline_cache(tb, torch, inputs, dev)
+        res.update(bench_window(tb, torch, inputs, dev, K, V, q, args.steps, args.warmup))
     else:
         res.update(bench_extra(tb, torch, inputs, dev, args, which=args.only))
     print(json.dumps(res), flush=True)
@@ -267,6 +290,7 @@ def run_gpu(args, rank, world):
 
     quant = bench_quantize(tb, torch, inputs, dev, args)
     depth = None if args.no_extra else bench_depth(tb, torch, dev, L, K, V, q, max(3, min(args.steps, 20)), 3)
+    window = None if args.no_extra else bench_window(tb, torch, inputs, dev, K, V, q, max(3, min(args.steps, 20)), 3)
     extra = {} if args.no_extra else bench_extra(tb, torch, inputs, dev, args)
     if rank == 0:
         line = {
@@ -286,6 +310,7 @@ def run_gpu(args, rank, world):
             "e2e": e2e,
             "quantize": quant,
             "decode_vs_depth": depth,
+            "decode_with_fp16_window": window,
             "other_workloads": extra,
             "gpu_launches": args.steps * 2,
             "clocks": clocks.summary(),
@@ -626,7 +651,8 @@ def main():
     ap.add_argument("--no-extra", action="store_true", help="skip the other workloads (headline only)")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--only", default=None,
-                    choices=["decode", "quantize", "prefill", "decode_d256", "decode_qjl", "quantize_qjl", "decode_depth"],
+                    choices=["decode", "quantize", "prefill", "decode_d256", "decode_qjl", "quantize_qjl", "decode_depth",
+                             "decode_window"],
                     help="time one workload alone and print its result only (profiler runs)")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -251,6 +251,35 @@ int tq_decode_attn_static(const tq_kv_view* K, const tq_kv_view* V, const uint16
 int tq_decode_workspace_bytes(int B, int Hq, int Hkv, int head_dim, int64_t ctx, int n_split,
                               size_t* bytes, int* n_split_out);
 
+/* Decode attention over the packed cache plus an unquantised fp16 residual
+ * window of the most recent tokens ("TurboQuant From Scratch on Real KV
+ * Tensors", Finding 5: the last tokens kept in full precision).  Batch b
+ * attends, in one softmax, to the cache tokens [0, min(ctx, kv_len[b])) and
+ * the window tokens [0, win_len[b]) (win_len NULL: win for every batch);
+ * attention does not depend on the order of the tokens.
+ *   k_win, v_win  device fp16 [B, Hkv, W_cap, head_dim]: unquantised keys and
+ *                 values in the original (unrotated) domain, 8-byte aligned;
+ *                 caller-owned, read only
+ *   W_cap         window slots per (batch, KV head), >= 0
+ *   win_len       device int32 [B] or NULL; entries are clamped to [0, W_cap]
+ *   win           window tokens of every batch when win_len is NULL,
+ *                 0 <= win <= W_cap
+ * The other arguments are tq_decode_attn's.  workspace: at least
+ * tq_decode_window_workspace_bytes(...) bytes, 16-byte aligned.  The window's
+ * softmax partial is one split slot more, rotated into V's coded domain and
+ * merged by the same combine.  Errors: TQ_ERR_ARG for a missing window
+ * array, W_cap < 0 or win outside [0, W_cap]; TQ_ERR_ALIGN for window
+ * arrays that are not 8-byte aligned; otherwise as tq_decode_attn. */
+int tq_decode_attn_window(const tq_kv_view* K, const tq_kv_view* V, const uint16_t* q, int B, int Hq,
+                          int Hkv, int64_t S_cap, const int32_t* kv_len, int64_t ctx,
+                          const uint16_t* k_win, const uint16_t* v_win, int W_cap,
+                          const int32_t* win_len, int win, float softmax_scale, uint16_t* out,
+                          void* workspace, size_t workspace_bytes, int n_split, void* stream);
+
+/* Workspace bytes for tq_decode_attn_window with these sizes (host). */
+int tq_decode_window_workspace_bytes(int B, int Hq, int Hkv, int head_dim, int64_t ctx, int n_split,
+                                     size_t* bytes);
+
 /* Prefill attention: Tq queries per (batch, q-head) at positions
  * ctx-Tq .. ctx-1 over cache positions [0, ctx); q fp16 [B, Hq, Tq, d],
  * out fp16 [B, Hq, Tq, d], both device.  causal != 0: query i attends

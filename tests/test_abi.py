@@ -154,6 +154,24 @@ def test_paging_checks_need_no_gpu(tqlib):
         assert f(view(16, 64, 2), view(16, 32, 4)) == -1
 
 
+def test_window_decode_checks_need_no_gpu(tqlib):
+    L = tb.make_layout(128, 32, 3)
+    P16 = ctypes.c_void_p(16)
+    K = tb.tq_kv_view(16, 16, None, None, None, L, None, 0, 0)
+
+    def win(kw, vw, W_cap, win_n):
+        return tqlib.tq_decode_attn_window(ctypes.byref(K), ctypes.byref(K), P16, 1, 4, 1, 128, None, 64, kw, vw,
+                                           W_cap, None, win_n, 0.0, P16, P16, 1 << 20, 0, None)
+
+    assert win(None, P16, 16, 8) == -1            # missing window array
+    assert win(P16, P16, 16, 17) == -1            # more window tokens than slots
+    assert win(P16, P16, -1, 0) == -1
+    assert win(ctypes.c_void_p(20), P16, 16, 8) == -3   # not 8-byte aligned
+    # one split slot more than the plain decode
+    nb, ns = tb.tq_decode_workspace_bytes(8, 32, 8, 128, 32768, 9)
+    assert tb.tq_decode_window_workspace_bytes(8, 32, 8, 128, 32768, 9) == _decode_ws(8, 32, 128, 10)
+
+
 def _decode_ws(B, Hq, d, ns):
     # split partials [B*Hq][n_split][d + 4] fp32, rounded up to 256 bytes, then
     # the tensor-core path's S q rows (fp16, m = 128) and row sums of QJL keys

@@ -221,3 +221,71 @@ def test_append_and_decode_replay_in_a_cuda_graph(tqlib):
         torch.cuda.synchronize()
         assert torch.equal(out, oe)
         assert torch.equal(Kg.codes[:, :, S_cap - 1], Ke.codes[:, :, S_cap - 1])
+
+
+WINDOW_CASES = [
+    # fp16 residual window: name, K (block, bits, m, nc, seed), V, B, Hq, Hkv, S_cap, ctx, kv_len, d, W_cap,
+    # win_len (None: every batch W_cap), qjl
+    ("turbo3_d128_tc", (32, 3, 0, 0, 1), (32, 3, 0, 0, 1), 2, 8, 2, 700, 650, [650, 300], 128, 128, [128, 5],
+     False),
+    ("empty_cache_or_window", (32, 3, 0, 0, 1), (32, 3, 0, 0, 2), 3, 8, 2, 300, 300, [0, 300, 0], 128, 40,
+     [40, 0, 0], False),
+    ("pervec_d64_cuda_core", (64, 4, 0, 0, 5), (64, 3, 0, 0, 6), 2, 2, 2, 200, 190, None, 64, 64, None, False),
+    ("d256_turbo4k_tc", (32, 4, 0, 0, 1), (32, 3, 0, 0, 1), 1, 8, 2, 530, 513, None, 256, 32, [17], False),
+    ("block64_v_gqa8", (64, 3, 0, 0, 1), (64, 4, 0, 0, 2), 1, 8, 1, 200, 190, None, 256, 96, None, False),
+    ("qjl_keys", (128, 2, 128, 0, 1), (128, 3, 0, 0, 1), 2, 8, 2, 400, 391, [391, 100], 128, 64, [64, 33], True),
+]
+
+
+@pytest.mark.parametrize("name,cK,cV,B,Hq,Hkv,S_cap,ctx,kv_len,d,W_cap,win_len,qjl", WINDOW_CASES)
+def test_decode_with_fp16_window(tqlib, name, cK, cV, B, Hq, Hkv, S_cap, ctx, kv_len, d, W_cap, win_len, qjl):
+    """tq_decode_attn_window against the oracle's attention over the
+    decoded cache tokens followed by the exact fp16 window tokens."""
+    from turboquant_kv_cache_gb300 import binding as tb
+    S = inputs.qjl_matrix(128, 128, 7) if qjl else None
+    Lk, Lv = O.Layout(d, *cK), O.Layout(d, *cV)
+    k = inputs.gaussian((B, Hkv, S_cap, d), 41)
+    v = inputs.gaussian((B, Hkv, S_cap, d), 42)
+    q = inputs.gaussian((B, Hq, d), 43)
+    kw = inputs.gaussian((B, Hkv, W_cap, d), 44)
+    vw = inputs.gaussian((B, Hkv, W_cap, d), 45)
+    (kc, ks, kq, kr), kd = _encode_cache(k, Lk, S)
+    (vc, vs, _, _), vd = _encode_cache(v, Lv)
+    Sg = torch.from_numpy(S).cuda() if S is not None else None
+    K = upload_packed(tb, tb.make_layout(d, *cK), Lk, kc, ks, kq, kr, (B, Hkv, S_cap), S=Sg)
+    V = upload_packed(tb, tb.make_layout(d, *cV), Lv, vc, vs, None, None, (B, Hkv, S_cap))
+    kvl = torch.tensor(kv_len, dtype=torch.int32, device="cuda") if kv_len is not None else None
+    wl = torch.tensor(win_len, dtype=torch.int32, device="cuda") if win_len is not None else None
+    out = tb.tq_decode_attn_window(K, V, torch.from_numpy(q).cuda(), torch.from_numpy(kw).cuda(),
+                                   torch.from_numpy(vw).cuda(), ctx=ctx, kv_len=kvl, win_len=wl)
+    torch.cuda.synchronize()
+    lens = kv_len if kv_len is not None else [ctx] * B
+    wls = win_len if win_len is not None else [W_cap] * B
+    n_all = [lens[b] + wls[b] for b in range(B)]
+    Kc = np.zeros((B, Hkv, max(max(n_all), 1), d))
+    Vc = np.zeros_like(Kc)
+    for b in range(B):
+        Kc[b, :, :lens[b]] = kd[b, :, :lens[b]]
+        Vc[b, :, :lens[b]] = vd[b, :, :lens[b]]
+        Kc[b, :, lens[b]:n_all[b]] = kw[b, :, :wls[b]].astype(np.float64)
+        Vc[b, :, lens[b]:n_all[b]] = vw[b, :, :wls[b]].astype(np.float64)
+    ref = O.decode_attention(q, Kc, Vc, n_all)
+    got = to_np(out.float())
+    err = np.abs(got - ref).max()
+    assert err < ATTN_ATOL, (name, err)
+    for b in range(B):
+        if n_all[b] == 0:
+            assert np.all(got[b] == 0)
+
+
+def test_decode_window_argument_errors(tqlib):
+    from turboquant_kv_cache_gb300 import binding as tb
+    L = tb.make_layout(128, 32, 3)
+    K = tb.PackedKV(L, (1, 2, 64))
+    q = torch.zeros(1, 8, 128, dtype=torch.float16, device="cuda")
+    kw = torch.zeros(1, 2, 16, 128, dtype=torch.float16, device="cuda")
+    with pytest.raises(tb.TQError) as e:   # more window tokens than slots
+        tb.tq_decode_attn_window(K, K, q, kw, kw, ctx=64, win=17)
+    assert e.value.status == -1
+    with pytest.raises(ValueError):
+        tb.tq_decode_attn_window(K, K, q, kw, kw[:, :, :8], ctx=64)

@@ -56,6 +56,8 @@ def _load():
         "tq_dequantize_kv": (I, [P, P, P, P, P, P, I64, P, I, P]),
         "tq_decode_attn": (I, [P, P, P, I, I, I, I64, P, I64, ctypes.c_float, P, P, SZ, I, P]),
         "tq_decode_workspace_bytes": (I, [I, I, I, I, I64, I, P, P]),
+        "tq_decode_attn_window": (I, [P, P, P, I, I, I, I64, P, I64, P, P, I, P, I, ctypes.c_float, P, P, SZ, I, P]),
+        "tq_decode_window_workspace_bytes": (I, [I, I, I, I, I64, I, P]),
         "tq_decode_attn_static": (I, [P, P, P, I, I, I, I64, P, I64, ctypes.c_float, P, I, P]),
         "tq_prefill_attn": (I, [P, P, P, I, I, I, I, I64, I64, I, ctypes.c_float, P, P, SZ, P]),
         "tq_prefill_workspace_bytes": (I, [I, I, I, I, I, I64, P]),
@@ -322,6 +324,46 @@ def tq_decode_attn_static(K, V, q, ctx=None, kv_len=None, softmax_scale=0.0, n_s
     st = lib.tq_decode_attn_static(ctypes.byref(kv), ctypes.byref(vv), _ptr(q), B, Hq, Hkv, S_cap, _ptr(kv_len),
                                    ctx, float(softmax_scale), _ptr(out), n_split, _stream(stream))
     _check(st, "tq_decode_attn_static")
+    return out
+
+
+def tq_decode_window_workspace_bytes(B, Hq, Hkv, head_dim, ctx, n_split=0):
+    lib = _load()
+    nb = ctypes.c_size_t()
+    _check(lib.tq_decode_window_workspace_bytes(B, Hq, Hkv, head_dim, ctx, n_split, ctypes.byref(nb)),
+           "tq_decode_window_workspace_bytes")
+    return nb.value
+
+
+def tq_decode_attn_window(K, V, q, k_win, v_win, ctx=None, kv_len=None, win_len=None, win=None, softmax_scale=0.0,
+                          n_split=0, workspace=None, out=None, stream=None):
+    """Decode over the packed cache plus an fp16 residual window: k_win,
+    v_win [B, Hkv, W_cap, d] fp16 CUDA (contiguous, unrotated); win_len an
+    int32 CUDA tensor [B] of window tokens, or win for every batch (default
+    W_cap)."""
+    lib = _load()
+    B, Hq, d = q.shape
+    Hkv, S_cap = _cache_for(K, V, B)
+    ctx = S_cap if ctx is None else ctx
+    if k_win.shape != v_win.shape or k_win.dim() != 4 or tuple(k_win.shape[:2]) != (B, Hkv) or k_win.shape[3] != d:
+        raise ValueError("k_win, v_win must be [B, Hkv, W_cap, head_dim]")
+    if k_win.dtype != torch.float16 or v_win.dtype != torch.float16:
+        raise ValueError("the window is fp16")
+    k_win, v_win = k_win.contiguous(), v_win.contiguous()
+    W_cap = k_win.shape[2]
+    if win_len is not None and (win_len.dtype != torch.int32 or win_len.numel() != B or not win_len.is_cuda):
+        raise ValueError("win_len must be an int32 CUDA tensor of B window lengths")
+    win = W_cap if win is None else win
+    need = tq_decode_window_workspace_bytes(B, Hq, Hkv, d, ctx, n_split)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    kv, vv = K.view(), V.view()
+    st = lib.tq_decode_attn_window(ctypes.byref(kv), ctypes.byref(vv), _ptr(q), B, Hq, Hkv, S_cap, _ptr(kv_len), ctx,
+                                   _ptr(k_win), _ptr(v_win), W_cap, _ptr(win_len), win, float(softmax_scale),
+                                   _ptr(out), _ptr(workspace), workspace.numel(), n_split, _stream(stream))
+    _check(st, "tq_decode_attn_window")
     return out
 
 

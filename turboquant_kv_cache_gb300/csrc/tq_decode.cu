@@ -23,7 +23,7 @@ bool decode_tc_eligible(const CodecParams& PK, const CodecParams& PV, int G, int
 size_t decode_tc_extra_bytes(int B, int Hq);
 int launch_decode_tc(const CodecParams& PK, const CodecParams& PV, const tq_kv_view* K, const tq_kv_view* V,
                      const uint16_t* q, const int32_t* kv_len, float* part, size_t part_bytes, int B, int Hq, int Hkv,
-                     int64_t S_cap, int64_t ctx, int n_split, float qscale, uint16_t* out, cudaStream_t st);
+                     int64_t S_cap, int64_t ctx, int n_split, int slots, bool pdl, float qscale, cudaStream_t st);
 size_t decode_ws_bytes(int B, int Hq, int d, int n_split);
 
 namespace {
@@ -41,12 +41,14 @@ struct DecodeArgs {
   const uint16_t* vs;
   const uint16_t* q;
   const int32_t* kv_len;
-  float* part;          // [B*Hq][n_split][d + 4]
+  float* part;          // [B*Hq][slots][d + 4]
   PageMap pages;        // paging of both caches (table NULL: contiguous)
   int64_t S_cap;
   int64_t ctx;
   int Hq, Hkv, n_split;
+  int slots;            // split slots per row (n_split, or more for extra partials)
   float qscale;         // softmax_scale * log2(e)
+  int pdl;              // launched as a programmatic dependent of the kernel before it
 };
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -243,7 +245,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const CodecPa
     float M = -INFINITY;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) M = fmaxf(M, s_ml[w][0][h]);
-    float* dst = a.part + (((int64_t)b * a.Hq + h0 + h) * a.n_split + split) * (D + 4);
+    float* dst = a.part + (((int64_t)b * a.Hq + h0 + h) * a.slots + split) * (D + 4);
     for (int i = threadIdx.x; i < D + 2; i += kDecThreads) {
       float val = 0.f;
       if (i == 0) {
@@ -259,6 +261,8 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const CodecPa
       dst[i] = val;
     }
   }
+  // finish only after the kernel this one may overlap (a no-op otherwise)
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
 }
 
 // Final step of a merged row: divide by the total mass, rotate back (D H per
@@ -418,10 +422,208 @@ __global__ void __launch_bounds__(kWideWarps * 32) decode_combine_wide_kernel(co
   finish_row<D>(PV, o, L, out + (int64_t)row * D, lane);
 }
 
+// Partials of the fp16 residual window, one CTA per (batch, KV head) and its
+// G <= 8 q heads, as split slot `slot` of their rows.  The window is walked
+// in chunks of 128 tokens with an online base-2 softmax: thread t scores
+// token t of the chunk against every head (its key row loaded with 16-byte
+// reads, all in flight at once; q in shared memory), one warp per head pair
+// takes the chunk maximum and sum, then warp w accumulates tokens w, w+4, ...
+// with lane holding D/32 consecutive coordinates (8- or 16-byte value
+// reads).  The four warps' accumulators are summed in shared memory and
+// rotated into V's coded domain (D signs, then H per V block over
+// sqrt(blk)), so the combine merges and rotates them back with the
+// quantised splits.  The kernel is small and latency-bound: every loop keeps
+// its loads independent so that they overlap.
+constexpr int kWinCh = 128;
+constexpr int kWinMaxG = 8;
+
+template <int D>
+__global__ void __launch_bounds__(128) decode_window_kernel(const CodecParams PV, const uint16_t* __restrict__ q,
+                                                            const uint16_t* __restrict__ kw,
+                                                            const uint16_t* __restrict__ vw,
+                                                            const int32_t* __restrict__ win_len, int win, int W_cap,
+                                                            int Hq, int Hkv, float qscale, float* __restrict__ part,
+                                                            int slots, int slot) {
+  constexpr int E = D / 32;
+  constexpr int KH = D / 8 > 16 ? 16 : D / 8;   // 16-byte key reads in flight per pass
+  __shared__ float s_q[kWinMaxG][D];
+  __shared__ float s_p[kWinMaxG][kWinCh];
+  __shared__ float s_acc[4][kWinMaxG][D];
+  __shared__ float s_m[kWinMaxG], s_al[kWinMaxG], s_l[kWinMaxG];
+  // the decode kernel that follows reads nothing of this one's output: it
+  // may start now (it waits for this grid before it finishes)
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+  const int bh = blockIdx.x, b = bh / Hkv, kvh = bh % Hkv, G = Hq / Hkv;
+  const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+  int wl = win_len ? win_len[b] : win;
+  wl = wl < 0 ? 0 : (wl > W_cap ? W_cap : wl);
+  for (int e = tid; e < G * D; e += 128) s_q[e / D][e % D] = h2f(q[((int64_t)b * Hq + kvh * G) * D + e]) * qscale;
+  if (tid < kWinMaxG) {
+    s_m[tid] = -INFINITY;
+    s_l[tid] = 0.f;
+  }
+  float acc[kWinMaxG][E];
+#pragma unroll
+  for (int h = 0; h < kWinMaxG; ++h)
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[h][e] = 0.f;
+  const uint16_t* kb = kw + ((int64_t)b * Hkv + kvh) * W_cap * D;
+  const uint16_t* vb = vw + ((int64_t)b * Hkv + kvh) * W_cap * D + E * lane;
+  __syncthreads();
+  for (int c0 = 0; c0 < wl; c0 += kWinCh) {
+    const int n = min(kWinCh, wl - c0);
+    // scores: thread tid takes token c0 + tid
+    float sc[kWinMaxG];
+#pragma unroll
+    for (int h = 0; h < kWinMaxG; ++h) sc[h] = tid < n ? 0.f : -INFINITY;
+    if (tid < n) {
+      const uint4* kr = reinterpret_cast<const uint4*>(kb + (int64_t)(c0 + tid) * D);
+#pragma unroll
+      for (int p0 = 0; p0 < D / 8; p0 += KH) {
+        uint4 u[KH];
+#pragma unroll
+        for (int k = 0; k < KH; ++k) u[k] = kr[p0 + k];
+#pragma unroll
+        for (int k = 0; k < KH; ++k) {
+          const uint32_t wv[4] = {u[k].x, u[k].y, u[k].z, u[k].w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float2 kk = __half22float2(*reinterpret_cast<const __half2*>(&wv[j]));
+            const int i = 8 * (p0 + k) + 2 * j;
+#pragma unroll
+            for (int h = 0; h < kWinMaxG; ++h)
+              if (h < G) sc[h] = fmaf(s_q[h][i], kk.x, fmaf(s_q[h][i + 1], kk.y, sc[h]));
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < kWinMaxG; ++h)
+      if (h < G) s_p[h][tid] = sc[h];
+    __syncthreads();
+    // chunk maximum, new running maximum, probabilities and their sum: warp w
+    // takes heads w and w + 4
+    for (int h = w; h < G; h += 4) {
+      float mx = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < kWinCh / 32; ++k) mx = fmaxf(mx, s_p[h][lane + 32 * k]);
+      mx = warp_max(mx);
+      const float mo = s_m[h], mn = fmaxf(mo, mx);
+      float sum = 0.f;
+#pragma unroll
+      for (int k = 0; k < kWinCh / 32; ++k) {
+        const float pv = exp2f(s_p[h][lane + 32 * k] - mn);
+        s_p[h][lane + 32 * k] = pv;
+        sum += pv;
+      }
+      sum = warp_sum(sum);
+      __syncwarp();
+      if (lane == 0) {
+        const float al = mo == -INFINITY ? 0.f : exp2f(mo - mn);
+        s_al[h] = al;
+        s_m[h] = mn;
+        s_l[h] = s_l[h] * al + sum;
+      }
+    }
+    __syncthreads();
+    // values: warp w takes tokens w, w + 4, ...
+#pragma unroll
+    for (int h = 0; h < kWinMaxG; ++h) {
+      const float al = h < G ? s_al[h] : 0.f;
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[h][e] *= al;
+    }
+#pragma unroll 8
+    for (int t = w; t < n; t += 4) {
+      float vv[E];
+      const uint16_t* vr = vb + (int64_t)(c0 + t) * D;
+      if (E == 8) {
+        const uint4 u = *reinterpret_cast<const uint4*>(vr);
+        const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&wv[j]));
+          vv[2 * j] = f.x;
+          vv[2 * j + 1] = f.y;
+        }
+      } else if (E == 4) {
+        const uint2 u = *reinterpret_cast<const uint2*>(vr);
+        const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+        const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+        vv[0] = f0.x; vv[1 % E] = f0.y; vv[2 % E] = f1.x; vv[3 % E] = f1.y;
+      } else {
+        const uint32_t u = *reinterpret_cast<const uint32_t*>(vr);
+        const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&u));
+        vv[0] = f0.x; vv[1 % E] = f0.y;
+      }
+#pragma unroll
+      for (int h = 0; h < kWinMaxG; ++h) {
+        if (h < G) {
+          const float pv = s_p[h][t];
+#pragma unroll
+          for (int e = 0; e < E; ++e) acc[h][e] = fmaf(pv, vv[e], acc[h][e]);
+        }
+      }
+    }
+    __syncthreads();   // s_p is rewritten by the next chunk
+  }
+#pragma unroll
+  for (int h = 0; h < kWinMaxG; ++h)
+#pragma unroll
+    for (int e = 0; e < E; ++e)
+      if (h < G) s_acc[w][h][E * lane + e] = acc[h][e];
+  __syncthreads();
+  // sum the warps, then into V's coded domain, one warp per head: D signs,
+  // unnormalised Walsh-Hadamard per V block (in the lane below E, across
+  // lanes above), then 1 / sqrt(blk)
+  for (int h = w; h < G; h += 4) {
+    float o[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const int i = E * lane + e;
+      const float x = (s_acc[0][h][i] + s_acc[1][h][i]) + (s_acc[2][h][i] + s_acc[3][h][i]);
+      o[e] = flip(x, (PV.sign_bits[i >> 5] >> (i & 31)) & 1u);
+    }
+    for (int hs = 1; hs < E && hs < PV.blk; hs <<= 1) {
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        if ((e & hs) == 0) {
+          const float x = o[e], y = o[e + hs];
+          o[e] = x + y;
+          o[e + hs] = x - y;
+        }
+      }
+    }
+    for (int hs = E; hs < PV.blk; hs <<= 1) {
+      const int lo = hs / E;
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        const float x = __shfl_xor_sync(kFull, o[e], lo);
+        o[e] = (lane & lo) ? (x - o[e]) : (o[e] + x);
+      }
+    }
+    float* dst = part + (((int64_t)b * Hq + kvh * G + h) * slots + slot) * (D + 4);
+#pragma unroll
+    for (int e = 0; e < E; ++e) dst[2 + E * lane + e] = o[e] * PV.inv_sqrt_blk;
+    if (lane == 0) {
+      dst[0] = s_m[h];
+      dst[1] = s_l[h];
+    }
+  }
+}
+
 template <int D, int G>
 int launch_decode(const CodecParams& PK, const CodecParams& PV, const DecodeArgs& a, int B, cudaStream_t st) {
-  dim3 grid(a.n_split, B * a.Hkv);
-  decode_split_kernel<D, G><<<grid, kDecThreads, 0, st>>>(PK, PV, a);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)a.n_split, (unsigned)(B * a.Hkv));
+  cfg.blockDim = dim3(kDecThreads);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = a.pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, decode_split_kernel<D, G>, PK, PV, a) != cudaSuccess) return TQ_ERR_CUDA;
   if (cudaGetLastError() != cudaSuccess) return TQ_ERR_CUDA;
   return TQ_OK;
 }
@@ -509,46 +711,113 @@ extern "C" int tq_decode_workspace_bytes(int B, int Hq, int Hkv, int head_dim, i
   return TQ_OK;
 }
 
-extern "C" int tq_decode_attn(const tq_kv_view* K, const tq_kv_view* V, const uint16_t* q, int B, int Hq,
-                              int Hkv, int64_t S_cap, const int32_t* kv_len, int64_t ctx, float softmax_scale,
-                              uint16_t* out, void* workspace, size_t workspace_bytes, int n_split,
-                              void* stream) {
+namespace tq {
+namespace {
+
+// The fp16 residual window of a decode call (see tq_decode_attn_window).
+struct Window {
+  const uint16_t* k;
+  const uint16_t* v;
+  const int32_t* len;
+  int win, W_cap;
+};
+
+int decode_impl(const tq_kv_view* K, const tq_kv_view* V, const uint16_t* q, int B, int Hq, int Hkv, int64_t S_cap,
+                const int32_t* kv_len, int64_t ctx, float softmax_scale, uint16_t* out, void* workspace,
+                size_t workspace_bytes, int n_split, void* stream, const Window* win) {
   if (!K || !V || !q || !out) return TQ_ERR_ARG;
-  tq::CodecParams PK, PV;
-  int st = tq::make_params(&K->layout, &PK);
+  CodecParams PK, PV;
+  int st = make_params(&K->layout, &PK);
   if (st != TQ_OK) return st;
-  st = tq::make_params(&V->layout, &PV);
+  st = make_params(&V->layout, &PV);
   if (st != TQ_OK) return st;
   if (PK.d != PV.d || PV.m) return TQ_ERR_UNSUPPORTED;
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || ctx < 0 || ctx > S_cap || n_split < 0) return TQ_ERR_ARG;
   if (!K->codes || !K->scales || !V->codes || !V->scales) return TQ_ERR_ARG;
   if (PK.m && (!K->qjl_bits || !K->qjl_rnorm || !K->S)) return TQ_ERR_ARG;
-  if (tq::check_paging(K, S_cap) != TQ_OK || !tq::same_paging(K, V)) return TQ_ERR_ARG;
-  if (!tq::aligned16(K->codes) || !tq::aligned16(V->codes) || !tq::aligned16(q) || !tq::aligned16(out))
+  if (check_paging(K, S_cap) != TQ_OK || !same_paging(K, V)) return TQ_ERR_ARG;
+  if (win && (!win->k || !win->v || win->W_cap < 0 || win->win < 0 || win->win > win->W_cap)) return TQ_ERR_ARG;
+  if (win && Hq / Hkv > kWinMaxG) return TQ_ERR_UNSUPPORTED;
+  if (!aligned16(K->codes) || !aligned16(V->codes) || !aligned16(q) || !aligned16(out)) return TQ_ERR_ALIGN;
+  if (win && (reinterpret_cast<uintptr_t>(win->k) % 8 || reinterpret_cast<uintptr_t>(win->v) % 8))
     return TQ_ERR_ALIGN;
-  const int ns = n_split ? n_split : tq::decode_auto_splits(B, Hkv, ctx);
-  const size_t need = tq::decode_ws_bytes(B, Hq, PK.d, ns);
+  const int ns = n_split ? n_split : decode_auto_splits(B, Hkv, ctx);
+  const int slots = ns + (win ? 1 : 0);
+  const size_t need = decode_ws_bytes(B, Hq, PK.d, slots);
   if (!workspace || workspace_bytes < need) return TQ_ERR_WORKSPACE;
-  if (!tq::aligned16(workspace)) return TQ_ERR_ALIGN;
+  if (!aligned16(workspace)) return TQ_ERR_ALIGN;
   const float sm = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)PK.d);
-  tq::DecodeArgs a{reinterpret_cast<const uint32_t*>(K->codes), K->scales,
-                   reinterpret_cast<const uint32_t*>(K->qjl_bits), K->qjl_rnorm, K->S,
-                   reinterpret_cast<const uint32_t*>(V->codes), V->scales, q, kv_len,
-                   static_cast<float*>(workspace),
-                   {K->page_table, K->page_table ? K->page_size : 0, K->page_table ? K->pages_per_seq : 0},
-                   S_cap, ctx, Hq, Hkv, ns, sm * tq::kLog2e};
+  DecodeArgs a{reinterpret_cast<const uint32_t*>(K->codes), K->scales,
+               reinterpret_cast<const uint32_t*>(K->qjl_bits), K->qjl_rnorm, K->S,
+               reinterpret_cast<const uint32_t*>(V->codes), V->scales, q, kv_len,
+               static_cast<float*>(workspace),
+               {K->page_table, K->page_table ? K->page_size : 0, K->page_table ? K->pages_per_seq : 0},
+               S_cap, ctx, Hq, Hkv, ns, slots, sm * kLog2e, 0};
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int G = Hq / Hkv;
-  if (tq::decode_tc_eligible(PK, PV, G, S_cap, K, V))
-    return tq::launch_decode_tc(PK, PV, K, V, q, kv_len, a.part, tq::decode_part_bytes(B, Hq, PK.d, ns), B, Hq,
-                                Hkv, S_cap, ctx, ns, a.qscale, out, s);
-  switch (PK.d) {
-    case 64: st = tq::launch_decode_g<64>(G, PK, PV, a, B, s); break;
-    case 128: st = tq::launch_decode_g<128>(G, PK, PV, a, B, s); break;
-    default: st = tq::launch_decode_g<256>(G, PK, PV, a, B, s); break;
+  if (win) {
+    // the window's partial first; the split kernel overlaps it
+    const int units = B * Hkv;
+    switch (PK.d) {
+      case 64:
+        decode_window_kernel<64><<<units, 128, 0, s>>>(PV, q, win->k, win->v, win->len, win->win, win->W_cap, Hq,
+                                                       Hkv, a.qscale, a.part, slots, ns);
+        break;
+      case 128:
+        decode_window_kernel<128><<<units, 128, 0, s>>>(PV, q, win->k, win->v, win->len, win->win, win->W_cap, Hq,
+                                                        Hkv, a.qscale, a.part, slots, ns);
+        break;
+      default:
+        decode_window_kernel<256><<<units, 128, 0, s>>>(PV, q, win->k, win->v, win->len, win->win, win->W_cap, Hq,
+                                                        Hkv, a.qscale, a.part, slots, ns);
+        break;
+    }
+    if (cudaGetLastError() != cudaSuccess) return TQ_ERR_CUDA;
+    a.pdl = 1;
+  }
+  if (decode_tc_eligible(PK, PV, G, S_cap, K, V)) {
+    st = launch_decode_tc(PK, PV, K, V, q, kv_len, a.part, decode_part_bytes(B, Hq, PK.d, slots), B, Hq, Hkv, S_cap,
+                          ctx, ns, slots, a.pdl != 0, a.qscale, s);
+  } else {
+    switch (PK.d) {
+      case 64: st = launch_decode_g<64>(G, PK, PV, a, B, s); break;
+      case 128: st = launch_decode_g<128>(G, PK, PV, a, B, s); break;
+      default: st = launch_decode_g<256>(G, PK, PV, a, B, s); break;
+    }
   }
   if (st != TQ_OK) return st;
-  return tq::decode_combine(PV, a.part, ns, out, B * Hq, s);
+  return decode_combine(PV, a.part, slots, out, B * Hq, s);
+}
+
+}  // namespace
+}  // namespace tq
+
+extern "C" int tq_decode_attn(const tq_kv_view* K, const tq_kv_view* V, const uint16_t* q, int B, int Hq,
+                              int Hkv, int64_t S_cap, const int32_t* kv_len, int64_t ctx, float softmax_scale,
+                              uint16_t* out, void* workspace, size_t workspace_bytes, int n_split,
+                              void* stream) {
+  return tq::decode_impl(K, V, q, B, Hq, Hkv, S_cap, kv_len, ctx, softmax_scale, out, workspace, workspace_bytes,
+                         n_split, stream, nullptr);
+}
+
+extern "C" int tq_decode_window_workspace_bytes(int B, int Hq, int Hkv, int head_dim, int64_t ctx, int n_split,
+                                                size_t* bytes) {
+  int ns = 0;
+  size_t b0 = 0;
+  const int st = tq_decode_workspace_bytes(B, Hq, Hkv, head_dim, ctx, n_split, &b0, &ns);
+  if (st != TQ_OK) return st;
+  *bytes = tq::decode_ws_bytes(B, Hq, head_dim, ns + 1);
+  return TQ_OK;
+}
+
+extern "C" int tq_decode_attn_window(const tq_kv_view* K, const tq_kv_view* V, const uint16_t* q, int B, int Hq,
+                                     int Hkv, int64_t S_cap, const int32_t* kv_len, int64_t ctx,
+                                     const uint16_t* k_win, const uint16_t* v_win, int W_cap,
+                                     const int32_t* win_len, int win, float softmax_scale, uint16_t* out,
+                                     void* workspace, size_t workspace_bytes, int n_split, void* stream) {
+  const tq::Window w{k_win, v_win, win_len, win, W_cap};
+  return tq::decode_impl(K, V, q, B, Hq, Hkv, S_cap, kv_len, ctx, softmax_scale, out, workspace, workspace_bytes,
+                         n_split, stream, &w);
 }
 
 // ---------------------------------------------------------------------------

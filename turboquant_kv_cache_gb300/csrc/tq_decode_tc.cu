@@ -91,6 +91,8 @@ struct TcArgs {
   int64_t ctx;
   int64_t per;  // tokens per split (multiple of 128)
   int Hq, Hkv, n_split;
+  int slots;    // split slots per row of the partials (n_split, or more for extra partials)
+  int pdl;      // launched as a programmatic dependent of the kernel before it
   float qscale;
 };
 
@@ -601,8 +603,10 @@ __global__ void __launch_bounds__(kThreads, 4) decode_tc_kernel(const CodecParam
         val += wt * (i == 1 ? s_ml[w][1][h] : sO[(w * kG + h) * D + i - 2]);
       }
     }
-    a.part[(((int64_t)b * a.Hq + h0 + h) * a.n_split + split) * (D + 4) + i] = val;
+    a.part[(((int64_t)b * a.Hq + h0 + h) * a.slots + split) * (D + 4) + i] = val;
   }
+  // finish only after the kernel this one may overlap (a no-op otherwise)
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
 }
 
 // S q of every (batch, q head) for QJL keys, times softmax_scale * log2 e *
@@ -664,7 +668,7 @@ int launch_cfg(const CodecParams& PK, const CodecParams& PV, const TcArgs& a, in
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = QJL ? 1 : 0;
+  attr[0].val.programmaticStreamSerializationAllowed = (QJL || a.pdl) ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (cudaLaunchKernelEx(&cfg, kern, PK, PV, a) != cudaSuccess) return TQ_ERR_CUDA;
@@ -717,9 +721,11 @@ size_t decode_tc_extra_bytes(int B, int Hq) {
   return (size_t)B * Hq * (kQjlM * 2 + 4) + 256;
 }
 
+// Writes the partials of splits 0 .. n_split-1 into rows of `slots` slots;
+// the caller merges them (decode_combine).
 int launch_decode_tc(const CodecParams& PK, const CodecParams& PV, const tq_kv_view* K, const tq_kv_view* V,
                      const uint16_t* q, const int32_t* kv_len, float* part, size_t part_bytes, int B, int Hq, int Hkv,
-                     int64_t S_cap, int64_t ctx, int n_split, float qscale, uint16_t* out, cudaStream_t st) {
+                     int64_t S_cap, int64_t ctx, int n_split, int slots, bool pdl, float qscale, cudaStream_t st) {
   TcArgs a{};
   a.kc = K->codes;
   a.ks = reinterpret_cast<const uint8_t*>(K->scales);
@@ -737,6 +743,8 @@ int launch_decode_tc(const CodecParams& PK, const CodecParams& PV, const tq_kv_v
   a.Hq = Hq;
   a.Hkv = Hkv;
   a.n_split = n_split;
+  a.slots = slots;
+  a.pdl = pdl ? 1 : 0;
   a.qscale = qscale;
   if (PK.m) {
     uint8_t* extra = reinterpret_cast<uint8_t*>(part) + ((part_bytes + 255) / 256) * 256;
@@ -764,8 +772,7 @@ int launch_decode_tc(const CodecParams& PK, const CodecParams& PV, const tq_kv_v
                               : launch_cfg<128, 3, 3, false, false, false>(PK, PV, a, B, st))
                        : launch_cfg<128, 2, 3, false, false, false>(PK, PV, a, B, st);
   }
-  if (r != TQ_OK) return r;
-  return decode_combine(PV, part, n_split, out, B * Hq, st);
+  return r;
 }
 
 }  // namespace tq

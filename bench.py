@@ -561,6 +561,17 @@ def _extra_qjl(tb, torch, inputs, dev, flush, hbm, steps, warm):
         "ms": round(ms, 4), "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1),
         "roofline": {"bound": "hbm", "achieved": round(nbytes / (ms * 1e-3) / 1e9, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(nbytes / (ms * 1e-3) / 1e9 / hbm, 4)}}
+    # QJL on the values too (2-bit + QJL m=128 for K and V, each its own S)
+    del V
+    Sv = torch.from_numpy(inputs.qjl_matrix(128, 128, 8)).to(dev)
+    V2 = _cache_from(tb, torch, Lk, w["v"], dev, S=Sv)
+    ms = _time(torch, lambda: tb.tq_decode_attn(K, V2, q, ctx=16384), flush, steps, warm)
+    nbytes = K.nbytes() + V2.nbytes()
+    out["decode_qjl_keys_values_ctx16384"] = {
+        "workload": "B=4, Hq=32, Hkv=8, d=128, ctx=16384; K and V 2-bit + QJL m=128, one norm per vector",
+        "ms": round(ms, 4), "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1),
+        "roofline": {"bound": "hbm", "achieved": round(nbytes / (ms * 1e-3) / 1e9, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(nbytes / (ms * 1e-3) / 1e9 / hbm, 4)}}
     return out
 
 

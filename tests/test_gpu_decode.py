@@ -289,3 +289,38 @@ def test_decode_window_argument_errors(tqlib):
     assert e.value.status == -1
     with pytest.raises(ValueError):
         tb.tq_decode_attn_window(K, K, q, kw, kw[:, :, :8], ctx=64)
+
+
+QJL_V_CASES = [
+    # QJL residual on V (CUDA-core kernel): name, K (block, bits, m, nc, seed), V, B, Hq, Hkv, S_cap, ctx, kv_len, d
+    ("v2bit_qjl_gqa4", (32, 3, 0, 0, 1), (128, 2, 128, 0, 2), 2, 8, 2, 400, 391, [391, 100], 128),
+    ("qjl_k_and_v", (128, 2, 128, 0, 1), (128, 2, 128, 0, 3), 2, 8, 2, 300, 300, None, 128),
+    ("v3bit_qjl64_nc_d64", (64, 3, 0, 0, 4), (64, 3, 64, 1, 5), 1, 2, 2, 260, 257, None, 64),
+    ("v1bit_qjl_d256_gqa8", (32, 4, 0, 0, 1), (256, 1, 128, 0, 6), 1, 8, 1, 150, 150, None, 256),
+]
+
+
+@pytest.mark.parametrize("name,cK,cV,B,Hq,Hkv,S_cap,ctx,kv_len,d", QJL_V_CASES)
+@pytest.mark.parametrize("n_split", [0, 5])
+def test_decode_qjl_values(tqlib, name, cK, cV, B, Hq, Hkv, S_cap, ctx, kv_len, d, n_split):
+    """Values with a QJL residual: the oracle dequantises V with its QJL term
+    (rho sqrt(pi/2)/m S^T (2s - 1), times the norm) and attends; the kernel
+    sums the signs per split and applies S^T once."""
+    from turboquant_kv_cache_gb300 import binding as tb
+    Lk, Lv = O.Layout(d, *cK), O.Layout(d, *cV)
+    Sk = inputs.qjl_matrix(Lk.m, d, 7) if Lk.m else None
+    Sv = inputs.qjl_matrix(Lv.m, d, 8)
+    k = inputs.gaussian((B, Hkv, S_cap, d), 51)
+    v = inputs.gaussian((B, Hkv, S_cap, d), 52)
+    q = inputs.gaussian((B, Hq, d), 53)
+    (kc, ks, kq, kr), kd = _encode_cache(k, Lk, Sk)
+    (vc, vs, vq, vr), vd = _encode_cache(v, Lv, Sv)
+    K = upload_packed(tb, tb.make_layout(d, *cK), Lk, kc, ks, kq, kr, (B, Hkv, S_cap),
+                      S=torch.from_numpy(Sk).cuda() if Sk is not None else None)
+    V = upload_packed(tb, tb.make_layout(d, *cV), Lv, vc, vs, vq, vr, (B, Hkv, S_cap), S=torch.from_numpy(Sv).cuda())
+    kvl = torch.tensor(kv_len, dtype=torch.int32, device="cuda") if kv_len is not None else None
+    out = tb.tq_decode_attn(K, V, torch.from_numpy(q).cuda(), ctx=ctx, kv_len=kvl, n_split=n_split)
+    torch.cuda.synchronize()
+    ref = O.decode_attention(q, kd, vd, kv_len if kv_len is not None else [ctx] * B)
+    err = np.abs(to_np(out.float()) - ref).max()
+    assert err < ATTN_ATOL, (name, err)

@@ -39,6 +39,9 @@ struct DecodeArgs {
   const float* S;
   const uint32_t* vc;
   const uint16_t* vs;
+  const uint32_t* vq;   // QJL bits of V
+  const uint16_t* vr;   // QJL rho of V
+  const float* Sv;      // V's QJL projection [m][d]
   const uint16_t* q;
   const int32_t* kv_len;
   float* part;          // [B*Hq][slots][d + 4]
@@ -82,10 +85,16 @@ __device__ void smem_wht(float* a, int rows, int blk, float norm) {
   __syncthreads();
 }
 
-template <int D, int G>
+// QV: V carries a QJL residual (m <= kMaxQjlV rows).  The split then also
+// accumulates sum_t p_t s_t rho_t (2 b_t - 1) (m values, lane holds rows
+// lane + 32 k), and its epilogue adds sqrt(pi/2)/m S^T of that, rotated into
+// V's coded domain, to the accumulator: the QJL term of every value, applied
+// once per split instead of once per token.
+template <int D, int G, bool QV>
 __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const CodecParams PK, const CodecParams PV,
                                                                    const DecodeArgs a) {
   constexpr int CPL = D / 32;  // V coordinates per lane
+  constexpr int CQ = QV ? kMaxQjlV / 32 : 1;   // QJL rows of V per lane
   __shared__ float s_q[G][D];          // q, then q^ (rotated, scaled)
   __shared__ float s_qT[D][G];         // q^ transposed: coordinate-major
   __shared__ float s_sq[kMaxQjl][G];   // S q (QJL keys)
@@ -93,6 +102,9 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const CodecPa
   __shared__ float s_p[kWarps][32][G];
   __shared__ float s_ml[kWarps][2][G];
   __shared__ float s_acc[kWarps][D];   // one head at a time in the final merge
+  __shared__ float s_accq[QV ? kWarps : 1][QV ? kMaxQjlV : 1];
+  __shared__ float s_aq[QV ? kMaxQjlV : 1];
+  __shared__ float s_proj[QV ? D : 1];
 
   const int split = blockIdx.x;
   const int bh = blockIdx.y;           // b * Hkv + kv head
@@ -136,14 +148,17 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const CodecPa
   const int64_t t_begin = (int64_t)split * per;
   const int64_t t_end = imin64(t_begin + per, len);
 
-  float m_run[G], l_run[G], acc[G][CPL];
+  float m_run[G], l_run[G], acc[G][CPL], accq[G][CQ];
 #pragma unroll
   for (int h = 0; h < G; ++h) {
     m_run[h] = -INFINITY;
     l_run[h] = 0.f;
 #pragma unroll
     for (int k = 0; k < CPL; ++k) acc[h][k] = 0.f;
+#pragma unroll
+    for (int k = 0; k < CQ; ++k) accq[h][k] = 0.f;
   }
+  const int mq = QV ? PV.m / 32 : 0;   // QJL words of a V record
   const int kwords = PK.code_bytes / 4, vwords = PV.code_bytes / 4;
   auto rec_of = [&](int64_t t) { return cache_rec(a.pages, a.Hkv, a.S_cap, b, kvh, t); };
 
@@ -210,6 +225,10 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const CodecPa
       m_run[h] = m_new;
 #pragma unroll
       for (int k = 0; k < CPL; ++k) acc[h][k] *= alpha;
+      if (QV) {
+#pragma unroll
+        for (int k = 0; k < CQ; ++k) accq[h][k] *= alpha;
+      }
       s_p[wid][lane][h] = p;
     }
     __syncwarp();
@@ -224,6 +243,19 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const CodecPa
         const float v = s_centV[code_at(rec, PV.bits, i)] * h2f(sc[i / PV.blk]);
 #pragma unroll
         for (int h = 0; h < G; ++h) acc[h][k] = fmaf(s_p[wid][tt][h], v, acc[h][k]);
+      }
+      if (QV) {
+        // the norm times rho weighs the +-1 signs of the token
+        const float wr = h2f(sc[0]) * h2f(a.vr[r]);
+        const uint32_t* qb = a.vq + r * mq;
+#pragma unroll
+        for (int k = 0; k < CQ; ++k) {
+          if (k < mq) {
+            const float sgn = ((qb[k] >> lane) & 1u) ? wr : -wr;
+#pragma unroll
+            for (int h = 0; h < G; ++h) accq[h][k] = fmaf(s_p[wid][tt][h], sgn, accq[h][k]);
+          }
+        }
       }
     }
     __syncwarp();
@@ -241,10 +273,34 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const CodecPa
     __syncthreads();
 #pragma unroll
     for (int k = 0; k < CPL; ++k) s_acc[wid][lane + 32 * k] = acc[h][k];
+    if (QV) {
+#pragma unroll
+      for (int k = 0; k < CQ; ++k) s_accq[wid][lane + 32 * k] = accq[h][k];
+    }
     __syncthreads();
     float M = -INFINITY;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) M = fmaxf(M, s_ml[w][0][h]);
+    if (QV) {
+      // the merged sign sums, then sqrt(pi/2)/m S^T of them (input domain),
+      // then into V's coded domain: D signs, H per block over sqrt(blk)
+      for (int k = threadIdx.x; k < PV.m; k += kDecThreads) {
+        float v = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+          const float mw = s_ml[w][0][h];
+          v += (mw == -INFINITY ? 0.f : exp2f(mw - M)) * s_accq[w][k];
+        }
+        s_aq[k] = v;
+      }
+      __syncthreads();
+      for (int i = threadIdx.x; i < D; i += kDecThreads) {
+        float v = 0.f;
+        for (int k = 0; k < PV.m; ++k) v = fmaf(__ldg(a.Sv + (int64_t)k * D + i), s_aq[k], v);
+        s_proj[i] = flip(v * (kSqrtHalfPi / (float)PV.m), (PV.sign_bits[i >> 5] >> (i & 31)) & 1u);
+      }
+      smem_wht<D>(s_proj, 1, PV.blk, PV.inv_sqrt_blk);
+    }
     float* dst = a.part + (((int64_t)b * a.Hq + h0 + h) * a.slots + split) * (D + 4);
     for (int i = threadIdx.x; i < D + 2; i += kDecThreads) {
       float val = 0.f;
@@ -257,6 +313,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const CodecPa
           const float wt = mw == -INFINITY ? 0.f : exp2f(mw - M);
           val += wt * (i == 1 ? s_ml[w][1][h] : s_acc[w][i - 2]);
         }
+        if (QV && i >= 2) val += s_proj[i - 2];
       }
       dst[i] = val;
     }
@@ -612,7 +669,7 @@ __global__ void __launch_bounds__(128) decode_window_kernel(const CodecParams PV
   }
 }
 
-template <int D, int G>
+template <int D, int G, bool QV>
 int launch_decode(const CodecParams& PK, const CodecParams& PV, const DecodeArgs& a, int B, cudaStream_t st) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)a.n_split, (unsigned)(B * a.Hkv));
@@ -623,7 +680,7 @@ int launch_decode(const CodecParams& PK, const CodecParams& PV, const DecodeArgs
   attr[0].val.programmaticStreamSerializationAllowed = a.pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, decode_split_kernel<D, G>, PK, PV, a) != cudaSuccess) return TQ_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, decode_split_kernel<D, G, QV>, PK, PV, a) != cudaSuccess) return TQ_ERR_CUDA;
   if (cudaGetLastError() != cudaSuccess) return TQ_ERR_CUDA;
   return TQ_OK;
 }
@@ -632,10 +689,10 @@ template <int D>
 int launch_decode_g(int G, const CodecParams& PK, const CodecParams& PV, const DecodeArgs& a, int B,
                     cudaStream_t st) {
   switch (G) {
-    case 1: return launch_decode<D, 1>(PK, PV, a, B, st);
-    case 2: return launch_decode<D, 2>(PK, PV, a, B, st);
-    case 4: return launch_decode<D, 4>(PK, PV, a, B, st);
-    case 8: return launch_decode<D, 8>(PK, PV, a, B, st);
+    case 1: return PV.m ? launch_decode<D, 1, true>(PK, PV, a, B, st) : launch_decode<D, 1, false>(PK, PV, a, B, st);
+    case 2: return PV.m ? launch_decode<D, 2, true>(PK, PV, a, B, st) : launch_decode<D, 2, false>(PK, PV, a, B, st);
+    case 4: return PV.m ? launch_decode<D, 4, true>(PK, PV, a, B, st) : launch_decode<D, 4, false>(PK, PV, a, B, st);
+    case 8: return PV.m ? launch_decode<D, 8, true>(PK, PV, a, B, st) : launch_decode<D, 8, false>(PK, PV, a, B, st);
     default: return TQ_ERR_UNSUPPORTED;
   }
 }
@@ -731,10 +788,11 @@ int decode_impl(const tq_kv_view* K, const tq_kv_view* V, const uint16_t* q, int
   if (st != TQ_OK) return st;
   st = make_params(&V->layout, &PV);
   if (st != TQ_OK) return st;
-  if (PK.d != PV.d || PV.m) return TQ_ERR_UNSUPPORTED;
+  if (PK.d != PV.d || PV.m > kMaxQjlV) return TQ_ERR_UNSUPPORTED;
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || ctx < 0 || ctx > S_cap || n_split < 0) return TQ_ERR_ARG;
   if (!K->codes || !K->scales || !V->codes || !V->scales) return TQ_ERR_ARG;
   if (PK.m && (!K->qjl_bits || !K->qjl_rnorm || !K->S)) return TQ_ERR_ARG;
+  if (PV.m && (!V->qjl_bits || !V->qjl_rnorm || !V->S)) return TQ_ERR_ARG;
   if (check_paging(K, S_cap) != TQ_OK || !same_paging(K, V)) return TQ_ERR_ARG;
   if (win && (!win->k || !win->v || win->W_cap < 0 || win->win < 0 || win->win > win->W_cap)) return TQ_ERR_ARG;
   if (win && Hq / Hkv > kWinMaxG) return TQ_ERR_UNSUPPORTED;
@@ -749,7 +807,8 @@ int decode_impl(const tq_kv_view* K, const tq_kv_view* V, const uint16_t* q, int
   const float sm = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)PK.d);
   DecodeArgs a{reinterpret_cast<const uint32_t*>(K->codes), K->scales,
                reinterpret_cast<const uint32_t*>(K->qjl_bits), K->qjl_rnorm, K->S,
-               reinterpret_cast<const uint32_t*>(V->codes), V->scales, q, kv_len,
+               reinterpret_cast<const uint32_t*>(V->codes), V->scales,
+               reinterpret_cast<const uint32_t*>(V->qjl_bits), V->qjl_rnorm, V->S, q, kv_len,
                static_cast<float*>(workspace),
                {K->page_table, K->page_table ? K->page_size : 0, K->page_table ? K->pages_per_seq : 0},
                S_cap, ctx, Hq, Hkv, ns, slots, sm * kLog2e, 0};
@@ -775,7 +834,7 @@ int decode_impl(const tq_kv_view* K, const tq_kv_view* V, const uint16_t* q, int
     if (cudaGetLastError() != cudaSuccess) return TQ_ERR_CUDA;
     a.pdl = 1;
   }
-  if (decode_tc_eligible(PK, PV, G, S_cap, K, V)) {
+  if (!PV.m && decode_tc_eligible(PK, PV, G, S_cap, K, V)) {
     st = launch_decode_tc(PK, PV, K, V, q, kv_len, a.part, decode_part_bytes(B, Hq, PK.d, slots), B, Hq, Hkv, S_cap,
                           ctx, ns, slots, a.pdl != 0, a.qscale, s);
   } else {

@@ -11,6 +11,7 @@ namespace tq {
 
 constexpr int kMaxDim = 256;
 constexpr int kMaxQjl = 256;
+constexpr int kMaxQjlV = 128;   // QJL rows of V the decode takes
 
 // Everything a kernel needs to know about one codec layout, passed by value
 // as a kernel parameter (no device-side state in the library).

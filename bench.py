@@ -220,6 +220,8 @@ def run_only(args, tb, torch, inputs, dev):
     elif args.only == "decode_depth":
         L, K, V, q = headline_cache(tb, torch, inputs, dev)
         res.update(bench_depth(tb, torch, dev, L, K, V, q, args.steps, args.warmup))
+    elif args.only == "polar":
+        res.update(bench_polar(tb, torch, inputs, dev, args.steps, args.warmup))
     elif args.only == "decode_window":
         L, K, V, q = headline_cache(tb, torch, inputs, dev)
         res.update(bench_window(tb, torch, inputs, dev, K, V, q, args.steps, args.warmup))
@@ -291,6 +293,7 @@ def run_gpu(args, rank, world):
     quant = bench_quantize(tb, torch, inputs, dev, args)
     depth = None if args.no_extra else bench_depth(tb, torch, dev, L, K, V, q, max(3, min(args.steps, 20)), 3)
     window = None if args.no_extra else bench_window(tb, torch, inputs, dev, K, V, q, max(3, min(args.steps, 20)), 3)
+    polar = None if args.no_extra else bench_polar(tb, torch, inputs, dev, max(3, min(args.steps, 20)), 3)
     extra = {} if args.no_extra else bench_extra(tb, torch, inputs, dev, args)
     if rank == 0:
         line = {
@@ -311,6 +314,7 @@ def run_gpu(args, rank, world):
             "quantize": quant,
             "decode_vs_depth": depth,
             "decode_with_fp16_window": window,
+            "polar_codec": polar,
             "other_workloads": extra,
             "gpu_launches": args.steps * 2,
             "clocks": clocks.summary(),
@@ -418,6 +422,30 @@ def bench_quantize(tb, torch, inputs, dev, args):
         res[name] = {"gvec_per_s": round(n_vec / (ms * 1e-3) / 1e9, 3), "ms": round(ms, 5),
                      "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
                                   "frac": round(gbs / peak, 4), "bytes_per_vector": bytes_per_vec}}
+    return res
+
+
+def bench_polar(tb, torch, inputs, dev, steps, warm):
+    """The recursive polar-angle quantizer on the Llama-3.2-1B-shaped K and V
+    (d = 64, 3-bit angles): quantise and dequantise (fp16 out) of all
+    vectors per step, L2 flushed before each."""
+    w = inputs.llama1b_kv_workload()
+    x = torch.cat([torch.from_numpy(w["k"]).reshape(-1, 64), torch.from_numpy(w["v"]).reshape(-1, 64)]).to(dev)
+    n = x.shape[0]
+    flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=dev)
+    peak, _ = _peaks()
+    bits = 3
+    codes, radius = tb.tq_polar_quantize(x, bits)
+    out = torch.empty_like(x)
+    ms_q = _time(torch, lambda: tb.tq_polar_quantize(x, bits), flush, steps, warm)
+    ms_d = _time(torch, lambda: tb.tq_polar_dequantize(codes, radius, 64, bits, out=out), flush, steps, warm)
+    bq = 64 * 2 + 64 * bits // 8 + 2        # fp16 in; angle codes and fp16 radius out
+    res = {"workload": "Llama-3.2-1B-shaped K and V (524,288 vectors of d=64), 3-bit angles", "vectors": n}
+    for name, ms in (("quantize", ms_q), ("dequantize", ms_d)):
+        gbs = n * bq / (ms * 1e-3) / 1e9
+        res[name] = {"ms": round(ms, 4), "gvec_per_s": round(n / (ms * 1e-3) / 1e9, 3),
+                     "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                                  "frac": round(gbs / peak, 4), "bytes_per_vector": bq}}
     return res
 
 
@@ -663,7 +691,7 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--only", default=None,
                     choices=["decode", "quantize", "prefill", "decode_d256", "decode_qjl", "quantize_qjl", "decode_depth",
-                             "decode_window"],
+                             "decode_window", "polar"],
                     help="time one workload alone and print its result only (profiler runs)")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -276,6 +276,31 @@ int tq_decode_attn_window(const tq_kv_view* K, const tq_kv_view* V, const uint16
                           const int32_t* win_len, int win, float softmax_scale, uint16_t* out,
                           void* workspace, size_t workspace_bytes, int n_split, void* stream);
 
+/* Recursive polar-angle quantizer ("TurboQuant: 3-Bit Compression with Zero
+ * Overhead", Part 1: the recursive polar transformation and its quantisation
+ * step), a codec of its own beside the rotation + Lloyd-Max one.  A vector
+ * of head_dim = 2^k values becomes its L2 norm and head_dim - 1 angles:
+ * level 1 pairs coordinates (x[2i], x[2i+1]) into radius sqrt(x0^2 + x1^2)
+ * and angle atan2(x1, x0), every further level pairs the previous radii the
+ * same way.  Each angle is stored as the index k of the nearest point
+ * k / (2^b - 1) * 2 pi - pi of a uniform grid over [-pi, pi] (ties to even).
+ *   x        device rows of x_row_stride elements (fp16 or fp32, 2/4-byte
+ *            aligned); row i holds vector i
+ *   codes    device [n_vec, head_dim*bits/8] bytes, 16-byte aligned: the
+ *            angle indices level by level (level 1 first, the root's last,
+ *            then one 0 index), packed like the MSE codes (32-code groups of
+ *            nibble words, see tq_kv_view)
+ *   radius   device fp16 [n_vec], 2-byte aligned
+ * head_dim 64, 128 or 256 and bits 1-4, else TQ_ERR_UNSUPPORTED.
+ * Dequantisation rebuilds the tree from the root: a radius r with angle t
+ * gives the children r cos(t), r sin(t); out is [n_vec, head_dim] fp16 or
+ * fp32, 16-byte aligned. */
+int tq_polar_code_bytes(int head_dim, int bits, int64_t* code_bytes);
+int tq_polar_quantize(const void* x, int x_dtype, int64_t n_vec, int head_dim, int64_t x_row_stride, int bits,
+                      uint8_t* codes, uint16_t* radius, void* stream);
+int tq_polar_dequantize(const uint8_t* codes, const uint16_t* radius, int64_t n_vec, int head_dim, int bits,
+                        void* out, int out_dtype, void* stream);
+
 /* Workspace bytes for tq_decode_attn_window with these sizes (host). */
 int tq_decode_window_workspace_bytes(int B, int Hq, int Hkv, int head_dim, int64_t ctx, int n_split,
                                      size_t* bytes);

@@ -172,6 +172,22 @@ def test_window_decode_checks_need_no_gpu(tqlib):
     assert tb.tq_decode_window_workspace_bytes(8, 32, 8, 128, 32768, 9) == _decode_ws(8, 32, 128, 10)
 
 
+def test_polar_checks_need_no_gpu(tqlib):
+    cb = ctypes.c_int64()
+    assert tqlib.tq_polar_code_bytes(128, 3, ctypes.byref(cb)) == 0 and cb.value == 48
+    assert tqlib.tq_polar_code_bytes(96, 3, ctypes.byref(cb)) == -2      # not a power of two
+    assert tqlib.tq_polar_code_bytes(128, 5, ctypes.byref(cb)) == -2
+    P16 = ctypes.c_void_p(16)
+    # no vectors: nothing to do, even without buffers
+    assert tqlib.tq_polar_quantize(None, 0, 0, 128, 128, 3, None, None, None) == 0
+    assert tqlib.tq_polar_dequantize(None, None, 0, 128, 3, None, 0, None) == 0
+    # bad stride, bad dtype, misaligned codes or radius
+    assert tqlib.tq_polar_quantize(P16, 0, 4, 128, 64, 3, P16, P16, None) == -1
+    assert tqlib.tq_polar_quantize(P16, 5, 4, 128, 128, 3, P16, P16, None) == -1
+    assert tqlib.tq_polar_quantize(P16, 0, 4, 128, 128, 3, ctypes.c_void_p(24), P16, None) == -3
+    assert tqlib.tq_polar_dequantize(P16, ctypes.c_void_p(17), 4, 128, 3, P16, 0, None) == -3
+
+
 def _decode_ws(B, Hq, d, ns):
     # split partials [B*Hq][n_split][d + 4] fp32, rounded up to 256 bytes, then
     # the tensor-core path's S q rows (fp16, m = 128) and row sums of QJL keys

@@ -58,6 +58,9 @@ def _load():
         "tq_decode_workspace_bytes": (I, [I, I, I, I, I64, I, P, P]),
         "tq_decode_attn_window": (I, [P, P, P, I, I, I, I64, P, I64, P, P, I, P, I, ctypes.c_float, P, P, SZ, I, P]),
         "tq_decode_window_workspace_bytes": (I, [I, I, I, I, I64, I, P]),
+        "tq_polar_code_bytes": (I, [I, I, P]),
+        "tq_polar_quantize": (I, [P, I, I64, I, I64, I, P, P, P]),
+        "tq_polar_dequantize": (I, [P, P, I64, I, I, P, I, P]),
         "tq_decode_attn_static": (I, [P, P, P, I, I, I, I64, P, I64, ctypes.c_float, P, I, P]),
         "tq_prefill_attn": (I, [P, P, P, I, I, I, I, I64, I64, I, ctypes.c_float, P, P, SZ, P]),
         "tq_prefill_workspace_bytes": (I, [I, I, I, I, I, I64, P]),
@@ -364,6 +367,38 @@ def tq_decode_attn_window(K, V, q, k_win, v_win, ctx=None, kv_len=None, win_len=
                                    _ptr(k_win), _ptr(v_win), W_cap, _ptr(win_len), win, float(softmax_scale),
                                    _ptr(out), _ptr(workspace), workspace.numel(), n_split, _stream(stream))
     _check(st, "tq_decode_attn_window")
+    return out
+
+
+def tq_polar_quantize(x, bits, stream=None):
+    """Polar-angle quantise x [..., d] (fp16/fp32, CUDA, last dim
+    contiguous): returns (codes uint8 [..., d*bits/8], radius fp16 [...])."""
+    lib = _load()
+    d = x.shape[-1]
+    if x.stride(-1) != 1:
+        raise ValueError("x must have a contiguous last dimension")
+    lead = tuple(x.shape[:-1])
+    x2 = x.reshape(-1, d)
+    n = x2.shape[0]
+    cb = ctypes.c_int64()
+    _check(lib.tq_polar_code_bytes(d, bits, ctypes.byref(cb)), "tq_polar_code_bytes")
+    codes = torch.empty(lead + (cb.value,), dtype=torch.uint8, device=x.device)
+    radius = torch.empty(lead, dtype=torch.float16, device=x.device)
+    st = lib.tq_polar_quantize(_ptr(x2), _dtype_code(x.dtype), n, d, x2.stride(0), bits, _ptr(codes), _ptr(radius),
+                               _stream(stream))
+    _check(st, "tq_polar_quantize")
+    return codes, radius
+
+
+def tq_polar_dequantize(codes, radius, head_dim, bits, out_dtype=torch.float16, out=None, stream=None):
+    lib = _load()
+    lead = tuple(radius.shape)
+    n = radius.numel()
+    if out is None:
+        out = torch.empty(lead + (head_dim,), dtype=out_dtype, device=codes.device)
+    st = lib.tq_polar_dequantize(_ptr(codes), _ptr(radius), n, head_dim, bits, _ptr(out), _dtype_code(out.dtype),
+                                 _stream(stream))
+    _check(st, "tq_polar_dequantize")
     return out
 
 

@@ -482,6 +482,48 @@ def dequantize(codes_packed, scales, L: Layout, qjl_packed=None, rho=None, S=Non
 
 
 # --------------------------------------------------------------------------
+# GGML-style blocks (llama.cpp-turboquant "GGML Types": 32 values per block,
+# a 2-byte norm then the packed codes, 14 bytes at 3 bits, 18 at 4 bits; the
+# "How it works" section: the norm of a 128-value rotation chunk is stored in
+# each of its 32-value blocks)
+# --------------------------------------------------------------------------
+def block_bytes(bits: int) -> int:
+    return 2 + 4 * bits
+
+
+def to_blocks(codes_packed: np.ndarray, scales: np.ndarray, L: Layout) -> np.ndarray:
+    """codes [N, d*bits/8] + scales fp16 [N, d/blk] -> uint8 [N, d/32 *
+    (2 + 4 bits)]: block j = the fp16 norm of the rotation block holding
+    values 32j .. 32j+31 (little-endian), then group j's packed code bytes."""
+    codes_packed = np.asarray(codes_packed, dtype=np.uint8)
+    sc = np.asarray(scales, dtype=np.float16).reshape(codes_packed.shape[0], L.nb)
+    N = codes_packed.shape[0]
+    bb, gb = block_bytes(L.bits), 4 * L.bits
+    out = np.zeros((N, (L.d // 32) * bb), dtype=np.uint8)
+    for j in range(L.d // 32):
+        norm = sc[:, (32 * j) // L.blk].view(np.uint16)
+        out[:, j * bb] = (norm & 0xFF).astype(np.uint8)
+        out[:, j * bb + 1] = (norm >> 8).astype(np.uint8)
+        out[:, j * bb + 2:(j + 1) * bb] = codes_packed[:, j * gb:(j + 1) * gb]
+    return out
+
+
+def from_blocks(blocks: np.ndarray, L: Layout):
+    """Inverse of ``to_blocks``: the norm of a rotation block is read from its
+    first 32-value block."""
+    blocks = np.asarray(blocks, dtype=np.uint8)
+    N = blocks.shape[0]
+    bb, gb = block_bytes(L.bits), 4 * L.bits
+    codes = np.zeros((N, L.d * L.bits // 8), dtype=np.uint8)
+    sc = np.zeros((N, L.nb), dtype=np.uint16)
+    for j in range(L.d // 32):
+        codes[:, j * gb:(j + 1) * gb] = blocks[:, j * bb + 2:(j + 1) * bb]
+        if (32 * j) % L.blk == 0:
+            sc[:, (32 * j) // L.blk] = blocks[:, j * bb].astype(np.uint16) | (blocks[:, j * bb + 1].astype(np.uint16) << 8)
+    return codes, sc.view(np.float16)
+
+
+# --------------------------------------------------------------------------
 # S9-S14  attention over the decoded cache (no Hadamard-domain shortcut)
 # --------------------------------------------------------------------------
 def softmax_rows(s: np.ndarray) -> np.ndarray:

@@ -403,3 +403,31 @@ def test_beta_codebook_tends_to_gaussian():
         errs.append(np.max(np.abs(c * np.sqrt(blk) - g)))
     assert errs[0] > errs[1] > errs[2]
     assert errs[2] < 2e-3
+
+
+# ---------------------------------------------------------------- GGML-style blocks
+def test_block_bytes_are_the_pages_ggml_types():
+    """14 bytes per 32 values at 3 bits and 18 at 4 bits (llama.cpp-turboquant
+    'GGML Types'), i.e. the pages' 0.4375 and 0.5625 bytes per element."""
+    import json
+    import os
+    g = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "pages_codec_figures.json")))
+    b = g["bytes_per_element"]
+    assert O.block_bytes(3) == b["turbo3"]["block_bytes"] and O.block_bytes(4) == b["turbo4"]["block_bytes"]
+    assert O.block_bytes(3) / 32 == b["turbo3"]["bytes_per_element"]
+
+
+@pytest.mark.parametrize("d,blk,bits", [(128, 128, 3), (256, 128, 4), (128, 32, 3), (64, 64, 2), (128, 128, 1)])
+def test_blocks_round_trip_and_replicate_the_norm(d, blk, bits):
+    L = O.Layout(d, blk, bits, 0, 0, 1)
+    x = np.random.default_rng(d + blk + bits).standard_normal((40, d))
+    codes, scales, _, _ = O.encode(x, L)
+    blocks = O.to_blocks(codes, scales, L)
+    assert blocks.shape == (40, (d // 32) * O.block_bytes(bits))
+    c2, s2 = O.from_blocks(blocks, L)
+    assert np.array_equal(c2, codes) and np.array_equal(s2.view(np.uint16), scales.view(np.uint16))
+    # every 32-value block of a rotation block carries that block's norm
+    bb = O.block_bytes(bits)
+    for j in range(d // 32):
+        norm = blocks[:, j * bb].astype(np.uint16) | (blocks[:, j * bb + 1].astype(np.uint16) << 8)
+        assert np.array_equal(norm.view(np.float16), scales.reshape(40, L.nb)[:, (32 * j) // blk])

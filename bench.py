@@ -220,6 +220,9 @@ def run_only(args, tb, torch, inputs, dev):
     elif args.only == "decode_depth":
         L, K, V, q = headline_cache(tb, torch, inputs, dev)
         res.update(bench_depth(tb, torch, dev, L, K, V, q, args.steps, args.warmup))
+    elif args.only == "blocks":
+        L, K, V, q = headline_cache(tb, torch, inputs, dev)
+        res.update(bench_blocks(tb, torch, dev, K, args.steps, args.warmup))
     elif args.only == "polar":
         res.update(bench_polar(tb, torch, inputs, dev, args.steps, args.warmup))
     elif args.only == "decode_window":
@@ -294,6 +297,7 @@ def run_gpu(args, rank, world):
     depth = None if args.no_extra else bench_depth(tb, torch, dev, L, K, V, q, max(3, min(args.steps, 20)), 3)
     window = None if args.no_extra else bench_window(tb, torch, inputs, dev, K, V, q, max(3, min(args.steps, 20)), 3)
     polar = None if args.no_extra else bench_polar(tb, torch, inputs, dev, max(3, min(args.steps, 20)), 3)
+    blocks = None if args.no_extra else bench_blocks(tb, torch, dev, K, max(3, min(args.steps, 20)), 3)
     extra = {} if args.no_extra else bench_extra(tb, torch, inputs, dev, args)
     if rank == 0:
         line = {
@@ -315,6 +319,7 @@ def run_gpu(args, rank, world):
             "decode_vs_depth": depth,
             "decode_with_fp16_window": window,
             "polar_codec": polar,
+            "ggml_blocks": blocks,
             "other_workloads": extra,
             "gpu_launches": args.steps * 2,
             "clocks": clocks.summary(),
@@ -422,6 +427,23 @@ def bench_quantize(tb, torch, inputs, dev, args):
         res[name] = {"gvec_per_s": round(n_vec / (ms * 1e-3) / 1e9, 3), "ms": round(ms, 5),
                      "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
                                   "frac": round(gbs / peak, 4), "bytes_per_vector": bytes_per_vec}}
+    return res
+
+
+def bench_blocks(tb, torch, dev, K, steps, warm):
+    """GGML-style blocks of the headline K cache (turbo3: 14-byte blocks of
+    32 values): tq_to_blocks and back, L2 flushed before each."""
+    flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=dev)
+    peak, _ = _peaks()
+    blocks = tb.tq_to_blocks(K)
+    nbytes = 2 * K.nbytes()                     # read the packed cache, write the same bytes as blocks
+    ms_to = _time(torch, lambda: tb.tq_to_blocks(K), flush, steps, warm)
+    ms_from = _time(torch, lambda: tb.tq_from_blocks(K.layout, blocks), flush, steps, warm)
+    res = {"workload": "the headline K cache (8 x 8 x 32768 turbo3 vectors of d=128) to 14-byte blocks and back"}
+    for name, ms in (("to_blocks", ms_to), ("from_blocks", ms_from)):
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        res[name] = {"ms": round(ms, 4), "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak,
+                                                      "unit": "GB/s", "frac": round(gbs / peak, 4)}}
     return res
 
 
@@ -691,7 +713,7 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--only", default=None,
                     choices=["decode", "quantize", "prefill", "decode_d256", "decode_qjl", "quantize_qjl", "decode_depth",
-                             "decode_window", "polar"],
+                             "decode_window", "polar", "blocks"],
                     help="time one workload alone and print its result only (profiler runs)")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -276,6 +276,24 @@ int tq_decode_attn_window(const tq_kv_view* K, const tq_kv_view* V, const uint16
                           const int32_t* win_len, int win, float softmax_scale, uint16_t* out,
                           void* workspace, size_t workspace_bytes, int n_split, void* stream);
 
+/* GGML-style blocks (llama.cpp-turboquant, "GGML Types" and "How it
+ * works"): the packed cache of a layout without QJL rewritten as blocks of
+ * 32 values, each the fp16 norm of the values' rotation block (little-endian)
+ * followed by their packed codes (the group's 4*bits bytes of this library's
+ * layout): 2 + 4*bits bytes, 14 at 3 bits and 18 at 4 bits.  With a 128-value
+ * rotation block (and the Beta codebook of a 128-value chunk, codebook 1)
+ * this is the page's turbo3/turbo4 arrangement: the chunk's norm is in each
+ * of its four blocks.  tq_from_blocks takes a rotation block's norm from its
+ * first 32-value block.
+ *   codes   device [n_vec, head_dim*bits/8], 4-byte aligned
+ *   scales  device fp16 [n_vec, head_dim/block], 2-byte aligned
+ *   blocks  device [n_vec, head_dim/32, 2 + 4*bits] bytes, 2-byte aligned
+ * TQ_ERR_UNSUPPORTED for QJL layouts. */
+int tq_to_blocks(const tq_layout* layout, const uint8_t* codes, const uint16_t* scales, int64_t n_vec,
+                 uint8_t* blocks, void* stream);
+int tq_from_blocks(const tq_layout* layout, const uint8_t* blocks, int64_t n_vec, uint8_t* codes,
+                   uint16_t* scales, void* stream);
+
 /* Recursive polar-angle quantizer ("TurboQuant: 3-Bit Compression with Zero
  * Overhead", Part 1: the recursive polar transformation and its quantisation
  * step), a codec of its own beside the rotation + Lloyd-Max one.  A vector

@@ -172,6 +172,17 @@ def test_window_decode_checks_need_no_gpu(tqlib):
     assert tb.tq_decode_window_workspace_bytes(8, 32, 8, 128, 32768, 9) == _decode_ws(8, 32, 128, 10)
 
 
+def test_block_conversion_checks_need_no_gpu(tqlib):
+    L = tb.make_layout(128, 128, 3, 0, 0, 1, codebook=1)
+    Lq = tb.make_layout(128, 128, 2, 128, 0, 1)
+    P16 = ctypes.c_void_p(16)
+    assert tqlib.tq_to_blocks(ctypes.byref(L), None, None, 0, None, None) == 0
+    assert tqlib.tq_to_blocks(ctypes.byref(Lq), P16, P16, 4, P16, None) == -2   # QJL: no block form
+    assert tqlib.tq_to_blocks(ctypes.byref(L), ctypes.c_void_p(18), P16, 4, P16, None) == -3
+    assert tqlib.tq_from_blocks(ctypes.byref(L), ctypes.c_void_p(17), 4, P16, P16, None) == -3
+    assert tqlib.tq_from_blocks(ctypes.byref(L), P16, -1, P16, P16, None) == -1
+
+
 def test_polar_checks_need_no_gpu(tqlib):
     cb = ctypes.c_int64()
     assert tqlib.tq_polar_code_bytes(128, 3, ctypes.byref(cb)) == 0 and cb.value == 48

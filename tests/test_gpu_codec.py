@@ -222,3 +222,26 @@ def test_beta_codebook_quantize_dequantize(tqlib, d, blk, bits, dt, nc, m):
     up = upload_packed(tb, L, Lo, codes, scales, qb, rho, (n,), S=Sg)
     got = to_np(tb.tq_dequantize_kv(up, torch.float32))
     assert rel_l2(got, ref).max() < 1e-5
+
+
+@pytest.mark.parametrize("d,blk,bits,cb", [(128, 128, 3, 1), (256, 128, 4, 1), (128, 32, 3, 0), (64, 64, 2, 0),
+                                           (128, 128, 1, 1)])
+def test_ggml_blocks_match_oracle(tqlib, d, blk, bits, cb):
+    """tq_to_blocks / tq_from_blocks against the oracle's block bytes, byte
+    for byte, on the library's own quantisation of seeded vectors (the
+    128-chunk Beta layout is the llama.cpp-turboquant arrangement)."""
+    from turboquant_kv_cache_gb300 import binding as tb
+    L = tb.make_layout(d, blk, bits, 0, 0, 1, codebook=cb)
+    Lo = O.Layout(d, blk, bits, 0, 0, 1, codebook=cb)
+    x = torch.from_numpy(inputs.gaussian((3, 5, 70, d), 77)).cuda()
+    pk = tb.tq_quantize_kv(L, x)
+    blocks = tb.tq_to_blocks(pk)
+    torch.cuda.synchronize()
+    codes = pk.codes.reshape(-1, pk.codes.shape[-1]).cpu().numpy()
+    scales = pk.scales.reshape(-1, pk.scales.shape[-1]).cpu().numpy()
+    want = O.to_blocks(codes, scales, Lo)
+    got = blocks.reshape(-1, (d // 32) * (2 + 4 * bits)).cpu().numpy()
+    assert np.array_equal(got, want)
+    back = tb.tq_from_blocks(L, blocks)
+    torch.cuda.synchronize()
+    assert torch.equal(back.codes, pk.codes) and torch.equal(back.scales, pk.scales)

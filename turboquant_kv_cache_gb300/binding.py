@@ -59,6 +59,8 @@ def _load():
         "tq_decode_attn_window": (I, [P, P, P, I, I, I, I64, P, I64, P, P, I, P, I, ctypes.c_float, P, P, SZ, I, P]),
         "tq_decode_window_workspace_bytes": (I, [I, I, I, I, I64, I, P]),
         "tq_polar_code_bytes": (I, [I, I, P]),
+        "tq_to_blocks": (I, [P, P, P, I64, P, P]),
+        "tq_from_blocks": (I, [P, P, I64, P, P, P]),
         "tq_polar_quantize": (I, [P, I, I64, I, I64, I, P, P, P]),
         "tq_polar_dequantize": (I, [P, P, I64, I, I, P, I, P]),
         "tq_decode_attn_static": (I, [P, P, P, I, I, I, I64, P, I64, ctypes.c_float, P, I, P]),
@@ -368,6 +370,30 @@ def tq_decode_attn_window(K, V, q, k_win, v_win, ctx=None, kv_len=None, win_len=
                                    _ptr(out), _ptr(workspace), workspace.numel(), n_split, _stream(stream))
     _check(st, "tq_decode_attn_window")
     return out
+
+
+def tq_to_blocks(pk, stream=None):
+    """GGML-style blocks of a PackedKV without QJL: uint8 [..., d/32,
+    2 + 4 bits] (fp16 norm of the rotation block, then the packed codes)."""
+    lib = _load()
+    L = pk.layout
+    n = pk.scales.numel() // pk.scales.shape[-1]
+    bb = 2 + 4 * L.bits
+    out = torch.empty(tuple(pk.lead_shape) + (L.head_dim // 32, bb), dtype=torch.uint8, device=pk.codes.device)
+    _check(lib.tq_to_blocks(ctypes.byref(L), _ptr(pk.codes), _ptr(pk.scales), n, _ptr(out), _stream(stream)),
+           "tq_to_blocks")
+    return out
+
+
+def tq_from_blocks(layout, blocks, stream=None):
+    """Inverse of tq_to_blocks: a PackedKV with leading shape blocks.shape[:-2]."""
+    lib = _load()
+    lead = tuple(blocks.shape[:-2])
+    pk = PackedKV(layout, lead, device=blocks.device)
+    n = pk.scales.numel() // pk.scales.shape[-1]
+    _check(lib.tq_from_blocks(ctypes.byref(layout), _ptr(blocks), n, _ptr(pk.codes), _ptr(pk.scales),
+                              _stream(stream)), "tq_from_blocks")
+    return pk
 
 
 def tq_polar_quantize(x, bits, stream=None):

@@ -389,6 +389,23 @@ struct PrefillTcArgs {
 };
 
 
+// Record of token 0 of a tile as the decoders address it: the item offsets
+// carry the token within the tile.  Contiguous caches: one base per
+// (batch, KV head).  Paged caches: the record of this CTA's half, less the
+// half's offset (a half never crosses a page: both are 32-token aligned).
+struct ContigRec {
+  int64_t rec0;
+  __device__ __forceinline__ int64_t tile(int64_t t0, int, int) const { return rec0 + t0; }
+};
+struct PagedRec {
+  PageMap pm;
+  int64_t S_cap;
+  int H, b, h;
+  __device__ __forceinline__ int64_t tile(int64_t t0, int half0, int nv) const {
+    return nv > half0 ? cache_rec(pm, H, S_cap, b, h, t0 + half0) - half0 : 0;
+  }
+};
+
 // A decoder role: NT threads of each CTA of a pair decode half of every tile
 // of one side (K or V), tokens [32 rank, 32 rank + 32), into the NB-deep ring
 // of shared buffers; in the core-matrix layout that half is one contiguous
@@ -414,11 +431,8 @@ __device__ __forceinline__ void decoder_role(const CodecParams& P, const CodeTab
   const uint32_t peer_buf0 = mapa_peer(buf0, rank ^ 1u), peer_full = mapa_peer(full, rank ^ 1u);
   ItemRegs<D, NT> r0, r1, r2;
   auto load = [&](int t, ItemRegs<D, NT>& r) {
-    // the record of this CTA's half, less the half's offset that the item
-    // offsets carry (a half never crosses a page: both are 32-token aligned)
-    const int half0 = (int)rank * ItemPlan<D, NT>::TOK;
     const int nv = n_valid_of(t);
-    const int64_t rec = nv > half0 ? rec_of(t_lo + (int64_t)t * kTok + half0) - half0 : 0;
+    const int64_t rec = rec_of.tile(t_lo + (int64_t)t * kTok, (int)rank * ItemPlan<D, NT>::TOK, nv);
     load_items<D, NT>(P.bits, pl, codes + rec * P.code_bytes, scales + rec * 2 * P.nb, nv, r);
   };
   // tile t decodes from registers loaded two steps earlier; the load of tile
@@ -510,7 +524,6 @@ __global__ void __launch_bounds__(192 + 32 * (NK + NV), 1) prefill_ws_kernel(con
   const int64_t t_lo = (int64_t)split * a.per;
   const int64_t t_hi = imin64(imin64(t_lo + a.per, a.ctx), max_pos + 1);
   const int n_tiles = t_hi > t_lo ? (int)((t_hi - t_lo + kTok - 1) / kTok) : 0;
-  auto rec_of = [&](int64_t t) { return cache_rec(a.pages, a.Hkv, a.S_cap, b, kvh, t); };
 
   const uint32_t a_smem = su32(smem);
   // NB decoded K buffers, then NB decoded V buffers
@@ -579,12 +592,25 @@ __global__ void __launch_bounds__(192 + 32 * (NK + NV), 1) prefill_ws_kernel(con
     // registers before decoding tile t, so the global latency hides behind
     // the decode.
     if (RB) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(kDecRegs));
-    if (warp < 6 + NK)
-      decoder_role<D, kNK, NB, 1>(PK, s_tabs[0], a.kc, a.ks, tid - 192, kfull, kfree, aK(0), kTileBytes, rec_of, t_lo,
-                               n_tiles, rank, n_valid_of, wait_cl, s_abort);
-    else
-      decoder_role<D, kNV, NB, 2>(PV, s_tabs[1], a.vc, a.vs, tid - 192 - kNK, vfull, vfree, aV(0), kTileBytes, rec_of,
-                               t_lo, n_tiles, rank, n_valid_of, wait_cl, s_abort);
+    // the contiguous and the paged cache get their own copy of the role, so
+    // the contiguous one keeps its single base address
+    const ContigRec crec{(int64_t)bh * a.S_cap};
+    const PagedRec prec{a.pages, a.S_cap, a.Hkv, b, kvh};
+    if (warp < 6 + NK) {
+      if (a.pages.table)
+        decoder_role<D, kNK, NB, 1>(PK, s_tabs[0], a.kc, a.ks, tid - 192, kfull, kfree, aK(0), kTileBytes, prec, t_lo,
+                                    n_tiles, rank, n_valid_of, wait_cl, s_abort);
+      else
+        decoder_role<D, kNK, NB, 1>(PK, s_tabs[0], a.kc, a.ks, tid - 192, kfull, kfree, aK(0), kTileBytes, crec, t_lo,
+                                    n_tiles, rank, n_valid_of, wait_cl, s_abort);
+    } else {
+      if (a.pages.table)
+        decoder_role<D, kNV, NB, 2>(PV, s_tabs[1], a.vc, a.vs, tid - 192 - kNK, vfull, vfree, aV(0), kTileBytes,
+                                    prec, t_lo, n_tiles, rank, n_valid_of, wait_cl, s_abort);
+      else
+        decoder_role<D, kNV, NB, 2>(PV, s_tabs[1], a.vc, a.vs, tid - 192 - kNK, vfull, vfree, aV(0), kTileBytes,
+                                    crec, t_lo, n_tiles, rank, n_valid_of, wait_cl, s_abort);
+    }
   } else if (warp == 4) {
     // ================= S issue: S(t) = Q^ (TMEM) K^(t)^T once K(t) is decoded
     // and S(t-1) has been read.  The whole warp walks the schedule, one

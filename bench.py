@@ -55,7 +55,7 @@ def _peaks():
 # DRAM bytes (read + write) of one decode_tc_kernel launch of the headline
 # workload, from the ncu capture summarised in
 # profiles/decode_tc_qwen3_8b_turbo3_ctx32768.md (None once the kernel changes).
-DECODE_TRAFFIC_BYTES = (235.011072 + 3.253504) * 1e6
+DECODE_TRAFFIC_BYTES = (235.013888 + 3.719424) * 1e6
 
 
 def decode_bytes(B, Hkv, ctx, d, k_bits, v_bits, k_block, v_block):

@@ -140,6 +140,11 @@ def lloyd_max_codebook(bits: int, blk: int, max_iter: int = 1000000):
     K = 1 << bits
     sigma = 1.0 / math.sqrt(blk)
     c = [_STD.inv_cdf((k + 0.5) / K) for k in range(K)]   # in units of sigma
+    if K > 16:
+        # 256 levels: Lloyd's linear convergence is too slow in pure Python;
+        # Newton's method on the same fixed point (see _lloyd_max_newton)
+        c = _lloyd_max_newton(c)
+        max_iter = 0
     last = math.inf
     for _ in range(max_iter):
         edges = [-math.inf] + [0.5 * (c[k] + c[k + 1]) for k in range(K - 1)] + [math.inf]
@@ -159,6 +164,46 @@ def lloyd_max_codebook(bits: int, blk: int, max_iter: int = 1000000):
     bnd = 0.5 * (cent[1:] + cent[:-1])
     _CODEBOOK_CACHE[key] = (cent.copy(), bnd.copy())
     return cent, bnd
+
+
+def _lloyd_max_newton(c: list) -> list:
+    """The Lloyd-Max fixed point for N(0, 1) by Newton's method: the
+    residual F_k = m_k - c_k, with m_k = (phi(l) - phi(u)) / P the mean of
+    cell [l, u] (midpoints of the neighbouring centroids) and P its mass, has
+    a tridiagonal Jacobian: dm/du = phi(u) (u - m) / P, dm/dl = phi(l) (m - l)
+    / P, each edge moving by half of either neighbour's step.  Solved by the
+    Thomas algorithm until the step is at rounding level."""
+    K = len(c)
+    c = list(c)
+    last = math.inf
+    for _ in range(200):
+        edges = [-math.inf] + [0.5 * (c[k] + c[k + 1]) for k in range(K - 1)] + [math.inf]
+        lo, di, up, rhs = [0.0] * K, [0.0] * K, [0.0] * K, [0.0] * K
+        for k in range(K):
+            l, u = edges[k], edges[k + 1]
+            P = _Phi_diff(l, u)
+            m = (_phi(l) - _phi(u)) / P
+            dmu = 0.0 if math.isinf(u) else _phi(u) * (u - m) / P
+            dml = 0.0 if math.isinf(l) else _phi(l) * (m - l) / P
+            lo[k] = 0.5 * dml
+            up[k] = 0.5 * dmu
+            di[k] = 0.5 * dml + 0.5 * dmu - 1.0
+            rhs[k] = -(m - c[k])
+        # Thomas algorithm
+        for k in range(1, K):
+            w = lo[k] / di[k - 1]
+            di[k] -= w * up[k - 1]
+            rhs[k] -= w * rhs[k - 1]
+        step = [0.0] * K
+        step[K - 1] = rhs[K - 1] / di[K - 1]
+        for k in range(K - 2, -1, -1):
+            step[k] = (rhs[k] - up[k] * step[k + 1]) / di[k]
+        c = [c[k] + step[k] for k in range(K)]
+        moved = max(abs(x) for x in step)
+        if moved == 0.0 or (moved < 1e-15 and moved >= last):
+            break
+        last = moved
+    return c
 
 
 def _beta_cell(alpha: float, e0: np.ndarray, e1: np.ndarray):
@@ -260,8 +305,10 @@ class Layout:
         self.seed = int(sign_seed)
         if self.d % self.blk or self.blk < 2 or self.blk & (self.blk - 1):
             raise ValueError("block must be a power of two dividing head_dim")
-        if not 1 <= self.bits <= 4:
-            raise ValueError("bits must be 1..4")
+        if not (1 <= self.bits <= 4 or self.bits == 8):
+            raise ValueError("bits must be 1..4 or 8")
+        if self.bits == 8 and (self.codebook != 0 or qjl_m):
+            raise ValueError("8-bit codes take the Gaussian codebook and no QJL")
         if self.m and (self.blk != self.d or self.m % 32):
             raise ValueError("QJL needs block == head_dim and m a multiple of 32")
 
@@ -389,6 +436,8 @@ def pack_codes(codes: np.ndarray, bits: int) -> np.ndarray:
     blocks of llama.cpp-turboquant (12 and 16 code bytes per 32 values)."""
     codes = np.asarray(codes, dtype=np.int64)
     N, d = codes.shape
+    if bits == 8:   # one byte per code, in coordinate order
+        return codes.astype(np.uint8)
     out = np.zeros((N, d * bits // 8), dtype=np.uint8)
     gb = 4 * bits
     for gi in range(d // 32):
@@ -403,6 +452,8 @@ def unpack_codes(packed: np.ndarray, bits: int, d: int) -> np.ndarray:
     """Inverse of ``pack_codes``."""
     packed = np.asarray(packed, dtype=np.uint8)
     N = packed.shape[0]
+    if bits == 8:
+        return packed[:, :d].astype(np.int64)
     codes = np.zeros((N, d), dtype=np.int64)
     gb = 4 * bits
     for gi in range(d // 32):

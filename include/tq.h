@@ -100,7 +100,9 @@ typedef struct {
  * Bytes per element with block 32: 0.4375 at 3 bits, 0.5625 at 4 bits. */
 
 /* Lloyd-Max codebook of N(0, 1/block) with 2^bits levels, solved in double
- * precision on the host and rounded to nearest float.  centroids: host,
+ * precision on the host and rounded to nearest float (bits 1..8; 16 levels
+ * or fewer by the Lloyd iteration, more by Newton's method on the same
+ * fixed point).  centroids: host,
  * 2^bits floats, ascending; boundaries: host, 2^bits - 1 midpoints.
  * "TurboQuant From Scratch", section 2, step 3; section 3 (distortion
  * about 0.118 / 0.0345 / 0.0095 at 2 / 3 / 4 bits). */

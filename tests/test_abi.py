@@ -27,7 +27,7 @@ def test_every_declared_symbol_is_exported(tqlib):
         assert hasattr(tqlib, n), n
 
 
-@pytest.mark.parametrize("bits", [1, 2, 3, 4])
+@pytest.mark.parametrize("bits", [1, 2, 3, 4, 8])
 @pytest.mark.parametrize("block", [32, 64, 128, 256])
 def test_codebook_matches_oracle(tqlib, bits, block):
     c, b = tb.tq_codebook(bits, block, f64=True)

@@ -10,6 +10,8 @@
 namespace tq {
 namespace {
 
+constexpr int kMaxBits = 8;                 // host codebooks: 1..8 bits
+constexpr int kMaxLevels = 1 << kMaxBits;
 constexpr double kInvSqrt2 = 0.70710678118654752440;
 constexpr double kInvSqrt2Pi = 0.39894228040143267794;
 
@@ -27,8 +29,8 @@ double cell_mass(double a, double b) {
 // fixed point of "boundaries = midpoints, centroids = conditional means"
 // ("TurboQuant From Scratch", section 2, step 3).  The iteration starts from
 // evenly spaced levels on [-2, 2]; for a log-concave density the fixed point
-// is unique, so the start only affects the iteration count.
-void solve_unit_codebook(int levels, double* c) {
+// is unique, so the start only affects the iteration count.  Up to 16 levels.
+void solve_unit_codebook_lloyd(int levels, double* c) {
   for (int k = 0; k < levels; ++k) c[k] = levels == 1 ? 0.0 : -2.0 + 4.0 * k / (levels - 1);
   double edge[17];
   double last = INFINITY;
@@ -47,9 +49,70 @@ void solve_unit_codebook(int levels, double* c) {
     if (moved == 0.0 || (moved < 1e-15 && moved >= last)) break;
     last = moved;
   }
+}
+
+// x with P(Z <= x) = p for a standard normal Z, by bisection on erfc (only
+// used for a starting point, so speed does not matter).
+double normal_quantile(double p) {
+  double lo = -40.0, hi = 40.0;
+  for (int it = 0; it < 200 && hi - lo > 1e-15; ++it) {
+    const double mid = 0.5 * (lo + hi);
+    if (0.5 * std::erfc(-mid * kInvSqrt2) < p) lo = mid; else hi = mid;
+  }
+  return 0.5 * (lo + hi);
+}
+
+// The same fixed point for many levels (256 at 8 bits), where the Lloyd
+// iteration's linear rate is far too slow: Newton's method on
+// F_k(c) = m_k(c) - c_k, m_k the mean of cell [l_k, u_k] whose edges are the
+// midpoints to the neighbouring centroids.  With P the cell's mass,
+// dm/du = phi(u) (u - m) / P and dm/dl = phi(l) (m - l) / P, and each edge
+// moves by half of a neighbour's step, so the Jacobian is tridiagonal and
+// each step is one forward/backward sweep.  Starting point: the centroid
+// density of high-resolution quantisation theory (proportional to the cube
+// root of the source density, i.e. N(0, 3) quantiles).
+void solve_unit_codebook_newton(int levels, double* c) {
+  double lo[kMaxLevels], di[kMaxLevels], up[kMaxLevels], rhs[kMaxLevels];
+  for (int k = 0; k < levels; ++k) c[k] = std::sqrt(3.0) * normal_quantile((k + 0.5) / levels);
+  double last = INFINITY;
+  for (int it = 0; it < 500; ++it) {
+    for (int k = 0; k < levels; ++k) {
+      const double l = k == 0 ? -INFINITY : 0.5 * (c[k - 1] + c[k]);
+      const double u = k + 1 == levels ? INFINITY : 0.5 * (c[k] + c[k + 1]);
+      const double P = cell_mass(l, u);
+      const double m = (density(l) - density(u)) / P;
+      const double dmu = std::isinf(u) ? 0.0 : density(u) * (u - m) / P;
+      const double dml = std::isinf(l) ? 0.0 : density(l) * (m - l) / P;
+      lo[k] = 0.5 * dml;
+      up[k] = 0.5 * dmu;
+      di[k] = 0.5 * (dml + dmu) - 1.0;
+      rhs[k] = c[k] - m;
+    }
+    for (int k = 1; k < levels; ++k) {
+      const double w = lo[k] / di[k - 1];
+      di[k] -= w * up[k - 1];
+      rhs[k] -= w * rhs[k - 1];
+    }
+    double moved = 0.0, next = 0.0;
+    for (int k = levels - 1; k >= 0; --k) {
+      const double step = (rhs[k] - (k + 1 < levels ? up[k] * next : 0.0)) / di[k];
+      next = step;
+      c[k] += step;
+      moved = std::fmax(moved, std::fabs(step));
+    }
+    // quadratic convergence until rounding level, then stop once the step
+    // no longer shrinks
+    if (moved == 0.0 || (moved < 1e-15 && moved >= last)) break;
+    last = moved;
+  }
+}
+
+void solve_unit_codebook(int levels, double* c) {
+  if (levels <= 16) solve_unit_codebook_lloyd(levels, c);
+  else solve_unit_codebook_newton(levels, c);
   // The density is symmetric, so is the exact codebook; symmetrise away the
   // rounding residue so that the middle boundary is exactly zero.
-  double sym[16];
+  double sym[kMaxLevels];
   for (int k = 0; k < levels; ++k) sym[k] = 0.5 * (c[k] - c[levels - 1 - k]);
   for (int k = 0; k < levels; ++k) c[k] = sym[k];
 }
@@ -158,8 +221,8 @@ void solve_beta_codebook(int levels, int blk, double* c) {
 
 struct CodebookCache {
   std::mutex mu;
-  bool ready[5] = {false, false, false, false, false};
-  double unit[5][16];
+  bool ready[kMaxBits + 1] = {};
+  double unit[kMaxBits + 1][kMaxLevels];
   // Beta codebooks per (bits, log2 block) for blocks 32..256
   bool beta_ready[5][9] = {};
   double beta[5][9][16];
@@ -246,7 +309,7 @@ int make_params(const tq_layout* L, CodecParams* p) {
 extern "C" {
 
 int tq_codebook_f64(int bits, int block, double* centroids, double* boundaries) {
-  if (bits < 1 || bits > 4 || block < 1 || !centroids) return TQ_ERR_ARG;
+  if (bits < 1 || bits > tq::kMaxBits || block < 1 || !centroids) return TQ_ERR_ARG;
   const double* u = tq::unit_codebook(bits);
   const int K = 1 << bits;
   const double sigma = 1.0 / std::sqrt(static_cast<double>(block));
@@ -269,7 +332,7 @@ int tq_codebook_kind(int bits, int block, int kind, double* centroids, double* b
 }
 
 int tq_codebook(int bits, int block, float* centroids, float* boundaries) {
-  double c[16], b[16];
+  double c[tq::kMaxLevels], b[tq::kMaxLevels];
   const int st = tq_codebook_f64(bits, block, c, b);
   if (st != TQ_OK) return st;
   const int K = 1 << bits;

@@ -199,6 +199,37 @@ def bench_window(tb, torch, inputs, dev, K, V, q, steps, warm, W=128):
             "bytes_per_step": nbytes, "plain_decode_us": round(ms_0 * 1e3, 2)}
 
 
+def bench_k8v4(tb, torch, inputs, dev, steps, warm):
+    """The headline decode batch (B=8, Hq=32, Hkv=8, d=128, ctx=32768) with
+    8-bit keys and 4-bit values, block 32 ("TurboQuant From Scratch": the
+    k8v4 setting), the same seeded K/V as the headline; one tq_decode_attn
+    call per step (the CUDA-core split kernel), L2 flushed before each."""
+    B, Hq, Hkv, d, ctx = DEC["B"], DEC["Hq"], DEC["Hkv"], DEC["d"], DEC["ctx"]
+    Lk = tb.make_layout(d, 32, 8, 0, 0, 1)
+    Lv = tb.make_layout(d, 32, 4, 0, 0, 1)
+    K = tb.PackedKV(Lk, (B, Hkv, ctx), device=dev)
+    V = tb.PackedKV(Lv, (B, Hkv, ctx), device=dev)
+    for b in range(B):
+        kb = inputs.gaussian((Hkv, ctx, d), 1000 * 11 + b)
+        vb = inputs.gaussian((Hkv, ctx, d), 1000 * 12 + b)
+        for src, dst, L in ((kb, K, Lk), (vb, V, Lv)):
+            part = tb.tq_quantize_kv(L, torch.from_numpy(src).to(dev))
+            dst.codes[b].copy_(part.codes)
+            dst.scales[b].copy_(part.scales)
+    q = torch.from_numpy(inputs.gaussian((B, Hq, d), 10)).to(dev)
+    ws_bytes, n_split = tb.tq_decode_workspace_bytes(B, Hq, Hkv, d, ctx, 0)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    out = torch.empty_like(q)
+    flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=dev)
+    ms = _time(torch, lambda: tb.tq_decode_attn(K, V, q, ctx=ctx, workspace=ws, out=out, n_split=n_split),
+               flush, steps, warm)
+    nbytes = decode_bytes(B, Hkv, ctx, d, 8, 4, 32, 32)
+    del K, V
+    torch.cuda.empty_cache()
+    return {"workload": "B=8, Hq=32, Hkv=8, d=128, ctx=32768; K 8-bit, V 4-bit, block 32 (k8v4)",
+            "us": round(ms * 1e3, 2), "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1), "bytes_per_step": nbytes}
+
+
 def run_only(args, tb, torch, inputs, dev):
     """One workload on its own (for profiler runs): the same inputs and calls
     as the full run, `--warmup` untimed then `--steps` timed passes, one JSON
@@ -225,6 +256,8 @@ def run_only(args, tb, torch, inputs, dev):
         res.update(bench_blocks(tb, torch, dev, K, args.steps, args.warmup))
     elif args.only == "polar":
         res.update(bench_polar(tb, torch, inputs, dev, args.steps, args.warmup))
+    elif args.only == "decode_k8v4":
+        res.update(bench_k8v4(tb, torch, inputs, dev, args.steps, args.warmup))
     elif args.only == "decode_window":
         L, K, V, q = headline_cache(tb, torch, inputs, dev)
         res.update(bench_window(tb, torch, inputs, dev, K, V, q, args.steps, args.warmup))
@@ -298,6 +331,7 @@ def run_gpu(args, rank, world):
     window = None if args.no_extra else bench_window(tb, torch, inputs, dev, K, V, q, max(3, min(args.steps, 20)), 3)
     polar = None if args.no_extra else bench_polar(tb, torch, inputs, dev, max(3, min(args.steps, 20)), 3)
     blocks = None if args.no_extra else bench_blocks(tb, torch, dev, K, max(3, min(args.steps, 20)), 3)
+    k8v4 = None if args.no_extra else bench_k8v4(tb, torch, inputs, dev, max(3, min(args.steps, 20)), 3)
     extra = {} if args.no_extra else bench_extra(tb, torch, inputs, dev, args)
     if rank == 0:
         line = {
@@ -320,6 +354,7 @@ def run_gpu(args, rank, world):
             "decode_with_fp16_window": window,
             "polar_codec": polar,
             "ggml_blocks": blocks,
+            "decode_k8v4": k8v4,
             "other_workloads": extra,
             "gpu_launches": args.steps * 2,
             "clocks": clocks.summary(),
@@ -713,7 +748,7 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--only", default=None,
                     choices=["decode", "quantize", "prefill", "decode_d256", "decode_qjl", "quantize_qjl", "decode_depth",
-                             "decode_window", "polar", "blocks"],
+                             "decode_window", "polar", "blocks", "decode_k8v4"],
                     help="time one workload alone and print its result only (profiler runs)")
     args = ap.parse_args()
     if args.warmup < 3:

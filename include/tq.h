@@ -59,7 +59,10 @@ typedef enum { TQ_CODEBOOK_GAUSSIAN = 0, TQ_CODEBOOK_BETA = 1 } tq_codebook_kind
  *   head_dim      d in {64, 128, 256}
  *   block         rotation + norm block: a power of two >= 32 dividing d
  *                 (d: one norm per vector; 32: block-32)
- *   bits          MSE bits per coordinate, 1..4
+ *   bits          MSE bits per coordinate, 1..4, or 8 (one byte per code:
+ *                 the 256-level Gaussian codebook, no QJL; the keys of
+ *                 "TurboQuant From Scratch"'s k8v4 setting, Finding 1 and
+ *                 Takeaways)
  *   qjl_m         0 = no QJL residual; else m rows of S, a multiple of 32,
  *                 <= 256, and block must equal head_dim
  *   norm_correct  0/1: store n / ||reconstructed direction|| instead of n,
@@ -92,6 +95,7 @@ typedef struct {
  *              bits=3: bits 0-2 = code(8w+k), bit 3 = bit w of code(24+k)
  *              bits=2: bits 0-1 = code(8w+k), bits 2-3 = code(16+8w+k)
  *              bits=1: bit p = code(8p+k)
+ *            and bits=8: byte i of the record = code(i).
  *            where code(i) = #{k : y_i > beta_k} indexes the ascending
  *            centroids of the Lloyd-Max codebook.
  *   scales:  d/block fp16 values (n, or the norm-corrected value).
@@ -215,7 +219,8 @@ typedef struct {
  * (n_split = 0: chosen by the library).  workspace: device, at least
  * tq_decode_workspace_bytes(...) bytes, 16-byte aligned.  With QJL keys the
  * score adds ||k|| rho sqrt(pi/2)/m <S q, 2s - 1> ("turboquant-pytorch",
- * QJL estimator formula). */
+ * QJL estimator formula).  8-bit keys are read by the CUDA-core kernel;
+ * 8-bit values, and QJL values beside 8-bit keys, are TQ_ERR_UNSUPPORTED. */
 int tq_decode_attn(const tq_kv_view* K, const tq_kv_view* V, const uint16_t* q, int B, int Hq,
                    int Hkv, int64_t S_cap, const int32_t* kv_len, int64_t ctx,
                    float softmax_scale, uint16_t* out, void* workspace, size_t workspace_bytes,
@@ -331,8 +336,8 @@ int tq_decode_window_workspace_bytes(int B, int Hq, int Hkv, int head_dim, int64
  * positions <= ctx-Tq+i (bottom-right aligned).  K/V tiles are decoded into
  * shared memory (rotated domain, scaled) and QK^T / PV run on the tensor
  * cores ("llama.cpp-turboquant", "Prompt processing": the conversion
- * amortises over the query batch).  QJL keys are not supported here
- * (TQ_ERR_UNSUPPORTED).  workspace: device, >= tq_prefill_workspace_bytes. */
+ * amortises over the query batch).  QJL and 8-bit codes are not supported
+ * here (TQ_ERR_UNSUPPORTED).  workspace: device, >= tq_prefill_workspace_bytes. */
 int tq_prefill_attn(const tq_kv_view* K, const tq_kv_view* V, const uint16_t* q, int B, int Hq,
                     int Hkv, int Tq, int64_t S_cap, int64_t ctx, int causal, float softmax_scale,
                     uint16_t* out, void* workspace, size_t workspace_bytes, void* stream);

@@ -86,6 +86,33 @@ def test_qjl_layout_rules(tqlib):
     assert tqlib.tq_layout_sizes(ctypes.byref(tb.make_layout(128, 128, 2, qjl_m=512)), None, None, None) == -2
 
 
+def test_8bit_layout_rules(tqlib):
+    """One byte per code: Gaussian codebook only, no QJL, d code bytes; the
+    decode takes 8-bit keys but not 8-bit values, the prefill neither."""
+    assert tb.tq_layout_sizes(tb.make_layout(128, 32, 8)) == (128, 4, 0)
+    assert tb.tq_layout_sizes(tb.make_layout(64, 64, 8)) == (64, 1, 0)
+    sizes = lambda L: tqlib.tq_layout_sizes(ctypes.byref(L), None, None, None)
+    assert sizes(tb.make_layout(128, 32, 8, codebook=1)) == -2
+    assert sizes(tb.make_layout(128, 128, 8, qjl_m=128)) == -2
+    for bits in (5, 6, 7, 9):
+        assert sizes(tb.make_layout(128, 32, bits)) == -2
+    with pytest.raises(ValueError):
+        O.Layout(128, 32, 8, codebook=1)
+    P16 = ctypes.c_void_p(16)
+    L4, L8 = tb.make_layout(128, 32, 4), tb.make_layout(128, 32, 8)
+    Lq = tb.make_layout(128, 128, 2, qjl_m=128)
+    view = lambda L: tb.tq_kv_view(16, 16, 16, 16, 16, L, None, 0, 0)
+
+    def dec(K, V):
+        return tqlib.tq_decode_attn(ctypes.byref(K), ctypes.byref(V), P16, 1, 4, 1, 128, None, 64, 0.0, P16, P16,
+                                    1 << 20, 0, None)
+
+    assert dec(view(L4), view(L8)) == -2        # 8-bit values
+    assert dec(view(L8), view(Lq)) == -2        # QJL values beside 8-bit keys
+    assert tqlib.tq_prefill_attn(ctypes.byref(view(L8)), ctypes.byref(view(L4)), P16, 1, 4, 1, 16, 128, 64, 1,
+                                 0.0, P16, P16, 1 << 20, None) == -2
+
+
 def test_host_side_argument_checks_need_no_gpu(tqlib):
     L = tb.make_layout(128, 32, 3)
     # zero vectors: nothing to do

@@ -40,6 +40,9 @@ CASES = [
     (64, 64, 1, np.float16, 0, 32),
     (256, 256, 2, np.float16, 0, 256),
     (128, 128, 2, np.float16, 1, 128),   # QJL + norm correction
+    (128, 32, 8, np.float16, 0, 0),      # 8-bit keys (k8v4)
+    (64, 64, 8, np.float32, 0, 0),
+    (256, 256, 8, np.float16, 1, 0),     # 8 bits + norm correction
 ]
 
 
@@ -124,6 +127,7 @@ APPEND_CASES = [
     (128, 128, 2, np.float16, 1, 0),
     (128, 128, 2, np.float16, 0, 128),
     (128, 128, 3, np.float32, 0, 64),
+    (128, 32, 8, np.float16, 0, 0),
 ]
 
 
@@ -225,7 +229,7 @@ def test_beta_codebook_quantize_dequantize(tqlib, d, blk, bits, dt, nc, m):
 
 
 @pytest.mark.parametrize("d,blk,bits,cb", [(128, 128, 3, 1), (256, 128, 4, 1), (128, 32, 3, 0), (64, 64, 2, 0),
-                                           (128, 128, 1, 1)])
+                                           (128, 128, 1, 1), (128, 32, 8, 0)])
 def test_ggml_blocks_match_oracle(tqlib, d, blk, bits, cb):
     """tq_to_blocks / tq_from_blocks against the oracle's block bytes, byte
     for byte, on the library's own quantisation of seeded vectors (the

@@ -35,15 +35,24 @@ struct QuantArgs {
   RowMap map;   // vector -> record
 };
 
-template <int D, bool F32>
-__global__ void __launch_bounds__(kThreads) quantize_kernel(const CodecParams P, const QuantArgs a) {
+// W8: one byte per code (256 levels, table in `cb`); otherwise 1..4 bits
+// with the table in P.
+template <int D, bool F32, bool W8>
+__global__ void __launch_bounds__(kThreads) quantize_kernel(const CodecParams P, const QuantArgs a,
+                                                            const Codebook8Param<W8> cb) {
   constexpr int TPV = D / 8;       // threads per vector
   constexpr int VPW = 32 / TPV;    // vectors per warp
-  __shared__ float s_cent[16];
-  __shared__ float s_bnd[16];
+  constexpr int NC = W8 ? 256 : 16;
+  __shared__ float s_cent[NC];
+  __shared__ float s_bnd[NC];
   __shared__ float s_r[kThreads / 32][VPW][D];        // QJL residual staging
   __shared__ uint32_t s_bits[kThreads / 32][VPW][kMaxQjl / 32];
-  if (threadIdx.x < 16) {
+  if constexpr (W8) {
+    for (int k = threadIdx.x; k < NC; k += kThreads) {
+      s_cent[k] = cb.c[k];
+      s_bnd[k] = cb.b[k];
+    }
+  } else if (threadIdx.x < 16) {
     s_cent[threadIdx.x] = P.centroids[threadIdx.x];
     s_bnd[threadIdx.x] = P.bounds[threadIdx.x];
   }
@@ -100,16 +109,26 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(const CodecParams P,
     // S4: code = #{k : y > beta_k}
     int code[8];
     float c[8];
-    uint32_t nib = 0;
+    uint32_t nib = 0;          // 1..4 bits: code r in bits 4r..4r+3
+    uint32_t byt[2] = {0, 0};  // 8 bits: code r in byte r
 #pragma unroll
     for (int r = 0; r < 8; ++r) {
       const float y = x[r] * inv;
       x[r] = y;
       int k = 0;
-      for (int j = 0; j < K - 1; ++j) k += (y > s_bnd[j]) ? 1 : 0;
+      if constexpr (W8) {
+        // the same count by bisection over the 255 ascending boundaries:
+        // after the step of size s, k = #{j < k + s : y > beta_j} rounded
+        // down to a multiple of s (indices stay <= 254)
+#pragma unroll
+        for (int step = 128; step >= 1; step >>= 1) k += (y > s_bnd[k + step - 1]) ? step : 0;
+        byt[r >> 2] |= (uint32_t)k << (8 * (r & 3));
+      } else {
+        for (int j = 0; j < K - 1; ++j) k += (y > s_bnd[j]) ? 1 : 0;
+        nib |= (uint32_t)k << (4 * r);
+      }
       code[r] = k;
       c[r] = s_cent[k];
-      nib |= (uint32_t)k << (4 * r);
     }
     float scale = n;
     if (P.nc && !P.m) {  // S5: n / ||c|| (the rotation is orthonormal)
@@ -178,8 +197,12 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(const CodecParams P,
     }
     // S7: pack and store
     if (rv >= 0 && (sub % tpb) == 0) a.scales[rv * P.nb + sub / tpb] = f2h(scale);
-    const int gi = sub >> 2, w = sub & 3;
     uint32_t* rec = a.codes + rv * words_per_vec;
+    if constexpr (W8) {   // bytes 8 sub .. 8 sub + 7 of the record
+      if (rv >= 0) *reinterpret_cast<uint2*>(rec + 2 * sub) = make_uint2(byt[0], byt[1]);
+      continue;
+    }
+    const int gi = sub >> 2, w = sub & 3;
     const uint32_t n1 = __shfl_sync(kFull, nib, lane + 1 < 32 ? lane + 1 : lane);
     const uint32_t n2 = __shfl_sync(kFull, nib, lane + 2 < 32 ? lane + 2 : lane);
     const uint32_t n3 = __shfl_sync(kFull, nib, lane | 3);
@@ -210,12 +233,17 @@ struct DequantArgs {
   void* out;
 };
 
-template <int D, bool F32>
-__global__ void __launch_bounds__(kThreads) dequantize_kernel(const CodecParams P, const DequantArgs a) {
+template <int D, bool F32, bool W8>
+__global__ void __launch_bounds__(kThreads) dequantize_kernel(const CodecParams P, const DequantArgs a,
+                                                              const Codebook8Param<W8> cb) {
   constexpr int TPV = D / 8;
   constexpr int VPW = 32 / TPV;
-  __shared__ float s_cent[16];
-  if (threadIdx.x < 16) s_cent[threadIdx.x] = P.centroids[threadIdx.x];
+  __shared__ float s_cent[W8 ? 256 : 16];
+  if constexpr (W8) {
+    for (int k = threadIdx.x; k < 256; k += kThreads) s_cent[k] = cb.c[k];
+  } else if (threadIdx.x < 16) {
+    s_cent[threadIdx.x] = P.centroids[threadIdx.x];
+  }
   __syncthreads();
   const int lane = threadIdx.x & 31;
   const int wid = threadIdx.x >> 5;
@@ -231,10 +259,17 @@ __global__ void __launch_bounds__(kThreads) dequantize_kernel(const CodecParams 
     const int64_t v = base + vs;
     const bool valid = v < a.n_vec;
     float x[8];
-    uint32_t nib = 0;
-    if (valid) nib = load_chunk(a.codes + v * words_per_vec + (sub >> 2) * P.bits, P.bits, sub & 3);
+    if constexpr (W8) {   // bytes 8 sub .. 8 sub + 7 of the record
+      uint2 u = make_uint2(0, 0);
+      if (valid) u = *reinterpret_cast<const uint2*>(a.codes + v * words_per_vec + 2 * sub);
 #pragma unroll
-    for (int r = 0; r < 8; ++r) x[r] = s_cent[(nib >> (4 * r)) & 0xf];
+      for (int r = 0; r < 8; ++r) x[r] = s_cent[((r < 4 ? u.x : u.y) >> (8 * (r & 3))) & 0xff];
+    } else {
+      uint32_t nib = 0;
+      if (valid) nib = load_chunk(a.codes + v * words_per_vec + (sub >> 2) * P.bits, P.bits, sub & 3);
+#pragma unroll
+      for (int r = 0; r < 8; ++r) x[r] = s_cent[(nib >> (4 * r)) & 0xf];
+    }
     wht8(x);
     wht_cross(x, sub, tpb);
 #pragma unroll
@@ -280,19 +315,32 @@ int grid_for(int64_t n_vec, int vpw) {
   return (int)(blocks < cap ? (blocks > 0 ? blocks : 1) : cap);
 }
 
+// cb8: the 256-level table when P.bits == 8, else unused
 template <int D>
-int launch_quantize(const CodecParams& P, const QuantArgs& a, bool f32, cudaStream_t st) {
+int launch_quantize(const CodecParams& P, const QuantArgs& a, bool f32, const Codebook8& cb8, cudaStream_t st) {
   const int g = grid_for(a.n_vec, 32 / (D / 8));
-  if (f32) quantize_kernel<D, true><<<g, kThreads, 0, st>>>(P, a);
-  else quantize_kernel<D, false><<<g, kThreads, 0, st>>>(P, a);
+  const NoCodebook8 none{};
+  if (P.bits == 8) {
+    if (f32) quantize_kernel<D, true, true><<<g, kThreads, 0, st>>>(P, a, cb8);
+    else quantize_kernel<D, false, true><<<g, kThreads, 0, st>>>(P, a, cb8);
+  } else {
+    if (f32) quantize_kernel<D, true, false><<<g, kThreads, 0, st>>>(P, a, none);
+    else quantize_kernel<D, false, false><<<g, kThreads, 0, st>>>(P, a, none);
+  }
   return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }
 
 template <int D>
-int launch_dequantize(const CodecParams& P, const DequantArgs& a, bool f32, cudaStream_t st) {
+int launch_dequantize(const CodecParams& P, const DequantArgs& a, bool f32, const Codebook8& cb8, cudaStream_t st) {
   const int g = grid_for(a.n_vec, 32 / (D / 8));
-  if (f32) dequantize_kernel<D, true><<<g, kThreads, 0, st>>>(P, a);
-  else dequantize_kernel<D, false><<<g, kThreads, 0, st>>>(P, a);
+  const NoCodebook8 none{};
+  if (P.bits == 8) {
+    if (f32) dequantize_kernel<D, true, true><<<g, kThreads, 0, st>>>(P, a, cb8);
+    else dequantize_kernel<D, false, true><<<g, kThreads, 0, st>>>(P, a, cb8);
+  } else {
+    if (f32) dequantize_kernel<D, true, false><<<g, kThreads, 0, st>>>(P, a, none);
+    else dequantize_kernel<D, false, false><<<g, kThreads, 0, st>>>(P, a, none);
+  }
   return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }
 
@@ -319,15 +367,17 @@ int quantize_common(const tq_layout* layout, const void* x, tq_dtype x_dtype, in
   if (P.m && (!aligned16(S) || !aligned16(qjl_bits) || !aligned16(qjl_rnorm))) return TQ_ERR_ALIGN;
   QuantArgs a{x, n_vec, x_row_stride, S, reinterpret_cast<uint32_t*>(codes), scales,
               reinterpret_cast<uint32_t*>(qjl_bits), qjl_rnorm, map};
+  Codebook8 cb8;
+  if (P.bits == 8 && make_codebook8(layout, &cb8) != TQ_OK) return TQ_ERR_UNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool f32 = x_dtype == TQ_F32;
   if (quantize_fast_eligible(P, f32)) return launch_quantize_fast(P, x, n_vec, x_row_stride, codes, scales, map, s);
   if (quantize_qjl_eligible(P))
     return launch_quantize_qjl(P, x, f32, n_vec, x_row_stride, S, codes, scales, qjl_bits, qjl_rnorm, map, s);
   switch (P.d) {
-    case 64: return launch_quantize<64>(P, a, f32, s);
-    case 128: return launch_quantize<128>(P, a, f32, s);
-    default: return launch_quantize<256>(P, a, f32, s);
+    case 64: return launch_quantize<64>(P, a, f32, cb8, s);
+    case 128: return launch_quantize<128>(P, a, f32, cb8, s);
+    default: return launch_quantize<256>(P, a, f32, cb8, s);
   }
 }
 
@@ -371,11 +421,13 @@ extern "C" int tq_dequantize_kv(const tq_layout* layout, const uint8_t* codes, c
   if (!tq::aligned16(codes) || !tq::aligned16(scales) || !tq::aligned16(out)) return TQ_ERR_ALIGN;
   tq::DequantArgs a{reinterpret_cast<const uint32_t*>(codes), scales,
                     reinterpret_cast<const uint32_t*>(qjl_bits), qjl_rnorm, S, n_vec, out};
+  tq::Codebook8 cb8;
+  if (P.bits == 8 && tq::make_codebook8(layout, &cb8) != TQ_OK) return TQ_ERR_UNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool f32 = out_dtype == TQ_F32;
   switch (P.d) {
-    case 64: return tq::launch_dequantize<64>(P, a, f32, s);
-    case 128: return tq::launch_dequantize<128>(P, a, f32, s);
-    default: return tq::launch_dequantize<256>(P, a, f32, s);
+    case 64: return tq::launch_dequantize<64>(P, a, f32, cb8, s);
+    case 128: return tq::launch_dequantize<128>(P, a, f32, cb8, s);
+    default: return tq::launch_dequantize<256>(P, a, f32, cb8, s);
   }
 }

@@ -90,15 +90,17 @@ __device__ void smem_wht(float* a, int rows, int blk, float norm) {
 // lane + 32 k), and its epilogue adds sqrt(pi/2)/m S^T of that, rotated into
 // V's coded domain, to the accumulator: the QJL term of every value, applied
 // once per split instead of once per token.
-template <int D, int G, bool QV>
+// K8: keys of one byte per code, their 256-level table in `cbk`.
+template <int D, int G, bool QV, bool K8>
 __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const CodecParams PK, const CodecParams PV,
-                                                                   const DecodeArgs a) {
+                                                                   const DecodeArgs a,
+                                                                   const Codebook8Param<K8> cbk) {
   constexpr int CPL = D / 32;  // V coordinates per lane
   constexpr int CQ = QV ? kMaxQjlV / 32 : 1;   // QJL rows of V per lane
   __shared__ float s_q[G][D];          // q, then q^ (rotated, scaled)
   __shared__ float s_qT[D][G];         // q^ transposed: coordinate-major
   __shared__ float s_sq[kMaxQjl][G];   // S q (QJL keys)
-  __shared__ float s_centK[16], s_centV[16];
+  __shared__ float s_centK[K8 ? 256 : 16], s_centV[16];
   __shared__ float s_p[kWarps][32][G];
   __shared__ float s_ml[kWarps][2][G];
   __shared__ float s_acc[kWarps][D];   // one head at a time in the final merge
@@ -113,10 +115,12 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const CodecPa
   const int h0 = kvh * G;
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
 
-  if (threadIdx.x < 16) {
+  if constexpr (K8) {
+    for (int k = threadIdx.x; k < 256; k += kDecThreads) s_centK[k] = cbk.c[k];
+  } else if (threadIdx.x < 16) {
     s_centK[threadIdx.x] = PK.centroids[threadIdx.x];
-    s_centV[threadIdx.x] = PV.centroids[threadIdx.x];
   }
+  if (threadIdx.x < 16) s_centV[threadIdx.x] = PV.centroids[threadIdx.x];
   for (int e = threadIdx.x; e < G * D; e += kDecThreads) {
     const int h = e / D, i = e % D;
     s_q[h][i] = h2f(a.q[((int64_t)b * a.Hq + h0 + h) * D + i]);
@@ -180,15 +184,34 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const CodecPa
         for (int gg = 0; gg < gpb; ++gg) {
           const int gi = j * gpb + gg;
           const uint32_t* gw = rec + gi * PK.bits;
+          if constexpr (K8) {
+            // 32 bytes, code i of the group in byte i: two 16-byte loads
 #pragma unroll
-          for (int w = 0; w < 4; ++w) {
-            const uint32_t nib = load_chunk(gw, PK.bits, w);
+            for (int hf = 0; hf < 2; ++hf) {
+              const uint4 u = reinterpret_cast<const uint4*>(gw)[hf];
+              const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-            for (int r = 0; r < 8; ++r) {
-              const float c = s_centK[(nib >> (4 * r)) & 0xf];
-              const int i = gi * 32 + w * 8 + r;
+              for (int w = 0; w < 4; ++w) {
 #pragma unroll
-              for (int h = 0; h < G; ++h) part[h] = fmaf(c, s_qT[i][h], part[h]);
+                for (int r = 0; r < 4; ++r) {
+                  const float c = s_centK[(wv[w] >> (8 * r)) & 0xff];
+                  const int i = gi * 32 + hf * 16 + w * 4 + r;
+#pragma unroll
+                  for (int h = 0; h < G; ++h) part[h] = fmaf(c, s_qT[i][h], part[h]);
+                }
+              }
+            }
+          } else {
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+              const uint32_t nib = load_chunk(gw, PK.bits, w);
+#pragma unroll
+              for (int r = 0; r < 8; ++r) {
+                const float c = s_centK[(nib >> (4 * r)) & 0xf];
+                const int i = gi * 32 + w * 8 + r;
+#pragma unroll
+                for (int h = 0; h < G; ++h) part[h] = fmaf(c, s_qT[i][h], part[h]);
+              }
             }
           }
         }
@@ -669,8 +692,9 @@ __global__ void __launch_bounds__(128) decode_window_kernel(const CodecParams PV
   }
 }
 
-template <int D, int G, bool QV>
-int launch_decode(const CodecParams& PK, const CodecParams& PV, const DecodeArgs& a, int B, cudaStream_t st) {
+template <int D, int G, bool QV, bool K8>
+int launch_decode(const CodecParams& PK, const CodecParams& PV, const DecodeArgs& a, int B,
+                  const Codebook8Param<K8>& cbk, cudaStream_t st) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)a.n_split, (unsigned)(B * a.Hkv));
   cfg.blockDim = dim3(kDecThreads);
@@ -680,19 +704,35 @@ int launch_decode(const CodecParams& PK, const CodecParams& PV, const DecodeArgs
   attr[0].val.programmaticStreamSerializationAllowed = a.pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, decode_split_kernel<D, G, QV>, PK, PV, a) != cudaSuccess) return TQ_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, decode_split_kernel<D, G, QV, K8>, PK, PV, a, cbk) != cudaSuccess) return TQ_ERR_CUDA;
   if (cudaGetLastError() != cudaSuccess) return TQ_ERR_CUDA;
   return TQ_OK;
 }
 
+// cbk: the 256-level key table when PK.bits == 8 (values then without QJL)
 template <int D>
 int launch_decode_g(int G, const CodecParams& PK, const CodecParams& PV, const DecodeArgs& a, int B,
-                    cudaStream_t st) {
+                    const Codebook8& cbk, cudaStream_t st) {
+  const NoCodebook8 none{};
+  if (PK.bits == 8) {
+    if (PV.m) return TQ_ERR_UNSUPPORTED;
+    switch (G) {
+      case 1: return launch_decode<D, 1, false, true>(PK, PV, a, B, cbk, st);
+      case 2: return launch_decode<D, 2, false, true>(PK, PV, a, B, cbk, st);
+      case 4: return launch_decode<D, 4, false, true>(PK, PV, a, B, cbk, st);
+      case 8: return launch_decode<D, 8, false, true>(PK, PV, a, B, cbk, st);
+      default: return TQ_ERR_UNSUPPORTED;
+    }
+  }
   switch (G) {
-    case 1: return PV.m ? launch_decode<D, 1, true>(PK, PV, a, B, st) : launch_decode<D, 1, false>(PK, PV, a, B, st);
-    case 2: return PV.m ? launch_decode<D, 2, true>(PK, PV, a, B, st) : launch_decode<D, 2, false>(PK, PV, a, B, st);
-    case 4: return PV.m ? launch_decode<D, 4, true>(PK, PV, a, B, st) : launch_decode<D, 4, false>(PK, PV, a, B, st);
-    case 8: return PV.m ? launch_decode<D, 8, true>(PK, PV, a, B, st) : launch_decode<D, 8, false>(PK, PV, a, B, st);
+    case 1: return PV.m ? launch_decode<D, 1, true, false>(PK, PV, a, B, none, st)
+                        : launch_decode<D, 1, false, false>(PK, PV, a, B, none, st);
+    case 2: return PV.m ? launch_decode<D, 2, true, false>(PK, PV, a, B, none, st)
+                        : launch_decode<D, 2, false, false>(PK, PV, a, B, none, st);
+    case 4: return PV.m ? launch_decode<D, 4, true, false>(PK, PV, a, B, none, st)
+                        : launch_decode<D, 4, false, false>(PK, PV, a, B, none, st);
+    case 8: return PV.m ? launch_decode<D, 8, true, false>(PK, PV, a, B, none, st)
+                        : launch_decode<D, 8, false, false>(PK, PV, a, B, none, st);
     default: return TQ_ERR_UNSUPPORTED;
   }
 }
@@ -789,6 +829,11 @@ int decode_impl(const tq_kv_view* K, const tq_kv_view* V, const uint16_t* q, int
   st = make_params(&V->layout, &PV);
   if (st != TQ_OK) return st;
   if (PK.d != PV.d || PV.m > kMaxQjlV) return TQ_ERR_UNSUPPORTED;
+  // 8-bit codes: keys only (the value path reads 1..4-bit codes), no QJL
+  // on the values beside them
+  if (PV.bits > 4 || (PK.bits > 4 && PV.m)) return TQ_ERR_UNSUPPORTED;
+  Codebook8 cbk;
+  if (PK.bits == 8 && make_codebook8(&K->layout, &cbk) != TQ_OK) return TQ_ERR_UNSUPPORTED;
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || ctx < 0 || ctx > S_cap || n_split < 0) return TQ_ERR_ARG;
   if (!K->codes || !K->scales || !V->codes || !V->scales) return TQ_ERR_ARG;
   if (PK.m && (!K->qjl_bits || !K->qjl_rnorm || !K->S)) return TQ_ERR_ARG;
@@ -839,9 +884,9 @@ int decode_impl(const tq_kv_view* K, const tq_kv_view* V, const uint16_t* q, int
                           ctx, ns, slots, a.pdl != 0, a.qscale, s);
   } else {
     switch (PK.d) {
-      case 64: st = launch_decode_g<64>(G, PK, PV, a, B, s); break;
-      case 128: st = launch_decode_g<128>(G, PK, PV, a, B, s); break;
-      default: st = launch_decode_g<256>(G, PK, PV, a, B, s); break;
+      case 64: st = launch_decode_g<64>(G, PK, PV, a, B, cbk, s); break;
+      case 128: st = launch_decode_g<128>(G, PK, PV, a, B, cbk, s); break;
+      default: st = launch_decode_g<256>(G, PK, PV, a, B, cbk, s); break;
     }
   }
   if (st != TQ_OK) return st;

@@ -272,7 +272,9 @@ int check_layout(const tq_layout* L) {
   if (L->codebook != TQ_CODEBOOK_GAUSSIAN && L->codebook != TQ_CODEBOOK_BETA) return TQ_ERR_ARG;
   if (L->head_dim != 64 && L->head_dim != 128 && L->head_dim != 256) return TQ_ERR_UNSUPPORTED;
   if (!pow2(L->block) || L->block < 32 || L->head_dim % L->block) return TQ_ERR_UNSUPPORTED;
-  if (L->bits < 1 || L->bits > 4) return TQ_ERR_UNSUPPORTED;
+  // 1..4 bits, or one byte per code (Gaussian codebook, no QJL)
+  if (!((L->bits >= 1 && L->bits <= 4) || L->bits == 8)) return TQ_ERR_UNSUPPORTED;
+  if (L->bits == 8 && (L->codebook != TQ_CODEBOOK_GAUSSIAN || L->qjl_m)) return TQ_ERR_UNSUPPORTED;
   if (L->norm_correct != 0 && L->norm_correct != 1) return TQ_ERR_ARG;
   if (L->qjl_m < 0) return TQ_ERR_ARG;
   if (L->qjl_m > 0 && (L->qjl_m % 32 || L->qjl_m > kMaxQjl || L->block != L->head_dim))
@@ -296,11 +298,24 @@ int make_params(const tq_layout* L, CodecParams* p) {
   uint64_t state = L->sign_seed;
   for (int i = 0; i < L->head_dim; ++i)
     if (splitmix64_next(state) >> 63) p->sign_bits[i >> 5] |= 1u << (i & 31);
+  if (L->bits > 4) return TQ_OK;   // 8-bit tables: make_codebook8
   double c[16], b[16];
   tq_codebook_kind(L->bits, L->block, L->codebook, c, b);
   const int K = 1 << L->bits;
   for (int k = 0; k < K; ++k) p->centroids[k] = static_cast<float>(c[k]);
   for (int k = 0; k + 1 < K; ++k) p->bounds[k] = static_cast<float>(b[k]);
+  return TQ_OK;
+}
+
+int make_codebook8(const tq_layout* L, Codebook8* cb) {
+  const int st = check_layout(L);
+  if (st != TQ_OK) return st;
+  if (L->bits != 8) return TQ_ERR_ARG;
+  double c[256], b[256];
+  tq_codebook_kind(8, L->block, L->codebook, c, b);
+  for (int k = 0; k < 256; ++k) cb->c[k] = static_cast<float>(c[k]);
+  for (int k = 0; k < 255; ++k) cb->b[k] = static_cast<float>(b[k]);
+  cb->b[255] = INFINITY;   // never compared: 255 boundaries
   return TQ_OK;
 }
 

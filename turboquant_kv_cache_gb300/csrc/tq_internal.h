@@ -5,6 +5,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 #include "tq.h"
 
 namespace tq {
@@ -30,8 +32,22 @@ struct CodecParams {
   float bounds[16];                   // 2^bits - 1 used
 };
 
-// Fills `p` from a public layout; returns TQ_OK or a tq_status.
+// Fills `p` from a public layout; returns TQ_OK or a tq_status.  For 8-bit
+// codes the centroid and boundary arrays stay empty: see Codebook8.
 int make_params(const tq_layout* layout, CodecParams* p);
+
+// The 256-level codebook of an 8-bit layout.  Too large for CodecParams
+// (which every kernel takes), so only the kernels that read 8-bit codes
+// take it, as a separate by-value parameter.
+struct Codebook8 {
+  float c[256];   // centroids, ascending
+  float b[256];   // 255 midpoints, then +inf
+};
+struct NoCodebook8 {};
+template <bool W8>
+using Codebook8Param = typename std::conditional<W8, Codebook8, NoCodebook8>::type;
+
+int make_codebook8(const tq_layout* layout, Codebook8* cb);
 
 // Validates a public layout without building tables.
 int check_layout(const tq_layout* layout);

@@ -29,7 +29,7 @@ extern "C" int tq_prefill_attn(const tq_kv_view* K, const tq_kv_view* V, const u
   if (st != TQ_OK) return st;
   st = tq::make_params(&V->layout, &PV);
   if (st != TQ_OK) return st;
-  if (PK.d != PV.d || PK.m || PV.m) return TQ_ERR_UNSUPPORTED;
+  if (PK.d != PV.d || PK.m || PV.m || PK.bits > 4 || PV.bits > 4) return TQ_ERR_UNSUPPORTED;
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || Tq < 0 || ctx < Tq || ctx > S_cap) return TQ_ERR_ARG;
   if (!K->codes || !K->scales || !V->codes || !V->scales) return TQ_ERR_ARG;
   if (tq::check_paging(K, S_cap) != TQ_OK || !tq::same_paging(K, V)) return TQ_ERR_ARG;

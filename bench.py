@@ -254,6 +254,9 @@ def run_only(args, tb, torch, inputs, dev):
     elif args.only == "blocks":
         L, K, V, q = headline_cache(tb, torch, inputs, dev)
         res.update(bench_blocks(tb, torch, dev, K, args.steps, args.warmup))
+    elif args.only == "decode_blocks":
+        L, K, V, q = headline_cache(tb, torch, inputs, dev)
+        res.update(bench_decode_blocks(tb, torch, dev, K, V, q, args.steps, args.warmup))
     elif args.only == "polar":
         res.update(bench_polar(tb, torch, inputs, dev, args.steps, args.warmup))
     elif args.only == "decode_k8v4":
@@ -331,6 +334,7 @@ def run_gpu(args, rank, world):
     window = None if args.no_extra else bench_window(tb, torch, inputs, dev, K, V, q, max(3, min(args.steps, 20)), 3)
     polar = None if args.no_extra else bench_polar(tb, torch, inputs, dev, max(3, min(args.steps, 20)), 3)
     blocks = None if args.no_extra else bench_blocks(tb, torch, dev, K, max(3, min(args.steps, 20)), 3)
+    dblocks = None if args.no_extra else bench_decode_blocks(tb, torch, dev, K, V, q, max(3, min(args.steps, 20)), 3)
     k8v4 = None if args.no_extra else bench_k8v4(tb, torch, inputs, dev, max(3, min(args.steps, 20)), 3)
     extra = {} if args.no_extra else bench_extra(tb, torch, inputs, dev, args)
     if rank == 0:
@@ -355,6 +359,7 @@ def run_gpu(args, rank, world):
             "polar_codec": polar,
             "ggml_blocks": blocks,
             "decode_k8v4": k8v4,
+            "decode_over_blocks": dblocks,
             "other_workloads": extra,
             "gpu_launches": args.steps * 2,
             "clocks": clocks.summary(),
@@ -480,6 +485,27 @@ def bench_blocks(tb, torch, dev, K, steps, warm):
         res[name] = {"ms": round(ms, 4), "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak,
                                                       "unit": "GB/s", "frac": round(gbs / peak, 4)}}
     return res
+
+
+def bench_decode_blocks(tb, torch, dev, K, V, q, steps, warm):
+    """The headline decode read straight from the block form of its K and V
+    caches (14-byte turbo3 blocks, tq_decode_attn_blocks), L2 flushed before
+    each call; the packed-layout call is timed beside it."""
+    B, Hq, Hkv, d, ctx = DEC["B"], DEC["Hq"], DEC["Hkv"], DEC["d"], DEC["ctx"]
+    flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=dev)
+    kb, vb = tb.tq_to_blocks(K), tb.tq_to_blocks(V)
+    ws_bytes, n_split = tb.tq_decode_workspace_bytes(B, Hq, Hkv, d, ctx, 0)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    out = torch.empty_like(q)
+    ms = _time(torch, lambda: tb.tq_decode_attn_blocks(K.layout, kb, V.layout, vb, q, ctx=ctx, workspace=ws,
+                                                       out=out, n_split=n_split), flush, steps, warm)
+    ms_packed = _time(torch, lambda: tb.tq_decode_attn(K, V, q, ctx=ctx, workspace=ws, out=out, n_split=n_split),
+                      flush, steps, warm)
+    nbytes = kb.numel() + vb.numel()
+    del kb, vb
+    return {"workload": "the headline decode (B=8, Hq=32, Hkv=8, d=128, ctx=32768, turbo3) over 14-byte blocks",
+            "us": round(ms * 1e3, 2), "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1), "bytes_per_step": nbytes,
+            "packed_layout_us": round(ms_packed * 1e3, 2)}
 
 
 def bench_polar(tb, torch, inputs, dev, steps, warm):
@@ -748,7 +774,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--only", default=None,
                     choices=["decode", "quantize", "prefill", "decode_d256", "decode_qjl", "quantize_qjl", "decode_depth",
-                             "decode_window", "polar", "blocks", "decode_k8v4"],
+                             "decode_window", "polar", "blocks", "decode_k8v4",
+                             "decode_blocks"],
                     help="time one workload alone and print its result only (profiler runs)")
     args = ap.parse_args()
     if args.warmup < 3:

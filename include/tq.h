@@ -301,6 +301,24 @@ int tq_to_blocks(const tq_layout* layout, const uint8_t* codes, const uint16_t* 
 int tq_from_blocks(const tq_layout* layout, const uint8_t* blocks, int64_t n_vec, uint8_t* codes,
                    uint16_t* scales, void* stream);
 
+/* Decode attention read straight from caches in the block form above, with
+ * no conversion of the cache ("llama.cpp-turboquant", "Token generation
+ * degrades with context depth" and "Fused tile path": a bulk conversion
+ * costs O(context) per generated token; decoding the blocks inside the
+ * attention kernel avoids it).  Same arguments, results and workspace
+ * (tq_decode_workspace_bytes) as tq_decode_attn, with each cache given as
+ * its layout and its blocks:
+ *   k_blocks, v_blocks  device [B, Hkv, S_cap, head_dim/32, 2 + 4*bits]
+ *                       bytes (tq_to_blocks of a contiguous cache),
+ *                       2-byte aligned, else TQ_ERR_ALIGN
+ *   q, out, workspace   16-byte aligned, as for tq_decode_attn
+ * Runs the CUDA-core split kernel for every group size 1, 2, 4, 8.  Layouts
+ * with QJL or 8-bit codes, and other group sizes, are TQ_ERR_UNSUPPORTED. */
+int tq_decode_attn_blocks(const tq_layout* k_layout, const uint8_t* k_blocks, const tq_layout* v_layout,
+                          const uint8_t* v_blocks, const uint16_t* q, int B, int Hq, int Hkv, int64_t S_cap,
+                          const int32_t* kv_len, int64_t ctx, float softmax_scale, uint16_t* out,
+                          void* workspace, size_t workspace_bytes, int n_split, void* stream);
+
 /* Recursive polar-angle quantizer ("TurboQuant: 3-Bit Compression with Zero
  * Overhead", Part 1: the recursive polar transformation and its quantisation
  * step), a codec of its own beside the rotation + Lloyd-Max one.  A vector

@@ -210,6 +210,25 @@ def test_block_conversion_checks_need_no_gpu(tqlib):
     assert tqlib.tq_from_blocks(ctypes.byref(L), P16, -1, P16, P16, None) == -1
 
 
+def test_block_decode_checks_need_no_gpu(tqlib):
+    L = tb.make_layout(128, 128, 3, codebook=1)
+    Lq = tb.make_layout(128, 128, 2, qjl_m=128)
+    L8 = tb.make_layout(128, 32, 8)
+    P16 = ctypes.c_void_p(16)
+
+    def dec(Lk, kb, Lv, Hq=4, Hkv=1, ws=P16, ws_bytes=1 << 20):
+        return tqlib.tq_decode_attn_blocks(ctypes.byref(Lk), kb, ctypes.byref(Lv), P16, P16, 1, Hq, Hkv, 128, None,
+                                           64, 0.0, P16, ws, ws_bytes, 0, None)
+
+    assert dec(Lq, P16, L) == -2          # blocks carry no QJL data
+    assert dec(L, P16, L8) == -2          # 8-bit codes: packed layout only
+    assert dec(L, P16, L, Hq=6, Hkv=2) == -2   # group of 3
+    assert dec(L, None, L) == -1
+    assert dec(L, ctypes.c_void_p(17), L) == -3   # blocks are 2-byte aligned
+    assert dec(L, P16, L, ws=None) == -4
+    assert dec(L, P16, L, ws_bytes=64) == -4
+
+
 def test_polar_checks_need_no_gpu(tqlib):
     cb = ctypes.c_int64()
     assert tqlib.tq_polar_code_bytes(128, 3, ctypes.byref(cb)) == 0 and cb.value == 48

@@ -328,3 +328,47 @@ def test_decode_qjl_values(tqlib, name, cK, cV, B, Hq, Hkv, S_cap, ctx, kv_len, 
     ref = O.decode_attention(q, kd, vd, kv_len if kv_len is not None else [ctx] * B)
     err = np.abs(to_np(out.float()) - ref).max()
     assert err < ATTN_ATOL, (name, err)
+
+
+BLOCK_CASES = [
+    # name, K (block, bits, m, nc, seed[, codebook]), V (...), B, Hq, Hkv, S_cap, ctx, kv_len, d
+    # the llama.cpp arrangement: 128-value chunks, Beta codebook of a chunk, 14/18-byte blocks
+    ("llama_turbo3_d128_gqa4", (128, 3, 0, 0, 1, 1), (128, 3, 0, 0, 2, 1), 2, 8, 2, 300, 290, None, 128),
+    ("llama_turbo4_d256_halves_gqa8", (128, 4, 0, 0, 3, 1), (128, 4, 0, 0, 4, 1), 1, 8, 1, 150, 150, None, 256),
+    ("b32_turbo4k_turbo3v_d256_gqa2", (32, 4, 0, 0, 1), (32, 3, 0, 0, 2), 1, 4, 2, 200, 199, None, 256),
+    ("b64_2bit_nc_k_1bit_v_d64_mha", (64, 2, 0, 1, 5), (32, 1, 0, 0, 6), 2, 2, 2, 100, 97, [97, 0], 64),
+]
+
+
+@pytest.mark.parametrize("name,cK,cV,B,Hq,Hkv,S_cap,ctx,kv_len,d", BLOCK_CASES)
+@pytest.mark.parametrize("n_split", [0, 3])
+def test_decode_over_blocks(tqlib, name, cK, cV, B, Hq, Hkv, S_cap, ctx, kv_len, d, n_split):
+    """tq_decode_attn_blocks reads the oracle's own block bytes (its
+    quantisation, its to_blocks): the result matches the oracle's attention
+    over its dequantised cache, and the packed-layout decode of the same codes."""
+    from turboquant_kv_cache_gb300 import binding as tb
+    Lk, Lv = O.Layout(d, *cK), O.Layout(d, *cV)
+    k = inputs.gaussian((B, Hkv, S_cap, d), 31)
+    v = inputs.gaussian((B, Hkv, S_cap, d), 32)
+    q = inputs.gaussian((B, Hq, d), 33)
+    (kc, ks, _, _), kd = _encode_cache(k, Lk)
+    (vc, vs, _, _), vd = _encode_cache(v, Lv)
+    kb = O.to_blocks(kc, ks, Lk).reshape(B, Hkv, S_cap, d // 32, 2 + 4 * Lk.bits)
+    vb = O.to_blocks(vc, vs, Lv).reshape(B, Hkv, S_cap, d // 32, 2 + 4 * Lv.bits)
+    tLk, tLv = tb.make_layout(d, *cK), tb.make_layout(d, *cV)
+    kvl = torch.tensor(kv_len, dtype=torch.int32, device="cuda") if kv_len is not None else None
+    qg = torch.from_numpy(q).cuda()
+    got = tb.tq_decode_attn_blocks(tLk, torch.from_numpy(kb).cuda(), tLv, torch.from_numpy(vb).cuda(), qg,
+                                   ctx=ctx, kv_len=kvl, n_split=n_split)
+    K = upload_packed(tb, tLk, Lk, kc, ks, None, None, (B, Hkv, S_cap))
+    V = upload_packed(tb, tLv, Lv, vc, vs, None, None, (B, Hkv, S_cap))
+    packed = tb.tq_decode_attn(K, V, qg, ctx=ctx, kv_len=kvl, n_split=n_split)
+    torch.cuda.synchronize()
+    lens = kv_len if kv_len is not None else [ctx] * B
+    ref = O.decode_attention(q, kd, vd, lens)
+    got = to_np(got.float())
+    assert np.abs(got - ref).max() < ATTN_ATOL, (name, np.abs(got - ref).max())
+    assert np.abs(got - to_np(packed.float())).max() <= 1e-3
+    for b, n in enumerate(lens):
+        if n == 0:
+            assert np.all(got[b] == 0)

@@ -61,6 +61,7 @@ def _load():
         "tq_polar_code_bytes": (I, [I, I, P]),
         "tq_to_blocks": (I, [P, P, P, I64, P, P]),
         "tq_from_blocks": (I, [P, P, I64, P, P, P]),
+        "tq_decode_attn_blocks": (I, [P, P, P, P, P, I, I, I, I64, P, I64, ctypes.c_float, P, P, SZ, I, P]),
         "tq_polar_quantize": (I, [P, I, I64, I, I64, I, P, P, P]),
         "tq_polar_dequantize": (I, [P, P, I64, I, I, P, I, P]),
         "tq_decode_attn_static": (I, [P, P, P, I, I, I, I64, P, I64, ctypes.c_float, P, I, P]),
@@ -382,6 +383,34 @@ def tq_to_blocks(pk, stream=None):
     out = torch.empty(tuple(pk.lead_shape) + (L.head_dim // 32, bb), dtype=torch.uint8, device=pk.codes.device)
     _check(lib.tq_to_blocks(ctypes.byref(L), _ptr(pk.codes), _ptr(pk.scales), n, _ptr(out), _stream(stream)),
            "tq_to_blocks")
+    return out
+
+
+def tq_decode_attn_blocks(Lk, k_blocks, Lv, v_blocks, q, ctx=None, kv_len=None, softmax_scale=0.0, n_split=0,
+                          workspace=None, out=None, stream=None):
+    """Decode attention read straight from block-form caches: q [B, Hq, d]
+    fp16; k_blocks / v_blocks uint8 [B, Hkv, S_cap, d/32, 2 + 4 bits] (as
+    tq_to_blocks gives for a contiguous cache) of layouts Lk / Lv."""
+    lib = _load()
+    B, Hq, d = q.shape
+    for blk, L in ((k_blocks, Lk), (v_blocks, Lv)):
+        if blk.dim() != 5 or blk.dtype != torch.uint8 or tuple(blk.shape[3:]) != (L.head_dim // 32, 2 + 4 * L.bits):
+            raise ValueError("blocks must be uint8 [B, Hkv, S_cap, head_dim/32, 2 + 4 bits]")
+        if not blk.is_contiguous():
+            raise ValueError("blocks must be contiguous")
+    if tuple(k_blocks.shape[:3]) != tuple(v_blocks.shape[:3]) or k_blocks.shape[0] != B:
+        raise ValueError("K and V blocks must share [B, Hkv, S_cap] with q's batch")
+    Hkv, S_cap = k_blocks.shape[1], k_blocks.shape[2]
+    ctx = S_cap if ctx is None else ctx
+    need, ns = tq_decode_workspace_bytes(B, Hq, Hkv, d, ctx, n_split)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    st = lib.tq_decode_attn_blocks(ctypes.byref(Lk), _ptr(k_blocks), ctypes.byref(Lv), _ptr(v_blocks), _ptr(q), B,
+                                   Hq, Hkv, S_cap, _ptr(kv_len), ctx, float(softmax_scale), _ptr(out),
+                                   _ptr(workspace), workspace.numel(), n_split, _stream(stream))
+    _check(st, "tq_decode_attn_blocks")
     return out
 
 

@@ -52,7 +52,19 @@ struct DecodeArgs {
   int slots;            // split slots per row (n_split, or more for extra partials)
   float qscale;         // softmax_scale * log2(e)
   int pdl;              // launched as a programmatic dependent of the kernel before it
+  // block layout (AOS kernels only): per token d/32 blocks of [fp16 norm of
+  // the rotation block, 4*bits code bytes], read as 16-bit units
+  const uint16_t* kblk = nullptr;
+  const uint16_t* vblk = nullptr;
 };
+
+// The packed words of one 32-code group stored inside a block record
+// (2-byte aligned): g16 points at the block's first code byte.
+__device__ __forceinline__ void block_group_words(const uint16_t* g16, int bits, uint32_t gw[4]) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    gw[k] = k < bits ? (uint32_t)g16[2 * k] | ((uint32_t)g16[2 * k + 1] << 16) : 0u;
+}
 
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
@@ -91,7 +103,9 @@ __device__ void smem_wht(float* a, int rows, int blk, float norm) {
 // V's coded domain, to the accumulator: the QJL term of every value, applied
 // once per split instead of once per token.
 // K8: keys of one byte per code, their 256-level table in `cbk`.
-template <int D, int G, bool QV, bool K8>
+// AOS: K and V read from the block layout (a.kblk, a.vblk) instead of the
+// separate code and norm arrays (no QJL, no 8-bit codes, contiguous cache).
+template <int D, int G, bool QV, bool K8, bool AOS = false>
 __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const CodecParams PK, const CodecParams PV,
                                                                    const DecodeArgs a,
                                                                    const Codebook8Param<K8> cbk) {
@@ -172,7 +186,35 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const CodecPa
     float s[G];
 #pragma unroll
     for (int h = 0; h < G; ++h) s[h] = 0.f;
-    if (valid) {
+    if (valid && AOS) {
+      const int kb16 = 1 + 2 * PK.bits;   // 16-bit units per 32-value block
+      const uint16_t* tr = a.kblk + rec_of(t) * (int64_t)(D / 32) * kb16;
+      const int gpb = PK.blk / 32;
+      for (int j = 0; j < PK.nb; ++j) {
+        float part[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) part[h] = 0.f;
+        for (int gg = 0; gg < gpb; ++gg) {
+          const int gi = j * gpb + gg;
+          uint32_t gw[4];
+          block_group_words(tr + gi * kb16 + 1, PK.bits, gw);
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            const uint32_t nib = load_chunk(gw, PK.bits, w);
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+              const float c = s_centK[(nib >> (4 * r)) & 0xf];
+              const int i = gi * 32 + w * 8 + r;
+#pragma unroll
+              for (int h = 0; h < G; ++h) part[h] = fmaf(c, s_qT[i][h], part[h]);
+            }
+          }
+        }
+        const float scj = h2f(tr[j * gpb * kb16]);   // the norm heads each block of the rotation block
+#pragma unroll
+        for (int h = 0; h < G; ++h) s[h] = fmaf(scj, part[h], s[h]);
+      }
+    } else if (valid) {
       const int64_t rt = rec_of(t);
       const uint32_t* rec = a.kc + rt * kwords;
       const uint16_t* sc = a.ks + rt * PK.nb;
@@ -257,6 +299,22 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const CodecPa
     __syncwarp();
     const int n_tok = (int)imin64(32, t_end - c0);
     for (int tt = 0; tt < n_tok; ++tt) {
+      if constexpr (AOS) {
+        const int vb16 = 1 + 2 * PV.bits;
+        const uint16_t* tr = a.vblk + rec_of(c0 + tt) * (int64_t)(D / 32) * vb16;
+#pragma unroll
+        for (int k = 0; k < CPL; ++k) {
+          // coordinate lane + 32 k: group k, position lane
+          const uint16_t* g16 = tr + k * vb16 + 1;
+          const auto word = [g16](int j) { return (uint32_t)g16[2 * j] | ((uint32_t)g16[2 * j + 1] << 16); };
+          const int code = (load_chunk_by(word, PV.bits, lane >> 3) >> (4 * (lane & 7))) & 0xf;
+          const int i = lane + 32 * k;
+          const float v = s_centV[code] * h2f(tr[(i / PV.blk) * (PV.blk / 32) * vb16]);
+#pragma unroll
+          for (int h = 0; h < G; ++h) acc[h][k] = fmaf(s_p[wid][tt][h], v, acc[h][k]);
+        }
+        continue;
+      }
       const int64_t r = rec_of(c0 + tt);
       const uint32_t* rec = a.vc + r * vwords;
       const uint16_t* sc = a.vs + r * PV.nb;
@@ -737,6 +795,22 @@ int launch_decode_g(int G, const CodecParams& PK, const CodecParams& PV, const D
   }
 }
 
+// The split kernel over the block layout (no QJL, no 8-bit codes).
+template <int D>
+int launch_decode_blocks(int G, const CodecParams& PK, const CodecParams& PV, const DecodeArgs& a, int B,
+                         cudaStream_t st) {
+  const dim3 grid((unsigned)a.n_split, (unsigned)(B * a.Hkv));
+  const NoCodebook8 none{};
+  switch (G) {
+    case 1: decode_split_kernel<D, 1, false, false, true><<<grid, kDecThreads, 0, st>>>(PK, PV, a, none); break;
+    case 2: decode_split_kernel<D, 2, false, false, true><<<grid, kDecThreads, 0, st>>>(PK, PV, a, none); break;
+    case 4: decode_split_kernel<D, 4, false, false, true><<<grid, kDecThreads, 0, st>>>(PK, PV, a, none); break;
+    case 8: decode_split_kernel<D, 8, false, false, true><<<grid, kDecThreads, 0, st>>>(PK, PV, a, none); break;
+    default: return TQ_ERR_UNSUPPORTED;
+  }
+  return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+}
+
 }  // namespace
 
 int decode_combine(const CodecParams& PV, const float* part, int n_split, uint16_t* out, int rows, cudaStream_t s) {
@@ -895,6 +969,69 @@ int decode_impl(const tq_kv_view* K, const tq_kv_view* V, const uint16_t* q, int
 
 }  // namespace
 }  // namespace tq
+
+namespace tq {
+namespace {
+
+int decode_blocks_impl(const tq_layout* Lk, const uint8_t* k_blocks, const tq_layout* Lv, const uint8_t* v_blocks,
+                       const uint16_t* q, int B, int Hq, int Hkv, int64_t S_cap, const int32_t* kv_len, int64_t ctx,
+                       float softmax_scale, uint16_t* out, void* workspace, size_t workspace_bytes, int n_split,
+                       void* stream) {
+  if (!Lk || !Lv || !q || !out) return TQ_ERR_ARG;
+  CodecParams PK, PV;
+  int st = make_params(Lk, &PK);
+  if (st != TQ_OK) return st;
+  st = make_params(Lv, &PV);
+  if (st != TQ_OK) return st;
+  // the block form has no QJL data; 8-bit codes are read by the packed path only
+  if (PK.d != PV.d || PK.m || PV.m || PK.bits > 4 || PV.bits > 4) return TQ_ERR_UNSUPPORTED;
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || ctx < 0 || ctx > S_cap || n_split < 0) return TQ_ERR_ARG;
+  if (Hq / Hkv != 1 && Hq / Hkv != 2 && Hq / Hkv != 4 && Hq / Hkv != 8) return TQ_ERR_UNSUPPORTED;
+  if (!k_blocks || !v_blocks) return TQ_ERR_ARG;
+  if ((reinterpret_cast<uintptr_t>(k_blocks) & 1) || (reinterpret_cast<uintptr_t>(v_blocks) & 1) ||
+      !aligned16(q) || !aligned16(out))
+    return TQ_ERR_ALIGN;
+  const int ns = n_split ? n_split : decode_auto_splits(B, Hkv, ctx);
+  const size_t need = decode_ws_bytes(B, Hq, PK.d, ns);
+  if (!workspace || workspace_bytes < need) return TQ_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return TQ_ERR_ALIGN;
+  const float sm = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)PK.d);
+  DecodeArgs a{};
+  a.q = q;
+  a.kv_len = kv_len;
+  a.part = static_cast<float*>(workspace);
+  a.pages = {nullptr, 0, 0};
+  a.S_cap = S_cap;
+  a.ctx = ctx;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.n_split = ns;
+  a.slots = ns;
+  a.qscale = sm * kLog2e;
+  a.kblk = reinterpret_cast<const uint16_t*>(k_blocks);
+  a.vblk = reinterpret_cast<const uint16_t*>(v_blocks);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int G = Hq / Hkv;
+  switch (PK.d) {
+    case 64: st = launch_decode_blocks<64>(G, PK, PV, a, B, s); break;
+    case 128: st = launch_decode_blocks<128>(G, PK, PV, a, B, s); break;
+    default: st = launch_decode_blocks<256>(G, PK, PV, a, B, s); break;
+  }
+  if (st != TQ_OK) return st;
+  return decode_combine(PV, a.part, ns, out, B * Hq, s);
+}
+
+}  // namespace
+}  // namespace tq
+
+extern "C" int tq_decode_attn_blocks(const tq_layout* k_layout, const uint8_t* k_blocks, const tq_layout* v_layout,
+                                     const uint8_t* v_blocks, const uint16_t* q, int B, int Hq, int Hkv,
+                                     int64_t S_cap, const int32_t* kv_len, int64_t ctx, float softmax_scale,
+                                     uint16_t* out, void* workspace, size_t workspace_bytes, int n_split,
+                                     void* stream) {
+  return tq::decode_blocks_impl(k_layout, k_blocks, v_layout, v_blocks, q, B, Hq, Hkv, S_cap, kv_len, ctx,
+                                softmax_scale, out, workspace, workspace_bytes, n_split, stream);
+}
 
 extern "C" int tq_decode_attn(const tq_kv_view* K, const tq_kv_view* V, const uint16_t* q, int B, int Hq,
                               int Hkv, int64_t S_cap, const int32_t* kv_len, int64_t ctx, float softmax_scale,

@@ -92,6 +92,22 @@ __device__ __forceinline__ uint32_t load_chunk(const uint32_t* g, int bits, int 
   }
 }
 
+// load_chunk over a group whose k-th packed word is word(k) (for groups
+// that are not 4-byte aligned, e.g. inside a block record).
+template <class Word>
+__device__ __forceinline__ uint32_t load_chunk_by(Word word, int bits, int w) {
+  switch (bits) {
+    case 4: return word(w);
+    case 3:
+      if (w < 3) return word(w) & 0x77777777u;
+      return ((word(0) >> 3) & 0x11111111u) | ((word(1) >> 2) & 0x22222222u) | ((word(2) >> 1) & 0x44444444u);
+    case 2:
+      return w < 2 ? (word(w) & 0x33333333u) : ((word(w - 2) >> 2) & 0x33333333u);
+    default:
+      return (word(0) >> w) & 0x11111111u;
+  }
+}
+
 // Code of coordinate i (0..d-1) of one packed vector record.
 __device__ __forceinline__ int code_at(const uint32_t* rec, int bits, int i) {
   const uint32_t* g = rec + (i >> 5) * bits;

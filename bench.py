@@ -269,6 +269,24 @@ def run_only(args, tb, torch, inputs, dev):
     print(json.dumps(res), flush=True)
 
 
+def max_over_ranks(ms, dist=None, device="cpu"):
+    """The slowest rank's mean step time: every rank passes its own and gets
+    the maximum back (an all-reduce of one float; `dist` None = one rank).
+    NCCL wants `device` to be the rank's GPU, gloo takes the CPU."""
+    if dist is None:
+        return float(ms)
+    import torch
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbs(world, nbytes_per_rank, ms_max):
+    """Whole-job GB/s of `world` replicas that each read `nbytes_per_rank`
+    per step, clocked by the slowest rank's step time."""
+    return world * nbytes_per_rank / (ms_max * 1e-3) / 1e9
+
+
 def run_gpu(args, rank, world):
     import torch
     from turboquant_kv_cache_gb300 import binding as tb
@@ -316,13 +334,8 @@ def run_gpu(args, rank, world):
     if dist:
         dist.barrier()
     times = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    ms = statistics.mean(times)
-    ms_max = ms
-    if dist:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_max = float(t.item())
-    value = world * nbytes / (ms_max * 1e-3) / 1e9
+    ms_max = max_over_ranks(statistics.mean(times), dist, dev)
+    value = job_gbs(world, nbytes, ms_max)
     peak, peak_kind = _peaks()
 
     # end to end through the public API: per step, H2D of the new query and

@@ -52,9 +52,9 @@ def _peaks():
         return 6800.0, "fallback"
 
 
-# DRAM bytes (read + write) of one decode_tc_kernel launch of the headline
-# workload, from the ncu capture summarised in
-# profiles/decode_tc_qwen3_8b_turbo3_ctx32768.md (None once the kernel changes).
+# DRAM bytes (read + write) of one launch of the headline decode kernel,
+# dram__bytes_read.sum + dram__bytes_write.sum from an ncu capture of the
+# kernel as it is now (None once the kernel changes); not measured by this run.
 DECODE_TRAFFIC_BYTES = (235.013888 + 3.719424) * 1e6
 
 
@@ -67,8 +67,45 @@ def decode_bytes(B, Hkv, ctx, d, k_bits, v_bits, k_block, v_block):
 
 
 # ---------------------------------------------------------------- clocks
+class _Nvml:
+    """Just enough of NVML through ctypes to read the SM clock and the clock
+    event reasons of one GPU (read-only queries)."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, index):
+        import ctypes
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        if self.lib.nvmlDeviceGetHandleByIndex_v2(index, ctypes.byref(self.h)) != 0:
+            raise RuntimeError("no NVML handle")
+
+    def sm_mhz(self):
+        v = self.ct.c_uint()
+        self.lib.nvmlDeviceGetClockInfo(self.h, 1, self.ct.byref(v))   # NVML_CLOCK_SM
+        return v.value
+
+    def sm_max_mhz(self):
+        v = self.ct.c_uint()
+        self.lib.nvmlDeviceGetMaxClockInfo(self.h, 1, self.ct.byref(v))
+        return v.value
+
+    def reasons(self):
+        v = self.ct.c_ulonglong()
+        self.lib.nvmlDeviceGetCurrentClocksEventReasons(self.h, self.ct.byref(v))
+        return [n for bit, n in self.REASONS.items() if v.value & bit]
+
+
 class ClockSampler:
-    """Samples nvidia-smi while the timed region runs."""
+    """Samples the SM clock and the clock event reasons while the timed
+    region runs: NVML every ~0.2 ms from a thread (the timed region of a
+    short run lasts milliseconds), and nvidia-smi every 20 ms as a second
+    record.  Enter it before the warm-up; ``wait_ready`` blocks until both
+    samplers have produced a first sample."""
 
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -78,6 +115,9 @@ class ClockSampler:
         self.index = index
         self.proc = None
         self.lines = []
+        self.fast = []          # (time, sm MHz, reasons)
+        self.window = None
+        self._stop = threading.Event()
 
     def __enter__(self):
         try:
@@ -88,13 +128,37 @@ class ClockSampler:
             self.thread.start()
         except Exception:
             self.proc = None
+        try:
+            self.nvml = _Nvml(self.index)
+            self.max_mhz = self.nvml.sm_max_mhz()
+            self.fthread = threading.Thread(target=self._poll, daemon=True)
+            self.fthread.start()
+        except Exception:
+            self.nvml = None
         return self
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.perf_counter(), line.strip()))
+
+    def _poll(self):
+        while not self._stop.is_set():
+            self.fast.append((time.perf_counter(), self.nvml.sm_mhz(), tuple(self.nvml.reasons())))
+            time.sleep(0.0002)
+
+    def wait_ready(self, timeout=10.0):
+        t0 = time.perf_counter()
+        while time.perf_counter() - t0 < timeout:
+            if (self.proc is None or self.lines) and (self.nvml is None or self.fast):
+                return
+            time.sleep(0.01)
+
+    def mark(self, t0, t1):
+        """The timed region, in perf_counter seconds."""
+        self.window = (t0, t1)
 
     def __exit__(self, *exc):
+        self._stop.set()
         if self.proc:
             self.proc.terminate()
             try:
@@ -102,25 +166,40 @@ class ClockSampler:
             except Exception:
                 self.proc.kill()
 
+    def _in(self, t):
+        return self.window is None or self.window[0] <= t <= self.window[1]
+
     def summary(self):
         sm, mx, reasons = [], [], set()
+        src = None
+        fast = [(m, r) for t, m, r in self.fast if self._in(t)]
+        if fast:
+            src = "nvml, ~0.2 ms period, timed region only"
+            sm = [m for m, _ in fast]
+            mx = [self.max_mhz]
+            for _, r in fast:
+                reasons.update(r)
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        smi = [ln for t, ln in self.lines if self._in(t)]
+        for ln in smi:
             f = [x.strip() for x in ln.split(",")]
             if len(f) < 9:
                 continue
             try:
-                sm.append(float(f[1]))
-                mx.append(float(f[2]))
+                if not fast:
+                    sm.append(float(f[1]))
+                    mx.append(float(f[2]))
             except ValueError:
                 continue
             for n, val in zip(names, f[5:9]):
                 if val.lower().startswith("active"):
                     reasons.add(n)
+        if smi and not fast:
+            src = "nvidia-smi, 20 ms period, timed region only"
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "nvidia_smi_samples": len(smi), "source": src}
 
 
 # ---------------------------------------------------------------- GPU arm
@@ -142,21 +221,42 @@ def headline_cache(tb, torch, inputs, dev):
     return L, K, V, q
 
 
+def _prefix(tb, C, ctx):
+    """A contiguous copy of the first ctx tokens of a [B, H, S] cache."""
+    B, H, _ = C.lead_shape
+    P = tb.PackedKV(C.layout, (B, H, ctx), device=C.codes.device)
+    P.codes.copy_(C.codes[:, :, :ctx])
+    P.scales.copy_(C.scales[:, :, :ctx])
+    return P
+
+
 def bench_depth(tb, torch, dev, L, K, V, q, steps, warm):
     """The headline decode at growing context depth (same batch, heads and
-    layout): one tq_decode_attn call per step, L2 flushed before each.  Depths
-    up to the headline's 32768 read prefixes of its cache; 65536 and 131072
-    read a cache of that length made by repeating it along the context (the
-    kernel reads every byte either way).  GB/s that holds or rises with depth
-    is decode that does not degrade with context."""
+    layout), L2 flushed before each call.  Depths up to the headline's 32768
+    read prefixes of its cache; 65536 and 131072 read a cache of that length
+    made by repeating it along the context (the kernel reads every byte
+    either way).
+
+    Two arms per depth: the fused decode (one tq_decode_attn call), and the
+    bulk path the pages describe for the llama.cpp fork - tq_dequantize_kv
+    of the whole K and V context to fp16, then dense fp16 attention (PyTorch's
+    scaled_dot_product_attention, a library call used as the comparison only).
+    Both report GB/s of the same compressed bytes, so the curves compare
+    directly; the bulk arm also gives the dequantise kernel's own HBM
+    fraction (packed bytes in + fp16 bytes out)."""
+    import torch.nn.functional as F
     B, Hq, Hkv, d = DEC["B"], DEC["Hq"], DEC["Hkv"], DEC["d"]
+    G = Hq // Hkv
     flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=dev)
     out = torch.empty_like(q)
+    hbm, _ = _peaks()
     res = {}
     S0 = K.lead_shape[2]
     for ctx in (2048, 8192, 32768, 65536, 131072):
-        if ctx <= S0:
+        if ctx == S0:
             Kc, Vc = K, V
+        elif ctx < S0:
+            Kc, Vc = _prefix(tb, K, ctx), _prefix(tb, V, ctx)
         else:
             rep_n = ctx // S0
             Kc = tb.PackedKV(L, (B, Hkv, ctx), device=dev)
@@ -170,12 +270,41 @@ def bench_depth(tb, torch, dev, L, K, V, q, steps, warm):
         ms = _time(torch, lambda: tb.tq_decode_attn(Kc, Vc, q, ctx=ctx, workspace=ws, out=out, n_split=n_split),
                    flush, steps, warm)
         nbytes = decode_bytes(B, Hkv, ctx, d, 3, 3, 32, 32)
+        # bulk arm: dequantise everything, then dense attention over fp16
+        Kd = torch.empty((B, Hkv, ctx, d), dtype=torch.float16, device=dev)
+        Vd = torch.empty_like(Kd)
+        q4 = q.view(B, Hkv, G, d)
+
+        def deq():
+            tb.tq_dequantize_kv(Kc, torch.float16, out=Kd)
+            tb.tq_dequantize_kv(Vc, torch.float16, out=Vd)
+
+        def bulk():
+            deq()
+            return F.scaled_dot_product_attention(q4, Kd, Vd)
+
+        ms_bulk = _time(torch, bulk, flush, steps, warm)
+        ms_deq = _time(torch, deq, flush, steps, warm)
+        deq_bytes = nbytes + 2 * Kd.numel() * 2          # packed in, fp16 K and V out
+        o_bulk = bulk().reshape(B, Hq, d)
+        tb.tq_decode_attn(Kc, Vc, q, ctx=ctx, workspace=ws, out=out, n_split=n_split)
+        torch.cuda.synchronize()
         res[str(ctx)] = {"us": round(ms * 1e3, 2), "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1),
-                         "n_split": n_split}
+                         "n_split": n_split,
+                         "bulk": {"us": round(ms_bulk * 1e3, 2), "GB/s": round(nbytes / (ms_bulk * 1e-3) / 1e9, 1),
+                                  "dequantize_us": round(ms_deq * 1e3, 2),
+                                  "dequantize_roofline": {"bound": "hbm",
+                                                          "achieved": round(deq_bytes / (ms_deq * 1e-3) / 1e9, 1),
+                                                          "peak": hbm, "unit": "GB/s",
+                                                          "frac": round(deq_bytes / (ms_deq * 1e-3) / 1e9 / hbm, 4),
+                                                          "bytes_per_step": deq_bytes},
+                                  "max_abs_diff_vs_fused": round(float((o_bulk.float() - out.float()).abs().max()), 5)}}
+        del Kd, Vd
         if Kc is not K:
             del Kc, Vc
-            torch.cuda.empty_cache()
-    return {"workload": "the headline decode (B=8, Hq=32, Hkv=8, d=128, turbo3) at context depth 2K-128K",
+        torch.cuda.empty_cache()
+    return {"workload": "the headline decode (B=8, Hq=32, Hkv=8, d=128, turbo3) at context depth 2K-128K; "
+                        "fused decode vs bulk dequantise + dense fp16 attention",
             "by_ctx": res}
 
 
@@ -248,6 +377,8 @@ def run_only(args, tb, torch, inputs, dev):
         res.update(workload=WORKLOAD, ms=round(ms, 5), GBps=round(nbytes / (ms * 1e-3) / 1e9, 1))
     elif args.only == "quantize":
         res.update(bench_quantize(tb, torch, inputs, dev, args))
+    elif args.only == "c1":
+        res.update(bench_c1(tb, torch, inputs, dev, args.steps, args.warmup))
     elif args.only == "decode_depth":
         L, K, V, q = headline_cache(tb, torch, inputs, dev)
         res.update(bench_depth(tb, torch, dev, L, K, V, q, args.steps, args.warmup))
@@ -313,16 +444,17 @@ def run_gpu(args, rank, world):
     def step():
         tb.tq_decode_attn(K, V, q, ctx=ctx, workspace=ws, out=out, n_split=n_split)
 
-    for _ in range(args.warmup):
-        flush.zero_()
-        step()
-    torch.cuda.synchronize()
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize()
     with ClockSampler(dev.index) as clocks:
+        clocks.wait_ready()
+        for _ in range(args.warmup):
+            flush.zero_()
+            step()
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
         t0 = time.perf_counter()
         for i in range(args.steps):
             flush.zero_()                     # L2 flush between steps, outside the events
@@ -330,7 +462,9 @@ def run_gpu(args, rank, world):
             step()
             ends[i].record(stream)
         torch.cuda.synchronize()
-        wall = time.perf_counter() - t0
+        t1 = time.perf_counter()
+        wall = t1 - t0
+        clocks.mark(t0, t1)
     if dist:
         dist.barrier()
     times = [s.elapsed_time(e) for s, e in zip(starts, ends)]
@@ -343,6 +477,7 @@ def run_gpu(args, rank, world):
     e2e = e2e_decode(tb, torch, inputs, dev, K, V, L, ws, n_split, args)
 
     quant = bench_quantize(tb, torch, inputs, dev, args)
+    c1 = bench_c1(tb, torch, inputs, dev, max(3, min(args.steps, 20)), 3)
     depth = None if args.no_extra else bench_depth(tb, torch, dev, L, K, V, q, max(3, min(args.steps, 20)), 3)
     window = None if args.no_extra else bench_window(tb, torch, inputs, dev, K, V, q, max(3, min(args.steps, 20)), 3)
     polar = None if args.no_extra else bench_polar(tb, torch, inputs, dev, max(3, min(args.steps, 20)), 3)
@@ -350,6 +485,7 @@ def run_gpu(args, rank, world):
     dblocks = None if args.no_extra else bench_decode_blocks(tb, torch, dev, K, V, q, max(3, min(args.steps, 20)), 3)
     k8v4 = None if args.no_extra else bench_k8v4(tb, torch, inputs, dev, max(3, min(args.steps, 20)), 3)
     extra = {} if args.no_extra else bench_extra(tb, torch, inputs, dev, args)
+    clk = clocks.summary()
     if rank == 0:
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
@@ -367,6 +503,7 @@ def run_gpu(args, rank, world):
                          "kernel": "decode_tc_kernel + decode_combine_kernel (one tq_decode_attn call, events around both)"},
             "e2e": e2e,
             "quantize": quant,
+            "c1_roundtrip": c1,
             "decode_vs_depth": depth,
             "decode_with_fp16_window": window,
             "polar_codec": polar,
@@ -375,7 +512,8 @@ def run_gpu(args, rank, world):
             "decode_over_blocks": dblocks,
             "other_workloads": extra,
             "gpu_launches": args.steps * 2,
-            "clocks": clocks.summary(),
+            "clocks": clk,
+            "cycles_per_step_at_median_clock": (round(ms_max * 1e-3 * clk["sm_mhz"] * 1e6) if clk["sm_mhz"] else None),
             "wall_s_timed": round(wall, 4),
         }
         if not args.no_cpu_baseline:
@@ -477,10 +615,46 @@ def bench_quantize(tb, torch, inputs, dev, args):
         ms = statistics.mean(s.elapsed_time(e) for s, e in times)
         bytes_per_vec = 64 * 2 + 64 * 4 // 8 + 2 * (64 // block)
         gbs = n_vec * bytes_per_vec / (ms * 1e-3) / 1e9
+        # relative reconstruction error sum ||x - x~||^2 / sum ||x||^2 over K and V
+        num = den = 0.0
+        for x, o in ((k, ok), (v, ov)):
+            xr = tb.tq_dequantize_kv(o, torch.float32)
+            xf = x.float()
+            num += float(((xr - xf) ** 2).sum())
+            den += float((xf ** 2).sum())
+            del xr, xf
         res[name] = {"gvec_per_s": round(n_vec / (ms * 1e-3) / 1e9, 3), "ms": round(ms, 5),
+                     "relative_sq_error": round(num / den, 5),
                      "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
                                   "frac": round(gbs / peak, 4), "bytes_per_vector": bytes_per_vec}}
     return res
+
+
+def bench_c1(tb, torch, inputs, dev, steps, warm):
+    """4096 random unit vectors of d=128 in fp32, 3-bit Lloyd-Max codes,
+    one norm per vector (sign seed 1): quantise -> dequantise round trip
+    on the GPU, its time and its mean squared error next to the pages'
+    0.034 ("turboquant-pytorch" MSE table, 3 bits) and the Lloyd-Max
+    distortion of N(0, 1/d) at 3 bits.  2.1 MB in: a launch-bound size."""
+    from oracle import tq_oracle as O
+    w = inputs.unit_roundtrip_workload()
+    x = torch.from_numpy(w["x"]).to(dev)
+    L = tb.make_layout(128, 128, 3, 0, 0, 1)
+    pk = tb.tq_quantize_kv(L, x)
+    xr = torch.empty_like(x)
+
+    def rt():
+        tb.tq_quantize_kv(L, x, out=pk)
+        tb.tq_dequantize_kv(pk, torch.float32, out=xr)
+
+    flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=dev)
+    ms = _time(torch, rt, flush, steps, warm)
+    rt()
+    mse = float(((xr - x) ** 2).sum(dim=1).mean())
+    return {"workload": "4096 unit vectors, d=128, fp32, 3-bit, one norm per vector (quantise + dequantise)",
+            "us": round(ms * 1e3, 2), "mse": round(mse, 5), "pages_mse_3bit": 0.034,
+            "lloyd_max_distortion_3bit": round(O.relative_distortion(3), 5),
+            "bound": "launch (2.1 MB in, 0.2 MB packed)"}
 
 
 def bench_blocks(tb, torch, dev, K, steps, warm):
@@ -786,7 +960,7 @@ def main():
     ap.add_argument("--no-extra", action="store_true", help="skip the other workloads (headline only)")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--only", default=None,
-                    choices=["decode", "quantize", "prefill", "decode_d256", "decode_qjl", "quantize_qjl", "decode_depth",
+                    choices=["decode", "quantize", "c1", "prefill", "decode_d256", "decode_qjl", "quantize_qjl", "decode_depth",
                              "decode_window", "polar", "blocks", "decode_k8v4",
                              "decode_blocks"],
                     help="time one workload alone and print its result only (profiler runs)")

@@ -243,7 +243,10 @@ int tq_decode_attn(const tq_kv_view* K, const tq_kv_view* V, const uint16_t* q, 
  *     are refused with TQ_ERR_WORKSPACE before anything is enqueued.
  *   - The first call on a device looks up that device's copy of the array
  *     (cudaGetSymbolAddress, with the device current) and caches it; make
- *     that first call before any stream capture.
+ *     that first call before any stream capture.  A failed lookup returns
+ *     TQ_ERR_CUDA and clears the runtime's last error, so later calls do
+ *     not see it.  cudaDeviceReset on that device invalidates the cached
+ *     address: do not call this function on the device after a reset.
  *   - All calls on a device share the one array and it keeps the last
  *     call's contents (no call needs it zeroed): calls that overlap on the
  *     GPU (other streams, other host threads) race on it and must be

@@ -607,26 +607,36 @@ def decode_attention(q, Kd, Vd, kv_len=None, softmax_scale=None):
     return out
 
 
-def prefill_attention(q, Kd, Vd, ctx, causal=True, softmax_scale=None):
+def prefill_attention(q, Kd, Vd, ctx, causal=True, softmax_scale=None, rows=None, group=None):
     """Tq queries per (batch, q-head) at positions ctx-Tq .. ctx-1 over the
     decoded cache positions [0, ctx).  With ``causal`` query i attends to
-    positions <= ctx - Tq + i (bottom-right aligned mask)."""
+    positions <= ctx - Tq + i (bottom-right aligned mask).
+
+    ``rows`` (query indices) restricts the result to those queries, at their
+    own positions.  ``group`` = (first q-head, count) restricts it to q-heads
+    that share one KV head, which Kd and Vd then hold alone ([B, 1, S, d])."""
     q = np.asarray(q, dtype=np.float64)
     B, Hq, Tq, d = q.shape
-    Hkv = Kd.shape[1]
-    g = Hq // Hkv
     sc = 1.0 / math.sqrt(d) if not softmax_scale or softmax_scale <= 0 else softmax_scale
-    out = np.zeros((B, Hq, Tq, d))
+    rows = np.arange(Tq) if rows is None else np.asarray(rows)
+    if group is None:
+        heads = list(range(Hq))
+        g = Hq // Kd.shape[1]
+        kv_of = [h // g for h in heads]
+    else:
+        heads = list(range(group[0], group[0] + group[1]))
+        kv_of = [0] * len(heads)
+    out = np.zeros((B, len(heads), len(rows), d))
     for b in range(B):
-        for h in range(Hq):
-            kh = h // g
-            s = q[b, h] @ Kd[b, kh, :ctx].T * sc              # [Tq, ctx]
+        for j, h in enumerate(heads):
+            kh = kv_of[j]
+            s = q[b, h, rows] @ Kd[b, kh, :ctx].T * sc        # [rows, ctx]
             if causal:
-                pos = ctx - Tq + np.arange(Tq)
+                pos = ctx - Tq + rows
                 mask = np.arange(ctx)[None, :] > pos[:, None]
                 s = np.where(mask, -np.inf, s)
             p = softmax_rows(s)
-            out[b, h] = p @ Vd[b, kh, :ctx]
+            out[b, j] = p @ Vd[b, kh, :ctx]
     return out
 
 

@@ -9,6 +9,8 @@ Acceptance rules (the codec's stated tolerances):
   * decoded vectors within 1e-3 relative L2;
   * attention outputs within 2e-3 absolute.
 """
+import os
+
 import numpy as np
 import torch
 
@@ -17,6 +19,15 @@ from oracle import tq_oracle as O
 TIE = 1e-5
 ATTN_ATOL = 2e-3
 DEQ_RTOL = 1e-3
+
+# Boundary-tie mismatches seen by the comparisons below, one entry per call:
+# (test id, kind, mismatches, compared); printed at the end of the session.
+TIE_LOG = []
+
+
+def _log_ties(kind, n_bad, n_total):
+    test = os.environ.get("PYTEST_CURRENT_TEST", "?").split(" (")[0]
+    TIE_LOG.append((test, kind, int(n_bad), int(n_total)))
 
 
 def fp16_ulp_diff(a, b):
@@ -38,6 +49,7 @@ def compare_codes(gpu_packed, oq, L):
         near = np.min(np.abs(y[:, None] - bnd[None, :]), axis=1) < TIE
         assert near.all(), f"{(~near).sum()} code mismatches away from a boundary"
         assert np.all(np.abs(gcodes[diff] - ocodes[diff]) == 1)
+    _log_ties("codes", diff.sum(), diff.size)
     return int(diff.sum()), np.any(diff, axis=1)
 
 
@@ -55,6 +67,7 @@ def compare_qjl(gpu_bits, oq, L, skip_rows):
     diff[skip_rows] = False
     if diff.any():
         assert np.all(np.abs(oq["proj"][diff]) < TIE), "QJL sign mismatch away from zero"
+    _log_ties("qjl", diff.sum(), diff.size)
     return int(diff.sum())
 
 

@@ -34,3 +34,24 @@ def tqlib():
     if not os.path.exists(build.LIB):
         build.build()
     return binding.library()
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    """Reports the boundary-tie mismatches of every GPU-vs-oracle code
+    comparison: codes may differ from the oracle only for coordinates within
+    1e-5 of a decision boundary (QJL bits: |S r| < 1e-5), and those are
+    counted here per case."""
+    try:
+        from _parity import TIE_LOG
+    except Exception:  # pragma: no cover
+        return
+    if not TIE_LOG:
+        return
+    tr = terminalreporter
+    tr.section("boundary-tie mismatches (GPU vs oracle)")
+    tot_bad = tot = 0
+    for test, kind, bad, n in TIE_LOG:
+        tr.write_line(f"{bad:6d} / {n:9d} {kind:5s} {test}")
+        tot_bad += bad
+        tot += n
+    tr.write_line(f"total: {tot_bad} of {tot} compared codes/bits differ, every one a boundary tie")

@@ -92,6 +92,52 @@ def test_dequantize_matches_oracle(tqlib, d, blk, bits, dt, nc, m, out_dtype):
     assert np.all(got[3] == 0)
 
 
+def _golden(name):
+    import json
+    import os
+    with open(os.path.join(os.path.dirname(__file__), "golden", name)) as f:
+        return json.load(f)
+
+
+@pytest.mark.parametrize("idx", range(5))
+def test_dequantize_reads_known_answer_bytes(tqlib, idx):
+    """The GPU reads the hand-derived bytes of the packed layout
+    (tests/golden/packed_layout_known_answers.json, worked out from the
+    definition in include/tq.h) as the codes they encode: dequantising
+    records made of those groups gives scale * D (H c(code)) per 32-block,
+    formed here from the oracle's signs, Hadamard matrix and codebook."""
+    from turboquant_kv_cache_gb300 import binding as tb
+    e = _golden("packed_layout_known_answers.json")["groups"][idx]
+    bits, d = e["bits"], 128
+    i = np.arange(32)
+    if bits == 3:
+        codes = np.where(i < 24, i % 8, 7 - (i - 24))
+    elif bits == 4:
+        codes = i % 16
+    elif bits == 2:
+        codes = (i // 8) % 4 if "//" in e["codes"] else i % 4
+    else:
+        codes = np.isin(i, [0, 9, 18, 27]).astype(np.int64)
+    group = np.array([int(x, 16) for x in e["bytes"]], dtype=np.uint8)
+    n = 3
+    rec = np.tile(group, (n, d // 32))                          # every 32-block of every record
+    scales = np.array([[1.0, 0.5, 2.0, 0.25]] * n, dtype=np.float16) * np.arange(1, n + 1, dtype=np.float16)[:, None]
+    L = tb.make_layout(d, 32, bits, 0, 0, 7)
+    Lo = O.Layout(d, 32, bits, 0, 0, 7)
+    pk = tb.PackedKV(L, (n,))
+    pk.codes.copy_(torch.from_numpy(rec))
+    pk.scales.copy_(torch.from_numpy(scales))
+    got = to_np(tb.tq_dequantize_kv(pk, torch.float32))
+    cent, _ = O.codebook_for(Lo)
+    H = O.hadamard_matrix(32)
+    D = O.sign_vector(7, d)
+    ref = np.zeros((n, d))
+    for r in range(n):
+        for j in range(d // 32):
+            ref[r, 32 * j:32 * j + 32] = float(scales[r, j]) * D[32 * j:32 * j + 32] * (H @ np.asarray(cent)[codes])
+    assert np.abs(got - ref).max() < 1e-5 * max(1.0, np.abs(ref).max())
+
+
 def test_roundtrip_unit_vectors_mse(tqlib):
     """4096 unit vectors, d=128, 3 bits: GPU quantise -> GPU dequantise MSE
     against the oracle's closed-form distortion (3-bit: 0.0345)."""

@@ -39,14 +39,31 @@ CASES = [
     ("q4", (32, 3, 0, 0, 1), (32, 3, 0, 0, 1), 1, 4, 1, 100, 97, 4, 128),
     ("q16_gqa8", (64, 3, 0, 0, 1), (32, 4, 0, 0, 1), 1, 8, 1, 90, 80, 16, 128),
     ("q512_long", (32, 3, 0, 0, 1), (32, 3, 0, 0, 1), 1, 8, 2, 700, 650, 512, 128),
+    # Gaussian keys in the shape class of the benchmarked head_dim-256 prefill: 16 q / 4 KV heads, 512
+    # causal queries, turbo4 K / turbo3 V; 8192 context makes the library split the context 7 ways as
+    # it does at 131072
+    ("d256_q512_ctx8192_splits_gauss", (32, 4, 0, 0, 1), (32, 3, 0, 0, 1), 1, 16, 4, 8192, 8192, 512, 256),
 ]
 
 
 @pytest.mark.parametrize("name,cK,cV,B,Hq,Hkv,S_cap,ctx,Tq,d", CASES)
 def test_prefill_matches_oracle(tqlib, name, cK, cV, B, Hq, Hkv, S_cap, ctx, Tq, d):
     from turboquant_kv_cache_gb300 import binding as tb
-    got, ref = _run(tb, cK, cV, B, Hq, Hkv, S_cap, ctx, Tq, d, heavy=(d == 256))
+    got, ref = _run(tb, cK, cV, B, Hq, Hkv, S_cap, ctx, Tq, d, heavy=(d == 256 and "gauss" not in name))
     assert np.abs(got - ref).max() < ATTN_ATOL, (name, np.abs(got - ref).max())
+
+
+@pytest.mark.xfail(strict=True, reason=(
+    "fp16 operands: with Student-t(4) keys a few large scores compete in the softmax and the fp16 "
+    "rounding of q^ (alone 6.1e-3 in a float64 emulation of the kernel's arithmetic) and of the "
+    "decoded keys (2.3e-3) moves the output by up to 6.8e-3 > 2e-3; hi/lo fp16 splits of both "
+    "operands bring the emulated error to 1.1e-3"))
+def test_prefill_heavy_tailed_keys_ctx8192(tqlib):
+    """The benchmarked head_dim-256 prefill class with its Student-t(4) keys
+    at 8192 context (7 context splits), every output against the oracle."""
+    from turboquant_kv_cache_gb300 import binding as tb
+    got, ref = _run(tb, (32, 4, 0, 0, 1), (32, 3, 0, 0, 1), 1, 16, 4, 8192, 8192, 512, 256, heavy=True)
+    assert np.abs(got - ref).max() < ATTN_ATOL, np.abs(got - ref).max()
 
 
 def test_prefill_non_causal(tqlib):

@@ -297,6 +297,48 @@ def test_pack_roundtrip(bits, d):
     assert not np.array_equal(O.pack_codes(flips, bits), p)
 
 
+def _known_answer_codes(entry):
+    i = np.arange(32)
+    b = entry["bits"]
+    if b == 3:
+        return np.where(i < 24, i % 8, 7 - (i - 24))
+    if b == 4:
+        return i % 16
+    if b == 2:
+        return (i // 8) % 4 if "//" in entry["codes"] else i % 4
+    return np.isin(i, [0, 9, 18, 27]).astype(np.int64)
+
+
+def test_pack_known_answers():
+    """Bytes worked out by hand from the layout definition in include/tq.h
+    (not from the oracle): a misread of the definition shared by the oracle
+    and the kernels would fail here."""
+    g = _golden("packed_layout_known_answers.json")
+    for e in g["groups"]:
+        exp = np.array([int(x, 16) for x in e["bytes"]], dtype=np.uint8)
+        codes = _known_answer_codes(e)
+        assert np.array_equal(O.pack_codes(codes[None], e["bits"])[0], exp), e["bits"]
+        assert np.array_equal(O.unpack_codes(exp[None], e["bits"], 32)[0], codes), e["bits"]
+    q = g["qjl"]
+    s = np.zeros((1, q["m"]), dtype=np.uint8)
+    s[0, q["ones_at"]] = 1
+    exp = np.array([int(x, 16) for x in q["bytes"]], dtype=np.uint8)
+    assert np.array_equal(O.pack_qjl(s)[0], exp)
+    assert np.array_equal(O.unpack_qjl(exp[None], q["m"])[0], s[0])
+
+
+def test_prefill_attention_restriction():
+    """The sampled form (query rows, one GQA group) equals the matching
+    slice of the full result."""
+    rng = np.random.default_rng(5)
+    q = rng.standard_normal((1, 8, 9, 16))
+    Kd, Vd = rng.standard_normal((1, 2, 30, 16)), rng.standard_normal((1, 2, 30, 16))
+    full = O.prefill_attention(q, Kd, Vd, 27, causal=True)
+    rows = np.array([0, 4, 8])
+    part = O.prefill_attention(q, Kd[:, 1:2], Vd[:, 1:2], 27, causal=True, rows=rows, group=(4, 4))
+    assert np.allclose(part, full[:, 4:8][:, :, rows], atol=1e-13)
+
+
 def test_qjl_pack_roundtrip():
     s = np.random.default_rng(0).integers(0, 2, size=(9, 128)).astype(np.uint8)
     assert np.array_equal(O.unpack_qjl(O.pack_qjl(s), 128), s)

@@ -278,10 +278,13 @@ def tq_append_kv(cache, x, pos, stream=None):
     return cache
 
 
-def tq_dequantize_kv(packed, out_dtype=torch.float16, stream=None):
+def tq_dequantize_kv(packed, out_dtype=torch.float16, stream=None, out=None):
     lib = _load()
     d = packed.layout.head_dim
-    out = torch.empty(packed.lead_shape + (d,), dtype=out_dtype, device=packed.codes.device)
+    if out is None:
+        out = torch.empty(packed.lead_shape + (d,), dtype=out_dtype, device=packed.codes.device)
+    elif out.dtype != out_dtype or out.numel() != packed.n_vec * d or not out.is_contiguous():
+        raise ValueError("out must be a contiguous tensor of n_vec x head_dim elements of out_dtype")
     st = lib.tq_dequantize_kv(ctypes.byref(packed.layout), _ptr(packed.codes), _ptr(packed.scales),
                               _ptr(packed.qjl), _ptr(packed.rnorm), _ptr(packed.S), packed.n_vec, _ptr(out),
                               _dtype_code(out_dtype), _stream(stream))

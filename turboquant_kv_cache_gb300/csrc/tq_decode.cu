@@ -1101,7 +1101,10 @@ extern "C" int tq_decode_attn_static(const tq_kv_view* K, const tq_kv_view* V, c
     std::lock_guard<std::mutex> lock(tq::g_scratch_mu);
     if (!tq::g_scratch_addr[dev]) {
       void* p = nullptr;
-      if (cudaGetSymbolAddress(&p, tq::g_decode_scratch) != cudaSuccess || !p) return TQ_ERR_CUDA;
+      if (cudaGetSymbolAddress(&p, tq::g_decode_scratch) != cudaSuccess || !p) {
+        cudaGetLastError();  // leave no error behind for the caller's next launch check
+        return TQ_ERR_CUDA;
+      }
       tq::g_scratch_addr[dev] = p;
     }
     scratch = tq::g_scratch_addr[dev];

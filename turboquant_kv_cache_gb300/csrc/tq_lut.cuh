@@ -100,15 +100,10 @@ __device__ __forceinline__ Cent<BITS> make_cent(const CodecParams& P) {
   return c;
 }
 
-// tables of the centroids (fp16 pairs c2[k] = (c_2k, c_2k+1)) times the fp16
-// norm s (s = 1.0 for unscaled)
+// Byte tables from fp16 entry pairs h[k] = (e_2k, e_2k+1).
 template <int BITS>
-__device__ __forceinline__ Tab make_tab_p(const uint32_t* c2, uint32_t s) {
-  const uint32_t s2 = s | (s << 16);
+__device__ __forceinline__ Tab tab_from_pairs(const uint32_t* h) {
   Tab T;
-  uint32_t h[8];
-#pragma unroll
-  for (int k = 0; k < (1 << BITS) / 2; ++k) h[k] = lut_hmul2(c2[k], s2);
   if (BITS == 1) {
     T.t[0] = lut_prmt(h[0], h[0], 0x6420);
     T.t[2] = lut_prmt(h[0], h[0], 0x7531);
@@ -134,9 +129,37 @@ __device__ __forceinline__ Tab make_tab_p(const uint32_t* c2, uint32_t s) {
   return T;
 }
 
+// tables of the centroids (fp16 pairs c2[k] = (c_2k, c_2k+1)) times the fp16
+// norm s (s = 1.0 for unscaled): fp16 products of the fp16 centroids
+template <int BITS>
+__device__ __forceinline__ Tab make_tab_p(const uint32_t* c2, uint32_t s) {
+  const uint32_t s2 = s | (s << 16);
+  uint32_t h[8];
+#pragma unroll
+  for (int k = 0; k < (1 << BITS) / 2; ++k) h[k] = lut_hmul2(c2[k], s2);
+  return tab_from_pairs<BITS>(h);
+}
+
 template <int BITS>
 __device__ __forceinline__ Tab make_tab(const Cent<BITS>& c, uint32_t s) {
   return make_tab_p<BITS>(c.c2, s);
+}
+
+// Tables of the centroids c (fp32) times the norm s, each entry the fp32
+// product rounded once to fp16.  The fp16-product tables above round the
+// centroid first and the product again; for keys that double rounding is
+// the largest error of the attention output, because the softmax turns a
+// score error into a relative weight error (with heavy-tailed keys at long
+// context it alone exceeds the 2e-3 attention tolerance).
+template <int BITS>
+__device__ __forceinline__ Tab make_tab_f32(const float* c, float s) {
+  uint32_t h[8];
+#pragma unroll
+  for (int k = 0; k < (1 << BITS) / 2; ++k) {
+    const __half2 v = __floats2half2_rn(c[2 * k] * s, c[2 * k + 1] * s);
+    h[k] = *reinterpret_cast<const uint32_t*>(&v);
+  }
+  return tab_from_pairs<BITS>(h);
 }
 
 // Four fp16x2 registers (codes 0-1, 2-3, 4-5, 6-7) of a nibble word.

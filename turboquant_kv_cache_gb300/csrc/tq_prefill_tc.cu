@@ -304,9 +304,11 @@ __device__ __forceinline__ void load_items(int bits, const ItemPlan<D, NT>& pl, 
 
 // Decode a thread's items of one tile from registers into the core-matrix
 // tile at shared address `tile` (same rules as decode_tile_items).
-template <int D, int NT, int BITS>
+// EXACT (the keys): each (token, block) table holds the fp32 products of the
+// centroids and the block norm rounded once to fp16 (make_tab_f32).
+template <int D, int NT, int BITS, bool EXACT>
 __device__ __forceinline__ void decode_regs_b(const ItemPlan<D, NT>& pl, const ItemRegs<D, NT>& r, const uint32_t* c2,
-                                              const Tab& fixed, int n_valid, uint32_t tile) {
+                                              const Tab& fixed, const float* cent, int n_valid, uint32_t tile) {
   auto sts2 = [&](uint32_t off, uint4 v) { sts128(tile + off, v); };
 #pragma unroll
   for (int k = 0; k < ItemPlan<D, NT>::N; ++k) {
@@ -324,7 +326,9 @@ __device__ __forceinline__ void decode_regs_b(const ItemPlan<D, NT>& pl, const I
       const uint32_t sc = r.sc[k];
       Tab T;
       uint32_t s2 = 0;
-      if (BITS == 4) {
+      if (EXACT) {
+        T = make_tab_f32<BITS>(cent, h2f((uint16_t)sc));
+      } else if (BITS == 4) {
         T = fixed;
         s2 = sc | (sc << 16);
       } else {
@@ -334,7 +338,7 @@ __device__ __forceinline__ void decode_regs_b(const ItemPlan<D, NT>& pl, const I
       for (int c = 0; c < 4; ++c) {
         uint32_t o[4];
         lut8<BITS>(n[c], T, o);
-        if (BITS == 4) {
+        if (BITS == 4 && !EXACT) {
 #pragma unroll
           for (int e = 0; e < 4; ++e) o[e] = lut_hmul2(o[e], s2);
         }
@@ -362,14 +366,14 @@ __device__ __forceinline__ CodeTabs make_code_tabs(const CodecParams& P) {
   return c;
 }
 
-template <int D, int NT>
+template <int D, int NT, bool EXACT>
 __device__ __forceinline__ void decode_regs(int bits, const ItemPlan<D, NT>& pl, const ItemRegs<D, NT>& r,
-                                            const CodeTabs& ct, int n_valid, uint32_t tile) {
+                                            const CodeTabs& ct, const float* cent, int n_valid, uint32_t tile) {
   switch (bits) {
-    case 4: decode_regs_b<D, NT, 4>(pl, r, ct.c2, ct.fixed, n_valid, tile); break;
-    case 3: decode_regs_b<D, NT, 3>(pl, r, ct.c2, ct.fixed, n_valid, tile); break;
-    case 2: decode_regs_b<D, NT, 2>(pl, r, ct.c2, ct.fixed, n_valid, tile); break;
-    default: decode_regs_b<D, NT, 1>(pl, r, ct.c2, ct.fixed, n_valid, tile); break;
+    case 4: decode_regs_b<D, NT, 4, EXACT>(pl, r, ct.c2, ct.fixed, cent, n_valid, tile); break;
+    case 3: decode_regs_b<D, NT, 3, EXACT>(pl, r, ct.c2, ct.fixed, cent, n_valid, tile); break;
+    case 2: decode_regs_b<D, NT, 2, EXACT>(pl, r, ct.c2, ct.fixed, cent, n_valid, tile); break;
+    default: decode_regs_b<D, NT, 1, EXACT>(pl, r, ct.c2, ct.fixed, cent, n_valid, tile); break;
   }
 }
 
@@ -441,7 +445,7 @@ __device__ __forceinline__ void decoder_role(const CodecParams& P, const CodeTab
     const int kb = t % NB;
     if (t >= NB) wait(free_bar + 8 * kb, (uint32_t)(t / NB - 1) & 1);   // the products NB tiles back are done
     const uint32_t tile = buf0 + (uint32_t)kb * tile_bytes;
-    if (!abort) decode_regs<D, NT>(P.bits, pl, r, ct, n_valid_of(t), tile);
+    if (!abort) decode_regs<D, NT, BAR_ID == 1>(P.bits, pl, r, ct, P.centroids, n_valid_of(t), tile);
     // the stores before the tensor cores and the bulk copy (async proxy) read them
     asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
     asm volatile("bar.sync %0, %1;\n" ::"n"(BAR_ID), "n"(NT) : "memory");

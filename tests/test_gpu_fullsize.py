@@ -53,7 +53,7 @@ def _plant(C, Lo, b, h, x, S=None):
 
 def test_headline_decode_full_size(tqlib):
     """Qwen3-8B-shaped turbo3 decode, B=8, Hq=32, Hkv=8, d=128, ctx=32768,
-    with the library's split count and an explicit workspace (the timed
+    with the library's own split count and an explicit workspace (the timed
     call); slices (0, 0) and (7, 5) against the oracle."""
     from turboquant_kv_cache_gb300 import binding as tb
     B, Hq, Hkv, d, ctx = 8, 32, 8, 128, 32768
@@ -68,9 +68,9 @@ def test_headline_decode_full_size(tqlib):
         kd = _plant(K, Lo, b, h, inputs.gaussian((ctx, d), 900 + 2 * i))
         vd = _plant(V, Lo, b, h, inputs.gaussian((ctx, d), 901 + 2 * i))
         dec[(b, h)] = (kd, vd)
-    ws_bytes, ns = tb.tq_decode_workspace_bytes(B, Hq, Hkv, d, ctx, 0)
+    ws_bytes, _ = tb.tq_decode_workspace_bytes(B, Hq, Hkv, d, ctx, 0)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
-    out = tb.tq_decode_attn(K, V, torch.from_numpy(q).cuda(), ctx=ctx, workspace=ws, n_split=ns)
+    out = tb.tq_decode_attn(K, V, torch.from_numpy(q).cuda(), ctx=ctx, workspace=ws)
     got = to_np(out.float())
     g = Hq // Hkv
     for (b, h), (kd, vd) in dec.items():

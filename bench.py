@@ -587,48 +587,80 @@ def e2e_decode(tb, torch, inputs, dev, K, V, L, ws, n_split, args):
 
 
 def bench_quantize(tb, torch, inputs, dev, args):
+    """Quantise the K and V caches of a Llama-3.2-1B-shaped model step.
+    Main figure: K and V stacked in one [2 x 16 layers x 8 heads x 2048, 64]
+    input, one call (one launch) per step, as a fused K/V projection hands
+    them over; `two_calls` is the same work as separate K and V calls (two
+    launches, each paying the fixed launch cost).  Both are timed as CUDA
+    graph replays (device time without the per-call host overhead, which at
+    this size is as long as a kernel); *_eager is call by call."""
     w = inputs.llama1b_kv_workload()
     k = torch.from_numpy(w["k"]).to(dev)
     v = torch.from_numpy(w["v"]).to(dev)
-    n_vec = k.numel() // 64 + v.numel() // 64
+    kv = torch.cat([k, v])
+    n_vec = kv.numel() // 64
     flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=dev)
     res = {"workload": "Llama-3.2-1B-shaped K and V: 16 layers x 8 heads x 2048 x d=64 fp16, 4 outlier channels x8",
            "vectors_per_step": n_vec, "unit": "Gvectors/s"}
     peak, _ = _peaks()
-    for name, block in (("per_vector", 64), ("block32", 32)):
-        L = tb.make_layout(64, block, 4, 0, 0, 1)
-        ok = tb.tq_quantize_kv(L, k)
-        ov = tb.tq_quantize_kv(L, v)
+
+    def timed(fn):
         for _ in range(args.warmup if args.only else max(3, args.warmup)):
             flush.zero_()
-            tb.tq_quantize_kv(L, k, out=ok)
-            tb.tq_quantize_kv(L, v, out=ov)
+            fn()
         torch.cuda.synchronize()
         times = []
         for _ in range(min(args.steps, 100)):
             flush.zero_()
             s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             s.record()
-            tb.tq_quantize_kv(L, k, out=ok)
-            tb.tq_quantize_kv(L, v, out=ov)
+            fn()
             e.record()
             times.append((s, e))
         torch.cuda.synchronize()
-        ms = statistics.mean(s.elapsed_time(e) for s, e in times)
+        return statistics.mean(s.elapsed_time(e) for s, e in times)
+
+    def graph_ms(fn):
+        try:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                fn()
+            return timed(g.replay), True
+        except Exception:
+            return timed(fn), False
+
+    for name, block in (("per_vector", 64), ("block32", 32)):
+        L = tb.make_layout(64, block, 4, 0, 0, 1)
+        okv = tb.tq_quantize_kv(L, kv)
+        ok = tb.tq_quantize_kv(L, k)
+        ov = tb.tq_quantize_kv(L, v)
+
+        def stacked():
+            tb.tq_quantize_kv(L, kv, out=okv)
+
+        def two():
+            tb.tq_quantize_kv(L, k, out=ok)
+            tb.tq_quantize_kv(L, v, out=ov)
+
+        ms, graphed = graph_ms(stacked)
+        ms_eager = timed(stacked)
+        ms2, _ = graph_ms(two)
+        ms2_eager = timed(two)
         bytes_per_vec = 64 * 2 + 64 * 4 // 8 + 2 * (64 // block)
         gbs = n_vec * bytes_per_vec / (ms * 1e-3) / 1e9
+        gbs2 = n_vec * bytes_per_vec / (ms2 * 1e-3) / 1e9
         # relative reconstruction error sum ||x - x~||^2 / sum ||x||^2 over K and V
-        num = den = 0.0
-        for x, o in ((k, ok), (v, ov)):
-            xr = tb.tq_dequantize_kv(o, torch.float32)
-            xf = x.float()
-            num += float(((xr - xf) ** 2).sum())
-            den += float((xf ** 2).sum())
-            del xr, xf
+        xr = tb.tq_dequantize_kv(okv, torch.float32)
+        xf = kv.float()
+        rel = float(((xr - xf) ** 2).sum()) / float((xf ** 2).sum())
+        del xr, xf
         res[name] = {"gvec_per_s": round(n_vec / (ms * 1e-3) / 1e9, 3), "ms": round(ms, 5),
-                     "relative_sq_error": round(num / den, 5),
+                     "ms_eager": round(ms_eager, 5), "cuda_graph": graphed, "launches_per_step": 1,
+                     "relative_sq_error": round(rel, 5),
                      "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
-                                  "frac": round(gbs / peak, 4), "bytes_per_vector": bytes_per_vec}}
+                                  "frac": round(gbs / peak, 4), "bytes_per_vector": bytes_per_vec},
+                     "two_calls": {"ms": round(ms2, 5), "ms_eager": round(ms2_eager, 5), "launches_per_step": 2,
+                                   "achieved_gbs": round(gbs2, 1), "frac": round(gbs2 / peak, 4)}}
     return res
 
 

@@ -371,7 +371,12 @@ int quantize_common(const tq_layout* layout, const void* x, tq_dtype x_dtype, in
   if (P.bits == 8 && make_codebook8(layout, &cb8) != TQ_OK) return TQ_ERR_UNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool f32 = x_dtype == TQ_F32;
-  if (quantize_fast_eligible(P, f32)) return launch_quantize_fast(P, x, n_vec, x_row_stride, codes, scales, map, s);
+  if (quantize_fast_eligible(P, f32)) {
+    // TQ_ERR_UNSUPPORTED: the input cannot be described to the tensor-memory
+    // loads (e.g. 2^32 rows or more); the general kernel takes it
+    const int fst = launch_quantize_fast(P, x, n_vec, x_row_stride, codes, scales, map, s);
+    if (fst != TQ_ERR_UNSUPPORTED) return fst;
+  }
   if (quantize_qjl_eligible(P))
     return launch_quantize_qjl(P, x, f32, n_vec, x_row_stride, S, codes, scales, qjl_bits, qjl_rnorm, map, s);
   switch (P.d) {

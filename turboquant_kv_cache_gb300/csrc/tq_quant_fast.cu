@@ -1,29 +1,62 @@
 // Fast quantise path: fp16 input, rotation block of 32 or 64, 2-4 bits, no
 // QJL, no norm correction (those layouts use the general kernel).
 //
-// One thread owns one (vector, block): the whole block sits in registers, so
-// the Walsh-Hadamard butterflies need no shuffles.  A warp takes 32 vectors
-// at one block index j, so the sign pattern D_j is the same for every lane.
-// Rows arrive through a per-warp double buffer filled by 16-byte cp.async
-// (coalesced), stored with an XOR swizzle so the per-thread 16-byte reads
-// are free of bank conflicts.
+// A CTA quantises a contiguous range of tiles of 128 vectors x one rotation
+// block.  The rotation of a tile is one small dense product on the tensor
+// cores,
+//   Y = X B,  B[k][n] = D_k H[n][k]  (entries +-1, exact in fp16),
+// tcgen05.mma (M = 128 vectors, N = K = block) with the fp16 input tile and
+// B in shared memory and the fp32 result in TMEM: the products are exact and
+// the sums fp32, as in a scalar transform.  One consumer thread owns one
+// vector (its TMEM lane), so the norm, the codes and the packed words of a
+// vector never leave the thread.
 //
-// Bucketize: code = #{k : y > beta_k}.  With a = |y| scaled by 2^20 / beta
-// units, each positive boundary contributes sat(a*A - B_k) (an exact 0/1
-// step except within 2^-20 of the boundary, far inside the 1e-5 tie band);
-// the sign picks the half of the codebook.  The code is turned into an
-// integer by adding 1.5*2^23 (round to nearest) and packed with integer
-// multiply-adds.
+// Roles: a producer thread loads input tiles with TMA (one 128-row box per
+// tile, rows past the end zero-filled, 128- or 64-byte swizzled rows, the
+// layout the MMA reads) four stages deep, an MMA warp issues the products
+// into four TMEM accumulators, and two groups of four consumer warps take
+// turns on the finished ones.  They meet only on mbarriers.  The producer
+// issues the first loads before the CTA's set-up (B, the cell table, TMEM),
+// and the kernel is launched as a programmatic dependent of the previous one
+// in the stream, so both the set-up and the launch overlap other work.
+//
+// Bucketize, code = #{k : y > beta_k}: with s = sat(y / (2R ||y||) + 1/2)
+// in [0, 1], round(s*C) picks one of C+1 cells that hold at most one
+// boundary each (rounding is monotone, so every boundary in a lower cell is
+// below s and every one in a higher cell above it).  A cell entry holds that
+// boundary in s units with the count of boundaries below the cell in its low
+// four mantissa bits (a shift of at most 15 ulp, far inside the 1e-5 tie
+// band); code = count + (s > boundary).  The table is replicated per lane so
+// the lookup has no bank conflicts.
+//
+// Every mbarrier wait is bounded: on expiry the CTA stops, frees its TMEM and
+// records TQ_ERR_TIMEOUT in this file's device status word.
+#include <cuda.h>
 #include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
 
 #include "tq_device.cuh"
 
 namespace tq {
 namespace {
 
-constexpr int kFW = 4;            // warps per CTA
-constexpr float kStepScale = 1048576.0f;   // 2^20
-constexpr float kMagic = 12582912.0f;      // 1.5 * 2^23
+// consumer warps: two groups of four, group g takes the CTA's tiles i with
+// i % 2 == g; in a group, one vector per thread (one TMEM lane each)
+constexpr int kConsumers = 8;
+constexpr int kThreads = 32 * (kConsumers + 2);   // + a producer warp and an MMA warp
+constexpr int kStages = 4;                  // input stages
+constexpr int kAcc = 4;                     // TMEM accumulators (two per consumer group)
+constexpr float kMagic = 12582912.0f;       // 1.5 * 2^23
+constexpr int kMaxCells = 64;
+constexpr uint32_t kSuspendNs = 100000;     // try_wait sleep hint
+constexpr uint64_t kWaitNs = 2000000000ull; // give up a wait after 2 s
+constexpr unsigned kPollNs = 128;           // sleep between polls of an mbarrier
+
+// first failure status of a quantise launch since the last read (0 = none)
+__device__ int g_quant_status;
 
 struct FastQuantArgs {
   const __half* x;
@@ -32,200 +65,525 @@ struct FastQuantArgs {
   uint32_t* codes;  // [records][words per vector]
   uint16_t* scales;
   RowMap map;       // vector -> record
-  float bstep[8];   // 2^20 * positive boundaries beta_{K/2} .. beta_{K-2}
-  uint32_t sgn[128];  // fp16x2 +-1 multipliers of D, pairs (2i, 2i+1)
+  int64_t n_tiles;  // ceil(n_vec / 128) * nb
+  int64_t per_cta;  // tiles of each CTA (a contiguous range)
+  int n_cells;      // C
+  float inv2r;      // 1 / (2R), R beyond the outermost boundary
+  uint32_t cell[kMaxCells + 1];
 };
 
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+__device__ __forceinline__ uint32_t su32(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
+
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
 }
 
-__device__ __forceinline__ void cp_async16(void* dst, const void* src, int bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(smem_u32(dst)), "l"(src), "r"(bytes));
+// TMA: the 2-D box at (x, y) of a tensor map into shared memory, completing
+// on an mbarrier
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];\n" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes) : "memory");
 }
 
-template <int BLK>
-__device__ __forceinline__ int swz(int item, int k) {
-  return BLK == 64 ? (k ^ (item & 7)) : (k ^ ((item >> 1) & 3));
+// byte offset of element (row, col) in a core-matrix tile of `cols` columns:
+// core matrix (row/8, col/8) at ((row/8) * (cols/8) + col/8) * 128, row-major
+// 8 x 16 bytes inside
+__host__ __device__ __forceinline__ uint32_t cm_off(int row, int col, int cols) {
+  return (uint32_t)(((row >> 3) * (cols >> 3) + (col >> 3)) * 128 + (row & 7) * 16 + (col & 7) * 2);
 }
 
-template <int BLK, int BITS>
-__global__ void __launch_bounds__(kFW * 32) quantize_fast_kernel(const CodecParams P, const FastQuantArgs a) {
-  constexpr int CPI = BLK / 8;               // 16-byte chunks per item
-  constexpr int TILE_BYTES = 32 * BLK * 2;
-  constexpr int HALF_K = (1 << BITS) / 2;    // codes per half of the codebook
-  constexpr int WPB = BLK * BITS / 32;       // packed words per block
-  __shared__ __align__(128) uint8_t s_buf[kFW][2][TILE_BYTES];
+// shared-memory matrix descriptor, no swizzle: lbo = byte step between core
+// matrices along K, sbo = along M / N
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | ((uint64_t)1 << 46);
+}
 
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  const int nb = P.nb;
-  const int64_t vec_tiles = (a.n_vec + 31) / 32;
-  const int64_t n_tiles = vec_tiles * nb;
-  const int64_t gw = (int64_t)blockIdx.x * kFW + wid;
-  const int64_t stride_w = (int64_t)gridDim.x * kFW;
-  const int words_per_vec = P.code_bytes / 4;
+// descriptor of a K-major operand whose rows are `row_bytes` (128 or 64)
+// long, 16-byte chunks swizzled within each 8-row atom (128B / 64B modes);
+// the atom stride is 8 rows
+__device__ __forceinline__ uint64_t sdesc_swz(uint32_t saddr, int row_bytes) {
+  const uint64_t mode = row_bytes == 128 ? 2 : 4;
+  return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)1 << 16) | ((uint64_t)((8 * row_bytes) >> 4) << 32) |
+         ((uint64_t)1 << 46) | (mode << 61);
+}
 
-  auto issue = [&](int64_t tile, int buf) {
-    const int j = (int)(tile % nb);
-    const int64_t v0 = (tile / nb) * 32;
-    uint8_t* dst = s_buf[wid][buf];
-#pragma unroll
-    for (int r = 0; r < CPI; ++r) {
-      const int c = lane + 32 * r;
-      const int item = c / CPI, k = c % CPI;
-      const int64_t v = v0 + item;
-      const bool ok = v < a.n_vec;
-      const __half* src = ok ? a.x + v * a.stride + (int64_t)j * BLK + k * 8 : a.x;
-      cp_async16(dst + item * BLK * 2 + swz<BLK>(item, k) * 16, src, ok ? 16 : 0);
-    }
-    asm volatile("cp.async.commit_group;\n" ::);
-  };
+// warp-wide: the lane elect.sync picks issues the MMA / the commit, so an MMA
+// and the commit that tracks it come from one thread
+__device__ __forceinline__ void mma_ss_elect(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, int acc) {
+  asm volatile(
+      "{\n .reg .pred p, e;\n elect.sync _|e, 0xffffffff;\n setp.ne.b32 p, %4, 0;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void commit_elect(uint32_t bar) {
+  asm volatile(
+      "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
+      " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
+__device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory"); }
+// generic-proxy writes to shared memory (stores, cp.async) before the tensor
+// cores read them
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
 
-  int64_t tile = gw;
-  int buf = 0;
-  if (tile < n_tiles) issue(tile, 0);
-  for (; tile < n_tiles; tile += stride_w, buf ^= 1) {
-    const int64_t nx = tile + stride_w;
-    if (nx < n_tiles) {
-      issue(nx, buf ^ 1);
-      asm volatile("cp.async.wait_group 1;\n" ::);
-    } else {
-      asm volatile("cp.async.wait_group 0;\n" ::);
-    }
-    __syncwarp();
-    const int j = (int)(tile % nb);
-    const int64_t v = (tile / nb) * 32 + lane;
-    const uint8_t* src = s_buf[wid][buf] + lane * BLK * 2;
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
 
-    // load, apply D, widen to fp32 pairs (2i, 2i+1)
-    float2 x[BLK / 2];
-    float2 ss2 = make_float2(0.f, 0.f);
-#pragma unroll
-    for (int k = 0; k < CPI; ++k) {
-      const uint4 u = *reinterpret_cast<const uint4*>(src + swz<BLK>(lane, k) * 16);
-      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const uint32_t sg = a.sgn[(j * BLK) / 2 + 4 * k + e];
-        const __half2 h = __hmul2(*reinterpret_cast<const __half2*>(&w[e]), *reinterpret_cast<const __half2*>(&sg));
-        x[4 * k + e] = __half22float2(h);
-        ss2 = __ffma2_rn(x[4 * k + e], x[4 * k + e], ss2);
-      }
+// Wait for phase `parity` of an mbarrier, bounded by kWaitNs of wall time.
+// Callers combine the lanes' results with __all_sync, so a warp takes one
+// decision even when its lanes time out at different moments.
+__device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity) {
+  uint32_t done = 0;
+  uint64_t t0 = 0;
+  for (int it = 0;; ++it) {
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(bar), "r"(parity), "r"(kSuspendNs)
+        : "memory");
+    if (done) return true;
+    if (it == 0) {
+      t0 = global_ns();
+    } else if (global_ns() - t0 > kWaitNs) {
+      return false;
     }
-    __syncwarp();   // the buffer is refilled two tiles later
-    // unnormalised Walsh-Hadamard transform: stride 1 inside each pair, the
-    // wider strides on whole pairs with packed fp32x2 adds
-#pragma unroll
-    for (int i = 0; i < BLK / 2; ++i) {
-      const float p = x[i].x, q = x[i].y;
-      x[i] = make_float2(p + q, p - q);
-    }
-    const float2 neg1 = make_float2(-1.f, -1.f);
-#pragma unroll
-    for (int h = 1; h < BLK / 2; h <<= 1) {
-#pragma unroll
-      for (int i = 0; i < BLK / 2; ++i) {
-        if ((i & h) == 0) {
-          const float2 p = x[i], q = x[i + h];
-          x[i] = __fadd2_rn(p, q);
-          x[i + h] = __ffma2_rn(q, neg1, p);
-        }
-      }
-    }
-    const float n = sqrtf(ss2.x + ss2.y);
-    // a*A - B_k with A = 2^20 / (n sqrt(blk)): |y| > beta_k  <=>  step = 1
-    const float A = n > 0.f ? kStepScale / (n * sqrtf((float)BLK)) : 0.f;
-    const float2 base2 = make_float2((float)HALF_K - 0.5f, (float)HALF_K - 0.5f);
-    const float2 magic2 = make_float2(kMagic, kMagic);
-    // integer of the magic-shifted code is (bits - magic bits); the magic part
-    // of all 8 nibbles is removed once per chunk
-    const uint32_t magic_all = __float_as_uint(kMagic) * 0x11111111u;
-    uint32_t words[WPB];
-    uint32_t nib[BLK / 8];
-#pragma unroll
-    for (int c = 0; c < BLK / 8; ++c) {
-      uint32_t acc = 0u - magic_all;
-#pragma unroll
-      for (int r2 = 0; r2 < 4; ++r2) {
-        const float2 y = x[4 * c + r2];
-        const float ay0 = fabsf(y.x), ay1 = fabsf(y.y);
-        float2 cnt = make_float2(0.5f, 0.5f);
-#pragma unroll
-        for (int kk = 0; kk < HALF_K - 1; ++kk)
-          cnt = __fadd2_rn(cnt, make_float2(__saturatef(fmaf(ay0, A, -a.bstep[kk])),
-                                            __saturatef(fmaf(ay1, A, -a.bstep[kk]))));
-        // code = HALF_K - 1 - cnt + 0.5 (y <= 0) or HALF_K - 0.5 + cnt (y > 0)
-        const float2 sc = make_float2(copysignf(cnt.x, y.x), copysignf(cnt.y, y.y));
-        // small exact sum first; adding 1.5*2^23 then rounds it to an integer
-        const float2 codef = __fadd2_rn(__fadd2_rn(base2, sc), magic2);
-        acc += __float_as_uint(codef.x) << (8 * r2);
-        acc += __float_as_uint(codef.y) << (8 * r2 + 4);
-      }
-      nib[c] = n > 0.f ? acc : (uint32_t)(HALF_K - 1) * 0x11111111u;
-    }
-    // pack nibble chunks into the layout's words
-#pragma unroll
-    for (int gi = 0; gi < BLK / 32; ++gi) {
-      const uint32_t* N = nib + 4 * gi;
-      if (BITS == 4) {
-#pragma unroll
-        for (int w = 0; w < 4; ++w) words[4 * gi + w] = N[w];
-      } else if (BITS == 3) {
-#pragma unroll
-        for (int w = 0; w < 3; ++w) words[3 * gi + w] = N[w] | (((N[3] >> w) & 0x11111111u) << 3);
-      } else {
-#pragma unroll
-        for (int w = 0; w < 2; ++w) words[2 * gi + w] = N[w] | (N[w + 2] << 2);
-      }
-    }
-    const int64_t r = v < a.n_vec ? map_row(a.map, v) : -1;
-    if (r >= 0) {
-      uint32_t* dst = a.codes + r * words_per_vec + j * WPB;
-#pragma unroll
-      for (int w = 0; w < WPB; ++w) dst[w] = words[w];
-      a.scales[r * nb + j] = f2h(n);
-    }
+    __nanosleep(kPollNs);   // leave the issue slots to the warps that have work
   }
 }
 
+#define TQ_LD32(taddr, v)                                                                                          \
+  asm volatile(                                                                                                    \
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"  \
+      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"                                             \
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),            \
+        "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),      \
+        "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),    \
+        "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])     \
+      : "r"(taddr))
+
+// w += inc when s > the boundary held in entry e (as a float)
+__device__ __forceinline__ void add_if_gt(uint32_t& w, float s, uint32_t e, uint32_t inc) {
+  asm("{\n .reg .pred p;\n setp.gt.f32 p, %1, %2;\n @p add.u32 %0, %0, %3;\n}"
+      : "+r"(w)
+      : "f"(s), "f"(__uint_as_float(e)), "r"(inc));
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
 template <int BLK, int BITS>
-int launch_fast(const CodecParams& P, const FastQuantArgs& a, cudaStream_t st) {
-  int dev = 0, sms = 152;
-  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int64_t tiles = (a.n_vec + 31) / 32 * P.nb;
-  int64_t blocks = (tiles + kFW - 1) / kFW;
-  const int64_t cap = (int64_t)sms * 8;
-  if (blocks > cap) blocks = cap;
-  quantize_fast_kernel<BLK, BITS><<<(int)(blocks > 0 ? blocks : 1), kFW * 32, 0, st>>>(P, a);
+__global__ void __launch_bounds__(kThreads, 2) quantize_tc_kernel(const CodecParams P, const FastQuantArgs a,
+                                                                   const __grid_constant__ CUtensorMap xmap) {
+  constexpr int CPR = BLK / 8;              // 16-byte chunks per row
+  constexpr int STAGE = 128 * BLK * 2;      // bytes of one input tile
+  constexpr uint32_t kCols = kAcc * BLK;    // kAcc fp32 accumulators of BLK columns
+  constexpr int WPB = BLK * BITS / 32;      // packed words per block
+  // f32 accumulate, f16 A and B, both K-major, N = BLK, M = 128
+  constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(BLK >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // full: stage s loaded (TMA bytes); empty: its product read it;
+  // tfull: accumulator b written; tempty: accumulator b read (4 warps)
+  __shared__ __align__(8) uint64_t s_full[kStages], s_empty[kStages], s_tfull[kAcc], s_tempty[kAcc];
+  __shared__ uint32_t s_tmem;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nb = P.nb;
+  // swizzled tiles want 1024-byte alignment (the launch adds the slack)
+  uint8_t* smem = smem_raw + ((1024u - (su32(smem_raw) & 1023u)) & 1023u);
+  uint8_t* s_x = smem;                                           // [kStages][128 rows x BLK] swizzled rows
+  uint8_t* s_b = smem + kStages * STAGE;                         // [nb][BLK n x BLK k] core matrices
+  uint32_t* s_cell = reinterpret_cast<uint32_t*>(s_b + (size_t)nb * BLK * BLK * 2);   // [C + 1][32]
+
+  const int64_t t_begin = (int64_t)blockIdx.x * a.per_cta;
+  const int64_t t_end = imin64(t_begin + a.per_cta, a.n_tiles);
+  const int n = (int)(t_end > t_begin ? t_end - t_begin : 0);   // tiles of this CTA
+  const uint32_t xs = su32(s_x), bs = su32(s_b);
+  const bool producer = warp == kConsumers && lane == 0;
+  if (producer) {
+    // barriers first, then (once the kernels this one depends on are done)
+    // the first kStages tiles, so their loads overlap the set-up below
+#pragma unroll
+    for (int s = 0; s < kStages; ++s) {
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(su32(&s_full[s])) : "memory");
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(su32(&s_empty[s])) : "memory");
+    }
+#pragma unroll
+    for (int b = 0; b < kAcc; ++b) {
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(su32(&s_tfull[b])) : "memory");
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 4;\n" ::"r"(su32(&s_tempty[b])) : "memory");
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&xmap)) : "memory");
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
+    int64_t vg = t_begin / nb;
+    int j = (int)(t_begin - vg * nb);
+    for (int i = 0; i < n && i < kStages; ++i) {
+      arrive_expect_tx(su32(&s_full[i]), STAGE);
+      tma_load_2d(xs + i * STAGE, &xmap, j * BLK, (int)(vg * 128), su32(&s_full[i]));
+      if (++j == nb) { j = 0; ++vg; }
+    }
+  }
+  // B of every block j, stored as B^T (row n, column k): 8 k values per 16 bytes
+  for (int idx = tid; idx < nb * BLK * CPR; idx += kThreads) {
+    const int j = idx / (BLK * CPR);
+    const int rem = idx - j * (BLK * CPR);
+    const int n = rem / CPR, ch = rem % CPR;
+    uint32_t w[4];
+#pragma unroll
+    for (int e = 0; e < 8; e += 2) {
+      uint32_t h2 = 0;
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int k = 8 * ch + e + q;
+        const int c = j * BLK + k;
+        const uint32_t neg = (__popc(n & k) + (P.sign_bits[c >> 5] >> (c & 31))) & 1u;
+        h2 |= (neg ? 0xBC00u : 0x3C00u) << (16 * q);
+      }
+      w[e >> 1] = h2;
+    }
+    *reinterpret_cast<uint4*>(s_b + (size_t)j * BLK * BLK * 2 + cm_off(n, 8 * ch, BLK)) =
+        make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  for (int idx = tid; idx < (a.n_cells + 1) * 32; idx += kThreads) s_cell[idx] = a.cell[idx >> 5];
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(su32(&s_tmem)),
+                 "n"(kCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
+  }
+  fence_async_smem();   // B, written by ordinary stores
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = s_tmem;
+
+  // the next kernel in the stream may start its own set-up now
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+  int failed = 0;   // a wait of this thread gave up; its role stops
+
+  if (warp == kConsumers) {
+    // ================= producer (one thread): tile i >= kStages into stage
+    // i % kStages once the product of tile i - kStages has read it
+    if (lane == 0) {
+      int64_t vg = (t_begin + kStages) / nb;
+      int j = (int)(t_begin + kStages - vg * nb);
+      for (int i = kStages; i < n; ++i) {
+        const int s = i % kStages;
+        if (!bar_wait(su32(&s_empty[s]), (uint32_t)(i / kStages - 1) & 1)) {
+          failed = 1;
+          break;
+        }
+        arrive_expect_tx(su32(&s_full[s]), STAGE);
+        tma_load_2d(xs + s * STAGE, &xmap, j * BLK, (int)(vg * 128), su32(&s_full[s]));
+        if (++j == nb) { j = 0; ++vg; }
+      }
+    }
+    __syncwarp();
+  } else if (warp == kConsumers + 1) {
+    // ================= MMA: Y(b) = X(stage) B_j once the stage has landed
+    // and accumulator b has been read
+    int j = (int)(t_begin % nb);
+    for (int i = 0; i < n; ++i) {
+      const int s = i % kStages, b = i % kAcc;
+      const bool ok = bar_wait(su32(&s_full[s]), (uint32_t)(i / kStages) & 1) &&
+                      (i < kAcc || bar_wait(su32(&s_tempty[b]), (uint32_t)(i / kAcc - 1) & 1));
+      if (!__all_sync(kFull, ok)) {
+        failed = 1;
+        break;
+      }
+      fence_after();
+      __syncwarp();
+      const uint64_t da = sdesc_swz(xs + s * STAGE, BLK * 2);
+      const uint64_t db = sdesc(bs + (uint32_t)(j * BLK * BLK * 2), 128, BLK * 16);
+#pragma unroll
+      // K step k: 32 bytes further along the swizzled A rows, two core
+      // matrices further along B
+      for (int k = 0; k < BLK / 16; ++k) mma_ss_elect(tmem + b * BLK, da + 2 * k, db + 16 * k, kIdesc, k > 0);
+      commit_elect(su32(&s_empty[s]));
+      commit_elect(su32(&s_tfull[b]));
+      if (++j == nb) j = 0;
+    }
+  } else {
+    // ================= consumers: one vector per thread (TMEM lane
+    // 32 (warp % 4) + lane, columns = coordinates)
+    const int words_per_vec = P.code_bytes / 4;
+    const float2 cells2 = make_float2((float)a.n_cells, (float)a.n_cells);
+    const float2 magic2 = make_float2(kMagic, kMagic);
+    // cell c of this lane's copy at s_cell + 4 (32 c + lane); the magic bits
+    // of round(s C) + 1.5 * 2^23 are folded into the base (mod 2^32)
+    const uint32_t cell_base = su32(s_cell) + 4u * lane - (__float_as_uint(kMagic) << 7);
+    const int grp = warp >> 2, wq = warp & 3;   // group, quarter of the TMEM lanes
+    int64_t vg = (t_begin + grp) / nb;
+    int j = (int)(t_begin + grp - vg * nb);
+    for (int i = grp; i < n; i += 2) {
+      const int b = i % kAcc;
+      if (!__all_sync(kFull, bar_wait(su32(&s_tfull[b]), (uint32_t)(i / kAcc) & 1))) {
+        failed = 1;
+        break;
+      }
+      fence_after();
+      const uint32_t taddr = tmem + ((uint32_t)(32 * wq) << 16) + (uint32_t)(b * BLK);
+      // pass 1: ||y||^2 = BLK ||x||^2
+      float2 s2 = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int c0 = 0; c0 < BLK; c0 += 32) {
+        uint32_t v[32];
+        TQ_LD32(taddr + c0, v);
+        asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+#pragma unroll
+        for (int c = 0; c < 32; c += 2)
+          s2 = __ffma2_rn(make_float2(__uint_as_float(v[c]), __uint_as_float(v[c + 1])),
+                          make_float2(__uint_as_float(v[c]), __uint_as_float(v[c + 1])), s2);
+      }
+      const float ss = s2.x + s2.y;
+      const float A1 = ss > 0.f ? a.inv2r * rsqrtf(ss) : 0.f;
+      // pass 2, 32 coordinates at a time: nibble word c holds the codes of
+      // coordinates 8c .. 8c+7; a coordinate pair forms one byte, inserted
+      // with a byte permute
+      uint32_t N[BLK / 8];
+#pragma unroll
+      for (int c0 = 0; c0 < BLK; c0 += 32) {
+        uint32_t v[32];
+        TQ_LD32(taddr + c0, v);
+        asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t w = 0;
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            const float y0 = __uint_as_float(v[8 * cc + 2 * m]), y1 = __uint_as_float(v[8 * cc + 2 * m + 1]);
+            const float2 s = make_float2(__saturatef(fmaf(y0, A1, 0.5f)), __saturatef(fmaf(y1, A1, 0.5f)));
+            const float2 u = __ffma2_rn(s, cells2, magic2);
+            const uint32_t e0 = lds32(cell_base + (__float_as_uint(u.x) << 7));
+            const uint32_t e1 = lds32(cell_base + (__float_as_uint(u.y) << 7));
+            // low byte: count of e0 | count of e1 << 4 (higher bytes are dropped)
+            const uint32_t pair = (e0 & 0x0Fu) | ((e1 << 4) & ~0x0Fu);
+            w = prmt(w, pair, m == 0 ? 0x3214u : m == 1 ? 0x3240u : m == 2 ? 0x3410u : 0x4210u);
+            add_if_gt(w, s.x, e0, 1u << (8 * m));
+            add_if_gt(w, s.y, e1, 1u << (8 * m + 4));
+          }
+          N[c0 / 8 + cc] = w;
+        }
+      }
+      fence_before();
+      __syncwarp();
+      if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(su32(&s_tempty[b])) : "memory");
+      // packed words of the block (32-code groups of four nibble words)
+      uint32_t W[WPB];
+#pragma unroll
+      for (int gi = 0; gi < BLK / 32; ++gi) {
+        const uint32_t* G = N + 4 * gi;
+        if (BITS == 4) {
+#pragma unroll
+          for (int w = 0; w < 4; ++w) W[4 * gi + w] = G[w];
+        } else if (BITS == 3) {
+#pragma unroll
+          for (int w = 0; w < 3; ++w) W[3 * gi + w] = G[w] | (((G[3] >> w) & 0x11111111u) << 3);
+        } else {
+#pragma unroll
+          for (int w = 0; w < 2; ++w) W[2 * gi + w] = G[w] | (G[w + 2] << 2);
+        }
+      }
+      const int64_t v = vg * 128 + 32 * wq + lane;
+      const int64_t r = v < a.n_vec ? map_row(a.map, v) : -1;
+      if (r >= 0) {
+        uint32_t* dst = a.codes + r * words_per_vec + j * WPB;
+        // widest store the record and block alignment allow
+        if (WPB % 4 == 0 && words_per_vec % 4 == 0) {
+#pragma unroll
+          for (int w = 0; w < WPB; w += 4)
+            *reinterpret_cast<uint4*>(dst + w) = make_uint4(W[w], W[w + 1], W[w + 2], W[w + 3]);
+        } else if (WPB % 2 == 0 && words_per_vec % 2 == 0) {
+#pragma unroll
+          for (int w = 0; w < WPB; w += 2) *reinterpret_cast<uint2*>(dst + w) = make_uint2(W[w], W[w + 1]);
+        } else {
+#pragma unroll
+          for (int w = 0; w < WPB; ++w) dst[w] = W[w];
+        }
+        a.scales[r * nb + j] = f2h(sqrtf(ss * (1.0f / BLK)));
+      }
+      j += 2;   // the group's next tile
+      while (j >= nb) { j -= nb; ++vg; }
+    }
+  }
+  if (failed) atomicCAS(&g_quant_status, 0, (int)TQ_ERR_TIMEOUT);
+  fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "n"(kCols) : "memory");
+  }
+}
+
+// The cell table of a codebook (see the file comment); false when no
+// C <= kMaxCells separates the boundaries.
+bool make_cells(const CodecParams& P, FastQuantArgs* a) {
+  const int K = 1 << P.bits;
+  float bmax = 0.f;
+  for (int k = 0; k < K - 1; ++k) bmax = std::fmax(bmax, std::fabs(P.bounds[k]));
+  if (!(bmax > 0.f) || !std::isfinite(bmax)) return false;
+  a->inv2r = 0.5f / (bmax * 1.0625f);
+  float sig[16];
+  for (int k = 0; k < K - 1; ++k) sig[k] = std::fmaf(P.bounds[k], a->inv2r, 0.5f);
+  for (int C = 16; C <= kMaxCells; C *= 2) {
+    int cellk[16];
+    bool ok = true;
+    for (int k = 0; k < K - 1; ++k) {
+      cellk[k] = (int)std::nearbyintf(sig[k] * (float)C);
+      if (k > 0 && cellk[k] <= cellk[k - 1]) ok = false;
+    }
+    if (!ok) continue;
+    a->n_cells = C;
+    for (int c = 0; c <= C; ++c) {
+      uint32_t below = 0;
+      float bnd = 2.0f;
+      for (int k = 0; k < K - 1; ++k) {
+        if (cellk[k] < c) ++below;
+        if (cellk[k] == c) bnd = sig[k];
+      }
+      uint32_t bits;
+      std::memcpy(&bits, &bnd, 4);
+      a->cell[c] = (bits & ~15u) | below;
+    }
+    return true;
+  }
+  return false;
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// cuTensorMapEncodeTiled from the driver (a host-only encoding call)
+EncodeTiledFn encode_tiled() {
+  static EncodeTiledFn fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+
+// Tensor map of the input rows: [n_vec][d] fp16, rows `stride` elements
+// apart, read in boxes of 128 rows x BLK columns with the swizzle the MMA's
+// A descriptor names; rows past n_vec read as zero.
+template <int BLK>
+bool make_xmap(const FastQuantArgs& a, int d, CUtensorMap* map) {
+  const EncodeTiledFn fn = encode_tiled();
+  if (!fn || a.n_vec >= ((int64_t)1 << 31) - 128) return false;   // row coordinates are 32-bit
+  const cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)a.n_vec};
+  const cuuint64_t strides[1] = {(cuuint64_t)a.stride * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)BLK, 128u};
+  const cuuint32_t estr[2] = {1u, 1u};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half*>(a.x), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, BLK == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Launch shape of one kernel instantiation on one device, worked out once.
+struct LaunchShape {
+  bool ready = false;
+  int sms = 0, occ = 0;
+  size_t smem = 0;
+};
+
+template <int BLK, int BITS>
+int launch_fast(const CodecParams& P, FastQuantArgs& a, cudaStream_t st) {
+  static std::mutex mu;
+  static LaunchShape shapes[64][5];   // [device][nb - 1 for nb = 1, 2, 4, 8 -> index by log2]
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return TQ_ERR_CUDA;
+  int lg = 0;
+  while ((1 << lg) < P.nb && lg < 4) ++lg;
+  auto kern = quantize_tc_kernel<BLK, BITS>;
+  LaunchShape sh;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    LaunchShape& c = shapes[dev][lg];
+    if (!c.ready) {
+      int sms = 0, smem_sm = 0, smem_blk_res = 0;
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+      cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+      cudaDeviceGetAttribute(&smem_blk_res, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+      // stages (+ 1024 bytes of alignment slack), B of every block, cell table
+      const size_t smem = 1024 + (size_t)kStages * 128 * BLK * 2 + (size_t)P.nb * BLK * BLK * 2 +
+                          (size_t)(kMaxCells + 1) * 32 * 4;
+      cudaFuncAttributes fa;
+      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
+          cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess ||
+          cudaFuncGetAttributes(&fa, kern) != cudaSuccess)
+        return TQ_ERR_CUDA;
+      // CTAs per SM: shared memory, registers, and TMEM (kAcc * BLK of 512 columns)
+      int occ = (int)((size_t)smem_sm / (smem + fa.sharedSizeBytes + (size_t)smem_blk_res));
+      const int by_regs = 65536 / (kThreads * (fa.numRegs > 0 ? fa.numRegs : 1));
+      occ = occ < by_regs ? occ : by_regs;
+      occ = occ < 512 / (kAcc * BLK) ? occ : 512 / (kAcc * BLK);
+      c.sms = sms > 0 ? sms : 1;
+      c.occ = occ > 0 ? occ : 1;
+      c.smem = smem;
+      c.ready = true;
+    }
+    sh = c;
+  }
+  CUtensorMap xmap;
+  if (!make_xmap<BLK>(a, P.d, &xmap)) return TQ_ERR_UNSUPPORTED;
+  a.n_tiles = (a.n_vec + 127) / 128 * P.nb;
+  // every CTA takes the same number of tiles, so no CTA runs a tail alone
+  const int64_t max_ctas = (int64_t)sh.sms * sh.occ;
+  a.per_cta = (a.n_tiles + max_ctas - 1) / max_ctas;
+  const int64_t blocks = (a.n_tiles + a.per_cta - 1) / a.per_cta;
+  // programmatic dependent launch: this kernel's set-up may overlap the tail
+  // of the previous kernel in the stream (its loads wait for that kernel)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = sh.smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, P, a, xmap) != cudaSuccess) return TQ_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }
 
 }  // namespace
 
 bool quantize_fast_eligible(const CodecParams& P, bool f32_input) {
-  return !f32_input && !P.m && !P.nc && (P.blk == 32 || P.blk == 64) && P.bits >= 2 && P.bits <= 4;
+  if (f32_input || P.m || P.nc || (P.blk != 32 && P.blk != 64) || P.bits < 2 || P.bits > 4) return false;
+  FastQuantArgs a;
+  return make_cells(P, &a);
 }
 
 int launch_quantize_fast(const CodecParams& P, const void* x, int64_t n_vec, int64_t stride, uint8_t* codes,
                          uint16_t* scales, const RowMap& map, cudaStream_t st) {
   FastQuantArgs a;
+  if (!make_cells(P, &a)) return TQ_ERR_UNSUPPORTED;
   a.map = map;
   a.x = static_cast<const __half*>(x);
   a.n_vec = n_vec;
   a.stride = stride;
   a.codes = reinterpret_cast<uint32_t*>(codes);
   a.scales = scales;
-  const int K = 1 << P.bits;
-  for (int k = 0; k < 8; ++k) a.bstep[k] = 0.f;
-  // positive boundaries beta_{K/2} .. beta_{K-2}, in units of the rotated
-  // unit vector, times 2^20
-  for (int k = K / 2; k < K - 1; ++k) a.bstep[k - K / 2] = P.bounds[k] * kStepScale;
-  for (int i = 0; i < 128; ++i) {
-    const int c0 = 2 * i, c1 = 2 * i + 1;
-    const uint16_t h0 = (c0 < P.d && ((P.sign_bits[c0 >> 5] >> (c0 & 31)) & 1u)) ? 0xBC00 : 0x3C00;
-    const uint16_t h1 = (c1 < P.d && ((P.sign_bits[c1 >> 5] >> (c1 & 31)) & 1u)) ? 0xBC00 : 0x3C00;
-    a.sgn[i] = (uint32_t)h0 | ((uint32_t)h1 << 16);
-  }
   if (P.blk == 64) {
     if (P.bits == 4) return launch_fast<64, 4>(P, a, st);
     if (P.bits == 3) return launch_fast<64, 3>(P, a, st);
@@ -234,6 +592,19 @@ int launch_quantize_fast(const CodecParams& P, const void* x, int64_t n_vec, int
   if (P.bits == 4) return launch_fast<32, 4>(P, a, st);
   if (P.bits == 3) return launch_fast<32, 3>(P, a, st);
   return launch_fast<32, 2>(P, a, st);
+}
+
+// First failure status a fast quantise launch recorded since the last call
+// with clear set (0 = none).  Synchronises with the device.
+int quantize_fast_status(bool clear, int* status) {
+  int s = 0;
+  if (cudaMemcpyFromSymbol(&s, g_quant_status, sizeof(int)) != cudaSuccess) return TQ_ERR_CUDA;
+  if (clear && s != 0) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_quant_status, &zero, sizeof(int)) != cudaSuccess) return TQ_ERR_CUDA;
+  }
+  *status = s;
+  return TQ_OK;
 }
 
 }  // namespace tq

@@ -43,12 +43,15 @@
 namespace tq {
 namespace {
 
-// consumer warps: two groups of four, group g takes the CTA's tiles i with
-// i % 2 == g; in a group, one vector per thread (one TMEM lane each)
-constexpr int kConsumers = 8;
+// One CTA per SM.  Consumer warps: kGroups groups of four, group g takes the
+// CTA's tiles i with i % kGroups == g; in a group, one vector per thread (one
+// TMEM lane each)
+constexpr int kGroups = 4;
+constexpr int kConsumers = 4 * kGroups;
 constexpr int kThreads = 32 * (kConsumers + 2);   // + a producer warp and an MMA warp
-constexpr int kStages = 4;                  // input stages
-constexpr int kAcc = 4;                     // TMEM accumulators (two per consumer group)
+constexpr int kTileCols = 64;               // input columns per tile: one or two rotation blocks
+constexpr int kStages = 10;                 // input stages (16 KB each)
+constexpr int kAcc = 2 * kGroups;           // TMEM accumulators of 64 columns (two per group, all 512)
 constexpr float kMagic = 12582912.0f;       // 1.5 * 2^23
 constexpr int kMaxCells = 64;
 constexpr uint32_t kSuspendNs = 100000;     // try_wait sleep hint
@@ -65,7 +68,7 @@ struct FastQuantArgs {
   uint32_t* codes;  // [records][words per vector]
   uint16_t* scales;
   RowMap map;       // vector -> record
-  int64_t n_tiles;  // ceil(n_vec / 128) * nb
+  int64_t n_tiles;  // ceil(n_vec / 128) * d / 64
   int64_t per_cta;  // tiles of each CTA (a contiguous range)
   int n_cells;      // C
   float inv2r;      // 1 / (2R), R beyond the outermost boundary
@@ -188,24 +191,26 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
 }
 
 template <int BLK, int BITS>
-__global__ void __launch_bounds__(kThreads, 2) quantize_tc_kernel(const CodecParams P, const FastQuantArgs a,
+__global__ void __launch_bounds__(kThreads, 1) quantize_tc_kernel(const CodecParams P, const FastQuantArgs a,
                                                                    const __grid_constant__ CUtensorMap xmap) {
-  constexpr int CPR = BLK / 8;              // 16-byte chunks per row
-  constexpr int STAGE = 128 * BLK * 2;      // bytes of one input tile
-  constexpr uint32_t kCols = kAcc * BLK;    // kAcc fp32 accumulators of BLK columns
+  constexpr int CPR = BLK / 8;              // 16-byte chunks per row of B
+  constexpr int BPT = kTileCols / BLK;      // rotation blocks per tile
+  constexpr int STAGE = 128 * kTileCols * 2;   // bytes of one input tile
+  constexpr uint32_t kCols = kAcc * kTileCols;  // TMEM columns: kAcc fp32 accumulators
   constexpr int WPB = BLK * BITS / 32;      // packed words per block
   // f32 accumulate, f16 A and B, both K-major, N = BLK, M = 128
   constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(BLK >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  // full: stage s loaded (TMA bytes); empty: its product read it;
+  // full: stage s loaded (TMA bytes); empty: its products read it;
   // tfull: accumulator b written; tempty: accumulator b read (4 warps)
   __shared__ __align__(8) uint64_t s_full[kStages], s_empty[kStages], s_tfull[kAcc], s_tempty[kAcc];
   __shared__ uint32_t s_tmem;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nb = P.nb;
+  const int tpg = nb / BPT;                 // tiles per 128-vector group
   // swizzled tiles want 1024-byte alignment (the launch adds the slack)
   uint8_t* smem = smem_raw + ((1024u - (su32(smem_raw) & 1023u)) & 1023u);
-  uint8_t* s_x = smem;                                           // [kStages][128 rows x BLK] swizzled rows
+  uint8_t* s_x = smem;                                           // [kStages][128 rows x 64 columns] swizzled
   uint8_t* s_b = smem + kStages * STAGE;                         // [nb][BLK n x BLK k] core matrices
   uint32_t* s_cell = reinterpret_cast<uint32_t*>(s_b + (size_t)nb * BLK * BLK * 2);   // [C + 1][32]
 
@@ -213,8 +218,7 @@ __global__ void __launch_bounds__(kThreads, 2) quantize_tc_kernel(const CodecPar
   const int64_t t_end = imin64(t_begin + a.per_cta, a.n_tiles);
   const int n = (int)(t_end > t_begin ? t_end - t_begin : 0);   // tiles of this CTA
   const uint32_t xs = su32(s_x), bs = su32(s_b);
-  const bool producer = warp == kConsumers && lane == 0;
-  if (producer) {
+  if (warp == kConsumers && lane == 0) {
     // barriers first, then (once the kernels this one depends on are done)
     // the first kStages tiles, so their loads overlap the set-up below
 #pragma unroll
@@ -230,19 +234,19 @@ __global__ void __launch_bounds__(kThreads, 2) quantize_tc_kernel(const CodecPar
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&xmap)) : "memory");
     asm volatile("griddepcontrol.wait;\n" ::: "memory");
-    int64_t vg = t_begin / nb;
-    int j = (int)(t_begin - vg * nb);
+    int64_t vg = t_begin / tpg;
+    int jt = (int)(t_begin - vg * tpg);
     for (int i = 0; i < n && i < kStages; ++i) {
       arrive_expect_tx(su32(&s_full[i]), STAGE);
-      tma_load_2d(xs + i * STAGE, &xmap, j * BLK, (int)(vg * 128), su32(&s_full[i]));
-      if (++j == nb) { j = 0; ++vg; }
+      tma_load_2d(xs + i * STAGE, &xmap, jt * kTileCols, (int)(vg * 128), su32(&s_full[i]));
+      if (++jt == tpg) { jt = 0; ++vg; }
     }
   }
   // B of every block j, stored as B^T (row n, column k): 8 k values per 16 bytes
   for (int idx = tid; idx < nb * BLK * CPR; idx += kThreads) {
     const int j = idx / (BLK * CPR);
     const int rem = idx - j * (BLK * CPR);
-    const int n = rem / CPR, ch = rem % CPR;
+    const int nn = rem / CPR, ch = rem % CPR;
     uint32_t w[4];
 #pragma unroll
     for (int e = 0; e < 8; e += 2) {
@@ -251,12 +255,12 @@ __global__ void __launch_bounds__(kThreads, 2) quantize_tc_kernel(const CodecPar
       for (int q = 0; q < 2; ++q) {
         const int k = 8 * ch + e + q;
         const int c = j * BLK + k;
-        const uint32_t neg = (__popc(n & k) + (P.sign_bits[c >> 5] >> (c & 31))) & 1u;
+        const uint32_t neg = (__popc(nn & k) + (P.sign_bits[c >> 5] >> (c & 31))) & 1u;
         h2 |= (neg ? 0xBC00u : 0x3C00u) << (16 * q);
       }
       w[e >> 1] = h2;
     }
-    *reinterpret_cast<uint4*>(s_b + (size_t)j * BLK * BLK * 2 + cm_off(n, 8 * ch, BLK)) =
+    *reinterpret_cast<uint4*>(s_b + (size_t)j * BLK * BLK * 2 + cm_off(nn, 8 * ch, BLK)) =
         make_uint4(w[0], w[1], w[2], w[3]);
   }
   for (int idx = tid; idx < (a.n_cells + 1) * 32; idx += kThreads) s_cell[idx] = a.cell[idx >> 5];
@@ -278,10 +282,10 @@ __global__ void __launch_bounds__(kThreads, 2) quantize_tc_kernel(const CodecPar
 
   if (warp == kConsumers) {
     // ================= producer (one thread): tile i >= kStages into stage
-    // i % kStages once the product of tile i - kStages has read it
+    // i % kStages once the products of tile i - kStages have read it
     if (lane == 0) {
-      int64_t vg = (t_begin + kStages) / nb;
-      int j = (int)(t_begin + kStages - vg * nb);
+      int64_t vg = (t_begin + kStages) / tpg;
+      int jt = (int)(t_begin + kStages - vg * tpg);
       for (int i = kStages; i < n; ++i) {
         const int s = i % kStages;
         if (!bar_wait(su32(&s_empty[s]), (uint32_t)(i / kStages - 1) & 1)) {
@@ -289,15 +293,16 @@ __global__ void __launch_bounds__(kThreads, 2) quantize_tc_kernel(const CodecPar
           break;
         }
         arrive_expect_tx(su32(&s_full[s]), STAGE);
-        tma_load_2d(xs + s * STAGE, &xmap, j * BLK, (int)(vg * 128), su32(&s_full[s]));
-        if (++j == nb) { j = 0; ++vg; }
+        tma_load_2d(xs + s * STAGE, &xmap, jt * kTileCols, (int)(vg * 128), su32(&s_full[s]));
+        if (++jt == tpg) { jt = 0; ++vg; }
       }
     }
     __syncwarp();
   } else if (warp == kConsumers + 1) {
-    // ================= MMA: Y(b) = X(stage) B_j once the stage has landed
-    // and accumulator b has been read
-    int j = (int)(t_begin % nb);
+    // ================= MMA: for each block jj of tile i, columns
+    // jj*BLK.. of accumulator b = X(stage, block jj) B_j, once the stage has
+    // landed and accumulator b has been read
+    int jt = (int)(t_begin % tpg);
     for (int i = 0; i < n; ++i) {
       const int s = i % kStages, b = i % kAcc;
       const bool ok = bar_wait(su32(&s_full[s]), (uint32_t)(i / kStages) & 1) &&
@@ -308,19 +313,23 @@ __global__ void __launch_bounds__(kThreads, 2) quantize_tc_kernel(const CodecPar
       }
       fence_after();
       __syncwarp();
-      const uint64_t da = sdesc_swz(xs + s * STAGE, BLK * 2);
-      const uint64_t db = sdesc(bs + (uint32_t)(j * BLK * BLK * 2), 128, BLK * 16);
+      const uint64_t da = sdesc_swz(xs + s * STAGE, kTileCols * 2);
 #pragma unroll
-      // K step k: 32 bytes further along the swizzled A rows, two core
-      // matrices further along B
-      for (int k = 0; k < BLK / 16; ++k) mma_ss_elect(tmem + b * BLK, da + 2 * k, db + 16 * k, kIdesc, k > 0);
+      for (int jj = 0; jj < BPT; ++jj) {
+        const uint64_t db = sdesc(bs + (uint32_t)((jt * BPT + jj) * BLK * BLK * 2), 128, BLK * 16);
+        // K step k: 32 bytes further along the swizzled A rows (block jj
+        // starts jj*BLK*2 bytes in), two core matrices further along B
+#pragma unroll
+        for (int k = 0; k < BLK / 16; ++k)
+          mma_ss_elect(tmem + b * kTileCols + jj * BLK, da + (jj * BLK * 2) / 16 + 2 * k, db + 16 * k, kIdesc, k > 0);
+      }
       commit_elect(su32(&s_empty[s]));
       commit_elect(su32(&s_tfull[b]));
-      if (++j == nb) j = 0;
+      if (++jt == tpg) jt = 0;
     }
   } else {
     // ================= consumers: one vector per thread (TMEM lane
-    // 32 (warp % 4) + lane, columns = coordinates)
+    // 32 (warp % 4) + lane, columns = coordinates of the tile)
     const int words_per_vec = P.code_bytes / 4;
     const float2 cells2 = make_float2((float)a.n_cells, (float)a.n_cells);
     const float2 magic2 = make_float2(kMagic, kMagic);
@@ -328,97 +337,102 @@ __global__ void __launch_bounds__(kThreads, 2) quantize_tc_kernel(const CodecPar
     // of round(s C) + 1.5 * 2^23 are folded into the base (mod 2^32)
     const uint32_t cell_base = su32(s_cell) + 4u * lane - (__float_as_uint(kMagic) << 7);
     const int grp = warp >> 2, wq = warp & 3;   // group, quarter of the TMEM lanes
-    int64_t vg = (t_begin + grp) / nb;
-    int j = (int)(t_begin + grp - vg * nb);
-    for (int i = grp; i < n; i += 2) {
+    int64_t vg = (t_begin + grp) / tpg;
+    int jt = (int)(t_begin + grp - vg * tpg);
+    for (int i = grp; i < n; i += kGroups) {
       const int b = i % kAcc;
       if (!__all_sync(kFull, bar_wait(su32(&s_tfull[b]), (uint32_t)(i / kAcc) & 1))) {
         failed = 1;
         break;
       }
       fence_after();
-      const uint32_t taddr = tmem + ((uint32_t)(32 * wq) << 16) + (uint32_t)(b * BLK);
-      // pass 1: ||y||^2 = BLK ||x||^2
-      float2 s2 = make_float2(0.f, 0.f);
+      const uint32_t taddr = tmem + ((uint32_t)(32 * wq) << 16) + (uint32_t)(b * kTileCols);
+      const int64_t v = vg * 128 + 32 * wq + lane;
+      const int64_t r = v < a.n_vec ? map_row(a.map, v) : -1;
 #pragma unroll
-      for (int c0 = 0; c0 < BLK; c0 += 32) {
-        uint32_t v[32];
-        TQ_LD32(taddr + c0, v);
-        asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+      for (int jj = 0; jj < BPT; ++jj) {
+        const int j = jt * BPT + jj;
+        const uint32_t tb = taddr + jj * BLK;
+        // pass 1: ||y||^2 = BLK ||x||^2 over the block's columns
+        float2 s2 = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int c = 0; c < 32; c += 2)
-          s2 = __ffma2_rn(make_float2(__uint_as_float(v[c]), __uint_as_float(v[c + 1])),
-                          make_float2(__uint_as_float(v[c]), __uint_as_float(v[c + 1])), s2);
-      }
-      const float ss = s2.x + s2.y;
-      const float A1 = ss > 0.f ? a.inv2r * rsqrtf(ss) : 0.f;
-      // pass 2, 32 coordinates at a time: nibble word c holds the codes of
-      // coordinates 8c .. 8c+7; a coordinate pair forms one byte, inserted
-      // with a byte permute
-      uint32_t N[BLK / 8];
+        for (int c0 = 0; c0 < BLK; c0 += 32) {
+          uint32_t vv[32];
+          TQ_LD32(tb + c0, vv);
+          asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
 #pragma unroll
-      for (int c0 = 0; c0 < BLK; c0 += 32) {
-        uint32_t v[32];
-        TQ_LD32(taddr + c0, v);
-        asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+          for (int c = 0; c < 32; c += 2)
+            s2 = __ffma2_rn(make_float2(__uint_as_float(vv[c]), __uint_as_float(vv[c + 1])),
+                            make_float2(__uint_as_float(vv[c]), __uint_as_float(vv[c + 1])), s2);
+        }
+        const float ss = s2.x + s2.y;
+        const float A1 = ss > 0.f ? a.inv2r * rsqrtf(ss) : 0.f;
+        // pass 2, 32 coordinates at a time: nibble word c holds the codes of
+        // coordinates 8c .. 8c+7; a coordinate pair forms one byte, inserted
+        // with a byte permute
+        uint32_t N[BLK / 8];
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          uint32_t w = 0;
+        for (int c0 = 0; c0 < BLK; c0 += 32) {
+          uint32_t vv[32];
+          TQ_LD32(tb + c0, vv);
+          asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
 #pragma unroll
-          for (int m = 0; m < 4; ++m) {
-            const float y0 = __uint_as_float(v[8 * cc + 2 * m]), y1 = __uint_as_float(v[8 * cc + 2 * m + 1]);
-            const float2 s = make_float2(__saturatef(fmaf(y0, A1, 0.5f)), __saturatef(fmaf(y1, A1, 0.5f)));
-            const float2 u = __ffma2_rn(s, cells2, magic2);
-            const uint32_t e0 = lds32(cell_base + (__float_as_uint(u.x) << 7));
-            const uint32_t e1 = lds32(cell_base + (__float_as_uint(u.y) << 7));
-            // low byte: count of e0 | count of e1 << 4 (higher bytes are dropped)
-            const uint32_t pair = (e0 & 0x0Fu) | ((e1 << 4) & ~0x0Fu);
-            w = prmt(w, pair, m == 0 ? 0x3214u : m == 1 ? 0x3240u : m == 2 ? 0x3410u : 0x4210u);
-            add_if_gt(w, s.x, e0, 1u << (8 * m));
-            add_if_gt(w, s.y, e1, 1u << (8 * m + 4));
+          for (int cc = 0; cc < 4; ++cc) {
+            uint32_t w = 0;
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+              const float y0 = __uint_as_float(vv[8 * cc + 2 * m]), y1 = __uint_as_float(vv[8 * cc + 2 * m + 1]);
+              const float2 s = make_float2(__saturatef(fmaf(y0, A1, 0.5f)), __saturatef(fmaf(y1, A1, 0.5f)));
+              const float2 u = __ffma2_rn(s, cells2, magic2);
+              const uint32_t e0 = lds32(cell_base + (__float_as_uint(u.x) << 7));
+              const uint32_t e1 = lds32(cell_base + (__float_as_uint(u.y) << 7));
+              // low byte: count of e0 | count of e1 << 4 (higher bytes are dropped)
+              const uint32_t pair = (e0 & 0x0Fu) | ((e1 << 4) & ~0x0Fu);
+              w = prmt(w, pair, m == 0 ? 0x3214u : m == 1 ? 0x3240u : m == 2 ? 0x3410u : 0x4210u);
+              add_if_gt(w, s.x, e0, 1u << (8 * m));
+              add_if_gt(w, s.y, e1, 1u << (8 * m + 4));
+            }
+            N[c0 / 8 + cc] = w;
           }
-          N[c0 / 8 + cc] = w;
+        }
+        // packed words of the block (32-code groups of four nibble words)
+        uint32_t W[WPB];
+#pragma unroll
+        for (int gi = 0; gi < BLK / 32; ++gi) {
+          const uint32_t* G = N + 4 * gi;
+          if (BITS == 4) {
+#pragma unroll
+            for (int w = 0; w < 4; ++w) W[4 * gi + w] = G[w];
+          } else if (BITS == 3) {
+#pragma unroll
+            for (int w = 0; w < 3; ++w) W[3 * gi + w] = G[w] | (((G[3] >> w) & 0x11111111u) << 3);
+          } else {
+#pragma unroll
+            for (int w = 0; w < 2; ++w) W[2 * gi + w] = G[w] | (G[w + 2] << 2);
+          }
+        }
+        if (r >= 0) {
+          uint32_t* dst = a.codes + r * words_per_vec + j * WPB;
+          // widest store the record and block alignment allow
+          if (WPB % 4 == 0 && words_per_vec % 4 == 0) {
+#pragma unroll
+            for (int w = 0; w < WPB; w += 4)
+              *reinterpret_cast<uint4*>(dst + w) = make_uint4(W[w], W[w + 1], W[w + 2], W[w + 3]);
+          } else if (WPB % 2 == 0 && words_per_vec % 2 == 0) {
+#pragma unroll
+            for (int w = 0; w < WPB; w += 2) *reinterpret_cast<uint2*>(dst + w) = make_uint2(W[w], W[w + 1]);
+          } else {
+#pragma unroll
+            for (int w = 0; w < WPB; ++w) dst[w] = W[w];
+          }
+          a.scales[r * nb + j] = f2h(sqrtf(ss * (1.0f / BLK)));
         }
       }
       fence_before();
       __syncwarp();
       if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(su32(&s_tempty[b])) : "memory");
-      // packed words of the block (32-code groups of four nibble words)
-      uint32_t W[WPB];
-#pragma unroll
-      for (int gi = 0; gi < BLK / 32; ++gi) {
-        const uint32_t* G = N + 4 * gi;
-        if (BITS == 4) {
-#pragma unroll
-          for (int w = 0; w < 4; ++w) W[4 * gi + w] = G[w];
-        } else if (BITS == 3) {
-#pragma unroll
-          for (int w = 0; w < 3; ++w) W[3 * gi + w] = G[w] | (((G[3] >> w) & 0x11111111u) << 3);
-        } else {
-#pragma unroll
-          for (int w = 0; w < 2; ++w) W[2 * gi + w] = G[w] | (G[w + 2] << 2);
-        }
-      }
-      const int64_t v = vg * 128 + 32 * wq + lane;
-      const int64_t r = v < a.n_vec ? map_row(a.map, v) : -1;
-      if (r >= 0) {
-        uint32_t* dst = a.codes + r * words_per_vec + j * WPB;
-        // widest store the record and block alignment allow
-        if (WPB % 4 == 0 && words_per_vec % 4 == 0) {
-#pragma unroll
-          for (int w = 0; w < WPB; w += 4)
-            *reinterpret_cast<uint4*>(dst + w) = make_uint4(W[w], W[w + 1], W[w + 2], W[w + 3]);
-        } else if (WPB % 2 == 0 && words_per_vec % 2 == 0) {
-#pragma unroll
-          for (int w = 0; w < WPB; w += 2) *reinterpret_cast<uint2*>(dst + w) = make_uint2(W[w], W[w + 1]);
-        } else {
-#pragma unroll
-          for (int w = 0; w < WPB; ++w) dst[w] = W[w];
-        }
-        a.scales[r * nb + j] = f2h(sqrtf(ss * (1.0f / BLK)));
-      }
-      j += 2;   // the group's next tile
-      while (j >= nb) { j -= nb; ++vg; }
+      jt += kGroups;   // the group's next tile
+      while (jt >= tpg) { jt -= tpg; ++vg; }
     }
   }
   if (failed) atomicCAS(&g_quant_status, 0, (int)TQ_ERR_TIMEOUT);
@@ -483,18 +497,17 @@ EncodeTiledFn encode_tiled() {
 }
 
 // Tensor map of the input rows: [n_vec][d] fp16, rows `stride` elements
-// apart, read in boxes of 128 rows x BLK columns with the swizzle the MMA's
-// A descriptor names; rows past n_vec read as zero.
-template <int BLK>
+// apart, read in boxes of 128 rows x 64 columns (128-byte rows, the swizzle
+// the MMA's A descriptor names); rows past n_vec read as zero.
 bool make_xmap(const FastQuantArgs& a, int d, CUtensorMap* map) {
   const EncodeTiledFn fn = encode_tiled();
   if (!fn || a.n_vec >= ((int64_t)1 << 31) - 128) return false;   // row coordinates are 32-bit
   const cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)a.n_vec};
   const cuuint64_t strides[1] = {(cuuint64_t)a.stride * 2};
-  const cuuint32_t box[2] = {(cuuint32_t)BLK, 128u};
+  const cuuint32_t box[2] = {(cuuint32_t)kTileCols, 128u};
   const cuuint32_t estr[2] = {1u, 1u};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half*>(a.x), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, BLK == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -524,18 +537,18 @@ int launch_fast(const CodecParams& P, FastQuantArgs& a, cudaStream_t st) {
       cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
       cudaDeviceGetAttribute(&smem_blk_res, cudaDevAttrReservedSharedMemoryPerBlock, dev);
       // stages (+ 1024 bytes of alignment slack), B of every block, cell table
-      const size_t smem = 1024 + (size_t)kStages * 128 * BLK * 2 + (size_t)P.nb * BLK * BLK * 2 +
+      const size_t smem = 1024 + (size_t)kStages * 128 * kTileCols * 2 + (size_t)P.nb * BLK * BLK * 2 +
                           (size_t)(kMaxCells + 1) * 32 * 4;
       cudaFuncAttributes fa;
       if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
           cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess ||
           cudaFuncGetAttributes(&fa, kern) != cudaSuccess)
         return TQ_ERR_CUDA;
-      // CTAs per SM: shared memory, registers, and TMEM (kAcc * BLK of 512 columns)
+      // CTAs per SM: shared memory, registers, and TMEM (kAcc * 64 of 512 columns)
       int occ = (int)((size_t)smem_sm / (smem + fa.sharedSizeBytes + (size_t)smem_blk_res));
       const int by_regs = 65536 / (kThreads * (fa.numRegs > 0 ? fa.numRegs : 1));
       occ = occ < by_regs ? occ : by_regs;
-      occ = occ < 512 / (kAcc * BLK) ? occ : 512 / (kAcc * BLK);
+      occ = occ < 512 / (kAcc * kTileCols) ? occ : 512 / (kAcc * kTileCols);
       c.sms = sms > 0 ? sms : 1;
       c.occ = occ > 0 ? occ : 1;
       c.smem = smem;
@@ -544,8 +557,8 @@ int launch_fast(const CodecParams& P, FastQuantArgs& a, cudaStream_t st) {
     sh = c;
   }
   CUtensorMap xmap;
-  if (!make_xmap<BLK>(a, P.d, &xmap)) return TQ_ERR_UNSUPPORTED;
-  a.n_tiles = (a.n_vec + 127) / 128 * P.nb;
+  if (!make_xmap(a, P.d, &xmap)) return TQ_ERR_UNSUPPORTED;
+  a.n_tiles = (a.n_vec + 127) / 128 * (P.d / kTileCols);
   // every CTA takes the same number of tiles, so no CTA runs a tail alone
   const int64_t max_ctas = (int64_t)sh.sms * sh.occ;
   a.per_cta = (a.n_tiles + max_ctas - 1) / max_ctas;
@@ -569,7 +582,8 @@ int launch_fast(const CodecParams& P, FastQuantArgs& a, cudaStream_t st) {
 }  // namespace
 
 bool quantize_fast_eligible(const CodecParams& P, bool f32_input) {
-  if (f32_input || P.m || P.nc || (P.blk != 32 && P.blk != 64) || P.bits < 2 || P.bits > 4) return false;
+  if (f32_input || P.m || P.nc || (P.blk != 32 && P.blk != 64) || P.bits < 2 || P.bits > 4 || P.d % kTileCols)
+    return false;
   FastQuantArgs a;
   return make_cells(P, &a);
 }

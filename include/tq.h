@@ -366,6 +366,35 @@ int tq_prefill_attn(const tq_kv_view* K, const tq_kv_view* V, const uint16_t* q,
 int tq_prefill_workspace_bytes(int B, int Hq, int Hkv, int head_dim, int Tq, int64_t ctx,
                                size_t* bytes);
 
+/* ---- Device-side waits and status ----------------------------------------
+ * The tensor-core prefill (tq_prefill_attn) and the fast quantiser
+ * (tq_quantize_kv / tq_append_kv with fp16 input, block 32 or 64, 2-4 bits,
+ * no QJL) hand work between the warps of a CTA through mbarriers, and every
+ * such wait is bounded.  A wait longer than the wait limit records
+ * TQ_ERR_TIMEOUT in the library's device status word for that device and
+ * goes on waiting, so the launch still completes and its outputs are valid;
+ * a call returns before its kernels run, so this is the only way a caller
+ * learns of it.  A wait longer than the hard bound (2 s, or the limit if
+ * larger) stops its CTA: the fast quantiser first waits for every load and
+ * product it has in flight, then stops with its outputs incomplete; the
+ * prefill stops without that drain (a device that has stopped making
+ * progress).  Either way the status word says TQ_ERR_TIMEOUT. */
+
+/* Sets the wait limit, in nanoseconds, for launches issued after the call
+ * (process-wide, all devices); 0 restores the default of 2 s.  Always
+ * returns TQ_OK. */
+int tq_set_wait_limit_ns(uint64_t ns);
+
+/* Reads the device status word of `device`: *status = TQ_OK when no launch
+ * of this library recorded a failure since the last clear, else the first
+ * failure recorded (TQ_ERR_TIMEOUT).  It first synchronises the device, so
+ * every launch issued before the call is counted; clear != 0 resets the word
+ * after reading.  The calling thread's current device is left unchanged.
+ * Returns TQ_ERR_ARG for a NULL status or an invalid device, TQ_ERR_CUDA
+ * when the synchronisation or the read fails (a fault of an earlier launch
+ * shows up here). */
+int tq_device_status(int device, int clear, int* status);
+
 /* Human-readable text of a tq_status (static storage). */
 const char* tq_strerror(int status);
 

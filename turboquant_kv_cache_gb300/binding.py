@@ -67,6 +67,8 @@ def _load():
         "tq_decode_attn_static": (I, [P, P, P, I, I, I, I64, P, I64, ctypes.c_float, P, I, P]),
         "tq_prefill_attn": (I, [P, P, P, I, I, I, I, I64, I64, I, ctypes.c_float, P, P, SZ, P]),
         "tq_prefill_workspace_bytes": (I, [I, I, I, I, I, I64, P]),
+        "tq_set_wait_limit_ns": (I, [ctypes.c_uint64]),
+        "tq_device_status": (I, [I, I, P]),
         "tq_strerror": (ctypes.c_char_p, [I]),
         "tq_version": (I, []),
     }
@@ -476,6 +478,23 @@ def tq_prefill_attn(K, V, q, ctx, causal=True, softmax_scale=0.0, workspace=None
                              workspace.numel(), _stream(stream))
     _check(st, "tq_prefill_attn")
     return out
+
+
+def tq_set_wait_limit_ns(ns):
+    """Wait limit (ns) of the library's bounded device-side waits for later
+    launches; 0 restores the default (2 s)."""
+    _check(_load().tq_set_wait_limit_ns(int(ns)), "tq_set_wait_limit_ns")
+
+
+def tq_device_status(device=None, clear=False):
+    """The library's device status word of `device` (default: the current
+    one) after synchronising it: 0 when no launch recorded a failure since
+    the last clear, else the first failure (TQ_ERR_TIMEOUT = -6)."""
+    if device is None:
+        device = torch.cuda.current_device()
+    st = ctypes.c_int(0)
+    _check(_load().tq_device_status(int(device), 1 if clear else 0, ctypes.byref(st)), "tq_device_status")
+    return st.value
 
 
 def tq_strerror(status):

@@ -1,5 +1,8 @@
 // Host layer of libtq: the Lloyd-Max codebook solver, the sign vector,
 // layout checks and sizes, status strings.  Pure C++ (no device code).
+#include <cuda_runtime.h>
+
+#include <atomic>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -307,6 +310,16 @@ int make_params(const tq_layout* L, CodecParams* p) {
   return TQ_OK;
 }
 
+namespace {
+std::atomic<uint64_t> g_wait_limit_ns{0};   // 0: the default
+}  // namespace
+
+WaitLimits wait_limits() {
+  const uint64_t v = g_wait_limit_ns.load(std::memory_order_relaxed);
+  const uint64_t report = v ? v : kDefaultWaitNs;
+  return WaitLimits{report, report > kDefaultWaitNs ? report : kDefaultWaitNs};
+}
+
 int make_codebook8(const tq_layout* L, Codebook8* cb) {
   const int st = check_layout(L);
   if (st != TQ_OK) return st;
@@ -388,5 +401,25 @@ const char* tq_strerror(int status) {
 }
 
 int tq_version(void) { return 100; }
+
+int tq_set_wait_limit_ns(uint64_t ns) {
+  tq::g_wait_limit_ns.store(ns, std::memory_order_relaxed);
+  return TQ_OK;
+}
+
+int tq_device_status(int device, int clear, int* status) {
+  if (!status) return TQ_ERR_ARG;
+  int prev = 0;
+  if (cudaGetDevice(&prev) != cudaSuccess) return TQ_ERR_CUDA;
+  if (device != prev && cudaSetDevice(device) != cudaSuccess) return TQ_ERR_ARG;
+  int st = cudaDeviceSynchronize() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+  int q = 0, p = 0;
+  if (st == TQ_OK) st = tq::quantize_fast_status(clear, &q);
+  if (st == TQ_OK) st = tq::prefill_tc_status(clear, &p);
+  if (device != prev) cudaSetDevice(prev);
+  if (st != TQ_OK) return st;
+  *status = q != 0 ? q : p;
+  return TQ_OK;
+}
 
 }  // extern "C"

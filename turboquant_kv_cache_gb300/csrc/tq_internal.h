@@ -84,4 +84,20 @@ inline bool same_paging(const tq_kv_view* a, const tq_kv_view* b) {
                                                                a->pages_per_seq == b->pages_per_seq));
 }
 
+// Bounded device-side waits.  A wait longer than the caller's limit
+// (tq_set_wait_limit_ns; default kDefaultWaitNs) records TQ_ERR_TIMEOUT in
+// the device status word of its translation unit and goes on waiting; one
+// longer than the hard bound stops its CTA.
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;
+struct WaitLimits {
+  uint64_t report_ns;   // record TQ_ERR_TIMEOUT past this
+  uint64_t hard_ns;     // stop past this (>= report_ns, at least 2 s)
+};
+WaitLimits wait_limits();
+
+// Device status words of the translation units whose kernels wait (read, and
+// reset when clear != 0, on the current device; synchronous).
+int quantize_fast_status(int clear, int* status);
+int prefill_tc_status(int clear, int* status);
+
 }  // namespace tq

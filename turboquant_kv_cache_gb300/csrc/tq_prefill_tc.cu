@@ -22,8 +22,13 @@
 // call by a small kernel.  Partial (m, l, O) per row and context slice go to
 // the workspace in the decode-split format, and the decode combine kernel
 // merges the slices and rotates each output row back (D H per V block).
-// Every mbarrier wait is bounded: on expiry the CTA records an error word in
-// the workspace, frees its TMEM and returns.
+// Every mbarrier wait is bounded.  A wait longer than the caller's limit
+// (tq_set_wait_limit_ns) records TQ_ERR_TIMEOUT in this file's device status
+// word and goes on waiting, so the launch still completes; a wait longer than
+// the hard bound raises the CTA's abort flag, the roles run out their loops
+// without work, and the CTA frees its TMEM and returns.  That abort path does
+// not wait for products or peer copies already in flight: it is the last
+// resort for a device that has stopped making progress, not a way to cancel.
 #include <cuda_runtime.h>
 #include <math.h>
 
@@ -51,8 +56,10 @@ constexpr uint32_t kColS = 0, kColP = 64;
 template <int D> __host__ __device__ constexpr uint32_t col_o() { return 128u + D / 2; }
 template <int D> __host__ __device__ constexpr uint32_t tmem_cols() { return col_o<D>() + D <= 256u ? 256u : 512u; }
 constexpr float kLazyP = 8.0f;
+
+// first failure status of a prefill launch since the last read (0 = none)
+__device__ int g_prefill_status;
 constexpr uint32_t kSuspendNs = 1000000;        // try_wait sleep hint
-constexpr uint64_t kWaitNs = 2000000000ull;     // give up a wait after 2 s
 
 __device__ __forceinline__ uint32_t su32(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
 
@@ -104,11 +111,13 @@ __device__ __forceinline__ uint64_t global_ns() {
 
 // Wait for the phase of parity `phase` of an mbarrier.  The thread sleeps in
 // try_wait (suspend-time hint 1 ms; it wakes as soon as the phase completes)
-// instead of spinning; the whole wait is bounded by kWaitNs of wall time.
+// instead of spinning.  Past report_ns of wall time the wait sets `late` and
+// goes on; past hard_ns it gives up (returns false).
 // CLUSTER: the arrivals come from the other CTA of the pair as well, so the
 // wait acquires at cluster scope.
 template <bool CLUSTER = false>
-__device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t phase) {
+__device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t phase, uint64_t report_ns, uint64_t hard_ns,
+                                         volatile int& late) {
   uint32_t done;
   if (CLUSTER)
     asm volatile(
@@ -124,8 +133,10 @@ __device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t phase) {
         : "r"(bar), "r"(phase)
         : "memory");
   if (done) return true;
-  uint64_t t0 = 0;
-  for (int it = 0; !done; ++it) {
+  // try_wait sleeps until the phase completes (up to its hint), so the
+  // elapsed time is checked after every return, the successful one too
+  const uint64_t t0 = global_ns();
+  for (;;) {
     if (CLUSTER)
       asm volatile(
           "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n"
@@ -139,14 +150,11 @@ __device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t phase) {
           : "=r"(done)
           : "r"(bar), "r"(phase), "r"(kSuspendNs)
           : "memory");
-    if (done) break;
-    if (it == 0) {
-      t0 = global_ns();
-    } else if (global_ns() - t0 > kWaitNs) {
-      return false;
-    }
+    const uint64_t el = global_ns() - t0;
+    if (el > report_ns) late = 1;
+    if (done) return true;
+    if (el > hard_ns) return false;
   }
-  return true;
 }
 
 __device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
@@ -385,7 +393,7 @@ struct PrefillTcArgs {
   const uint8_t* vs;
   const __half* qhat;   // [B*Hkv][R_pad][D]
   float* part;          // [(b*Hq + h)*Tq + i][n_split][D + 4]
-  int* err;
+  uint64_t report_ns, hard_ns;   // wait limits (see WaitLimits)
   int64_t S_cap, ctx;
   int Hq, Hkv, Tq, R_pad, n_split, causal;
   int64_t per;          // tokens per split (multiple of kTok)
@@ -512,7 +520,8 @@ __global__ void __launch_bounds__(192 + 32 * (NK + NV), 1) prefill_ws_kernel(con
   // kfull[NB], vfull[NB], kfree[NB], vfree[NB], q_full, s_full, s_free, p_full[2], o_done[2]
   __shared__ __align__(8) uint64_t bars[4 * NB + 7];
   __shared__ uint32_t tmem_base;
-  __shared__ volatile int s_abort;
+  __shared__ volatile int s_abort;   // a wait passed the hard bound: the roles run out without work
+  __shared__ volatile int s_late;    // a wait passed the caller's limit (reported, not stopped)
   __shared__ CodeTabs s_tabs[2];   // K and V codebooks (fp16 pairs, unscaled 4-bit tables)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -540,13 +549,13 @@ __global__ void __launch_bounds__(192 + 32 * (NK + NV), 1) prefill_ws_kernel(con
   auto n_valid_of = [&](int tile) { return (int)imin64(kTok, t_hi - (t_lo + (int64_t)tile * kTok)); };
   auto wait = [&](uint32_t bar, uint32_t parity) {
     if (s_abort) return false;
-    if (bar_wait(bar, parity)) return true;
+    if (bar_wait(bar, parity, a.report_ns, a.hard_ns, s_late)) return true;
     s_abort = 1;
     return false;
   };
   auto wait_cl = [&](uint32_t bar, uint32_t parity) {   // barriers the peer CTA arrives on
     if (s_abort) return false;
-    if (bar_wait<true>(bar, parity)) return true;
+    if (bar_wait<true>(bar, parity, a.report_ns, a.hard_ns, s_late)) return true;
     s_abort = 1;
     return false;
   };
@@ -555,6 +564,7 @@ __global__ void __launch_bounds__(192 + 32 * (NK + NV), 1) prefill_ws_kernel(con
     s_tabs[0] = make_code_tabs(PK);
     s_tabs[1] = make_code_tabs(PV);
     s_abort = 0;
+    s_late = 0;
 #pragma unroll
     for (int i = 0; i < NB; ++i) {
       asm volatile("mbarrier.init.shared::cta.b64 [%0], 2;\n" ::"r"(kfull + 8 * i) : "memory");
@@ -781,7 +791,7 @@ __global__ void __launch_bounds__(192 + 32 * (NK + NV), 1) prefill_ws_kernel(con
   // neither CTA leaves while the other may still store into its shared memory
   fence_before();
   cluster_sync();
-  if (tid == 0 && s_abort) atomicExch(a.err, 1);
+  if (tid == 0 && (s_abort || s_late)) atomicCAS(&g_prefill_status, 0, (int)TQ_ERR_TIMEOUT);
   if (warp == 0) {
     fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(kTmemCols) : "memory");
@@ -855,7 +865,7 @@ size_t prefill_tc_workspace(int B, int Hq, int Hkv, int d, int Tq, int64_t ctx) 
   const int ns = prefill_tc_splits(B, Hkv, G, Tq, ctx);
   const size_t qbytes = (size_t)B * Hkv * R_pad * d * 2;
   const size_t pbytes = (size_t)B * Hq * Tq * ns * (d + 4) * 4;
-  return 256 + ((qbytes + 255) / 256) * 256 + pbytes;
+  return ((qbytes + 255) / 256) * 256 + pbytes;
 }
 
 // The warp-specialised kernel with 18 decoder warps and setmaxnreg moving
@@ -912,15 +922,14 @@ int launch_prefill_tc(const CodecParams& PK, const CodecParams& PV, const uint8_
   const int R_pad = (Tq * G + 2 * kRowsTc - 1) / (2 * kRowsTc) * (2 * kRowsTc);
   const int ns = prefill_tc_splits(B, Hkv, G, Tq, ctx);
   uint8_t* base = static_cast<uint8_t*>(ws);
-  int* err = reinterpret_cast<int*>(base);
   const size_t qbytes = (size_t)B * Hkv * R_pad * d * 2;
-  __half* qhat = reinterpret_cast<__half*>(base + 256);
-  float* part = reinterpret_cast<float*>(base + 256 + ((qbytes + 255) / 256) * 256);
-  if (cudaMemsetAsync(err, 0, sizeof(int), st) != cudaSuccess) return TQ_ERR_CUDA;
+  __half* qhat = reinterpret_cast<__half*>(base);
+  float* part = reinterpret_cast<float*>(base + ((qbytes + 255) / 256) * 256);
+  const WaitLimits wl = wait_limits();
   int64_t per = (ctx + ns - 1) / ns;
   per = (per + kTok - 1) / kTok * kTok;
   PrefillTcArgs a{kc, reinterpret_cast<const uint8_t*>(ks), vc, reinterpret_cast<const uint8_t*>(vs), qhat, part,
-                  err, S_cap, ctx, Hq, Hkv, Tq, R_pad, ns, causal, per, pages};
+                  wl.report_ns, wl.hard_ns, S_cap, ctx, Hq, Hkv, Tq, R_pad, ns, causal, per, pages};
   dim3 qgrid(R_pad, B * Hkv);
   dim3 grid(R_pad / kRowsTc, ns, B * Hkv);
   int r;
@@ -941,6 +950,19 @@ int launch_prefill_tc(const CodecParams& PK, const CodecParams& PV, const uint8_
   if (r != TQ_OK) return r;
   if (cudaGetLastError() != cudaSuccess) return TQ_ERR_CUDA;
   return decode_combine(PV, part, ns, out, B * Hq * Tq, st);
+}
+
+// First failure status a prefill launch recorded since the last read with
+// clear set (0 = none).
+int prefill_tc_status(int clear, int* status) {
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_prefill_status, sizeof(int)) != cudaSuccess) return TQ_ERR_CUDA;
+  if (clear && v != 0) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_prefill_status, &zero, sizeof(int)) != cudaSuccess) return TQ_ERR_CUDA;
+  }
+  *status = v;
+  return TQ_OK;
 }
 
 }  // namespace tq

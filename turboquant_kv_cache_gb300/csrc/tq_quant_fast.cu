@@ -29,8 +29,11 @@
 // band); code = count + (s > boundary).  The table is replicated per lane so
 // the lookup has no bank conflicts.
 //
-// Every mbarrier wait is bounded: on expiry the CTA stops, frees its TMEM and
-// records TQ_ERR_TIMEOUT in this file's device status word.
+// Every mbarrier wait is bounded.  A wait longer than the caller's limit
+// records TQ_ERR_TIMEOUT in this file's device status word and goes on; one
+// longer than the hard bound stops its role.  Before the CTA frees its TMEM
+// and leaves, the producer waits for every load it issued and the MMA warp
+// for every product (a final commit), so nothing in flight outlives it.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -55,7 +58,6 @@ constexpr int kAcc = 2 * kGroups;           // TMEM accumulators of 64 columns (
 constexpr float kMagic = 12582912.0f;       // 1.5 * 2^23
 constexpr int kMaxCells = 64;
 constexpr uint32_t kSuspendNs = 100000;     // try_wait sleep hint
-constexpr uint64_t kWaitNs = 2000000000ull; // give up a wait after 2 s
 constexpr unsigned kPollNs = 128;           // sleep between polls of an mbarrier
 
 // first failure status of a quantise launch since the last read (0 = none)
@@ -70,6 +72,7 @@ struct FastQuantArgs {
   RowMap map;       // vector -> record
   int64_t n_tiles;  // ceil(n_vec / 128) * d / 64
   int64_t per_cta;  // tiles of each CTA (a contiguous range)
+  uint64_t report_ns, hard_ns;   // wait limits (see WaitLimits)
   int n_cells;      // C
   float inv2r;      // 1 / (2R), R beyond the outermost boundary
   uint32_t cell[kMaxCells + 1];
@@ -145,24 +148,32 @@ __device__ __forceinline__ uint64_t global_ns() {
   return t;
 }
 
-// Wait for phase `parity` of an mbarrier, bounded by kWaitNs of wall time.
+// Wait for phase `parity` of an mbarrier.  Past report_ns of wall time the
+// wait sets `late` and goes on; past hard_ns it gives up (returns false).
 // Callers combine the lanes' results with __all_sync, so a warp takes one
 // decision even when its lanes time out at different moments.
-__device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity, uint64_t report_ns, uint64_t hard_ns,
+                                         int& late) {
   uint32_t done = 0;
-  uint64_t t0 = 0;
-  for (int it = 0;; ++it) {
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  if (done) return true;
+  // try_wait may itself sleep until the phase completes (up to its hint), so
+  // the elapsed time is checked after every return, the successful one too
+  const uint64_t t0 = global_ns();
+  for (;;) {
     asm volatile(
         "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
         : "=r"(done)
         : "r"(bar), "r"(parity), "r"(kSuspendNs)
         : "memory");
+    const uint64_t el = global_ns() - t0;
+    if (el > report_ns) late = 1;
     if (done) return true;
-    if (it == 0) {
-      t0 = global_ns();
-    } else if (global_ns() - t0 > kWaitNs) {
-      return false;
-    }
+    if (el > hard_ns) return false;
     __nanosleep(kPollNs);   // leave the issue slots to the warps that have work
   }
 }
@@ -203,7 +214,8 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_tc_kernel(const CodecPar
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // full: stage s loaded (TMA bytes); empty: its products read it;
   // tfull: accumulator b written; tempty: accumulator b read (4 warps)
-  __shared__ __align__(8) uint64_t s_full[kStages], s_empty[kStages], s_tfull[kAcc], s_tempty[kAcc];
+  // drain: the MMA warp's last commit (every product it issued is done)
+  __shared__ __align__(8) uint64_t s_full[kStages], s_empty[kStages], s_tfull[kAcc], s_tempty[kAcc], s_drain;
   __shared__ uint32_t s_tmem;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nb = P.nb;
@@ -231,6 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_tc_kernel(const CodecPar
       asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(su32(&s_tfull[b])) : "memory");
       asm volatile("mbarrier.init.shared::cta.b64 [%0], 4;\n" ::"r"(su32(&s_tempty[b])) : "memory");
     }
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(su32(&s_drain)) : "memory");
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&xmap)) : "memory");
     asm volatile("griddepcontrol.wait;\n" ::: "memory");
@@ -278,7 +291,9 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_tc_kernel(const CodecPar
 
   // the next kernel in the stream may start its own set-up now
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
-  int failed = 0;   // a wait of this thread gave up; its role stops
+  int failed = 0;   // a wait of this thread gave up (hard bound); its role stops
+  int late = 0;     // a wait of this thread passed the report limit
+  auto wait = [&](uint32_t bar, uint32_t parity) { return bar_wait(bar, parity, a.report_ns, a.hard_ns, late); };
 
   if (warp == kConsumers) {
     // ================= producer (one thread): tile i >= kStages into stage
@@ -286,9 +301,10 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_tc_kernel(const CodecPar
     if (lane == 0) {
       int64_t vg = (t_begin + kStages) / tpg;
       int jt = (int)(t_begin + kStages - vg * tpg);
-      for (int i = kStages; i < n; ++i) {
+      int i = kStages;
+      for (; i < n; ++i) {
         const int s = i % kStages;
-        if (!bar_wait(su32(&s_empty[s]), (uint32_t)(i / kStages - 1) & 1)) {
+        if (!wait(su32(&s_empty[s]), (uint32_t)(i / kStages - 1) & 1)) {
           failed = 1;
           break;
         }
@@ -296,6 +312,11 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_tc_kernel(const CodecPar
         tma_load_2d(xs + s * STAGE, &xmap, jt * kTileCols, (int)(vg * 128), su32(&s_full[s]));
         if (++jt == tpg) { jt = 0; ++vg; }
       }
+      // drain: every load issued has landed before the CTA may leave (at
+      // most one phase per stage is outstanding, so a parity wait is exact)
+      const int issued = i < n ? i : n;
+      for (int q = issued > kStages ? issued - kStages : 0; q < issued; ++q)
+        bar_wait(su32(&s_full[q % kStages]), (uint32_t)(q / kStages) & 1, a.hard_ns, a.hard_ns, late);
     }
     __syncwarp();
   } else if (warp == kConsumers + 1) {
@@ -305,8 +326,8 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_tc_kernel(const CodecPar
     int jt = (int)(t_begin % tpg);
     for (int i = 0; i < n; ++i) {
       const int s = i % kStages, b = i % kAcc;
-      const bool ok = bar_wait(su32(&s_full[s]), (uint32_t)(i / kStages) & 1) &&
-                      (i < kAcc || bar_wait(su32(&s_tempty[b]), (uint32_t)(i / kAcc - 1) & 1));
+      const bool ok = wait(su32(&s_full[s]), (uint32_t)(i / kStages) & 1) &&
+                      (i < kAcc || wait(su32(&s_tempty[b]), (uint32_t)(i / kAcc - 1) & 1));
       if (!__all_sync(kFull, ok)) {
         failed = 1;
         break;
@@ -327,6 +348,9 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_tc_kernel(const CodecPar
       commit_elect(su32(&s_tfull[b]));
       if (++jt == tpg) jt = 0;
     }
+    // drain: every product issued is done before TMEM is freed
+    commit_elect(su32(&s_drain));
+    __all_sync(kFull, bar_wait(su32(&s_drain), 0, a.hard_ns, a.hard_ns, late));
   } else {
     // ================= consumers: one vector per thread (TMEM lane
     // 32 (warp % 4) + lane, columns = coordinates of the tile)
@@ -341,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_tc_kernel(const CodecPar
     int jt = (int)(t_begin + grp - vg * tpg);
     for (int i = grp; i < n; i += kGroups) {
       const int b = i % kAcc;
-      if (!__all_sync(kFull, bar_wait(su32(&s_tfull[b]), (uint32_t)(i / kAcc) & 1))) {
+      if (!__all_sync(kFull, wait(su32(&s_tfull[b]), (uint32_t)(i / kAcc) & 1))) {
         failed = 1;
         break;
       }
@@ -435,7 +459,7 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_tc_kernel(const CodecPar
       while (jt >= tpg) { jt -= tpg; ++vg; }
     }
   }
-  if (failed) atomicCAS(&g_quant_status, 0, (int)TQ_ERR_TIMEOUT);
+  if (failed || late) atomicCAS(&g_quant_status, 0, (int)TQ_ERR_TIMEOUT);
   fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -558,6 +582,9 @@ int launch_fast(const CodecParams& P, FastQuantArgs& a, cudaStream_t st) {
   }
   CUtensorMap xmap;
   if (!make_xmap(a, P.d, &xmap)) return TQ_ERR_UNSUPPORTED;
+  const WaitLimits wl = wait_limits();
+  a.report_ns = wl.report_ns;
+  a.hard_ns = wl.hard_ns;
   a.n_tiles = (a.n_vec + 127) / 128 * (P.d / kTileCols);
   // every CTA takes the same number of tiles, so no CTA runs a tail alone
   const int64_t max_ctas = (int64_t)sh.sms * sh.occ;
@@ -608,9 +635,9 @@ int launch_quantize_fast(const CodecParams& P, const void* x, int64_t n_vec, int
   return launch_fast<32, 2>(P, a, st);
 }
 
-// First failure status a fast quantise launch recorded since the last call
-// with clear set (0 = none).  Synchronises with the device.
-int quantize_fast_status(bool clear, int* status) {
+// First failure status a fast quantise launch recorded since the last read
+// with clear set (0 = none).
+int quantize_fast_status(int clear, int* status) {
   int s = 0;
   if (cudaMemcpyFromSymbol(&s, g_quant_status, sizeof(int)) != cudaSuccess) return TQ_ERR_CUDA;
   if (clear && s != 0) {

@@ -15,6 +15,10 @@ bool quantize_fast_eligible(const CodecParams& P, bool f32_input);
 int launch_quantize_fast(const CodecParams& P, const void* x, int64_t n_vec, int64_t stride, uint8_t* codes,
                          uint16_t* scales, const RowMap& map, cudaStream_t st);
 bool quantize_qjl_eligible(const CodecParams& P);
+bool quantize_qjl_tc_eligible(const CodecParams& P, bool f32_input);
+int launch_quantize_qjl_tc(const CodecParams& P, const void* x, int64_t n_vec, int64_t stride, const float* S,
+                           uint8_t* codes, uint16_t* scales, uint8_t* qjl_bits, uint16_t* qjl_rnorm, const RowMap& map,
+                           cudaStream_t st);
 int launch_quantize_qjl(const CodecParams& P, const void* x, bool f32, int64_t n_vec, int64_t stride, const float* S,
                         uint8_t* codes, uint16_t* scales, uint8_t* qjl_bits, uint16_t* qjl_rnorm, const RowMap& map,
                         cudaStream_t st);
@@ -376,6 +380,11 @@ int quantize_common(const tq_layout* layout, const void* x, tq_dtype x_dtype, in
     // loads (e.g. 2^32 rows or more); the general kernel takes it
     const int fst = launch_quantize_fast(P, x, n_vec, x_row_stride, codes, scales, map, s);
     if (fst != TQ_ERR_UNSUPPORTED) return fst;
+  }
+  if (quantize_qjl_tc_eligible(P, f32)) {
+    // TQ_ERR_UNSUPPORTED: more rows than the tensor-memory loads describe
+    const int qst = launch_quantize_qjl_tc(P, x, n_vec, x_row_stride, S, codes, scales, qjl_bits, qjl_rnorm, map, s);
+    if (qst != TQ_ERR_UNSUPPORTED) return qst;
   }
   if (quantize_qjl_eligible(P))
     return launch_quantize_qjl(P, x, f32, n_vec, x_row_stride, S, codes, scales, qjl_bits, qjl_rnorm, map, s);

@@ -413,12 +413,13 @@ int tq_device_status(int device, int clear, int* status) {
   if (cudaGetDevice(&prev) != cudaSuccess) return TQ_ERR_CUDA;
   if (device != prev && cudaSetDevice(device) != cudaSuccess) return TQ_ERR_ARG;
   int st = cudaDeviceSynchronize() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
-  int q = 0, p = 0;
+  int q = 0, j = 0, p = 0;
   if (st == TQ_OK) st = tq::quantize_fast_status(clear, &q);
+  if (st == TQ_OK) st = tq::quantize_qjl_tc_status(clear, &j);
   if (st == TQ_OK) st = tq::prefill_tc_status(clear, &p);
   if (device != prev) cudaSetDevice(prev);
   if (st != TQ_OK) return st;
-  *status = q != 0 ? q : p;
+  *status = q != 0 ? q : (j != 0 ? j : p);
   return TQ_OK;
 }
 

@@ -98,6 +98,7 @@ WaitLimits wait_limits();
 // Device status words of the translation units whose kernels wait (read, and
 // reset when clear != 0, on the current device; synchronous).
 int quantize_fast_status(int clear, int* status);
+int quantize_qjl_tc_status(int clear, int* status);
 int prefill_tc_status(int clear, int* status);
 
 }  // namespace tq

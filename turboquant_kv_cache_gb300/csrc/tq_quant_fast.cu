@@ -13,38 +13,29 @@
 //
 // Roles: a producer thread loads input tiles with TMA (one 128-row box per
 // tile, rows past the end zero-filled, 128- or 64-byte swizzled rows, the
-// layout the MMA reads) four stages deep, an MMA warp issues the products
-// into four TMEM accumulators, and two groups of four consumer warps take
+// layout the MMA reads) ten stages deep, an MMA warp issues the products
+// into eight TMEM accumulators, and four groups of four consumer warps take
 // turns on the finished ones.  They meet only on mbarriers.  The producer
 // issues the first loads before the CTA's set-up (B, the cell table, TMEM),
 // and the kernel is launched as a programmatic dependent of the previous one
 // in the stream, so both the set-up and the launch overlap other work.
 //
-// Bucketize, code = #{k : y > beta_k}: with s = sat(y / (2R ||y||) + 1/2)
-// in [0, 1], round(s*C) picks one of C+1 cells that hold at most one
-// boundary each (rounding is monotone, so every boundary in a lower cell is
-// below s and every one in a higher cell above it).  A cell entry holds that
-// boundary in s units with the count of boundaries below the cell in its low
-// four mantissa bits (a shift of at most 15 ulp, far inside the 1e-5 tie
-// band); code = count + (s > boundary).  The table is replicated per lane so
-// the lookup has no bank conflicts.
+// Codes come from the cell-table bucketize of tq_tc.cuh: one shared load and
+// one compare per code.
 //
 // Every mbarrier wait is bounded.  A wait longer than the caller's limit
 // records TQ_ERR_TIMEOUT in this file's device status word and goes on; one
 // longer than the hard bound stops its role.  Before the CTA frees its TMEM
 // and leaves, the producer waits for every load it issued and the MMA warp
 // for every product (a final commit), so nothing in flight outlives it.
-#include <cuda.h>
-#include <cuda_runtime.h>
-
-#include <cmath>
-#include <cstring>
 #include <mutex>
 
-#include "tq_device.cuh"
+#include "tq_tc.cuh"
 
 namespace tq {
 namespace {
+
+using namespace tcq;
 
 // One CTA per SM.  Consumer warps: kGroups groups of four, group g takes the
 // CTA's tiles i with i % kGroups == g; in a group, one vector per thread (one
@@ -55,10 +46,6 @@ constexpr int kThreads = 32 * (kConsumers + 2);   // + a producer warp and an MM
 constexpr int kTileCols = 64;               // input columns per tile: one or two rotation blocks
 constexpr int kStages = 10;                 // input stages (16 KB each)
 constexpr int kAcc = 2 * kGroups;           // TMEM accumulators of 64 columns (two per group, all 512)
-constexpr float kMagic = 12582912.0f;       // 1.5 * 2^23
-constexpr int kMaxCells = 64;
-constexpr uint32_t kSuspendNs = 100000;     // try_wait sleep hint
-constexpr unsigned kPollNs = 128;           // sleep between polls of an mbarrier
 
 // first failure status of a quantise launch since the last read (0 = none)
 __device__ int g_quant_status;
@@ -73,133 +60,8 @@ struct FastQuantArgs {
   int64_t n_tiles;  // ceil(n_vec / 128) * d / 64
   int64_t per_cta;  // tiles of each CTA (a contiguous range)
   uint64_t report_ns, hard_ns;   // wait limits (see WaitLimits)
-  int n_cells;      // C
-  float inv2r;      // 1 / (2R), R beyond the outermost boundary
-  uint32_t cell[kMaxCells + 1];
+  CellTable ct;     // bucketize cells
 };
-
-__device__ __forceinline__ uint32_t su32(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
-
-__device__ __forceinline__ uint32_t lds32(uint32_t a) {
-  uint32_t v;
-  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(a));
-  return v;
-}
-
-// TMA: the 2-D box at (x, y) of a tensor map into shared memory, completing
-// on an mbarrier
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];\n" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-      : "memory");
-}
-__device__ __forceinline__ void arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes) : "memory");
-}
-
-// byte offset of element (row, col) in a core-matrix tile of `cols` columns:
-// core matrix (row/8, col/8) at ((row/8) * (cols/8) + col/8) * 128, row-major
-// 8 x 16 bytes inside
-__host__ __device__ __forceinline__ uint32_t cm_off(int row, int col, int cols) {
-  return (uint32_t)(((row >> 3) * (cols >> 3) + (col >> 3)) * 128 + (row & 7) * 16 + (col & 7) * 2);
-}
-
-// shared-memory matrix descriptor, no swizzle: lbo = byte step between core
-// matrices along K, sbo = along M / N
-__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
-         ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | ((uint64_t)1 << 46);
-}
-
-// descriptor of a K-major operand whose rows are `row_bytes` (128 or 64)
-// long, 16-byte chunks swizzled within each 8-row atom (128B / 64B modes);
-// the atom stride is 8 rows
-__device__ __forceinline__ uint64_t sdesc_swz(uint32_t saddr, int row_bytes) {
-  const uint64_t mode = row_bytes == 128 ? 2 : 4;
-  return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)1 << 16) | ((uint64_t)((8 * row_bytes) >> 4) << 32) |
-         ((uint64_t)1 << 46) | (mode << 61);
-}
-
-// warp-wide: the lane elect.sync picks issues the MMA / the commit, so an MMA
-// and the commit that tracks it come from one thread
-__device__ __forceinline__ void mma_ss_elect(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, int acc) {
-  asm volatile(
-      "{\n .reg .pred p, e;\n elect.sync _|e, 0xffffffff;\n setp.ne.b32 p, %4, 0;\n"
-      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
-      "l"(a), "l"(b), "r"(idesc), "r"(acc)
-      : "memory");
-}
-__device__ __forceinline__ void commit_elect(uint32_t bar) {
-  asm volatile(
-      "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
-      " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(bar)
-      : "memory");
-}
-__device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
-__device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory"); }
-// generic-proxy writes to shared memory (stores, cp.async) before the tensor
-// cores read them
-__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
-
-__device__ __forceinline__ uint64_t global_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-// Wait for phase `parity` of an mbarrier.  Past report_ns of wall time the
-// wait sets `late` and goes on; past hard_ns it gives up (returns false).
-// Callers combine the lanes' results with __all_sync, so a warp takes one
-// decision even when its lanes time out at different moments.
-__device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity, uint64_t report_ns, uint64_t hard_ns,
-                                         int& late) {
-  uint32_t done = 0;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(done)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  if (done) return true;
-  // try_wait may itself sleep until the phase completes (up to its hint), so
-  // the elapsed time is checked after every return, the successful one too
-  const uint64_t t0 = global_ns();
-  for (;;) {
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(done)
-        : "r"(bar), "r"(parity), "r"(kSuspendNs)
-        : "memory");
-    const uint64_t el = global_ns() - t0;
-    if (el > report_ns) late = 1;
-    if (done) return true;
-    if (el > hard_ns) return false;
-    __nanosleep(kPollNs);   // leave the issue slots to the warps that have work
-  }
-}
-
-#define TQ_LD32(taddr, v)                                                                                          \
-  asm volatile(                                                                                                    \
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"  \
-      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"                                             \
-      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),            \
-        "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),      \
-        "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),    \
-        "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])     \
-      : "r"(taddr))
-
-// w += inc when s > the boundary held in entry e (as a float)
-__device__ __forceinline__ void add_if_gt(uint32_t& w, float s, uint32_t e, uint32_t inc) {
-  asm("{\n .reg .pred p;\n setp.gt.f32 p, %1, %2;\n @p add.u32 %0, %0, %3;\n}"
-      : "+r"(w)
-      : "f"(s), "f"(__uint_as_float(e)), "r"(inc));
-}
-
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
-  uint32_t d;
-  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
-  return d;
-}
 
 template <int BLK, int BITS>
 __global__ void __launch_bounds__(kThreads, 1) quantize_tc_kernel(const CodecParams P, const FastQuantArgs a,
@@ -276,7 +138,7 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_tc_kernel(const CodecPar
     *reinterpret_cast<uint4*>(s_b + (size_t)j * BLK * BLK * 2 + cm_off(nn, 8 * ch, BLK)) =
         make_uint4(w[0], w[1], w[2], w[3]);
   }
-  for (int idx = tid; idx < (a.n_cells + 1) * 32; idx += kThreads) s_cell[idx] = a.cell[idx >> 5];
+  for (int idx = tid; idx < (a.ct.n_cells + 1) * 32; idx += kThreads) s_cell[idx] = a.ct.cell[idx >> 5];
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(su32(&s_tmem)),
                  "n"(kCols)
@@ -355,7 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_tc_kernel(const CodecPar
     // ================= consumers: one vector per thread (TMEM lane
     // 32 (warp % 4) + lane, columns = coordinates of the tile)
     const int words_per_vec = P.code_bytes / 4;
-    const float2 cells2 = make_float2((float)a.n_cells, (float)a.n_cells);
+    const float2 cells2 = make_float2((float)a.ct.n_cells, (float)a.ct.n_cells);
     const float2 magic2 = make_float2(kMagic, kMagic);
     // cell c of this lane's copy at s_cell + 4 (32 c + lane); the magic bits
     // of round(s C) + 1.5 * 2^23 are folded into the base (mod 2^32)
@@ -390,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_tc_kernel(const CodecPar
                             make_float2(__uint_as_float(vv[c]), __uint_as_float(vv[c + 1])), s2);
         }
         const float ss = s2.x + s2.y;
-        const float A1 = ss > 0.f ? a.inv2r * rsqrtf(ss) : 0.f;
+        const float A1 = ss > 0.f ? a.ct.inv2r * rsqrtf(ss) : 0.f;
         // pass 2, 32 coordinates at a time: nibble word c holds the codes of
         // coordinates 8c .. 8c+7; a coordinate pair forms one byte, inserted
         // with a byte permute
@@ -468,73 +330,6 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_tc_kernel(const CodecPar
   }
 }
 
-// The cell table of a codebook (see the file comment); false when no
-// C <= kMaxCells separates the boundaries.
-bool make_cells(const CodecParams& P, FastQuantArgs* a) {
-  const int K = 1 << P.bits;
-  float bmax = 0.f;
-  for (int k = 0; k < K - 1; ++k) bmax = std::fmax(bmax, std::fabs(P.bounds[k]));
-  if (!(bmax > 0.f) || !std::isfinite(bmax)) return false;
-  a->inv2r = 0.5f / (bmax * 1.0625f);
-  float sig[16];
-  for (int k = 0; k < K - 1; ++k) sig[k] = std::fmaf(P.bounds[k], a->inv2r, 0.5f);
-  for (int C = 16; C <= kMaxCells; C *= 2) {
-    int cellk[16];
-    bool ok = true;
-    for (int k = 0; k < K - 1; ++k) {
-      cellk[k] = (int)std::nearbyintf(sig[k] * (float)C);
-      if (k > 0 && cellk[k] <= cellk[k - 1]) ok = false;
-    }
-    if (!ok) continue;
-    a->n_cells = C;
-    for (int c = 0; c <= C; ++c) {
-      uint32_t below = 0;
-      float bnd = 2.0f;
-      for (int k = 0; k < K - 1; ++k) {
-        if (cellk[k] < c) ++below;
-        if (cellk[k] == c) bnd = sig[k];
-      }
-      uint32_t bits;
-      std::memcpy(&bits, &bnd, 4);
-      a->cell[c] = (bits & ~15u) | below;
-    }
-    return true;
-  }
-  return false;
-}
-
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-// cuTensorMapEncodeTiled from the driver (a host-only encoding call)
-EncodeTiledFn encode_tiled() {
-  static EncodeTiledFn fn = [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      p = nullptr;
-    return reinterpret_cast<EncodeTiledFn>(p);
-  }();
-  return fn;
-}
-
-// Tensor map of the input rows: [n_vec][d] fp16, rows `stride` elements
-// apart, read in boxes of 128 rows x 64 columns (128-byte rows, the swizzle
-// the MMA's A descriptor names); rows past n_vec read as zero.
-bool make_xmap(const FastQuantArgs& a, int d, CUtensorMap* map) {
-  const EncodeTiledFn fn = encode_tiled();
-  if (!fn || a.n_vec >= ((int64_t)1 << 31) - 128) return false;   // row coordinates are 32-bit
-  const cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)a.n_vec};
-  const cuuint64_t strides[1] = {(cuuint64_t)a.stride * 2};
-  const cuuint32_t box[2] = {(cuuint32_t)kTileCols, 128u};
-  const cuuint32_t estr[2] = {1u, 1u};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half*>(a.x), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 // Launch shape of one kernel instantiation on one device, worked out once.
 struct LaunchShape {
   bool ready = false;
@@ -581,7 +376,7 @@ int launch_fast(const CodecParams& P, FastQuantArgs& a, cudaStream_t st) {
     sh = c;
   }
   CUtensorMap xmap;
-  if (!make_xmap(a, P.d, &xmap)) return TQ_ERR_UNSUPPORTED;
+  if (!make_rows_map(a.x, P.d, a.n_vec, a.stride, &xmap)) return TQ_ERR_UNSUPPORTED;
   const WaitLimits wl = wait_limits();
   a.report_ns = wl.report_ns;
   a.hard_ns = wl.hard_ns;
@@ -611,14 +406,14 @@ int launch_fast(const CodecParams& P, FastQuantArgs& a, cudaStream_t st) {
 bool quantize_fast_eligible(const CodecParams& P, bool f32_input) {
   if (f32_input || P.m || P.nc || (P.blk != 32 && P.blk != 64) || P.bits < 2 || P.bits > 4 || P.d % kTileCols)
     return false;
-  FastQuantArgs a;
-  return make_cells(P, &a);
+  CellTable ct;
+  return make_cells(P, &ct);
 }
 
 int launch_quantize_fast(const CodecParams& P, const void* x, int64_t n_vec, int64_t stride, uint8_t* codes,
                          uint16_t* scales, const RowMap& map, cudaStream_t st) {
   FastQuantArgs a;
-  if (!make_cells(P, &a)) return TQ_ERR_UNSUPPORTED;
+  if (!make_cells(P, &a.ct)) return TQ_ERR_UNSUPPORTED;
   a.map = map;
   a.x = static_cast<const __half*>(x);
   a.n_vec = n_vec;

@@ -18,6 +18,11 @@
 namespace tq {
 
 int decode_auto_splits(int B, int Hkv, int64_t ctx);
+bool decode_tc_blocks_eligible(const CodecParams& PK, const CodecParams& PV, int G, int64_t S_cap,
+                               const uint8_t* k_blocks, const uint8_t* v_blocks);
+int launch_decode_tc_blocks(const CodecParams& PK, const CodecParams& PV, const uint8_t* k_blocks,
+                            const uint8_t* v_blocks, const uint16_t* q, const int32_t* kv_len, float* part, int B,
+                            int Hq, int Hkv, int64_t S_cap, int64_t ctx, int n_split, float qscale, cudaStream_t st);
 bool decode_tc_eligible(const CodecParams& PK, const CodecParams& PV, int G, int64_t S_cap, const tq_kv_view* K,
                         const tq_kv_view* V);
 size_t decode_tc_extra_bytes(int B, int Hq);
@@ -1012,10 +1017,15 @@ int decode_blocks_impl(const tq_layout* Lk, const uint8_t* k_blocks, const tq_la
   a.vblk = reinterpret_cast<const uint16_t*>(v_blocks);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int G = Hq / Hkv;
-  switch (PK.d) {
-    case 64: st = launch_decode_blocks<64>(G, PK, PV, a, B, s); break;
-    case 128: st = launch_decode_blocks<128>(G, PK, PV, a, B, s); break;
-    default: st = launch_decode_blocks<256>(G, PK, PV, a, B, s); break;
+  if (decode_tc_blocks_eligible(PK, PV, G, S_cap, k_blocks, v_blocks)) {
+    st = launch_decode_tc_blocks(PK, PV, k_blocks, v_blocks, q, kv_len, a.part, B, Hq, Hkv, S_cap, ctx, ns, a.qscale,
+                                 s);
+  } else {
+    switch (PK.d) {
+      case 64: st = launch_decode_blocks<64>(G, PK, PV, a, B, s); break;
+      case 128: st = launch_decode_blocks<128>(G, PK, PV, a, B, s); break;
+      default: st = launch_decode_blocks<256>(G, PK, PV, a, B, s); break;
+    }
   }
   if (st != TQ_OK) return st;
   return decode_combine(PV, a.part, ns, out, B * Hq, s);

@@ -50,16 +50,20 @@ constexpr int kSlots = 3;
 constexpr int kQjlM = 128;     // QJL rows supported here
 constexpr float kLazy = 8.0f;  // rescale threshold, log2 units
 
-template <int D, int KB, int VB, bool KPV, bool VPV, bool QJL>
+// AOS: the caches are arrays of 32-value blocks, [fp16 norm | packed codes of
+// the group] (2 + 4*bits bytes), a token's blocks contiguous; a token's record
+// holds its norms, so there is no separate norm stream.
+template <int D, int KB, int VB, bool KPV, bool VPV, bool QJL, bool AOS = false>
 struct Cfg {
   static constexpr int NH = D / 128;  // warps per pipeline
   static constexpr int P = 4 / NH;    // pipelines per CTA
-  static constexpr int KREC = D * KB / 8;
-  static constexpr int KSB = KPV ? 2 : D / 16;
+  static constexpr int KBB = 2 + 4 * KB, VBB = 2 + 4 * VB;   // block bytes (AOS)
+  static constexpr int KREC = AOS ? (D / 32) * KBB : D * KB / 8;
+  static constexpr int KSB = AOS ? 0 : (KPV ? 2 : D / 16);
   static constexpr int QB = QJL ? kQjlM / 8 : 0;
   static constexpr int QR = QJL ? 2 : 0;
-  static constexpr int VREC = D * VB / 8;
-  static constexpr int VSB = VPV ? 2 : D / 16;
+  static constexpr int VREC = AOS ? (D / 32) * VBB : D * VB / 8;
+  static constexpr int VSB = AOS ? 0 : (VPV ? 2 : D / 16);
   static constexpr int OKC = 0;
   static constexpr int OKS = OKC + kTok * KREC;
   static constexpr int OQB = OKS + kTok * KSB;
@@ -70,7 +74,7 @@ struct Cfg {
   static constexpr size_t SMEM = (size_t)P * kSlots * STAGE      // rings
                                  + (size_t)4 * kG * kTok * 2       // p per warp
                                  + (NH > 1 ? (size_t)4 * 32 * 8 * 4 : 0);  // partial-score exchange
-  static_assert(STAGE % 16 == 0, "stage sub-arrays stay 16-byte aligned");
+  static_assert(STAGE % 16 == 0 && OVC % 16 == 0, "stage sub-arrays stay 16-byte aligned");
   static_assert((size_t)P * kSlots * STAGE >= (size_t)P * kG * D * 4, "ring too small for the merge");
 };
 
@@ -184,6 +188,7 @@ __device__ __forceinline__ float2 unpack_h2(uint32_t v) {
 // as 16-byte copies spread over the pipeline's 32 * NH lanes.
 template <int BYTES, int NH>
 __device__ __forceinline__ void copy_full(uint32_t dst, const uint8_t* src, int plane) {
+  if (BYTES == 0) return;
   constexpr int CH = kTok * BYTES / 16, STEP = 32 * NH;
 #pragma unroll
   for (int k = 0; k < (CH + STEP - 1) / STEP; ++k) {
@@ -195,6 +200,7 @@ __device__ __forceinline__ void copy_full(uint32_t dst, const uint8_t* src, int 
 // The same for a step with only nv valid tokens: the rest is zero-filled.
 template <int BYTES, int NH>
 __device__ __forceinline__ void copy_part(uint32_t dst, const uint8_t* base, int64_t tok0, int nv, int plane) {
+  if (BYTES == 0) return;
   constexpr int CH = kTok * BYTES / 16, STEP = 32 * NH;
   const uint8_t* src = base + tok0 * BYTES;
 #pragma unroll
@@ -208,10 +214,28 @@ __device__ __forceinline__ void copy_part(uint32_t dst, const uint8_t* base, int
   }
 }
 
-template <int D, int KB, int VB, bool KPV, bool VPV, bool QJL>
+// The packed words of a 32-code group at shared address `addr`; with AOS the
+// group's codes follow its 2-byte norm, so they start 2 bytes past a word
+// boundary for every other group (sh = 2): bits+1 aligned words and a byte
+// permute per word.
+template <int BITS, bool AOS>
+__device__ __forceinline__ void group_words(uint32_t addr, uint32_t* w) {
+  if (!AOS) {
+    load_group<BITS>(addr, w);
+  } else {
+    const uint32_t base = addr & ~3u, sh = addr & 3u;
+    uint32_t x[BITS + 1];
+#pragma unroll
+    for (int i = 0; i <= BITS; ++i) x[i] = lds32(base + 4 * i);
+#pragma unroll
+    for (int i = 0; i < BITS; ++i) w[i] = sh ? prmt(x[i], x[i + 1], 0x5432u) : x[i];
+  }
+}
+
+template <int D, int KB, int VB, bool KPV, bool VPV, bool QJL, bool AOS = false>
 __global__ void __launch_bounds__(kThreads, 4) decode_tc_kernel(const CodecParams PK, const CodecParams PV,
                                                                const TcArgs a) {
-  using C = Cfg<D, KB, VB, KPV, VPV, QJL>;
+  using C = Cfg<D, KB, VB, KPV, VPV, QJL, AOS>;
   constexpr int NH = C::NH, P = C::P;
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ float s_ml[4][2][kG];
@@ -372,24 +396,28 @@ __global__ void __launch_bounds__(kThreads, 4) decode_tc_kernel(const CodecParam
       float Pq[4] = {0.f, 0.f, 0.f, 0.f};
       const int tok0 = 16 * u + g, tok1 = tok0 + 8;
       uint32_t w0[4], w1[4], n0[4], n1[4];
-      load_group<KB>(st + C::OKC + tok0 * C::KREC + grp * 4 * KB, w0);
-      load_group<KB>(st + C::OKC + tok1 * C::KREC + grp * 4 * KB, w1);
+      group_words<KB, AOS>(st + C::OKC + tok0 * C::KREC + (AOS ? grp * C::KBB + 2 : grp * 4 * KB), w0);
+      group_words<KB, AOS>(st + C::OKC + tok1 * C::KREC + (AOS ? grp * C::KBB + 2 : grp * 4 * KB), w1);
       chunk_words<KB>(w0, n0);
       chunk_words<KB>(w1, n1);
+      // the group's norm: its block header (AOS) or the norm stream
+      auto knorm = [&](int tok) {
+        return lds16(AOS ? st + C::OKC + tok * C::KREC + grp * C::KBB : st + C::OKS + tok * C::KSB + 2 * grp);
+      };
       Tab T0, T1;
       uint32_t s0h = 0, s1h = 0;
       if (KPV || KB == 4) {
         T0 = kfix;
         T1 = kfix;
         if (!KPV) {
-          s0h = lds16(st + C::OKS + tok0 * C::KSB + 2 * grp);
-          s1h = lds16(st + C::OKS + tok1 * C::KSB + 2 * grp);
+          s0h = knorm(tok0);
+          s1h = knorm(tok1);
           s0h |= s0h << 16;
           s1h |= s1h << 16;
         }
       } else {
-        T0 = make_tab<KB>(kcent, lds16(st + C::OKS + tok0 * C::KSB + 2 * grp));
-        T1 = make_tab<KB>(kcent, lds16(st + C::OKS + tok1 * C::KSB + 2 * grp));
+        T0 = make_tab<KB>(kcent, knorm(tok0));
+        T1 = make_tab<KB>(kcent, knorm(tok1));
       }
 #pragma unroll
       for (int s = 0; s < 4; ++s) {
@@ -421,8 +449,9 @@ __global__ void __launch_bounds__(kThreads, 4) decode_tc_kernel(const CodecParam
         }
       }
       if (KPV) {
-        const float sc0 = h2f((uint16_t)lds16(st + C::OKS + tok0 * C::KSB));
-        const float sc1 = h2f((uint16_t)lds16(st + C::OKS + tok1 * C::KSB));
+        // one norm per vector (AOS: every block header holds it; block 0's)
+        const float sc0 = h2f((uint16_t)lds16(AOS ? st + C::OKC + tok0 * C::KREC : st + C::OKS + tok0 * C::KSB));
+        const float sc1 = h2f((uint16_t)lds16(AOS ? st + C::OKC + tok1 * C::KREC : st + C::OKS + tok1 * C::KSB));
         if (QJL) {
           const float r0 = sc0 * h2f((uint16_t)lds16(st + C::OQR + tok0 * 2));
           const float r1 = sc1 * h2f((uint16_t)lds16(st + C::OQR + tok1 * 2));
@@ -500,7 +529,9 @@ __global__ void __launch_bounds__(kThreads, 4) decode_tc_kernel(const CodecParam
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
         float vs = 1.f;
-        if (VPV) vs = h2f((uint16_t)lds16(st + C::OVS + (16 * u + 8 * r + g) * C::VSB));
+        if (VPV)
+          vs = h2f((uint16_t)lds16(AOS ? st + C::OVC + (16 * u + 8 * r + g) * C::VREC
+                                       : st + C::OVS + (16 * u + 8 * r + g) * C::VSB));
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           // no valid token seen yet implies every score here is -inf
@@ -519,8 +550,8 @@ __global__ void __launch_bounds__(kThreads, 4) decode_tc_kernel(const CodecParam
       const uint32_t pb1 = lds32(pR + 2 * (16 * u + 8));
       const int tok0 = 16 * u + g, tok1 = tok0 + 8;
       uint32_t w0[4], w1[4], n0[4], n1[4];
-      load_group<VB>(st + C::OVC + tok0 * C::VREC + grp * 4 * VB, w0);
-      load_group<VB>(st + C::OVC + tok1 * C::VREC + grp * 4 * VB, w1);
+      group_words<VB, AOS>(st + C::OVC + tok0 * C::VREC + (AOS ? grp * C::VBB + 2 : grp * 4 * VB), w0);
+      group_words<VB, AOS>(st + C::OVC + tok1 * C::VREC + (AOS ? grp * C::VBB + 2 : grp * 4 * VB), w1);
       chunk_words<VB>(w0, n0);
       chunk_words<VB>(w1, n1);
       Tab T0, T1;
@@ -528,8 +559,10 @@ __global__ void __launch_bounds__(kThreads, 4) decode_tc_kernel(const CodecParam
         T0 = vfix;
         T1 = vfix;
       } else {
-        T0 = make_tab<VB>(vcent, lds16(st + C::OVS + tok0 * C::VSB + 2 * grp));
-        T1 = make_tab<VB>(vcent, lds16(st + C::OVS + tok1 * C::VSB + 2 * grp));
+        T0 = make_tab<VB>(vcent, lds16(AOS ? st + C::OVC + tok0 * C::VREC + grp * C::VBB
+                                           : st + C::OVS + tok0 * C::VSB + 2 * grp));
+        T1 = make_tab<VB>(vcent, lds16(AOS ? st + C::OVC + tok1 * C::VREC + grp * C::VBB
+                                           : st + C::OVS + tok1 * C::VSB + 2 * grp));
       }
 #pragma unroll
       for (int s = 0; s < 4; ++s) {
@@ -649,10 +682,10 @@ __global__ void __launch_bounds__(kQjlM) qjl_prep_kernel(const uint16_t* __restr
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 }
 
-template <int D, int KB, int VB, bool KPV, bool VPV, bool QJL>
+template <int D, int KB, int VB, bool KPV, bool VPV, bool QJL, bool AOS = false>
 int launch_cfg(const CodecParams& PK, const CodecParams& PV, const TcArgs& a, int B, cudaStream_t st) {
-  using C = Cfg<D, KB, VB, KPV, VPV, QJL>;
-  auto kern = decode_tc_kernel<D, KB, VB, KPV, VPV, QJL>;
+  using C = Cfg<D, KB, VB, KPV, VPV, QJL, AOS>;
+  auto kern = decode_tc_kernel<D, KB, VB, KPV, VPV, QJL, AOS>;
   static bool attr_set[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return TQ_ERR_CUDA;
@@ -773,6 +806,49 @@ int launch_decode_tc(const CodecParams& PK, const CodecParams& PV, const tq_kv_v
                        : launch_cfg<128, 2, 3, false, false, false>(PK, PV, a, B, st);
   }
   return r;
+}
+
+// The block form (arrays of [fp16 norm | packed codes] 32-value blocks) on
+// the same kernel: head_dim 128 or 256, 4 q heads per KV head, K codes of 2-4
+// bits and V codes of 3 bits with one norm per 32 values, contiguous caches
+// whose arrays are 16-byte aligned with 16-byte multiples of row pitch.
+bool decode_tc_blocks_eligible(const CodecParams& PK, const CodecParams& PV, int G, int64_t S_cap,
+                               const uint8_t* k_blocks, const uint8_t* v_blocks) {
+  if (G != kG || PK.d != PV.d || (PK.d != 128 && PK.d != 256) || PV.bits != 3 || PK.bits < 2 || PK.bits > 4)
+    return false;
+  if (PK.blk != 32 || PV.blk != 32 || PK.m || PV.m) return false;
+  const int64_t krec = (int64_t)(PK.d / 32) * (2 + 4 * PK.bits), vrec = (int64_t)(PV.d / 32) * (2 + 4 * PV.bits);
+  if ((S_cap * krec) % 16 || (S_cap * vrec) % 16) return false;
+  return aligned16(k_blocks) && aligned16(v_blocks);
+}
+
+int launch_decode_tc_blocks(const CodecParams& PK, const CodecParams& PV, const uint8_t* k_blocks,
+                            const uint8_t* v_blocks, const uint16_t* q, const int32_t* kv_len, float* part, int B,
+                            int Hq, int Hkv, int64_t S_cap, int64_t ctx, int n_split, float qscale, cudaStream_t st) {
+  TcArgs a{};
+  a.kc = k_blocks;
+  a.vc = v_blocks;
+  a.q = q;
+  a.kv_len = kv_len;
+  a.part = part;
+  a.pages = {nullptr, 0, 0};
+  a.S_cap = S_cap;
+  a.ctx = ctx;
+  a.per = decode_tc_per_split(ctx, n_split);
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.n_split = n_split;
+  a.slots = n_split;
+  a.pdl = 0;
+  a.qscale = qscale;
+  if (PK.d == 256) {
+    return PK.bits == 4 ? launch_cfg<256, 4, 3, false, false, false, true>(PK, PV, a, B, st)
+           : PK.bits == 3 ? launch_cfg<256, 3, 3, false, false, false, true>(PK, PV, a, B, st)
+                          : launch_cfg<256, 2, 3, false, false, false, true>(PK, PV, a, B, st);
+  }
+  return PK.bits == 4 ? launch_cfg<128, 4, 3, false, false, false, true>(PK, PV, a, B, st)
+         : PK.bits == 3 ? launch_cfg<128, 3, 3, false, false, false, true>(PK, PV, a, B, st)
+                        : launch_cfg<128, 2, 3, false, false, false, true>(PK, PV, a, B, st);
 }
 
 }  // namespace tq

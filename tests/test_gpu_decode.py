@@ -58,6 +58,7 @@ CASES = [
     ("beta_pervec_d64", (64, 4, 0, 0, 5, 1), (64, 2, 0, 0, 6, 1), 1, 2, 2, 300, 280, 64),
     # 8-bit keys (one byte per code) beside 4- and 3-bit values
     ("k8v4_d128_gqa4", (32, 8, 0, 0, 1), (32, 4, 0, 0, 1), 2, 8, 2, 700, 650, 128),
+    ("k8v4_d128_gqa4_long", (32, 8, 0, 0, 2), (32, 4, 0, 0, 3), 1, 8, 2, 2048, 2000, 128),
     ("k8v4_pervec_d64_mha", (64, 8, 0, 0, 5), (64, 4, 0, 0, 6), 1, 2, 2, 300, 280, 64),
     ("k8nc_v3_d256_gqa8", (256, 8, 0, 1, 2), (32, 3, 0, 0, 3), 1, 8, 1, 200, 190, 256),
 ]

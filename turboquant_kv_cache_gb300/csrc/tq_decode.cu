@@ -28,7 +28,8 @@ bool decode_tc_eligible(const CodecParams& PK, const CodecParams& PV, int G, int
 size_t decode_tc_extra_bytes(int B, int Hq);
 int launch_decode_tc(const CodecParams& PK, const CodecParams& PV, const tq_kv_view* K, const tq_kv_view* V,
                      const uint16_t* q, const int32_t* kv_len, float* part, size_t part_bytes, int B, int Hq, int Hkv,
-                     int64_t S_cap, int64_t ctx, int n_split, int slots, bool pdl, float qscale, cudaStream_t st);
+                     int64_t S_cap, int64_t ctx, int n_split, int slots, bool pdl, float qscale, const Codebook8* cbk,
+                     cudaStream_t st);
 size_t decode_ws_bytes(int B, int Hq, int d, int n_split);
 
 namespace {
@@ -960,7 +961,7 @@ int decode_impl(const tq_kv_view* K, const tq_kv_view* V, const uint16_t* q, int
   }
   if (!PV.m && decode_tc_eligible(PK, PV, G, S_cap, K, V)) {
     st = launch_decode_tc(PK, PV, K, V, q, kv_len, a.part, decode_part_bytes(B, Hq, PK.d, slots), B, Hq, Hkv, S_cap,
-                          ctx, ns, slots, a.pdl != 0, a.qscale, s);
+                          ctx, ns, slots, a.pdl != 0, a.qscale, &cbk, s);
   } else {
     switch (PK.d) {
       case 64: st = launch_decode_g<64>(G, PK, PV, a, B, cbk, s); break;

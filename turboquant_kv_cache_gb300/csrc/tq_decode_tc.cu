@@ -34,6 +34,8 @@
 #include <cuda_runtime.h>
 #include <math.h>
 
+#include <type_traits>
+
 #include "tq_device.cuh"
 #include "tq_lut.cuh"
 
@@ -71,12 +73,21 @@ struct Cfg {
   static constexpr int OVC = OQR + kTok * QR;
   static constexpr int OVS = OVC + kTok * VREC;
   static constexpr int STAGE = OVS + kTok * VSB;
-  static constexpr size_t SMEM = (size_t)P * kSlots * STAGE      // rings
-                                 + (size_t)4 * kG * kTok * 2       // p per warp
-                                 + (NH > 1 ? (size_t)4 * 32 * 8 * 4 : 0);  // partial-score exchange
+  static constexpr size_t K8OFF = (size_t)P * kSlots * STAGE + (size_t)4 * kG * kTok * 2 +
+                                  (NH > 1 ? (size_t)4 * 32 * 8 * 4 : 0);
+  static constexpr size_t SMEM = K8OFF                             // rings, p per warp, score exchange
+                                 + (KB == 8 ? (size_t)256 * 32 * 4 : 0);   // 8-bit key table, one copy per lane
   static_assert(STAGE % 16 == 0 && OVC % 16 == 0, "stage sub-arrays stay 16-byte aligned");
   static_assert((size_t)P * kSlots * STAGE >= (size_t)P * kG * D * 4, "ring too small for the merge");
 };
+
+// fp16 centroids of the 256-level key codebook (8-bit keys only)
+struct K8Tab {
+  uint16_t c[256];
+};
+struct NoK8Tab {};
+template <int KB>
+using K8Param = typename std::conditional<KB == 8, K8Tab, NoK8Tab>::type;
 
 struct TcArgs {
   const uint8_t* kc;
@@ -234,7 +245,7 @@ __device__ __forceinline__ void group_words(uint32_t addr, uint32_t* w) {
 
 template <int D, int KB, int VB, bool KPV, bool VPV, bool QJL, bool AOS = false>
 __global__ void __launch_bounds__(kThreads, 4) decode_tc_kernel(const CodecParams PK, const CodecParams PV,
-                                                               const TcArgs a) {
+                                                               const TcArgs a, const K8Param<KB> k8) {
   using C = Cfg<D, KB, VB, KPV, VPV, QJL, AOS>;
   constexpr int NH = C::NH, P = C::P;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -357,12 +368,21 @@ __global__ void __launch_bounds__(kThreads, 4) decode_tc_kernel(const CodecParam
     sqs[1] = a.sqsum[(int64_t)b * a.Hq + h0 + ((2 * t + 1) & 3)];
   }
 
-  const Cent<KB> kcent = make_cent<KB>(PK);
+  // 8-bit keys: centroid c of lane l at k8base + 128 c + 4 l (fp16 in the low half)
+  uint32_t k8base = 0;
+  if constexpr (KB == 8) {
+    k8base = su32(smem + C::K8OFF);
+    uint32_t* t8 = reinterpret_cast<uint32_t*>(smem + C::K8OFF);
+    for (int e = tid; e < 256 * 32; e += kThreads) t8[e] = k8.c[e >> 5];
+    __syncthreads();
+    k8base += 4u * lane;
+  }
+  const Cent<KB == 8 ? 4 : KB> kcent = make_cent<KB == 8 ? 4 : KB>(PK);
   const Cent<VB> vcent = make_cent<VB>(PV);
   const uint32_t one_h = 0x3C00u;
   // tables that do not depend on the token
   Tab kfix, vfix;
-  if (KPV || KB == 4) kfix = make_tab<KB>(kcent, one_h);
+  if (KPV || KB == 4) kfix = make_tab<KB == 8 ? 4 : KB>(kcent, one_h);
   if (VPV) vfix = make_tab<VB>(vcent, one_h);
 
   float acc[4][2][4];
@@ -395,18 +415,26 @@ __global__ void __launch_bounds__(kThreads, 4) decode_tc_kernel(const CodecParam
       float Pm[4] = {0.f, 0.f, 0.f, 0.f};
       float Pq[4] = {0.f, 0.f, 0.f, 0.f};
       const int tok0 = 16 * u + g, tok1 = tok0 + 8;
-      uint32_t w0[4], w1[4], n0[4], n1[4];
-      group_words<KB, AOS>(st + C::OKC + tok0 * C::KREC + (AOS ? grp * C::KBB + 2 : grp * 4 * KB), w0);
-      group_words<KB, AOS>(st + C::OKC + tok1 * C::KREC + (AOS ? grp * C::KBB + 2 : grp * 4 * KB), w1);
-      chunk_words<KB>(w0, n0);
-      chunk_words<KB>(w1, n1);
+      uint32_t w0[KB == 8 ? 8 : 4], w1[KB == 8 ? 8 : 4], n0[4], n1[4];
+      if constexpr (KB == 8) {
+        // one byte per code: the group's 32 codes are 32 bytes
+        const uint32_t a0 = st + C::OKC + tok0 * C::KREC + grp * 32, a1 = st + C::OKC + tok1 * C::KREC + grp * 32;
+        const uint4 u0 = lds128(a0), u1 = lds128(a0 + 16), v0 = lds128(a1), v1 = lds128(a1 + 16);
+        w0[0] = u0.x; w0[1] = u0.y; w0[2] = u0.z; w0[3] = u0.w; w0[4] = u1.x; w0[5] = u1.y; w0[6] = u1.z; w0[7] = u1.w;
+        w1[0] = v0.x; w1[1] = v0.y; w1[2] = v0.z; w1[3] = v0.w; w1[4] = v1.x; w1[5] = v1.y; w1[6] = v1.z; w1[7] = v1.w;
+      } else {
+        group_words<KB, AOS>(st + C::OKC + tok0 * C::KREC + (AOS ? grp * C::KBB + 2 : grp * 4 * KB), w0);
+        group_words<KB, AOS>(st + C::OKC + tok1 * C::KREC + (AOS ? grp * C::KBB + 2 : grp * 4 * KB), w1);
+        chunk_words<KB>(w0, n0);
+        chunk_words<KB>(w1, n1);
+      }
       // the group's norm: its block header (AOS) or the norm stream
       auto knorm = [&](int tok) {
         return lds16(AOS ? st + C::OKC + tok * C::KREC + grp * C::KBB : st + C::OKS + tok * C::KSB + 2 * grp);
       };
       Tab T0, T1;
       uint32_t s0h = 0, s1h = 0;
-      if (KPV || KB == 4) {
+      if (KPV || KB == 4 || KB == 8) {
         T0 = kfix;
         T1 = kfix;
         if (!KPV) {
@@ -416,15 +444,31 @@ __global__ void __launch_bounds__(kThreads, 4) decode_tc_kernel(const CodecParam
           s1h |= s1h << 16;
         }
       } else {
-        T0 = make_tab<KB>(kcent, knorm(tok0));
-        T1 = make_tab<KB>(kcent, knorm(tok1));
+        T0 = make_tab<KB == 8 ? 4 : KB>(kcent, knorm(tok0));
+        T1 = make_tab<KB == 8 ? 4 : KB>(kcent, knorm(tok1));
       }
 #pragma unroll
       for (int s = 0; s < 4; ++s) {
         uint32_t x0[4], x1[4];
-        lut8<KB>(n0[s], T0, x0);
-        lut8<KB>(n1[s], T1, x1);
-        if (KB == 4 && !KPV) {
+        if constexpr (KB == 8) {
+          // codes 8s .. 8s+7 are bytes of words 2s, 2s+1; each pair of
+          // table words gives an fp16 pair (low halves)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const uint32_t wa = w0[2 * s + (e >> 1)], wb = w1[2 * s + (e >> 1)];
+            const int sh = 16 * (e & 1);
+            const uint32_t lo0 = lds32(k8base + (((wa >> sh) & 0xFFu) << 7));
+            const uint32_t hi0 = lds32(k8base + (((wa >> (sh + 8)) & 0xFFu) << 7));
+            const uint32_t lo1 = lds32(k8base + (((wb >> sh) & 0xFFu) << 7));
+            const uint32_t hi1 = lds32(k8base + (((wb >> (sh + 8)) & 0xFFu) << 7));
+            x0[e] = prmt(lo0, hi0, 0x5410u);
+            x1[e] = prmt(lo1, hi1, 0x5410u);
+          }
+        } else {
+          lut8<KB>(n0[s], T0, x0);
+          lut8<KB>(n1[s], T1, x1);
+        }
+        if ((KB == 4 || KB == 8) && !KPV) {
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             x0[e] = hmul2(x0[e], s0h);
@@ -683,7 +727,8 @@ __global__ void __launch_bounds__(kQjlM) qjl_prep_kernel(const uint16_t* __restr
 }
 
 template <int D, int KB, int VB, bool KPV, bool VPV, bool QJL, bool AOS = false>
-int launch_cfg(const CodecParams& PK, const CodecParams& PV, const TcArgs& a, int B, cudaStream_t st) {
+int launch_cfg(const CodecParams& PK, const CodecParams& PV, const TcArgs& a, int B, cudaStream_t st,
+               const K8Param<KB>& k8 = K8Param<KB>{}) {
   using C = Cfg<D, KB, VB, KPV, VPV, QJL, AOS>;
   auto kern = decode_tc_kernel<D, KB, VB, KPV, VPV, QJL, AOS>;
   static bool attr_set[64] = {};
@@ -704,7 +749,7 @@ int launch_cfg(const CodecParams& PK, const CodecParams& PV, const TcArgs& a, in
   attr[0].val.programmaticStreamSerializationAllowed = (QJL || a.pdl) ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, kern, PK, PV, a) != cudaSuccess) return TQ_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, kern, PK, PV, a, k8) != cudaSuccess) return TQ_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }
 
@@ -712,14 +757,18 @@ int launch_cfg(const CodecParams& PK, const CodecParams& PV, const TcArgs& a, in
 
 // Eligible layouts: head_dim 128 or 256 with 4 q heads per KV head; K codes
 // of 2-4 bits, V codes of 3 bits, each with one norm per 32 values or per
-// vector (the combinations instantiated below); QJL keys with m = 128 on
+// vector (the combinations instantiated below); 8-bit K with 4-bit V, one
+// norm per 32 values, at head_dim 128; QJL keys with m = 128 on
 // 2-bit per-vector K at head_dim 128; every array 16-byte aligned and every
 // per-token stream's row pitch (S_cap times its bytes per token) a multiple
 // of 16.
 bool decode_tc_eligible(const CodecParams& PK, const CodecParams& PV, int G, int64_t S_cap, const tq_kv_view* K,
                         const tq_kv_view* V) {
-  if (G != kG || PK.d != PV.d || (PK.d != 128 && PK.d != 256) || PV.bits != 3) return false;
+  if (G != kG || PK.d != PV.d || (PK.d != 128 && PK.d != 256)) return false;
   const bool kpv = PK.blk == PK.d, vpv = PV.blk == PV.d;
+  // 8-bit keys beside 4-bit values (k8v4), one norm per 32 values, head_dim 128
+  const bool k8v4 = PK.bits == 8 && PV.bits == 4 && PK.d == 128 && PK.blk == 32 && PV.blk == 32 && !PK.m && !PV.m;
+  if (PV.bits != 3 && !k8v4) return false;
   // every per-token stream must keep 16-byte aligned rows for cp.async
   const int64_t streams[6] = {PK.code_bytes, 2 * PK.nb, PK.qjl_bytes, PK.m ? 2 : 0, PV.code_bytes, 2 * PV.nb};
   // (a paged cache's rows are its pages)
@@ -728,7 +777,9 @@ bool decode_tc_eligible(const CodecParams& PK, const CodecParams& PV, int G, int
     if ((row * streams[i]) % 16 != 0) return false;
   if ((!kpv && PK.blk != 32) || (!vpv && PV.blk != 32)) return false;
   bool ok;
-  if (PK.d == 256) {
+  if (k8v4) {
+    ok = true;
+  } else if (PK.d == 256) {
     ok = !kpv && !vpv && !PK.m && PK.bits >= 2 && PK.bits <= 4;
   } else if (PK.m) {
     ok = PK.m == kQjlM && kpv && vpv && PK.bits == 2;
@@ -758,7 +809,8 @@ size_t decode_tc_extra_bytes(int B, int Hq) {
 // the caller merges them (decode_combine).
 int launch_decode_tc(const CodecParams& PK, const CodecParams& PV, const tq_kv_view* K, const tq_kv_view* V,
                      const uint16_t* q, const int32_t* kv_len, float* part, size_t part_bytes, int B, int Hq, int Hkv,
-                     int64_t S_cap, int64_t ctx, int n_split, int slots, bool pdl, float qscale, cudaStream_t st) {
+                     int64_t S_cap, int64_t ctx, int n_split, int slots, bool pdl, float qscale, const Codebook8* cbk,
+                     cudaStream_t st) {
   TcArgs a{};
   a.kc = K->codes;
   a.ks = reinterpret_cast<const uint8_t*>(K->scales);
@@ -790,7 +842,15 @@ int launch_decode_tc(const CodecParams& PK, const CodecParams& PV, const tq_kv_v
   }
   const bool kpv = PK.blk == PK.d, vpv = PV.blk == PV.d;
   int r;
-  if (PK.d == 256) {
+  if (PK.bits == 8) {
+    if (!cbk) return TQ_ERR_ARG;
+    K8Tab tab;
+    for (int k = 0; k < 256; ++k) {
+      const __half h = __float2half_rn(cbk->c[k]);
+      tab.c[k] = *reinterpret_cast<const uint16_t*>(&h);
+    }
+    r = launch_cfg<128, 8, 4, false, false, false>(PK, PV, a, B, st, tab);
+  } else if (PK.d == 256) {
     r = PK.bits == 4 ? launch_cfg<256, 4, 3, false, false, false>(PK, PV, a, B, st)
         : PK.bits == 3 ? launch_cfg<256, 3, 3, false, false, false>(PK, PV, a, B, st)
                        : launch_cfg<256, 2, 3, false, false, false>(PK, PV, a, B, st);

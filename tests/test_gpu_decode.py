@@ -297,11 +297,18 @@ def test_decode_window_argument_errors(tqlib):
 
 
 QJL_V_CASES = [
-    # QJL residual on V (CUDA-core kernel): name, K (block, bits, m, nc, seed), V, B, Hq, Hkv, S_cap, ctx, kv_len, d
+    # QJL residual on V: name, K (block, bits, m, nc, seed), V, B, Hq, Hkv, S_cap, ctx, kv_len, d
     ("v2bit_qjl_gqa4", (32, 3, 0, 0, 1), (128, 2, 128, 0, 2), 2, 8, 2, 400, 391, [391, 100], 128),
     ("qjl_k_and_v", (128, 2, 128, 0, 1), (128, 2, 128, 0, 3), 2, 8, 2, 300, 300, None, 128),
     ("v3bit_qjl64_nc_d64", (64, 3, 0, 0, 4), (64, 3, 64, 1, 5), 1, 2, 2, 260, 257, None, 64),
     ("v1bit_qjl_d256_gqa8", (32, 4, 0, 0, 1), (256, 1, 128, 0, 6), 1, 8, 1, 150, 150, None, 256),
+    # on the tensor-core decode (4 q heads per KV head, head_dim 128, 2-bit per-vector K with or without
+    # QJL, 2/3-bit per-vector V with m = 128, row pitches a multiple of 16 bytes): ragged lengths, one
+    # empty row, several steps per split
+    ("qjl_k_and_v_tc", (128, 2, 128, 0, 1), (128, 2, 128, 0, 3), 2, 8, 2, 320, 300, [300, 177], 128),
+    ("v2bit_qjl_kpv2_tc", (128, 2, 0, 0, 1), (128, 2, 128, 0, 2), 1, 16, 4, 400, 391, None, 128),
+    ("v3bit_qjl_tc", (128, 2, 128, 0, 1), (128, 3, 128, 0, 5), 2, 4, 1, 256, 256, [256, 0], 128),
+    ("v3bit_qjl_nokq_long_tc", (128, 2, 0, 0, 4), (128, 3, 128, 0, 6), 1, 8, 2, 2048, 2000, None, 128),
 ]
 
 

@@ -17,7 +17,8 @@
 
 namespace tq {
 
-int decode_auto_splits(int B, int Hkv, int64_t ctx);
+int decode_auto_splits(int B, int Hkv, int64_t ctx, int per_sm = 4);
+int decode_tc_ctas_per_sm(const CodecParams& PV);
 bool decode_tc_blocks_eligible(const CodecParams& PK, const CodecParams& PV, int G, int64_t S_cap,
                                const uint8_t* k_blocks, const uint8_t* v_blocks);
 int launch_decode_tc_blocks(const CodecParams& PK, const CodecParams& PV, const uint8_t* k_blocks,
@@ -855,10 +856,10 @@ int sm_count() {
   return sms;
 }
 
-int decode_auto_splits(int B, int Hkv, int64_t ctx) {
-  // one wave at four 4-warp CTAs per SM
+int decode_auto_splits(int B, int Hkv, int64_t ctx, int per_sm) {
+  // one wave at per_sm (default four) 4-warp CTAs per SM
   const int units = B * Hkv;
-  int want = (4 * sm_count()) / units;
+  int want = (per_sm * sm_count()) / units;
   const int64_t max_by_len = (ctx + 255) / 256;
   if (want > max_by_len) want = (int)max_by_len;
   if (want < 1) want = 1;
@@ -924,7 +925,9 @@ int decode_impl(const tq_kv_view* K, const tq_kv_view* V, const uint16_t* q, int
   if (!aligned16(K->codes) || !aligned16(V->codes) || !aligned16(q) || !aligned16(out)) return TQ_ERR_ALIGN;
   if (win && (reinterpret_cast<uintptr_t>(win->k) % 8 || reinterpret_cast<uintptr_t>(win->v) % 8))
     return TQ_ERR_ALIGN;
-  const int ns = n_split ? n_split : decode_auto_splits(B, Hkv, ctx);
+  const int G = Hq / Hkv;
+  const bool tc = decode_tc_eligible(PK, PV, G, S_cap, K, V);
+  const int ns = n_split ? n_split : decode_auto_splits(B, Hkv, ctx, tc ? decode_tc_ctas_per_sm(PV) : 4);
   const int slots = ns + (win ? 1 : 0);
   const size_t need = decode_ws_bytes(B, Hq, PK.d, slots);
   if (!workspace || workspace_bytes < need) return TQ_ERR_WORKSPACE;
@@ -938,7 +941,6 @@ int decode_impl(const tq_kv_view* K, const tq_kv_view* V, const uint16_t* q, int
                {K->page_table, K->page_table ? K->page_size : 0, K->page_table ? K->pages_per_seq : 0},
                S_cap, ctx, Hq, Hkv, ns, slots, sm * kLog2e, 0};
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int G = Hq / Hkv;
   if (win) {
     // the window's partial first; the split kernel overlaps it
     const int units = B * Hkv;
@@ -959,7 +961,7 @@ int decode_impl(const tq_kv_view* K, const tq_kv_view* V, const uint16_t* q, int
     if (cudaGetLastError() != cudaSuccess) return TQ_ERR_CUDA;
     a.pdl = 1;
   }
-  if (!PV.m && decode_tc_eligible(PK, PV, G, S_cap, K, V)) {
+  if (tc) {
     st = launch_decode_tc(PK, PV, K, V, q, kv_len, a.part, decode_part_bytes(B, Hq, PK.d, slots), B, Hq, Hkv, S_cap,
                           ctx, ns, slots, a.pdl != 0, a.qscale, &cbk, s);
   } else {

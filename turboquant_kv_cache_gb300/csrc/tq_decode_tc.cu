@@ -55,7 +55,8 @@ constexpr float kLazy = 8.0f;  // rescale threshold, log2 units
 // AOS: the caches are arrays of 32-value blocks, [fp16 norm | packed codes of
 // the group] (2 + 4*bits bytes), a token's blocks contiguous; a token's record
 // holds its norms, so there is no separate norm stream.
-template <int D, int KB, int VB, bool KPV, bool VPV, bool QJL, bool AOS = false>
+// QV: values with a QJL residual (m = 128, one norm per vector, head_dim 128).
+template <int D, int KB, int VB, bool KPV, bool VPV, bool QJL, bool AOS = false, bool QV = false>
 struct Cfg {
   static constexpr int NH = D / 128;  // warps per pipeline
   static constexpr int P = 4 / NH;    // pipelines per CTA
@@ -72,13 +73,19 @@ struct Cfg {
   static constexpr int OQR = OQB + kTok * QB;
   static constexpr int OVC = OQR + kTok * QR;
   static constexpr int OVS = OVC + kTok * VREC;
-  static constexpr int STAGE = OVS + kTok * VSB;
+  static constexpr int VQB = QV ? kQjlM / 8 : 0;   // V QJL sign bits per token
+  static constexpr int VQR = QV ? 2 : 0;           // V rho per token
+  static constexpr int OVQ = OVS + kTok * VSB;
+  static constexpr int OVR = OVQ + kTok * VQB;
+  static constexpr int STAGE = OVR + kTok * VQR;
+  static constexpr int MINB = QV ? 3 : 4;          // CTAs per SM the register budget is cut for
   static constexpr size_t K8OFF = (size_t)P * kSlots * STAGE + (size_t)4 * kG * kTok * 2 +
                                   (NH > 1 ? (size_t)4 * 32 * 8 * 4 : 0);
   static constexpr size_t SMEM = K8OFF                             // rings, p per warp, score exchange
                                  + (KB == 8 ? (size_t)256 * 32 * 4 : 0);   // 8-bit key table, one copy per lane
   static_assert(STAGE % 16 == 0 && OVC % 16 == 0, "stage sub-arrays stay 16-byte aligned");
-  static_assert((size_t)P * kSlots * STAGE >= (size_t)P * kG * D * 4, "ring too small for the merge");
+  static_assert((size_t)P * kSlots * STAGE >= (size_t)P * kG * D * 4 + (QV ? (size_t)(P + 2) * kG * kQjlM * 4 : 0),
+                "ring too small for the merge");
 };
 
 // fp16 centroids of the 256-level key codebook (8-bit keys only)
@@ -96,6 +103,9 @@ struct TcArgs {
   const uint8_t* kr;   // QJL rho
   const uint8_t* vc;
   const uint8_t* vs;
+  const uint8_t* vq;   // V QJL bits
+  const uint8_t* vr;   // V QJL rho
+  const float* Sv;     // V's QJL matrix [128][D]
   const uint16_t* q;
   const uint16_t* sq;  // S q * scale, fp16 [B*Hq][128] (QJL)
   const float* sqsum;  // per-head sum of sq (QJL)
@@ -243,10 +253,10 @@ __device__ __forceinline__ void group_words(uint32_t addr, uint32_t* w) {
   }
 }
 
-template <int D, int KB, int VB, bool KPV, bool VPV, bool QJL, bool AOS = false>
-__global__ void __launch_bounds__(kThreads, 4) decode_tc_kernel(const CodecParams PK, const CodecParams PV,
-                                                               const TcArgs a, const K8Param<KB> k8) {
-  using C = Cfg<D, KB, VB, KPV, VPV, QJL, AOS>;
+template <int D, int KB, int VB, bool KPV, bool VPV, bool QJL, bool AOS = false, bool QV = false>
+__global__ void __launch_bounds__(kThreads, Cfg<D, KB, VB, KPV, VPV, QJL, AOS, QV>::MINB)
+    decode_tc_kernel(const CodecParams PK, const CodecParams PV, const TcArgs a, const K8Param<KB> k8) {
+  using C = Cfg<D, KB, VB, KPV, VPV, QJL, AOS, QV>;
   constexpr int NH = C::NH, P = C::P;
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ float s_ml[4][2][kG];
@@ -284,6 +294,10 @@ __global__ void __launch_bounds__(kThreads, 4) decode_tc_kernel(const CodecParam
       }
       copy_full<C::VREC, NH>(dst + C::OVC, a.vc + tok0 * C::VREC, plane);
       copy_full<C::VSB, NH>(dst + C::OVS, a.vs + tok0 * C::VSB, plane);
+      if (QV) {
+        copy_full<C::VQB, NH>(dst + C::OVQ, a.vq + tok0 * C::VQB, plane);
+        copy_full<C::VQR, NH>(dst + C::OVR, a.vr + tok0 * C::VQR, plane);
+      }
     } else {
       const int nv = (int)rem;
       copy_part<C::KREC, NH>(dst + C::OKC, a.kc, tok0, nv, plane);
@@ -294,6 +308,10 @@ __global__ void __launch_bounds__(kThreads, 4) decode_tc_kernel(const CodecParam
       }
       copy_part<C::VREC, NH>(dst + C::OVC, a.vc, tok0, nv, plane);
       copy_part<C::VSB, NH>(dst + C::OVS, a.vs, tok0, nv, plane);
+      if (QV) {
+        copy_part<C::VQB, NH>(dst + C::OVQ, a.vq, tok0, nv, plane);
+        copy_part<C::VQR, NH>(dst + C::OVR, a.vr, tok0, nv, plane);
+      }
     }
     ++ld_it;
   };
@@ -390,6 +408,11 @@ __global__ void __launch_bounds__(kThreads, 4) decode_tc_kernel(const CodecParam
   for (int s = 0; s < 4; ++s)
 #pragma unroll
     for (int pr = 0; pr < 2; ++pr) acc[s][pr][0] = acc[s][pr][1] = acc[s][pr][2] = acc[s][pr][3] = 0.f;
+  // QV: Z[j][head] = sum_t rho_t (2 s_tj - 1) p_t norm_t, rows j in 8 tiles of 16
+  // (same fragment layout as acc: row 16 mt + g (+8), heads of columns 2t, 2t+1)
+  float zq[QV ? 8 : 1][4];
+#pragma unroll
+  for (int mt = 0; mt < (QV ? 8 : 1); ++mt) zq[mt][0] = zq[mt][1] = zq[mt][2] = zq[mt][3] = 0.f;
   // running max / partial sums of the lane's heads 2(t&1), 2(t&1)+1
   float m_run[2] = {-INFINITY, -INFINITY}, l_part[2] = {0.f, 0.f};
   const uint32_t pBase = su32(smem + (size_t)P * kSlots * C::STAGE) + wid * kG * kTok * 2;
@@ -567,6 +590,15 @@ __global__ void __launch_bounds__(kThreads, 4) decode_tc_kernel(const CodecParam
           acc[s][pr][2] *= al[0];
           acc[s][pr][3] *= al[1];
         }
+      if (QV) {
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+          zq[mt][0] *= al[0];
+          zq[mt][1] *= al[1];
+          zq[mt][2] *= al[0];
+          zq[mt][3] *= al[1];
+        }
+      }
     }
 #pragma unroll
     for (int u = 0; u < 2; ++u)
@@ -618,6 +650,37 @@ __global__ void __launch_bounds__(kThreads, 4) decode_tc_kernel(const CodecParam
           mma16816(acc[s][pr], movtrans(x0[pr]), movtrans(x0[pr + 2]), movtrans(x1[pr]), movtrans(x1[pr + 2]), pb0,
                    pb1);
       }
+      if constexpr (QV) {
+        // A = rho_t (2 s_tj - 1) as fp16, rows j, columns the tokens of this
+        // k step: the lane's columns are tokens ta, ta+1 and tb, tb+1.  Sign
+        // word w of a token shifted so that bit 32 w + 8 k + g lands on bit
+        // 8 k + 7; a byte permute brings the bits of two tokens to bits 15 and
+        // 31, and one logic op keeps them inverted (set where s = 0) and signs
+        // the rho pair with them.
+        const int ta = 16 * u + 2 * t, tb = ta + 8;
+        const uint32_t ra = lds32(st + C::OVR + 2 * ta), rb = lds32(st + C::OVR + 2 * tb);
+        const uint4 qa0 = lds128(st + C::OVQ + 16 * ta), qa1 = lds128(st + C::OVQ + 16 * (ta + 1));
+        const uint4 qb0 = lds128(st + C::OVQ + 16 * tb), qb1 = lds128(st + C::OVQ + 16 * (tb + 1));
+        const uint32_t sh = 7 - g;
+        const uint32_t wa0[4] = {qa0.x, qa0.y, qa0.z, qa0.w}, wa1[4] = {qa1.x, qa1.y, qa1.z, qa1.w};
+        const uint32_t wb0[4] = {qb0.x, qb0.y, qb0.z, qb0.w}, wb1[4] = {qb1.x, qb1.y, qb1.z, qb1.w};
+#pragma unroll
+        for (int wi = 0; wi < 4; ++wi) {
+          const uint32_t xa0 = wa0[wi] << sh, xa1 = wa1[wi] << sh;
+          const uint32_t xb0 = wb0[wi] << sh, xb1 = wb1[wi] << sh;
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {   // row tiles mt = 2 wi + hf: rows 32 wi + 16 hf + g (+8)
+            const int mt = 2 * wi + hf, k0 = 2 * hf, k1 = 2 * hf + 1;
+            // result bytes 1 and 3 take byte k of the first and second token
+            const uint32_t s0 = (uint32_t)((4 + k0) << 12 | k0 << 4), s1 = (uint32_t)((4 + k1) << 12 | k1 << 4);
+            const uint32_t r0 = (~prmt(xa0, xa1, s0) & 0x80008000u) ^ ra;   // row 16 mt + g, tokens ta, ta+1
+            const uint32_t r1 = (~prmt(xa0, xa1, s1) & 0x80008000u) ^ ra;   // row + 8
+            const uint32_t r2 = (~prmt(xb0, xb1, s0) & 0x80008000u) ^ rb;   // row, tokens tb, tb+1
+            const uint32_t r3 = (~prmt(xb0, xb1, s1) & 0x80008000u) ^ rb;
+            mma16816(zq[mt], r0, r1, r2, r3, pb0, pb1);
+          }
+        }
+      }
     }
     __syncwarp();
   }
@@ -662,8 +725,96 @@ __global__ void __launch_bounds__(kThreads, 4) decode_tc_kernel(const CodecParam
         s_ml[pi][1][2 * t + c] = l_run[c];
       }
     }
+    if (QV && t < 2) {
+      float* zw = sO + P * kG * D + pi * kG * kQjlM;   // [P][kG][128]
+#pragma unroll
+      for (int mt = 0; mt < (QV ? 8 : 0); ++mt) {
+        const int j = 16 * mt + g;
+        zw[(2 * t) * kQjlM + j] = zq[mt][0];
+        zw[(2 * t + 1) * kQjlM + j] = zq[mt][1];
+        zw[(2 * t) * kQjlM + j + 8] = zq[mt][2];
+        zw[(2 * t + 1) * kQjlM + j + 8] = zq[mt][3];
+      }
+    }
   }
   __syncthreads();
+  // QV: the pipelines' sign sums merged with the softmax weights, then
+  // sqrt(pi/2)/m S^T of them (input domain), then into V's coded domain: D
+  // signs and the block's Walsh-Hadamard transform over sqrt(blk)
+  float* s_prj = sO + P * kG * D + P * kG * kQjlM + kG * kQjlM;   // [kG][D]
+  if constexpr (QV) {
+    float* s_az = sO + P * kG * D + P * kG * kQjlM;              // [kG][128]
+    const float* zs = sO + P * kG * D;
+    for (int e = tid; e < kG * kQjlM; e += kThreads) {
+      const int h = e / kQjlM;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < P; ++w) M = fmaxf(M, s_ml[w][0][h]);
+      float v = 0.f;
+#pragma unroll
+      for (int w = 0; w < P; ++w) {
+        const float mw = s_ml[w][0][h];
+        v += (mw == -INFINITY ? 0.f : exp2f(mw - M)) * zs[w * kG * kQjlM + e];
+      }
+      s_az[e] = v;
+    }
+    __syncthreads();
+    // warp w: rows 32 w .. 32 w + 31 of S, lane l: columns 4 l .. 4 l + 3;
+    // the four warps' partial products meet in the (now free) sign-sum area
+    static_assert(kThreads == 128 && kG == 4 && D == 128 && kQjlM == 128, "QV layout: 4 warps x 32 rows x 128 columns");
+    float* red = sO + P * kG * D;   // [4 warps][kG][D]
+    {
+      const int j0 = 32 * wid, c0 = 4 * lane;
+      const float4* sp = reinterpret_cast<const float4*>(a.Sv + (int64_t)j0 * D + c0);
+      float v[kG][4] = {};
+#pragma unroll 8
+      for (int jj = 0; jj < 32; ++jj) {
+        const float4 s4 = __ldg(sp + jj * (D / 4));
+#pragma unroll
+        for (int h = 0; h < kG; ++h) {
+          const float z = s_az[h * kQjlM + j0 + jj];
+          v[h][0] = fmaf(s4.x, z, v[h][0]);
+          v[h][1] = fmaf(s4.y, z, v[h][1]);
+          v[h][2] = fmaf(s4.z, z, v[h][2]);
+          v[h][3] = fmaf(s4.w, z, v[h][3]);
+        }
+      }
+#pragma unroll
+      for (int h = 0; h < kG; ++h) sts128f(su32(red + (wid * kG + h) * D + c0), v[h][0], v[h][1], v[h][2], v[h][3]);
+    }
+    __syncthreads();
+    // warp h: head h.  Sum the partials, sqrt(pi/2)/m, V's signs D, then the
+    // unnormalised 128-point Walsh-Hadamard (one V block per vector): strides
+    // 1 and 2 inside the lane, 4 .. 64 across lanes
+    {
+      const int h = wid, c0 = 4 * lane;
+      const float coef = kSqrtHalfPi / (float)kQjlM;
+      const uint32_t sb = PV.sign_bits[c0 >> 5] >> (c0 & 31);
+      float x[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float v = 0.f;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) v += red[(w * kG + h) * D + c0 + e];
+        x[e] = flip(v * coef, (sb >> e) & 1u);
+      }
+      float y0 = x[0] + x[1], y1 = x[0] - x[1], y2 = x[2] + x[3], y3 = x[2] - x[3];
+      x[0] = y0 + y2;
+      x[2] = y0 - y2;
+      x[1] = y1 + y3;
+      x[3] = y1 - y3;
+#pragma unroll
+      for (int m = 1; m < 32; m <<= 1) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float o = __shfl_xor_sync(kFull, x[e], m);
+          x[e] = (lane & m) ? o - x[e] : x[e] + o;
+        }
+      }
+      sts128f(su32(s_prj + h * D + c0), x[0], x[1], x[2], x[3]);
+    }
+    __syncthreads();
+  }
   for (int e = tid; e < kG * (D + 2); e += kThreads) {
     const int h = e / (D + 2), i = e % (D + 2);
     float M = -INFINITY;
@@ -679,6 +830,7 @@ __global__ void __launch_bounds__(kThreads, 4) decode_tc_kernel(const CodecParam
         const float wt = mw == -INFINITY ? 0.f : exp2f(mw - M);
         val += wt * (i == 1 ? s_ml[w][1][h] : sO[(w * kG + h) * D + i - 2]);
       }
+      if (QV && i >= 2) val += s_prj[h * D + i - 2] * PV.inv_sqrt_blk;
     }
     a.part[(((int64_t)b * a.Hq + h0 + h) * a.slots + split) * (D + 4) + i] = val;
   }
@@ -688,23 +840,32 @@ __global__ void __launch_bounds__(kThreads, 4) decode_tc_kernel(const CodecParam
 
 // S q of every (batch, q head) for QJL keys, times softmax_scale * log2 e *
 // sqrt(pi/2) / m, rounded to fp16, and the sum of each row of it.  One CTA
-// per (batch, KV head) serves its 4 q heads; thread i owns row i of S.
+// per (batch, KV head) serves its 4 q heads; thread i owns row i of S.  The
+// decode launched after it may start at once (its CTAs stage their first
+// cache steps, then wait for this grid to finish before reading S q); the
+// whole row of S is loaded before q, one round trip for both.
+template <int D>
 __global__ void __launch_bounds__(kQjlM) qjl_prep_kernel(const uint16_t* __restrict__ q, const float* __restrict__ S,
-                                                         int d, float coef, uint16_t* __restrict__ sq,
+                                                         float coef, uint16_t* __restrict__ sq,
                                                          float* __restrict__ sqsum) {
-  __shared__ float s_q[kG][kMaxDim];
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+  __shared__ __align__(16) float s_q[kG][D];
   __shared__ float s_red[kG][kQjlM / 32];
   const int grp = blockIdx.x, i = threadIdx.x;  // rows grp*4 .. grp*4+3 of q
-  for (int e = i; e < kG * d; e += kQjlM) s_q[e / d][e % d] = h2f(q[(int64_t)grp * kG * d + e]);
+  float4 sr[D / 4];
+  const float4* Si = reinterpret_cast<const float4*>(S + (int64_t)i * D);
+#pragma unroll
+  for (int j4 = 0; j4 < D / 4; ++j4) sr[j4] = __ldg(Si + j4);
+  for (int e = i; e < kG * D; e += kQjlM) s_q[e / D][e % D] = h2f(q[(int64_t)grp * kG * D + e]);
   __syncthreads();
   float v[kG] = {0.f, 0.f, 0.f, 0.f};
-  const float4* Si = reinterpret_cast<const float4*>(S + (int64_t)i * d);
-  for (int j4 = 0; j4 < d / 4; ++j4) {
-    const float4 sv = Si[j4];
+#pragma unroll
+  for (int j4 = 0; j4 < D / 4; ++j4) {
+    const float4 sv = sr[j4];
 #pragma unroll
     for (int h = 0; h < kG; ++h) {
-      const float* qh = s_q[h] + 4 * j4;
-      v[h] = fmaf(sv.x, qh[0], fmaf(sv.y, qh[1], fmaf(sv.z, qh[2], fmaf(sv.w, qh[3], v[h]))));
+      const float4 qh = *reinterpret_cast<const float4*>(s_q[h] + 4 * j4);
+      v[h] = fmaf(sv.x, qh.x, fmaf(sv.y, qh.y, fmaf(sv.z, qh.z, fmaf(sv.w, qh.w, v[h]))));
     }
   }
 #pragma unroll
@@ -723,14 +884,13 @@ __global__ void __launch_bounds__(kQjlM) qjl_prep_kernel(const uint16_t* __restr
     for (int w = 0; w < kQjlM / 32; ++w) tot += s_red[i][w];
     sqsum[(int64_t)grp * kG + i] = tot;
   }
-  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 }
 
-template <int D, int KB, int VB, bool KPV, bool VPV, bool QJL, bool AOS = false>
+template <int D, int KB, int VB, bool KPV, bool VPV, bool QJL, bool AOS = false, bool QV = false>
 int launch_cfg(const CodecParams& PK, const CodecParams& PV, const TcArgs& a, int B, cudaStream_t st,
                const K8Param<KB>& k8 = K8Param<KB>{}) {
-  using C = Cfg<D, KB, VB, KPV, VPV, QJL, AOS>;
-  auto kern = decode_tc_kernel<D, KB, VB, KPV, VPV, QJL, AOS>;
+  using C = Cfg<D, KB, VB, KPV, VPV, QJL, AOS, QV>;
+  auto kern = decode_tc_kernel<D, KB, VB, KPV, VPV, QJL, AOS, QV>;
   static bool attr_set[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return TQ_ERR_CUDA;
@@ -759,25 +919,33 @@ int launch_cfg(const CodecParams& PK, const CodecParams& PV, const TcArgs& a, in
 // of 2-4 bits, V codes of 3 bits, each with one norm per 32 values or per
 // vector (the combinations instantiated below); 8-bit K with 4-bit V, one
 // norm per 32 values, at head_dim 128; QJL keys with m = 128 on
-// 2-bit per-vector K at head_dim 128; every array 16-byte aligned and every
-// per-token stream's row pitch (S_cap times its bytes per token) a multiple
-// of 16.
+// 2-bit per-vector K at head_dim 128; values with a QJL residual (m = 128)
+// on 2- or 3-bit per-vector V at head_dim 128, beside 2-bit per-vector K with
+// or without QJL keys; every array 16-byte aligned and every per-token
+// stream's row pitch (S_cap times its bytes per token) a multiple of 16.
 bool decode_tc_eligible(const CodecParams& PK, const CodecParams& PV, int G, int64_t S_cap, const tq_kv_view* K,
                         const tq_kv_view* V) {
   if (G != kG || PK.d != PV.d || (PK.d != 128 && PK.d != 256)) return false;
   const bool kpv = PK.blk == PK.d, vpv = PV.blk == PV.d;
   // 8-bit keys beside 4-bit values (k8v4), one norm per 32 values, head_dim 128
   const bool k8v4 = PK.bits == 8 && PV.bits == 4 && PK.d == 128 && PK.blk == 32 && PV.blk == 32 && !PK.m && !PV.m;
-  if (PV.bits != 3 && !k8v4) return false;
+  // values with a QJL residual: m = 128, one norm per vector, 2- or 3-bit
+  // codes, beside 2-bit per-vector keys (with or without QJL keys of m = 128)
+  const bool qv = PV.m != 0;
+  if (qv && !(PV.m == kQjlM && vpv && PK.d == 128 && (PV.bits == 2 || PV.bits == 3) && kpv && PK.bits == 2 &&
+              (!PK.m || PK.m == kQjlM)))
+    return false;
+  if (PV.bits != 3 && !k8v4 && !qv) return false;
   // every per-token stream must keep 16-byte aligned rows for cp.async
-  const int64_t streams[6] = {PK.code_bytes, 2 * PK.nb, PK.qjl_bytes, PK.m ? 2 : 0, PV.code_bytes, 2 * PV.nb};
+  const int64_t streams[8] = {PK.code_bytes, 2 * PK.nb,       PK.qjl_bytes, PK.m ? 2 : 0,
+                              PV.code_bytes, 2 * PV.nb,       PV.qjl_bytes, PV.m ? 2 : 0};
   // (a paged cache's rows are its pages)
   const int64_t row = K->page_table ? K->page_size : S_cap;
-  for (int i = 0; i < 6; ++i)
+  for (int i = 0; i < 8; ++i)
     if ((row * streams[i]) % 16 != 0) return false;
   if ((!kpv && PK.blk != 32) || (!vpv && PV.blk != 32)) return false;
   bool ok;
-  if (k8v4) {
+  if (k8v4 || qv) {
     ok = true;
   } else if (PK.d == 256) {
     ok = !kpv && !vpv && !PK.m && PK.bits >= 2 && PK.bits <= 4;
@@ -791,7 +959,13 @@ bool decode_tc_eligible(const CodecParams& PK, const CodecParams& PV, int G, int
   if (!ok) return false;
   if (!aligned16(K->codes) || !aligned16(K->scales) || !aligned16(V->codes) || !aligned16(V->scales)) return false;
   if (PK.m && (!aligned16(K->qjl_bits) || !aligned16(K->qjl_rnorm) || !K->S || !aligned16(K->S))) return false;
+  if (PV.m && (!aligned16(V->qjl_bits) || !aligned16(V->qjl_rnorm) || !V->S || !aligned16(V->S))) return false;
   return true;
+}
+
+// CTAs of the kernel resident per SM (the register budget it is built for).
+int decode_tc_ctas_per_sm(const CodecParams& PV) {
+  return PV.m ? Cfg<128, 2, 2, true, true, false, false, true>::MINB : Cfg<128, 2, 3, true, true, false>::MINB;
 }
 
 int64_t decode_tc_per_split(int64_t ctx, int n_split) {
@@ -818,6 +992,9 @@ int launch_decode_tc(const CodecParams& PK, const CodecParams& PV, const tq_kv_v
   a.kr = reinterpret_cast<const uint8_t*>(K->qjl_rnorm);
   a.vc = V->codes;
   a.vs = reinterpret_cast<const uint8_t*>(V->scales);
+  a.vq = V->qjl_bits;
+  a.vr = reinterpret_cast<const uint8_t*>(V->qjl_rnorm);
+  a.Sv = V->S;
   a.q = q;
   a.kv_len = kv_len;
   a.part = part;
@@ -837,7 +1014,8 @@ int launch_decode_tc(const CodecParams& PK, const CodecParams& PV, const tq_kv_v
     float* sqsum = reinterpret_cast<float*>(extra + (((size_t)B * Hq * kQjlM * 2 + 15) / 16) * 16);
     a.sq = sq;
     a.sqsum = sqsum;
-    qjl_prep_kernel<<<B * Hkv, kQjlM, 0, st>>>(q, K->S, PK.d, qscale * kSqrtHalfPi / (float)PK.m, sq, sqsum);
+    if (PK.d != 128) return TQ_ERR_UNSUPPORTED;
+    qjl_prep_kernel<128><<<B * Hkv, kQjlM, 0, st>>>(q, K->S, qscale * kSqrtHalfPi / (float)PK.m, sq, sqsum);
     if (cudaGetLastError() != cudaSuccess) return TQ_ERR_CUDA;
   }
   const bool kpv = PK.blk == PK.d, vpv = PV.blk == PV.d;
@@ -854,6 +1032,13 @@ int launch_decode_tc(const CodecParams& PK, const CodecParams& PV, const tq_kv_v
     r = PK.bits == 4 ? launch_cfg<256, 4, 3, false, false, false>(PK, PV, a, B, st)
         : PK.bits == 3 ? launch_cfg<256, 3, 3, false, false, false>(PK, PV, a, B, st)
                        : launch_cfg<256, 2, 3, false, false, false>(PK, PV, a, B, st);
+  } else if (PV.m) {
+    if (PK.m)
+      r = PV.bits == 2 ? launch_cfg<128, 2, 2, true, true, true, false, true>(PK, PV, a, B, st)
+                       : launch_cfg<128, 2, 3, true, true, true, false, true>(PK, PV, a, B, st);
+    else
+      r = PV.bits == 2 ? launch_cfg<128, 2, 2, true, true, false, false, true>(PK, PV, a, B, st)
+                       : launch_cfg<128, 2, 3, true, true, false, false, true>(PK, PV, a, B, st);
   } else if (PK.m) {
     r = launch_cfg<128, 2, 3, true, true, true>(PK, PV, a, B, st);
   } else if (kpv) {

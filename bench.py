@@ -719,7 +719,7 @@ def bench_decode_blocks(tb, torch, dev, K, V, q, steps, warm):
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     out = torch.empty_like(q)
     ms = _time(torch, lambda: tb.tq_decode_attn_blocks(K.layout, kb, V.layout, vb, q, ctx=ctx, workspace=ws,
-                                                       out=out, n_split=n_split), flush, steps, warm)
+                                                       out=out), flush, steps, warm)
     ms_packed = _time(torch, lambda: tb.tq_decode_attn(K, V, q, ctx=ctx, workspace=ws, out=out),
                       flush, steps, warm)
     nbytes = kb.numel() + vb.numel()

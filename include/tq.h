@@ -257,7 +257,9 @@ int tq_decode_attn_static(const tq_kv_view* K, const tq_kv_view* V, const uint16
 
 /* Workspace bytes for tq_decode_attn with these sizes (host).  n_split = 0
  * gives the size for the library's own choice; *n_split_out (may be NULL)
- * receives the split count that will be used. */
+ * receives the largest split count that choice takes for these sizes (the
+ * count used depends on the layouts: each kernel splits the context to fill
+ * one wave of its own CTAs, so a call may use fewer). */
 int tq_decode_workspace_bytes(int B, int Hq, int Hkv, int head_dim, int64_t ctx, int n_split,
                               size_t* bytes, int* n_split_out);
 

@@ -18,7 +18,8 @@
 namespace tq {
 
 int decode_auto_splits(int B, int Hkv, int64_t ctx, int per_sm = 4);
-int decode_tc_ctas_per_sm(const CodecParams& PV);
+int decode_tc_ctas_per_sm(const CodecParams& PK, const CodecParams& PV);
+int decode_tc_max_ctas_per_sm();
 bool decode_tc_blocks_eligible(const CodecParams& PK, const CodecParams& PV, int G, int64_t S_cap,
                                const uint8_t* k_blocks, const uint8_t* v_blocks);
 int launch_decode_tc_blocks(const CodecParams& PK, const CodecParams& PV, const uint8_t* k_blocks,
@@ -883,7 +884,9 @@ extern "C" int tq_decode_workspace_bytes(int B, int Hq, int Hkv, int head_dim, i
                                          size_t* bytes, int* n_split_out) {
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || ctx < 0 || n_split < 0 || !bytes) return TQ_ERR_ARG;
   if (head_dim != 64 && head_dim != 128 && head_dim != 256) return TQ_ERR_UNSUPPORTED;
-  const int ns = n_split ? n_split : tq::decode_auto_splits(B, Hkv, ctx);
+  // the layout decides the kernel and its residency; size for the most splits any choice takes
+  const int per_sm = tq::decode_tc_max_ctas_per_sm() > 4 ? tq::decode_tc_max_ctas_per_sm() : 4;
+  const int ns = n_split ? n_split : tq::decode_auto_splits(B, Hkv, ctx, per_sm);
   *bytes = tq::decode_ws_bytes(B, Hq, head_dim, ns);
   if (n_split_out) *n_split_out = ns;
   return TQ_OK;
@@ -927,7 +930,7 @@ int decode_impl(const tq_kv_view* K, const tq_kv_view* V, const uint16_t* q, int
     return TQ_ERR_ALIGN;
   const int G = Hq / Hkv;
   const bool tc = decode_tc_eligible(PK, PV, G, S_cap, K, V);
-  const int ns = n_split ? n_split : decode_auto_splits(B, Hkv, ctx, tc ? decode_tc_ctas_per_sm(PV) : 4);
+  const int ns = n_split ? n_split : decode_auto_splits(B, Hkv, ctx, tc ? decode_tc_ctas_per_sm(PK, PV) : 4);
   const int slots = ns + (win ? 1 : 0);
   const size_t need = decode_ws_bytes(B, Hq, PK.d, slots);
   if (!workspace || workspace_bytes < need) return TQ_ERR_WORKSPACE;
@@ -999,7 +1002,8 @@ int decode_blocks_impl(const tq_layout* Lk, const uint8_t* k_blocks, const tq_la
   if ((reinterpret_cast<uintptr_t>(k_blocks) & 1) || (reinterpret_cast<uintptr_t>(v_blocks) & 1) ||
       !aligned16(q) || !aligned16(out))
     return TQ_ERR_ALIGN;
-  const int ns = n_split ? n_split : decode_auto_splits(B, Hkv, ctx);
+  const bool tc = decode_tc_blocks_eligible(PK, PV, Hq / Hkv, S_cap, k_blocks, v_blocks);
+  const int ns = n_split ? n_split : decode_auto_splits(B, Hkv, ctx, tc ? decode_tc_ctas_per_sm(PK, PV) : 4);
   const size_t need = decode_ws_bytes(B, Hq, PK.d, ns);
   if (!workspace || workspace_bytes < need) return TQ_ERR_WORKSPACE;
   if (!aligned16(workspace)) return TQ_ERR_ALIGN;
@@ -1020,7 +1024,7 @@ int decode_blocks_impl(const tq_layout* Lk, const uint8_t* k_blocks, const tq_la
   a.vblk = reinterpret_cast<const uint16_t*>(v_blocks);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int G = Hq / Hkv;
-  if (decode_tc_blocks_eligible(PK, PV, G, S_cap, k_blocks, v_blocks)) {
+  if (tc) {
     st = launch_decode_tc_blocks(PK, PV, k_blocks, v_blocks, q, kv_len, a.part, B, Hq, Hkv, S_cap, ctx, ns, a.qscale,
                                  s);
   } else {

@@ -964,8 +964,16 @@ bool decode_tc_eligible(const CodecParams& PK, const CodecParams& PV, int G, int
 }
 
 // CTAs of the kernel resident per SM (the register budget it is built for).
-int decode_tc_ctas_per_sm(const CodecParams& PV) {
-  return PV.m ? Cfg<128, 2, 2, true, true, false, false, true>::MINB : Cfg<128, 2, 3, true, true, false>::MINB;
+int decode_tc_ctas_per_sm(const CodecParams& PK, const CodecParams& PV) {
+  if (PV.m) return Cfg<128, 2, 2, true, true, false, false, true>::MINB;
+  if (PK.bits == 8) return Cfg<128, 8, 4, false, false, false>::MINB;
+  return Cfg<128, 2, 3, true, true, false>::MINB;
+}
+// The most any layout uses: the split count a workspace is sized for.
+int decode_tc_max_ctas_per_sm() {
+  const int a = Cfg<128, 2, 2, true, true, false, false, true>::MINB, b = Cfg<128, 8, 4, false, false, false>::MINB,
+            c = Cfg<128, 2, 3, true, true, false>::MINB;
+  return a > b ? (a > c ? a : c) : (b > c ? b : c);
 }
 
 int64_t decode_tc_per_split(int64_t ctx, int n_split) {

@@ -65,6 +65,9 @@ DECODE_CASES = [
     ("tc_d256_turbo4k_p64", (32, 4, 0, 0, 1), (32, 3, 0, 0, 1), 1, 8, 2, 1536, 1500, None, 0, 256, 64, False),
     ("tc_qjl_keys_p128", (128, 2, 128, 0, 1), (128, 3, 0, 0, 1), 2, 8, 2, 1024, 1000, [1000, 333], 3, 128, 128,
      True),
+    # QJL on the values too: the tensor-core kernel's sign and rho streams come from the pages as well
+    ("tc_qjl_keys_values_p64", (128, 2, 128, 0, 1), (128, 2, 128, 0, 3), 2, 8, 2, 1024, 1000, [1000, 333], 0, 128,
+     64, True),
     ("cuda_core_pervec_d64_p32", (64, 4, 0, 0, 5), (64, 3, 0, 0, 6), 2, 2, 2, 320, 300, [300, 31], 0, 64, 32, False),
     ("cuda_core_gqa2_d128_p512", (32, 3, 0, 0, 1), (32, 2, 0, 0, 2), 1, 4, 2, 1024, 1024, None, 2, 128, 512, False),
 ]
@@ -75,8 +78,9 @@ def test_paged_decode_matches_contiguous(tqlib, name, cK, cV, B, Hq, Hkv, S_cap,
                                          page_size, qjl):
     from turboquant_kv_cache_gb300 import binding as tb
     S = inputs.qjl_matrix(cK[2], d, 7) if qjl else None
+    Sv = inputs.qjl_matrix(cV[2], d, 8) if cV[2] else None
     K = _cache(tb, cK, B, Hkv, S_cap, d, 101, S=S, heavy=(d == 256))
-    V = _cache(tb, cV, B, Hkv, S_cap, d, 102)
+    V = _cache(tb, cV, B, Hkv, S_cap, d, 102, S=Sv)
     table, n_pages = _page_table(B, S_cap // page_size, 3, 5)
     Kp = _to_paged(tb, K, table, n_pages, page_size)
     Vp = _to_paged(tb, V, table, n_pages, page_size)

@@ -258,53 +258,94 @@ __global__ void __launch_bounds__(kThreads) dequantize_kernel(const CodecParams 
   const uint32_t sb = sign_byte(P, i0);
   const int64_t nwarps = (int64_t)gridDim.x * (kThreads / 32);
   const int words_per_vec = P.code_bytes / 4;
+  const int64_t step = nwarps * VPW;
+  // the packed words a thread's chunk needs: word wi of its group, and for the
+  // fourth 3-bit chunk (bit 3 of every nibble) words 0..2
+  const int w = sub & 3;
+  const int wi = P.bits == 4 ? w : P.bits == 3 ? (w < 3 ? w : 0) : P.bits == 2 ? (w & 1) : 0;
+  const bool three = P.bits == 3 && w == 3;
+  // kBatch iterations at a time: every load of the batch is issued before the
+  // first decode, so a warp keeps kBatch vector pairs of reads in flight
+  constexpr int kBatch = D >= 256 ? 2 : 4;
   for (int64_t base = ((int64_t)blockIdx.x * (kThreads / 32) + wid) * VPW; base < a.n_vec;
-       base += nwarps * VPW) {
-    const int64_t v = base + vs;
-    const bool valid = v < a.n_vec;
-    float x[8];
-    if constexpr (W8) {   // bytes 8 sub .. 8 sub + 7 of the record
-      uint2 u = make_uint2(0, 0);
-      if (valid) u = *reinterpret_cast<const uint2*>(a.codes + v * words_per_vec + 2 * sub);
+       base += kBatch * step) {
+    uint32_t r0[kBatch], r1[kBatch], r2[kBatch], sc16[kBatch];
 #pragma unroll
-      for (int r = 0; r < 8; ++r) x[r] = s_cent[((r < 4 ? u.x : u.y) >> (8 * (r & 3))) & 0xff];
-    } else {
-      uint32_t nib = 0;
-      if (valid) nib = load_chunk(a.codes + v * words_per_vec + (sub >> 2) * P.bits, P.bits, sub & 3);
-#pragma unroll
-      for (int r = 0; r < 8; ++r) x[r] = s_cent[(nib >> (4 * r)) & 0xf];
-    }
-    wht8(x);
-    wht_cross(x, sub, tpb);
-#pragma unroll
-    for (int r = 0; r < 8; ++r) x[r] = flip(x[r] * P.inv_sqrt_blk, (sb >> r) & 1u);
-    if (P.m && valid) {
-      const float coef = h2f(a.rnorm[v]) * kSqrtHalfPi / (float)P.m;
-      const uint32_t* bits = a.qjl + v * (P.m / 32);
-#pragma unroll
-      for (int r = 0; r < 8; ++r) {
-        float corr = 0.f;
-        for (int i = 0; i < P.m; ++i) {
-          const float sgn = ((__ldg(bits + (i >> 5)) >> (i & 31)) & 1u) ? 1.f : -1.f;
-          corr = fmaf(sgn, __ldg(a.S + (int64_t)i * D + i0 + r), corr);
+    for (int k = 0; k < kBatch; ++k) {
+      const int64_t v = base + k * step + vs;
+      r0[k] = r1[k] = r2[k] = sc16[k] = 0;
+      if (v < a.n_vec) {
+        if constexpr (W8) {
+          const uint32_t* g = a.codes + v * words_per_vec + 2 * sub;
+          r0[k] = __ldg(g);
+          r1[k] = __ldg(g + 1);
+        } else {
+          const uint32_t* g = a.codes + v * words_per_vec + (sub >> 2) * P.bits;
+          r0[k] = __ldg(g + wi);
+          if (three) {
+            r1[k] = __ldg(g + 1);
+            r2[k] = __ldg(g + 2);
+          }
         }
-        x[r] = fmaf(coef, corr, x[r]);
+        sc16[k] = __ldg(a.scales + v * P.nb + sub / tpb);
       }
     }
-    if (valid) {
-      const float sc = h2f(a.scales[v * P.nb + sub / tpb]);
-      if (F32) {
-        float4* o = reinterpret_cast<float4*>(static_cast<float*>(a.out) + v * D + i0);
-        o[0] = make_float4(x[0] * sc, x[1] * sc, x[2] * sc, x[3] * sc);
-        o[1] = make_float4(x[4] * sc, x[5] * sc, x[6] * sc, x[7] * sc);
-      } else {
-        uint32_t w[4];
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          const __half2 h = __floats2half2_rn(x[2 * r] * sc, x[2 * r + 1] * sc);
-          w[r] = *reinterpret_cast<const uint32_t*>(&h);
+    for (int k = 0; k < kBatch; ++k) {
+      const int64_t v = base + k * step + vs;
+      if (base + k * step >= a.n_vec) break;   // the warp's vectors of this and later iterations are all past the end
+      const bool valid = v < a.n_vec;
+      float x[8];
+      if constexpr (W8) {   // bytes 8 sub .. 8 sub + 7 of the record
+#pragma unroll
+        for (int r = 0; r < 8; ++r) x[r] = s_cent[((r < 4 ? r0[k] : r1[k]) >> (8 * (r & 3))) & 0xff];
+      } else {
+        uint32_t nib;
+        if (three)
+          nib = ((r0[k] >> 3) & 0x11111111u) | ((r1[k] >> 2) & 0x22222222u) | ((r2[k] >> 1) & 0x44444444u);
+        else if (P.bits == 4)
+          nib = r0[k];
+        else if (P.bits == 3)
+          nib = r0[k] & 0x77777777u;
+        else if (P.bits == 2)
+          nib = w < 2 ? (r0[k] & 0x33333333u) : ((r0[k] >> 2) & 0x33333333u);
+        else
+          nib = (r0[k] >> w) & 0x11111111u;
+#pragma unroll
+        for (int r = 0; r < 8; ++r) x[r] = s_cent[(nib >> (4 * r)) & 0xf];
+      }
+      wht8(x);
+      wht_cross(x, sub, tpb);
+#pragma unroll
+      for (int r = 0; r < 8; ++r) x[r] = flip(x[r] * P.inv_sqrt_blk, (sb >> r) & 1u);
+      if (P.m && valid) {
+        const float coef = h2f(a.rnorm[v]) * kSqrtHalfPi / (float)P.m;
+        const uint32_t* bits = a.qjl + v * (P.m / 32);
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          float corr = 0.f;
+          for (int i = 0; i < P.m; ++i) {
+            const float sgn = ((__ldg(bits + (i >> 5)) >> (i & 31)) & 1u) ? 1.f : -1.f;
+            corr = fmaf(sgn, __ldg(a.S + (int64_t)i * D + i0 + r), corr);
+          }
+          x[r] = fmaf(coef, corr, x[r]);
         }
-        *reinterpret_cast<uint4*>(static_cast<__half*>(a.out) + v * D + i0) = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+      if (valid) {
+        const float sc = h2f((uint16_t)sc16[k]);
+        if (F32) {
+          float4* o = reinterpret_cast<float4*>(static_cast<float*>(a.out) + v * D + i0);
+          o[0] = make_float4(x[0] * sc, x[1] * sc, x[2] * sc, x[3] * sc);
+          o[1] = make_float4(x[4] * sc, x[5] * sc, x[6] * sc, x[7] * sc);
+        } else {
+          uint32_t wv[4];
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            const __half2 h = __floats2half2_rn(x[2 * r] * sc, x[2 * r + 1] * sc);
+            wv[r] = *reinterpret_cast<const uint32_t*>(&h);
+          }
+          *reinterpret_cast<uint4*>(static_cast<__half*>(a.out) + v * D + i0) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+        }
       }
     }
   }

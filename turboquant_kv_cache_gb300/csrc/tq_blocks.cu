@@ -58,20 +58,35 @@ __device__ __forceinline__ void stage16(uint16_t* dst, const uint8_t* src, int b
 // to blocks: one thread per 8 consecutive blocks (8 * (2 + 4 bits) bytes out,
 // a whole number of 16-byte words): their codes in 16-byte loads, their 8
 // norms, and each output word assembled from two halfwords at positions
-// known at compile time; a ragged last group goes block by block
+// known at compile time.  The words go through shared memory so that the
+// CTA's stores are contiguous; a CTA whose range runs past the end writes
+// its last, ragged group block by block.
+// threads of a to-blocks CTA: its staged output (8 blocks a thread) within 32 KB
 template <int BITS>
-__global__ void __launch_bounds__(kTileThreads) to_blocks_g8(const uint8_t* __restrict__ codes,
+__host__ __device__ constexpr int g8_threads() {
+  return 2 + 4 * BITS <= 14 ? 256 : (2 + 4 * BITS <= 18 ? 128 : 64);
+}
+
+template <int BITS>
+__global__ void __launch_bounds__(g8_threads<BITS>()) to_blocks_g8(const uint8_t* __restrict__ codes,
                                                             const uint16_t* __restrict__ scales, int64_t n_blocks,
                                                             int gshift, int jshift, int nb,
                                                             uint8_t* __restrict__ out) {
   constexpr int GB = 4 * BITS, BB = 2 + GB, HW = GB / 2;   // bytes of codes / of a block; code halfwords
-  const int64_t i0 = ((int64_t)blockIdx.x * kTileThreads + threadIdx.x) * 8;
-  if (i0 >= n_blocks) return;
+  constexpr int kT = g8_threads<BITS>();
+  __shared__ uint4 s_out[kT * BB / 2];           // the CTA's output words
+  const int64_t cta0 = (int64_t)blockIdx.x * kT * 8;   // the CTA's first block
+  const int64_t i0 = cta0 + (int64_t)threadIdx.x * 8;
   const int mask = (1 << gshift) - 1;
+  if (cta0 + (int64_t)kT * 8 > n_blocks) {
+    // the last CTA: plain per-thread stores (no barrier, threads past the end leave)
+    if (i0 >= n_blocks) return;
+  }
   auto norm_of = [&](int64_t i) -> uint32_t {
     return __ldg(scales + (i >> gshift) * nb + ((int)(i & mask) >> jshift));
   };
-  if (i0 + 8 > n_blocks) {
+  const bool last_cta = cta0 + (int64_t)kT * 8 > n_blocks;
+  if (last_cta && i0 + 8 > n_blocks) {
     for (int64_t i = i0; i < n_blocks; ++i) {
       uint16_t* dst = reinterpret_cast<uint16_t*>(out + i * BB);
       dst[0] = (uint16_t)norm_of(i);
@@ -97,7 +112,9 @@ __global__ void __launch_bounds__(kTileThreads) to_blocks_g8(const uint8_t* __re
     const int c = b * HW + k - 1;
     return (cw[c >> 1] >> (16 * (c & 1))) & 0xFFFFu;
   };
-  uint4* o4 = reinterpret_cast<uint4*>(out + i0 * BB);
+  // a lane's words sit BB / 2 words apart: with BB / 2 odd for every width, eight
+  // consecutive lanes hit eight different 16-byte bank groups
+  uint4* o4 = last_cta ? reinterpret_cast<uint4*>(out + i0 * BB) : s_out + threadIdx.x * (BB / 2);
 #pragma unroll
   for (int q = 0; q < BB / 2; ++q) {
     uint32_t w[4];
@@ -105,6 +122,11 @@ __global__ void __launch_bounds__(kTileThreads) to_blocks_g8(const uint8_t* __re
     for (int e = 0; e < 4; ++e) w[e] = hw(8 * q + 2 * e) | (hw(8 * q + 2 * e + 1) << 16);
     o4[q] = make_uint4(w[0], w[1], w[2], w[3]);
   }
+  if (last_cta) return;
+  __syncthreads();
+  uint4* dst = reinterpret_cast<uint4*>(out + cta0 * BB);
+#pragma unroll
+  for (int q = 0; q < BB / 2; ++q) dst[q * kT + threadIdx.x] = s_out[q * kT + threadIdx.x];
 }
 
 // from blocks: a tile of blocks into shared memory, then the codes as
@@ -148,7 +170,8 @@ void launch_to_tiled(const uint8_t* codes, const uint16_t* scales, int64_t n, in
   int jshift = 0;
   while ((32 << jshift) < blk) ++jshift;
   const int64_t groups8 = (n + 7) / 8;
-  to_blocks_g8<BITS><<<(unsigned)((groups8 + kTileThreads - 1) / kTileThreads), kTileThreads, 0, st>>>(
+  constexpr int kT = g8_threads<BITS>();
+  to_blocks_g8<BITS><<<(unsigned)((groups8 + kT - 1) / kT), kT, 0, st>>>(
       codes, scales, n, gshift, jshift, nb, out);
 }
 template <int BITS>

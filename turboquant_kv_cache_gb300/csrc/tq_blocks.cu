@@ -61,10 +61,12 @@ __device__ __forceinline__ void stage16(uint16_t* dst, const uint8_t* src, int b
 // known at compile time.  The words go through shared memory so that the
 // CTA's stores are contiguous; a CTA whose range runs past the end writes
 // its last, ragged group block by block.
-// threads of a to-blocks CTA: its staged output (8 blocks a thread) within 32 KB
+// threads of a to-blocks CTA (8 blocks a thread): its staged codes and
+// output words within 40 KB, a power of two of at most 256
 template <int BITS>
 __host__ __device__ constexpr int g8_threads() {
-  return 2 + 4 * BITS <= 14 ? 256 : (2 + 4 * BITS <= 18 ? 128 : 64);
+  constexpr int per_thread = 8 * (4 * BITS + 2 + 4 * BITS);   // code bytes in + block bytes out
+  return 40960 / per_thread >= 256 ? 256 : 40960 / per_thread >= 128 ? 128 : 64;
 }
 
 template <int BITS>
@@ -75,6 +77,7 @@ __global__ void __launch_bounds__(g8_threads<BITS>()) to_blocks_g8(const uint8_t
   constexpr int GB = 4 * BITS, BB = 2 + GB, HW = GB / 2;   // bytes of codes / of a block; code halfwords
   constexpr int kT = g8_threads<BITS>();
   __shared__ uint4 s_out[kT * BB / 2];           // the CTA's output words
+  __shared__ uint4 s_in[kT * GB / 2];            // the CTA's codes
   const int64_t cta0 = (int64_t)blockIdx.x * kT * 8;   // the CTA's first block
   const int64_t i0 = cta0 + (int64_t)threadIdx.x * 8;
   const int mask = (1 << gshift) - 1;
@@ -96,10 +99,20 @@ __global__ void __launch_bounds__(g8_threads<BITS>()) to_blocks_g8(const uint8_t
     return;
   }
   uint32_t cw[2 * GB];   // the 8 blocks' codes: 8 GB bytes
-  const uint4* c4 = reinterpret_cast<const uint4*>(codes + i0 * GB);
+  const uint4* c4;
+  if (last_cta) {
+    c4 = reinterpret_cast<const uint4*>(codes + i0 * GB);
+  } else {
+    // the CTA's codes in one contiguous, coalesced pass
+    const uint4* g4 = reinterpret_cast<const uint4*>(codes + cta0 * GB);
+#pragma unroll
+    for (int q = 0; q < GB / 2; ++q) s_in[q * kT + threadIdx.x] = __ldg(g4 + q * kT + threadIdx.x);
+    __syncthreads();
+    c4 = s_in + threadIdx.x * (GB / 2);
+  }
 #pragma unroll
   for (int k = 0; k < GB / 2; ++k) {
-    const uint4 v = __ldg(c4 + k);
+    const uint4 v = c4[k];
     cw[4 * k] = v.x; cw[4 * k + 1] = v.y; cw[4 * k + 2] = v.z; cw[4 * k + 3] = v.w;
   }
   uint32_t nr[8];

@@ -257,6 +257,15 @@ def test_decode_workspace_query(tqlib):
     assert ns == 16 and nb == _decode_ws(8, 32, 128, 16)
     nb, ns = tb.tq_decode_workspace_bytes(1, 16, 4, 256, 131072, 0)
     assert ns >= 1 and nb == _decode_ws(1, 16, 256, ns)
+    # the library's own choice: one wave of the most resident decode CTAs (four
+    # per SM; with no device the SM count is taken as 152), never more splits
+    # than 256-token slices, so the workspace covers every layout's choice
+    import torch
+    sms = torch.cuda.get_device_properties(0).multi_processor_count if torch.cuda.is_available() else 152
+    nb, ns = tb.tq_decode_workspace_bytes(4, 32, 8, 128, 16384, 0)
+    assert ns == min(4 * sms // 32, 64) and nb == _decode_ws(4, 32, 128, ns)
+    nb, ns = tb.tq_decode_workspace_bytes(1, 8, 2, 128, 600, 0)
+    assert ns == (600 + 255) // 256
     with pytest.raises(tb.TQError):
         tb.tq_decode_workspace_bytes(2, 6, 4, 128, 100)
 
